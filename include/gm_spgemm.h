@@ -1,0 +1,221 @@
+/*
+ * gm_spgemm.h -- C ABI of the GB300 gMAGNUS SpGEMM, C = A * B over CSR.
+ *
+ * Method: gMAGNUS, "Fast SpGEMM on GPUs for Irregular Matrices via Hierarchical
+ * Multisplit" (Wolfson-Pou, Helal, Petrini). Algorithm 3 there states the problem
+ * as "Input: A, B. Output: C" with every array in device memory (Sec. III-A), a
+ * symbolic phase that yields C.rowPtr and C.nnz and a numeric phase that fills
+ * C.col and C.val (Sec. II-B, Algorithm 1). This interface follows that split:
+ *
+ *   gm_spgemm_analyze   -- Algorithm 3 lines 2-5: parameters (Sec. III-D), per-row
+ *                          intermediate-product counts, heavy/light partition.
+ *   gm_spgemm_symbolic  -- lines 7-25: outer product, hierarchical multisplit,
+ *                          symbolic accumulation, prefix sum of C.rowPtr.
+ *   gm_spgemm_numeric   -- lines 26-28: numeric accumulation, C.col / C.val.
+ *
+ * Conventions common to every call
+ *   - Matrices are CSR: row_ptr int64[n_rows+1] (row_ptr[0] = 0, non-decreasing,
+ *     row_ptr[n_rows] = nnz), col_idx int32[nnz] in [0, n_cols), vals double[nnz].
+ *     Rows need not be sorted and may repeat a column; repeated entries add.
+ *   - Pointers documented "device" must be device (or managed) memory of the
+ *     current CUDA device; "host" pointers are ordinary host memory.
+ *   - Every call returns a gm_status; nothing is thrown across the ABI. A call
+ *     made out of order returns GM_ERR_STATE and leaves the plan unchanged.
+ *   - Work is issued on the stream given to gm_spgemm_analyze (a cudaStream_t;
+ *     NULL is the legacy default stream). Calls block the host only where a
+ *     count must be known on the host (documented per call).
+ *   - Results: C rows sorted by column; an entry exists when some stored A[i,k]
+ *     meets a stored B[k,j], also when its value is zero (structure is symbolic).
+ *     fp64 sums are formed in an unspecified order.
+ */
+#ifndef GM_SPGEMM_H
+#define GM_SPGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gm_status {
+  GM_OK = 0,
+  GM_ERR_INVALID_ARG = 1,     /* null pointer, negative size, malformed CSR      */
+  GM_ERR_DIM_MISMATCH = 2,    /* A.n_cols != B.n_rows                            */
+  GM_ERR_INDEX_OVERFLOW = 3,  /* a size that does not fit the index types        */
+  GM_ERR_OOM = 4,             /* device allocation failed                        */
+  GM_ERR_WORKSPACE = 5,       /* one heavy row needs more than the workspace cap */
+  GM_ERR_CUDA = 6,            /* a CUDA call failed; see gm_plan_info.cuda_error */
+  GM_ERR_DEVICE_TIMEOUT = 7,  /* a bounded device-side wait gave up              */
+  GM_ERR_STATE = 8,           /* call out of order (analyze, symbolic, numeric)  */
+  GM_ERR_BAD_INDEX = 9        /* a column index out of range, found on device    */
+} gm_status;
+
+/* A CSR matrix. The library only reads these arrays; they stay owned by the
+ * caller and must remain valid and unchanged until gm_spgemm_numeric returns. */
+typedef struct gm_csr {
+  int64_t n_rows;
+  int64_t n_cols;
+  int64_t nnz;
+  const int64_t* row_ptr; /* device, n_rows + 1 */
+  const int32_t* col_idx; /* device, nnz        */
+  const double* vals;     /* device, nnz        */
+} gm_csr;
+
+/* Flags for gm_config.flags. */
+#define GM_FLAG_TIMING 1             /* record per-stage device times (gm_plan_info.stage_ms) */
+#define GM_FLAG_KEEP_INTERMEDIATES 2 /* keep C-hat / C-hat_reord of a single batch for gm_spgemm_debug_copy */
+#define GM_FLAG_LOG 4                /* print the plan to stderr (also env GM_SPGEMM_LOG=1) */
+
+/* Heavy-path pipelines for gm_config.pipeline. */
+#define GM_PIPE_AUTO 0
+#define GM_PIPE_UNFUSED 1 /* outer product -> C-hat -> histogram -> multisplit (Algorithm 3 as printed) */
+#define GM_PIPE_FUSED_HISTO 2 /* outer product counts the level-0 chunk histogram while it writes C-hat */
+
+/* Tuning and test overrides; zero selects the automatic value for every field.
+ * Overrides change how the work is split, never the result. A NULL config is
+ * the same as all zeros. */
+typedef struct gm_config {
+  int64_t smem_budget_bytes;   /* s_LM; 0 = the device's opt-in shared memory per block        */
+  int64_t tau;                 /* heavy-row threshold; 0 = Eq. (4)                             */
+  int64_t dense_width;         /* last-level chunk width (power of two); 0 = derived           */
+  int64_t n_chunks_max;        /* chunks per multisplit level (power of two >= 2); 0 = Eq. (6) */
+  int64_t workspace_cap_bytes; /* cap on heavy-path workspace; 0 = free memory minus a reserve  */
+  int32_t pipeline;            /* GM_PIPE_*                                                    */
+  int32_t flags;               /* GM_FLAG_*                                                    */
+} gm_config;
+
+#define GM_MAX_LEVELS 16
+
+/* Parameters of gMAGNUS Sec. III-D (GetMagnusParams). */
+typedef struct gm_params {
+  int64_t s_lm;                /* local-memory budget in bytes                          */
+  int64_t tau;                 /* Eq. (4): heavy when intermediate products exceed tau   */
+  int64_t dense_width;         /* n_denseNumeric floored to a power of two               */
+  int64_t n_chunks_required;   /* ceil(C.m / dense_width) rounded up to a power of two   */
+  int64_t n_chunks_max;        /* Eq. (5)/(6), floored to a power of two                 */
+  int64_t n_levels;            /* Eq. (7); 0 when n_chunks_required == 1                 */
+  int64_t v_chunks[GM_MAX_LEVELS]; /* chunks per row at each level                       */
+  int64_t widths[GM_MAX_LEVELS];   /* column width of a chunk after each level           */
+} gm_params;
+
+#define GM_NUM_STAGES 12
+/* Stage indices of gm_plan_info.stage_ms (device time, filled with GM_FLAG_TIMING). */
+enum {
+  GM_STAGE_ANALYZE = 0,      /* counts, validation, partition, heavy row pointers */
+  GM_STAGE_TRANSPOSE = 1,    /* masked CSR -> CSC of the heavy rows                */
+  GM_STAGE_OUTER = 2,        /* outer product                                      */
+  GM_STAGE_HISTOGRAM = 3,    /* chunk histograms and scans                         */
+  GM_STAGE_MULTISPLIT = 4,   /* multisplit levels                                  */
+  GM_STAGE_SYM_HEAVY = 5,    /* symbolic accumulation of chunks                    */
+  GM_STAGE_SYM_LIGHT = 6,    /* symbolic accumulation of light rows                */
+  GM_STAGE_SCAN = 7,         /* prefix sum of C.rowPtr and chunk offsets           */
+  GM_STAGE_NUM_HEAVY = 8,    /* numeric accumulation of chunks                     */
+  GM_STAGE_NUM_LIGHT = 9,    /* numeric accumulation of light rows                 */
+  GM_STAGE_OTHER = 10        /* everything else                                    */
+};
+
+typedef struct gm_plan_info {
+  gm_params params;
+  int64_t n_rows;              /* C.n                                   */
+  int64_t n_cols;              /* C.m                                   */
+  int64_t n_heavy_rows;
+  int64_t n_light_rows;        /* rows with 0 < u(i) <= tau             */
+  int64_t n_empty_rows;        /* rows with u(i) == 0                   */
+  int64_t ip_total;            /* sum of u(i): intermediate products    */
+  int64_t ip_heavy;            /* C-hat.nnz                             */
+  int64_t c_nnz;               /* -1 before symbolic                    */
+  int64_t chat_bytes;          /* C-hat size (col + val) in bytes       */
+  int64_t n_batches;           /* heavy-row batches under the workspace cap */
+  int64_t workspace_peak_bytes;
+  int64_t n_leaves;            /* chunks accumulated                    */
+  int32_t keeps_reordered;     /* 1 when symbolic kept C-hat_reord for numeric */
+  int32_t pipeline;            /* GM_PIPE_* in effect                   */
+  int32_t cuda_error;          /* last cudaError_t seen, 0 if none      */
+  int32_t device_status;       /* device-side error bits, 0 if none     */
+  float stage_ms[GM_NUM_STAGES];
+} gm_plan_info;
+
+typedef struct gm_plan gm_plan; /* opaque; owns every workspace buffer */
+
+/* Device memory hooks for the plan's workspace. alloc returns NULL on failure.
+ * Both run on the host, in stream order on `stream`. NULL hooks select
+ * cudaMallocAsync / cudaFreeAsync. Set before gm_spgemm_analyze. */
+typedef void* (*gm_alloc_fn)(void* ctx, size_t bytes, void* stream);
+typedef void (*gm_free_fn)(void* ctx, void* ptr, size_t bytes, void* stream);
+void gm_set_allocator(gm_alloc_fn alloc_fn, gm_free_fn free_fn, void* ctx);
+
+/* Host only. Fills *out with the parameters gMAGNUS Sec. III-D derives for a
+ * product with c_m columns (Eqs. (4)-(7)), honouring the overrides in cfg
+ * (nullable). cfg->smem_budget_bytes == 0 means 232448 bytes (227 KB, the opt-in
+ * shared memory per block of sm_103a). Errors: GM_ERR_INVALID_ARG for c_m < 1,
+ * a null out, or overrides that are not powers of two / too small. */
+gm_status gm_spgemm_params(int64_t c_m, const gm_config* cfg, gm_params* out);
+
+/* Algorithm 3 lines 2-5. Validates A and B (sizes on the host, indices on the
+ * device), derives the parameters, counts the intermediate products of every row
+ * (u(i) = sum over stored A[i,k] of nnz(B[k,:]), Sec. III-A InterOffsets), splits
+ * rows into heavy (u > tau) and light ones and computes C-hat.rowPtr.
+ * A and B: host pointers to descriptors of device arrays (copied; the arrays are
+ * not). cfg: nullable. stream: a cudaStream_t used for all later work of the plan.
+ * Blocks until the row counts are on the host. On success *plan_out owns all
+ * workspace; release it with gm_spgemm_plan_destroy.
+ * Errors: GM_ERR_INVALID_ARG, GM_ERR_DIM_MISMATCH, GM_ERR_INDEX_OVERFLOW,
+ * GM_ERR_BAD_INDEX (a column out of range or a malformed row_ptr), GM_ERR_OOM,
+ * GM_ERR_CUDA. *plan_out is NULL on error. */
+gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* cfg, void* stream,
+                            gm_plan** plan_out);
+
+/* Algorithm 3 lines 7-25. Writes C.rowPtr (device, A.n_rows + 1 int64, caller
+ * allocated) and *C_nnz (host). Heavy rows go through the outer product and the
+ * hierarchical multisplit in batches that fit the workspace cap; light rows are
+ * counted with a shared-memory accumulator. Blocks until C.nnz is on the host.
+ * Errors: GM_ERR_STATE (not right after analyze), GM_ERR_INVALID_ARG,
+ * GM_ERR_WORKSPACE (a single heavy row does not fit the cap), GM_ERR_OOM,
+ * GM_ERR_CUDA, GM_ERR_DEVICE_TIMEOUT. */
+gm_status gm_spgemm_symbolic(gm_plan* plan, int64_t* C_row_ptr, int64_t* C_nnz);
+
+/* Algorithm 3 lines 26-28. Fills C.col (device int32[C_nnz]) and C.val (device
+ * double[C_nnz]), both caller allocated after gm_spgemm_symbolic; each row sorted
+ * by column. Returns once the work is issued and has completed (stream synchronised).
+ * Errors: GM_ERR_STATE (symbolic not done, or numeric already done),
+ * GM_ERR_INVALID_ARG, GM_ERR_WORKSPACE, GM_ERR_OOM, GM_ERR_CUDA. */
+gm_status gm_spgemm_numeric(gm_plan* plan, int32_t* C_col_idx, double* C_vals);
+
+/* Copies the plan's parameters, sizes and statistics (gMAGNUS Tables V/VI:
+ * C-hat size, heavy IP and row fractions, chunks per level) into *out (host). */
+gm_status gm_spgemm_plan_info(const gm_plan* plan, gm_plan_info* out);
+
+/* Releases every buffer the plan owns (stream-ordered on the plan's stream). NULL is a no-op. */
+void gm_spgemm_plan_destroy(gm_plan* plan);
+
+/* A static, human-readable name of a status code. */
+const char* gm_status_string(gm_status s);
+
+/* Debug view of a plan's device arrays, copied to host memory `dst` of `bytes`
+ * bytes (which must equal the array size reported through *out_bytes when dst is
+ * NULL). Available after analyze (GM_DBG_IP_COUNTS, GM_DBG_HEAVY_ROWS,
+ * GM_DBG_LIGHT_ROWS, GM_DBG_CHAT_ROWPTR) and, with GM_FLAG_KEEP_INTERMEDIATES and a
+ * single heavy batch, after symbolic (C-hat and the C-hat_reord of each level).
+ * `level` selects the multisplit level for the GM_DBG_REORD_* views.
+ * Errors: GM_ERR_INVALID_ARG (unknown view or size), GM_ERR_STATE (not available). */
+enum {
+  GM_DBG_IP_COUNTS = 0,    /* int64[n_rows]   u(i)                          */
+  GM_DBG_HEAVY_ROWS = 1,   /* int32[n_heavy]  x_heavy, ascending            */
+  GM_DBG_LIGHT_ROWS = 2,   /* int32[n_light + n_empty] x_light, ascending   */
+  GM_DBG_CHAT_ROWPTR = 3,  /* int64[n_heavy+1] C-hat.rowPtr                 */
+  GM_DBG_CHAT_COL = 4,     /* int32[ip_heavy] C-hat.col                     */
+  GM_DBG_CHAT_VAL = 5,     /* double[ip_heavy] C-hat.val                    */
+  GM_DBG_REORD_ROWPTR = 6, /* int64[rows+1]   C-hat_reord.rowPtr at `level` */
+  GM_DBG_REORD_COL = 7,    /* int32[...]      chunk-local columns           */
+  GM_DBG_REORD_VAL = 8,    /* double[...]                                   */
+  GM_DBG_REORD_CHILD = 9   /* int64[rows]     id (parent * v + chunk) of each C-hat_reord row */
+};
+gm_status gm_spgemm_debug_copy(const gm_plan* plan, int view, int level, void* dst, int64_t bytes,
+                               int64_t* out_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GM_SPGEMM_H */

@@ -1,0 +1,214 @@
+"""ctypes binding of libgm_spgemm.so (include/gm_spgemm.h), same names as the C ABI.
+
+Argument marshalling only: every step of the SpGEMM runs in the CUDA library.
+torch supplies device memory and the stream. There is no CPU fallback: when the
+library is missing or cannot load, ``load()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgm_spgemm.so")
+
+GM_MAX_LEVELS = 16
+GM_NUM_STAGES = 12
+STATUS_NAMES = ["GM_OK", "GM_ERR_INVALID_ARG", "GM_ERR_DIM_MISMATCH", "GM_ERR_INDEX_OVERFLOW", "GM_ERR_OOM",
+                "GM_ERR_WORKSPACE", "GM_ERR_CUDA", "GM_ERR_DEVICE_TIMEOUT", "GM_ERR_STATE", "GM_ERR_BAD_INDEX"]
+GM_FLAG_TIMING, GM_FLAG_KEEP_INTERMEDIATES, GM_FLAG_LOG = 1, 2, 4
+GM_PIPE_AUTO, GM_PIPE_UNFUSED, GM_PIPE_FUSED_HISTO = 0, 1, 2
+(GM_DBG_IP_COUNTS, GM_DBG_HEAVY_ROWS, GM_DBG_LIGHT_ROWS, GM_DBG_CHAT_ROWPTR, GM_DBG_CHAT_COL, GM_DBG_CHAT_VAL,
+ GM_DBG_REORD_ROWPTR, GM_DBG_REORD_COL, GM_DBG_REORD_VAL, GM_DBG_REORD_CHILD) = range(10)
+STAGES = ["analyze", "transpose", "outer", "histogram", "multisplit", "sym_heavy", "sym_light", "scan",
+          "num_heavy", "num_light", "other", "unused"]
+EXPORTS = ["gm_set_allocator", "gm_spgemm_params", "gm_spgemm_analyze", "gm_spgemm_symbolic", "gm_spgemm_numeric",
+           "gm_spgemm_plan_info", "gm_spgemm_plan_destroy", "gm_status_string", "gm_spgemm_debug_copy"]
+
+
+class gm_csr(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int64), ("n_cols", ctypes.c_int64), ("nnz", ctypes.c_int64),
+                ("row_ptr", ctypes.c_void_p), ("col_idx", ctypes.c_void_p), ("vals", ctypes.c_void_p)]
+
+
+class gm_config(ctypes.Structure):
+    _fields_ = [("smem_budget_bytes", ctypes.c_int64), ("tau", ctypes.c_int64), ("dense_width", ctypes.c_int64),
+                ("n_chunks_max", ctypes.c_int64), ("workspace_cap_bytes", ctypes.c_int64),
+                ("pipeline", ctypes.c_int32), ("flags", ctypes.c_int32)]
+
+
+class gm_params(ctypes.Structure):
+    _fields_ = [("s_lm", ctypes.c_int64), ("tau", ctypes.c_int64), ("dense_width", ctypes.c_int64),
+                ("n_chunks_required", ctypes.c_int64), ("n_chunks_max", ctypes.c_int64),
+                ("n_levels", ctypes.c_int64), ("v_chunks", ctypes.c_int64 * GM_MAX_LEVELS),
+                ("widths", ctypes.c_int64 * GM_MAX_LEVELS)]
+
+
+class gm_plan_info(ctypes.Structure):
+    _fields_ = [("params", gm_params), ("n_rows", ctypes.c_int64), ("n_cols", ctypes.c_int64),
+                ("n_heavy_rows", ctypes.c_int64), ("n_light_rows", ctypes.c_int64),
+                ("n_empty_rows", ctypes.c_int64), ("ip_total", ctypes.c_int64), ("ip_heavy", ctypes.c_int64),
+                ("c_nnz", ctypes.c_int64), ("chat_bytes", ctypes.c_int64), ("n_batches", ctypes.c_int64),
+                ("workspace_peak_bytes", ctypes.c_int64), ("n_leaves", ctypes.c_int64),
+                ("keeps_reordered", ctypes.c_int32), ("pipeline", ctypes.c_int32),
+                ("cuda_error", ctypes.c_int32), ("device_status", ctypes.c_int32),
+                ("stage_ms", ctypes.c_float * GM_NUM_STAGES)]
+
+
+class GmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        name = STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else str(status)
+        super().__init__(f"{where}: {name}")
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libgm_spgemm.so (built by ``build.build()``); raises when it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library {path} is missing: run __graft_entry__.build() first")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER
+    lib.gm_set_allocator.restype = None
+    lib.gm_set_allocator.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    lib.gm_spgemm_params.restype = ctypes.c_int
+    lib.gm_spgemm_params.argtypes = [ctypes.c_int64, P(gm_config), P(gm_params)]
+    lib.gm_spgemm_analyze.restype = ctypes.c_int
+    lib.gm_spgemm_analyze.argtypes = [P(gm_csr), P(gm_csr), P(gm_config), ctypes.c_void_p, P(ctypes.c_void_p)]
+    lib.gm_spgemm_symbolic.restype = ctypes.c_int
+    lib.gm_spgemm_symbolic.argtypes = [ctypes.c_void_p, ctypes.c_void_p, P(ctypes.c_int64)]
+    lib.gm_spgemm_numeric.restype = ctypes.c_int
+    lib.gm_spgemm_numeric.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    lib.gm_spgemm_plan_info.restype = ctypes.c_int
+    lib.gm_spgemm_plan_info.argtypes = [ctypes.c_void_p, P(gm_plan_info)]
+    lib.gm_spgemm_plan_destroy.restype = None
+    lib.gm_spgemm_plan_destroy.argtypes = [ctypes.c_void_p]
+    lib.gm_status_string.restype = ctypes.c_char_p
+    lib.gm_status_string.argtypes = [ctypes.c_int]
+    lib.gm_spgemm_debug_copy.restype = ctypes.c_int
+    lib.gm_spgemm_debug_copy.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                         ctypes.c_int64, P(ctypes.c_int64)]
+    _lib = lib
+    return lib
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise GmError(rc, where)
+
+
+def make_config(**kw) -> gm_config:
+    cfg = gm_config()
+    for k, v in kw.items():
+        setattr(cfg, k, int(v))
+    return cfg
+
+
+def gm_status_string(status: int) -> str:
+    return load().gm_status_string(status).decode()
+
+
+def gm_spgemm_params(c_m: int, cfg: gm_config | None = None) -> gm_params:
+    out = gm_params()
+    _check(load().gm_spgemm_params(int(c_m), ctypes.byref(cfg) if cfg else None, ctypes.byref(out)),
+           "gm_spgemm_params")
+    return out
+
+
+@dataclass
+class DeviceCSR:
+    """CSR operand whose arrays are torch CUDA tensors (int64 / int32 / float64)."""
+
+    n_rows: int
+    n_cols: int
+    row_ptr: object
+    col: object
+    val: object
+
+    @property
+    def nnz(self) -> int:
+        return int(self.col.numel())
+
+    def desc(self) -> gm_csr:
+        return gm_csr(self.n_rows, self.n_cols, self.nnz, self.row_ptr.data_ptr(),
+                      self.col.data_ptr() if self.nnz else None, self.val.data_ptr() if self.nnz else None)
+
+
+def to_device(M, device="cuda") -> DeviceCSR:
+    """Copy a host CSR (``inputs.CSR``) to torch CUDA tensors."""
+    import torch
+    return DeviceCSR(M.n_rows, M.n_cols, torch.from_numpy(M.row_ptr).to(device),
+                     torch.from_numpy(M.col).to(device), torch.from_numpy(M.val).to(device))
+
+
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def gm_spgemm_analyze(A: DeviceCSR, B: DeviceCSR, cfg: gm_config | None = None, stream=None):
+    plan = ctypes.c_void_p()
+    a, b = A.desc(), B.desc()
+    _check(load().gm_spgemm_analyze(ctypes.byref(a), ctypes.byref(b), ctypes.byref(cfg) if cfg else None,
+                                    _stream_handle(stream), ctypes.byref(plan)), "gm_spgemm_analyze")
+    return plan
+
+
+def gm_spgemm_symbolic(plan, c_row_ptr) -> int:
+    nnz = ctypes.c_int64(-1)
+    _check(load().gm_spgemm_symbolic(plan, c_row_ptr.data_ptr(), ctypes.byref(nnz)), "gm_spgemm_symbolic")
+    return int(nnz.value)
+
+
+def gm_spgemm_numeric(plan, c_col, c_val):
+    _check(load().gm_spgemm_numeric(plan, c_col.data_ptr() if c_col.numel() else None,
+                                    c_val.data_ptr() if c_val.numel() else None), "gm_spgemm_numeric")
+
+
+def gm_spgemm_plan_info(plan) -> gm_plan_info:
+    out = gm_plan_info()
+    _check(load().gm_spgemm_plan_info(plan, ctypes.byref(out)), "gm_spgemm_plan_info")
+    return out
+
+
+def gm_spgemm_plan_destroy(plan):
+    load().gm_spgemm_plan_destroy(plan)
+
+
+def gm_spgemm_debug_copy(plan, view: int, level: int = 0):
+    """Host numpy copy of a plan array (see the GM_DBG_* views of the header)."""
+    import numpy as np
+    size = ctypes.c_int64(0)
+    _check(load().gm_spgemm_debug_copy(plan, view, level, None, 0, ctypes.byref(size)), "gm_spgemm_debug_copy")
+    dtype = {GM_DBG_HEAVY_ROWS: np.int32, GM_DBG_LIGHT_ROWS: np.int32, GM_DBG_CHAT_COL: np.int32,
+             GM_DBG_REORD_COL: np.int32, GM_DBG_CHAT_VAL: np.float64, GM_DBG_REORD_VAL: np.float64}.get(view, np.int64)
+    out = np.empty(size.value // np.dtype(dtype).itemsize, dtype=dtype)
+    if size.value:
+        _check(load().gm_spgemm_debug_copy(plan, view, level, out.ctypes.data, size.value, None),
+               "gm_spgemm_debug_copy")
+    return out
+
+
+def spgemm(A: DeviceCSR, B: DeviceCSR, cfg: gm_config | None = None, stream=None, return_info: bool = False):
+    """C = A @ B on the GPU: analyze, symbolic, allocate C with torch, numeric."""
+    import torch
+    dev = A.row_ptr.device
+    plan = gm_spgemm_analyze(A, B, cfg, stream)
+    try:
+        c_rp = torch.empty(A.n_rows + 1, dtype=torch.int64, device=dev)
+        nnz = gm_spgemm_symbolic(plan, c_rp)
+        c_col = torch.empty(nnz, dtype=torch.int32, device=dev)
+        c_val = torch.empty(nnz, dtype=torch.float64, device=dev)
+        gm_spgemm_numeric(plan, c_col, c_val)
+        info = gm_spgemm_plan_info(plan) if return_info else None
+    finally:
+        gm_spgemm_plan_destroy(plan)
+    C = DeviceCSR(A.n_rows, B.n_cols, c_rp, c_col, c_val)
+    return (C, info) if return_info else C

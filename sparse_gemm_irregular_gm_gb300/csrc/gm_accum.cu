@@ -1,0 +1,422 @@
+// gm_accum.cu -- local-memory accumulators of gMAGNUS (Sec. III-E, Algorithm 3
+// lines 21-22 and 26-27). Nothing here falls back to global-memory accumulation.
+//
+// * Light rows (u(i) <= tau): rows are binned by u(i) and each bin gets a work
+//   group size (the binning of Sec. III-E). Rows with u <= 256 use one warp and a
+//   per-warp shared array: the products are sorted by column (bitonic network)
+//   and equal columns are merged. Larger rows use one block and a shared hash
+//   table of >= 2u slots (load factor alpha = 2, modulo hashing, linear probing),
+//   then a bitonic sort of the occupied slots (Sec. III-E).
+// * Chunks of C-hat_reord narrower than the dense width: a shared bitmap of the
+//   chunk's columns gives nnz (symbolic) and, by a prefix sum over the bitmap
+//   words, the rank of every column, so values are summed straight into their
+//   sorted output slot (the dense accumulator with the bitmap prefix sum of
+//   Sec. III-E, indexed by rank instead of by column).
+// * Light chunks of a wider level: the block hash accumulator with list input.
+#include <algorithm>
+#include <climits>
+
+#include "gm_device.cuh"
+#include "gm_internal.h"
+
+namespace gm {
+
+namespace {
+
+constexpr int32_t kEmpty = -1;
+
+// ---- light rows: one warp per row, sort-based ---------------------------------
+
+template <bool SYM, int CAPW, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32) k_light_warp(LightArgs a) {
+  __shared__ int32_t s_key[WARPS][CAPW];
+  __shared__ double s_val[SYM ? 1 : WARPS][SYM ? 1 : CAPW];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int32_t* key = s_key[w];
+  double* val = SYM ? nullptr : s_val[w];
+  for (int64_t item = static_cast<int64_t>(blockIdx.x) * WARPS + w; item < a.n_items;
+       item += static_cast<int64_t>(gridDim.x) * WARPS) {
+    const int64_t r = a.rows[item];
+    const int64_t lo = a.a_rp[r], hi = a.a_rp[r + 1];
+    int pos = 0;
+    for (int64_t p0 = lo; p0 < hi; p0 += 32) {
+      const int64_t p = p0 + lane;
+      int len = 0;
+      int64_t bs = 0;
+      double av = 0.0;
+      if (p < hi) {
+        const int k = a.a_col[p];
+        bs = a.b_rp[k];
+        len = static_cast<int>(a.b_rp[k + 1] - bs);
+        if (!SYM) av = a.a_val[p];
+      }
+      const int inc = warp_inclusive_scan(len);
+      const int off = pos + inc - len;
+      for (int q = 0; q < len; ++q) {
+        if (off + q < CAPW) {
+          key[off + q] = a.b_col[bs + q];
+          if (!SYM) val[off + q] = av * a.b_val[bs + q];
+        }
+      }
+      pos += __shfl_sync(kFull, inc, 31);
+    }
+    const int n = pos;
+    if (n > CAPW && lane == 0) atomicOr(a.status, kStInternal);
+    for (int i = n + lane; i < CAPW; i += 32) key[i] = INT_MAX;
+    __syncwarp();
+    for (int k = 2; k <= CAPW; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = lane; i < CAPW; i += 32) {
+          const int ixj = i ^ j;
+          if (ixj > i) {
+            const int32_t ki = key[i], kj = key[ixj];
+            const bool up = (i & k) == 0;
+            if ((ki > kj) == up) {
+              key[i] = kj;
+              key[ixj] = ki;
+              if (!SYM) {
+                const double t = val[i];
+                val[i] = val[ixj];
+                val[ixj] = t;
+              }
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
+    const int nn = min(n, CAPW);
+    int run = 0;
+    const int64_t out = SYM ? 0 : a.c_rp[r];
+    for (int i0 = 0; i0 < nn; i0 += 32) {
+      const int i = i0 + lane;
+      const bool head = i < nn && (i == 0 || key[i] != key[i - 1]);
+      const unsigned hb = __ballot_sync(kFull, head);
+      if (!SYM && head) {
+        double s = 0.0;
+        const int32_t c = key[i];
+        for (int t = i; t < nn && key[t] == c; ++t) s += val[t];
+        const int rank = run + __popc(hb & lanemask_lt());
+        a.c_col[out + rank] = c;
+        a.c_val[out + rank] = s;
+      }
+      run += __popc(hb);
+    }
+    if (SYM && lane == 0) a.c_rp[r] = run;
+    __syncwarp();
+  }
+}
+
+// ---- block hash accumulator (light rows and light chunks) ---------------------
+
+template <bool POW2>
+__device__ __forceinline__ int slot_of(uint32_t c, int cap) {
+  return POW2 ? static_cast<int>(c & static_cast<uint32_t>(cap - 1)) : static_cast<int>(c % static_cast<uint32_t>(cap));
+}
+
+// Insert column c; returns the slot and sets *fresh when the key was new.
+template <bool POW2>
+__device__ __forceinline__ int hash_insert(int32_t* keys, int cap, int32_t c, bool* fresh, bool* full) {
+  int s = slot_of<POW2>(static_cast<uint32_t>(c), cap);
+  for (int t = 0; t < cap; ++t) {
+    const int32_t old = atomicCAS(&keys[s], kEmpty, c);
+    if (old == kEmpty) {
+      *fresh = true;
+      return s;
+    }
+    if (old == c) return s;
+    s = (s + 1 == cap) ? 0 : s + 1;
+  }
+  *full = true;
+  return -1;
+}
+
+// After accumulation: move the occupied slots to the front (order kept), sort
+// them by column and write nnz entries at out. keys/vals hold cap slots.
+__device__ void compact_sort_write(int32_t* keys, double* vals, int cap, int nnz, int32_t* c_col, double* c_val,
+                                   int64_t out, int64_t col_base) {
+  __shared__ int ws[33];
+  int run = 0;
+  for (int base = 0; base < cap; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    const int32_t k = i < cap ? keys[i] : kEmpty;
+    const double v = i < cap ? vals[i] : 0.0;
+    const int flag = k != kEmpty;
+    int tot;
+    const int pre = block_exclusive_scan(flag, ws, &tot);
+    __syncthreads();
+    if (flag) {
+      keys[run + pre] = k;
+      vals[run + pre] = v;
+    }
+    run += tot;
+    __syncthreads();
+  }
+  int P = 1;
+  while (P < nnz) P <<= 1;
+  for (int i = nnz + threadIdx.x; i < P; i += blockDim.x) keys[i] = INT_MAX;
+  __syncthreads();
+  for (int k = 2; k <= P; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < P; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const int32_t ki = keys[i], kj = keys[ixj];
+          const bool up = (i & k) == 0;
+          if ((ki > kj) == up) {
+            keys[i] = kj;
+            keys[ixj] = ki;
+            const double t = vals[i];
+            vals[i] = vals[ixj];
+            vals[ixj] = t;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < nnz; i += blockDim.x) {
+    c_col[out + i] = static_cast<int32_t>(col_base + keys[i]);
+    c_val[out + i] = vals[i];
+  }
+}
+
+template <bool SYM, bool POW2>
+__global__ void k_light_hash(LightArgs a, int cap) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  double* vals = reinterpret_cast<double*>(smem);
+  int32_t* keys = reinterpret_cast<int32_t*>(smem + (SYM ? 0 : static_cast<size_t>(cap) * 8));
+  __shared__ int ws[33];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  for (int64_t item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+    const int64_t r = a.rows[item];
+    for (int i = threadIdx.x; i < cap; i += blockDim.x) {
+      keys[i] = kEmpty;
+      if (!SYM) vals[i] = 0.0;
+    }
+    __syncthreads();
+    int fresh_count = 0;
+    bool full = false;
+    for (int64_t p = a.a_rp[r] + warp; p < a.a_rp[r + 1]; p += nwarps) {
+      const int k = a.a_col[p];
+      const double av = SYM ? 0.0 : a.a_val[p];
+      for (int64_t q = a.b_rp[k] + lane; q < a.b_rp[k + 1]; q += 32) {
+        bool fresh = false;
+        const int s = hash_insert<POW2>(keys, cap, a.b_col[q], &fresh, &full);
+        fresh_count += fresh;
+        if (!SYM && s >= 0) atomicAdd(&vals[s], av * a.b_val[q]);
+      }
+    }
+    if (full) atomicOr(a.status, kStHashFull);
+    __syncthreads();
+    if (SYM) {
+      int tot;
+      block_exclusive_scan(fresh_count, ws, &tot);
+      if (threadIdx.x == 0) a.c_rp[r] = tot;
+    } else {
+      const int64_t out = a.c_rp[r];
+      const int nnz = static_cast<int>(a.c_rp[r + 1] - out);
+      compact_sort_write(keys, vals, cap, nnz, a.c_col, a.c_val, out, 0);
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+namespace {
+
+__device__ __forceinline__ int64_t leaf_col_base(const ListArgs& a, int64_t child_local) {
+  const int64_t parent = child_local / a.v;
+  const int64_t base = a.parent_colbase ? a.parent_colbase[parent] : 0;
+  return base + (child_local % a.v) * a.width;
+}
+
+// Chunk of width <= dense width: bitmap of its columns, prefix sum over the
+// bitmap words, values summed into their rank (= sorted output position).
+template <bool SYM>
+__global__ void k_leaf_bitmap(ListArgs a, int nwords, int cap_vals) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  double* vals = reinterpret_cast<double*>(smem);
+  int32_t* cols = reinterpret_cast<int32_t*>(smem + (SYM ? 0 : static_cast<size_t>(cap_vals) * 8));
+  uint32_t* bm = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(cols) + (SYM ? 0 : static_cast<size_t>(cap_vals) * 4));
+  int* pre = reinterpret_cast<int*>(bm + nwords);
+  __shared__ int ws[33];
+  const int T = blockDim.x;
+  const int per = (nwords + T - 1) / T;
+  const int w0 = threadIdx.x * per, w1 = min(nwords, w0 + per);
+  for (int64_t item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+    const int64_t m = a.items[item];
+    const int64_t lo = a.rp[m], hi = a.rp[m + 1];
+    const int64_t child_local = a.child_of ? a.child_of[m] : m;
+    for (int w = threadIdx.x; w < nwords; w += T) bm[w] = 0u;
+    __syncthreads();
+    for (int64_t e = lo + threadIdx.x; e < hi; e += T) {
+      const uint32_t c = static_cast<uint32_t>(a.col[e]);
+      atomicOr(&bm[c >> 5], 1u << (c & 31));
+    }
+    __syncthreads();
+    int acc = 0;
+    for (int w = w0; w < w1; ++w) acc += __popc(bm[w]);
+    int nnz;
+    int run = block_exclusive_scan(acc, ws, &nnz);
+    if (SYM) {
+      if (threadIdx.x == 0) a.nnz_out[a.child_base + child_local] = nnz;
+      __syncthreads();
+      continue;
+    }
+    if (nnz > cap_vals) {
+      if (threadIdx.x == 0) atomicOr(a.status, kStInternal);
+      __syncthreads();
+      continue;
+    }
+    for (int w = w0; w < w1; ++w) {
+      pre[w] = run;
+      uint32_t bits = bm[w];
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        cols[run++] = w * 32 + b;
+      }
+    }
+    for (int r = threadIdx.x; r < nnz; r += T) vals[r] = 0.0;
+    __syncthreads();
+    for (int64_t e = lo + threadIdx.x; e < hi; e += T) {
+      const uint32_t c = static_cast<uint32_t>(a.col[e]);
+      const int w = c >> 5;
+      const int r = pre[w] + __popc(bm[w] & ((1u << (c & 31)) - 1u));
+      atomicAdd(&vals[r], a.val[e]);
+    }
+    __syncthreads();
+    const int64_t out = a.off_in[a.child_base + child_local];
+    const int64_t cb = leaf_col_base(a, child_local);
+    for (int r = threadIdx.x; r < nnz; r += T) {
+      a.c_col[out + r] = static_cast<int32_t>(cb + cols[r]);
+      a.c_val[out + r] = vals[r];
+    }
+    __syncthreads();
+  }
+}
+
+// Light chunk of a level wider than the dense width: block hash accumulator.
+template <bool SYM, bool POW2>
+__global__ void k_leaf_hash(ListArgs a, int cap) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  double* vals = reinterpret_cast<double*>(smem);
+  int32_t* keys = reinterpret_cast<int32_t*>(smem + (SYM ? 0 : static_cast<size_t>(cap) * 8));
+  __shared__ int ws[33];
+  for (int64_t item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+    const int64_t m = a.items[item];
+    const int64_t child_local = a.child_of ? a.child_of[m] : m;
+    for (int i = threadIdx.x; i < cap; i += blockDim.x) {
+      keys[i] = kEmpty;
+      if (!SYM) vals[i] = 0.0;
+    }
+    __syncthreads();
+    int fresh_count = 0;
+    bool full = false;
+    for (int64_t e = a.rp[m] + threadIdx.x; e < a.rp[m + 1]; e += blockDim.x) {
+      bool fresh = false;
+      const int s = hash_insert<POW2>(keys, cap, a.col[e], &fresh, &full);
+      fresh_count += fresh;
+      if (!SYM && s >= 0) atomicAdd(&vals[s], a.val[e]);
+    }
+    if (full) atomicOr(a.status, kStHashFull);
+    int nnz;
+    block_exclusive_scan(fresh_count, ws, &nnz);
+    if (SYM) {
+      if (threadIdx.x == 0) a.nnz_out[a.child_base + child_local] = nnz;
+    } else {
+      compact_sort_write(keys, vals, cap, nnz, a.c_col, a.c_val, a.off_in[a.child_base + child_local],
+                         leaf_col_base(a, child_local));
+    }
+    __syncthreads();
+  }
+}
+
+template <class K>
+void set_smem(K fn, size_t smem) {
+  if (smem > 48 * 1024) cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+}
+
+unsigned item_grid(int64_t n_items, int per_sm) {
+  int64_t g = n_items;
+  const int64_t cap = 152LL * per_sm * 4;
+  if (g > cap) g = cap;
+  return static_cast<unsigned>(g < 1 ? 1 : g);
+}
+
+int hash_threads(int cap) { return cap <= 1024 ? 128 : cap <= 2048 ? 256 : cap <= 4096 ? 512 : 1024; }
+
+}  // namespace
+
+int64_t light_bin_ub(int b) { return int64_t(16) << b; }  // bins 1..9: 32 .. 8192
+
+int light_bin_cap(int b, int64_t tau) {
+  if (b <= kLightWarpBins) return static_cast<int>(light_bin_ub(b));
+  if (b <= 9) return static_cast<int>(2 * light_bin_ub(b));
+  return static_cast<int>(2 * tau);
+}
+
+void launch_light_rows(const LightArgs& a, int cap, bool symbolic, cudaStream_t s) {
+  if (a.n_items <= 0) return;
+  if (cap <= 256) {
+    constexpr int W = 8;
+    const unsigned g = static_cast<unsigned>(std::min<int64_t>((a.n_items + W - 1) / W, 152LL * 64));
+    switch (cap) {
+      case 32: symbolic ? k_light_warp<true, 32, W><<<g, W * 32, 0, s>>>(a) : k_light_warp<false, 32, W><<<g, W * 32, 0, s>>>(a); break;
+      case 64: symbolic ? k_light_warp<true, 64, W><<<g, W * 32, 0, s>>>(a) : k_light_warp<false, 64, W><<<g, W * 32, 0, s>>>(a); break;
+      case 128: symbolic ? k_light_warp<true, 128, W><<<g, W * 32, 0, s>>>(a) : k_light_warp<false, 128, W><<<g, W * 32, 0, s>>>(a); break;
+      default: symbolic ? k_light_warp<true, 256, W><<<g, W * 32, 0, s>>>(a) : k_light_warp<false, 256, W><<<g, W * 32, 0, s>>>(a); break;
+    }
+    return;
+  }
+  const bool pow2 = (cap & (cap - 1)) == 0;
+  const size_t smem = static_cast<size_t>(cap) * (symbolic ? 4 : 12);
+  const int T = hash_threads(cap);
+  const unsigned g = item_grid(a.n_items, 2);
+  if (symbolic) {
+    auto fn = pow2 ? k_light_hash<true, true> : k_light_hash<true, false>;
+    set_smem(fn, smem);
+    fn<<<g, T, smem, s>>>(a, cap);
+  } else {
+    auto fn = pow2 ? k_light_hash<false, true> : k_light_hash<false, false>;
+    set_smem(fn, smem);
+    fn<<<g, T, smem, s>>>(a, cap);
+  }
+}
+
+int leaf_bitmap_smem(int64_t width, int cap_vals, bool symbolic) {
+  const int64_t nwords = (width + 31) / 32;
+  return static_cast<int>(nwords * 8 + (symbolic ? 0 : static_cast<int64_t>(cap_vals) * 12));
+}
+
+void launch_leaf_bitmap(const ListArgs& a, int cap_vals, bool symbolic, cudaStream_t s) {
+  if (a.n_items <= 0) return;
+  const int nwords = static_cast<int>((a.width + 31) / 32);
+  const size_t smem = static_cast<size_t>(leaf_bitmap_smem(a.width, cap_vals, symbolic));
+  const int T = symbolic ? 256 : (cap_vals <= 1024 ? 256 : cap_vals <= 4096 ? 512 : 1024);
+  const unsigned g = item_grid(a.n_items, 4);
+  auto fn = symbolic ? k_leaf_bitmap<true> : k_leaf_bitmap<false>;
+  set_smem(fn, smem);
+  fn<<<g, T, smem, s>>>(a, nwords, cap_vals);
+}
+
+void launch_leaf_hash(const ListArgs& a, int cap, bool symbolic, cudaStream_t s) {
+  if (a.n_items <= 0) return;
+  const bool pow2 = (cap & (cap - 1)) == 0;
+  const size_t smem = static_cast<size_t>(cap) * (symbolic ? 4 : 12);
+  const int T = hash_threads(cap);
+  const unsigned g = item_grid(a.n_items, 2);
+  if (symbolic) {
+    auto fn = pow2 ? k_leaf_hash<true, true> : k_leaf_hash<true, false>;
+    set_smem(fn, smem);
+    fn<<<g, T, smem, s>>>(a, cap);
+  } else {
+    auto fn = pow2 ? k_leaf_hash<false, true> : k_leaf_hash<false, false>;
+    set_smem(fn, smem);
+    fn<<<g, T, smem, s>>>(a, cap);
+  }
+}
+
+}  // namespace gm

@@ -1,0 +1,1074 @@
+// gm_api.cu -- the C ABI (include/gm_spgemm.h) and the host driver of gMAGNUS
+// Algorithm 3: setup, heavy-row batches through outer product and hierarchical
+// multisplit, light rows through the binned shared-memory accumulators, and the
+// prefix sums that place every row and chunk of C.
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <memory>
+#include <vector>
+
+#include "gm_device.cuh"
+#include "gm_internal.h"
+
+namespace gm {
+
+// ---- workspace allocation ------------------------------------------------------
+
+static gm_alloc_fn g_alloc = nullptr;
+static gm_free_fn g_free = nullptr;
+static void* g_ctx = nullptr;
+static std::atomic<int64_t> g_ws_now{0}, g_ws_peak{0};
+
+void* ws_alloc(size_t bytes, cudaStream_t s) {
+  if (bytes == 0) return nullptr;
+  void* p = nullptr;
+  if (g_alloc) {
+    p = g_alloc(g_ctx, bytes, s);
+  } else if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    p = nullptr;
+  }
+  if (p) {
+    const int64_t now = g_ws_now += static_cast<int64_t>(bytes);
+    int64_t pk = g_ws_peak.load();
+    while (now > pk && !g_ws_peak.compare_exchange_weak(pk, now)) {
+    }
+  }
+  return p;
+}
+
+void ws_free(void* p, size_t bytes, cudaStream_t s) {
+  if (!p) return;
+  g_ws_now -= static_cast<int64_t>(bytes);
+  if (g_free) g_free(g_ctx, p, bytes, s);
+  else cudaFreeAsync(p, s);
+}
+
+// ---- small helper kernels --------------------------------------------------------
+
+namespace {
+
+__global__ void k_sub_to_u64(const int64_t* __restrict__ src, int64_t n, int64_t base,
+                             unsigned long long* __restrict__ dst) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    dst[i] = static_cast<unsigned long long>(src[i] - base);
+}
+__global__ void k_sub_i64(const int64_t* __restrict__ src, int64_t n, int64_t base, int64_t* __restrict__ dst) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    dst[i] = src[i] - base;
+}
+__global__ void k_i32_to_i64(const int32_t* __restrict__ src, int64_t n, int64_t add, int64_t* __restrict__ dst) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    dst[i] = static_cast<int64_t>(src[i]) + add;
+}
+// heavy children first: bin 0 when count > tau, else bin 1
+__global__ void k_heavy_bin(const unsigned long long* __restrict__ cnt, int64_t n, int64_t tau,
+                            uint8_t* __restrict__ bin) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    bin[i] = cnt[i] > static_cast<unsigned long long>(tau) ? 0 : 1;
+}
+// mapped counts: out[m] = cnt[perm[m]] (perm null: identity)
+__global__ void k_mapped_counts(const unsigned long long* __restrict__ cnt, const int32_t* __restrict__ perm,
+                                int64_t n, int64_t* __restrict__ out, int64_t* __restrict__ inv) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t m = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; m < n; m += stride) {
+    const int64_t c = perm ? perm[m] : m;
+    out[m] = static_cast<int64_t>(cnt[c]);
+    if (inv) inv[c] = m;
+  }
+}
+// column base of each new parent: base_prev[g / v] + (g % v) * w, g = global child id at the previous level
+__global__ void k_child_colbase(const int64_t* __restrict__ ids, int64_t n, const int64_t* __restrict__ base_prev,
+                                int64_t v, int64_t w, int64_t* __restrict__ out) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int64_t g = ids[i];
+    out[i] = (base_prev ? base_prev[g / v] : 0) + (g % v) * w;
+  }
+}
+__global__ void k_i32_gather_to_i64(const int32_t* __restrict__ perm, int64_t n, int64_t add,
+                                    int64_t* __restrict__ out) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    out[i] = perm[i] + add;
+}
+
+}  // namespace
+
+static void sub_to_u64(const int64_t* src, int64_t n, int64_t base, unsigned long long* dst, cudaStream_t s) {
+  if (n > 0) k_sub_to_u64<<<grid_for(n, 256), 256, 0, s>>>(src, n, base, dst);
+}
+static void sub_i64(const int64_t* src, int64_t n, int64_t base, int64_t* dst, cudaStream_t s) {
+  if (n > 0) k_sub_i64<<<grid_for(n, 256), 256, 0, s>>>(src, n, base, dst);
+}
+static void i32_to_i64(const int32_t* src, int64_t n, int64_t add, int64_t* dst, cudaStream_t s) {
+  if (n > 0) k_i32_to_i64<<<grid_for(n, 256), 256, 0, s>>>(src, n, add, dst);
+}
+
+// ---- parameters (Sec. III-D) -----------------------------------------------------
+
+static int64_t floor_pow2(int64_t x) {
+  int64_t p = 1;
+  while (p * 2 <= x) p *= 2;
+  return p;
+}
+static int64_t next_pow2(int64_t x) {
+  int64_t p = 1;
+  while (p < x) p *= 2;
+  return p;
+}
+static int ilog2(int64_t x) {
+  int l = 0;
+  while ((int64_t(1) << l) < x) ++l;
+  return l;
+}
+static bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+constexpr int64_t kSizeCol = 4, kSizeVal = 8, kSizeRowPtr = 8, kSizeHisto = 4, kSizeBitmap = 1, kSubGroups = 32;
+constexpr int64_t kDefaultSmem = 232448;  // opt-in shared memory per block on sm_103a
+
+// GetMagnusParams: Eq. (4) tau, n_denseNumeric, Eq. (5)-(6) n_chunksMax, Eq. (7) levels.
+static gm_status compute_params(int64_t c_m, const gm_config* cfg, int64_t smem_dev, gm_params* out) {
+  if (!out || c_m < 1) return GM_ERR_INVALID_ARG;
+  gm_params p;
+  std::memset(&p, 0, sizeof(p));
+  p.s_lm = (cfg && cfg->smem_budget_bytes) ? cfg->smem_budget_bytes : smem_dev;
+  if (p.s_lm < 1024 || p.s_lm > smem_dev) return GM_ERR_INVALID_ARG;
+  const int64_t tau_eq4 = p.s_lm / (2 * (kSizeCol + kSizeVal));
+  p.tau = (cfg && cfg->tau) ? cfg->tau : tau_eq4;
+  if (p.tau < 1 || p.tau > tau_eq4) return GM_ERR_INVALID_ARG;
+  const int64_t n_dense = p.s_lm / (kSizeVal + kSizeBitmap);
+  p.dense_width = (cfg && cfg->dense_width) ? cfg->dense_width : floor_pow2(n_dense);
+  if (!is_pow2(p.dense_width) || p.dense_width * 12 + p.dense_width / 4 > smem_dev) return GM_ERR_INVALID_ARG;
+  p.n_chunks_required = next_pow2((c_m + p.dense_width - 1) / p.dense_width);
+  const int64_t n_min = p.s_lm / (2 * (kSizeCol + kSizeVal));
+  const int64_t n_gr = (n_min - 1 + p.tau - 1) / p.tau + 1;
+  const int64_t ncm_raw = (p.s_lm - n_min * (kSizeCol + kSizeVal) - kSizeHisto) /
+                          (n_gr * kSubGroups * kSizeHisto + kSizeRowPtr * n_gr);
+  if (cfg && cfg->n_chunks_max) {
+    if (!is_pow2(cfg->n_chunks_max) || cfg->n_chunks_max < 2) return GM_ERR_INVALID_ARG;
+    p.n_chunks_max = cfg->n_chunks_max;
+  } else {
+    if (ncm_raw < 2) return GM_ERR_INVALID_ARG;
+    p.n_chunks_max = floor_pow2(ncm_raw);
+  }
+  const int64_t req = p.n_chunks_required;
+  if (req == 1) {
+    p.n_levels = 0;
+  } else if (req <= p.n_chunks_max) {
+    p.n_levels = 1;
+    p.v_chunks[0] = req;
+  } else {
+    const int lr = ilog2(req), lm = ilog2(p.n_chunks_max);
+    p.n_levels = (lr + lm - 1) / lm;
+    if (p.n_levels > GM_MAX_LEVELS) return GM_ERR_INDEX_OVERFLOW;
+    int64_t prod = 1;
+    for (int64_t i = 0; i + 1 < p.n_levels; ++i) {
+      p.v_chunks[i] = p.n_chunks_max;
+      prod *= p.n_chunks_max;
+    }
+    p.v_chunks[p.n_levels - 1] = req / prod;
+  }
+  int64_t w = p.dense_width * req;
+  for (int64_t i = 0; i < p.n_levels; ++i) {
+    w /= p.v_chunks[i];
+    p.widths[i] = w;
+  }
+  if (p.dense_width * req > (int64_t(1) << 32)) return GM_ERR_INDEX_OVERFLOW;
+  *out = p;
+  return GM_OK;
+}
+
+}  // namespace gm
+
+namespace gm {
+
+namespace {
+__global__ void k_row_len(const int64_t* __restrict__ rp, const int32_t* __restrict__ idx, int64_t n,
+                          int64_t* __restrict__ out) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int64_t r = idx[i];
+    out[i] = rp[r + 1] - rp[r];
+  }
+}
+}  // namespace
+
+// Device array that keeps its contents when it grows.
+struct GrowBuf {
+  int64_t* p = nullptr;
+  size_t cap = 0;
+  cudaStream_t s = nullptr;
+  bool ensure(size_t need, size_t keep, cudaStream_t stream) {
+    s = stream;
+    if (need <= cap) return true;
+    size_t nc = std::max(need, cap * 2);
+    int64_t* q = static_cast<int64_t*>(ws_alloc(nc * sizeof(int64_t), stream));
+    if (!q) return false;
+    if (p && keep) cudaMemcpyAsync(q, p, keep * sizeof(int64_t), cudaMemcpyDeviceToDevice, stream);
+    if (p) ws_free(p, cap * sizeof(int64_t), stream);
+    p = q;
+    cap = nc;
+    return true;
+  }
+  void release() {
+    if (p) ws_free(p, cap * sizeof(int64_t), s);
+    p = nullptr;
+    cap = 0;
+  }
+  ~GrowBuf() { release(); }
+};
+
+struct StageEv {
+  int stage;
+  cudaEvent_t a, b;
+};
+
+struct LevelDbg {
+  DevBuf<int64_t> rp;
+  DevBuf<int32_t> col;
+  DevBuf<double> val;
+  DevBuf<int64_t> child;
+  int64_t rows = 0, nnz = 0;
+};
+
+// Row bins of the analysis: 0 empty, 1..10 light (u <= tau), 11 heavy.
+constexpr int kRowBins = 12;
+constexpr int kHeavyBin = 11;
+
+}  // namespace gm
+
+struct gm_plan {
+  gm_csr A{}, B{};
+  gm_config cfg{};
+  cudaStream_t s = nullptr;
+  int device = 0;
+  int64_t smem_dev = 0;
+  int64_t c_m = 1;
+  gm_params P{};
+  int L = 0;
+  int state = 0;  // 1 analyzed, 2 symbolic done, 3 numeric done
+  int pipeline = GM_PIPE_FUSED_HISTO;
+  bool timing = false, log = false, keep = false;
+  gm::DevBuf<int> status;
+  gm::DevBuf<int64_t> u;
+  gm::DevBuf<uint8_t> bin;
+  gm::DevBuf<int32_t> rows_by_bin;
+  gm::DevBuf<int64_t> bin_start_d;
+  int64_t bin_start[gm::kMaxBins + 1] = {};
+  int64_t n_heavy = 0, n_light = 0, n_empty = 0, ip_total = 0, ip_heavy = 0;
+  gm::DevBuf<int64_t> chat_rp;      // C-hat.rowPtr over all heavy rows (n_heavy + 1)
+  gm::DevBuf<int64_t> heavy_ids64;  // x_heavy as int64
+  std::vector<int64_t> h_chat_rp;   // host copy of chat_rp
+  std::vector<int64_t> h_anz;       // prefix of nnz(A[x_heavy[h], :])
+  gm::GrowBuf nnz[GM_MAX_LEVELS];        // per level, per child: nnz (symbolic) then output offset
+  gm::GrowBuf heavy_list[GM_MAX_LEVELS]; // per level: global ids of heavy children (parents of the next level)
+  gm::GrowBuf pbase[GM_MAX_LEVELS];      // per level >= 1: column base of each parent
+  int64_t n_par[GM_MAX_LEVELS + 1] = {};
+  int64_t c_nnz = -1;
+  int64_t* c_rp = nullptr;
+  int64_t n_batches = 0, n_leaves = 0, ws_peak = 0;
+  int cuda_error = 0, dev_status = 0;
+  float stage_ms[GM_NUM_STAGES] = {};
+  std::vector<gm::StageEv> evs;
+  // intermediates kept for gm_spgemm_debug_copy
+  gm::DevBuf<int32_t> dbg_chat_col;
+  gm::DevBuf<double> dbg_chat_val;
+  gm::DevBuf<int64_t> dbg_chat_rp;
+  std::vector<std::unique_ptr<gm::LevelDbg>> dbg_levels;
+  bool dbg_ok = false;
+
+  int stage_begin(int stage) {
+    if (!timing) return -1;
+    gm::StageEv e{stage, nullptr, nullptr};
+    cudaEventCreate(&e.a);
+    cudaEventCreate(&e.b);
+    cudaEventRecord(e.a, s);
+    evs.push_back(e);
+    return static_cast<int>(evs.size()) - 1;
+  }
+  void stage_end(int idx) {
+    if (idx >= 0) cudaEventRecord(evs[idx].b, s);
+  }
+  void collect_times() {
+    for (auto& e : evs) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, e.a, e.b) == cudaSuccess) stage_ms[e.stage] += ms;
+      cudaEventDestroy(e.a);
+      cudaEventDestroy(e.b);
+    }
+    evs.clear();
+    cudaGetLastError();
+  }
+  ~gm_plan() {
+    if (!evs.empty()) {
+      cudaStreamSynchronize(s);
+      collect_times();
+    }
+  }
+};
+
+namespace gm {
+
+static gm_status cuda_status(gm_plan* p, cudaError_t e) {
+  if (e == cudaSuccess) return GM_OK;
+  if (p) p->cuda_error = static_cast<int>(e);
+  if (e == cudaErrorMemoryAllocation) return GM_ERR_OOM;
+  return GM_ERR_CUDA;
+}
+
+// Synchronise the plan's stream and turn CUDA errors and device status bits into a status.
+static gm_status sync_check(gm_plan* p) {
+  cudaError_t e = cudaStreamSynchronize(p->s);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_status(p, e);
+  int st = 0;
+  e = cudaMemcpy(&st, p->status.p, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_status(p, e);
+  p->dev_status |= st;
+  if (st & (kStBadARowPtr | kStBadBRowPtr | kStBadACol | kStBadBCol)) return GM_ERR_BAD_INDEX;
+  if (st) return GM_ERR_CUDA;
+  return GM_OK;
+}
+
+static bool env_log() {
+  const char* e = std::getenv("GM_SPGEMM_LOG");
+  return e && e[0] == '1';
+}
+
+static gm_status check_csr(const gm_csr* M) {
+  if (!M || M->n_rows < 0 || M->n_cols < 0 || M->nnz < 0 || !M->row_ptr) return GM_ERR_INVALID_ARG;
+  if (M->nnz > 0 && (!M->col_idx || !M->vals)) return GM_ERR_INVALID_ARG;
+  if (M->n_rows >= (int64_t(1) << 31) || M->n_cols > (int64_t(1) << 31)) return GM_ERR_INDEX_OVERFLOW;
+  return GM_OK;
+}
+
+static gm_status analyze_impl(gm_plan* p) {
+  const cudaStream_t s = p->s;
+  const int64_t n = p->A.n_rows;
+  if (!p->status.alloc(1, s)) return GM_ERR_OOM;
+  cudaMemsetAsync(p->status.p, 0, sizeof(int), s);
+  const int t0 = p->stage_begin(GM_STAGE_ANALYZE);
+  // Validation first: nothing below may index with unchecked row pointers or columns.
+  launch_validate_rowptr(p->A.row_ptr, p->A.n_rows, p->A.nnz, kStBadARowPtr, p->status.p, s);
+  launch_validate_rowptr(p->B.row_ptr, p->B.n_rows, p->B.nnz, kStBadBRowPtr, p->status.p, s);
+  launch_validate_cols(p->A.col_idx, p->A.nnz, p->A.n_cols, kStBadACol, p->status.p, s);
+  launch_validate_cols(p->B.col_idx, p->B.nnz, p->B.n_cols, kStBadBCol, p->status.p, s);
+  gm_status st = sync_check(p);
+  if (st != GM_OK) return st;
+
+  BinSpec spec{};
+  spec.nbins = kRowBins;
+  spec.ub[0] = 0;
+  for (int b = 1; b <= 9; ++b) spec.ub[b] = std::min<int64_t>(light_bin_ub(b), p->P.tau);
+  spec.ub[10] = p->P.tau;
+  spec.ub[kHeavyBin] = INT64_MAX;
+  if (!p->u.alloc(n, s) || !p->bin.alloc(n, s) || !p->rows_by_bin.alloc(n, s) ||
+      !p->bin_start_d.alloc(kRowBins + 1, s))
+    return GM_ERR_OOM;
+  launch_ip_count(p->A.row_ptr, p->A.col_idx, n, p->B.row_ptr, p->u.p, p->bin.p, spec, s);
+  if (!partition_by_bin(p->bin.p, n, kRowBins, p->rows_by_bin.p, p->bin_start_d.p, s)) return GM_ERR_OOM;
+  DevBuf<int64_t> tmp, tot;
+  if (!tmp.alloc(std::max<int64_t>(n, 1), s) || !tot.alloc(2, s)) return GM_ERR_OOM;
+  if (!scan_exclusive_i64(p->u.p, tmp.p, n, tot.p, s)) return GM_ERR_OOM;
+  cudaMemcpyAsync(p->bin_start, p->bin_start_d.p, (kRowBins + 1) * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+  cudaMemcpyAsync(&p->ip_total, tot.p, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+  st = sync_check(p);
+  if (st != GM_OK) return st;
+  p->n_empty = p->bin_start[1] - p->bin_start[0];
+  p->n_heavy = p->bin_start[kRowBins] - p->bin_start[kHeavyBin];
+  p->n_light = p->bin_start[kHeavyBin] - p->bin_start[1];
+
+  // C-hat.rowPtr over the heavy rows and the nnz of their A rows (for batching).
+  const int64_t nh = p->n_heavy;
+  const int32_t* heavy = p->rows_by_bin.p + p->bin_start[kHeavyBin];
+  if (!p->chat_rp.alloc(nh + 1, s) || !p->heavy_ids64.alloc(std::max<int64_t>(nh, 1), s)) return GM_ERR_OOM;
+  DevBuf<int64_t> anz;
+  if (!anz.alloc(nh + 1, s)) return GM_ERR_OOM;
+  cudaMemsetAsync(p->chat_rp.p + nh, 0, sizeof(int64_t), s);
+  cudaMemsetAsync(anz.p + nh, 0, sizeof(int64_t), s);
+  launch_gather_i64(p->u.p, heavy, nh, p->chat_rp.p, s);
+  if (nh > 0) k_row_len<<<grid_for(nh, 256), 256, 0, s>>>(p->A.row_ptr, heavy, nh, anz.p);
+  if (!scan_exclusive_i64(p->chat_rp.p, p->chat_rp.p, nh + 1, nullptr, s)) return GM_ERR_OOM;
+  if (!scan_exclusive_i64(anz.p, anz.p, nh + 1, nullptr, s)) return GM_ERR_OOM;
+  i32_to_i64(heavy, nh, 0, p->heavy_ids64.p, s);
+  p->h_chat_rp.resize(nh + 1);
+  p->h_anz.resize(nh + 1);
+  cudaMemcpyAsync(p->h_chat_rp.data(), p->chat_rp.p, (nh + 1) * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+  cudaMemcpyAsync(p->h_anz.data(), anz.p, (nh + 1) * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+  p->stage_end(t0);
+  st = sync_check(p);
+  if (st != GM_OK) return st;
+  p->ip_heavy = p->h_chat_rp[nh];
+  p->n_par[0] = nh;
+  return GM_OK;
+}
+
+}  // namespace gm
+
+namespace gm {
+
+namespace {
+constexpr int64_t kOuterE = 8192;  // outer-product work-group elements (flattened space)
+
+BinSpec bitmap_leaf_spec() {
+  BinSpec s{};
+  s.nbins = 4;
+  s.ub[1] = 1024;
+  s.ub[2] = 4096;
+  s.ub[3] = INT64_MAX;
+  return s;
+}
+int bitmap_leaf_cap(int b, int64_t width) {
+  const int64_t c = b == 1 ? 1024 : b == 2 ? 4096 : width;
+  return static_cast<int>(std::min<int64_t>(c, width));
+}
+BinSpec hash_leaf_spec() {
+  BinSpec s{};
+  s.nbins = 11;
+  for (int b = 1; b <= 9; ++b) s.ub[b] = light_bin_ub(b);
+  s.ub[10] = INT64_MAX;
+  return s;
+}
+int hash_leaf_cap(int b, int64_t tau) {
+  if (b <= 9) return static_cast<int>(std::max<int64_t>(64, 2 * light_bin_ub(b)));
+  return static_cast<int>(2 * tau);
+}
+}  // namespace
+
+// Accumulates the chunks [lo, lo + n) (mapped rows of one level's output) whose
+// element counts are mcount[lo ...]: bitmap accumulator when `dense`, hash otherwise.
+static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int64_t lo, int64_t n, bool dense,
+                            bool numeric) {
+  if (n <= 0) return GM_OK;
+  const cudaStream_t s = p->s;
+  const BinSpec spec = dense ? bitmap_leaf_spec() : hash_leaf_spec();
+  DevBuf<uint8_t> bins;
+  DevBuf<int32_t> idx;
+  DevBuf<int64_t> starts_d, items;
+  if (!bins.alloc(n, s) || !idx.alloc(n, s) || !starts_d.alloc(spec.nbins + 1, s) || !items.alloc(n, s))
+    return GM_ERR_OOM;
+  launch_bin_sizes(mcount + lo, n, bins.p, spec, s);
+  if (!partition_by_bin(bins.p, n, spec.nbins, idx.p, starts_d.p, s)) return GM_ERR_OOM;
+  int64_t starts[kMaxBins + 1];
+  cudaMemcpyAsync(starts, starts_d.p, (spec.nbins + 1) * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_status(p, e);
+  i32_to_i64(idx.p, n, lo, items.p, s);
+  for (int b = 1; b < spec.nbins; ++b) {
+    const int64_t cnt = starts[b + 1] - starts[b];
+    if (cnt <= 0) continue;
+    ListArgs a = la;
+    a.items = items.p + starts[b];
+    a.n_items = cnt;
+    p->n_leaves += numeric ? 0 : cnt;
+    if (dense) launch_leaf_bitmap(a, bitmap_leaf_cap(b, la.width), !numeric, s);
+    else launch_leaf_hash(a, hash_leaf_cap(b, p->P.tau), !numeric, s);
+  }
+  e = cudaGetLastError();
+  return cuda_status(p, e);
+}
+
+template <class T>
+static void dbg_copy(DevBuf<T>& dst, const T* src, int64_t n, cudaStream_t s) {
+  if (dst.alloc(std::max<int64_t>(n, 1), s) && n > 0)
+    cudaMemcpyAsync(dst.p, src, n * sizeof(T), cudaMemcpyDeviceToDevice, s);
+}
+
+// Heavy rows [h0, h1): outer product, multisplit levels and chunk accumulation.
+// Symbolic: leaf nnz into p->nnz[level], heavy children into p->heavy_list / p->pbase.
+// Numeric: C entries at the offsets held in p->nnz[level].
+static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int64_t* par_base, int32_t* c_col,
+                           double* c_val) {
+  const cudaStream_t s = p->s;
+  const int64_t nb = h1 - h0;
+  const int64_t ip = p->h_chat_rp[h1] - p->h_chat_rp[h0];
+  const int64_t anz = p->h_anz[h1] - p->h_anz[h0];
+  const bool with_val = numeric || p->keep;
+  const int32_t* heavy = p->rows_by_bin.p + p->bin_start[kHeavyBin] + h0;
+  const int64_t ncols = p->A.n_cols;
+  const int L = p->L;
+  gm_status st = GM_OK;
+
+  // 1. Masked CSR -> CSC of the batch rows and the slice offsets (Algorithm 3 line 7).
+  int t = p->stage_begin(GM_STAGE_TRANSPOSE);
+  DevBuf<int64_t> col_ptr, slice_off;
+  DevBuf<int32_t> t_row, wg_op;
+  DevBuf<double> t_val;
+  const int64_t n_wg_op = (ip + kOuterE - 1) / kOuterE;
+  if (!col_ptr.alloc(ncols + 1, s) || !slice_off.alloc(ncols + 1, s) || !t_row.alloc(anz, s) ||
+      !t_val.alloc(anz, s) || !wg_op.alloc(n_wg_op, s))
+    return GM_ERR_OOM;
+  TransposeArgs ta{heavy, nb, p->A.row_ptr, p->A.col_idx, p->A.vals, ncols};
+  if (!masked_transpose(ta, anz, col_ptr.p, t_row.p, t_val.p, s)) return GM_ERR_OOM;
+  if (!slice_offsets(col_ptr.p, p->B.row_ptr, ncols, slice_off.p, s)) return GM_ERR_OOM;
+  launch_wg_slice(slice_off.p, ncols, kOuterE, wg_op.p, s);
+  p->stage_end(t);
+
+  // 2. Outer product into C-hat (Algorithm 4), optionally counting level-0 chunks.
+  t = p->stage_begin(GM_STAGE_OUTER);
+  DevBuf<int32_t> chat_col;
+  DevBuf<double> chat_val;
+  DevBuf<int64_t> lrp;
+  DevBuf<unsigned long long> cursor, cnt0;
+  if (!chat_col.alloc(ip, s) || !chat_val.alloc(with_val ? ip : 0, s) || !lrp.alloc(nb + 1, s) ||
+      !cursor.alloc(nb, s))
+    return GM_ERR_OOM;
+  sub_i64(p->chat_rp.p + h0, nb + 1, p->h_chat_rp[h0], lrp.p, s);
+  sub_to_u64(p->chat_rp.p + h0, nb, p->h_chat_rp[h0], cursor.p, s);
+  const bool fused = L >= 1 && p->pipeline == GM_PIPE_FUSED_HISTO;
+  if (L >= 1) {
+    if (!cnt0.alloc(nb * p->P.v_chunks[0], s)) return GM_ERR_OOM;
+    cudaMemsetAsync(cnt0.p, 0, cnt0.bytes(), s);
+  }
+  OuterArgs oa{};
+  oa.slice_off = slice_off.p;
+  oa.col_ptr = col_ptr.p;
+  oa.t_row = t_row.p;
+  oa.t_val = t_val.p;
+  oa.b_rp = p->B.row_ptr;
+  oa.b_col = p->B.col_idx;
+  oa.b_val = p->B.vals;
+  oa.n_slices = ncols;
+  oa.total = ip;
+  oa.E = kOuterE;
+  oa.wg_first = wg_op.p;
+  oa.cursor = cursor.p;
+  oa.out_col = chat_col.p;
+  oa.out_val = with_val ? chat_val.p : nullptr;
+  oa.histo = fused ? cnt0.p : nullptr;
+  oa.v = L >= 1 ? static_cast<int>(p->P.v_chunks[0]) : 1;
+  oa.shift = L >= 1 ? ilog2(p->P.widths[0]) : 0;
+  launch_outer_product(oa, s);
+  p->stage_end(t);
+  t_row.release();
+  t_val.release();
+  col_ptr.release();
+  slice_off.release();
+  wg_op.release();
+  cursor.release();
+  if (p->keep) {
+    dbg_copy(p->dbg_chat_col, chat_col.p, ip, s);
+    if (with_val) dbg_copy(p->dbg_chat_val, chat_val.p, ip, s);
+    dbg_copy(p->dbg_chat_rp, lrp.p, nb + 1, s);
+  }
+
+  ListArgs base_la{};
+  base_la.status = p->status.p;
+  base_la.c_col = c_col;
+  base_la.c_val = c_val;
+
+  if (L == 0) {  // C.m <= dense width: the rows of C-hat are the chunks
+    DevBuf<int64_t> rows_cnt;
+    if (!rows_cnt.alloc(nb, s)) return GM_ERR_OOM;
+    launch_gather_i64(p->u.p, heavy, nb, rows_cnt.p, s);
+    ListArgs la = base_la;
+    la.rp = lrp.p;
+    la.col = chat_col.p;
+    la.val = with_val ? chat_val.p : nullptr;
+    la.child_base = par_base[0];
+    la.v = 1;
+    la.width = p->c_m;
+    la.nnz_out = p->nnz[0].p;
+    la.off_in = p->nnz[0].p;
+    t = p->stage_begin(numeric ? GM_STAGE_NUM_HEAVY : GM_STAGE_SYM_HEAVY);
+    st = run_leaves(p, la, rows_cnt.p, 0, nb, true, numeric);
+    p->stage_end(t);
+    par_base[0] += nb;
+    return st;
+  }
+
+  // 3. Hierarchical multisplit (Algorithm 3 lines 10-20) and accumulation of the
+  //    chunks that leave the hierarchy at each level.
+  const int64_t* in_rp = lrp.p;
+  const int32_t* in_col = chat_col.p;
+  const double* in_val = with_val ? chat_val.p : nullptr;
+  int64_t P_b = nb, in_total = ip;
+  std::unique_ptr<DevBuf<int64_t>> prev_rp;
+  std::unique_ptr<DevBuf<int32_t>> prev_col;
+  std::unique_ptr<DevBuf<double>> prev_val;
+  for (int i = 0; i < L; ++i) {
+    const bool last = i == L - 1;
+    const int v = static_cast<int>(p->P.v_chunks[i]);
+    const int shift = ilog2(p->P.widths[i]);
+    const int64_t children = P_b * v;
+    int ngr = 0;
+    const int64_t E = multisplit_pick_E(v, p->P.tau, with_val, p->smem_dev, &ngr);
+    if (E == 0) return GM_ERR_INVALID_ARG;
+
+    t = p->stage_begin(GM_STAGE_HISTOGRAM);
+    DevBuf<int32_t> wg;
+    if (!wg.alloc((in_total + E - 1) / E, s)) return GM_ERR_OOM;
+    launch_wg_row(in_rp, P_b, E, wg.p, s);
+    SplitArgs sa{};
+    sa.in_rp = in_rp;
+    sa.n_parents = P_b;
+    sa.in_col = in_col;
+    sa.in_val = in_val;
+    sa.base = 0;
+    sa.total = in_total;
+    sa.v = v;
+    sa.shift = shift;
+    sa.E = E;
+    sa.n_group_rows = ngr;
+    sa.wg_first = wg.p;
+    sa.status = p->status.p;
+    DevBuf<unsigned long long> cnt_own;
+    unsigned long long* cnt = cnt0.p;
+    if (!(i == 0 && fused)) {
+      if (!cnt_own.alloc(children, s)) return GM_ERR_OOM;
+      cudaMemsetAsync(cnt_own.p, 0, cnt_own.bytes(), s);
+      cnt = cnt_own.p;
+      sa.counts = cnt;
+      launch_histogram(sa, s);
+    }
+    // Heavy chunks first (ThreshPartition on the chunk sizes), order kept.
+    DevBuf<int32_t> perm;
+    DevBuf<int64_t> inv, perm64;
+    int64_t nH = 0;
+    if (!last) {
+      DevBuf<uint8_t> hb;
+      DevBuf<int64_t> st2;
+      if (!hb.alloc(children, s) || !perm.alloc(children, s) || !st2.alloc(3, s) || !inv.alloc(children, s) ||
+          !perm64.alloc(children, s))
+        return GM_ERR_OOM;
+      k_heavy_bin<<<grid_for(children, 256), 256, 0, s>>>(cnt, children, p->P.tau, hb.p);
+      if (!partition_by_bin(hb.p, children, 2, perm.p, st2.p, s)) return GM_ERR_OOM;
+      int64_t hst[3];
+      cudaMemcpyAsync(hst, st2.p, sizeof(hst), cudaMemcpyDeviceToHost, s);
+      cudaError_t e = cudaStreamSynchronize(s);
+      if (e != cudaSuccess) return cuda_status(p, e);
+      nH = hst[1] - hst[0];
+      i32_to_i64(perm.p, children, 0, perm64.p, s);
+    }
+    DevBuf<int64_t> mcount;
+    auto rrp = std::make_unique<DevBuf<int64_t>>();
+    DevBuf<unsigned long long> cur;
+    if (!mcount.alloc(children, s) || !rrp->alloc(children + 1, s) || !cur.alloc(children, s)) return GM_ERR_OOM;
+    k_mapped_counts<<<grid_for(children, 256), 256, 0, s>>>(cnt, last ? nullptr : perm.p, children, mcount.p,
+                                                            last ? nullptr : inv.p);
+    if (!scan_exclusive_i64(mcount.p, rrp->p, children, rrp->p + children, s)) return GM_ERR_OOM;
+    sub_to_u64(rrp->p, children, 0, cur.p, s);
+    p->stage_end(t);
+
+    t = p->stage_begin(GM_STAGE_MULTISPLIT);
+    auto out_col = std::make_unique<DevBuf<int32_t>>();
+    auto out_val = std::make_unique<DevBuf<double>>();
+    if (!out_col->alloc(in_total, s) || !out_val->alloc(with_val ? in_total : 0, s)) return GM_ERR_OOM;
+    sa.inv = last ? nullptr : inv.p;
+    sa.cursor = cur.p;
+    sa.out_col = out_col->p;
+    sa.out_val = with_val ? out_val->p : nullptr;
+    launch_multisplit(sa, s);
+    p->stage_end(t);
+    // the level's input is consumed
+    if (i == 0) {
+      chat_col.release();
+      chat_val.release();
+      cnt0.release();
+    }
+    prev_col.reset();
+    prev_val.reset();
+    if (p->keep) {
+      auto d = std::make_unique<LevelDbg>();
+      dbg_copy(d->rp, rrp->p, children + 1, s);
+      dbg_copy(d->col, out_col->p, in_total, s);
+      if (with_val) dbg_copy(d->val, out_val->p, in_total, s);
+      if (!d->child.alloc(children, s)) return GM_ERR_OOM;
+      if (last) launch_iota_i64(d->child.p, children, 0, s);
+      else cudaMemcpyAsync(d->child.p, perm64.p, children * sizeof(int64_t), cudaMemcpyDeviceToDevice, s);
+      d->rows = children;
+      d->nnz = in_total;
+      p->dbg_levels.push_back(std::move(d));
+    }
+
+    // Chunks that leave the hierarchy here: all chunks of the last level (width
+    // <= dense width, bitmap accumulator) or the light chunks of a wider level (hash).
+    if (!numeric) {
+      if (!p->nnz[i].ensure((par_base[i] + P_b) * v, par_base[i] * v, s)) return GM_ERR_OOM;
+      cudaMemsetAsync(p->nnz[i].p + par_base[i] * v, 0, children * sizeof(int64_t), s);
+    }
+    ListArgs la = base_la;
+    la.rp = rrp->p;
+    la.col = out_col->p;
+    la.val = with_val ? out_val->p : nullptr;
+    la.child_of = last ? nullptr : perm64.p;
+    la.child_base = par_base[i] * v;
+    la.v = v;
+    la.width = p->P.widths[i];
+    la.parent_colbase = i == 0 ? nullptr : p->pbase[i].p + par_base[i];
+    la.nnz_out = p->nnz[i].p;
+    la.off_in = p->nnz[i].p;
+    t = p->stage_begin(numeric ? GM_STAGE_NUM_HEAVY : GM_STAGE_SYM_HEAVY);
+    st = last ? run_leaves(p, la, mcount.p, 0, children, true, numeric)
+              : run_leaves(p, la, mcount.p, nH, children - nH, false, numeric);
+    p->stage_end(t);
+    if (st != GM_OK) return st;
+
+    const int64_t P_old = P_b;
+    if (!last && nH > 0) {
+      int64_t next_total = 0;
+      cudaMemcpyAsync(&next_total, rrp->p + nH, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+      if (!numeric) {
+        const int64_t at = par_base[i + 1];
+        if (!p->heavy_list[i].ensure(at + nH, at, s) || !p->pbase[i + 1].ensure(at + nH, at, s)) return GM_ERR_OOM;
+        k_i32_gather_to_i64<<<grid_for(nH, 256), 256, 0, s>>>(perm.p, nH, par_base[i] * v, p->heavy_list[i].p + at);
+        k_child_colbase<<<grid_for(nH, 256), 256, 0, s>>>(p->heavy_list[i].p + at, nH,
+                                                          i == 0 ? nullptr : p->pbase[i].p, v, p->P.widths[i],
+                                                          p->pbase[i + 1].p + at);
+      }
+      cudaError_t e = cudaStreamSynchronize(s);
+      if (e != cudaSuccess) return cuda_status(p, e);
+      prev_rp = std::move(rrp);
+      prev_col = std::move(out_col);
+      prev_val = std::move(out_val);
+      in_rp = prev_rp->p;
+      in_col = prev_col->p;
+      in_val = with_val ? prev_val->p : nullptr;
+      P_b = nH;
+      in_total = next_total;
+    }
+    par_base[i] += P_old;
+    if (last || nH == 0) break;
+  }
+  return cuda_status(p, cudaGetLastError());
+}
+
+}  // namespace gm
+
+namespace gm {
+
+// Splits the heavy rows into consecutive batches whose workspace fits `cap`.
+static gm_status plan_batches(gm_plan* p, int64_t bytes_per_ip, int64_t cap,
+                              std::vector<std::pair<int64_t, int64_t>>& out) {
+  const int64_t nh = p->n_heavy;
+  const int64_t v0 = p->L >= 1 ? p->P.v_chunks[0] : 1;
+  const int64_t fixed = (p->A.n_cols + 1) * 8 * 3 + (int64_t(64) << 20);
+  auto bytes = [&](int64_t h0, int64_t h1) {
+    const int64_t ip = p->h_chat_rp[h1] - p->h_chat_rp[h0];
+    const int64_t anz = p->h_anz[h1] - p->h_anz[h0];
+    return fixed + ip * bytes_per_ip + anz * 12 + (h1 - h0) * (32 + v0 * 72) + ip / 64;
+  };
+  out.clear();
+  int64_t h0 = 0;
+  while (h0 < nh) {
+    if (bytes(h0, h0 + 1) > cap) return GM_ERR_WORKSPACE;
+    // largest h1 with bytes(h0, h1) <= cap (bytes grows with h1)
+    int64_t lo = h0 + 1, hi = nh;
+    while (lo < hi) {
+      const int64_t mid = (lo + hi + 1) / 2;
+      if (bytes(h0, mid) <= cap) lo = mid; else hi = mid - 1;
+    }
+    out.emplace_back(h0, lo);
+    h0 = lo;
+  }
+  return GM_OK;
+}
+
+static int64_t workspace_cap(gm_plan* p) {
+  if (p->cfg.workspace_cap_bytes > 0) return p->cfg.workspace_cap_bytes;
+  size_t free_b = 0, total_b = 0;
+  cudaStreamSynchronize(p->s);
+  if (cudaMemGetInfo(&free_b, &total_b) != cudaSuccess) {
+    cudaGetLastError();
+    return int64_t(1) << 30;
+  }
+  const int64_t reserve = (int64_t(1) << 30) + static_cast<int64_t>(total_b) / 50;
+  return std::max<int64_t>(static_cast<int64_t>(free_b) - reserve, int64_t(256) << 20);
+}
+
+static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, double* c_val) {
+  for (int b = 1; b <= 10; ++b) {
+    const int64_t cnt = p->bin_start[b + 1] - p->bin_start[b];
+    if (cnt <= 0) continue;
+    LightArgs la{};
+    la.rows = p->rows_by_bin.p + p->bin_start[b];
+    la.n_items = cnt;
+    la.a_rp = p->A.row_ptr;
+    la.a_col = p->A.col_idx;
+    la.a_val = p->A.vals;
+    la.b_rp = p->B.row_ptr;
+    la.b_col = p->B.col_idx;
+    la.b_val = p->B.vals;
+    la.c_rp = p->c_rp;
+    la.c_col = c_col;
+    la.c_val = c_val;
+    la.status = p->status.p;
+    launch_light_rows(la, light_bin_cap(b, p->P.tau), !numeric, p->s);
+  }
+}
+
+static gm_status symbolic_impl(gm_plan* p, int64_t* C_rp, int64_t* C_nnz) {
+  const cudaStream_t s = p->s;
+  const int64_t n = p->A.n_rows;
+  p->c_rp = C_rp;
+  cudaMemsetAsync(C_rp, 0, (n + 1) * sizeof(int64_t), s);
+  int t = p->stage_begin(GM_STAGE_SYM_LIGHT);
+  launch_light(p, false, nullptr, nullptr);
+  p->stage_end(t);
+  const int L = p->L;
+  const int64_t nh = p->n_heavy;
+  if (nh > 0) {
+    const int64_t v0 = L >= 1 ? p->P.v_chunks[0] : 1;
+    if (!p->nnz[0].ensure(nh * v0, 0, s)) return GM_ERR_OOM;
+    cudaMemsetAsync(p->nnz[0].p, 0, nh * v0 * sizeof(int64_t), s);
+    std::vector<std::pair<int64_t, int64_t>> batches;
+    gm_status st = plan_batches(p, p->keep ? 24 : 8, workspace_cap(p), batches);
+    if (st != GM_OK) return st;
+    if (p->keep && batches.size() != 1) p->keep = false;
+    p->n_batches = static_cast<int64_t>(batches.size());
+    int64_t par_base[GM_MAX_LEVELS + 1] = {};
+    for (auto& bt : batches) {
+      st = run_batch(p, bt.first, bt.second, false, par_base, nullptr, nullptr);
+      if (st != GM_OK) return st;
+    }
+    for (int i = 0; i <= L; ++i) p->n_par[i] = par_base[i];
+    p->n_par[0] = nh;
+    // bottom-up: a heavy chunk's nnz is the sum over its chunks at the next level
+    for (int i = L - 2; i >= 0; --i)
+      if (p->n_par[i + 1] > 0)
+        sum_children(p->nnz[i + 1].p, p->heavy_list[i].p, p->nnz[i].p, p->n_par[i + 1],
+                     static_cast<int>(p->P.v_chunks[i + 1]), s);
+    if (L >= 1) sum_children(p->nnz[0].p, p->heavy_ids64.p, C_rp, nh, static_cast<int>(v0), s);
+    else launch_scatter_i64(p->nnz[0].p, p->rows_by_bin.p + p->bin_start[kHeavyBin], nh, C_rp, s);
+  }
+  t = p->stage_begin(GM_STAGE_SCAN);
+  if (!scan_exclusive_i64(C_rp, C_rp, n + 1, nullptr, s)) return GM_ERR_OOM;
+  cudaMemcpyAsync(&p->c_nnz, C_rp + n, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+  // top-down: output offset of every chunk = its parent's offset + nnz of earlier siblings
+  if (nh > 0) {
+    if (L >= 1) {
+      DevBuf<int64_t> base;
+      if (!base.alloc(nh, s)) return GM_ERR_OOM;
+      launch_gather_i64_i64(C_rp, p->heavy_ids64.p, nh, base.p, s);
+      segmented_offsets(p->nnz[0].p, p->nnz[0].p, base.p, nh, static_cast<int>(p->P.v_chunks[0]), nullptr, s);
+      for (int i = 1; i < L; ++i) {
+        const int64_t np = p->n_par[i];
+        if (np <= 0) break;
+        DevBuf<int64_t> b2;
+        if (!b2.alloc(np, s)) return GM_ERR_OOM;
+        launch_gather_i64_i64(p->nnz[i - 1].p, p->heavy_list[i - 1].p, np, b2.p, s);
+        segmented_offsets(p->nnz[i].p, p->nnz[i].p, b2.p, np, static_cast<int>(p->P.v_chunks[i]), nullptr, s);
+      }
+    } else {
+      launch_gather_i64_i64(C_rp, p->heavy_ids64.p, nh, p->nnz[0].p, s);
+    }
+  }
+  p->stage_end(t);
+  gm_status st = sync_check(p);
+  if (st != GM_OK) return st;
+  p->dbg_ok = p->keep;
+  if (C_nnz) *C_nnz = p->c_nnz;
+  return GM_OK;
+}
+
+static gm_status numeric_impl(gm_plan* p, int32_t* C_col, double* C_val) {
+  int t = p->stage_begin(GM_STAGE_NUM_LIGHT);
+  launch_light(p, true, C_col, C_val);
+  p->stage_end(t);
+  if (p->n_heavy > 0) {
+    const bool keep = p->keep;
+    p->keep = false;
+    std::vector<std::pair<int64_t, int64_t>> batches;
+    gm_status st = plan_batches(p, 24, workspace_cap(p), batches);
+    if (st != GM_OK) return st;
+    p->n_batches = std::max<int64_t>(p->n_batches, static_cast<int64_t>(batches.size()));
+    int64_t par_base[GM_MAX_LEVELS + 1] = {};
+    for (auto& bt : batches) {
+      st = run_batch(p, bt.first, bt.second, true, par_base, C_col, C_val);
+      if (st != GM_OK) return st;
+    }
+    p->keep = keep;
+  }
+  return sync_check(p);
+}
+
+static void log_plan(const gm_plan* p) {
+  std::fprintf(stderr,
+               "[gm_spgemm] C %lld x %lld  tau=%lld D=%lld chunks_req=%lld chunks_max=%lld levels=%lld  "
+               "rows: heavy=%lld light=%lld empty=%lld  IP total=%lld heavy=%lld\n",
+               (long long)p->A.n_rows, (long long)p->c_m, (long long)p->P.tau, (long long)p->P.dense_width,
+               (long long)p->P.n_chunks_required, (long long)p->P.n_chunks_max, (long long)p->P.n_levels,
+               (long long)p->n_heavy, (long long)p->n_light, (long long)p->n_empty, (long long)p->ip_total,
+               (long long)p->ip_heavy);
+}
+
+}  // namespace gm
+
+extern "C" {
+
+void gm_set_allocator(gm_alloc_fn alloc_fn, gm_free_fn free_fn, void* ctx) {
+  gm::g_alloc = alloc_fn;
+  gm::g_free = free_fn;
+  gm::g_ctx = ctx;
+}
+
+gm_status gm_spgemm_params(int64_t c_m, const gm_config* cfg, gm_params* out) {
+  return gm::compute_params(c_m, cfg, gm::kDefaultSmem, out);
+}
+
+gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* cfg, void* stream,
+                            gm_plan** plan_out) {
+  if (!plan_out) return GM_ERR_INVALID_ARG;
+  *plan_out = nullptr;
+  gm_status st = gm::check_csr(A);
+  if (st == GM_OK) st = gm::check_csr(B);
+  if (st != GM_OK) return st;
+  if (A->n_cols != B->n_rows) return GM_ERR_DIM_MISMATCH;
+  std::unique_ptr<gm_plan> p(new (std::nothrow) gm_plan);
+  if (!p) return GM_ERR_OOM;
+  p->A = *A;
+  p->B = *B;
+  if (cfg) p->cfg = *cfg;
+  p->s = static_cast<cudaStream_t>(stream);
+  p->pipeline = p->cfg.pipeline == GM_PIPE_UNFUSED ? GM_PIPE_UNFUSED : GM_PIPE_FUSED_HISTO;
+  p->timing = (p->cfg.flags & GM_FLAG_TIMING) != 0;
+  p->keep = (p->cfg.flags & GM_FLAG_KEEP_INTERMEDIATES) != 0;
+  p->log = (p->cfg.flags & GM_FLAG_LOG) != 0 || gm::env_log();
+  cudaError_t e = cudaGetDevice(&p->device);
+  int smem = 0;
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GM_ERR_CUDA;
+  }
+  p->smem_dev = smem;
+  p->c_m = std::max<int64_t>(B->n_cols, 1);
+  st = gm::compute_params(p->c_m, &p->cfg, p->smem_dev, &p->P);
+  if (st != GM_OK) return st;
+  p->L = static_cast<int>(p->P.n_levels);
+  gm::g_ws_peak = gm::g_ws_now.load();
+  st = gm::analyze_impl(p.get());
+  if (p->timing) p->collect_times();
+  if (st != GM_OK) {
+    cudaStreamSynchronize(p->s);
+    cudaGetLastError();
+    return st;
+  }
+  p->state = 1;
+  if (p->log) gm::log_plan(p.get());
+  *plan_out = p.release();
+  return GM_OK;
+}
+
+gm_status gm_spgemm_symbolic(gm_plan* plan, int64_t* C_row_ptr, int64_t* C_nnz) {
+  if (!plan) return GM_ERR_INVALID_ARG;
+  if (plan->state != 1) return GM_ERR_STATE;
+  if (!C_row_ptr) return GM_ERR_INVALID_ARG;
+  gm_status st = gm::symbolic_impl(plan, C_row_ptr, C_nnz);
+  if (plan->timing) {
+    cudaStreamSynchronize(plan->s);
+    plan->collect_times();
+  }
+  plan->ws_peak = std::max<int64_t>(plan->ws_peak, gm::g_ws_peak.load());
+  if (st == GM_OK) plan->state = 2;
+  return st;
+}
+
+gm_status gm_spgemm_numeric(gm_plan* plan, int32_t* C_col_idx, double* C_vals) {
+  if (!plan) return GM_ERR_INVALID_ARG;
+  if (plan->state != 2) return GM_ERR_STATE;
+  if (plan->c_nnz > 0 && (!C_col_idx || !C_vals)) return GM_ERR_INVALID_ARG;
+  gm_status st = gm::numeric_impl(plan, C_col_idx, C_vals);
+  if (plan->timing) {
+    cudaStreamSynchronize(plan->s);
+    plan->collect_times();
+  }
+  plan->ws_peak = std::max<int64_t>(plan->ws_peak, gm::g_ws_peak.load());
+  if (st == GM_OK) plan->state = 3;
+  return st;
+}
+
+gm_status gm_spgemm_plan_info(const gm_plan* plan, gm_plan_info* out) {
+  if (!plan || !out) return GM_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  out->params = plan->P;
+  out->n_rows = plan->A.n_rows;
+  out->n_cols = plan->B.n_cols;
+  out->n_heavy_rows = plan->n_heavy;
+  out->n_light_rows = plan->n_light;
+  out->n_empty_rows = plan->n_empty;
+  out->ip_total = plan->ip_total;
+  out->ip_heavy = plan->ip_heavy;
+  out->c_nnz = plan->c_nnz;
+  out->chat_bytes = plan->ip_heavy * 12;
+  out->n_batches = plan->n_batches;
+  out->workspace_peak_bytes = plan->ws_peak;
+  out->n_leaves = plan->n_leaves;
+  out->keeps_reordered = 0;
+  out->pipeline = plan->pipeline;
+  out->cuda_error = plan->cuda_error;
+  out->device_status = plan->dev_status;
+  for (int i = 0; i < GM_NUM_STAGES; ++i) out->stage_ms[i] = plan->stage_ms[i];
+  return GM_OK;
+}
+
+void gm_spgemm_plan_destroy(gm_plan* plan) {
+  if (!plan) return;
+  cudaStreamSynchronize(plan->s);
+  cudaGetLastError();
+  delete plan;
+}
+
+const char* gm_status_string(gm_status s) {
+  switch (s) {
+    case GM_OK: return "GM_OK";
+    case GM_ERR_INVALID_ARG: return "GM_ERR_INVALID_ARG: invalid argument";
+    case GM_ERR_DIM_MISMATCH: return "GM_ERR_DIM_MISMATCH: A.n_cols != B.n_rows";
+    case GM_ERR_INDEX_OVERFLOW: return "GM_ERR_INDEX_OVERFLOW: size exceeds the index types";
+    case GM_ERR_OOM: return "GM_ERR_OOM: device allocation failed";
+    case GM_ERR_WORKSPACE: return "GM_ERR_WORKSPACE: a heavy row needs more than the workspace cap";
+    case GM_ERR_CUDA: return "GM_ERR_CUDA: a CUDA call failed";
+    case GM_ERR_DEVICE_TIMEOUT: return "GM_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
+    case GM_ERR_STATE: return "GM_ERR_STATE: call out of order";
+    case GM_ERR_BAD_INDEX: return "GM_ERR_BAD_INDEX: column index or row pointer out of range";
+  }
+  return "unknown gm_status";
+}
+
+gm_status gm_spgemm_debug_copy(const gm_plan* plan, int view, int level, void* dst, int64_t bytes,
+                               int64_t* out_bytes) {
+  if (!plan) return GM_ERR_INVALID_ARG;
+  if (plan->state < 1) return GM_ERR_STATE;
+  const void* src = nullptr;
+  int64_t size = 0;
+  const int64_t nh = plan->n_heavy;
+  const gm::LevelDbg* L = nullptr;
+  if (view >= GM_DBG_CHAT_COL) {
+    if (!plan->dbg_ok) return GM_ERR_STATE;
+    if (view >= GM_DBG_REORD_ROWPTR) {
+      if (level < 0 || level >= static_cast<int>(plan->dbg_levels.size())) return GM_ERR_INVALID_ARG;
+      L = plan->dbg_levels[level].get();
+    }
+  }
+  switch (view) {
+    case GM_DBG_IP_COUNTS: src = plan->u.p; size = plan->A.n_rows * 8; break;
+    case GM_DBG_HEAVY_ROWS: src = plan->rows_by_bin.p + plan->bin_start[gm::kHeavyBin]; size = nh * 4; break;
+    case GM_DBG_LIGHT_ROWS: src = plan->rows_by_bin.p; size = plan->bin_start[gm::kHeavyBin] * 4; break;
+    case GM_DBG_CHAT_ROWPTR: src = plan->chat_rp.p; size = (nh + 1) * 8; break;
+    case GM_DBG_CHAT_COL: src = plan->dbg_chat_col.p; size = plan->ip_heavy * 4; break;
+    case GM_DBG_CHAT_VAL: src = plan->dbg_chat_val.p; size = plan->ip_heavy * 8; break;
+    case GM_DBG_REORD_ROWPTR: src = L->rp.p; size = (L->rows + 1) * 8; break;
+    case GM_DBG_REORD_COL: src = L->col.p; size = L->nnz * 4; break;
+    case GM_DBG_REORD_VAL: src = L->val.p; size = L->nnz * 8; break;
+    case GM_DBG_REORD_CHILD: src = L->child.p; size = L->rows * 8; break;
+    default: return GM_ERR_INVALID_ARG;
+  }
+  if (out_bytes) *out_bytes = size;
+  if (!dst) return GM_OK;
+  if (bytes != size) return GM_ERR_INVALID_ARG;
+  if (size == 0) return GM_OK;
+  if (!src) return GM_ERR_STATE;
+  cudaStreamSynchronize(plan->s);
+  const cudaError_t e = cudaMemcpy(dst, src, static_cast<size_t>(size), cudaMemcpyDeviceToHost);
+  return e == cudaSuccess ? GM_OK : GM_ERR_CUDA;
+}
+
+}  // extern "C"

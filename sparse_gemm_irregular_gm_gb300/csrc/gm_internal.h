@@ -1,0 +1,224 @@
+// gm_internal.h -- declarations shared by the CUDA translation units of libgm_spgemm.
+//
+// Layout conventions (device memory):
+//   * CSR inputs: row_ptr int64, col int32, val fp64.
+//   * C-hat (intermediate matrix of the heavy rows, gMAGNUS Sec. III-A): CSR over
+//     the rows of one heavy batch, int64 row pointers, int32 columns, fp64 values.
+//   * C-hat_reord (one multisplit level, Sec. III-C): CSR over children
+//     (parent * v + chunk) in "mapped" order (heavy children first), int32
+//     chunk-local columns, fp64 values.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gm_spgemm.h"
+
+namespace gm {
+
+// ---- device status bits (written with atomicOr into a status word) ----------
+enum : int {
+  kStBadARowPtr = 1 << 0,
+  kStBadBRowPtr = 1 << 1,
+  kStBadACol = 1 << 2,
+  kStBadBCol = 1 << 3,
+  kStHashFull = 1 << 4,     // a probe sequence ran through the whole table
+  kStGroupRows = 1 << 5,    // a multisplit work group met more rows than planned
+  kStInternal = 1 << 6,     // an internal consistency check failed
+};
+
+constexpr int kMaxBins = 16;
+
+// Binning by size: bin 0 holds items of size 0; otherwise the first b >= 1 with
+// size <= ub[b]. ub must be non-decreasing and ub[nbins-1] must cover every size.
+struct BinSpec {
+  int nbins;
+  int64_t ub[kMaxBins];
+};
+
+// ---- workspace ------------------------------------------------------------
+// Stream-ordered device allocations routed through the caller's hooks (or
+// cudaMallocAsync). Returns nullptr on failure.
+void* ws_alloc(size_t bytes, cudaStream_t s);
+void ws_free(void* p, size_t bytes, cudaStream_t s);
+
+template <class T>
+struct DevBuf {
+  T* p = nullptr;
+  size_t n = 0;
+  cudaStream_t s = nullptr;
+  bool alloc(size_t count, cudaStream_t stream) {
+    release();
+    s = stream;
+    n = count;
+    if (count == 0) return true;
+    p = static_cast<T*>(ws_alloc(count * sizeof(T), stream));
+    if (!p) n = 0;
+    return p != nullptr;
+  }
+  void release() {
+    if (p) ws_free(p, n * sizeof(T), s);
+    p = nullptr;
+    n = 0;
+  }
+  size_t bytes() const { return n * sizeof(T); }
+  ~DevBuf() { release(); }
+  DevBuf() = default;
+  DevBuf(const DevBuf&) = delete;
+  DevBuf& operator=(const DevBuf&) = delete;
+};
+
+// ---- scans (gm_scan.cu) -----------------------------------------------------
+// out[i] = sum_{j<i} in[j] for i in [0, n); in == out allowed. When d_total is
+// not null it receives sum of all n inputs. Returns false on allocation failure.
+bool scan_exclusive_i64(const int64_t* in, int64_t* out, int64_t n, int64_t* d_total, cudaStream_t s);
+// Fixed-size segments: for each parent p, the v children p*v .. p*v+v-1 get
+// off[p*v+c] = base[p] + sum_{c'<c} val[p*v+c'] (in place: val may equal off).
+// Returns the per-parent sums in sums (nullable).
+void segmented_offsets(const int64_t* val, int64_t* off, const int64_t* base, int64_t n_parents, int v,
+                       int64_t* sums, cudaStream_t s);
+// Sum of v consecutive children into their parent slot: dst[idx[p]] = sum_c src[p*v+c].
+void sum_children(const int64_t* src, const int64_t* parent_slot, int64_t* dst, int64_t n_parents, int v,
+                  cudaStream_t s);
+
+// ---- analysis (gm_analyze.cu) ---------------------------------------------
+void launch_validate_rowptr(const int64_t* rp, int64_t n_rows, int64_t nnz, int bad_bit, int* status,
+                            cudaStream_t s);
+void launch_validate_cols(const int32_t* col, int64_t nnz, int64_t n_cols, int bad_bit, int* status,
+                          cudaStream_t s);
+// u[i] = sum over stored A[i,k] of nnz(B[k,:]); bin[i] from spec.
+void launch_ip_count(const int64_t* a_rp, const int32_t* a_col, int64_t n_rows, const int64_t* b_rp,
+                     int64_t* u, uint8_t* bin, BinSpec spec, cudaStream_t s);
+// bin[i] for sizes given in an int64 array (optionally gathered: size[idx[i]]).
+void launch_bin_sizes(const int64_t* size, int64_t n, uint8_t* bin, BinSpec spec, cudaStream_t s);
+// Stable partition of [0, n) by bin: out_idx holds the indices bin-major, ascending
+// within a bin; d_bin_start[b] (nbins+1 entries) the start of each bin.
+bool partition_by_bin(const uint8_t* bin, int64_t n, int nbins, int32_t* out_idx, int64_t* d_bin_start,
+                      cudaStream_t s);
+// dst[i] = src[idx[i]] for i in [0, n).
+void launch_gather_i64(const int64_t* src, const int32_t* idx, int64_t n, int64_t* dst, cudaStream_t s);
+void launch_gather_i64_i64(const int64_t* src, const int64_t* idx, int64_t n, int64_t* dst, cudaStream_t s);
+// dst[idx[i]] = src[i].
+void launch_scatter_i64(const int64_t* src, const int32_t* idx, int64_t n, int64_t* dst, cudaStream_t s);
+void launch_iota_i64(int64_t* dst, int64_t n, int64_t start, cudaStream_t s);
+void launch_fill_i64(int64_t* dst, int64_t n, int64_t value, cudaStream_t s);
+
+// ---- expansion (gm_expand.cu) -----------------------------------------------
+struct TransposeArgs {
+  const int32_t* heavy_rows;  // original row id of each batch row
+  int64_t n_batch;
+  const int64_t* a_rp;
+  const int32_t* a_col;
+  const double* a_val;
+  int64_t n_cols;             // A.n_cols
+};
+// Masked CSR -> CSC of A[heavy_rows, :] (counting sort by column):
+// col_ptr[n_cols+1], t_row[nnz_batch] (batch-local row), t_val[nnz_batch].
+bool masked_transpose(const TransposeArgs& a, int64_t nnz_batch, int64_t* col_ptr, int32_t* t_row,
+                      double* t_val, cudaStream_t s);
+// slice_off[k] = sum_{k'<k} (col_ptr[k'+1]-col_ptr[k']) * nnz(B[k',:]), k in [0, n_cols].
+bool slice_offsets(const int64_t* col_ptr, const int64_t* b_rp, int64_t n_cols, int64_t* slice_off,
+                   cudaStream_t s);
+// wg_first[g] = the slice holding flattened position g*E (g in [0, n_wg)).
+void launch_wg_slice(const int64_t* slice_off, int64_t n_slices, int64_t E, int32_t* wg_first, cudaStream_t s);
+
+struct OuterArgs {
+  const int64_t* slice_off;   // n_cols + 1
+  const int64_t* col_ptr;     // n_cols + 1 (A-tilde CSC)
+  const int32_t* t_row;       // A-tilde rows (batch-local C-hat rows)
+  const double* t_val;
+  const int64_t* b_rp;
+  const int32_t* b_col;
+  const double* b_val;
+  int64_t n_slices;
+  int64_t total;              // C-hat.nnz of the batch
+  int64_t E;                  // flattened elements per work group
+  const int32_t* wg_first;
+  unsigned long long* cursor; // write cursor per C-hat row (starts at C-hat.rowPtr)
+  int32_t* out_col;
+  double* out_val;            // null: columns only
+  // fused level-0 histogram (null when not fused)
+  unsigned long long* histo;  // [rows * v]
+  int v;
+  int shift;                  // chunk = col >> shift
+};
+void launch_outer_product(const OuterArgs& a, cudaStream_t s);
+
+// ---- multisplit (gm_multisplit.cu) ------------------------------------------
+// wg_first[g] = the row holding position g*E.
+void launch_wg_row(const int64_t* rp, int64_t n_rows, int64_t E, int32_t* wg_first, cudaStream_t s);
+
+struct SplitArgs {
+  const int64_t* in_rp;       // parent row pointers (batch-local, in_rp[0] may be > 0)
+  int64_t n_parents;
+  const int32_t* in_col;      // parent-local columns
+  const double* in_val;       // null: columns only
+  int64_t base;               // in_rp[0]
+  int64_t total;              // in_rp[n_parents] - in_rp[0]
+  int v;                      // chunks per parent
+  int shift;                  // chunk = col >> shift
+  int64_t E;
+  int n_group_rows;           // rows a work group may meet
+  const int32_t* wg_first;
+  int* status;
+  // histogram output
+  unsigned long long* counts; // [n_parents * v]
+  // multisplit output
+  const int64_t* inv;         // child -> mapped row (null: identity)
+  unsigned long long* cursor; // write cursor per mapped row (starts at its row pointer)
+  int32_t* out_col;
+  double* out_val;
+};
+void launch_histogram(const SplitArgs& a, cudaStream_t s);
+void launch_multisplit(const SplitArgs& a, cudaStream_t s);
+// Largest work-group size E whose shared arrays fit smem_max bytes (0: none);
+// *ngr_out gets the rows a work group may meet when input rows exceed tau elements.
+int64_t multisplit_pick_E(int v, int64_t tau, bool with_val, int64_t smem_max, int* ngr_out);
+
+// ---- accumulation (gm_accum.cu) ---------------------------------------------
+struct LightArgs {
+  const int32_t* rows;        // rows of this bin
+  int64_t n_items;
+  const int64_t* a_rp;
+  const int32_t* a_col;
+  const double* a_val;
+  const int64_t* b_rp;
+  const int32_t* b_col;
+  const double* b_val;
+  int64_t* c_rp;              // symbolic: counts out at c_rp[row]; numeric: row offsets in
+  int32_t* c_col;
+  double* c_val;
+  int* status;
+};
+// Light rows of one bin: cap = table slots (>= 2 * max u in bin).
+void launch_light_rows(const LightArgs& a, int bin_cap, bool symbolic, cudaStream_t s);
+
+struct ListArgs {
+  const int64_t* items;       // mapped C-hat_reord rows to accumulate
+  int64_t n_items;
+  const int64_t* rp;          // C-hat_reord row pointers (mapped order)
+  const int32_t* col;         // chunk-local columns
+  const double* val;
+  const int64_t* child_of;    // mapped row -> batch-local child id (null: identity)
+  int64_t child_base;         // global child id of batch-local child 0
+  int v;                      // chunks per parent (child = parent * v + chunk)
+  int64_t width;              // chunk width
+  const int64_t* parent_colbase; // batch-local parent -> global column base (null: 0)
+  int64_t* nnz_out;           // symbolic: [global child] nnz
+  const int64_t* off_in;      // numeric: [global child] output offset
+  int32_t* c_col;
+  double* c_val;
+  int* status;
+};
+// Chunks narrower than the dense width: shared-memory bitmap + rank accumulator.
+void launch_leaf_bitmap(const ListArgs& a, int cap_vals, bool symbolic, cudaStream_t s);
+// Light chunks of a wide level: shared-memory hash accumulator (cap slots).
+void launch_leaf_hash(const ListArgs& a, int cap, bool symbolic, cudaStream_t s);
+int leaf_bitmap_smem(int64_t width, int cap_vals, bool symbolic);
+
+// Light-row bins: upper bounds on u and table capacity per bin.
+constexpr int kLightWarpBins = 4;   // bins 1..4 use a warp per row
+int64_t light_bin_ub(int b);        // b in [1, 10]
+int light_bin_cap(int b, int64_t tau);
+
+}  // namespace gm

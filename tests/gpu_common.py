@@ -1,0 +1,80 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI and
+compare it with the CPU oracle (structure bit-exact, fp64 values within
+1e-12 * sum|a_ik * b_kj| per entry)."""
+import numpy as np
+
+import oracle
+from sparse_gemm_irregular_gm_gb300 import binding
+
+REL_TOL = 1e-12
+
+
+def run_gpu(A, B, return_info=False, **cfg):
+    import torch
+    Ad, Bd = binding.to_device(A), binding.to_device(B)
+    C, info = binding.spgemm(Ad, Bd, binding.make_config(**cfg) if cfg else None, return_info=True)
+    torch.cuda.synchronize()
+    out = (C.row_ptr.cpu().numpy(), C.col.cpu().numpy(), C.val.cpu().numpy())
+    return (out, info) if return_info else out
+
+
+def assert_matches(ref, rp, col, val, exact=False):
+    """ref: oracle.OracleC over the same rows (in order); rp/col/val: GPU rows."""
+    np.testing.assert_array_equal(np.diff(rp), np.diff(ref.row_ptr), err_msg="row nnz differ")
+    np.testing.assert_array_equal(col, ref.col, err_msg="columns differ")
+    if exact:
+        np.testing.assert_array_equal(val, ref.val, err_msg="integer-valued results differ")
+    else:
+        err = np.abs(val - ref.val)
+        bound = REL_TOL * ref.abs_scale
+        bad = np.nonzero(err > bound)[0]
+        assert bad.size == 0, f"{bad.size} values outside 1e-12*sum|ab|; worst rel {np.max(err / np.maximum(ref.abs_scale, 1e-300))}"
+
+
+def check_full(A, B, exact=False, **cfg):
+    (rp, col, val), info = run_gpu(A, B, return_info=True, **cfg)
+    ref = oracle.spgemm(A, B)
+    assert rp[0] == 0
+    assert_matches(ref, rp, col, val, exact)
+    return info
+
+
+def gather_rows(C, rows):
+    """Host copies of the given rows of a device CSR result."""
+    import torch
+    rp = C.row_ptr.cpu().numpy()
+    lo, hi = rp[rows], rp[np.asarray(rows) + 1]
+    lens = hi - lo
+    idx = np.concatenate([np.arange(a, b) for a, b in zip(lo, hi)]) if len(rows) else np.zeros(0, np.int64)
+    t = torch.from_numpy(idx.astype(np.int64)).to(C.col.device)
+    col = C.col[t].cpu().numpy()
+    val = C.val[t].cpu().numpy()
+    srp = np.zeros(len(rows) + 1, dtype=np.int64)
+    np.cumsum(lens, out=srp[1:])
+    return srp, col, val
+
+
+def check_invariants(C, u):
+    """Properties every result must have, checked on the device in slices."""
+    import torch
+    rp = C.row_ptr
+    n = rp.numel() - 1
+    assert int(rp[0]) == 0 and int(rp[-1]) == C.col.numel()
+    lens = rp[1:] - rp[:-1]
+    assert bool((lens >= 0).all())
+    assert bool((lens.cpu() <= torch.from_numpy(u)).all()), "a row has more entries than products"
+    nnz = C.col.numel()
+    start = torch.zeros(1, dtype=torch.bool, device=rp.device)
+    step = 1 << 28
+    rp_cpu = rp.cpu().numpy()
+    for lo in range(0, nnz, step):
+        hi = min(nnz, lo + step + 1)
+        c = C.col[lo:hi].to(torch.int64)
+        first = torch.zeros(hi - lo, dtype=torch.bool, device=rp.device)
+        s = rp_cpu[(rp_cpu >= lo) & (rp_cpu < hi)] - lo
+        first[torch.from_numpy(s).to(rp.device)] = True
+        ok = (c[1:] > c[:-1]) | first[1:]
+        assert bool(ok.all()), "columns not strictly increasing within a row"
+        assert int(c.min()) >= 0 and int(c.max()) < C.n_cols
+    del start
+    return n

@@ -1,0 +1,127 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library loads, exports every function include/gm_spgemm.h declares, its
+parameter selection equals the oracle's (gMAGNUS Sec. III-D) including the
+51 chunk counts of Tables V/VI, and argument errors are caught on the host.
+"""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import oracle
+from sparse_gemm_irregular_gm_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return binding.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "gm_spgemm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = set(re.findall(r"^\s*(?:const\s+)?[a-z_]+\s*\**\s*(gm_[a-z_]+)\s*\(", src, flags=re.M))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(binding.EXPORTS) == names
+
+
+def test_status_strings(lib):
+    for i, name in enumerate(binding.STATUS_NAMES):
+        assert binding.gm_status_string(i).startswith(name)
+
+
+def _lib_params(c_m, **kw):
+    return binding.gm_spgemm_params(c_m, binding.make_config(**kw) if kw else None)
+
+
+@pytest.mark.parametrize("c_m", [1, 2, 8, 1000, 1 << 10, (1 << 14) + 1, 1 << 18, 1 << 20, (1 << 21) + 7, 10 ** 8])
+@pytest.mark.parametrize("over", [{}, {"tau": 64, "dense_width": 64, "n_chunks_max": 4},
+                                  {"dense_width": 256, "n_chunks_max": 2}, {"smem_budget_bytes": 65536},
+                                  {"smem_budget_bytes": 49152, "tau": 100, "n_chunks_max": 8}])
+def test_params_match_oracle(lib, c_m, over):
+    kw = {}
+    if "smem_budget_bytes" in over:
+        kw["s_lm"] = over["smem_budget_bytes"]
+    for k in ("tau", "dense_width", "n_chunks_max"):
+        if k in over:
+            kw[k] = over[k]
+    ref = oracle.magnus_params(c_m, **kw)
+    if ref.n_levels > binding.GM_MAX_LEVELS:  # the ABI holds at most 16 levels
+        with pytest.raises(binding.GmError) as e:
+            _lib_params(c_m, **over)
+        assert e.value.status == 3
+        return
+    got = _lib_params(c_m, **over)
+    assert got.s_lm == ref.s_lm and got.tau == ref.tau
+    assert got.dense_width == ref.dense_width and got.n_chunks_max == ref.n_chunks_max
+    assert got.n_chunks_required == ref.n_chunks_required and got.n_levels == ref.n_levels
+    assert list(got.v_chunks[:got.n_levels]) == ref.v_chunks
+    assert list(got.widths[:got.n_levels]) == ref.widths
+
+
+def test_params_tables_v_vi(lib):
+    with open(os.path.join(ROOT, "tests", "golden", "magnus_chunk_tables.json")) as f:
+        g = json.load(f)
+    n = 0
+    for row in g["suitesparse"] + [[f"rmat{s}", 1 << s, p, h] for s, p, h in g["rmat"]]:
+        _, c_m, pvc, h200 = row
+        for gpu, entry in (("PVC", pvc), ("H200", h200)):
+            if entry is None:
+                continue
+            cal = g["calibration"][gpu]
+            p = _lib_params(c_m, dense_width=cal["dense_width"], n_chunks_max=cal["n_chunks_max"])
+            req = int(entry.split(":")[0])
+            levels = [int(x) for x in entry.split(":")[1].split(",")] if ":" in entry else [req]
+            assert p.n_chunks_required == req
+            assert list(p.v_chunks[:p.n_levels]) == levels
+            n += 1
+    assert n == 51
+
+
+def test_params_rejects_bad_overrides(lib):
+    for kw in ({"dense_width": 100}, {"n_chunks_max": 3}, {"n_chunks_max": 1}, {"tau": 10 ** 6},
+               {"smem_budget_bytes": 10 ** 7}):
+        with pytest.raises(binding.GmError) as e:
+            _lib_params(1 << 20, **kw)
+        assert e.value.status == 1
+    with pytest.raises(binding.GmError):
+        _lib_params(0)
+
+
+def test_analyze_host_argument_errors(lib):
+    fake = 0x1000  # never dereferenced: every check below fails on the host
+    A = binding.gm_csr(4, 5, 3, fake, fake, fake)
+    B = binding.gm_csr(6, 5, 3, fake, fake, fake)
+    plan = ctypes.c_void_p()
+    assert lib.gm_spgemm_analyze(ctypes.byref(A), ctypes.byref(B), None, None, ctypes.byref(plan)) == 2
+    B.n_rows = 5
+    assert lib.gm_spgemm_analyze(None, ctypes.byref(B), None, None, ctypes.byref(plan)) == 1
+    assert lib.gm_spgemm_analyze(ctypes.byref(A), ctypes.byref(B), None, None, None) == 1
+    bad = binding.gm_csr(-1, 5, 3, fake, fake, fake)
+    assert lib.gm_spgemm_analyze(ctypes.byref(bad), ctypes.byref(B), None, None, ctypes.byref(plan)) == 1
+    nul = binding.gm_csr(4, 5, 3, fake, None, fake)
+    assert lib.gm_spgemm_analyze(ctypes.byref(nul), ctypes.byref(B), None, None, ctypes.byref(plan)) == 1
+    big = binding.gm_csr(1 << 31, 5, 3, fake, fake, fake)
+    assert lib.gm_spgemm_analyze(ctypes.byref(big), ctypes.byref(B), None, None, ctypes.byref(plan)) == 3
+    assert not plan.value
+
+
+def test_plan_calls_reject_null(lib):
+    assert lib.gm_spgemm_symbolic(None, None, None) == 1
+    assert lib.gm_spgemm_numeric(None, None, None) == 1
+    assert lib.gm_spgemm_plan_info(None, None) == 1
+    lib.gm_spgemm_plan_destroy(None)

@@ -1,0 +1,292 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Structure (row pointers, columns, nnz) must match bit for bit; fp64 values
+within 1e-12 * sum|a_ik * b_kj| per entry; integer-valued inputs exactly.
+Small inputs force every path (heavy rows, one and several multisplit levels,
+no level, several workspace batches, both pipelines); the five workloads run
+at their full sizes, the two largest checked on sampled rows plus invariants.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from sparse_gemm_irregular_gm_gb300 import binding, inputs as gi
+from tests.gpu_common import assert_matches, check_full, check_invariants, gather_rows, run_gpu
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+# forced paths on small inputs: (name, config)
+FORCED = [
+    ("auto", {}),
+    ("heavy_L0", {"tau": 16}),                                          # C.m <= D: no multisplit
+    ("heavy_L1", {"tau": 16, "dense_width": 128, "n_chunks_max": 16}),  # one level, 8 chunks
+    ("heavy_L2", {"tau": 16, "dense_width": 64, "n_chunks_max": 4}),    # two levels
+    ("heavy_L3", {"tau": 16, "dense_width": 16, "n_chunks_max": 4}),    # three levels
+    ("unfused", {"tau": 16, "dense_width": 64, "n_chunks_max": 4, "pipeline": binding.GM_PIPE_UNFUSED}),
+    ("batched", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "workspace_cap_bytes": 70 << 20}),
+]
+
+
+@pytest.mark.parametrize("name,cfg", FORCED, ids=[f[0] for f in FORCED])
+@pytest.mark.parametrize("values", ["uniform", "int"])
+def test_rmat10_forced_paths(name, cfg, values):
+    A = gi.rmat(10, 8, seed=1, values=values)
+    info = check_full(A, A, exact=values == "int", **cfg)
+    if name != "auto":
+        assert info.n_heavy_rows > 0
+        if name == "batched":
+            assert info.n_batches > 1
+
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("shape", [(33, 20, 41), (64, 64, 64), (200, 90, 300), (1, 50, 7), (70, 1, 70)])
+@pytest.mark.parametrize("cfg", [{}, {"tau": 2, "dense_width": 4, "n_chunks_max": 2}], ids=["auto", "forced"])
+def test_random_irregular(seed, shape, cfg):
+    m, k, n = shape
+    A = gi.random_csr(m, k, 0.3, seed, values="int", unsorted=True, duplicates=True, explicit_zeros=True,
+                      empty_rows=0.2)
+    B = gi.random_csr(k, n, 0.3, seed + 50, values="int", unsorted=True, duplicates=True, explicit_zeros=True,
+                      empty_rows=0.2)
+    check_full(A, B, exact=True, **cfg)
+
+
+def test_empty_and_degenerate():
+    empty = gi.random_csr(8, 6, 0.0, 1)
+    B = gi.random_csr(6, 9, 0.5, 2)
+    (rp, col, val) = run_gpu(empty, B)
+    assert rp.tolist() == [0] * 9 and col.size == 0
+    (rp, col, val) = run_gpu(B.__class__(6, 6, np.zeros(7, np.int64), np.zeros(0, np.int32), np.zeros(0)), B)
+    assert col.size == 0
+    one = gi.identity(1)
+    (rp, col, val) = run_gpu(one, one)
+    assert rp.tolist() == [0, 1] and col.tolist() == [0] and val.tolist() == [1.0]
+    zero_rows = gi.CSR(0, 5, np.zeros(1, np.int64), np.zeros(0, np.int32), np.zeros(0))
+    (rp, col, val) = run_gpu(zero_rows, gi.random_csr(5, 4, 0.5, 3))
+    assert rp.tolist() == [0] and col.size == 0
+    # one dense row against a dense block: a single heavy row
+    A = gi.random_csr(3, 300, 1.0, 4, values="int")
+    Bd = gi.random_csr(300, 500, 0.9, 5, values="int")
+    check_full(A, Bd, exact=True, tau=100, dense_width=128, n_chunks_max=4)
+
+
+def test_bad_index_and_bad_row_ptr_are_reported():
+    A = gi.random_csr(10, 10, 0.4, 1)
+    bad = gi.CSR(A.n_rows, A.n_cols, A.row_ptr.copy(), A.col.copy(), A.val.copy())
+    bad.col[3] = 10  # == n_cols: out of range
+    with pytest.raises(binding.GmError) as e:
+        binding.spgemm(binding.to_device(bad), binding.to_device(A))
+    assert e.value.status == 9
+    bad2 = gi.CSR(A.n_rows, A.n_cols, A.row_ptr.copy(), A.col.copy(), A.val.copy())
+    bad2.row_ptr[4], bad2.row_ptr[5] = bad2.row_ptr[5] + 1, bad2.row_ptr[4]
+    with pytest.raises(binding.GmError) as e:
+        binding.spgemm(binding.to_device(A), binding.to_device(bad2))
+    assert e.value.status == 9
+
+
+def test_call_order_is_enforced():
+    A = gi.random_csr(10, 10, 0.4, 1)
+    Ad = binding.to_device(A)
+    plan = binding.gm_spgemm_analyze(Ad, Ad)
+    try:
+        c = torch.empty(0, dtype=torch.int32, device="cuda")
+        v = torch.empty(0, dtype=torch.float64, device="cuda")
+        with pytest.raises(binding.GmError) as e:
+            binding.gm_spgemm_numeric(plan, c, v)
+        assert e.value.status == 8
+        rp = torch.empty(11, dtype=torch.int64, device="cuda")
+        nnz = binding.gm_spgemm_symbolic(plan, rp)
+        with pytest.raises(binding.GmError) as e:
+            binding.gm_spgemm_symbolic(plan, rp)
+        assert e.value.status == 8
+        binding.gm_spgemm_numeric(plan, torch.empty(nnz, dtype=torch.int32, device="cuda"),
+                                  torch.empty(nnz, dtype=torch.float64, device="cuda"))
+    finally:
+        binding.gm_spgemm_plan_destroy(plan)
+
+
+# --- stage parity through the debug views -----------------------------------------
+
+def _analyze_keep(A, B, **cfg):
+    Ad, Bd = binding.to_device(A), binding.to_device(B)
+    cfg["flags"] = cfg.get("flags", 0) | binding.GM_FLAG_KEEP_INTERMEDIATES
+    plan = binding.gm_spgemm_analyze(Ad, Bd, binding.make_config(**cfg))
+    return plan, (Ad, Bd)
+
+
+def test_stage1_counts_partition_and_chat_rowptr():
+    A = gi.rmat(10, 8, seed=2)
+    tau = 300
+    plan, keep = _analyze_keep(A, A, tau=tau)
+    try:
+        u = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_IP_COUNTS)
+        np.testing.assert_array_equal(u, oracle.ip_counts(A, A))
+        heavy, light = oracle.thresh_partition(u, tau)
+        np.testing.assert_array_equal(binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_HEAVY_ROWS), heavy)
+        np.testing.assert_array_equal(np.sort(binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_LIGHT_ROWS)), light)
+        rp = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_CHAT_ROWPTR)
+        np.testing.assert_array_equal(np.diff(rp), u[heavy])
+        assert rp[0] == 0
+    finally:
+        binding.gm_spgemm_plan_destroy(plan)
+
+
+def _run_symbolic(plan, n_rows):
+    rp = torch.empty(n_rows + 1, dtype=torch.int64, device="cuda")
+    return binding.gm_spgemm_symbolic(plan, rp)
+
+
+def _multiset(cols, vals):
+    return sorted(zip(cols.tolist(), np.round(vals, 12).tolist()))
+
+
+@pytest.mark.parametrize("cfg", [{"tau": 16, "dense_width": 64, "n_chunks_max": 4},
+                                 {"tau": 16, "dense_width": 128, "n_chunks_max": 16},
+                                 {"tau": 16, "dense_width": 16, "n_chunks_max": 4,
+                                  "pipeline": binding.GM_PIPE_UNFUSED}])
+def test_outer_product_and_multisplit_levels(cfg):
+    A = gi.rmat(9, 8, seed=4, values="int")
+    plan, keep = _analyze_keep(A, A, **cfg)
+    try:
+        _run_symbolic(plan, A.n_rows)
+        params = binding.gm_spgemm_plan_info(plan).params
+        heavy = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_HEAVY_ROWS)
+        rp = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_CHAT_ROWPTR)
+        col = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_CHAT_COL)
+        val = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_CHAT_VAL)
+        ref = oracle.expand_rows(A, A, heavy)
+        for h, items in enumerate(ref):  # C-hat rows as multisets (Fig. 1, outer product)
+            got = _multiset(col[rp[h]:rp[h + 1]], val[rp[h]:rp[h + 1]])
+            assert got == sorted((c, round(v, 12)) for c, v in items)
+        # each level: chunk c of parent p holds the parent's elements in its column range
+        parents = [sorted((c, round(v, 12)) for c, v in items) for items in ref]
+        for lev in range(params.n_levels):
+            v, w = params.v_chunks[lev], params.widths[lev]
+            rrp = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_REORD_ROWPTR, lev)
+            rcol = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_REORD_COL, lev)
+            rval = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_REORD_VAL, lev)
+            child = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_REORD_CHILD, lev)
+            expect = {}
+            for pi, items in enumerate(parents):
+                for ci, ch in enumerate(oracle.split_chunks(items, v, w)):
+                    expect[pi * v + ci] = sorted(ch)
+            assert len(child) == len(expect)
+            for m, ch in enumerate(child):
+                assert _multiset(rcol[rrp[m]:rrp[m + 1]], rval[rrp[m]:rrp[m + 1]]) == expect[int(ch)]
+            # heavy chunks first, in order; they are the next level's parents
+            counts = np.diff(rrp)
+            nh = int((counts > params.tau).sum()) if lev < params.n_levels - 1 else 0
+            if lev < params.n_levels - 1:
+                assert np.all(counts[:nh] > params.tau) and np.all(counts[nh:] <= params.tau)
+                assert np.all(np.diff(child[:nh]) > 0)
+            parents = [expect[int(ch)] for ch in child[:nh]]
+    finally:
+        binding.gm_spgemm_plan_destroy(plan)
+
+
+def test_fig1_worked_example_on_gpu():
+    with open(os.path.join(GOLDEN, "fig1_worked_example.json")) as f:
+        g = json.load(f)
+    rng = np.random.default_rng(7)
+    syms = {}
+
+    def sym(s):
+        return syms.setdefault(s, float(rng.integers(2, 40)))
+
+    def build(rows, shape):
+        rp, col, val = [0], [], []
+        for i in range(shape[0]):
+            for c, s in rows.get(str(i), []):
+                col.append(c)
+                val.append(sym(s))
+            rp.append(len(col))
+        return gi.CSR(shape[0], shape[1], np.array(rp, np.int64), np.array(col, np.int32), np.array(val))
+
+    A, B = build(g["A_rows"], g["A_shape"]), build(g["B_rows"], g["B_shape"])
+    plan, keep = _analyze_keep(A, B, tau=2, dense_width=4, n_chunks_max=2)
+    try:
+        _run_symbolic(plan, A.n_rows)
+        assert binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_HEAVY_ROWS).tolist() == g["heavy_rows"]
+        rp = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_CHAT_ROWPTR)
+        col = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_CHAT_COL)
+        for h, cols in enumerate(g["Chat_col"]):
+            assert sorted(col[rp[h]:rp[h + 1]].tolist()) == sorted(cols)
+        rrp = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_REORD_ROWPTR, 0)
+        rcol = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_REORD_COL, 0)
+        for k, cols in enumerate(g["Creord_col"]):
+            assert sorted(rcol[rrp[k]:rrp[k + 1]].tolist()) == sorted(cols)
+    finally:
+        binding.gm_spgemm_plan_destroy(plan)
+    prod = lambda s: sym(s[:3]) * sym(s[3:])
+    (crp, ccol, cval) = run_gpu(A, B, tau=2, dense_width=4, n_chunks_max=2)
+    for r, entries in g["C_rows"].items():
+        i = int(r)
+        assert ccol[crp[i]:crp[i + 1]].tolist() == [c for c, _ in entries]
+        assert cval[crp[i]:crp[i + 1]].tolist() == [sum(prod(s) for s in labels) for _, labels in entries]
+
+
+# --- the workloads ------------------------------------------------------------------
+
+def test_workload_rmat10_fp64_and_int():
+    A = gi.named_workload("rmat10")
+    check_full(A, A)
+    Ai = gi.named_workload("rmat10_int")
+    check_full(Ai, Ai, exact=True)
+
+
+def test_workload_laplacian_1024():
+    A = gi.named_workload("laplace1024")
+    info = check_full(A, A, exact=True)
+    assert info.c_nnz == 13_611_012 and info.n_heavy_rows == 0
+
+
+def test_workload_erdos_renyi_2_21():
+    A = gi.named_workload("er21")
+    info = check_full(A, A)
+    assert info.ip_total == 64 << 21
+
+
+def _sampled_check(name, n_random=400, seed=0):
+    A = gi.named_workload(name)
+    u = oracle.ip_counts(A, A)
+    Ad = binding.to_device(A)
+    C, info = binding.spgemm(Ad, Ad, return_info=True)
+    torch.cuda.synchronize()
+    assert info.ip_total == int(u.sum()) and info.n_heavy_rows == int((u > info.params.tau).sum())
+    check_invariants(C, u)
+    rng = np.random.default_rng(seed)
+    heavy = np.nonzero(u > info.params.tau)[0]
+    light = np.nonzero((u > 0) & (u <= info.params.tau))[0]
+    top = np.argsort(u)[-6:]
+    rows = np.unique(np.concatenate([top, rng.choice(heavy, min(n_random, heavy.size), replace=False),
+                                     rng.choice(light, min(n_random, light.size), replace=False)]))
+    ref = oracle.spgemm_rows(A, A, rows)
+    srp, col, val = gather_rows(C, rows)
+    assert_matches(ref, srp, col, val)
+    return info
+
+
+@pytest.mark.slow
+def test_workload_rmat18_sampled():
+    info = _sampled_check("rmat18")
+    assert info.n_heavy_rows > 0 and info.params.n_levels == 1
+
+
+@pytest.mark.slow
+def test_workload_rmat20_sampled():
+    info = _sampled_check("rmat20", n_random=200)
+    assert info.n_heavy_rows > 0
