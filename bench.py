@@ -1,0 +1,401 @@
+#!/usr/bin/env python
+"""Benchmark of the gMAGNUS SpGEMM C = A*A on GB300.
+
+Workload: A = R-MAT scale 20 (1,048,576 x 1,048,576), edge factor 16, quadrant
+probabilities 0.57/0.19/0.19/0.05, duplicates collapsed, fp64 U[-1,1), seed 1;
+C = A*A (2.09e10 intermediate products, 9.7e9 nonzeros). A step is one full
+SpGEMM through the C ABI: analyze, symbolic, allocation of C, numeric.
+
+Printed: one JSON line with GFLOP/s = 2 * intermediate products / time, the
+roofline of the dominant stage, the whole-path roofline on the method's byte
+model, an end-to-end figure with host buffers (inputs copied in, C copied out),
+clocks sampled during the timed region and the CPU oracle as a baseline.
+``--impl reference`` times the CPU oracle instead (bounded row samples).
+Multi-GPU (torchrun): every rank runs an independent replica (the path is not
+sharded here); value = total products of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SpGEMM GFLOP/s (2×intermediate products/s) and % of HBM roofline, 1×GB300"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="rmat20")
+    ap.add_argument("--seed", type=int, default=1)
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--pipeline", type=int, default=0)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        sm, smax, power, reasons = [], [], [], set()
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(self.NAMES, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.file.name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+def byte_model(info, A, nnz_c):
+    """Algorithmic bytes per step.
+
+    Whole path (the method's byte model, one multisplit level): read A and B once,
+    C-hat written once (12 B/product), per level a histogram read of columns (4) and
+    a multisplit read + write (12 + 12), a symbolic column read (4), a numeric read
+    (12), C written once. Per stage: the bytes that stage must move in this
+    implementation (symbolic passes carry columns only, numeric passes columns and
+    values; the level-0 histogram is counted inside the outer product).
+    """
+    ip_h = info.ip_heavy
+    L = max(1, info.params.n_levels)
+    a_bytes = 8 * (A.n_rows + 1) + 12 * A.nnz
+    c_bytes = 8 * (A.n_rows + 1) + 12 * nnz_c
+    b_alg = 2 * a_bytes + ip_h * (12 + L * (4 + 12 + 12) + 4 + 12) + c_bytes
+    stages = {
+        "outer": ip_h * (4 + 12),                 # C-hat writes, symbolic (col) + numeric (col, val)
+        "multisplit": ip_h * ((4 + 4) + (12 + 12)),  # read + write, both passes
+        "sym_heavy": ip_h * 4,                    # chunk columns read
+        "num_heavy": ip_h * 12,                   # chunk columns and values read (+ C writes, below)
+    }
+    return b_alg, stages
+
+
+def log(msg):
+    print(f"[bench] {msg}", file=sys.stderr, flush=True)
+
+
+def host_available_bytes():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        return None
+    return None
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(A, u, target_s, seed):
+    """The oracle, as it stands, on a bounded random sample of A's rows."""
+    import numpy as np
+
+    import oracle
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(A.n_rows)
+    csum = np.cumsum(u[order])
+    # calibrate on ~2e7 products, then size the sample for target_s seconds
+    k = int(np.searchsorted(csum, 2e7)) + 1
+    t0 = time.perf_counter()
+    oracle.spgemm_rows(A, A, np.sort(order[:k]))
+    rate = float(csum[k - 1]) / max(time.perf_counter() - t0, 1e-3)
+    k = int(np.searchsorted(csum, rate * target_s)) + 1
+    k = min(k, A.n_rows)
+    rows = np.sort(order[:k])
+    ip = int(csum[k - 1])
+    t0 = time.perf_counter()
+    oracle.spgemm_rows(A, A, rows)
+    dt = time.perf_counter() - t0
+    return {"value": 2.0 * ip / dt / 1e9, "unit": "GFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{k} random rows of the workload ({ip:.3e} of {int(u.sum()):.3e} intermediate products), "
+                      f"{dt:.1f} s on the host cores"}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    from sparse_gemm_irregular_gm_gb300 import binding, inputs
+    rank, world, local = dist_setup(args)
+    __graft_entry__.build()
+    A = inputs.named_workload(args.workload, seed=args.seed)
+    Ad = binding.to_device(A)
+    cfg = binding.make_config(flags=binding.GM_FLAG_TIMING, pipeline=args.pipeline)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        plan = binding.gm_spgemm_analyze(Ad, Ad, cfg, stream)
+        c_rp = torch.empty(A.n_rows + 1, dtype=torch.int64, device="cuda")
+        nnz = binding.gm_spgemm_symbolic(plan, c_rp)
+        c_col = torch.empty(nnz, dtype=torch.int32, device="cuda")
+        c_val = torch.empty(nnz, dtype=torch.float64, device="cuda")
+        binding.gm_spgemm_numeric(plan, c_col, c_val)
+        info = binding.gm_spgemm_plan_info(plan)
+        binding.gm_spgemm_plan_destroy(plan)
+        return info, c_rp
+
+    log(f"workload {args.workload}: n={A.n_rows} nnz={A.nnz}")
+    for w in range(args.warmup):
+        t0 = time.perf_counter()
+        info, c_rp = step()
+        del c_rp
+        log(f"warmup {w}: {time.perf_counter() - t0:.3f} s, stages {[round(x, 1) for x in info.stage_ms]}")
+    # per-row products and the heavy rows (for the byte model and the CPU sample)
+    plan = binding.gm_spgemm_analyze(Ad, Ad, None, stream)
+    u = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_IP_COUNTS)
+    heavy = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_HEAVY_ROWS)
+    binding.gm_spgemm_plan_destroy(plan)
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stage_ms = np.zeros(binding.GM_NUM_STAGES)
+    launches = 0
+    e0.record(stream)
+    for _ in range(args.steps):
+        info, c_rp = step()
+        stage_ms += np.array(info.stage_ms[:])
+        launches += info.kernel_launches
+        last_rp = c_rp
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    stage_ms /= args.steps
+    rp = last_rp.cpu().numpy()
+    nnz_c = int(rp[-1])
+    nnz_heavy = int((rp[heavy.astype(np.int64) + 1] - rp[heavy.astype(np.int64)]).sum())
+    del last_rp, c_rp
+    flops = 2.0 * info.ip_total
+    value = world * flops / (ms / 1e3) / 1e9
+    peak, peak_kind = peaks()
+    b_alg, stage_bytes = byte_model(info, A, nnz_c)
+    stage_bytes["num_heavy"] += 12 * nnz_heavy + 8 * len(heavy)
+    names = binding.STAGES
+    stage_table = {names[i]: round(float(stage_ms[i]), 3) for i in range(len(names)) if stage_ms[i] > 0}
+    dom = max(stage_bytes, key=lambda k: stage_ms[names.index(k)])
+    dom_s = stage_ms[names.index(dom)] / 1e3
+    achieved = stage_bytes[dom] / dom_s / 1e9 if dom_s > 0 else 0.0
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "A*A, A = R-MAT scale 20, edge factor 16, a=.57 b=.19 c=.19, fp64 U[-1,1), seed 1"
+                   if args.workload == "rmat20" else args.workload,
+                   "n": A.n_rows, "nnz_A": A.nnz, "intermediate_products": info.ip_total,
+                   "heavy_products": info.ip_heavy, "nnz_C": nnz_c, "heavy_rows": info.n_heavy_rows,
+                   "levels": info.params.n_levels, "chunks": list(info.params.v_chunks[:info.params.n_levels]),
+                   "batches": info.n_batches, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs and outputs larger than L2 (C alone is %.0f GB)" % (12 * nnz_c / 1e9)},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_kind": peak_kind, "alg_bytes_per_step": int(stage_bytes[dom])},
+        "path_roofline": {"alg_bytes": int(b_alg), "frac": round((b_alg / (peak * 1e9)) / (ms / 1e3), 4),
+                          "peak": peak, "unit": "GB/s", "peak_kind": peak_kind},
+        "stages_ms": stage_table,
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    log("timed: " + json.dumps({k: result[k] for k in ("value", "ms_per_step", "stages_ms", "roofline")}))
+    if not args.no_e2e and rank == 0:
+        result["e2e"] = run_e2e(args, A, cfg, stream, nnz_c, info.ip_total)
+        log("e2e: " + json.dumps(result["e2e"]))
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        result["cpu_baseline"] = cpu_baseline(A, u, args.cpu_seconds, args.seed)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def run_e2e(args, A, cfg, stream, nnz_c, ip_total):
+    """Same metric with host buffers: copy A in from pinned memory, run, copy C out."""
+    import torch
+
+    from sparse_gemm_irregular_gm_gb300 import binding
+    h2d = (A.n_rows + 1) * 8 + A.nnz * 12
+    d2h = (A.n_rows + 1) * 8 + nnz_c * 12
+    avail = host_available_bytes()
+    if avail is not None and d2h + h2d > 0.85 * avail:
+        return {"value": None, "unit": "GFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "skipped": f"C needs {d2h / 1e9:.0f} GB of pinned host memory, {avail / 1e9:.0f} GB available"}
+    h_rp = torch.from_numpy(A.row_ptr).pin_memory()
+    h_col = torch.from_numpy(A.col).pin_memory()
+    h_val = torch.from_numpy(A.val).pin_memory()
+    t0 = time.perf_counter()
+    o_rp = torch.empty(A.n_rows + 1, dtype=torch.int64, pin_memory=True)
+    o_col = torch.empty(nnz_c, dtype=torch.int32, pin_memory=True)
+    o_val = torch.empty(nnz_c, dtype=torch.float64, pin_memory=True)
+    log(f"e2e: pinned {d2h / 1e9:.1f} GB of host memory in {time.perf_counter() - t0:.1f} s")
+
+    def step():
+        d_rp = h_rp.to("cuda", non_blocking=True)
+        d_col = h_col.to("cuda", non_blocking=True)
+        d_val = h_val.to("cuda", non_blocking=True)
+        Ad = binding.DeviceCSR(A.n_rows, A.n_cols, d_rp, d_col, d_val)
+        C = binding.spgemm(Ad, Ad, cfg, stream)
+        o_rp.copy_(C.row_ptr, non_blocking=True)
+        o_col.copy_(C.col, non_blocking=True)
+        o_val.copy_(C.val, non_blocking=True)
+        torch.cuda.synchronize()
+
+    step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.e2e_steps
+    return {"value": round(2.0 * ip_total / dt / 1e9, 3), "unit": "GFLOP/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(dt * 1e3, 2), "steps": args.e2e_steps}
+
+
+def run_reference(args):
+    """The CPU oracle, as it stands, on bounded row samples of the same workload."""
+    import numpy as np
+
+    import oracle
+    from sparse_gemm_irregular_gm_gb300 import inputs
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    oracle.build()
+    A = inputs.named_workload(args.workload, seed=args.seed)
+    u = oracle.ip_counts(A, A)
+    per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    rng = np.random.default_rng(args.seed)
+    order = rng.permutation(A.n_rows)
+    csum = np.cumsum(u[order])
+    k = int(np.searchsorted(csum, 2e7)) + 1
+    t0 = time.perf_counter()
+    oracle.spgemm_rows(A, A, np.sort(order[:k]))
+    rate = float(csum[k - 1]) / max(time.perf_counter() - t0, 1e-3)
+    k = min(A.n_rows, int(np.searchsorted(csum, rate * per_step)) + 1)
+    rows = np.sort(order[:k])
+    ip = int(csum[k - 1])
+    for _ in range(args.warmup):
+        oracle.spgemm_rows(A, A, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.spgemm_rows(A, A, rows)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 2.0 * ip / dt / 1e9
+    sample = f"{k} random rows per step ({ip:.3e} of {int(u.sum()):.3e} intermediate products)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "A*A, A = R-MAT scale 20, edge factor 16, a=.57 b=.19 c=.19, fp64 U[-1,1), seed 1"
+                   if args.workload == "rmat20" else args.workload, "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GFLOP/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

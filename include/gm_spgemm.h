@@ -134,6 +134,7 @@ typedef struct gm_plan_info {
   int32_t cuda_error;          /* last cudaError_t seen, 0 if none      */
   int32_t device_status;       /* device-side error bits, 0 if none     */
   float stage_ms[GM_NUM_STAGES];
+  int64_t kernel_launches;     /* kernels this plan has launched so far */
 } gm_plan_info;
 
 typedef struct gm_plan gm_plan; /* opaque; owns every workspace buffer */

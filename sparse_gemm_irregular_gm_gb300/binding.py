@@ -53,7 +53,7 @@ class gm_plan_info(ctypes.Structure):
                 ("workspace_peak_bytes", ctypes.c_int64), ("n_leaves", ctypes.c_int64),
                 ("keeps_reordered", ctypes.c_int32), ("pipeline", ctypes.c_int32),
                 ("cuda_error", ctypes.c_int32), ("device_status", ctypes.c_int32),
-                ("stage_ms", ctypes.c_float * GM_NUM_STAGES)]
+                ("stage_ms", ctypes.c_float * GM_NUM_STAGES), ("kernel_launches", ctypes.c_int64)]
 
 
 class GmError(RuntimeError):

@@ -334,9 +334,10 @@ __global__ void k_leaf_hash(ListArgs a, int cap) {
   }
 }
 
+// Always opt in: the kernels' static shared arrays add to the dynamic size.
 template <class K>
 void set_smem(K fn, size_t smem) {
-  if (smem > 48 * 1024) cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
 }
 
 unsigned item_grid(int64_t n_items, int per_sm) {
@@ -352,10 +353,10 @@ int hash_threads(int cap) { return cap <= 1024 ? 128 : cap <= 2048 ? 256 : cap <
 
 int64_t light_bin_ub(int b) { return int64_t(16) << b; }  // bins 1..9: 32 .. 8192
 
-int light_bin_cap(int b, int64_t tau) {
+int light_bin_cap(int b, int64_t tau, int64_t smem_max) {
   if (b <= kLightWarpBins) return static_cast<int>(light_bin_ub(b));
   if (b <= 9) return static_cast<int>(2 * light_bin_ub(b));
-  return static_cast<int>(2 * tau);
+  return static_cast<int>(std::min<int64_t>(2 * tau, (smem_max - 1024) / 12));
 }
 
 void launch_light_rows(const LightArgs& a, int cap, bool symbolic, cudaStream_t s) {
@@ -364,10 +365,10 @@ void launch_light_rows(const LightArgs& a, int cap, bool symbolic, cudaStream_t 
     constexpr int W = 8;
     const unsigned g = static_cast<unsigned>(std::min<int64_t>((a.n_items + W - 1) / W, 152LL * 64));
     switch (cap) {
-      case 32: symbolic ? k_light_warp<true, 32, W><<<g, W * 32, 0, s>>>(a) : k_light_warp<false, 32, W><<<g, W * 32, 0, s>>>(a); break;
-      case 64: symbolic ? k_light_warp<true, 64, W><<<g, W * 32, 0, s>>>(a) : k_light_warp<false, 64, W><<<g, W * 32, 0, s>>>(a); break;
-      case 128: symbolic ? k_light_warp<true, 128, W><<<g, W * 32, 0, s>>>(a) : k_light_warp<false, 128, W><<<g, W * 32, 0, s>>>(a); break;
-      default: symbolic ? k_light_warp<true, 256, W><<<g, W * 32, 0, s>>>(a) : k_light_warp<false, 256, W><<<g, W * 32, 0, s>>>(a); break;
+      case 32: symbolic ? (k_light_warp<true, 32, W><<<g, W * 32, 0, s>>>(a), note_launch()) : (k_light_warp<false, 32, W><<<g, W * 32, 0, s>>>(a), note_launch()); break;
+      case 64: symbolic ? (k_light_warp<true, 64, W><<<g, W * 32, 0, s>>>(a), note_launch()) : (k_light_warp<false, 64, W><<<g, W * 32, 0, s>>>(a), note_launch()); break;
+      case 128: symbolic ? (k_light_warp<true, 128, W><<<g, W * 32, 0, s>>>(a), note_launch()) : (k_light_warp<false, 128, W><<<g, W * 32, 0, s>>>(a), note_launch()); break;
+      default: symbolic ? (k_light_warp<true, 256, W><<<g, W * 32, 0, s>>>(a), note_launch()) : (k_light_warp<false, 256, W><<<g, W * 32, 0, s>>>(a), note_launch()); break;
     }
     return;
   }
@@ -378,11 +379,11 @@ void launch_light_rows(const LightArgs& a, int cap, bool symbolic, cudaStream_t 
   if (symbolic) {
     auto fn = pow2 ? k_light_hash<true, true> : k_light_hash<true, false>;
     set_smem(fn, smem);
-    fn<<<g, T, smem, s>>>(a, cap);
+    (fn<<<g, T, smem, s>>>(a, cap), note_launch());
   } else {
     auto fn = pow2 ? k_light_hash<false, true> : k_light_hash<false, false>;
     set_smem(fn, smem);
-    fn<<<g, T, smem, s>>>(a, cap);
+    (fn<<<g, T, smem, s>>>(a, cap), note_launch());
   }
 }
 
@@ -399,7 +400,7 @@ void launch_leaf_bitmap(const ListArgs& a, int cap_vals, bool symbolic, cudaStre
   const unsigned g = item_grid(a.n_items, 4);
   auto fn = symbolic ? k_leaf_bitmap<true> : k_leaf_bitmap<false>;
   set_smem(fn, smem);
-  fn<<<g, T, smem, s>>>(a, nwords, cap_vals);
+  (fn<<<g, T, smem, s>>>(a, nwords, cap_vals), note_launch());
 }
 
 void launch_leaf_hash(const ListArgs& a, int cap, bool symbolic, cudaStream_t s) {
@@ -411,11 +412,11 @@ void launch_leaf_hash(const ListArgs& a, int cap, bool symbolic, cudaStream_t s)
   if (symbolic) {
     auto fn = pow2 ? k_leaf_hash<true, true> : k_leaf_hash<true, false>;
     set_smem(fn, smem);
-    fn<<<g, T, smem, s>>>(a, cap);
+    (fn<<<g, T, smem, s>>>(a, cap), note_launch());
   } else {
     auto fn = pow2 ? k_leaf_hash<false, true> : k_leaf_hash<false, false>;
     set_smem(fn, smem);
-    fn<<<g, T, smem, s>>>(a, cap);
+    (fn<<<g, T, smem, s>>>(a, cap), note_launch());
   }
 }
 

@@ -168,24 +168,24 @@ __global__ void k_fill_i64(int64_t* __restrict__ dst, int64_t n, int64_t v) {
 
 void launch_validate_rowptr(const int64_t* rp, int64_t n_rows, int64_t nnz, int bad_bit, int* status,
                             cudaStream_t s) {
-  k_validate_rowptr<<<grid_for(n_rows + 1, 256), 256, 0, s>>>(rp, n_rows, nnz, bad_bit, status);
+  (k_validate_rowptr<<<grid_for(n_rows + 1, 256), 256, 0, s>>>(rp, n_rows, nnz, bad_bit, status), note_launch());
 }
 
 void launch_validate_cols(const int32_t* col, int64_t nnz, int64_t n_cols, int bad_bit, int* status,
                           cudaStream_t s) {
   if (nnz <= 0) return;
-  k_validate_cols<<<grid_for(nnz, 256), 256, 0, s>>>(col, nnz, n_cols, bad_bit, status);
+  (k_validate_cols<<<grid_for(nnz, 256), 256, 0, s>>>(col, nnz, n_cols, bad_bit, status), note_launch());
 }
 
 void launch_ip_count(const int64_t* a_rp, const int32_t* a_col, int64_t n_rows, const int64_t* b_rp,
                      int64_t* u, uint8_t* bin, BinSpec spec, cudaStream_t s) {
   if (n_rows <= 0) return;
-  k_ip_count<<<grid_for(n_rows * 32, 256), 256, 0, s>>>(a_rp, a_col, n_rows, b_rp, u, bin, spec);
+  (k_ip_count<<<grid_for(n_rows * 32, 256), 256, 0, s>>>(a_rp, a_col, n_rows, b_rp, u, bin, spec), note_launch());
 }
 
 void launch_bin_sizes(const int64_t* size, int64_t n, uint8_t* bin, BinSpec spec, cudaStream_t s) {
   if (n <= 0) return;
-  k_bin_sizes<<<grid_for(n, 256), 256, 0, s>>>(size, n, bin, spec);
+  (k_bin_sizes<<<grid_for(n, 256), 256, 0, s>>>(size, n, bin, spec), note_launch());
 }
 
 bool partition_by_bin(const uint8_t* bin, int64_t n, int nbins, int32_t* out_idx, int64_t* d_bin_start,
@@ -197,32 +197,32 @@ bool partition_by_bin(const uint8_t* bin, int64_t n, int nbins, int32_t* out_idx
   const int64_t tiles = (n + kPartTile - 1) / kPartTile;
   DevBuf<int64_t> counts;
   if (!counts.alloc(static_cast<size_t>(tiles) * nbins, s)) return false;
-  k_part_count<<<static_cast<unsigned>(tiles), kPartThreads, 0, s>>>(bin, n, nbins, tiles, counts.p);
+  (k_part_count<<<static_cast<unsigned>(tiles), kPartThreads, 0, s>>>(bin, n, nbins, tiles, counts.p), note_launch());
   if (!scan_exclusive_i64(counts.p, counts.p, tiles * nbins, nullptr, s)) return false;
-  k_part_scatter<<<static_cast<unsigned>(tiles), kPartThreads, 0, s>>>(bin, n, nbins, tiles, counts.p, out_idx);
-  k_bin_starts<<<1, 32, 0, s>>>(counts.p, nbins, tiles, n, d_bin_start);
+  (k_part_scatter<<<static_cast<unsigned>(tiles), kPartThreads, 0, s>>>(bin, n, nbins, tiles, counts.p, out_idx), note_launch());
+  (k_bin_starts<<<1, 32, 0, s>>>(counts.p, nbins, tiles, n, d_bin_start), note_launch());
   return true;
 }
 
 void launch_gather_i64(const int64_t* src, const int32_t* idx, int64_t n, int64_t* dst, cudaStream_t s) {
   if (n <= 0) return;
-  k_gather_i64<<<grid_for(n, 256), 256, 0, s>>>(src, idx, n, dst);
+  (k_gather_i64<<<grid_for(n, 256), 256, 0, s>>>(src, idx, n, dst), note_launch());
 }
 void launch_gather_i64_i64(const int64_t* src, const int64_t* idx, int64_t n, int64_t* dst, cudaStream_t s) {
   if (n <= 0) return;
-  k_gather_i64_i64<<<grid_for(n, 256), 256, 0, s>>>(src, idx, n, dst);
+  (k_gather_i64_i64<<<grid_for(n, 256), 256, 0, s>>>(src, idx, n, dst), note_launch());
 }
 void launch_scatter_i64(const int64_t* src, const int32_t* idx, int64_t n, int64_t* dst, cudaStream_t s) {
   if (n <= 0) return;
-  k_scatter_i64<<<grid_for(n, 256), 256, 0, s>>>(src, idx, n, dst);
+  (k_scatter_i64<<<grid_for(n, 256), 256, 0, s>>>(src, idx, n, dst), note_launch());
 }
 void launch_iota_i64(int64_t* dst, int64_t n, int64_t start, cudaStream_t s) {
   if (n <= 0) return;
-  k_iota_i64<<<grid_for(n, 256), 256, 0, s>>>(dst, n, start);
+  (k_iota_i64<<<grid_for(n, 256), 256, 0, s>>>(dst, n, start), note_launch());
 }
 void launch_fill_i64(int64_t* dst, int64_t n, int64_t value, cudaStream_t s) {
   if (n <= 0) return;
-  k_fill_i64<<<grid_for(n, 256), 256, 0, s>>>(dst, n, value);
+  (k_fill_i64<<<grid_for(n, 256), 256, 0, s>>>(dst, n, value), note_launch());
 }
 
 }  // namespace gm

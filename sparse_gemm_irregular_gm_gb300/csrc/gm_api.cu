@@ -21,6 +21,17 @@ static gm_alloc_fn g_alloc = nullptr;
 static gm_free_fn g_free = nullptr;
 static void* g_ctx = nullptr;
 static std::atomic<int64_t> g_ws_now{0}, g_ws_peak{0};
+static std::atomic<int64_t> g_launches{0};
+
+static std::atomic<int> g_launch_err{0};
+
+// Counts the launch and records a failed launch (checked at the next sync point).
+void note_launch(int n) {
+  g_launches += n;
+  const cudaError_t e = cudaPeekAtLastError();
+  if (e != cudaSuccess) g_launch_err = static_cast<int>(e);
+}
+int64_t launch_count() { return g_launches.load(); }
 
 void* ws_alloc(size_t bytes, cudaStream_t s) {
   if (bytes == 0) return nullptr;
@@ -103,13 +114,13 @@ __global__ void k_i32_gather_to_i64(const int32_t* __restrict__ perm, int64_t n,
 }  // namespace
 
 static void sub_to_u64(const int64_t* src, int64_t n, int64_t base, unsigned long long* dst, cudaStream_t s) {
-  if (n > 0) k_sub_to_u64<<<grid_for(n, 256), 256, 0, s>>>(src, n, base, dst);
+  if (n > 0) (k_sub_to_u64<<<grid_for(n, 256), 256, 0, s>>>(src, n, base, dst), note_launch());
 }
 static void sub_i64(const int64_t* src, int64_t n, int64_t base, int64_t* dst, cudaStream_t s) {
-  if (n > 0) k_sub_i64<<<grid_for(n, 256), 256, 0, s>>>(src, n, base, dst);
+  if (n > 0) (k_sub_i64<<<grid_for(n, 256), 256, 0, s>>>(src, n, base, dst), note_launch());
 }
 static void i32_to_i64(const int32_t* src, int64_t n, int64_t add, int64_t* dst, cudaStream_t s) {
-  if (n > 0) k_i32_to_i64<<<grid_for(n, 256), 256, 0, s>>>(src, n, add, dst);
+  if (n > 0) (k_i32_to_i64<<<grid_for(n, 256), 256, 0, s>>>(src, n, add, dst), note_launch());
 }
 
 // ---- parameters (Sec. III-D) -----------------------------------------------------
@@ -146,7 +157,7 @@ static gm_status compute_params(int64_t c_m, const gm_config* cfg, int64_t smem_
   if (p.tau < 1 || p.tau > tau_eq4) return GM_ERR_INVALID_ARG;
   const int64_t n_dense = p.s_lm / (kSizeVal + kSizeBitmap);
   p.dense_width = (cfg && cfg->dense_width) ? cfg->dense_width : floor_pow2(n_dense);
-  if (!is_pow2(p.dense_width) || p.dense_width * 12 + p.dense_width / 4 > smem_dev) return GM_ERR_INVALID_ARG;
+  if (!is_pow2(p.dense_width) || p.dense_width * 12 + p.dense_width / 4 + 1024 > smem_dev) return GM_ERR_INVALID_ARG;
   p.n_chunks_required = next_pow2((c_m + p.dense_width - 1) / p.dense_width);
   const int64_t n_min = p.s_lm / (2 * (kSizeCol + kSizeVal));
   const int64_t n_gr = (n_min - 1 + p.tau - 1) / p.tau + 1;
@@ -156,10 +167,11 @@ static gm_status compute_params(int64_t c_m, const gm_config* cfg, int64_t smem_
     if (!is_pow2(cfg->n_chunks_max) || cfg->n_chunks_max < 2) return GM_ERR_INVALID_ARG;
     p.n_chunks_max = cfg->n_chunks_max;
   } else {
-    if (ncm_raw < 2) return GM_ERR_INVALID_ARG;
+    if (ncm_raw < 1) return GM_ERR_INVALID_ARG;
     p.n_chunks_max = floor_pow2(ncm_raw);
   }
   const int64_t req = p.n_chunks_required;
+  if (req > 1 && p.n_chunks_max < 2) return GM_ERR_INVALID_ARG;  // levels needed but none can split
   if (req == 1) {
     p.n_levels = 0;
   } else if (req <= p.n_chunks_max) {
@@ -274,7 +286,7 @@ struct gm_plan {
   int64_t n_par[GM_MAX_LEVELS + 1] = {};
   int64_t c_nnz = -1;
   int64_t* c_rp = nullptr;
-  int64_t n_batches = 0, n_leaves = 0, ws_peak = 0;
+  int64_t n_batches = 0, n_leaves = 0, ws_peak = 0, launches = 0;
   int cuda_error = 0, dev_status = 0;
   float stage_ms[GM_NUM_STAGES] = {};
   std::vector<gm::StageEv> evs;
@@ -328,6 +340,7 @@ static gm_status cuda_status(gm_plan* p, cudaError_t e) {
 static gm_status sync_check(gm_plan* p) {
   cudaError_t e = cudaStreamSynchronize(p->s);
   if (e == cudaSuccess) e = cudaGetLastError();
+  if (e == cudaSuccess && g_launch_err.load() != 0) e = static_cast<cudaError_t>(g_launch_err.exchange(0));
   if (e != cudaSuccess) return cuda_status(p, e);
   int st = 0;
   e = cudaMemcpy(&st, p->status.p, sizeof(int), cudaMemcpyDeviceToHost);
@@ -395,7 +408,7 @@ static gm_status analyze_impl(gm_plan* p) {
   cudaMemsetAsync(p->chat_rp.p + nh, 0, sizeof(int64_t), s);
   cudaMemsetAsync(anz.p + nh, 0, sizeof(int64_t), s);
   launch_gather_i64(p->u.p, heavy, nh, p->chat_rp.p, s);
-  if (nh > 0) k_row_len<<<grid_for(nh, 256), 256, 0, s>>>(p->A.row_ptr, heavy, nh, anz.p);
+  if (nh > 0) (k_row_len<<<grid_for(nh, 256), 256, 0, s>>>(p->A.row_ptr, heavy, nh, anz.p), note_launch());
   if (!scan_exclusive_i64(p->chat_rp.p, p->chat_rp.p, nh + 1, nullptr, s)) return GM_ERR_OOM;
   if (!scan_exclusive_i64(anz.p, anz.p, nh + 1, nullptr, s)) return GM_ERR_OOM;
   i32_to_i64(heavy, nh, 0, p->heavy_ids64.p, s);
@@ -437,9 +450,9 @@ BinSpec hash_leaf_spec() {
   s.ub[10] = INT64_MAX;
   return s;
 }
-int hash_leaf_cap(int b, int64_t tau) {
+int hash_leaf_cap(int b, int64_t tau, int64_t smem_max) {
   if (b <= 9) return static_cast<int>(std::max<int64_t>(64, 2 * light_bin_ub(b)));
-  return static_cast<int>(2 * tau);
+  return light_bin_cap(10, tau, smem_max);
 }
 }  // namespace
 
@@ -470,7 +483,7 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
     a.n_items = cnt;
     p->n_leaves += numeric ? 0 : cnt;
     if (dense) launch_leaf_bitmap(a, bitmap_leaf_cap(b, la.width), !numeric, s);
-    else launch_leaf_hash(a, hash_leaf_cap(b, p->P.tau), !numeric, s);
+    else launch_leaf_hash(a, hash_leaf_cap(b, p->P.tau, p->smem_dev), !numeric, s);
   }
   e = cudaGetLastError();
   return cuda_status(p, e);
@@ -600,7 +613,7 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
     const int shift = ilog2(p->P.widths[i]);
     const int64_t children = P_b * v;
     int ngr = 0;
-    const int64_t E = multisplit_pick_E(v, p->P.tau, with_val, p->smem_dev, &ngr);
+    const int64_t E = multisplit_pick_E(v, p->P.tau, with_val, p->smem_dev - 1024, &ngr);
     if (E == 0) return GM_ERR_INVALID_ARG;
 
     t = p->stage_begin(GM_STAGE_HISTOGRAM);
@@ -639,7 +652,7 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
       if (!hb.alloc(children, s) || !perm.alloc(children, s) || !st2.alloc(3, s) || !inv.alloc(children, s) ||
           !perm64.alloc(children, s))
         return GM_ERR_OOM;
-      k_heavy_bin<<<grid_for(children, 256), 256, 0, s>>>(cnt, children, p->P.tau, hb.p);
+      (k_heavy_bin<<<grid_for(children, 256), 256, 0, s>>>(cnt, children, p->P.tau, hb.p), note_launch());
       if (!partition_by_bin(hb.p, children, 2, perm.p, st2.p, s)) return GM_ERR_OOM;
       int64_t hst[3];
       cudaMemcpyAsync(hst, st2.p, sizeof(hst), cudaMemcpyDeviceToHost, s);
@@ -652,8 +665,8 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
     auto rrp = std::make_unique<DevBuf<int64_t>>();
     DevBuf<unsigned long long> cur;
     if (!mcount.alloc(children, s) || !rrp->alloc(children + 1, s) || !cur.alloc(children, s)) return GM_ERR_OOM;
-    k_mapped_counts<<<grid_for(children, 256), 256, 0, s>>>(cnt, last ? nullptr : perm.p, children, mcount.p,
-                                                            last ? nullptr : inv.p);
+    (k_mapped_counts<<<grid_for(children, 256), 256, 0, s>>>(cnt, last ? nullptr : perm.p, children, mcount.p,
+                                                            last ? nullptr : inv.p), note_launch());
     if (!scan_exclusive_i64(mcount.p, rrp->p, children, rrp->p + children, s)) return GM_ERR_OOM;
     sub_to_u64(rrp->p, children, 0, cur.p, s);
     p->stage_end(t);
@@ -719,10 +732,10 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
       if (!numeric) {
         const int64_t at = par_base[i + 1];
         if (!p->heavy_list[i].ensure(at + nH, at, s) || !p->pbase[i + 1].ensure(at + nH, at, s)) return GM_ERR_OOM;
-        k_i32_gather_to_i64<<<grid_for(nH, 256), 256, 0, s>>>(perm.p, nH, par_base[i] * v, p->heavy_list[i].p + at);
-        k_child_colbase<<<grid_for(nH, 256), 256, 0, s>>>(p->heavy_list[i].p + at, nH,
+        (k_i32_gather_to_i64<<<grid_for(nH, 256), 256, 0, s>>>(perm.p, nH, par_base[i] * v, p->heavy_list[i].p + at), note_launch());
+        (k_child_colbase<<<grid_for(nH, 256), 256, 0, s>>>(p->heavy_list[i].p + at, nH,
                                                           i == 0 ? nullptr : p->pbase[i].p, v, p->P.widths[i],
-                                                          p->pbase[i + 1].p + at);
+                                                          p->pbase[i + 1].p + at), note_launch());
       }
       cudaError_t e = cudaStreamSynchronize(s);
       if (e != cudaSuccess) return cuda_status(p, e);
@@ -801,7 +814,7 @@ static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, double* c_val
     la.c_col = c_col;
     la.c_val = c_val;
     la.status = p->status.p;
-    launch_light_rows(la, light_bin_cap(b, p->P.tau), !numeric, p->s);
+    launch_light_rows(la, light_bin_cap(b, p->P.tau, p->smem_dev), !numeric, p->s);
   }
 }
 
@@ -945,7 +958,9 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
   if (st != GM_OK) return st;
   p->L = static_cast<int>(p->P.n_levels);
   gm::g_ws_peak = gm::g_ws_now.load();
+  const int64_t l0 = gm::launch_count();
   st = gm::analyze_impl(p.get());
+  p->launches += gm::launch_count() - l0;
   if (p->timing) p->collect_times();
   if (st != GM_OK) {
     cudaStreamSynchronize(p->s);
@@ -962,7 +977,9 @@ gm_status gm_spgemm_symbolic(gm_plan* plan, int64_t* C_row_ptr, int64_t* C_nnz) 
   if (!plan) return GM_ERR_INVALID_ARG;
   if (plan->state != 1) return GM_ERR_STATE;
   if (!C_row_ptr) return GM_ERR_INVALID_ARG;
+  const int64_t l0 = gm::launch_count();
   gm_status st = gm::symbolic_impl(plan, C_row_ptr, C_nnz);
+  plan->launches += gm::launch_count() - l0;
   if (plan->timing) {
     cudaStreamSynchronize(plan->s);
     plan->collect_times();
@@ -976,7 +993,9 @@ gm_status gm_spgemm_numeric(gm_plan* plan, int32_t* C_col_idx, double* C_vals) {
   if (!plan) return GM_ERR_INVALID_ARG;
   if (plan->state != 2) return GM_ERR_STATE;
   if (plan->c_nnz > 0 && (!C_col_idx || !C_vals)) return GM_ERR_INVALID_ARG;
+  const int64_t l0 = gm::launch_count();
   gm_status st = gm::numeric_impl(plan, C_col_idx, C_vals);
+  plan->launches += gm::launch_count() - l0;
   if (plan->timing) {
     cudaStreamSynchronize(plan->s);
     plan->collect_times();
@@ -1007,6 +1026,7 @@ gm_status gm_spgemm_plan_info(const gm_plan* plan, gm_plan_info* out) {
   out->cuda_error = plan->cuda_error;
   out->device_status = plan->dev_status;
   for (int i = 0; i < GM_NUM_STAGES; ++i) out->stage_ms[i] = plan->stage_ms[i];
+  out->kernel_launches = plan->launches;
   return GM_OK;
 }
 

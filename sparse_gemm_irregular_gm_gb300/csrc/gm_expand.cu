@@ -158,24 +158,24 @@ bool masked_transpose(const TransposeArgs& a, int64_t nnz_batch, int64_t* col_pt
   DevBuf<unsigned long long> cnt;
   if (!cnt.alloc(a.n_cols + 1, s)) return false;
   cudaMemsetAsync(cnt.p, 0, (a.n_cols + 1) * sizeof(unsigned long long), s);
-  if (a.n_batch > 0) k_col_count<<<grid_for(a.n_batch * 32, 256), 256, 0, s>>>(a, cnt.p);
+  if (a.n_batch > 0) (k_col_count<<<grid_for(a.n_batch * 32, 256), 256, 0, s>>>(a, cnt.p), note_launch());
   // counts -> exclusive offsets; the extra last slot (zero) receives the total
   if (!scan_exclusive_i64(reinterpret_cast<int64_t*>(cnt.p), col_ptr, a.n_cols + 1, nullptr, s)) return false;
-  k_copy_u64<<<grid_for(a.n_cols + 1, 256), 256, 0, s>>>(col_ptr, cnt.p, a.n_cols + 1);
-  if (a.n_batch > 0 && nnz_batch > 0) k_csc_fill<<<grid_for(a.n_batch * 32, 256), 256, 0, s>>>(a, cnt.p, t_row, t_val);
+  (k_copy_u64<<<grid_for(a.n_cols + 1, 256), 256, 0, s>>>(col_ptr, cnt.p, a.n_cols + 1), note_launch());
+  if (a.n_batch > 0 && nnz_batch > 0) (k_csc_fill<<<grid_for(a.n_batch * 32, 256), 256, 0, s>>>(a, cnt.p, t_row, t_val), note_launch());
   return true;
 }
 
 bool slice_offsets(const int64_t* col_ptr, const int64_t* b_rp, int64_t n_cols, int64_t* slice_off,
                    cudaStream_t s) {
   cudaMemsetAsync(slice_off + n_cols, 0, sizeof(int64_t), s);
-  if (n_cols > 0) k_slice_sizes<<<grid_for(n_cols, 256), 256, 0, s>>>(col_ptr, b_rp, n_cols, slice_off);
+  if (n_cols > 0) (k_slice_sizes<<<grid_for(n_cols, 256), 256, 0, s>>>(col_ptr, b_rp, n_cols, slice_off), note_launch());
   return scan_exclusive_i64(slice_off, slice_off, n_cols + 1, nullptr, s);
 }
 
 void launch_wg_slice(const int64_t* slice_off, int64_t n_slices, int64_t E, int32_t* wg_first, cudaStream_t s) {
   if (n_slices <= 0) return;
-  k_wg_slice<<<grid_for(n_slices, 256), 256, 0, s>>>(slice_off, n_slices, E, wg_first);
+  (k_wg_slice<<<grid_for(n_slices, 256), 256, 0, s>>>(slice_off, n_slices, E, wg_first), note_launch());
 }
 
 void launch_outer_product(const OuterArgs& a, cudaStream_t s) {
@@ -183,11 +183,11 @@ void launch_outer_product(const OuterArgs& a, cudaStream_t s) {
   const int64_t n_wg = (a.total + a.E - 1) / a.E;
   const unsigned g = static_cast<unsigned>(n_wg);
   if (a.out_val) {
-    if (a.histo) k_outer<true, true><<<g, kOpThreads, 0, s>>>(a);
-    else k_outer<true, false><<<g, kOpThreads, 0, s>>>(a);
+    if (a.histo) (k_outer<true, true><<<g, kOpThreads, 0, s>>>(a), note_launch());
+    else (k_outer<true, false><<<g, kOpThreads, 0, s>>>(a), note_launch());
   } else {
-    if (a.histo) k_outer<false, true><<<g, kOpThreads, 0, s>>>(a);
-    else k_outer<false, false><<<g, kOpThreads, 0, s>>>(a);
+    if (a.histo) (k_outer<false, true><<<g, kOpThreads, 0, s>>>(a), note_launch());
+    else (k_outer<false, false><<<g, kOpThreads, 0, s>>>(a), note_launch());
   }
 }
 

@@ -36,6 +36,11 @@ struct BinSpec {
   int64_t ub[kMaxBins];
 };
 
+// ---- kernel launch accounting ----------------------------------------------
+// Every launch site calls note_launch(); plans report the count they caused.
+void note_launch(int n = 1);
+int64_t launch_count();
+
 // ---- workspace ------------------------------------------------------------
 // Stream-ordered device allocations routed through the caller's hooks (or
 // cudaMallocAsync). Returns nullptr on failure.
@@ -219,6 +224,8 @@ int leaf_bitmap_smem(int64_t width, int cap_vals, bool symbolic);
 // Light-row bins: upper bounds on u and table capacity per bin.
 constexpr int kLightWarpBins = 4;   // bins 1..4 use a warp per row
 int64_t light_bin_ub(int b);        // b in [1, 10]
-int light_bin_cap(int b, int64_t tau);
+// Table slots for bin b; the top bin holds 2 * tau slots, fewer when they would
+// not leave 1 KB of the block's shared memory (smem_max bytes) for static arrays.
+int light_bin_cap(int b, int64_t tau, int64_t smem_max);
 
 }  // namespace gm

@@ -192,7 +192,7 @@ void launch_split_t(const SplitArgs& a, cudaStream_t s) {
   auto fn = k_split<VAL, ITEMS, SPLIT>;
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   const int64_t n_wg = (a.total + E - 1) / E;
-  fn<<<static_cast<unsigned>(n_wg), kMsThreads, smem, s>>>(a);
+  (fn<<<static_cast<unsigned>(n_wg), kMsThreads, smem, s>>>(a), note_launch());
 }
 
 template <bool SPLIT>
@@ -210,7 +210,7 @@ void launch_split(const SplitArgs& a, cudaStream_t s) {
 
 void launch_wg_row(const int64_t* rp, int64_t n_rows, int64_t E, int32_t* wg_first, cudaStream_t s) {
   if (n_rows <= 0) return;
-  k_wg_row<<<grid_for(n_rows, 256), 256, 0, s>>>(rp, n_rows, E, wg_first);
+  (k_wg_row<<<grid_for(n_rows, 256), 256, 0, s>>>(rp, n_rows, E, wg_first), note_launch());
 }
 
 void launch_histogram(const SplitArgs& a, cudaStream_t s) { launch_split<false>(a, s); }

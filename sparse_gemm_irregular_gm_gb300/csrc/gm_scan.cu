@@ -96,27 +96,27 @@ bool scan_exclusive_i64(const int64_t* in, int64_t* out, int64_t n, int64_t* d_t
   }
   const int64_t tiles = (n + kScanTile - 1) / kScanTile;
   if (tiles == 1) {
-    k_tile_scan<<<1, kScanThreads, 0, s>>>(in, n, out, nullptr, d_total);
+    (k_tile_scan<<<1, kScanThreads, 0, s>>>(in, n, out, nullptr, d_total), note_launch());
     return true;
   }
   DevBuf<int64_t> sums;
   if (!sums.alloc(tiles, s)) return false;
-  k_tile_sums<<<static_cast<unsigned>(tiles), kScanThreads, 0, s>>>(in, n, sums.p);
+  (k_tile_sums<<<static_cast<unsigned>(tiles), kScanThreads, 0, s>>>(in, n, sums.p), note_launch());
   if (!scan_exclusive_i64(sums.p, sums.p, tiles, nullptr, s)) return false;
-  k_tile_scan<<<static_cast<unsigned>(tiles), kScanThreads, 0, s>>>(in, n, out, sums.p, d_total);
+  (k_tile_scan<<<static_cast<unsigned>(tiles), kScanThreads, 0, s>>>(in, n, out, sums.p, d_total), note_launch());
   return true;
 }
 
 void segmented_offsets(const int64_t* val, int64_t* off, const int64_t* base, int64_t n_parents, int v,
                        int64_t* sums, cudaStream_t s) {
   if (n_parents <= 0) return;
-  k_segmented_offsets<<<grid_for(n_parents * 32, 256), 256, 0, s>>>(val, off, base, n_parents, v, sums);
+  (k_segmented_offsets<<<grid_for(n_parents * 32, 256), 256, 0, s>>>(val, off, base, n_parents, v, sums), note_launch());
 }
 
 void sum_children(const int64_t* src, const int64_t* parent_slot, int64_t* dst, int64_t n_parents, int v,
                   cudaStream_t s) {
   if (n_parents <= 0) return;
-  k_sum_children<<<grid_for(n_parents * 32, 256), 256, 0, s>>>(src, parent_slot, dst, n_parents, v);
+  (k_sum_children<<<grid_for(n_parents * 32, 256), 256, 0, s>>>(src, parent_slot, dst, n_parents, v), note_launch());
 }
 
 }  // namespace gm

@@ -125,3 +125,12 @@ def test_plan_calls_reject_null(lib):
     assert lib.gm_spgemm_numeric(None, None, None) == 1
     assert lib.gm_spgemm_plan_info(None, None) == 1
     lib.gm_spgemm_plan_destroy(None)
+
+
+def test_params_no_level_needed_with_small_tau(lib):
+    # tau = 16 leaves Eq. (6) a single chunk per level; fine while C.m <= D needs no level.
+    got = _lib_params(1024, tau=16)
+    ref = oracle.magnus_params(1024, tau=16)
+    assert (got.n_chunks_max, got.n_levels) == (ref.n_chunks_max, ref.n_levels) == (1, 0)
+    with pytest.raises(binding.GmError):
+        _lib_params(1 << 20, tau=16)
