@@ -99,20 +99,26 @@ typedef struct gm_params {
   int64_t widths[GM_MAX_LEVELS];   /* column width of a chunk after each level           */
 } gm_params;
 
-#define GM_NUM_STAGES 12
-/* Stage indices of gm_plan_info.stage_ms (device time, filled with GM_FLAG_TIMING). */
+#define GM_NUM_STAGES 16
+/* Stage indices of gm_plan_info.stage_ms (device time, filled with GM_FLAG_TIMING).
+ * The heavy-row expansion and multisplit run once in the symbolic pass (columns
+ * only) and once in the numeric pass (columns and values); they are timed apart. */
 enum {
-  GM_STAGE_ANALYZE = 0,      /* counts, validation, partition, heavy row pointers */
-  GM_STAGE_TRANSPOSE = 1,    /* masked CSR -> CSC of the heavy rows                */
-  GM_STAGE_OUTER = 2,        /* outer product                                      */
-  GM_STAGE_HISTOGRAM = 3,    /* chunk histograms and scans                         */
-  GM_STAGE_MULTISPLIT = 4,   /* multisplit levels                                  */
-  GM_STAGE_SYM_HEAVY = 5,    /* symbolic accumulation of chunks                    */
-  GM_STAGE_SYM_LIGHT = 6,    /* symbolic accumulation of light rows                */
-  GM_STAGE_SCAN = 7,         /* prefix sum of C.rowPtr and chunk offsets           */
-  GM_STAGE_NUM_HEAVY = 8,    /* numeric accumulation of chunks                     */
-  GM_STAGE_NUM_LIGHT = 9,    /* numeric accumulation of light rows                 */
-  GM_STAGE_OTHER = 10        /* everything else                                    */
+  GM_STAGE_ANALYZE = 0,        /* counts, validation, partition, heavy row pointers */
+  GM_STAGE_TRANSPOSE = 1,      /* masked CSR -> CSC of the heavy rows (numeric pass) */
+  GM_STAGE_OUTER = 2,          /* outer product (numeric pass)                      */
+  GM_STAGE_HISTOGRAM = 3,      /* chunk histograms, partitions, scans (numeric)      */
+  GM_STAGE_MULTISPLIT = 4,     /* multisplit levels (numeric pass)                  */
+  GM_STAGE_SYM_HEAVY = 5,      /* symbolic accumulation of chunks                    */
+  GM_STAGE_SYM_LIGHT = 6,      /* symbolic accumulation of light rows                */
+  GM_STAGE_SCAN = 7,           /* prefix sum of C.rowPtr and chunk offsets           */
+  GM_STAGE_NUM_HEAVY = 8,      /* numeric accumulation of chunks                     */
+  GM_STAGE_NUM_LIGHT = 9,      /* numeric accumulation of light rows                 */
+  GM_STAGE_OTHER = 10,         /* everything else                                    */
+  GM_STAGE_TRANSPOSE_SYM = 11, /* the same four stages in the symbolic pass          */
+  GM_STAGE_OUTER_SYM = 12,
+  GM_STAGE_HISTOGRAM_SYM = 13,
+  GM_STAGE_MULTISPLIT_SYM = 14
 };
 
 typedef struct gm_plan_info {
@@ -140,11 +146,16 @@ typedef struct gm_plan_info {
 typedef struct gm_plan gm_plan; /* opaque; owns every workspace buffer */
 
 /* Device memory hooks for the plan's workspace. alloc returns NULL on failure.
- * Both run on the host, in stream order on `stream`. NULL hooks select
- * cudaMallocAsync / cudaFreeAsync. Set before gm_spgemm_analyze. */
+ * Both run on the host, in stream order on `stream`. avail (nullable) returns the
+ * bytes further allocations can still obtain (for sizing heavy-row batches; a
+ * caching allocator counts its cached free blocks), or a negative value when
+ * unknown, in which case cudaMemGetInfo is used. NULL alloc/free hooks select
+ * cudaMallocAsync / cudaFreeAsync. Set before gm_spgemm_analyze; the hooks are
+ * process-wide. */
 typedef void* (*gm_alloc_fn)(void* ctx, size_t bytes, void* stream);
 typedef void (*gm_free_fn)(void* ctx, void* ptr, size_t bytes, void* stream);
-void gm_set_allocator(gm_alloc_fn alloc_fn, gm_free_fn free_fn, void* ctx);
+typedef int64_t (*gm_avail_fn)(void* ctx);
+void gm_set_allocator(gm_alloc_fn alloc_fn, gm_free_fn free_fn, gm_avail_fn avail_fn, void* ctx);
 
 /* Host only. Fills *out with the parameters gMAGNUS Sec. III-D derives for a
  * product with c_m columns (Eqs. (4)-(7)), honouring the overrides in cfg

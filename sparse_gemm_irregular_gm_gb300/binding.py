@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libgm_spgemm.so")
 
 GM_MAX_LEVELS = 16
-GM_NUM_STAGES = 12
+GM_NUM_STAGES = 16
 STATUS_NAMES = ["GM_OK", "GM_ERR_INVALID_ARG", "GM_ERR_DIM_MISMATCH", "GM_ERR_INDEX_OVERFLOW", "GM_ERR_OOM",
                 "GM_ERR_WORKSPACE", "GM_ERR_CUDA", "GM_ERR_DEVICE_TIMEOUT", "GM_ERR_STATE", "GM_ERR_BAD_INDEX"]
 GM_FLAG_TIMING, GM_FLAG_KEEP_INTERMEDIATES, GM_FLAG_LOG = 1, 2, 4
@@ -22,7 +22,8 @@ GM_PIPE_AUTO, GM_PIPE_UNFUSED, GM_PIPE_FUSED_HISTO = 0, 1, 2
 (GM_DBG_IP_COUNTS, GM_DBG_HEAVY_ROWS, GM_DBG_LIGHT_ROWS, GM_DBG_CHAT_ROWPTR, GM_DBG_CHAT_COL, GM_DBG_CHAT_VAL,
  GM_DBG_REORD_ROWPTR, GM_DBG_REORD_COL, GM_DBG_REORD_VAL, GM_DBG_REORD_CHILD) = range(10)
 STAGES = ["analyze", "transpose", "outer", "histogram", "multisplit", "sym_heavy", "sym_light", "scan",
-          "num_heavy", "num_light", "other", "unused"]
+          "num_heavy", "num_light", "other", "transpose_sym", "outer_sym", "histogram_sym", "multisplit_sym",
+          "unused"]
 EXPORTS = ["gm_set_allocator", "gm_spgemm_params", "gm_spgemm_analyze", "gm_spgemm_symbolic", "gm_spgemm_numeric",
            "gm_spgemm_plan_info", "gm_spgemm_plan_destroy", "gm_status_string", "gm_spgemm_debug_copy"]
 
@@ -76,7 +77,7 @@ def load(path: str = LIB_PATH):
     lib = ctypes.CDLL(path)
     P = ctypes.POINTER
     lib.gm_set_allocator.restype = None
-    lib.gm_set_allocator.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    lib.gm_set_allocator.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     lib.gm_spgemm_params.restype = ctypes.c_int
     lib.gm_spgemm_params.argtypes = [ctypes.c_int64, P(gm_config), P(gm_params)]
     lib.gm_spgemm_analyze.restype = ctypes.c_int
@@ -95,7 +96,64 @@ def load(path: str = LIB_PATH):
     lib.gm_spgemm_debug_copy.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                          ctypes.c_int64, P(ctypes.c_int64)]
     _lib = lib
+    use_torch_allocator(True)
     return lib
+
+
+# ---- workspace through torch's caching allocator ---------------------------------
+# The plan's workspace (up to hundreds of GB for large products) is taken from and
+# returned to torch's cache, so repeated products reuse the same device memory
+# instead of mapping and unmapping it each time.
+_ALLOC_T = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p)
+_FREE_T = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p)
+_AVAIL_T = ctypes.CFUNCTYPE(ctypes.c_int64, ctypes.c_void_p)
+_hooks = None
+
+
+def _torch_alloc(ctx, nbytes, stream):
+    import torch
+    for attempt in range(2):
+        try:
+            return torch.cuda.caching_allocator_alloc(int(nbytes), torch.cuda.current_device(), stream or 0)
+        except Exception:
+            if attempt == 0:
+                torch.cuda.empty_cache()
+    return None
+
+
+def _torch_free(ctx, ptr, nbytes, stream):
+    import torch
+    torch.cuda.caching_allocator_delete(ptr)
+
+
+def _torch_avail(ctx):
+    import torch
+    try:
+        free, _ = torch.cuda.mem_get_info()
+        return int(free + torch.cuda.memory_reserved() - torch.cuda.memory_allocated())
+    except Exception:
+        return -1
+
+
+def use_torch_allocator(enable: bool = True):
+    """Route workspace allocations through torch (enable) or back to cudaMallocAsync."""
+    global _hooks
+    lib = _lib
+    if lib is None:
+        return
+    if enable:
+        try:
+            import torch
+            if not torch.cuda.is_available():
+                return
+        except ImportError:
+            return
+        _hooks = (_ALLOC_T(_torch_alloc), _FREE_T(_torch_free), _AVAIL_T(_torch_avail))
+        lib.gm_set_allocator(ctypes.cast(_hooks[0], ctypes.c_void_p), ctypes.cast(_hooks[1], ctypes.c_void_p),
+                             ctypes.cast(_hooks[2], ctypes.c_void_p), None)
+    else:
+        lib.gm_set_allocator(None, None, None, None)
+        _hooks = None
 
 
 def _check(rc: int, where: str):

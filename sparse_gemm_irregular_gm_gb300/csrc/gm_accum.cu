@@ -5,8 +5,9 @@
 //   group size (the binning of Sec. III-E). Rows with u <= 256 use one warp and a
 //   per-warp shared array: the products are sorted by column (bitonic network)
 //   and equal columns are merged. Larger rows use one block and a shared hash
-//   table of >= 2u slots (load factor alpha = 2, modulo hashing, linear probing),
-//   then a bitonic sort of the occupied slots (Sec. III-E).
+//   table of >= 2u slots (load factor alpha = 2, linear probing; the column is
+//   scrambled by a multiplicative hash before the modulo), then a bitonic sort of
+//   the occupied slots (Sec. III-E).
 // * Chunks of C-hat_reord narrower than the dense width: a shared bitmap of the
 //   chunk's columns gives nnz (symbolic) and, by a prefix sum over the bitmap
 //   words, the rank of every column, so values are summed straight into their
@@ -109,9 +110,14 @@ __global__ void __launch_bounds__(WARPS * 32) k_light_warp(LightArgs a) {
 
 // ---- block hash accumulator (light rows and light chunks) ---------------------
 
+// Home slot of column c: the column is scrambled by a multiplicative (Fibonacci)
+// hash before the reduction to [0, cap). Plain c mod cap clusters badly on
+// power-law columns, whose low bits are far from uniform.
 template <bool POW2>
 __device__ __forceinline__ int slot_of(uint32_t c, int cap) {
-  return POW2 ? static_cast<int>(c & static_cast<uint32_t>(cap - 1)) : static_cast<int>(c % static_cast<uint32_t>(cap));
+  const uint32_t h = c * 0x9E3779B1u;
+  return POW2 ? static_cast<int>(h >> (__clz(cap) + 1))
+              : static_cast<int>((static_cast<uint64_t>(h) * static_cast<uint32_t>(cap)) >> 32);
 }
 
 // Insert column c; returns the slot and sets *fresh when the key was new.

@@ -19,6 +19,7 @@ namespace gm {
 
 static gm_alloc_fn g_alloc = nullptr;
 static gm_free_fn g_free = nullptr;
+static gm_avail_fn g_avail = nullptr;
 static void* g_ctx = nullptr;
 static std::atomic<int64_t> g_ws_now{0}, g_ws_peak{0};
 static std::atomic<int64_t> g_launches{0};
@@ -291,6 +292,10 @@ struct gm_plan {
   float stage_ms[GM_NUM_STAGES] = {};
   std::vector<gm::StageEv> evs;
   // intermediates kept for gm_spgemm_debug_copy
+  // Two element buffers (columns, values) reused by every batch and level of a
+  // pass: C-hat in buffer 0, level i writes buffer (i + 1) % 2.
+  gm::DevBuf<int32_t> arena_col[2];
+  gm::DevBuf<double> arena_val[2];
   gm::DevBuf<int32_t> dbg_chat_col;
   gm::DevBuf<double> dbg_chat_val;
   gm::DevBuf<int64_t> dbg_chat_rp;
@@ -511,7 +516,7 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
   gm_status st = GM_OK;
 
   // 1. Masked CSR -> CSC of the batch rows and the slice offsets (Algorithm 3 line 7).
-  int t = p->stage_begin(GM_STAGE_TRANSPOSE);
+  int t = p->stage_begin(numeric ? GM_STAGE_TRANSPOSE : GM_STAGE_TRANSPOSE_SYM);
   DevBuf<int64_t> col_ptr, slice_off;
   DevBuf<int32_t> t_row, wg_op;
   DevBuf<double> t_val;
@@ -526,14 +531,14 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
   p->stage_end(t);
 
   // 2. Outer product into C-hat (Algorithm 4), optionally counting level-0 chunks.
-  t = p->stage_begin(GM_STAGE_OUTER);
-  DevBuf<int32_t> chat_col;
-  DevBuf<double> chat_val;
+  t = p->stage_begin(numeric ? GM_STAGE_OUTER : GM_STAGE_OUTER_SYM);
+  if (p->arena_col[0].n < static_cast<size_t>(ip) || (with_val && p->arena_val[0].n < static_cast<size_t>(ip)))
+    return GM_ERR_WORKSPACE;
+  int32_t* const chat_col = p->arena_col[0].p;
+  double* const chat_val = with_val ? p->arena_val[0].p : nullptr;
   DevBuf<int64_t> lrp;
   DevBuf<unsigned long long> cursor, cnt0;
-  if (!chat_col.alloc(ip, s) || !chat_val.alloc(with_val ? ip : 0, s) || !lrp.alloc(nb + 1, s) ||
-      !cursor.alloc(nb, s))
-    return GM_ERR_OOM;
+  if (!lrp.alloc(nb + 1, s) || !cursor.alloc(nb, s)) return GM_ERR_OOM;
   sub_i64(p->chat_rp.p + h0, nb + 1, p->h_chat_rp[h0], lrp.p, s);
   sub_to_u64(p->chat_rp.p + h0, nb, p->h_chat_rp[h0], cursor.p, s);
   const bool fused = L >= 1 && p->pipeline == GM_PIPE_FUSED_HISTO;
@@ -554,8 +559,8 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
   oa.E = kOuterE;
   oa.wg_first = wg_op.p;
   oa.cursor = cursor.p;
-  oa.out_col = chat_col.p;
-  oa.out_val = with_val ? chat_val.p : nullptr;
+  oa.out_col = chat_col;
+  oa.out_val = chat_val;
   oa.histo = fused ? cnt0.p : nullptr;
   oa.v = L >= 1 ? static_cast<int>(p->P.v_chunks[0]) : 1;
   oa.shift = L >= 1 ? ilog2(p->P.widths[0]) : 0;
@@ -568,8 +573,8 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
   wg_op.release();
   cursor.release();
   if (p->keep) {
-    dbg_copy(p->dbg_chat_col, chat_col.p, ip, s);
-    if (with_val) dbg_copy(p->dbg_chat_val, chat_val.p, ip, s);
+    dbg_copy(p->dbg_chat_col, static_cast<const int32_t*>(chat_col), ip, s);
+    if (with_val) dbg_copy(p->dbg_chat_val, static_cast<const double*>(chat_val), ip, s);
     dbg_copy(p->dbg_chat_rp, lrp.p, nb + 1, s);
   }
 
@@ -584,8 +589,8 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
     launch_gather_i64(p->u.p, heavy, nb, rows_cnt.p, s);
     ListArgs la = base_la;
     la.rp = lrp.p;
-    la.col = chat_col.p;
-    la.val = with_val ? chat_val.p : nullptr;
+    la.col = chat_col;
+    la.val = chat_val;
     la.child_base = par_base[0];
     la.v = 1;
     la.width = p->c_m;
@@ -601,12 +606,10 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
   // 3. Hierarchical multisplit (Algorithm 3 lines 10-20) and accumulation of the
   //    chunks that leave the hierarchy at each level.
   const int64_t* in_rp = lrp.p;
-  const int32_t* in_col = chat_col.p;
-  const double* in_val = with_val ? chat_val.p : nullptr;
+  const int32_t* in_col = chat_col;
+  const double* in_val = chat_val;
   int64_t P_b = nb, in_total = ip;
   std::unique_ptr<DevBuf<int64_t>> prev_rp;
-  std::unique_ptr<DevBuf<int32_t>> prev_col;
-  std::unique_ptr<DevBuf<double>> prev_val;
   for (int i = 0; i < L; ++i) {
     const bool last = i == L - 1;
     const int v = static_cast<int>(p->P.v_chunks[i]);
@@ -616,7 +619,7 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
     const int64_t E = multisplit_pick_E(v, p->P.tau, with_val, p->smem_dev - 1024, &ngr);
     if (E == 0) return GM_ERR_INVALID_ARG;
 
-    t = p->stage_begin(GM_STAGE_HISTOGRAM);
+    t = p->stage_begin(numeric ? GM_STAGE_HISTOGRAM : GM_STAGE_HISTOGRAM_SYM);
     DevBuf<int32_t> wg;
     if (!wg.alloc((in_total + E - 1) / E, s)) return GM_ERR_OOM;
     launch_wg_row(in_rp, P_b, E, wg.p, s);
@@ -671,29 +674,21 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
     sub_to_u64(rrp->p, children, 0, cur.p, s);
     p->stage_end(t);
 
-    t = p->stage_begin(GM_STAGE_MULTISPLIT);
-    auto out_col = std::make_unique<DevBuf<int32_t>>();
-    auto out_val = std::make_unique<DevBuf<double>>();
-    if (!out_col->alloc(in_total, s) || !out_val->alloc(with_val ? in_total : 0, s)) return GM_ERR_OOM;
+    t = p->stage_begin(numeric ? GM_STAGE_MULTISPLIT : GM_STAGE_MULTISPLIT_SYM);
+    int32_t* const out_col = p->arena_col[(i + 1) % 2].p;
+    double* const out_val = with_val ? p->arena_val[(i + 1) % 2].p : nullptr;
     sa.inv = last ? nullptr : inv.p;
     sa.cursor = cur.p;
-    sa.out_col = out_col->p;
-    sa.out_val = with_val ? out_val->p : nullptr;
+    sa.out_col = out_col;
+    sa.out_val = out_val;
     launch_multisplit(sa, s);
     p->stage_end(t);
-    // the level's input is consumed
-    if (i == 0) {
-      chat_col.release();
-      chat_val.release();
-      cnt0.release();
-    }
-    prev_col.reset();
-    prev_val.reset();
+    if (i == 0) cnt0.release();
     if (p->keep) {
       auto d = std::make_unique<LevelDbg>();
       dbg_copy(d->rp, rrp->p, children + 1, s);
-      dbg_copy(d->col, out_col->p, in_total, s);
-      if (with_val) dbg_copy(d->val, out_val->p, in_total, s);
+      dbg_copy(d->col, static_cast<const int32_t*>(out_col), in_total, s);
+      if (with_val) dbg_copy(d->val, static_cast<const double*>(out_val), in_total, s);
       if (!d->child.alloc(children, s)) return GM_ERR_OOM;
       if (last) launch_iota_i64(d->child.p, children, 0, s);
       else cudaMemcpyAsync(d->child.p, perm64.p, children * sizeof(int64_t), cudaMemcpyDeviceToDevice, s);
@@ -710,8 +705,8 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
     }
     ListArgs la = base_la;
     la.rp = rrp->p;
-    la.col = out_col->p;
-    la.val = with_val ? out_val->p : nullptr;
+    la.col = out_col;
+    la.val = out_val;
     la.child_of = last ? nullptr : perm64.p;
     la.child_base = par_base[i] * v;
     la.v = v;
@@ -740,11 +735,9 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
       cudaError_t e = cudaStreamSynchronize(s);
       if (e != cudaSuccess) return cuda_status(p, e);
       prev_rp = std::move(rrp);
-      prev_col = std::move(out_col);
-      prev_val = std::move(out_val);
       in_rp = prev_rp->p;
-      in_col = prev_col->p;
-      in_val = with_val ? prev_val->p : nullptr;
+      in_col = out_col;
+      in_val = out_val;
       P_b = nH;
       in_total = next_total;
     }
@@ -785,6 +778,25 @@ static gm_status plan_batches(gm_plan* p, int64_t bytes_per_ip, int64_t cap,
   return GM_OK;
 }
 
+// Element buffers for the largest batch of a pass (values only in the numeric pass
+// or when intermediates are kept).
+static gm_status alloc_arena(gm_plan* p, const std::vector<std::pair<int64_t, int64_t>>& batches, bool with_val) {
+  int64_t mx = 0;
+  for (auto& b : batches) mx = std::max(mx, p->h_chat_rp[b.second] - p->h_chat_rp[b.first]);
+  for (int k = 0; k < 2; ++k) {
+    if (!p->arena_col[k].alloc(mx, p->s)) return GM_ERR_OOM;
+    if (!p->arena_val[k].alloc(with_val ? mx : 0, p->s)) return GM_ERR_OOM;
+  }
+  return GM_OK;
+}
+
+static void free_arena(gm_plan* p) {
+  for (int k = 0; k < 2; ++k) {
+    p->arena_col[k].release();
+    p->arena_val[k].release();
+  }
+}
+
 static int64_t workspace_cap(gm_plan* p) {
   if (p->cfg.workspace_cap_bytes > 0) return p->cfg.workspace_cap_bytes;
   size_t free_b = 0, total_b = 0;
@@ -793,8 +805,13 @@ static int64_t workspace_cap(gm_plan* p) {
     cudaGetLastError();
     return int64_t(1) << 30;
   }
+  int64_t avail = static_cast<int64_t>(free_b);
+  if (g_avail) {
+    const int64_t a = g_avail(g_ctx);
+    if (a >= 0) avail = a;
+  }
   const int64_t reserve = (int64_t(1) << 30) + static_cast<int64_t>(total_b) / 50;
-  return std::max<int64_t>(static_cast<int64_t>(free_b) - reserve, int64_t(256) << 20);
+  return std::max<int64_t>(avail - reserve, int64_t(256) << 20);
 }
 
 static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, double* c_val) {
@@ -837,11 +854,14 @@ static gm_status symbolic_impl(gm_plan* p, int64_t* C_rp, int64_t* C_nnz) {
     if (st != GM_OK) return st;
     if (p->keep && batches.size() != 1) p->keep = false;
     p->n_batches = static_cast<int64_t>(batches.size());
+    st = alloc_arena(p, batches, p->keep);
+    if (st != GM_OK) return st;
     int64_t par_base[GM_MAX_LEVELS + 1] = {};
     for (auto& bt : batches) {
       st = run_batch(p, bt.first, bt.second, false, par_base, nullptr, nullptr);
       if (st != GM_OK) return st;
     }
+    free_arena(p);
     for (int i = 0; i <= L; ++i) p->n_par[i] = par_base[i];
     p->n_par[0] = nh;
     // bottom-up: a heavy chunk's nnz is the sum over its chunks at the next level
@@ -893,11 +913,14 @@ static gm_status numeric_impl(gm_plan* p, int32_t* C_col, double* C_val) {
     gm_status st = plan_batches(p, 24, workspace_cap(p), batches);
     if (st != GM_OK) return st;
     p->n_batches = std::max<int64_t>(p->n_batches, static_cast<int64_t>(batches.size()));
+    st = alloc_arena(p, batches, true);
+    if (st != GM_OK) return st;
     int64_t par_base[GM_MAX_LEVELS + 1] = {};
     for (auto& bt : batches) {
       st = run_batch(p, bt.first, bt.second, true, par_base, C_col, C_val);
       if (st != GM_OK) return st;
     }
+    free_arena(p);
     p->keep = keep;
   }
   return sync_check(p);
@@ -917,9 +940,10 @@ static void log_plan(const gm_plan* p) {
 
 extern "C" {
 
-void gm_set_allocator(gm_alloc_fn alloc_fn, gm_free_fn free_fn, void* ctx) {
+void gm_set_allocator(gm_alloc_fn alloc_fn, gm_free_fn free_fn, gm_avail_fn avail_fn, void* ctx) {
   gm::g_alloc = alloc_fn;
   gm::g_free = free_fn;
+  gm::g_avail = avail_fn;
   gm::g_ctx = ctx;
 }
 

@@ -214,6 +214,8 @@ WORKLOADS = {
              lambda seed=1: erdos_renyi(1 << 21, 8, seed=seed)),
     "rmat18": ("A*A, R-MAT scale 18, edge factor 16, fp64 U[-1,1)",
                lambda seed=1: rmat(18, 16, seed=seed)),
+    "rmat16": ("A*A, R-MAT scale 16, edge factor 16, fp64 U[-1,1) (small profiling case)",
+               lambda seed=1: rmat(16, 16, seed=seed)),
     "rmat20": ("A*A, R-MAT scale 20, edge factor 16, fp64 U[-1,1)",
                lambda seed=1: rmat(20, 16, seed=seed)),
 }
