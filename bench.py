@@ -342,11 +342,15 @@ def run_e2e(args, A, cfg, stream, nnz_c, ip_total):
     o_val = torch.empty(nnz_c, dtype=torch.float64, pin_memory=True)
     log(f"e2e: pinned {d2h / 1e9:.1f} GB of host memory in {time.perf_counter() - t0:.1f} s")
 
+    d_rp = torch.empty_like(h_rp, device="cuda")
+    d_col = torch.empty_like(h_col, device="cuda")
+    d_val = torch.empty_like(h_val, device="cuda")
+    Ad = binding.DeviceCSR(A.n_rows, A.n_cols, d_rp, d_col, d_val)
+
     def step():
-        d_rp = h_rp.to("cuda", non_blocking=True)
-        d_col = h_col.to("cuda", non_blocking=True)
-        d_val = h_val.to("cuda", non_blocking=True)
-        Ad = binding.DeviceCSR(A.n_rows, A.n_cols, d_rp, d_col, d_val)
+        d_rp.copy_(h_rp, non_blocking=True)
+        d_col.copy_(h_col, non_blocking=True)
+        d_val.copy_(h_val, non_blocking=True)
         C = binding.spgemm(Ad, Ad, cfg, stream)
         o_rp.copy_(C.row_ptr, non_blocking=True)
         o_col.copy_(C.col, non_blocking=True)

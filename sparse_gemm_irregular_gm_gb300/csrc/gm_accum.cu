@@ -257,9 +257,13 @@ __global__ void k_leaf_bitmap(ListArgs a, int nwords, int cap_vals) {
     const int64_t child_local = a.child_of ? a.child_of[m] : m;
     for (int w = threadIdx.x; w < nwords; w += T) bm[w] = 0u;
     __syncthreads();
-    for (int64_t e = lo + threadIdx.x; e < hi; e += T) {
-      const uint32_t c = static_cast<uint32_t>(a.col[e]);
-      atomicOr(&bm[c >> 5], 1u << (c & 31));
+    for (int64_t e0 = lo + threadIdx.x; e0 < hi; e0 += 4 * T) {  // 4 loads in flight per thread
+      uint32_t c[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) c[u] = e0 + u * T < hi ? static_cast<uint32_t>(a.col[e0 + u * T]) : ~0u;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c[u] != ~0u) atomicOr(&bm[c[u] >> 5], 1u << (c[u] & 31));
     }
     __syncthreads();
     int acc = 0;
@@ -287,11 +291,22 @@ __global__ void k_leaf_bitmap(ListArgs a, int nwords, int cap_vals) {
     }
     for (int r = threadIdx.x; r < nnz; r += T) vals[r] = 0.0;
     __syncthreads();
-    for (int64_t e = lo + threadIdx.x; e < hi; e += T) {
-      const uint32_t c = static_cast<uint32_t>(a.col[e]);
-      const int w = c >> 5;
-      const int r = pre[w] + __popc(bm[w] & ((1u << (c & 31)) - 1u));
-      atomicAdd(&vals[r], a.val[e]);
+    for (int64_t e0 = lo + threadIdx.x; e0 < hi; e0 += 4 * T) {
+      uint32_t c[4];
+      double v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const bool in = e0 + u * T < hi;
+        c[u] = in ? static_cast<uint32_t>(a.col[e0 + u * T]) : ~0u;
+        v[u] = in ? a.val[e0 + u * T] : 0.0;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (c[u] == ~0u) continue;
+        const int w = c[u] >> 5;
+        const int r = pre[w] + __popc(bm[w] & ((1u << (c[u] & 31)) - 1u));
+        atomicAdd(&vals[r], v[u]);
+      }
     }
     __syncthreads();
     const int64_t out = a.off_in[a.child_base + child_local];
@@ -299,6 +314,105 @@ __global__ void k_leaf_bitmap(ListArgs a, int nwords, int cap_vals) {
     for (int r = threadIdx.x; r < nnz; r += T) {
       a.c_col[out + r] = static_cast<int32_t>(cb + cols[r]);
       a.c_val[out + r] = vals[r];
+    }
+    __syncthreads();
+  }
+}
+
+// Small chunk of width <= dense width, elements held in registers (n <= T * ITEMS).
+// Symbolic: bitmap popcount. Numeric without floating-point atomics: the bitmap
+// prefix gives each element its rank r (sorted output slot); an int32 atomic on
+// cnt[r] gives its arrival index j; a prefix sum over cnt turns counts into
+// segment starts; values are placed at seg[r] + j and each output entry sums its
+// own segment.
+template <bool SYM, int T, int ITEMS>
+__global__ void __launch_bounds__(T) k_leaf_small(ListArgs a, int nwords) {
+  constexpr int CAP = T * ITEMS;
+  extern __shared__ __align__(16) unsigned char smem[];
+  double* vbuf = reinterpret_cast<double*>(smem);                              // CAP
+  int32_t* cols = reinterpret_cast<int32_t*>(vbuf + (SYM ? 0 : CAP));           // CAP
+  int* seg = reinterpret_cast<int*>(cols + (SYM ? 0 : CAP));                     // CAP + 1
+  uint32_t* bm = reinterpret_cast<uint32_t*>(seg + (SYM ? 0 : CAP + 1));         // nwords
+  int* pre = reinterpret_cast<int*>(bm + nwords);                                // nwords
+  __shared__ int ws[33];
+  const int per = (nwords + T - 1) / T;
+  const int w0 = threadIdx.x * per, w1 = min(nwords, w0 + per);
+  for (int64_t item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+    const int64_t m = a.items[item];
+    const int64_t lo = a.rp[m], hi = a.rp[m + 1];
+    const int64_t child_local = a.child_of ? a.child_of[m] : m;
+    int key[ITEMS];   // column, later rank
+    int arr[ITEMS];   // arrival index within the rank
+    double val[ITEMS];
+#pragma unroll
+    for (int k = 0; k < ITEMS; ++k) {
+      const int64_t e = lo + k * T + threadIdx.x;
+      key[k] = -1;
+      val[k] = 0.0;
+      if (e < hi) {
+        key[k] = a.col[e];
+        if (!SYM) val[k] = a.val[e];
+      }
+    }
+    for (int w = threadIdx.x; w < nwords; w += T) bm[w] = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < ITEMS; ++k)
+      if (key[k] >= 0) atomicOr(&bm[key[k] >> 5], 1u << (key[k] & 31));
+    __syncthreads();
+    int acc = 0;
+    for (int w = w0; w < w1; ++w) acc += __popc(bm[w]);
+    int nnz;
+    int run = block_exclusive_scan(acc, ws, &nnz);
+    if (SYM) {
+      if (threadIdx.x == 0) a.nnz_out[a.child_base + child_local] = nnz;
+      __syncthreads();
+      continue;
+    }
+    for (int w = w0; w < w1; ++w) {
+      pre[w] = run;
+      uint32_t bits = bm[w];
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        cols[run++] = w * 32 + b;
+      }
+    }
+    for (int r = threadIdx.x; r <= nnz; r += T) seg[r] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < ITEMS; ++k) {
+      if (key[k] >= 0) {
+        const int w = key[k] >> 5;
+        key[k] = pre[w] + __popc(bm[w] & ((1u << (key[k] & 31)) - 1u));
+        arr[k] = atomicAdd(&seg[key[k]], 1);
+      }
+    }
+    __syncthreads();
+    {  // counts -> segment starts (exclusive), contiguous run per thread
+      const int per_r = (nnz + T) / T;
+      const int r0 = threadIdx.x * per_r, r1 = min(nnz + 1, r0 + per_r);
+      int c = 0;
+      for (int r = r0; r < r1; ++r) c += seg[r];
+      int base = block_exclusive_scan(c, ws, static_cast<int*>(nullptr));
+      for (int r = r0; r < r1; ++r) {
+        const int x = seg[r];
+        seg[r] = base;
+        base += x;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < ITEMS; ++k)
+      if (key[k] >= 0) vbuf[seg[key[k]] + arr[k]] = val[k];
+    __syncthreads();
+    const int64_t out = a.off_in[a.child_base + child_local];
+    const int64_t cb = leaf_col_base(a, child_local);
+    for (int r = threadIdx.x; r < nnz; r += T) {
+      double sum = 0.0;
+      for (int q = seg[r]; q < seg[r + 1]; ++q) sum += vbuf[q];
+      a.c_col[out + r] = static_cast<int32_t>(cb + cols[r]);
+      a.c_val[out + r] = sum;
     }
     __syncthreads();
   }
@@ -396,6 +510,28 @@ void launch_light_rows(const LightArgs& a, int cap, bool symbolic, cudaStream_t 
 int leaf_bitmap_smem(int64_t width, int cap_vals, bool symbolic) {
   const int64_t nwords = (width + 31) / 32;
   return static_cast<int>(nwords * 8 + (symbolic ? 0 : static_cast<int64_t>(cap_vals) * 12));
+}
+
+int leaf_small_smem(int64_t width, int cap, bool symbolic) {
+  const int64_t nwords = (width + 31) / 32;
+  return static_cast<int>(nwords * 8 + (symbolic ? 0 : static_cast<int64_t>(cap) * 16 + 4));
+}
+
+void launch_leaf_small(const ListArgs& a, int max_elems, bool symbolic, cudaStream_t s) {
+  if (a.n_items <= 0) return;
+  const int nwords = static_cast<int>((a.width + 31) / 32);
+  const unsigned g = item_grid(a.n_items, 8);
+  if (max_elems <= 1024) {
+    const size_t smem = static_cast<size_t>(leaf_small_smem(a.width, 1024, symbolic));
+    auto fn = symbolic ? k_leaf_small<true, 128, 8> : k_leaf_small<false, 128, 8>;
+    set_smem(fn, smem);
+    (fn<<<g, 128, smem, s>>>(a, nwords), note_launch());
+  } else {
+    const size_t smem = static_cast<size_t>(leaf_small_smem(a.width, 4096, symbolic));
+    auto fn = symbolic ? k_leaf_small<true, 256, 16> : k_leaf_small<false, 256, 16>;
+    set_smem(fn, smem);
+    (fn<<<g, 256, smem, s>>>(a, nwords), note_launch());
+  }
 }
 
 void launch_leaf_bitmap(const ListArgs& a, int cap_vals, bool symbolic, cudaStream_t s) {

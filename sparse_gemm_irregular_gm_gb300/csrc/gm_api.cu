@@ -34,6 +34,14 @@ void note_launch(int n) {
 }
 int64_t launch_count() { return g_launches.load(); }
 
+static bool env_log_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("GM_SPGEMM_LOG");
+    return e && e[0] == '1';
+  }();
+  return on;
+}
+
 void* ws_alloc(size_t bytes, cudaStream_t s) {
   if (bytes == 0) return nullptr;
   void* p = nullptr;
@@ -43,6 +51,9 @@ void* ws_alloc(size_t bytes, cudaStream_t s) {
     cudaGetLastError();
     p = nullptr;
   }
+  if (!p && env_log_enabled())
+    std::fprintf(stderr, "[gm_spgemm] workspace allocation of %.3f GB failed (%.3f GB held)\n", bytes / 1e9,
+                 g_ws_now.load() / 1e9);
   if (p) {
     const int64_t now = g_ws_now += static_cast<int64_t>(bytes);
     int64_t pk = g_ws_peak.load();
@@ -264,13 +275,16 @@ struct gm_plan {
   cudaStream_t s = nullptr;
   int device = 0;
   int64_t smem_dev = 0;
+  int num_sms = 1;
   int64_t c_m = 1;
+  bool sym_rowbm = false;  // heavy symbolic through whole-row bitmaps
   gm_params P{};
   int L = 0;
   int state = 0;  // 1 analyzed, 2 symbolic done, 3 numeric done
   int pipeline = GM_PIPE_FUSED_HISTO;
   bool timing = false, log = false, keep = false;
   gm::DevBuf<int> status;
+  gm::DevBuf<unsigned int> work_counter;
   gm::DevBuf<int64_t> u;
   gm::DevBuf<uint8_t> bin;
   gm::DevBuf<int32_t> rows_by_bin;
@@ -293,9 +307,17 @@ struct gm_plan {
   std::vector<gm::StageEv> evs;
   // intermediates kept for gm_spgemm_debug_copy
   // Two element buffers (columns, values) reused by every batch and level of a
-  // pass: C-hat in buffer 0, level i writes buffer (i + 1) % 2.
-  gm::DevBuf<int32_t> arena_col[2];
-  gm::DevBuf<double> arena_val[2];
+  // pass: C-hat in buffer 0, level i writes buffer (i + 1) % 2. One allocation
+  // (arena_block) holds all four, so a caching allocator sees one fixed size.
+  gm::DevBuf<unsigned char> arena_block;
+  struct {
+    int32_t* p = nullptr;
+    size_t n = 0;
+  } arena_col[2];
+  struct {
+    double* p = nullptr;
+    size_t n = 0;
+  } arena_val[2];
   gm::DevBuf<int32_t> dbg_chat_col;
   gm::DevBuf<double> dbg_chat_val;
   gm::DevBuf<int64_t> dbg_chat_rp;
@@ -371,7 +393,7 @@ static gm_status check_csr(const gm_csr* M) {
 static gm_status analyze_impl(gm_plan* p) {
   const cudaStream_t s = p->s;
   const int64_t n = p->A.n_rows;
-  if (!p->status.alloc(1, s)) return GM_ERR_OOM;
+  if (!p->status.alloc(1, s) || !p->work_counter.alloc(1, s)) return GM_ERR_OOM;
   cudaMemsetAsync(p->status.p, 0, sizeof(int), s);
   const int t0 = p->stage_begin(GM_STAGE_ANALYZE);
   // Validation first: nothing below may index with unchecked row pointers or columns.
@@ -487,7 +509,8 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
     a.items = items.p + starts[b];
     a.n_items = cnt;
     p->n_leaves += numeric ? 0 : cnt;
-    if (dense) launch_leaf_bitmap(a, bitmap_leaf_cap(b, la.width), !numeric, s);
+    if (dense && b <= 2) launch_leaf_small(a, b == 1 ? 1024 : 4096, !numeric, s);
+    else if (dense) launch_leaf_bitmap(a, bitmap_leaf_cap(b, la.width), !numeric, s);
     else launch_leaf_hash(a, hash_leaf_cap(b, p->P.tau, p->smem_dev), !numeric, s);
   }
   e = cudaGetLastError();
@@ -778,23 +801,55 @@ static gm_status plan_batches(gm_plan* p, int64_t bytes_per_ip, int64_t cap,
   return GM_OK;
 }
 
+static int64_t workspace_cap(gm_plan* p);
+
 // Element buffers for the largest batch of a pass (values only in the numeric pass
 // or when intermediates are kept).
 static gm_status alloc_arena(gm_plan* p, const std::vector<std::pair<int64_t, int64_t>>& batches, bool with_val) {
   int64_t mx = 0;
   for (auto& b : batches) mx = std::max(mx, p->h_chat_rp[b.second] - p->h_chat_rp[b.first]);
+  if (p->log)
+    std::fprintf(stderr, "[gm_spgemm] %zu batch(es), largest %lld products, arena %.2f GB\n", batches.size(),
+                 (long long)mx, mx * (with_val ? 24.0 : 8.0) / 1e9);
+  const size_t col_b = ((static_cast<size_t>(mx) * 4 + 255) / 256) * 256;
+  const size_t val_b = with_val ? static_cast<size_t>(mx) * 8 : 0;
+  if (!p->arena_block.alloc(2 * (col_b + val_b), p->s)) return GM_ERR_OOM;
+  unsigned char* base = p->arena_block.p;
   for (int k = 0; k < 2; ++k) {
-    if (!p->arena_col[k].alloc(mx, p->s)) return GM_ERR_OOM;
-    if (!p->arena_val[k].alloc(with_val ? mx : 0, p->s)) return GM_ERR_OOM;
+    p->arena_val[k].p = with_val ? reinterpret_cast<double*>(base + k * val_b) : nullptr;
+    p->arena_val[k].n = with_val ? mx : 0;
+    p->arena_col[k].p = reinterpret_cast<int32_t*>(base + 2 * val_b + k * col_b);
+    p->arena_col[k].n = mx;
   }
   return GM_OK;
 }
 
 static void free_arena(gm_plan* p) {
+  p->arena_block.release();
   for (int k = 0; k < 2; ++k) {
-    p->arena_col[k].release();
-    p->arena_val[k].release();
+    p->arena_col[k] = {};
+    p->arena_val[k] = {};
   }
+}
+
+// Plans batches under the workspace cap and allocates the arena; when the arena
+// does not fit after all (a caching allocator's blocks can be fragmented), the
+// cap is halved and the batches planned again, a few times.
+static gm_status plan_and_alloc(gm_plan* p, int64_t bytes_per_ip, bool with_val,
+                                std::vector<std::pair<int64_t, int64_t>>& batches) {
+  int64_t cap = workspace_cap(p);
+  for (int attempt = 0; attempt < 6; ++attempt) {
+    gm_status st = plan_batches(p, bytes_per_ip, cap, batches);
+    if (st != GM_OK) return st;
+    st = alloc_arena(p, batches, with_val);
+    if (st == GM_OK) return GM_OK;
+    free_arena(p);
+    cudaStreamSynchronize(p->s);
+    cudaGetLastError();
+    cap /= 2;
+    if (p->log) std::fprintf(stderr, "[gm_spgemm] arena did not fit; retrying with a cap of %.2f GB\n", cap / 1e9);
+  }
+  return GM_ERR_OOM;
 }
 
 static int64_t workspace_cap(gm_plan* p) {
@@ -811,13 +866,37 @@ static int64_t workspace_cap(gm_plan* p) {
     if (a >= 0) avail = a;
   }
   const int64_t reserve = (int64_t(1) << 30) + static_cast<int64_t>(total_b) / 50;
-  return std::max<int64_t>(avail - reserve, int64_t(256) << 20);
+  const int64_t cap = std::max<int64_t>(avail - reserve, int64_t(256) << 20);
+  if (p->log)
+    std::fprintf(stderr, "[gm_spgemm] free %.2f GB, available %.2f GB, workspace cap %.2f GB\n", free_b / 1e9,
+                 avail / 1e9, cap / 1e9);
+  return cap;
 }
 
 static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, double* c_val) {
   for (int b = 1; b <= 10; ++b) {
     const int64_t cnt = p->bin_start[b + 1] - p->bin_start[b];
     if (cnt <= 0) continue;
+    const int cap = b <= 9 ? static_cast<int>(light_bin_ub(b)) : static_cast<int>(p->P.tau);
+    if (numeric && b >= 7 && rowbm_numeric_smem(p->c_m, cap) + 1024 <= p->smem_dev) {
+      RowBitmapArgs ra{};
+      ra.rows = p->rows_by_bin.p + p->bin_start[b];
+      ra.n_items = cnt;
+      ra.a_rp = p->A.row_ptr;
+      ra.a_col = p->A.col_idx;
+      ra.a_val = p->A.vals;
+      ra.b_rp = p->B.row_ptr;
+      ra.b_col = p->B.col_idx;
+      ra.b_val = p->B.vals;
+      ra.c_m = p->c_m;
+      ra.c_rp = p->c_rp;
+      ra.c_col = c_col;
+      ra.c_val = c_val;
+      ra.work_counter = p->work_counter.p;
+      ra.status = p->status.p;
+      launch_rowbm(ra, false, cap, p->num_sms, p->smem_dev, p->s);
+      continue;
+    }
     LightArgs la{};
     la.rows = p->rows_by_bin.p + p->bin_start[b];
     la.n_items = cnt;
@@ -849,13 +928,44 @@ static gm_status symbolic_impl(gm_plan* p, int64_t* C_rp, int64_t* C_nnz) {
     const int64_t v0 = L >= 1 ? p->P.v_chunks[0] : 1;
     if (!p->nnz[0].ensure(nh * v0, 0, s)) return GM_ERR_OOM;
     cudaMemsetAsync(p->nnz[0].p, 0, nh * v0 * sizeof(int64_t), s);
+    if (p->sym_rowbm) {
+      // whole-row bitmaps: chunk nnz without expanding C-hat (at most one level)
+      RowBitmapArgs ra{};
+      ra.rows = p->rows_by_bin.p + p->bin_start[kHeavyBin];
+      ra.n_items = nh;
+      ra.a_rp = p->A.row_ptr;
+      ra.a_col = p->A.col_idx;
+      ra.a_val = p->A.vals;
+      ra.b_rp = p->B.row_ptr;
+      ra.b_col = p->B.col_idx;
+      ra.b_val = p->B.vals;
+      ra.c_m = p->c_m;
+      ra.v = static_cast<int>(v0);
+      ra.width = L >= 1 ? p->P.widths[0] : (int64_t(1) << 40);
+      ra.nnz_out = p->nnz[0].p;
+      ra.item_base = 0;
+      ra.c_rp = C_rp;
+      ra.work_counter = p->work_counter.p;
+      ra.status = p->status.p;
+      const int ts = p->stage_begin(GM_STAGE_SYM_HEAVY);
+      launch_rowbm(ra, true, 0, p->num_sms, p->smem_dev, s);
+      p->stage_end(ts);
+      p->n_batches = 0;
+      p->n_leaves += nh * v0;
+      if (L >= 1) sum_children(p->nnz[0].p, p->heavy_ids64.p, C_rp, nh, static_cast<int>(v0), s);
+      else launch_scatter_i64(p->nnz[0].p, p->rows_by_bin.p + p->bin_start[kHeavyBin], nh, C_rp, s);
+      goto heavy_done;
+    }
     std::vector<std::pair<int64_t, int64_t>> batches;
-    gm_status st = plan_batches(p, p->keep ? 24 : 8, workspace_cap(p), batches);
+    gm_status st = plan_and_alloc(p, p->keep ? 24 : 8, p->keep, batches);
     if (st != GM_OK) return st;
-    if (p->keep && batches.size() != 1) p->keep = false;
+    if (p->keep && batches.size() != 1) {  // intermediates are kept for a single batch only
+      p->keep = false;
+      free_arena(p);
+      st = alloc_arena(p, batches, false);
+      if (st != GM_OK) return st;
+    }
     p->n_batches = static_cast<int64_t>(batches.size());
-    st = alloc_arena(p, batches, p->keep);
-    if (st != GM_OK) return st;
     int64_t par_base[GM_MAX_LEVELS + 1] = {};
     for (auto& bt : batches) {
       st = run_batch(p, bt.first, bt.second, false, par_base, nullptr, nullptr);
@@ -872,6 +982,7 @@ static gm_status symbolic_impl(gm_plan* p, int64_t* C_rp, int64_t* C_nnz) {
     if (L >= 1) sum_children(p->nnz[0].p, p->heavy_ids64.p, C_rp, nh, static_cast<int>(v0), s);
     else launch_scatter_i64(p->nnz[0].p, p->rows_by_bin.p + p->bin_start[kHeavyBin], nh, C_rp, s);
   }
+heavy_done:
   t = p->stage_begin(GM_STAGE_SCAN);
   if (!scan_exclusive_i64(C_rp, C_rp, n + 1, nullptr, s)) return GM_ERR_OOM;
   cudaMemcpyAsync(&p->c_nnz, C_rp + n, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
@@ -910,11 +1021,9 @@ static gm_status numeric_impl(gm_plan* p, int32_t* C_col, double* C_val) {
     const bool keep = p->keep;
     p->keep = false;
     std::vector<std::pair<int64_t, int64_t>> batches;
-    gm_status st = plan_batches(p, 24, workspace_cap(p), batches);
+    gm_status st = plan_and_alloc(p, 24, true, batches);
     if (st != GM_OK) return st;
     p->n_batches = std::max<int64_t>(p->n_batches, static_cast<int64_t>(batches.size()));
-    st = alloc_arena(p, batches, true);
-    if (st != GM_OK) return st;
     int64_t par_base[GM_MAX_LEVELS + 1] = {};
     for (auto& bt : batches) {
       st = run_batch(p, bt.first, bt.second, true, par_base, C_col, C_val);
@@ -972,6 +1081,7 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
   cudaError_t e = cudaGetDevice(&p->device);
   int smem = 0;
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return GM_ERR_CUDA;
@@ -981,6 +1091,8 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
   st = gm::compute_params(p->c_m, &p->cfg, p->smem_dev, &p->P);
   if (st != GM_OK) return st;
   p->L = static_cast<int>(p->P.n_levels);
+  p->sym_rowbm = p->L <= 1 && p->pipeline != GM_PIPE_UNFUSED && !p->keep &&
+                 gm::rowbm_symbolic_smem(p->c_m) + 1024 <= p->smem_dev;
   gm::g_ws_peak = gm::g_ws_now.load();
   const int64_t l0 = gm::launch_count();
   st = gm::analyze_impl(p.get());

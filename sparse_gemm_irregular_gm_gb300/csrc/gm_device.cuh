@@ -15,6 +15,28 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   return m;
 }
 
+// Runs of equal keys in consecutive lanes. run_heads() returns the ballot of the
+// lanes that start a run; keys equal but not adjacent form separate runs (each
+// run then makes its own update, which stays correct).
+template <class K>
+__device__ __forceinline__ unsigned run_heads(K key) {
+  const int lane = threadIdx.x & 31;
+  const K prev = __shfl_up_sync(kFull, key, 1);
+  return __ballot_sync(kFull, lane == 0 || prev != key);
+}
+// First lane of the run holding this lane.
+__device__ __forceinline__ int run_head_lane(unsigned heads) {
+  const int lane = threadIdx.x & 31;
+  const unsigned le = lane == 31 ? kFull : ((2u << lane) - 1u);
+  return 31 - __clz(heads & le);
+}
+// Length of the run starting at this lane (meaningful on head lanes).
+__device__ __forceinline__ int run_length(unsigned heads) {
+  const int lane = threadIdx.x & 31;
+  const unsigned after = lane == 31 ? 0u : (heads & ~((2u << lane) - 1u));
+  return (after ? __ffs(after) - 1 : 32) - lane;
+}
+
 template <class T>
 __device__ __forceinline__ T warp_inclusive_scan(T x) {
   const int lane = threadIdx.x & 31;

@@ -121,12 +121,15 @@ __global__ void __launch_bounds__(kOpThreads) k_outer(OuterArgs a) {
     for (int base = p_beg + warp * 32; base < p_end; base += nwarps * 32) {
       const int p = base + lane;
       const bool ok = p < p_end;
-      // largest j with s_lo[j] <= p; entries only move forward with p
-      int hi_j = nr - 1;
+      // largest j with s_lo[j] <= p; entries only move forward with p. Fast path:
+      // the lane is still inside the warp's current entry.
       int lo_j = j;
-      while (lo_j < hi_j) {
-        const int mid = (lo_j + hi_j + 1) >> 1;
-        if (s_lo[mid] <= p) lo_j = mid; else hi_j = mid - 1;
+      if (lo_j + 1 < nr && s_lo[lo_j + 1] <= p) {
+        int hi_j = nr - 1;
+        while (lo_j < hi_j) {
+          const int mid = (lo_j + hi_j + 1) >> 1;
+          if (s_lo[mid] <= p) lo_j = mid; else hi_j = mid - 1;
+        }
       }
       const int jj = lo_j;
       j = __shfl_sync(kFull, jj, 0);
@@ -142,9 +145,9 @@ __global__ void __launch_bounds__(kOpThreads) k_outer(OuterArgs a) {
         const unsigned long long key =
             ok ? static_cast<unsigned long long>(s_row[jj]) * a.v + (static_cast<uint32_t>(col) >> a.shift)
                : ~0ull;
-        const unsigned peers = __match_any_sync(kFull, key);
-        if (ok && (peers & lanemask_lt()) == 0)
-          atomicAdd(&a.histo[key], static_cast<unsigned long long>(__popc(peers)));
+        const unsigned heads = run_heads(key);
+        if (ok && ((heads >> lane) & 1u))
+          atomicAdd(&a.histo[key], static_cast<unsigned long long>(run_length(heads)));
       }
     }
     __syncthreads();

@@ -220,6 +220,35 @@ void launch_leaf_bitmap(const ListArgs& a, int cap_vals, bool symbolic, cudaStre
 // Light chunks of a wide level: shared-memory hash accumulator (cap slots).
 void launch_leaf_hash(const ListArgs& a, int cap, bool symbolic, cudaStream_t s);
 int leaf_bitmap_smem(int64_t width, int cap_vals, bool symbolic);
+// Chunks with at most max_elems (<= 4096) elements, held in registers; no
+// floating-point atomics.
+void launch_leaf_small(const ListArgs& a, int max_elems, bool symbolic, cudaStream_t s);
+int leaf_small_smem(int64_t width, int cap, bool symbolic);
+
+// ---- whole-row bitmaps (gm_rowbitmap.cu) -----------------------------------------
+struct RowBitmapArgs {
+  const int32_t* rows;        // rows of A to process (original ids)
+  int64_t n_items;
+  const int64_t* a_rp;
+  const int32_t* a_col;
+  const double* a_val;
+  const int64_t* b_rp;
+  const int32_t* b_col;
+  const double* b_val;
+  int64_t c_m;                // columns of C
+  int v;                      // symbolic: chunks per row (1 with width >= C.m: whole row)
+  int64_t width;              // symbolic: chunk width
+  int64_t* nnz_out;           // symbolic: [(item_base + item) * v + c]; whole row: null writes c_rp[row]
+  int64_t item_base;
+  int64_t* c_rp;              // whole-row symbolic: counts out; numeric: row offsets in
+  int32_t* c_col;
+  double* c_val;
+  unsigned int* work_counter; // device counter for dynamic row scheduling
+  int* status;
+};
+int64_t rowbm_symbolic_smem(int64_t c_m);
+int64_t rowbm_numeric_smem(int64_t c_m, int cap);
+void launch_rowbm(const RowBitmapArgs& a, bool symbolic, int cap, int num_sms, int64_t smem_max, cudaStream_t s);
 
 // Light-row bins: upper bounds on u and table capacity per bin.
 constexpr int kLightWarpBins = 4;   // bins 1..4 use a warp per row

@@ -88,17 +88,14 @@ __global__ void __launch_bounds__(kMsThreads) k_split(SplitArgs a) {
 
   int key[ITEMS];
   int32_t col[ITEMS];
-  double val[ITEMS];
   bool bad = false;
 #pragma unroll
   for (int k = 0; k < ITEMS; ++k) {
     const int e = k * T + threadIdx.x;
     key[k] = -1;
     col[k] = 0;
-    val[k] = 0.0;
     if (e < n) {
       col[k] = a.in_col[a.base + S + e];
-      if (VAL && SPLIT) val[k] = a.in_val[a.base + S + e];
       const int j = local_row(L.row_end, a.n_group_rows, e);
       if (j < a.n_group_rows) key[k] = j * a.v + (static_cast<uint32_t>(col[k]) >> a.shift);
       else bad = true;
@@ -107,8 +104,8 @@ __global__ void __launch_bounds__(kMsThreads) k_split(SplitArgs a) {
   if (bad) atomicOr(a.status, kStGroupRows);
 #pragma unroll
   for (int k = 0; k < ITEMS; ++k) {
-    const unsigned peers = __match_any_sync(kFull, key[k]);
-    if (key[k] >= 0 && (peers & lanemask_lt()) == 0) atomicAdd(&L.hist[key[k]], __popc(peers));
+    const unsigned heads = run_heads(key[k]);
+    if (key[k] >= 0 && ((heads >> (threadIdx.x & 31)) & 1u)) atomicAdd(&L.hist[key[k]], run_length(heads));
   }
   __syncthreads();
 
@@ -152,15 +149,16 @@ __global__ void __launch_bounds__(kMsThreads) k_split(SplitArgs a) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int k = 0; k < ITEMS; ++k) {
-    const unsigned peers = __match_any_sync(kFull, key[k]);
-    const int leader = __ffs(peers) - 1;
+    const unsigned heads = run_heads(key[k]);
+    const int leader = run_head_lane(heads);
     int b = 0;
-    if (key[k] >= 0 && lane == leader) b = atomicAdd(&L.hist[key[k]], __popc(peers));
+    if (key[k] >= 0 && lane == leader) b = atomicAdd(&L.hist[key[k]], run_length(heads));
     b = __shfl_sync(kFull, b, leader);
     if (key[k] >= 0) {
-      const int pos = b + __popc(peers & lanemask_lt());
+      const int pos = b + (lane - leader);
       L.col_buf[pos] = col[k];
-      if (VAL) L.val_buf[pos] = val[k];
+      // values are read here, once, straight into their permuted slot
+      if (VAL) L.val_buf[pos] = a.in_val[a.base + S + k * T + threadIdx.x];
     }
   }
   __syncthreads();
@@ -200,7 +198,7 @@ void launch_split(const SplitArgs& a, cudaStream_t s) {
   if (a.total <= 0) return;
   const bool val = a.in_val != nullptr && SPLIT;
   switch (a.E / kMsThreads) {
-    case 16: val ? launch_split_t<true, 16, SPLIT>(a, s) : launch_split_t<false, 16, SPLIT>(a, s); break;
+    case 8: val ? launch_split_t<true, 8, SPLIT>(a, s) : launch_split_t<false, 8, SPLIT>(a, s); break;
     case 4: val ? launch_split_t<true, 4, SPLIT>(a, s) : launch_split_t<false, 4, SPLIT>(a, s); break;
     default: val ? launch_split_t<true, 1, SPLIT>(a, s) : launch_split_t<false, 1, SPLIT>(a, s); break;
   }
@@ -216,11 +214,11 @@ void launch_wg_row(const int64_t* rp, int64_t n_rows, int64_t E, int32_t* wg_fir
 void launch_histogram(const SplitArgs& a, cudaStream_t s) { launch_split<false>(a, s); }
 void launch_multisplit(const SplitArgs& a, cudaStream_t s) { launch_split<true>(a, s); }
 
-// Largest work-group size E (512 threads x {16, 4, 1} elements) whose shared
+// Largest work-group size E (512 threads x {8, 4, 1} elements) whose shared
 // arrays fit `smem_max` bytes for v chunks, given that every input row holds more
 // than tau elements; 0 when none fits. *ngr_out receives n_group_rows.
 int64_t multisplit_pick_E(int v, int64_t tau, bool with_val, int64_t smem_max, int* ngr_out) {
-  for (int items : {16, 4, 1}) {
+  for (int items : {8, 4, 1}) {
     const int64_t E = static_cast<int64_t>(kMsThreads) * items;
     const int64_t ngr = (E - 1 + tau) / (tau + 1) + 1;
     if (ngr > (1 << 20)) continue;

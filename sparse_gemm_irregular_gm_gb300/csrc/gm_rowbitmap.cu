@@ -1,0 +1,253 @@
+// gm_rowbitmap.cu -- whole-row shared-memory bitmaps (gMAGNUS Sec. III-E: any
+// local-memory accumulator may serve; here the dense accumulator keeps one bit
+// per column of C, so a row of up to 8 * s_LM columns fits one block).
+//
+// * Symbolic: a row's products set bits; the nnz of any column range (a level-0
+//   chunk of width w, or the whole row) is a popcount over the range. Used for
+//   the heavy rows when the hierarchy has at most one level, so the symbolic pass
+//   needs neither the outer product nor the multisplit.
+// * Numeric (light rows): prefix sums over groups of 8 bitmap words give every
+//   column its rank, i.e. its slot in the sorted row; products are summed into
+//   that slot and the row is written in column order with no sort.
+//
+// Rows are taken from a global work counter (dynamic scheduling; no waiting).
+#include <algorithm>
+
+#include "gm_device.cuh"
+#include "gm_internal.h"
+
+namespace gm {
+
+namespace {
+
+constexpr int kRbThreads = 1024;
+
+__device__ __forceinline__ void zero_words(uint32_t* bm, int nwords) {
+  uint4* b4 = reinterpret_cast<uint4*>(bm);
+  const int n4 = nwords >> 2;
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) b4[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = (n4 << 2) + threadIdx.x; i < nwords; i += blockDim.x) bm[i] = 0u;
+}
+
+// Warp-cooperative walk over the products of row r: 32 A entries at a time, their
+// B-row lengths prefix-summed across the warp, lanes stepping through the
+// flattened products with 4 independent loads in flight per lane. Calls
+// f(q, av): q[u] the position in B of product u (-1 past the end), av[u] the
+// value of its A entry (when WITH_A).
+template <bool WITH_A, class F>
+__device__ __forceinline__ void walk_products(const RowBitmapArgs& a, int64_t r, F&& f) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int64_t lo = a.a_rp[r], hi = a.a_rp[r + 1];
+  for (int64_t p0 = lo + static_cast<int64_t>(warp) * 32; p0 < hi; p0 += static_cast<int64_t>(nwarps) * 32) {
+    const int64_t p = p0 + lane;
+    int64_t bs = 0;
+    int len = 0;
+    double aval = 0.0;
+    if (p < hi) {
+      const int k = a.a_col[p];
+      bs = a.b_rp[k];
+      len = static_cast<int>(a.b_rp[k + 1] - bs);
+      if (WITH_A) aval = a.a_val[p];
+    }
+    const int inc = warp_inclusive_scan(len);
+    const int excl = inc - len;
+    const int total = __shfl_sync(kFull, inc, 31);
+    for (int base = 0; base < total; base += 128) {
+      int64_t q[4];
+      double av[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int pos = base + u * 32 + lane;
+        int j = 0;  // largest lane j with excl_j <= pos
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+          const int e = __shfl_sync(kFull, excl, j + d);
+          if (e <= pos) j += d;
+        }
+        const int64_t bj = __shfl_sync(kFull, bs, j);
+        const int ej = __shfl_sync(kFull, excl, j);
+        av[u] = WITH_A ? __shfl_sync(kFull, aval, j) : 0.0;
+        q[u] = pos < total ? bj + (pos - ej) : -1;
+      }
+      f(q, av);
+    }
+  }
+}
+
+// Sets the bit of every product column of row r.
+__device__ __forceinline__ void mark_row(const RowBitmapArgs& a, int64_t r, uint32_t* bm) {
+  walk_products<false>(a, r, [&](const int64_t (&q)[4], const double (&)[4]) {
+    uint32_t c[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) c[u] = q[u] >= 0 ? static_cast<uint32_t>(a.b_col[q[u]]) : 0u;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (q[u] >= 0) atomicOr(&bm[c[u] >> 5], 1u << (c[u] & 31));
+  });
+}
+
+// Number of set bits in [lo, hi).
+__device__ __forceinline__ int count_range(const uint32_t* bm, int64_t lo, int64_t hi) {
+  int n = 0;
+  while (lo < hi) {
+    const int64_t w = lo >> 5;
+    const int b0 = static_cast<int>(lo & 31);
+    const int64_t wend = (w + 1) << 5;
+    const int b1 = hi < wend ? static_cast<int>(hi & 31) : 32;
+    uint32_t m = bm[w] >> b0;
+    if (b1 - b0 < 32) m &= (1u << (b1 - b0)) - 1u;
+    n += __popc(m);
+    lo = (w << 5) + b1;
+  }
+  return n;
+}
+
+__global__ void __launch_bounds__(kRbThreads) k_rowbm_symbolic(RowBitmapArgs a, int nwords) {
+  extern __shared__ __align__(16) uint32_t bm[];
+  __shared__ int64_t s_item;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int64_t nbits = static_cast<int64_t>(nwords) * 32;
+  while (true) {
+    if (threadIdx.x == 0) s_item = atomicAdd(a.work_counter, 1u);
+    __syncthreads();
+    const int64_t item = s_item;
+    if (item >= a.n_items) break;
+    const int64_t r = a.rows[item];
+    zero_words(bm, nwords);
+    __syncthreads();
+    mark_row(a, r, bm);
+    __syncthreads();
+    if (a.v == 1 && a.width >= nbits) {  // whole row
+      int n = 0;
+      for (int w = threadIdx.x; w < nwords; w += blockDim.x) n += __popc(bm[w]);
+      n = warp_reduce_sum(n);
+      __shared__ int part[32];
+      if (lane == 0) part[warp] = n;
+      __syncthreads();
+      if (warp == 0) {
+        int t = lane < nwarps ? part[lane] : 0;
+        t = warp_reduce_sum(t);
+        if (lane == 0) {
+          if (a.nnz_out) a.nnz_out[a.item_base + item] = t;
+          else a.c_rp[r] = t;
+        }
+      }
+    } else {  // one warp per chunk of width w
+      for (int c = warp; c < a.v; c += nwarps) {
+        const int64_t lo = static_cast<int64_t>(c) * a.width;
+        const int64_t hi = min(lo + a.width, nbits);
+        const int64_t span = (hi - lo + 31) / 32;
+        int n = 0;
+        for (int64_t j = lane; j < span; j += 32) n += count_range(bm, lo + j * 32, min(hi, lo + j * 32 + 32));
+        n = warp_reduce_sum(n);
+        if (lane == 0) a.nnz_out[(a.item_base + item) * a.v + c] = n;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+constexpr int kGroupWords = 8;  // rank prefix kept per 8 bitmap words (256 columns)
+
+__global__ void __launch_bounds__(kRbThreads) k_rowbm_numeric(RowBitmapArgs a, int nwords, int cap) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  double* vals = reinterpret_cast<double*>(smem);                         // cap (rounded to even)
+  uint32_t* bm = reinterpret_cast<uint32_t*>(vals + ((cap + 1) & ~1));    // ngroups * 8 words
+  const int ngroups = (nwords + kGroupWords - 1) / kGroupWords;
+  int* gpre = reinterpret_cast<int*>(bm + ngroups * kGroupWords);         // ngroups
+  __shared__ int64_t s_item;
+  __shared__ int ws[33];
+  const int per = (ngroups + blockDim.x - 1) / blockDim.x;
+  const int g0 = threadIdx.x * per, g1 = min(ngroups, g0 + per);
+  while (true) {
+    if (threadIdx.x == 0) s_item = atomicAdd(a.work_counter, 1u);
+    __syncthreads();
+    const int64_t item = s_item;
+    if (item >= a.n_items) break;
+    const int64_t r = a.rows[item];
+    zero_words(bm, ngroups * kGroupWords);
+    __syncthreads();
+    mark_row(a, r, bm);
+    __syncthreads();
+    int acc = 0;
+    for (int g = g0; g < g1; ++g)
+      for (int w = 0; w < kGroupWords; ++w) acc += __popc(bm[g * kGroupWords + w]);
+    int nnz;
+    int run = block_exclusive_scan(acc, ws, &nnz);
+    for (int g = g0; g < g1; ++g) {
+      gpre[g] = run;
+      for (int w = 0; w < kGroupWords; ++w) run += __popc(bm[g * kGroupWords + w]);
+    }
+    const bool fits = nnz <= cap;
+    if (!fits && threadIdx.x == 0) atomicOr(a.status, kStInternal);
+    for (int i = threadIdx.x; i < min(nnz, cap); i += blockDim.x) vals[i] = 0.0;
+    __syncthreads();
+    if (fits) {
+      walk_products<true>(a, r, [&](const int64_t (&q)[4], const double (&av)[4]) {
+        uint32_t c[4];
+        double bv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          c[u] = q[u] >= 0 ? static_cast<uint32_t>(a.b_col[q[u]]) : 0u;
+          bv[u] = q[u] >= 0 ? a.b_val[q[u]] : 0.0;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (q[u] >= 0) {
+            const uint32_t cc = c[u];
+            const int w = cc >> 5, g = w / kGroupWords;
+            int rank = gpre[g] + __popc(bm[w] & ((1u << (cc & 31)) - 1u));
+            for (int x = g * kGroupWords; x < w; ++x) rank += __popc(bm[x]);
+            atomicAdd(&vals[rank], av[u] * bv[u]);
+          }
+        }
+      });
+    }
+    __syncthreads();
+    if (fits) {
+      const int64_t out = a.c_rp[r];
+      for (int g = g0; g < g1; ++g) {
+        int pos = gpre[g];
+        for (int w = 0; w < kGroupWords; ++w) {
+          uint32_t bits = bm[g * kGroupWords + w];
+          while (bits) {
+            const int b = __ffs(bits) - 1;
+            bits &= bits - 1;
+            a.c_col[out + pos] = (g * kGroupWords + w) * 32 + b;
+            a.c_val[out + pos] = vals[pos];
+            ++pos;
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+int64_t rowbm_symbolic_smem(int64_t c_m) { return ((c_m + 127) / 128) * 16; }
+
+int64_t rowbm_numeric_smem(int64_t c_m, int cap) {
+  const int64_t nwords = (c_m + 31) / 32;
+  const int64_t ngroups = (nwords + kGroupWords - 1) / kGroupWords;
+  return static_cast<int64_t>((cap + 1) & ~1) * 8 + ngroups * kGroupWords * 4 + ngroups * 4;
+}
+
+void launch_rowbm(const RowBitmapArgs& a, bool symbolic, int cap, int num_sms, int64_t smem_max, cudaStream_t s) {
+  if (a.n_items <= 0) return;
+  cudaMemsetAsync(a.work_counter, 0, sizeof(unsigned int), s);
+  const int64_t nwords4 = ((a.c_m + 127) / 128) * 4;  // whole uint4 stores
+  const size_t smem = static_cast<size_t>(symbolic ? rowbm_symbolic_smem(a.c_m) : rowbm_numeric_smem(a.c_m, cap));
+  const int per_sm = std::max<int>(1, static_cast<int>(smem_max / static_cast<int64_t>(smem + 1024)));
+  const int64_t blocks = std::min<int64_t>(a.n_items, static_cast<int64_t>(num_sms) * std::min(per_sm, 2));
+  if (symbolic) {
+    cudaFuncSetAttribute(k_rowbm_symbolic, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    (k_rowbm_symbolic<<<static_cast<unsigned>(blocks), kRbThreads, smem, s>>>(a, static_cast<int>(nwords4)), note_launch());
+  } else {
+    cudaFuncSetAttribute(k_rowbm_numeric, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    (k_rowbm_numeric<<<static_cast<unsigned>(blocks), kRbThreads, smem, s>>>(a, static_cast<int>((a.c_m + 31) / 32), cap), note_launch());
+  }
+}
+
+}  // namespace gm

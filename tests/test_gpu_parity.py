@@ -39,6 +39,8 @@ FORCED = [
     ("heavy_L3", {"tau": 16, "dense_width": 16, "n_chunks_max": 4}),    # three levels
     ("unfused", {"tau": 16, "dense_width": 64, "n_chunks_max": 4, "pipeline": binding.GM_PIPE_UNFUSED}),
     ("batched", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "workspace_cap_bytes": 70 << 20}),
+    ("L1_unfused", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_UNFUSED}),
+    ("L1_wide_chunks", {"tau": 64, "dense_width": 512}),                   # one level, 2 chunks of 512
 ]
 
 
@@ -63,6 +65,19 @@ def test_random_irregular(seed, shape, cfg):
     B = gi.random_csr(k, n, 0.3, seed + 50, values="int", unsorted=True, duplicates=True, explicit_zeros=True,
                       empty_rows=0.2)
     check_full(A, B, exact=True, **cfg)
+
+
+@pytest.mark.parametrize("scale", [11, 12])
+def test_symbolic_paths_agree(scale):
+    """Whole-row bitmap symbolic (default) and the C-hat_reord symbolic give the same C."""
+    A = gi.rmat(scale, 16, seed=scale)
+    cfg = {"tau": 256, "dense_width": 256, "n_chunks_max": 16}
+    r1 = run_gpu(A, A, **cfg)
+    r2 = run_gpu(A, A, pipeline=binding.GM_PIPE_UNFUSED, **cfg)
+    np.testing.assert_array_equal(r1[0], r2[0])
+    np.testing.assert_array_equal(r1[1], r2[1])
+    ref = oracle.spgemm(A, A)
+    assert_matches(ref, *r1)
 
 
 def test_empty_and_degenerate():
