@@ -342,6 +342,7 @@ def run_e2e(args, A, cfg, stream, nnz_c, ip_total):
     o_val = torch.empty(nnz_c, dtype=torch.float64, pin_memory=True)
     log(f"e2e: pinned {d2h / 1e9:.1f} GB of host memory in {time.perf_counter() - t0:.1f} s")
 
+    torch.cuda.empty_cache()  # let this leg's own allocation sizes form the cache
     d_rp = torch.empty_like(h_rp, device="cuda")
     d_col = torch.empty_like(h_col, device="cuda")
     d_val = torch.empty_like(h_val, device="cuda")

@@ -29,54 +29,43 @@ __device__ __forceinline__ void zero_words(uint32_t* bm, int nwords) {
   for (int i = (n4 << 2) + threadIdx.x; i < nwords; i += blockDim.x) bm[i] = 0u;
 }
 
-// Warp-cooperative walk over the products of row r: 32 A entries at a time, their
-// B-row lengths prefix-summed across the warp, lanes stepping through the
-// flattened products with 4 independent loads in flight per lane. Calls
-// f(q, av): q[u] the position in B of product u (-1 past the end), av[u] the
-// value of its A entry (when WITH_A).
+// Walk over the products of row r. Warp w takes the A entries w, w + nwarps, ...
+// (every warp busy even on rows with few entries); their metadata is loaded 32
+// entries at a time, then the lanes run along each entry's B row with 4
+// independent loads in flight. Calls f(q, av): q[u] the position in B of product
+// u (-1 when past the row's end), av the A entry's value (when WITH_A).
 template <bool WITH_A, class F>
 __device__ __forceinline__ void walk_products(const RowBitmapArgs& a, int64_t r, F&& f) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int64_t lo = a.a_rp[r], hi = a.a_rp[r + 1];
-  for (int64_t p0 = lo + static_cast<int64_t>(warp) * 32; p0 < hi; p0 += static_cast<int64_t>(nwarps) * 32) {
-    const int64_t p = p0 + lane;
-    int64_t bs = 0;
-    int len = 0;
+  for (int64_t g = lo + warp; g < hi; g += static_cast<int64_t>(nwarps) * 32) {
+    const int64_t p = g + static_cast<int64_t>(lane) * nwarps;
+    int64_t bs = 0, be = 0;
     double aval = 0.0;
     if (p < hi) {
       const int k = a.a_col[p];
       bs = a.b_rp[k];
-      len = static_cast<int>(a.b_rp[k + 1] - bs);
+      be = a.b_rp[k + 1];
       if (WITH_A) aval = a.a_val[p];
     }
-    const int inc = warp_inclusive_scan(len);
-    const int excl = inc - len;
-    const int total = __shfl_sync(kFull, inc, 31);
-    for (int base = 0; base < total; base += 128) {
-      int64_t q[4];
-      double av[4];
+    const unsigned live = __ballot_sync(kFull, be > bs);
+    for (unsigned m = live; m; m &= m - 1) {
+      const int j = __ffs(m) - 1;
+      const int64_t s0 = __shfl_sync(kFull, bs, j), s1 = __shfl_sync(kFull, be, j);
+      const double av = WITH_A ? __shfl_sync(kFull, aval, j) : 0.0;
+      for (int64_t q0 = s0 + lane; q0 < s1; q0 += 128) {
+        int64_t q[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int pos = base + u * 32 + lane;
-        int j = 0;  // largest lane j with excl_j <= pos
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) {
-          const int e = __shfl_sync(kFull, excl, j + d);
-          if (e <= pos) j += d;
-        }
-        const int64_t bj = __shfl_sync(kFull, bs, j);
-        const int ej = __shfl_sync(kFull, excl, j);
-        av[u] = WITH_A ? __shfl_sync(kFull, aval, j) : 0.0;
-        q[u] = pos < total ? bj + (pos - ej) : -1;
+        for (int u = 0; u < 4; ++u) q[u] = q0 + u * 32 < s1 ? q0 + u * 32 : -1;
+        f(q, av);
       }
-      f(q, av);
     }
   }
 }
 
 // Sets the bit of every product column of row r.
 __device__ __forceinline__ void mark_row(const RowBitmapArgs& a, int64_t r, uint32_t* bm) {
-  walk_products<false>(a, r, [&](const int64_t (&q)[4], const double (&)[4]) {
+  walk_products<false>(a, r, [&](const int64_t (&q)[4], double) {
     uint32_t c[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) c[u] = q[u] >= 0 ? static_cast<uint32_t>(a.b_col[q[u]]) : 0u;
@@ -183,7 +172,7 @@ __global__ void __launch_bounds__(kRbThreads) k_rowbm_numeric(RowBitmapArgs a, i
     for (int i = threadIdx.x; i < min(nnz, cap); i += blockDim.x) vals[i] = 0.0;
     __syncthreads();
     if (fits) {
-      walk_products<true>(a, r, [&](const int64_t (&q)[4], const double (&av)[4]) {
+      walk_products<true>(a, r, [&](const int64_t (&q)[4], double av) {
         uint32_t c[4];
         double bv[4];
 #pragma unroll
@@ -198,7 +187,7 @@ __global__ void __launch_bounds__(kRbThreads) k_rowbm_numeric(RowBitmapArgs a, i
             const int w = cc >> 5, g = w / kGroupWords;
             int rank = gpre[g] + __popc(bm[w] & ((1u << (cc & 31)) - 1u));
             for (int x = g * kGroupWords; x < w; ++x) rank += __popc(bm[x]);
-            atomicAdd(&vals[rank], av[u] * bv[u]);
+            atomicAdd(&vals[rank], av * bv[u]);
           }
         }
       });
