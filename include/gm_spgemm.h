@@ -226,6 +226,26 @@ enum {
 gm_status gm_spgemm_debug_copy(const gm_plan* plan, int view, int level, void* dst, int64_t bytes,
                                int64_t* out_bytes);
 
+/* Exclusive prefix sum that allocates nothing: out[i] = in[0] + ... + in[i-1] for
+ * i < n, and *total = the sum of all n inputs when total is not NULL. This has no
+ * counterpart in the gMAGNUS paper; it is the scan that places C.rowPtr, offered
+ * to callers that cannot allocate device memory while they run (work being
+ * captured into a CUDA graph, host callbacks or real-time loops that must not
+ * block on an allocator, hosts whose framework owns all device memory).
+ * in, out: device int64[n] (may be the same array); total: device int64 or NULL;
+ * stream: a cudaStream_t (NULL = legacy default stream). The work is queued on
+ * the stream; the call does not wait for it.
+ * Scratch: a fixed array inside the library, 65,600 int64 (about 525 KB) on every
+ * device that loads the library, held until the process exits. Largest n:
+ * 134,217,728 (2^27); larger n returns GM_ERR_WORKSPACE and queues nothing.
+ * The first call on a device looks the array's device address up (make that
+ * first call before any stream capture). Every call shares the array: calls whose
+ * work overlaps on the GPU race, so serialise them. Nothing needs clearing
+ * between calls.
+ * Errors: GM_ERR_INVALID_ARG (n < 0, or NULL in/out with n > 0), GM_ERR_WORKSPACE
+ * (n too large), GM_ERR_CUDA (the device lookup or a launch failed). */
+gm_status gm_prefix_sum_noalloc(const int64_t* in, int64_t* out, int64_t n, int64_t* total, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,8 @@ STAGES = ["analyze", "transpose", "outer", "histogram", "multisplit", "sym_heavy
           "num_heavy", "num_light", "other", "transpose_sym", "outer_sym", "histogram_sym", "multisplit_sym",
           "unused"]
 EXPORTS = ["gm_set_allocator", "gm_spgemm_params", "gm_spgemm_analyze", "gm_spgemm_symbolic", "gm_spgemm_numeric",
-           "gm_spgemm_plan_info", "gm_spgemm_plan_destroy", "gm_status_string", "gm_spgemm_debug_copy"]
+           "gm_spgemm_plan_info", "gm_spgemm_plan_destroy", "gm_status_string", "gm_spgemm_debug_copy",
+           "gm_prefix_sum_noalloc"]
 
 
 class gm_csr(ctypes.Structure):
@@ -95,6 +96,9 @@ def load(path: str = LIB_PATH):
     lib.gm_spgemm_debug_copy.restype = ctypes.c_int
     lib.gm_spgemm_debug_copy.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                          ctypes.c_int64, P(ctypes.c_int64)]
+    lib.gm_prefix_sum_noalloc.restype = ctypes.c_int
+    lib.gm_prefix_sum_noalloc.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                          ctypes.c_void_p]
     _lib = lib
     use_torch_allocator(True)
     return lib
@@ -252,6 +256,14 @@ def gm_spgemm_debug_copy(plan, view: int, level: int = 0):
         _check(load().gm_spgemm_debug_copy(plan, view, level, out.ctypes.data, size.value, None),
                "gm_spgemm_debug_copy")
     return out
+
+
+def gm_prefix_sum_noalloc(inp, out, total=None, stream=None):
+    """Exclusive scan of an int64 CUDA tensor into ``out`` using the library's fixed scratch."""
+    _check(load().gm_prefix_sum_noalloc(inp.data_ptr() if inp.numel() else None,
+                                        out.data_ptr() if out.numel() else None, inp.numel(),
+                                        total.data_ptr() if total is not None else None,
+                                        _stream_handle(stream)), "gm_prefix_sum_noalloc")
 
 
 def spgemm(A: DeviceCSR, B: DeviceCSR, cfg: gm_config | None = None, stream=None, return_info: bool = False):

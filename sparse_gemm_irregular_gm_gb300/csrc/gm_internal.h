@@ -77,6 +77,11 @@ struct DevBuf {
 // out[i] = sum_{j<i} in[j] for i in [0, n); in == out allowed. When d_total is
 // not null it receives sum of all n inputs. Returns false on allocation failure.
 bool scan_exclusive_i64(const int64_t* in, int64_t* out, int64_t n, int64_t* d_total, cudaStream_t s);
+// The same scan with caller-provided scratch (scratch_elems int64 entries; needs
+// scan_scratch_elems(n)). Returns false when the scratch is too small.
+int64_t scan_scratch_elems(int64_t n);
+bool scan_exclusive_i64_scratch(const int64_t* in, int64_t* out, int64_t n, int64_t* d_total, int64_t* scratch,
+                                int64_t scratch_elems, cudaStream_t s);
 // Fixed-size segments: for each parent p, the v children p*v .. p*v+v-1 get
 // off[p*v+c] = base[p] + sum_{c'<c} val[p*v+c'] (in place: val may equal off).
 // Returns the per-parent sums in sums (nullable).

@@ -107,6 +107,34 @@ bool scan_exclusive_i64(const int64_t* in, int64_t* out, int64_t n, int64_t* d_t
   return true;
 }
 
+int64_t scan_scratch_elems(int64_t n) {
+  int64_t need = 0;
+  while (n > kScanTile) {
+    n = (n + kScanTile - 1) / kScanTile;
+    need += n;
+  }
+  return need;
+}
+
+bool scan_exclusive_i64_scratch(const int64_t* in, int64_t* out, int64_t n, int64_t* d_total, int64_t* scratch,
+                                int64_t scratch_elems, cudaStream_t s) {
+  if (n <= 0) {
+    if (d_total) cudaMemsetAsync(d_total, 0, sizeof(int64_t), s);
+    return true;
+  }
+  const int64_t tiles = (n + kScanTile - 1) / kScanTile;
+  if (tiles == 1) {
+    (k_tile_scan<<<1, kScanThreads, 0, s>>>(in, n, out, nullptr, d_total), note_launch());
+    return true;
+  }
+  if (scratch_elems < tiles) return false;
+  (k_tile_sums<<<static_cast<unsigned>(tiles), kScanThreads, 0, s>>>(in, n, scratch), note_launch());
+  if (!scan_exclusive_i64_scratch(scratch, scratch, tiles, nullptr, scratch + tiles, scratch_elems - tiles, s))
+    return false;
+  (k_tile_scan<<<static_cast<unsigned>(tiles), kScanThreads, 0, s>>>(in, n, out, scratch, d_total), note_launch());
+  return true;
+}
+
 void segmented_offsets(const int64_t* val, int64_t* off, const int64_t* base, int64_t n_parents, int v,
                        int64_t* sums, cudaStream_t s) {
   if (n_parents <= 0) return;
