@@ -878,7 +878,7 @@ static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, double* c_val
     const int64_t cnt = p->bin_start[b + 1] - p->bin_start[b];
     if (cnt <= 0) continue;
     const int cap = b <= 9 ? static_cast<int>(light_bin_ub(b)) : static_cast<int>(p->P.tau);
-    if (numeric && b >= 7 && rowbm_numeric_smem(p->c_m, cap) + 1024 <= p->smem_dev) {
+    if (numeric && b >= 7 && rowbm_numeric_smem(p->c_m, cap) + 4096 <= p->smem_dev) {
       RowBitmapArgs ra{};
       ra.rows = p->rows_by_bin.p + p->bin_start[b];
       ra.n_items = cnt;
@@ -1092,7 +1092,7 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
   if (st != GM_OK) return st;
   p->L = static_cast<int>(p->P.n_levels);
   p->sym_rowbm = p->L <= 1 && p->pipeline != GM_PIPE_UNFUSED && !p->keep &&
-                 gm::rowbm_symbolic_smem(p->c_m) + 1024 <= p->smem_dev;
+                 gm::rowbm_symbolic_smem(p->c_m) + 4096 <= p->smem_dev;
   gm::g_ws_peak = gm::g_ws_now.load();
   const int64_t l0 = gm::launch_count();
   st = gm::analyze_impl(p.get());

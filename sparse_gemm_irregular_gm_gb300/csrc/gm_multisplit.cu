@@ -74,7 +74,7 @@ __device__ __forceinline__ void setup_rows(const SplitArgs& a, const Layout& L, 
 }
 
 template <bool VAL, int ITEMS, bool SPLIT>
-__global__ void __launch_bounds__(kMsThreads) k_split(SplitArgs a) {
+__global__ void __launch_bounds__(kMsThreads, 3) k_split(SplitArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int T = blockDim.x;
   const int E = T * ITEMS;
@@ -145,8 +145,10 @@ __global__ void __launch_bounds__(kMsThreads) k_split(SplitArgs a) {
   for (int k = threadIdx.x; k < nk; k += T) L.hist[k] = L.loff[k];  // running local cursor
   __syncthreads();
 
-  // Permute in shared memory.
+  // Permute in shared memory: slots first, then the values read once (all loads
+  // of a thread in flight together) straight into their permuted slots.
   const int lane = threadIdx.x & 31;
+  int pos[ITEMS];
 #pragma unroll
   for (int k = 0; k < ITEMS; ++k) {
     const unsigned heads = run_heads(key[k]);
@@ -154,12 +156,16 @@ __global__ void __launch_bounds__(kMsThreads) k_split(SplitArgs a) {
     int b = 0;
     if (key[k] >= 0 && lane == leader) b = atomicAdd(&L.hist[key[k]], run_length(heads));
     b = __shfl_sync(kFull, b, leader);
-    if (key[k] >= 0) {
-      const int pos = b + (lane - leader);
-      L.col_buf[pos] = col[k];
-      // values are read here, once, straight into their permuted slot
-      if (VAL) L.val_buf[pos] = a.in_val[a.base + S + k * T + threadIdx.x];
-    }
+    pos[k] = b + (lane - leader);
+    if (key[k] >= 0) L.col_buf[pos[k]] = col[k];
+  }
+  if (VAL) {
+    double v[ITEMS];
+#pragma unroll
+    for (int k = 0; k < ITEMS; ++k) v[k] = key[k] >= 0 ? a.in_val[a.base + S + k * T + threadIdx.x] : 0.0;
+#pragma unroll
+    for (int k = 0; k < ITEMS; ++k)
+      if (key[k] >= 0) L.val_buf[pos[k]] = v[k];
   }
   __syncthreads();
 

@@ -34,10 +34,21 @@ __device__ __forceinline__ void zero_words(uint32_t* bm, int nwords) {
 // entries at a time, then the lanes run along each entry's B row with 4
 // independent loads in flight. Calls f(q, av): q[u] the position in B of product
 // u (-1 when past the row's end), av the A entry's value (when WITH_A).
+constexpr int kLongRow = 4096;   // B rows longer than this are walked by the whole block
+constexpr int kMaxLong = 64;     // deferred long rows kept per pass (more are walked by their warp)
+
+struct LongRows {
+  int n;
+  int64_t s0[kMaxLong], s1[kMaxLong];
+  double av[kMaxLong];
+};
+
 template <bool WITH_A, class F>
-__device__ __forceinline__ void walk_products(const RowBitmapArgs& a, int64_t r, F&& f) {
+__device__ __forceinline__ void walk_products(const RowBitmapArgs& a, int64_t r, LongRows& longs, F&& f) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int64_t lo = a.a_rp[r], hi = a.a_rp[r + 1];
+  if (threadIdx.x == 0) longs.n = 0;
+  __syncthreads();
   for (int64_t g = lo + warp; g < hi; g += static_cast<int64_t>(nwarps) * 32) {
     const int64_t p = g + static_cast<int64_t>(lane) * nwarps;
     int64_t bs = 0, be = 0;
@@ -47,6 +58,16 @@ __device__ __forceinline__ void walk_products(const RowBitmapArgs& a, int64_t r,
       bs = a.b_rp[k];
       be = a.b_rp[k + 1];
       if (WITH_A) aval = a.a_val[p];
+    }
+    // long rows go to the shared list when there is room
+    if (be - bs > kLongRow) {
+      const int slot = atomicAdd(&longs.n, 1);
+      if (slot < kMaxLong) {
+        longs.s0[slot] = bs;
+        longs.s1[slot] = be;
+        longs.av[slot] = aval;
+        be = bs;
+      }
     }
     const unsigned live = __ballot_sync(kFull, be > bs);
     for (unsigned m = live; m; m &= m - 1) {
@@ -61,11 +82,23 @@ __device__ __forceinline__ void walk_products(const RowBitmapArgs& a, int64_t r,
       }
     }
   }
+  __syncthreads();
+  const int nl = min(longs.n, kMaxLong);
+  for (int i = 0; i < nl; ++i) {  // block-wide, no barrier needed between rows
+    const int64_t s0 = longs.s0[i], s1 = longs.s1[i];
+    const int T = blockDim.x;
+    for (int64_t q0 = s0 + threadIdx.x; q0 < s1; q0 += 4 * T) {
+      int64_t q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) q[u] = q0 + u * T < s1 ? q0 + u * T : -1;
+      f(q, longs.av[i]);
+    }
+  }
 }
 
 // Sets the bit of every product column of row r.
-__device__ __forceinline__ void mark_row(const RowBitmapArgs& a, int64_t r, uint32_t* bm) {
-  walk_products<false>(a, r, [&](const int64_t (&q)[4], double) {
+__device__ __forceinline__ void mark_row(const RowBitmapArgs& a, int64_t r, uint32_t* bm, LongRows& longs) {
+  walk_products<false>(a, r, longs, [&](const int64_t (&q)[4], double) {
     uint32_t c[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) c[u] = q[u] >= 0 ? static_cast<uint32_t>(a.b_col[q[u]]) : 0u;
@@ -94,6 +127,7 @@ __device__ __forceinline__ int count_range(const uint32_t* bm, int64_t lo, int64
 __global__ void __launch_bounds__(kRbThreads) k_rowbm_symbolic(RowBitmapArgs a, int nwords) {
   extern __shared__ __align__(16) uint32_t bm[];
   __shared__ int64_t s_item;
+  __shared__ LongRows longs;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int64_t nbits = static_cast<int64_t>(nwords) * 32;
   while (true) {
@@ -104,7 +138,7 @@ __global__ void __launch_bounds__(kRbThreads) k_rowbm_symbolic(RowBitmapArgs a, 
     const int64_t r = a.rows[item];
     zero_words(bm, nwords);
     __syncthreads();
-    mark_row(a, r, bm);
+    mark_row(a, r, bm, longs);
     __syncthreads();
     if (a.v == 1 && a.width >= nbits) {  // whole row
       int n = 0;
@@ -146,6 +180,7 @@ __global__ void __launch_bounds__(kRbThreads) k_rowbm_numeric(RowBitmapArgs a, i
   int* gpre = reinterpret_cast<int*>(bm + ngroups * kGroupWords);         // ngroups
   __shared__ int64_t s_item;
   __shared__ int ws[33];
+  __shared__ LongRows longs;
   const int per = (ngroups + blockDim.x - 1) / blockDim.x;
   const int g0 = threadIdx.x * per, g1 = min(ngroups, g0 + per);
   while (true) {
@@ -156,7 +191,7 @@ __global__ void __launch_bounds__(kRbThreads) k_rowbm_numeric(RowBitmapArgs a, i
     const int64_t r = a.rows[item];
     zero_words(bm, ngroups * kGroupWords);
     __syncthreads();
-    mark_row(a, r, bm);
+    mark_row(a, r, bm, longs);
     __syncthreads();
     int acc = 0;
     for (int g = g0; g < g1; ++g)
@@ -172,7 +207,7 @@ __global__ void __launch_bounds__(kRbThreads) k_rowbm_numeric(RowBitmapArgs a, i
     for (int i = threadIdx.x; i < min(nnz, cap); i += blockDim.x) vals[i] = 0.0;
     __syncthreads();
     if (fits) {
-      walk_products<true>(a, r, [&](const int64_t (&q)[4], double av) {
+      walk_products<true>(a, r, longs, [&](const int64_t (&q)[4], double av) {
         uint32_t c[4];
         double bv[4];
 #pragma unroll
@@ -193,19 +228,20 @@ __global__ void __launch_bounds__(kRbThreads) k_rowbm_numeric(RowBitmapArgs a, i
       });
     }
     __syncthreads();
-    if (fits) {
+    if (fits) {  // words round-robin over threads: balanced emission, adjacent output ranges per warp
       const int64_t out = a.c_rp[r];
-      for (int g = g0; g < g1; ++g) {
+      for (int w = threadIdx.x; w < nwords; w += blockDim.x) {
+        uint32_t bits = bm[w];
+        if (!bits) continue;
+        const int g = w / kGroupWords;
         int pos = gpre[g];
-        for (int w = 0; w < kGroupWords; ++w) {
-          uint32_t bits = bm[g * kGroupWords + w];
-          while (bits) {
-            const int b = __ffs(bits) - 1;
-            bits &= bits - 1;
-            a.c_col[out + pos] = (g * kGroupWords + w) * 32 + b;
-            a.c_val[out + pos] = vals[pos];
-            ++pos;
-          }
+        for (int x = g * kGroupWords; x < w; ++x) pos += __popc(bm[x]);
+        while (bits) {
+          const int b = __ffs(bits) - 1;
+          bits &= bits - 1;
+          a.c_col[out + pos] = w * 32 + b;
+          a.c_val[out + pos] = vals[pos];
+          ++pos;
         }
       }
     }
