@@ -243,10 +243,9 @@ __device__ __forceinline__ int64_t leaf_col_base(const ListArgs& a, int64_t chil
 template <bool SYM>
 __global__ void k_leaf_bitmap(ListArgs a, int nwords, int cap_vals) {
   extern __shared__ __align__(16) unsigned char smem[];
-  double* vals = reinterpret_cast<double*>(smem);
-  int32_t* cols = reinterpret_cast<int32_t*>(smem + (SYM ? 0 : static_cast<size_t>(cap_vals) * 8));
-  uint32_t* bm = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(cols) + (SYM ? 0 : static_cast<size_t>(cap_vals) * 4));
-  int* pre = reinterpret_cast<int*>(bm + nwords);
+  double* vals = reinterpret_cast<double*>(smem);                                                  // cap_vals
+  uint32_t* bm = reinterpret_cast<uint32_t*>(smem + (SYM ? 0 : static_cast<size_t>(cap_vals) * 8));  // nwords
+  int* pre = reinterpret_cast<int*>(bm + nwords);                                                    // nwords
   __shared__ int ws[33];
   const int T = blockDim.x;
   const int per = (nwords + T - 1) / T;
@@ -282,12 +281,7 @@ __global__ void k_leaf_bitmap(ListArgs a, int nwords, int cap_vals) {
     }
     for (int w = w0; w < w1; ++w) {
       pre[w] = run;
-      uint32_t bits = bm[w];
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1;
-        cols[run++] = w * 32 + b;
-      }
+      run += __popc(bm[w]);
     }
     for (int r = threadIdx.x; r < nnz; r += T) vals[r] = 0.0;
     __syncthreads();
@@ -309,11 +303,20 @@ __global__ void k_leaf_bitmap(ListArgs a, int nwords, int cap_vals) {
       }
     }
     __syncthreads();
+    // columns come back from the bitmap: words round-robin over threads, so the
+    // lanes of a warp write adjacent output ranges
     const int64_t out = a.off_in[a.child_base + child_local];
     const int64_t cb = leaf_col_base(a, child_local);
-    for (int r = threadIdx.x; r < nnz; r += T) {
-      a.c_col[out + r] = static_cast<int32_t>(cb + cols[r]);
-      a.c_val[out + r] = vals[r];
+    for (int w = threadIdx.x; w < nwords; w += T) {
+      uint32_t bits = bm[w];
+      int pos = pre[w];
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        a.c_col[out + pos] = static_cast<int32_t>(cb + w * 32 + b);
+        a.c_val[out + pos] = vals[pos];
+        ++pos;
+      }
     }
     __syncthreads();
   }
@@ -418,6 +421,66 @@ __global__ void __launch_bounds__(T) k_leaf_small(ListArgs a, int nwords) {
   }
 }
 
+// Tiny chunk (at most CAPW elements): one warp loads it into shared memory,
+// sorts (column, value) pairs with a bitonic network, merges equal columns and
+// writes the chunk in column order. No bitmap, no block barrier.
+template <int CAPW, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32) k_leaf_warp(ListArgs a) {
+  __shared__ int32_t s_key[WARPS][CAPW];
+  __shared__ double s_val[WARPS][CAPW];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int32_t* key = s_key[w];
+  double* val = s_val[w];
+  for (int64_t item = static_cast<int64_t>(blockIdx.x) * WARPS + w; item < a.n_items;
+       item += static_cast<int64_t>(gridDim.x) * WARPS) {
+    const int64_t m = a.items[item];
+    const int64_t lo = a.rp[m];
+    const int n = static_cast<int>(min(a.rp[m + 1] - lo, static_cast<int64_t>(CAPW)));
+    const int64_t child_local = a.child_of ? a.child_of[m] : m;
+    for (int i = lane; i < CAPW; i += 32) {
+      key[i] = i < n ? a.col[lo + i] : INT_MAX;
+      val[i] = i < n ? a.val[lo + i] : 0.0;
+    }
+    __syncwarp();
+    for (int k = 2; k <= CAPW; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = lane; i < CAPW; i += 32) {
+          const int ixj = i ^ j;
+          if (ixj > i) {
+            const int32_t ki = key[i], kj = key[ixj];
+            if ((ki > kj) == ((i & k) == 0)) {
+              key[i] = kj;
+              key[ixj] = ki;
+              const double t = val[i];
+              val[i] = val[ixj];
+              val[ixj] = t;
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
+    const int64_t out = a.off_in[a.child_base + child_local];
+    const int64_t cb = leaf_col_base(a, child_local);
+    int run = 0;
+    for (int i0 = 0; i0 < n; i0 += 32) {
+      const int i = i0 + lane;
+      const bool head = i < n && (i == 0 || key[i] != key[i - 1]);
+      const unsigned hb = __ballot_sync(kFull, head);
+      if (head) {
+        double sum = 0.0;
+        const int32_t c = key[i];
+        for (int t = i; t < n && key[t] == c; ++t) sum += val[t];
+        const int r = run + __popc(hb & lanemask_lt());
+        a.c_col[out + r] = static_cast<int32_t>(cb + c);
+        a.c_val[out + r] = sum;
+      }
+      run += __popc(hb);
+    }
+    __syncwarp();
+  }
+}
+
 // Light chunk of a level wider than the dense width: block hash accumulator.
 template <bool SYM, bool POW2>
 __global__ void k_leaf_hash(ListArgs a, int cap) {
@@ -509,7 +572,7 @@ void launch_light_rows(const LightArgs& a, int cap, bool symbolic, cudaStream_t 
 
 int leaf_bitmap_smem(int64_t width, int cap_vals, bool symbolic) {
   const int64_t nwords = (width + 31) / 32;
-  return static_cast<int>(nwords * 8 + (symbolic ? 0 : static_cast<int64_t>(cap_vals) * 12));
+  return static_cast<int>(nwords * 8 + (symbolic ? 0 : static_cast<int64_t>(cap_vals) * 8));
 }
 
 int leaf_small_smem(int64_t width, int cap, bool symbolic) {
@@ -534,11 +597,18 @@ void launch_leaf_small(const ListArgs& a, int max_elems, bool symbolic, cudaStre
   }
 }
 
+void launch_leaf_warp(const ListArgs& a, cudaStream_t s) {
+  if (a.n_items <= 0) return;
+  constexpr int W = 8;
+  const unsigned g = static_cast<unsigned>(std::min<int64_t>((a.n_items + W - 1) / W, 152LL * 64));
+  (k_leaf_warp<128, W><<<g, W * 32, 0, s>>>(a), note_launch());
+}
+
 void launch_leaf_bitmap(const ListArgs& a, int cap_vals, bool symbolic, cudaStream_t s) {
   if (a.n_items <= 0) return;
   const int nwords = static_cast<int>((a.width + 31) / 32);
   const size_t smem = static_cast<size_t>(leaf_bitmap_smem(a.width, cap_vals, symbolic));
-  const int T = symbolic ? 256 : (cap_vals <= 1024 ? 256 : cap_vals <= 4096 ? 512 : 1024);
+  const int T = symbolic ? 256 : (cap_vals <= 1024 ? 256 : cap_vals <= 8192 ? 512 : 1024);
   const unsigned g = item_grid(a.n_items, 4);
   auto fn = symbolic ? k_leaf_bitmap<true> : k_leaf_bitmap<false>;
   set_smem(fn, smem);

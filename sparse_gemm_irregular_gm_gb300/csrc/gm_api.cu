@@ -123,6 +123,28 @@ __global__ void k_i32_gather_to_i64(const int32_t* __restrict__ perm, int64_t n,
     out[i] = perm[i] + add;
 }
 
+// Size class of a last-level chunk for the numeric accumulators: 0 empty,
+// 1 (<= 128 elements, one warp sorts), 2 (<= 1024) and 3 (<= 4096) in registers,
+// 4 / 5 / 6 with a value array of 4096 / 8192 / width entries chosen by nnz.
+__global__ void k_leaf_class(const int64_t* __restrict__ mcount, const int64_t* __restrict__ nnz, int64_t n,
+                             int64_t nnz_base, uint8_t* __restrict__ cls) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int64_t c = mcount[i];
+    uint8_t k = 0;
+    if (c > 0) {
+      if (c <= 128) k = 1;
+      else if (c <= 1024) k = 2;
+      else if (c <= 4096) k = 3;
+      else {
+        const int64_t z = nnz[nnz_base + i];
+        k = z <= 4096 ? 4 : z <= 8192 ? 5 : 6;
+      }
+    }
+    cls[i] = k;
+  }
+}
+
 }  // namespace
 
 static void sub_to_u64(const int64_t* src, int64_t n, int64_t base, unsigned long long* dst, cudaStream_t s) {
@@ -298,6 +320,7 @@ struct gm_plan {
   gm::GrowBuf nnz[GM_MAX_LEVELS];        // per level, per child: nnz (symbolic) then output offset
   gm::GrowBuf heavy_list[GM_MAX_LEVELS]; // per level: global ids of heavy children (parents of the next level)
   gm::GrowBuf pbase[GM_MAX_LEVELS];      // per level >= 1: column base of each parent
+  gm::DevBuf<int64_t> leaf_nnz;          // nnz of each last-level chunk (kept for sizing numeric work)
   int64_t n_par[GM_MAX_LEVELS + 1] = {};
   int64_t c_nnz = -1;
   int64_t* c_rp = nullptr;
@@ -489,13 +512,20 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
                             bool numeric) {
   if (n <= 0) return GM_OK;
   const cudaStream_t s = p->s;
-  const BinSpec spec = dense ? bitmap_leaf_spec() : hash_leaf_spec();
+  // numeric last-level chunks with known nnz: classes sized by nnz (k_leaf_class)
+  const bool by_nnz = dense && numeric && p->leaf_nnz.p && la.child_of == nullptr;
+  BinSpec spec = dense ? bitmap_leaf_spec() : hash_leaf_spec();
+  if (by_nnz) spec.nbins = 7;
   DevBuf<uint8_t> bins;
   DevBuf<int32_t> idx;
   DevBuf<int64_t> starts_d, items;
   if (!bins.alloc(n, s) || !idx.alloc(n, s) || !starts_d.alloc(spec.nbins + 1, s) || !items.alloc(n, s))
     return GM_ERR_OOM;
-  launch_bin_sizes(mcount + lo, n, bins.p, spec, s);
+  if (by_nnz)
+    (k_leaf_class<<<grid_for(n, 256), 256, 0, s>>>(mcount + lo, p->leaf_nnz.p, n, la.child_base + lo, bins.p),
+     note_launch());
+  else
+    launch_bin_sizes(mcount + lo, n, bins.p, spec, s);
   if (!partition_by_bin(bins.p, n, spec.nbins, idx.p, starts_d.p, s)) return GM_ERR_OOM;
   int64_t starts[kMaxBins + 1];
   cudaMemcpyAsync(starts, starts_d.p, (spec.nbins + 1) * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
@@ -509,7 +539,11 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
     a.items = items.p + starts[b];
     a.n_items = cnt;
     p->n_leaves += numeric ? 0 : cnt;
-    if (dense && b <= 2) launch_leaf_small(a, b == 1 ? 1024 : 4096, !numeric, s);
+    if (by_nnz) {
+      if (b == 1) launch_leaf_warp(a, s);
+      else if (b <= 3) launch_leaf_small(a, b == 2 ? 1024 : 4096, false, s);
+      else launch_leaf_bitmap(a, static_cast<int>(std::min<int64_t>(b == 4 ? 4096 : b == 5 ? 8192 : la.width, la.width)), false, s);
+    } else if (dense && b <= 2) launch_leaf_small(a, b == 1 ? 1024 : 4096, !numeric, s);
     else if (dense) launch_leaf_bitmap(a, bitmap_leaf_cap(b, la.width), !numeric, s);
     else launch_leaf_hash(a, hash_leaf_cap(b, p->P.tau, p->smem_dev), !numeric, s);
   }
@@ -983,6 +1017,12 @@ static gm_status symbolic_impl(gm_plan* p, int64_t* C_rp, int64_t* C_nnz) {
     else launch_scatter_i64(p->nnz[0].p, p->rows_by_bin.p + p->bin_start[kHeavyBin], nh, C_rp, s);
   }
 heavy_done:
+  if (nh > 0) {  // nnz of the last level's chunks, before they turn into offsets
+    const int li = L >= 1 ? L - 1 : 0;
+    const int64_t cnt = L >= 1 ? p->n_par[li] * p->P.v_chunks[li] : nh;
+    if (cnt > 0 && p->leaf_nnz.alloc(cnt, s))
+      cudaMemcpyAsync(p->leaf_nnz.p, p->nnz[li].p, cnt * sizeof(int64_t), cudaMemcpyDeviceToDevice, s);
+  }
   t = p->stage_begin(GM_STAGE_SCAN);
   if (!scan_exclusive_i64(C_rp, C_rp, n + 1, nullptr, s)) return GM_ERR_OOM;
   cudaMemcpyAsync(&p->c_nnz, C_rp + n, sizeof(int64_t), cudaMemcpyDeviceToHost, s);

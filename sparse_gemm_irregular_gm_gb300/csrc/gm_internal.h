@@ -228,6 +228,8 @@ int leaf_bitmap_smem(int64_t width, int cap_vals, bool symbolic);
 // Chunks with at most max_elems (<= 4096) elements, held in registers; no
 // floating-point atomics.
 void launch_leaf_small(const ListArgs& a, int max_elems, bool symbolic, cudaStream_t s);
+// Numeric chunks of at most 128 elements: one warp sorts and merges each.
+void launch_leaf_warp(const ListArgs& a, cudaStream_t s);
 int leaf_small_smem(int64_t width, int cap, bool symbolic);
 
 // ---- whole-row bitmaps (gm_rowbitmap.cu) -----------------------------------------
