@@ -68,9 +68,11 @@ typedef struct gm_csr {
 #define GM_FLAG_LOG 4                /* print the plan to stderr (also env GM_SPGEMM_LOG=1) */
 
 /* Heavy-path pipelines for gm_config.pipeline. */
-#define GM_PIPE_AUTO 0
-#define GM_PIPE_UNFUSED 1 /* outer product -> C-hat -> histogram -> multisplit (Algorithm 3 as printed) */
+#define GM_PIPE_AUTO 0        /* GM_PIPE_ROWWISE when it applies, else GM_PIPE_FUSED_HISTO */
+#define GM_PIPE_UNFUSED 1     /* outer product -> C-hat -> histogram -> multisplit (Algorithm 3 as printed) */
 #define GM_PIPE_FUSED_HISTO 2 /* outer product counts the level-0 chunk histogram while it writes C-hat */
+#define GM_PIPE_ROWWISE 3     /* one level only: heavy rows expanded in row order straight into their
+                                 chunks (C-hat is not written); chunk sizes come from the symbolic pass */
 
 /* Tuning and test overrides; zero selects the automatic value for every field.
  * Overrides change how the work is split, never the result. A NULL config is

@@ -300,6 +300,7 @@ struct gm_plan {
   int num_sms = 1;
   int64_t c_m = 1;
   bool sym_rowbm = false;  // heavy symbolic through whole-row bitmaps
+  bool rowwise = false;    // numeric heavy path: row-order expansion fused with the multisplit
   gm_params P{};
   int L = 0;
   int state = 0;  // 1 analyzed, 2 symbolic done, 3 numeric done
@@ -315,6 +316,8 @@ struct gm_plan {
   int64_t n_heavy = 0, n_light = 0, n_empty = 0, ip_total = 0, ip_heavy = 0;
   gm::DevBuf<int64_t> chat_rp;      // C-hat.rowPtr over all heavy rows (n_heavy + 1)
   gm::DevBuf<int64_t> heavy_ids64;  // x_heavy as int64
+  gm::DevBuf<int64_t> anz;          // prefix of nnz(A[x_heavy[h], :]) (n_heavy + 1)
+  gm::DevBuf<int64_t> cnt0;         // row-order pipeline: elements of each level-0 chunk (n_heavy * v0)
   std::vector<int64_t> h_chat_rp;   // host copy of chat_rp
   std::vector<int64_t> h_anz;       // prefix of nnz(A[x_heavy[h], :])
   gm::GrowBuf nnz[GM_MAX_LEVELS];        // per level, per child: nnz (symbolic) then output offset
@@ -453,7 +456,7 @@ static gm_status analyze_impl(gm_plan* p) {
   const int64_t nh = p->n_heavy;
   const int32_t* heavy = p->rows_by_bin.p + p->bin_start[kHeavyBin];
   if (!p->chat_rp.alloc(nh + 1, s) || !p->heavy_ids64.alloc(std::max<int64_t>(nh, 1), s)) return GM_ERR_OOM;
-  DevBuf<int64_t> anz;
+  DevBuf<int64_t>& anz = p->anz;
   if (!anz.alloc(nh + 1, s)) return GM_ERR_OOM;
   cudaMemsetAsync(p->chat_rp.p + nh, 0, sizeof(int64_t), s);
   cudaMemsetAsync(anz.p + nh, 0, sizeof(int64_t), s);
@@ -555,6 +558,95 @@ template <class T>
 static void dbg_copy(DevBuf<T>& dst, const T* src, int64_t n, cudaStream_t s) {
   if (dst.alloc(std::max<int64_t>(n, 1), s) && n > 0)
     cudaMemcpyAsync(dst.p, src, n * sizeof(T), cudaMemcpyDeviceToDevice, s);
+}
+
+// Heavy rows [h0, h1), numeric pass of the row-order pipeline (one level): the
+// batch's A entries are gathered in row order, their products expanded straight
+// into the level-0 chunks (k_expand_split; C-hat is not written) whose sizes the
+// symbolic pass counted, then every chunk is accumulated.
+static gm_status run_batch_rowwise(gm_plan* p, int64_t h0, int64_t h1, int64_t* par_base, int32_t* c_col,
+                                   double* c_val) {
+  const cudaStream_t s = p->s;
+  const int64_t nb = h1 - h0;
+  const int64_t ip = p->h_chat_rp[h1] - p->h_chat_rp[h0];
+  const int64_t ne = p->h_anz[h1] - p->h_anz[h0];
+  const int32_t* heavy = p->rows_by_bin.p + p->bin_start[kHeavyBin] + h0;
+  const int v = static_cast<int>(p->P.v_chunks[0]);
+  const int64_t children = nb * v;
+  if (p->arena_col[0].n < static_cast<size_t>(ip)) return GM_ERR_WORKSPACE;
+
+  int t = p->stage_begin(GM_STAGE_TRANSPOSE);
+  DevBuf<int32_t> e_k, e_row, wg_entry;
+  DevBuf<double> e_a;
+  DevBuf<int64_t> e_off, lrp, bounds;
+  const int64_t n_wg = expand_num_wg(ip, ne);
+  if (!e_k.alloc(ne, s) || !e_row.alloc(ne, s) || !e_a.alloc(ne, s) || !e_off.alloc(ne + 1, s) ||
+      !lrp.alloc(nb + 1, s) || !bounds.alloc(n_wg + 1, s) || !wg_entry.alloc(n_wg, s))
+    return GM_ERR_OOM;
+  launch_gather_entries(heavy, nb, p->anz.p + h0, p->A.row_ptr, p->A.col_idx, p->A.vals, p->B.row_ptr, e_k.p, e_a.p,
+                        e_row.p, e_off.p, s);
+  cudaMemsetAsync(e_off.p + ne, 0, sizeof(int64_t), s);
+  if (!scan_exclusive_i64(e_off.p, e_off.p, ne + 1, nullptr, s)) return GM_ERR_OOM;
+  sub_i64(p->chat_rp.p + h0, nb + 1, p->h_chat_rp[h0], lrp.p, s);
+  launch_expand_bounds(e_off.p, ne, ip, bounds.p, wg_entry.p, s);
+  p->stage_end(t);
+
+  t = p->stage_begin(GM_STAGE_HISTOGRAM);
+  const int64_t* mcount = p->cnt0.p + h0 * v;  // chunk sizes from the symbolic pass
+  DevBuf<int64_t> rrp;
+  DevBuf<unsigned long long> cur;
+  if (!rrp.alloc(children + 1, s) || !cur.alloc(children, s)) return GM_ERR_OOM;
+  if (!scan_exclusive_i64(mcount, rrp.p, children, rrp.p + children, s)) return GM_ERR_OOM;
+  sub_to_u64(rrp.p, children, 0, cur.p, s);
+  p->stage_end(t);
+
+  t = p->stage_begin(GM_STAGE_MULTISPLIT);
+  ExpandArgs ea{};
+  ea.e_k = e_k.p;
+  ea.e_a = e_a.p;
+  ea.e_off = e_off.p;
+  ea.e_row = e_row.p;
+  ea.n_e = ne;
+  ea.b_rp = p->B.row_ptr;
+  ea.b_col = p->B.col_idx;
+  ea.b_val = p->B.vals;
+  ea.in_rp = lrp.p;
+  ea.n_parents = nb;
+  ea.bounds = bounds.p;
+  ea.wg_entry = wg_entry.p;
+  ea.n_wg = n_wg;
+  ea.v = v;
+  ea.shift = ilog2(p->P.widths[0]);
+  ea.n_group_rows = expand_group_rows(p->P.tau);
+  ea.status = p->status.p;
+  ea.cursor = cur.p;
+  ea.out_col = p->arena_col[0].p;
+  ea.out_val = p->arena_val[0].p;
+  launch_expand_split(ea, s);
+  p->stage_end(t);
+  e_k.release();
+  e_a.release();
+  e_row.release();
+  e_off.release();
+
+  ListArgs la{};
+  la.status = p->status.p;
+  la.c_col = c_col;
+  la.c_val = c_val;
+  la.rp = rrp.p;
+  la.col = p->arena_col[0].p;
+  la.val = p->arena_val[0].p;
+  la.child_base = par_base[0] * v;
+  la.v = v;
+  la.width = p->P.widths[0];
+  la.nnz_out = p->nnz[0].p;
+  la.off_in = p->nnz[0].p;
+  t = p->stage_begin(GM_STAGE_NUM_HEAVY);
+  const gm_status st = run_leaves(p, la, mcount, 0, children, true, true);
+  p->stage_end(t);
+  par_base[0] += nb;
+  if (st != GM_OK) return st;
+  return cuda_status(p, cudaGetLastError());
 }
 
 // Heavy rows [h0, h1): outer product, multisplit levels and chunk accumulation.
@@ -813,11 +905,11 @@ static gm_status plan_batches(gm_plan* p, int64_t bytes_per_ip, int64_t cap,
                               std::vector<std::pair<int64_t, int64_t>>& out) {
   const int64_t nh = p->n_heavy;
   const int64_t v0 = p->L >= 1 ? p->P.v_chunks[0] : 1;
-  const int64_t fixed = (p->A.n_cols + 1) * 8 * 3 + (int64_t(64) << 20);
+  const int64_t fixed = (p->A.n_cols + 1) * 8 * 3 + (int64_t(4) << 20);
   auto bytes = [&](int64_t h0, int64_t h1) {
     const int64_t ip = p->h_chat_rp[h1] - p->h_chat_rp[h0];
     const int64_t anz = p->h_anz[h1] - p->h_anz[h0];
-    return fixed + ip * bytes_per_ip + anz * 12 + (h1 - h0) * (32 + v0 * 72) + ip / 64;
+    return fixed + ip * bytes_per_ip + anz * 24 + (h1 - h0) * (32 + v0 * 72) + ip / 512 * 12;
   };
   out.clear();
   int64_t h0 = 0;
@@ -839,7 +931,8 @@ static int64_t workspace_cap(gm_plan* p);
 
 // Element buffers for the largest batch of a pass (values only in the numeric pass
 // or when intermediates are kept).
-static gm_status alloc_arena(gm_plan* p, const std::vector<std::pair<int64_t, int64_t>>& batches, bool with_val) {
+static gm_status alloc_arena(gm_plan* p, const std::vector<std::pair<int64_t, int64_t>>& batches, bool with_val,
+                             int nbuf = 2) {
   int64_t mx = 0;
   for (auto& b : batches) mx = std::max(mx, p->h_chat_rp[b.second] - p->h_chat_rp[b.first]);
   if (p->log)
@@ -847,12 +940,16 @@ static gm_status alloc_arena(gm_plan* p, const std::vector<std::pair<int64_t, in
                  (long long)mx, mx * (with_val ? 24.0 : 8.0) / 1e9);
   const size_t col_b = ((static_cast<size_t>(mx) * 4 + 255) / 256) * 256;
   const size_t val_b = with_val ? static_cast<size_t>(mx) * 8 : 0;
-  if (!p->arena_block.alloc(2 * (col_b + val_b), p->s)) return GM_ERR_OOM;
+  if (!p->arena_block.alloc(nbuf * (col_b + val_b), p->s)) return GM_ERR_OOM;
   unsigned char* base = p->arena_block.p;
   for (int k = 0; k < 2; ++k) {
+    p->arena_col[k] = {};
+    p->arena_val[k] = {};
+  }
+  for (int k = 0; k < nbuf; ++k) {
     p->arena_val[k].p = with_val ? reinterpret_cast<double*>(base + k * val_b) : nullptr;
     p->arena_val[k].n = with_val ? mx : 0;
-    p->arena_col[k].p = reinterpret_cast<int32_t*>(base + 2 * val_b + k * col_b);
+    p->arena_col[k].p = reinterpret_cast<int32_t*>(base + nbuf * val_b + k * col_b);
     p->arena_col[k].n = mx;
   }
   return GM_OK;
@@ -870,12 +967,12 @@ static void free_arena(gm_plan* p) {
 // does not fit after all (a caching allocator's blocks can be fragmented), the
 // cap is halved and the batches planned again, a few times.
 static gm_status plan_and_alloc(gm_plan* p, int64_t bytes_per_ip, bool with_val,
-                                std::vector<std::pair<int64_t, int64_t>>& batches) {
+                                std::vector<std::pair<int64_t, int64_t>>& batches, int nbuf = 2) {
   int64_t cap = workspace_cap(p);
   for (int attempt = 0; attempt < 6; ++attempt) {
     gm_status st = plan_batches(p, bytes_per_ip, cap, batches);
     if (st != GM_OK) return st;
-    st = alloc_arena(p, batches, with_val);
+    st = alloc_arena(p, batches, with_val, nbuf);
     if (st == GM_OK) return GM_OK;
     free_arena(p);
     cudaStreamSynchronize(p->s);
@@ -983,6 +1080,13 @@ static gm_status symbolic_impl(gm_plan* p, int64_t* C_rp, int64_t* C_nnz) {
       ra.status = p->status.p;
       const int ts = p->stage_begin(GM_STAGE_SYM_HEAVY);
       launch_rowbm(ra, true, 0, p->num_sms, p->smem_dev, s);
+      if (p->rowwise) {  // element counts of the level-0 chunks, for the numeric pass
+        if (!p->cnt0.alloc(nh * v0, s)) return GM_ERR_OOM;
+        if (!heavy_chunk_counts(p->rows_by_bin.p + p->bin_start[kHeavyBin], nh, p->anz.p, p->A.row_ptr,
+                                p->A.col_idx, p->B.row_ptr, p->B.col_idx, p->B.n_rows, static_cast<int>(v0),
+                                ilog2(p->P.widths[0]), p->cnt0.p, s))
+          return GM_ERR_OOM;
+      }
       p->stage_end(ts);
       p->n_batches = 0;
       p->n_leaves += nh * v0;
@@ -1061,12 +1165,13 @@ static gm_status numeric_impl(gm_plan* p, int32_t* C_col, double* C_val) {
     const bool keep = p->keep;
     p->keep = false;
     std::vector<std::pair<int64_t, int64_t>> batches;
-    gm_status st = plan_and_alloc(p, 24, true, batches);
+    gm_status st = p->rowwise ? plan_and_alloc(p, 12, true, batches, 1) : plan_and_alloc(p, 24, true, batches);
     if (st != GM_OK) return st;
     p->n_batches = std::max<int64_t>(p->n_batches, static_cast<int64_t>(batches.size()));
     int64_t par_base[GM_MAX_LEVELS + 1] = {};
     for (auto& bt : batches) {
-      st = run_batch(p, bt.first, bt.second, true, par_base, C_col, C_val);
+      st = p->rowwise ? run_batch_rowwise(p, bt.first, bt.second, par_base, C_col, C_val)
+                      : run_batch(p, bt.first, bt.second, true, par_base, C_col, C_val);
       if (st != GM_OK) return st;
     }
     free_arena(p);
@@ -1114,7 +1219,7 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
   p->B = *B;
   if (cfg) p->cfg = *cfg;
   p->s = static_cast<cudaStream_t>(stream);
-  p->pipeline = p->cfg.pipeline == GM_PIPE_UNFUSED ? GM_PIPE_UNFUSED : GM_PIPE_FUSED_HISTO;
+  p->pipeline = p->cfg.pipeline == GM_PIPE_UNFUSED ? GM_PIPE_UNFUSED : GM_PIPE_FUSED_HISTO;  // may become ROWWISE
   p->timing = (p->cfg.flags & GM_FLAG_TIMING) != 0;
   p->keep = (p->cfg.flags & GM_FLAG_KEEP_INTERMEDIATES) != 0;
   p->log = (p->cfg.flags & GM_FLAG_LOG) != 0 || gm::env_log();
@@ -1133,6 +1238,9 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
   p->L = static_cast<int>(p->P.n_levels);
   p->sym_rowbm = p->L <= 1 && p->pipeline != GM_PIPE_UNFUSED && !p->keep &&
                  gm::rowbm_symbolic_smem(p->c_m) + 4096 <= p->smem_dev;
+  p->rowwise = p->sym_rowbm && p->L == 1 && p->P.v_chunks[0] <= 256 &&
+               (p->cfg.pipeline == GM_PIPE_AUTO || p->cfg.pipeline == GM_PIPE_ROWWISE);
+  if (p->rowwise) p->pipeline = GM_PIPE_ROWWISE;
   gm::g_ws_peak = gm::g_ws_now.load();
   const int64_t l0 = gm::launch_count();
   st = gm::analyze_impl(p.get());

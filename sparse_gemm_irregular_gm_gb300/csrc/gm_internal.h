@@ -185,6 +185,46 @@ void launch_multisplit(const SplitArgs& a, cudaStream_t s);
 // *ngr_out gets the rows a work group may meet when input rows exceed tau elements.
 int64_t multisplit_pick_E(int v, int64_t tau, bool with_val, int64_t smem_max, int* ngr_out);
 
+// Row-order expansion fused with the first multisplit level (gm_multisplit.cu):
+// the products of a batch of heavy rows are generated in row order (A entry by
+// A entry, B row by B row) straight into their level-0 chunks; C-hat is never
+// written. Entries of the batch are concatenated in row order.
+struct ExpandArgs {
+  const int32_t* e_k;         // B row selected by each entry (A.col)
+  const double* e_a;          // A value of each entry (null: columns only)
+  const int64_t* e_off;       // flattened start of each entry's products, n_e + 1
+  const int32_t* e_row;       // batch-local row of each entry
+  int64_t n_e;
+  const int64_t* b_rp;
+  const int32_t* b_col;
+  const double* b_val;
+  const int64_t* in_rp;       // batch row starts in the flattened space, n_parents + 1
+  int64_t n_parents;
+  const int64_t* bounds;      // work group g covers [bounds[g], bounds[g+1])
+  const int32_t* wg_entry;    // entry holding bounds[g]
+  int64_t n_wg;
+  int v;
+  int shift;
+  int n_group_rows;
+  int* status;
+  unsigned long long* cursor; // per chunk (row * v + c): write cursor from its row pointer
+  int32_t* out_col;
+  double* out_val;            // null: columns only
+};
+constexpr int kExpandE = 4096;    // elements per work group (at most)
+constexpr int kExpandCap = 1024;  // entries starting inside a work group (at most)
+// Builds the batch entry arrays (e_len into e_off, then the caller scans it).
+void launch_gather_entries(const int32_t* heavy_rows, int64_t nb, const int64_t* anz_batch, const int64_t* a_rp,
+                           const int32_t* a_col, const double* a_val, const int64_t* b_rp, int32_t* e_k,
+                           double* e_a, int32_t* e_row, int64_t* e_len, cudaStream_t s);
+// Work-group bounds: multiples of kExpandE merged with the starts of every
+// kExpandCap-th entry; bounds has n_wg + 1 entries, wg_entry n_wg.
+int64_t expand_num_wg(int64_t total, int64_t n_e);
+void launch_expand_bounds(const int64_t* e_off, int64_t n_e, int64_t total, int64_t* bounds, int32_t* wg_entry,
+                          cudaStream_t s);
+void launch_expand_split(const ExpandArgs& a, cudaStream_t s);
+int expand_group_rows(int64_t tau);
+
 // ---- accumulation (gm_accum.cu) ---------------------------------------------
 struct LightArgs {
   const int32_t* rows;        // rows of this bin
@@ -256,6 +296,13 @@ struct RowBitmapArgs {
 int64_t rowbm_symbolic_smem(int64_t c_m);
 int64_t rowbm_numeric_smem(int64_t c_m, int cap);
 void launch_rowbm(const RowBitmapArgs& a, bool symbolic, int cap, int num_sms, int64_t smem_max, cudaStream_t s);
+
+// cnt[h * v + c] = products of heavy row h whose column falls in level-0 chunk c
+// (col >> shift == c), from per-B-row chunk histograms. False on allocation failure.
+// anz: prefix of the heavy rows' A-row lengths (n_heavy + 1).
+bool heavy_chunk_counts(const int32_t* heavy_rows, int64_t n_heavy, const int64_t* anz, const int64_t* a_rp,
+                        const int32_t* a_col, const int64_t* b_rp, const int32_t* b_col, int64_t b_rows, int v,
+                        int shift, int64_t* cnt, cudaStream_t s);
 
 // Light-row bins: upper bounds on u and table capacity per bin.
 constexpr int kLightWarpBins = 4;   // bins 1..4 use a warp per row

@@ -238,3 +238,256 @@ int64_t multisplit_pick_E(int v, int64_t tau, bool with_val, int64_t smem_max, i
 }
 
 }  // namespace gm
+
+namespace gm {
+
+namespace {
+
+constexpr int kExThreads = 512;
+constexpr int kExItems = kExpandE / kExThreads;  // 8
+
+__global__ void k_gather_entries(const int32_t* __restrict__ rows, int64_t nb, const int64_t* __restrict__ anz,
+                                 const int64_t* __restrict__ a_rp, const int32_t* __restrict__ a_col,
+                                 const double* __restrict__ a_val, const int64_t* __restrict__ b_rp,
+                                 int32_t* __restrict__ e_k, double* __restrict__ e_a, int32_t* __restrict__ e_row,
+                                 int64_t* __restrict__ e_len) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t h = warp; h < nb; h += nw) {
+    const int64_t r = rows[h];
+    const int64_t base = anz[h] - anz[0];
+    for (int64_t p = a_rp[r] + lane; p < a_rp[r + 1]; p += 32) {
+      const int64_t i = base + (p - a_rp[r]);
+      const int k = a_col[p];
+      e_k[i] = k;
+      if (e_a) e_a[i] = a_val[p];
+      e_row[i] = static_cast<int32_t>(h);
+      e_len[i] = b_rp[k + 1] - b_rp[k];
+    }
+  }
+}
+
+// largest j in [lo, hi] with arr[j] <= x (arr non-decreasing, arr[lo] <= x)
+__device__ __forceinline__ int64_t floor_index(const int64_t* __restrict__ arr, int64_t lo, int64_t hi, int64_t x) {
+  while (lo < hi) {
+    const int64_t mid = (lo + hi + 1) >> 1;
+    if (arr[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// bounds = sorted union of {g * E} and {e_off[m * CAP]}, then total.
+__global__ void k_expand_bounds(const int64_t* __restrict__ e_off, int64_t n_e, int64_t total, int64_t n1,
+                                int64_t n2, int64_t* __restrict__ bounds) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n1 + n2; t += stride) {
+    if (t < n1) {  // element boundary x = t * E: its rank counts the entry boundaries below x
+      const int64_t x = t * kExpandE;
+      int64_t lo = 0, hi = n2;  // number of m with e_off[m * CAP] < x
+      while (lo < hi) {
+        const int64_t mid = (lo + hi) >> 1;
+        if (e_off[mid * kExpandCap] < x) lo = mid + 1; else hi = mid;
+      }
+      bounds[t + lo] = x;
+    } else {       // entry boundary y = e_off[m * CAP]: its rank counts the element boundaries <= y
+      const int64_t m = t - n1;
+      const int64_t y = e_off[m * kExpandCap];
+      const int64_t c = min(n1, y / kExpandE + 1);
+      bounds[m + c] = y;
+    }
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) bounds[n1 + n2] = total;
+}
+
+__global__ void k_expand_wg_entry(const int64_t* __restrict__ e_off, int64_t n_e, const int64_t* __restrict__ bounds,
+                                  int64_t n_wg, int32_t* __restrict__ wg_entry) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < n_wg; g += stride) {
+    const int64_t x = bounds[g];
+    wg_entry[g] = static_cast<int32_t>(x >= e_off[n_e] ? n_e - 1 : floor_index(e_off, 0, n_e - 1, x));
+  }
+}
+
+template <bool VAL>
+__global__ void __launch_bounds__(kExThreads, 3) k_expand_split(ExpandArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int T = kExThreads;
+  const int E = kExpandE;
+  const int nk = a.n_group_rows * a.v;
+  const Layout L = carve(smem, nk, a.n_group_rows, E, true);
+  // entry table after the multisplit layout
+  unsigned char* tail = reinterpret_cast<unsigned char*>(L.val_buf + E);
+  int64_t* s_b = reinterpret_cast<int64_t*>(tail);                    // kExpandCap + 2
+  double* s_a = reinterpret_cast<double*>(s_b + kExpandCap + 2);      // kExpandCap + 2
+  int* s_lo = reinterpret_cast<int*>(s_a + kExpandCap + 2);           // kExpandCap + 2
+  __shared__ int s_ne;
+  __shared__ int64_t s_r0;
+
+  const int64_t g = blockIdx.x;
+  const int64_t S = a.bounds[g];
+  const int64_t end = a.bounds[g + 1];
+  const int n = static_cast<int>(end - S);
+  if (n <= 0) return;
+  const int64_t j0 = a.wg_entry[g];
+  if (threadIdx.x == 0) {
+    const int64_t j1 = floor_index(a.e_off, j0, min(a.n_e - 1, j0 + kExpandCap + 1), end - 1);
+    s_ne = static_cast<int>(j1 - j0 + 1);
+    s_r0 = a.e_row[j0];
+  }
+  __syncthreads();
+  const int ne = s_ne;
+  const int64_t r0 = s_r0;
+  if (ne > kExpandCap + 2) {  // bounds guarantee otherwise; never index past the table
+    if (threadIdx.x == 0) atomicOr(a.status, kStInternal);
+    return;
+  }
+  for (int i = threadIdx.x; i < ne; i += T) {
+    const int64_t j = j0 + i;
+    const int64_t off = a.e_off[j];
+    const int64_t lo = max(S, off);
+    const int lo_loc = static_cast<int>(min(lo, end) - S);
+    s_lo[i] = lo_loc;
+    s_b[i] = a.b_rp[a.e_k[j]] + (lo - off) - lo_loc;  // B index of local position p: s_b + p
+    s_a[i] = VAL ? a.e_a[j] : 0.0;
+  }
+  for (int k = threadIdx.x; k < nk; k += T) L.hist[k] = 0;
+  for (int jr = threadIdx.x; jr < a.n_group_rows; jr += T) {
+    const int64_t r = r0 + jr;
+    int64_t e = n;
+    if (r < a.n_parents) e = min(max(a.in_rp[r + 1] - S, int64_t(0)), static_cast<int64_t>(n));
+    L.row_end[jr] = static_cast<int>(e);
+  }
+  __syncthreads();
+
+  // generate this thread's elements: position p = k * T + tid (consecutive across lanes)
+  int key[kExItems], col[kExItems], ent[kExItems];
+  bool bad = false;
+  int jw = 0;  // entry of the warp's first lane at the previous item
+#pragma unroll
+  for (int k = 0; k < kExItems; ++k) {
+    const int p = k * T + threadIdx.x;
+    key[k] = -1;
+    col[k] = 0;
+    ent[k] = 0;
+    // entry: largest i with s_lo[i] <= p, searched from the warp's last entry
+    int lo_j = __shfl_sync(kFull, jw, 0);
+    if (p < n) {
+      if (lo_j + 1 < ne && s_lo[lo_j + 1] <= p) {
+        int hi_j = ne - 1;
+        while (lo_j < hi_j) {
+          const int mid = (lo_j + hi_j + 1) >> 1;
+          if (s_lo[mid] <= p) lo_j = mid; else hi_j = mid - 1;
+        }
+      }
+      ent[k] = lo_j;
+      col[k] = a.b_col[s_b[lo_j] + p];
+      const int jr = local_row(L.row_end, a.n_group_rows, p);
+      if (jr < a.n_group_rows) key[k] = jr * a.v + (static_cast<uint32_t>(col[k]) >> a.shift);
+      else bad = true;
+    }
+    jw = lo_j;
+  }
+  if (bad) atomicOr(a.status, kStGroupRows);
+#pragma unroll
+  for (int k = 0; k < kExItems; ++k) {
+    const unsigned heads = run_heads(key[k]);
+    if (key[k] >= 0 && ((heads >> (threadIdx.x & 31)) & 1u)) atomicAdd(&L.hist[key[k]], run_length(heads));
+  }
+  __syncthreads();
+  {
+    __shared__ int ws[33];
+    const int per = (nk + T - 1) / T;
+    const int k0 = threadIdx.x * per;
+    int acc = 0;
+    for (int k = k0; k < min(nk, k0 + per); ++k) acc += L.hist[k];
+    int pre = block_exclusive_scan(acc, ws, static_cast<int*>(nullptr));
+    for (int k = k0; k < min(nk, k0 + per); ++k) {
+      const int c = L.hist[k];
+      L.loff[k] = pre;
+      if (c > 0) {
+        const int64_t child = (r0 + k / a.v) * a.v + (k % a.v);
+        L.gpos[k] = static_cast<int64_t>(atomicAdd(&a.cursor[child], static_cast<unsigned long long>(c)));
+      }
+      pre += c;
+    }
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < nk; k += T) L.hist[k] = L.loff[k];
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  int pos[kExItems];
+#pragma unroll
+  for (int k = 0; k < kExItems; ++k) {
+    const unsigned heads = run_heads(key[k]);
+    const int leader = run_head_lane(heads);
+    int b = 0;
+    if (key[k] >= 0 && lane == leader) b = atomicAdd(&L.hist[key[k]], run_length(heads));
+    b = __shfl_sync(kFull, b, leader);
+    pos[k] = b + (lane - leader);
+    if (key[k] >= 0) L.col_buf[pos[k]] = col[k];
+  }
+  if (VAL) {
+    double vv[kExItems];
+#pragma unroll
+    for (int k = 0; k < kExItems; ++k) {
+      const int p = k * T + threadIdx.x;
+      vv[k] = key[k] >= 0 ? s_a[ent[k]] * a.b_val[s_b[ent[k]] + p] : 0.0;
+    }
+#pragma unroll
+    for (int k = 0; k < kExItems; ++k)
+      if (key[k] >= 0) L.val_buf[pos[k]] = vv[k];
+  }
+  __syncthreads();
+  const int32_t mask = static_cast<int32_t>((1u << a.shift) - 1u);
+  for (int i = threadIdx.x; i < n; i += T) {
+    const int32_t c = L.col_buf[i];
+    const int j = local_row(L.row_end, a.n_group_rows, i);
+    if (j >= a.n_group_rows) continue;
+    const int kk = j * a.v + (static_cast<uint32_t>(c) >> a.shift);
+    const int64_t dest = L.gpos[kk] + (i - L.loff[kk]);
+    a.out_col[dest] = c & mask;
+    if (VAL) a.out_val[dest] = L.val_buf[i];
+  }
+}
+
+size_t expand_smem_bytes(int v, int ngr) {
+  return split_smem_bytes(v, ngr, kExpandE, true, true) + static_cast<size_t>(kExpandCap + 2) * 20 + 64;
+}
+
+}  // namespace
+
+int expand_group_rows(int64_t tau) { return static_cast<int>((kExpandE - 1 + tau) / (tau + 1) + 1); }
+
+void launch_gather_entries(const int32_t* heavy_rows, int64_t nb, const int64_t* anz_batch, const int64_t* a_rp,
+                           const int32_t* a_col, const double* a_val, const int64_t* b_rp, int32_t* e_k,
+                           double* e_a, int32_t* e_row, int64_t* e_len, cudaStream_t s) {
+  if (nb <= 0) return;
+  (k_gather_entries<<<grid_for(nb * 32, 256), 256, 0, s>>>(heavy_rows, nb, anz_batch, a_rp, a_col, a_val, b_rp, e_k,
+                                                           e_a, e_row, e_len), note_launch());
+}
+
+int64_t expand_num_wg(int64_t total, int64_t n_e) {
+  return (total + kExpandE - 1) / kExpandE + (n_e + kExpandCap - 1) / kExpandCap;
+}
+
+void launch_expand_bounds(const int64_t* e_off, int64_t n_e, int64_t total, int64_t* bounds, int32_t* wg_entry,
+                          cudaStream_t s) {
+  const int64_t n1 = (total + kExpandE - 1) / kExpandE, n2 = (n_e + kExpandCap - 1) / kExpandCap;
+  (k_expand_bounds<<<grid_for(n1 + n2, 256), 256, 0, s>>>(e_off, n_e, total, n1, n2, bounds), note_launch());
+  (k_expand_wg_entry<<<grid_for(n1 + n2, 256), 256, 0, s>>>(e_off, n_e, bounds, n1 + n2, wg_entry), note_launch());
+}
+
+void launch_expand_split(const ExpandArgs& a, cudaStream_t s) {
+  if (a.n_wg <= 0) return;
+  const size_t smem = expand_smem_bytes(a.v, a.n_group_rows);
+  if (a.out_val) {
+    cudaFuncSetAttribute(k_expand_split<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    (k_expand_split<true><<<static_cast<unsigned>(a.n_wg), kExThreads, smem, s>>>(a), note_launch());
+  } else {
+    cudaFuncSetAttribute(k_expand_split<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    (k_expand_split<false><<<static_cast<unsigned>(a.n_wg), kExThreads, smem, s>>>(a), note_launch());
+  }
+}
+
+}  // namespace gm

@@ -276,3 +276,94 @@ void launch_rowbm(const RowBitmapArgs& a, bool symbolic, int cap, int num_sms, i
 }
 
 }  // namespace gm
+
+namespace gm {
+
+namespace {
+
+// hist[k * v + c] = number of stored B[k, j] with j >> shift == c (one warp per B row).
+__global__ void k_b_chunk_hist(const int64_t* __restrict__ b_rp, const int32_t* __restrict__ b_col, int64_t n_rows,
+                               int v, int shift, int32_t* __restrict__ hist) {
+  extern __shared__ int sh[];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int* h = sh + w * v;
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * nw + w; k < n_rows; k += static_cast<int64_t>(gridDim.x) * nw) {
+    for (int c = lane; c < v; c += 32) h[c] = 0;
+    __syncwarp();
+    for (int64_t q = b_rp[k] + lane; q < b_rp[k + 1]; q += 32)
+      atomicAdd(&h[static_cast<uint32_t>(b_col[q]) >> shift], 1);
+    __syncwarp();
+    for (int c = lane; c < v; c += 32) hist[k * v + c] = h[c];
+    __syncwarp();
+  }
+}
+
+// cnt[h * v + c] += elements of chunk c of heavy row h: the heavy rows' A entries,
+// concatenated (anz = prefix of their lengths), are cut into segments of 256 per
+// warp; each entry adds the chunk histogram of the B row it selects, and a warp
+// flushes its sums with one atomic per chunk whenever its segment leaves a row.
+constexpr int kSegEntries = 256;
+
+__global__ void k_heavy_chunk_counts(const int32_t* __restrict__ rows, int64_t n, const int64_t* __restrict__ anz,
+                                     const int64_t* __restrict__ a_rp, const int32_t* __restrict__ a_col,
+                                     const int32_t* __restrict__ hist, int v, unsigned long long* __restrict__ cnt) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t total = anz[n];
+  const int nc = (v + 31) / 32;  // <= 8 chunks per lane
+  for (int64_t seg = warp; seg * kSegEntries < total; seg += nw) {
+    const int64_t e0 = seg * kSegEntries, e1 = min(e0 + kSegEntries, total);
+    int64_t lo = 0, hi = n - 1;  // heavy row holding entry e0
+    while (lo < hi) {
+      const int64_t mid = (lo + hi + 1) >> 1;
+      if (anz[mid] <= e0) lo = mid; else hi = mid - 1;
+    }
+    int64_t h = lo;
+    int64_t row_end = anz[h + 1];
+    int64_t pbase = a_rp[rows[h]] - anz[h];
+    int acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int64_t e = e0; e < e1; ++e) {
+      while (e >= row_end) {
+        for (int i = 0; i < nc; ++i) {
+          const int c = i * 32 + lane;
+          if (c < v && acc[i]) atomicAdd(&cnt[h * v + c], static_cast<unsigned long long>(acc[i]));
+          acc[i] = 0;
+        }
+        ++h;
+        row_end = anz[h + 1];
+        pbase = a_rp[rows[h]] - anz[h];
+      }
+      const int64_t k = a_col[pbase + e];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = i * 32 + lane;
+        if (i < nc && c < v) acc[i] += hist[k * v + c];
+      }
+    }
+    for (int i = 0; i < nc; ++i) {
+      const int c = i * 32 + lane;
+      if (c < v && acc[i]) atomicAdd(&cnt[h * v + c], static_cast<unsigned long long>(acc[i]));
+    }
+  }
+}
+
+}  // namespace
+
+bool heavy_chunk_counts(const int32_t* heavy_rows, int64_t n_heavy, const int64_t* anz, const int64_t* a_rp,
+                        const int32_t* a_col, const int64_t* b_rp, const int32_t* b_col, int64_t b_rows, int v,
+                        int shift, int64_t* cnt, cudaStream_t s) {
+  if (n_heavy <= 0) return true;
+  if (v > 256) return false;
+  DevBuf<int32_t> hist;
+  if (!hist.alloc(static_cast<size_t>(b_rows) * v, s)) return false;
+  const int warps = 8;
+  (k_b_chunk_hist<<<grid_for(b_rows * 32, warps * 32), warps * 32, warps * v * sizeof(int), s>>>(
+       b_rp, b_col, b_rows, v, shift, hist.p), note_launch());
+  cudaMemsetAsync(cnt, 0, static_cast<size_t>(n_heavy) * v * sizeof(int64_t), s);
+  (k_heavy_chunk_counts<<<152 * 16, 256, 0, s>>>(heavy_rows, n_heavy, anz, a_rp, a_col, hist.p, v,
+                                                 reinterpret_cast<unsigned long long*>(cnt)), note_launch());
+  return true;
+}
+
+}  // namespace gm

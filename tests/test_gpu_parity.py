@@ -38,9 +38,13 @@ FORCED = [
     ("heavy_L2", {"tau": 16, "dense_width": 64, "n_chunks_max": 4}),    # two levels
     ("heavy_L3", {"tau": 16, "dense_width": 16, "n_chunks_max": 4}),    # three levels
     ("unfused", {"tau": 16, "dense_width": 64, "n_chunks_max": 4, "pipeline": binding.GM_PIPE_UNFUSED}),
-    ("batched", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "workspace_cap_bytes": 70 << 20}),
+    ("batched", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "workspace_cap_bytes": 6 << 20,
+                 "pipeline": binding.GM_PIPE_FUSED_HISTO}),
     ("L1_unfused", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_UNFUSED}),
     ("L1_wide_chunks", {"tau": 64, "dense_width": 512}),                   # one level, 2 chunks of 512
+    ("L1_outer", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_FUSED_HISTO}),
+    ("L1_rowwise_batched", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "workspace_cap_bytes": 5 << 20,
+                            "pipeline": binding.GM_PIPE_ROWWISE}),
 ]
 
 
@@ -51,8 +55,12 @@ def test_rmat10_forced_paths(name, cfg, values):
     info = check_full(A, A, exact=values == "int", **cfg)
     if name != "auto":
         assert info.n_heavy_rows > 0
-        if name == "batched":
+        if "batched" in name:
             assert info.n_batches > 1
+        if name in ("heavy_L1", "L1_wide_chunks", "L1_rowwise_batched"):
+            assert info.pipeline == binding.GM_PIPE_ROWWISE
+        if name == "L1_outer":
+            assert info.pipeline == binding.GM_PIPE_FUSED_HISTO
 
 
 @pytest.mark.parametrize("seed", range(4))
