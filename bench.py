@@ -111,20 +111,32 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power)}
 
 
-def byte_model(info, A, nnz_c):
+def byte_model(info, A, nnz_c, rowwise):
     """Algorithmic bytes per step.
 
-    Whole path (the method's byte model, one multisplit level): read A and B once,
-    C-hat written once (12 B/product), per level a histogram read of columns (4) and
-    a multisplit read + write (12 + 12), a symbolic column read (4), a numeric read
-    (12), C written once. Per stage: the bytes that stage must move in this
-    implementation (symbolic passes carry columns only, numeric passes columns and
-    values; the level-0 histogram is counted inside the outer product).
+    Whole path, outer-product pipelines (the method's byte model, one multisplit
+    level): read A and B once, C-hat written once (12 B/product), per level a
+    histogram read of columns (4) and a multisplit read + write (12 + 12), a
+    symbolic column read (4), a numeric read (12), C written once.
+    Row-order pipeline: C-hat is never written; the expansion writes each heavy
+    product once, already in its level-0 chunk (12), the symbolic pass reads the
+    B columns it walks (4) and the numeric pass reads the chunks once (12).
+    Per stage: the bytes that stage must move in this implementation (symbolic
+    passes carry columns only, numeric passes columns and values; the level-0
+    histogram is counted inside the outer product).
     """
     ip_h = info.ip_heavy
     L = max(1, info.params.n_levels)
     a_bytes = 8 * (A.n_rows + 1) + 12 * A.nnz
     c_bytes = 8 * (A.n_rows + 1) + 12 * nnz_c
+    if rowwise:
+        b_alg = 2 * a_bytes + ip_h * (12 + 4 + 12) + c_bytes
+        stages = {
+            "multisplit": ip_h * 12,    # products written once, into their level-0 chunks
+            "sym_heavy": ip_h * 4,      # B columns walked
+            "num_heavy": ip_h * 12,     # chunk columns and values read (+ C writes, added by the caller)
+        }
+        return b_alg, stages
     b_alg = 2 * a_bytes + ip_h * (12 + L * (4 + 12 + 12) + 4 + 12) + c_bytes
     stages = {
         "outer_sym": ip_h * 4,          # C-hat columns written (symbolic pass)
@@ -185,8 +197,8 @@ def max_over_ranks(x, world):
 def _cpu_baseline_child(workload, seed, target_s):
     import oracle
     from sparse_gemm_irregular_gm_gb300 import inputs
-    A = inputs.named_workload(workload, seed=seed)
-    return _cpu_baseline(A, oracle.ip_counts(A, A), target_s, seed)
+    A, B = inputs.named_pair(workload, seed=seed)
+    return _cpu_baseline(A, B, oracle.ip_counts(A, B), target_s, seed)
 
 
 def cpu_baseline(workload, seed, target_s):
@@ -196,7 +208,7 @@ def cpu_baseline(workload, seed, target_s):
         return pool.apply(_cpu_baseline_child, (workload, seed, target_s))
 
 
-def _cpu_baseline(A, u, target_s, seed):
+def _cpu_baseline(A, B, u, target_s, seed):
     """The oracle, as it stands, on a bounded random sample of A's rows."""
     import numpy as np
 
@@ -205,16 +217,16 @@ def _cpu_baseline(A, u, target_s, seed):
     order = rng.permutation(A.n_rows)
     csum = np.cumsum(u[order])
     # calibrate on ~2e7 products, then size the sample for target_s seconds
-    k = int(np.searchsorted(csum, 2e7)) + 1
+    k = min(A.n_rows, int(np.searchsorted(csum, 2e7)) + 1)
     t0 = time.perf_counter()
-    oracle.spgemm_rows(A, A, np.sort(order[:k]))
+    oracle.spgemm_rows(A, B, np.sort(order[:k]))
     rate = float(csum[k - 1]) / max(time.perf_counter() - t0, 1e-3)
     k = int(np.searchsorted(csum, rate * target_s)) + 1
     k = min(k, A.n_rows)
     rows = np.sort(order[:k])
     ip = int(csum[k - 1])
     t0 = time.perf_counter()
-    oracle.spgemm_rows(A, A, rows)
+    oracle.spgemm_rows(A, B, rows)
     dt = time.perf_counter() - t0
     return {"value": 2.0 * ip / dt / 1e9, "unit": "GFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
             "sample": f"{k} random rows of the workload ({ip:.3e} of {int(u.sum()):.3e} intermediate products), "
@@ -229,13 +241,14 @@ def run_ours(args):
     from sparse_gemm_irregular_gm_gb300 import binding, inputs
     rank, world, local = dist_setup(args)
     __graft_entry__.build()
-    A = inputs.named_workload(args.workload, seed=args.seed)
+    A, B = inputs.named_pair(args.workload, seed=args.seed)
     Ad = binding.to_device(A)
+    Bd = Ad if B is A else binding.to_device(B)
     cfg = binding.make_config(flags=binding.GM_FLAG_TIMING, pipeline=args.pipeline)
     stream = torch.cuda.current_stream()
 
     def step():
-        plan = binding.gm_spgemm_analyze(Ad, Ad, cfg, stream)
+        plan = binding.gm_spgemm_analyze(Ad, Bd, cfg, stream)
         c_rp = torch.empty(A.n_rows + 1, dtype=torch.int64, device="cuda")
         nnz = binding.gm_spgemm_symbolic(plan, c_rp)
         c_col = torch.empty(nnz, dtype=torch.int32, device="cuda")
@@ -252,7 +265,7 @@ def run_ours(args):
         del c_rp
         log(f"warmup {w}: {time.perf_counter() - t0:.3f} s, stages {[round(x, 1) for x in info.stage_ms]}")
     # per-row products and the heavy rows (for the byte model and the CPU sample)
-    plan = binding.gm_spgemm_analyze(Ad, Ad, None, stream)
+    plan = binding.gm_spgemm_analyze(Ad, Bd, None, stream)
     u = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_IP_COUNTS)
     heavy = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_HEAVY_ROWS)
     binding.gm_spgemm_plan_destroy(plan)
@@ -283,7 +296,7 @@ def run_ours(args):
     flops = 2.0 * info.ip_total
     value = world * flops / (ms / 1e3) / 1e9
     peak, peak_kind = peaks()
-    b_alg, stage_bytes = byte_model(info, A, nnz_c)
+    b_alg, stage_bytes = byte_model(info, A, nnz_c, info.pipeline == binding.GM_PIPE_ROWWISE)
     stage_bytes["num_heavy"] += 12 * nnz_heavy + 8 * len(heavy)
     names = binding.STAGES
     stage_table = {names[i]: round(float(stage_ms[i]), 3) for i in range(len(names)) if stage_ms[i] > 0}
@@ -299,7 +312,7 @@ def run_ours(args):
                    "n": A.n_rows, "nnz_A": A.nnz, "intermediate_products": info.ip_total,
                    "heavy_products": info.ip_heavy, "nnz_C": nnz_c, "heavy_rows": info.n_heavy_rows,
                    "levels": info.params.n_levels, "chunks": list(info.params.v_chunks[:info.params.n_levels]),
-                   "batches": info.n_batches, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "batches": info.n_batches, "pipeline": binding.PIPELINES[info.pipeline], "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs and outputs larger than L2 (C alone is %.0f GB)" % (12 * nnz_c / 1e9)},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
@@ -315,7 +328,7 @@ def run_ours(args):
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         result["cpu_baseline"] = cpu_baseline(args.workload, args.seed, args.cpu_seconds)
         log("cpu_baseline: " + json.dumps(result["cpu_baseline"]))
-    if not args.no_e2e and rank == 0:
+    if not args.no_e2e and rank == 0 and B is A:
         result["e2e"] = run_e2e(args, A, cfg, stream, nnz_c, info.ip_total)
         log("e2e: " + json.dumps(result["e2e"]))
     if rank == 0:
@@ -379,24 +392,24 @@ def run_reference(args):
     if rank != 0:
         return
     oracle.build()
-    A = inputs.named_workload(args.workload, seed=args.seed)
-    u = oracle.ip_counts(A, A)
+    A, B = inputs.named_pair(args.workload, seed=args.seed)
+    u = oracle.ip_counts(A, B)
     per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     rng = np.random.default_rng(args.seed)
     order = rng.permutation(A.n_rows)
     csum = np.cumsum(u[order])
-    k = int(np.searchsorted(csum, 2e7)) + 1
+    k = min(A.n_rows, int(np.searchsorted(csum, 2e7)) + 1)
     t0 = time.perf_counter()
-    oracle.spgemm_rows(A, A, np.sort(order[:k]))
+    oracle.spgemm_rows(A, B, np.sort(order[:k]))
     rate = float(csum[k - 1]) / max(time.perf_counter() - t0, 1e-3)
     k = min(A.n_rows, int(np.searchsorted(csum, rate * per_step)) + 1)
     rows = np.sort(order[:k])
     ip = int(csum[k - 1])
     for _ in range(args.warmup):
-        oracle.spgemm_rows(A, A, rows)
+        oracle.spgemm_rows(A, B, rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.spgemm_rows(A, A, rows)
+        oracle.spgemm_rows(A, B, rows)
     dt = (time.perf_counter() - t0) / args.steps
     value = 2.0 * ip / dt / 1e9
     sample = f"{k} random rows per step ({ip:.3e} of {int(u.sum()):.3e} intermediate products)"

@@ -22,8 +22,8 @@ from dataclasses import dataclass
 
 import numpy as np
 
-__all__ = ["CSR", "rmat", "laplacian_2d", "erdos_renyi", "random_csr",
-           "identity", "permutation", "named_workload", "WORKLOADS"]
+__all__ = ["CSR", "rmat", "laplacian_2d", "erdos_renyi", "random_csr", "row_slice",
+           "identity", "permutation", "named_workload", "named_pair", "WORKLOADS", "PAIRS"]
 
 
 @dataclass
@@ -221,5 +221,27 @@ WORKLOADS = {
 }
 
 
+def row_slice(M: CSR, lo: int, hi: int) -> CSR:
+    """Rows [lo, hi) of M (all columns kept)."""
+    a, b = int(M.row_ptr[lo]), int(M.row_ptr[hi])
+    return CSR(hi - lo, M.n_cols, (M.row_ptr[lo:hi + 1] - a).astype(np.int64), M.col[a:b].copy(), M.val[a:b].copy())
+
+
+# Products of two different matrices: (description, generator of (A, B)). C = A @ B.
+PAIRS = {
+    "rmat20_rows8k": ("A[2^19 : 2^19 + 8192, :] * A, A = R-MAT scale 20, edge factor 16 (profiling case: "
+                      "C.m = 2^20 at a few GB)",
+                      lambda seed=1: (lambda A: (row_slice(A, 1 << 19, (1 << 19) + 8192), A))(rmat(20, 16, seed=seed))),
+}
+
+
 def named_workload(name: str, seed: int = 1) -> CSR:
     return WORKLOADS[name][1](seed)
+
+
+def named_pair(name: str, seed: int = 1):
+    """(A, B) of a named product: the A*A workloads give (A, A)."""
+    if name in PAIRS:
+        return PAIRS[name][1](seed)
+    A = named_workload(name, seed)
+    return A, A
