@@ -575,20 +575,22 @@ static gm_status run_batch_rowwise(gm_plan* p, int64_t h0, int64_t h1, int64_t* 
   const int64_t children = nb * v;
   if (p->arena_col[0].n < static_cast<size_t>(ip)) return GM_ERR_WORKSPACE;
 
+  if (ne >= INT32_MAX) return GM_ERR_INDEX_OVERFLOW;  // entries are indexed by int32 inside the kernels
   int t = p->stage_begin(GM_STAGE_TRANSPOSE);
-  DevBuf<int32_t> e_k, e_row, wg_entry;
+  DevBuf<int32_t> e_row;
+  DevBuf<int4> wg_info;
   DevBuf<double> e_a;
-  DevBuf<int64_t> e_off, lrp, bounds;
+  DevBuf<int64_t> e_b, e_off, lrp, bounds;
   const int64_t n_wg = expand_num_wg(ip, ne);
-  if (!e_k.alloc(ne, s) || !e_row.alloc(ne, s) || !e_a.alloc(ne, s) || !e_off.alloc(ne + 1, s) ||
-      !lrp.alloc(nb + 1, s) || !bounds.alloc(n_wg + 1, s) || !wg_entry.alloc(n_wg, s))
+  if (!e_b.alloc(ne, s) || !e_row.alloc(ne, s) || !e_a.alloc(ne, s) || !e_off.alloc(ne + 1, s) ||
+      !lrp.alloc(nb + 1, s) || !bounds.alloc(n_wg + 1, s) || !wg_info.alloc(n_wg, s))
     return GM_ERR_OOM;
-  launch_gather_entries(heavy, nb, p->anz.p + h0, p->A.row_ptr, p->A.col_idx, p->A.vals, p->B.row_ptr, e_k.p, e_a.p,
+  launch_gather_entries(heavy, nb, p->anz.p + h0, p->A.row_ptr, p->A.col_idx, p->A.vals, p->B.row_ptr, e_b.p, e_a.p,
                         e_row.p, e_off.p, s);
   cudaMemsetAsync(e_off.p + ne, 0, sizeof(int64_t), s);
   if (!scan_exclusive_i64(e_off.p, e_off.p, ne + 1, nullptr, s)) return GM_ERR_OOM;
   sub_i64(p->chat_rp.p + h0, nb + 1, p->h_chat_rp[h0], lrp.p, s);
-  launch_expand_bounds(e_off.p, ne, ip, bounds.p, wg_entry.p, s);
+  launch_expand_bounds(e_off.p, e_row.p, ne, ip, bounds.p, wg_info.p, s);
   p->stage_end(t);
 
   t = p->stage_begin(GM_STAGE_HISTOGRAM);
@@ -602,7 +604,7 @@ static gm_status run_batch_rowwise(gm_plan* p, int64_t h0, int64_t h1, int64_t* 
 
   t = p->stage_begin(GM_STAGE_MULTISPLIT);
   ExpandArgs ea{};
-  ea.e_k = e_k.p;
+  ea.e_b = e_b.p;
   ea.e_a = e_a.p;
   ea.e_off = e_off.p;
   ea.e_row = e_row.p;
@@ -613,7 +615,7 @@ static gm_status run_batch_rowwise(gm_plan* p, int64_t h0, int64_t h1, int64_t* 
   ea.in_rp = lrp.p;
   ea.n_parents = nb;
   ea.bounds = bounds.p;
-  ea.wg_entry = wg_entry.p;
+  ea.wg_info = wg_info.p;
   ea.n_wg = n_wg;
   ea.v = v;
   ea.shift = ilog2(p->P.widths[0]);
@@ -624,7 +626,7 @@ static gm_status run_batch_rowwise(gm_plan* p, int64_t h0, int64_t h1, int64_t* 
   ea.out_val = p->arena_val[0].p;
   launch_expand_split(ea, s);
   p->stage_end(t);
-  e_k.release();
+  e_b.release();
   e_a.release();
   e_row.release();
   e_off.release();
@@ -1009,7 +1011,7 @@ static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, double* c_val
     const int64_t cnt = p->bin_start[b + 1] - p->bin_start[b];
     if (cnt <= 0) continue;
     const int cap = b <= 9 ? static_cast<int>(light_bin_ub(b)) : static_cast<int>(p->P.tau);
-    if (numeric && b >= 7 && rowbm_numeric_smem(p->c_m, cap) + 4096 <= p->smem_dev) {
+    if (b >= 7 && rowbm_light_fits(p->c_m, cap, !numeric, p->smem_dev)) {
       RowBitmapArgs ra{};
       ra.rows = p->rows_by_bin.p + p->bin_start[b];
       ra.n_items = cnt;
@@ -1025,7 +1027,7 @@ static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, double* c_val
       ra.c_val = c_val;
       ra.work_counter = p->work_counter.p;
       ra.status = p->status.p;
-      launch_rowbm(ra, false, cap, p->num_sms, p->smem_dev, p->s);
+      launch_rowbm_light(ra, !numeric, cap, p->num_sms, p->s);
       continue;
     }
     LightArgs la{};
@@ -1079,7 +1081,7 @@ static gm_status symbolic_impl(gm_plan* p, int64_t* C_rp, int64_t* C_nnz) {
       ra.work_counter = p->work_counter.p;
       ra.status = p->status.p;
       const int ts = p->stage_begin(GM_STAGE_SYM_HEAVY);
-      launch_rowbm(ra, true, 0, p->num_sms, p->smem_dev, s);
+      launch_rowbm(ra, p->num_sms, p->smem_dev, s);
       if (p->rowwise) {  // element counts of the level-0 chunks, for the numeric pass
         if (!p->cnt0.alloc(nh * v0, s)) return GM_ERR_OOM;
         if (!heavy_chunk_counts(p->rows_by_bin.p + p->bin_start[kHeavyBin], nh, p->anz.p, p->A.row_ptr,
@@ -1239,6 +1241,7 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
   p->sym_rowbm = p->L <= 1 && p->pipeline != GM_PIPE_UNFUSED && !p->keep &&
                  gm::rowbm_symbolic_smem(p->c_m) + 4096 <= p->smem_dev;
   p->rowwise = p->sym_rowbm && p->L == 1 && p->P.v_chunks[0] <= 256 &&
+               gm::expand_fits(static_cast<int>(p->P.v_chunks[0]), p->P.widths[0], p->P.tau, p->smem_dev) &&
                (p->cfg.pipeline == GM_PIPE_AUTO || p->cfg.pipeline == GM_PIPE_ROWWISE);
   if (p->rowwise) p->pipeline = GM_PIPE_ROWWISE;
   gm::g_ws_peak = gm::g_ws_now.load();

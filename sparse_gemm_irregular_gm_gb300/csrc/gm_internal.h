@@ -190,7 +190,7 @@ int64_t multisplit_pick_E(int v, int64_t tau, bool with_val, int64_t smem_max, i
 // A entry, B row by B row) straight into their level-0 chunks; C-hat is never
 // written. Entries of the batch are concatenated in row order.
 struct ExpandArgs {
-  const int32_t* e_k;         // B row selected by each entry (A.col)
+  const int64_t* e_b;         // B.rowPtr of the B row each entry selects (B.rowPtr[A.col])
   const double* e_a;          // A value of each entry (null: columns only)
   const int64_t* e_off;       // flattened start of each entry's products, n_e + 1
   const int32_t* e_row;       // batch-local row of each entry
@@ -201,7 +201,7 @@ struct ExpandArgs {
   const int64_t* in_rp;       // batch row starts in the flattened space, n_parents + 1
   int64_t n_parents;
   const int64_t* bounds;      // work group g covers [bounds[g], bounds[g+1])
-  const int32_t* wg_entry;    // entry holding bounds[g]
+  const int4* wg_info;        // per work group: first entry, number of entries, its first batch row
   int64_t n_wg;
   int v;
   int shift;
@@ -215,15 +215,18 @@ constexpr int kExpandE = 4096;    // elements per work group (at most)
 constexpr int kExpandCap = 1024;  // entries starting inside a work group (at most)
 // Builds the batch entry arrays (e_len into e_off, then the caller scans it).
 void launch_gather_entries(const int32_t* heavy_rows, int64_t nb, const int64_t* anz_batch, const int64_t* a_rp,
-                           const int32_t* a_col, const double* a_val, const int64_t* b_rp, int32_t* e_k,
+                           const int32_t* a_col, const double* a_val, const int64_t* b_rp, int64_t* e_b,
                            double* e_a, int32_t* e_row, int64_t* e_len, cudaStream_t s);
 // Work-group bounds: multiples of kExpandE merged with the starts of every
-// kExpandCap-th entry; bounds has n_wg + 1 entries, wg_entry n_wg.
+// kExpandCap-th entry; bounds has n_wg + 1 entries, wg_info n_wg.
 int64_t expand_num_wg(int64_t total, int64_t n_e);
-void launch_expand_bounds(const int64_t* e_off, int64_t n_e, int64_t total, int64_t* bounds, int32_t* wg_entry,
-                          cudaStream_t s);
+void launch_expand_bounds(const int64_t* e_off, const int32_t* e_row, int64_t n_e, int64_t total, int64_t* bounds,
+                          int4* wg_info, cudaStream_t s);
 void launch_expand_split(const ExpandArgs& a, cudaStream_t s);
 int expand_group_rows(int64_t tau);
+// Whether k_expand_split can take v chunks per row of width w at this tau within
+// smem bytes of shared memory (packed keys need n_group_rows * v < 65535, w <= 65536).
+bool expand_fits(int v, int64_t w, int64_t tau, size_t smem);
 
 // ---- accumulation (gm_accum.cu) ---------------------------------------------
 struct LightArgs {
@@ -294,8 +297,12 @@ struct RowBitmapArgs {
   int* status;
 };
 int64_t rowbm_symbolic_smem(int64_t c_m);
-int64_t rowbm_numeric_smem(int64_t c_m, int cap);
-void launch_rowbm(const RowBitmapArgs& a, bool symbolic, int cap, int num_sms, int64_t smem_max, cudaStream_t s);
+// Heavy rows: chunk nnz (v chunks of a.width) or whole-row nnz from a whole-row bitmap.
+void launch_rowbm(const RowBitmapArgs& a, int num_sms, int64_t smem_max, cudaStream_t s);
+// Light rows of at most cap products (symbolic: whole-row nnz into c_rp; numeric: the row of C).
+int64_t rowbm_light_smem(int64_t c_m, int cap, bool symbolic);
+bool rowbm_light_fits(int64_t c_m, int cap, bool symbolic, int64_t smem_max);
+void launch_rowbm_light(const RowBitmapArgs& a, bool symbolic, int cap, int num_sms, cudaStream_t s);
 
 // cnt[h * v + c] = products of heavy row h whose column falls in level-0 chunk c
 // (col >> shift == c), from per-B-row chunk histograms. False on allocation failure.

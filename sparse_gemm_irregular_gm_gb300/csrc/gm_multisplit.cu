@@ -249,7 +249,7 @@ constexpr int kExItems = kExpandE / kExThreads;  // 8
 __global__ void k_gather_entries(const int32_t* __restrict__ rows, int64_t nb, const int64_t* __restrict__ anz,
                                  const int64_t* __restrict__ a_rp, const int32_t* __restrict__ a_col,
                                  const double* __restrict__ a_val, const int64_t* __restrict__ b_rp,
-                                 int32_t* __restrict__ e_k, double* __restrict__ e_a, int32_t* __restrict__ e_row,
+                                 int64_t* __restrict__ e_b, double* __restrict__ e_a, int32_t* __restrict__ e_row,
                                  int64_t* __restrict__ e_len) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -260,10 +260,11 @@ __global__ void k_gather_entries(const int32_t* __restrict__ rows, int64_t nb, c
     for (int64_t p = a_rp[r] + lane; p < a_rp[r + 1]; p += 32) {
       const int64_t i = base + (p - a_rp[r]);
       const int k = a_col[p];
-      e_k[i] = k;
+      const int64_t b0 = b_rp[k];
+      e_b[i] = b0;
       if (e_a) e_a[i] = a_val[p];
       e_row[i] = static_cast<int32_t>(h);
-      e_len[i] = b_rp[k + 1] - b_rp[k];
+      e_len[i] = b_rp[k + 1] - b0;
     }
   }
 }
@@ -300,45 +301,55 @@ __global__ void k_expand_bounds(const int64_t* __restrict__ e_off, int64_t n_e, 
   if (blockIdx.x == 0 && threadIdx.x == 0) bounds[n1 + n2] = total;
 }
 
-__global__ void k_expand_wg_entry(const int64_t* __restrict__ e_off, int64_t n_e, const int64_t* __restrict__ bounds,
-                                  int64_t n_wg, int32_t* __restrict__ wg_entry) {
+// Per work group: the entry holding its first product, how many entries it
+// touches and the batch row of the first one (what every thread of the group
+// needs first, found here once instead of by a search inside the group).
+__global__ void k_expand_wg_info(const int64_t* __restrict__ e_off, const int32_t* __restrict__ e_row, int64_t n_e,
+                                 const int64_t* __restrict__ bounds, int64_t n_wg, int4* __restrict__ info) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < n_wg; g += stride) {
-    const int64_t x = bounds[g];
-    wg_entry[g] = static_cast<int32_t>(x >= e_off[n_e] ? n_e - 1 : floor_index(e_off, 0, n_e - 1, x));
+    const int64_t x = bounds[g], end = bounds[g + 1];
+    const int64_t j0 = x >= e_off[n_e] ? n_e - 1 : floor_index(e_off, 0, n_e - 1, x);
+    int64_t ne = 0;
+    if (end > x) ne = floor_index(e_off, j0, min(n_e - 1, j0 + kExpandCap + 1), end - 1) - j0 + 1;
+    info[g] = make_int4(static_cast<int>(j0), static_cast<int>(ne), e_row[j0], 0);
   }
 }
 
+constexpr uint32_t kNoKey = 0xFFFFFFFFu;
+
+// One work group: products [S, end) of the batch in row order (at most
+// kExpandE of them, from at most kExpandCap + 2 A entries). Each thread
+// generates kExItems products (position k * T + tid), loading the B column and
+// value of all of them before the first is used; chunk keys are counted, the
+// chunks' global ranges reserved, and the products permuted through shared
+// memory so that each chunk's run is written contiguously. A product is carried
+// as one word: its key (local row * v + chunk) in the high 16 bits and its
+// column inside the chunk in the low 16 bits.
 template <bool VAL>
 __global__ void __launch_bounds__(kExThreads, 3) k_expand_split(ExpandArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int T = kExThreads;
-  const int E = kExpandE;
   const int nk = a.n_group_rows * a.v;
-  const Layout L = carve(smem, nk, a.n_group_rows, E, true);
+  const Layout L = carve(smem, nk, a.n_group_rows, kExpandE, true);
+  uint32_t* const pk_buf = reinterpret_cast<uint32_t*>(L.col_buf);
   // entry table after the multisplit layout
-  unsigned char* tail = reinterpret_cast<unsigned char*>(L.val_buf + E);
+  unsigned char* tail = reinterpret_cast<unsigned char*>(L.val_buf + kExpandE);
   int64_t* s_b = reinterpret_cast<int64_t*>(tail);                    // kExpandCap + 2
   double* s_a = reinterpret_cast<double*>(s_b + kExpandCap + 2);      // kExpandCap + 2
   int* s_lo = reinterpret_cast<int*>(s_a + kExpandCap + 2);           // kExpandCap + 2
-  __shared__ int s_ne;
-  __shared__ int64_t s_r0;
+  __shared__ int s_total;
 
   const int64_t g = blockIdx.x;
   const int64_t S = a.bounds[g];
   const int64_t end = a.bounds[g + 1];
+  const int4 info = a.wg_info[g];
   const int n = static_cast<int>(end - S);
   if (n <= 0) return;
-  const int64_t j0 = a.wg_entry[g];
-  if (threadIdx.x == 0) {
-    const int64_t j1 = floor_index(a.e_off, j0, min(a.n_e - 1, j0 + kExpandCap + 1), end - 1);
-    s_ne = static_cast<int>(j1 - j0 + 1);
-    s_r0 = a.e_row[j0];
-  }
-  __syncthreads();
-  const int ne = s_ne;
-  const int64_t r0 = s_r0;
-  if (ne > kExpandCap + 2) {  // bounds guarantee otherwise; never index past the table
+  const int64_t j0 = info.x;
+  const int ne = info.y;
+  const int64_t r0 = info.z;
+  if (ne < 1 || ne > kExpandCap + 2) {  // bounds guarantee otherwise; never index past the table
     if (threadIdx.x == 0) atomicOr(a.status, kStInternal);
     return;
   }
@@ -348,9 +359,11 @@ __global__ void __launch_bounds__(kExThreads, 3) k_expand_split(ExpandArgs a) {
     const int64_t lo = max(S, off);
     const int lo_loc = static_cast<int>(min(lo, end) - S);
     s_lo[i] = lo_loc;
-    s_b[i] = a.b_rp[a.e_k[j]] + (lo - off) - lo_loc;  // B index of local position p: s_b + p
+    s_b[i] = a.e_b[j] + (lo - off) - lo_loc;  // B index of local position p: s_b + p
     s_a[i] = VAL ? a.e_a[j] : 0.0;
   }
+  int* const s_ent = reinterpret_cast<int*>(L.col_buf);  // entry of each position (until the permute)
+  for (int q = threadIdx.x; q < kExpandE; q += T) s_ent[q] = -1;
   for (int k = threadIdx.x; k < nk; k += T) L.hist[k] = 0;
   for (int jr = threadIdx.x; jr < a.n_group_rows; jr += T) {
     const int64_t r = r0 + jr;
@@ -359,40 +372,71 @@ __global__ void __launch_bounds__(kExThreads, 3) k_expand_split(ExpandArgs a) {
     L.row_end[jr] = static_cast<int>(e);
   }
   __syncthreads();
-
-  // generate this thread's elements: position p = k * T + tid (consecutive across lanes)
-  int key[kExItems], col[kExItems], ent[kExItems];
-  bool bad = false;
-  int jw = 0;  // entry of the warp's first lane at the previous item
+  // entry of each product = the last non-empty entry starting at or before it:
+  // mark each non-empty entry at its first position, then a block-wide max scan
+  for (int i = threadIdx.x; i < ne; i += T) {
+    const int lo = s_lo[i];
+    if (i + 1 == ne || s_lo[i + 1] > lo) s_ent[lo] = i;
+  }
+  __syncthreads();
+  {
+    __shared__ int s_wmax[kExThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int4* const q4 = reinterpret_cast<int4*>(s_ent + threadIdx.x * kExItems);
+    int4 u0 = q4[0], u1 = q4[1];
+    u0.y = max(u0.y, u0.x); u0.z = max(u0.z, u0.y); u0.w = max(u0.w, u0.z);
+    u1.x = max(u1.x, u0.w); u1.y = max(u1.y, u1.x); u1.z = max(u1.z, u1.y); u1.w = max(u1.w, u1.z);
+    int inc = u1.w;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(kFull, inc, d);
+      if (lane >= d) inc = max(inc, y);
+    }
+    if (lane == 31) s_wmax[warp] = inc;
+    int carry = __shfl_up_sync(kFull, inc, 1);
+    if (lane == 0) carry = -1;
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) carry = max(carry, s_wmax[w]);
+    u0.x = max(u0.x, carry); u0.y = max(u0.y, carry); u0.z = max(u0.z, carry); u0.w = max(u0.w, carry);
+    u1.x = max(u1.x, carry); u1.y = max(u1.y, carry); u1.z = max(u1.z, carry); u1.w = max(u1.w, carry);
+    q4[0] = u0;
+    q4[1] = u1;
+  }
+  __syncthreads();
+  // all B loads of the thread in flight together
+  int32_t col[kExItems];
+  double vv[kExItems];
 #pragma unroll
   for (int k = 0; k < kExItems; ++k) {
     const int p = k * T + threadIdx.x;
-    key[k] = -1;
-    col[k] = 0;
-    ent[k] = 0;
-    // entry: largest i with s_lo[i] <= p, searched from the warp's last entry
-    int lo_j = __shfl_sync(kFull, jw, 0);
+    const int64_t bi = s_b[max(s_ent[p], 0)] + p;
+    col[k] = p < n ? a.b_col[bi] : 0;
+    if (VAL) vv[k] = p < n ? a.b_val[bi] : 0.0;
+  }
+  uint32_t pk[kExItems];
+  bool bad = false;
+  const uint32_t mask = (1u << a.shift) - 1u;
+#pragma unroll
+  for (int k = 0; k < kExItems; ++k) {
+    const int p = k * T + threadIdx.x;
+    pk[k] = kNoKey;
     if (p < n) {
-      if (lo_j + 1 < ne && s_lo[lo_j + 1] <= p) {
-        int hi_j = ne - 1;
-        while (lo_j < hi_j) {
-          const int mid = (lo_j + hi_j + 1) >> 1;
-          if (s_lo[mid] <= p) lo_j = mid; else hi_j = mid - 1;
-        }
-      }
-      ent[k] = lo_j;
-      col[k] = a.b_col[s_b[lo_j] + p];
       const int jr = local_row(L.row_end, a.n_group_rows, p);
-      if (jr < a.n_group_rows) key[k] = jr * a.v + (static_cast<uint32_t>(col[k]) >> a.shift);
-      else bad = true;
+      if (jr < a.n_group_rows) {
+        const uint32_t key = static_cast<uint32_t>(jr * a.v) + (static_cast<uint32_t>(col[k]) >> a.shift);
+        pk[k] = (key << 16) | (static_cast<uint32_t>(col[k]) & mask);
+      } else {
+        bad = true;
+      }
     }
-    jw = lo_j;
+    if (VAL) vv[k] *= s_a[max(s_ent[p], 0)];
   }
   if (bad) atomicOr(a.status, kStGroupRows);
 #pragma unroll
   for (int k = 0; k < kExItems; ++k) {
-    const unsigned heads = run_heads(key[k]);
-    if (key[k] >= 0 && ((heads >> (threadIdx.x & 31)) & 1u)) atomicAdd(&L.hist[key[k]], run_length(heads));
+    const int key = pk[k] == kNoKey ? -1 : static_cast<int>(pk[k] >> 16);
+    const unsigned heads = run_heads(key);
+    if (key >= 0 && ((heads >> (threadIdx.x & 31)) & 1u)) atomicAdd(&L.hist[key], run_length(heads));
   }
   __syncthreads();
   {
@@ -411,42 +455,33 @@ __global__ void __launch_bounds__(kExThreads, 3) k_expand_split(ExpandArgs a) {
       }
       pre += c;
     }
+    if (k0 < nk && k0 + per >= nk) s_total = pre;
   }
   __syncthreads();
   for (int k = threadIdx.x; k < nk; k += T) L.hist[k] = L.loff[k];
   __syncthreads();
   const int lane = threadIdx.x & 31;
-  int pos[kExItems];
 #pragma unroll
   for (int k = 0; k < kExItems; ++k) {
-    const unsigned heads = run_heads(key[k]);
+    const int key = pk[k] == kNoKey ? -1 : static_cast<int>(pk[k] >> 16);
+    const unsigned heads = run_heads(key);
     const int leader = run_head_lane(heads);
     int b = 0;
-    if (key[k] >= 0 && lane == leader) b = atomicAdd(&L.hist[key[k]], run_length(heads));
+    if (key >= 0 && lane == leader) b = atomicAdd(&L.hist[key], run_length(heads));
     b = __shfl_sync(kFull, b, leader);
-    pos[k] = b + (lane - leader);
-    if (key[k] >= 0) L.col_buf[pos[k]] = col[k];
-  }
-  if (VAL) {
-    double vv[kExItems];
-#pragma unroll
-    for (int k = 0; k < kExItems; ++k) {
-      const int p = k * T + threadIdx.x;
-      vv[k] = key[k] >= 0 ? s_a[ent[k]] * a.b_val[s_b[ent[k]] + p] : 0.0;
+    if (key >= 0) {
+      const int pos = b + (lane - leader);
+      pk_buf[pos] = pk[k];
+      if (VAL) L.val_buf[pos] = vv[k];
     }
-#pragma unroll
-    for (int k = 0; k < kExItems; ++k)
-      if (key[k] >= 0) L.val_buf[pos[k]] = vv[k];
   }
   __syncthreads();
-  const int32_t mask = static_cast<int32_t>((1u << a.shift) - 1u);
-  for (int i = threadIdx.x; i < n; i += T) {
-    const int32_t c = L.col_buf[i];
-    const int j = local_row(L.row_end, a.n_group_rows, i);
-    if (j >= a.n_group_rows) continue;
-    const int kk = j * a.v + (static_cast<uint32_t>(c) >> a.shift);
+  const int placed = s_total;
+  for (int i = threadIdx.x; i < placed; i += T) {
+    const uint32_t q = pk_buf[i];
+    const int kk = static_cast<int>(q >> 16);
     const int64_t dest = L.gpos[kk] + (i - L.loff[kk]);
-    a.out_col[dest] = c & mask;
+    a.out_col[dest] = static_cast<int32_t>(q & 0xFFFFu);
     if (VAL) a.out_val[dest] = L.val_buf[i];
   }
 }
@@ -459,11 +494,16 @@ size_t expand_smem_bytes(int v, int ngr) {
 
 int expand_group_rows(int64_t tau) { return static_cast<int>((kExpandE - 1 + tau) / (tau + 1) + 1); }
 
+bool expand_fits(int v, int64_t w, int64_t tau, size_t smem) {
+  const int64_t nk = static_cast<int64_t>(expand_group_rows(tau)) * v;
+  return v >= 1 && w >= 1 && w <= 65536 && nk < 65535 && expand_smem_bytes(v, expand_group_rows(tau)) + 1024 <= smem;
+}
+
 void launch_gather_entries(const int32_t* heavy_rows, int64_t nb, const int64_t* anz_batch, const int64_t* a_rp,
-                           const int32_t* a_col, const double* a_val, const int64_t* b_rp, int32_t* e_k,
+                           const int32_t* a_col, const double* a_val, const int64_t* b_rp, int64_t* e_b,
                            double* e_a, int32_t* e_row, int64_t* e_len, cudaStream_t s) {
   if (nb <= 0) return;
-  (k_gather_entries<<<grid_for(nb * 32, 256), 256, 0, s>>>(heavy_rows, nb, anz_batch, a_rp, a_col, a_val, b_rp, e_k,
+  (k_gather_entries<<<grid_for(nb * 32, 256), 256, 0, s>>>(heavy_rows, nb, anz_batch, a_rp, a_col, a_val, b_rp, e_b,
                                                            e_a, e_row, e_len), note_launch());
 }
 
@@ -471,11 +511,12 @@ int64_t expand_num_wg(int64_t total, int64_t n_e) {
   return (total + kExpandE - 1) / kExpandE + (n_e + kExpandCap - 1) / kExpandCap;
 }
 
-void launch_expand_bounds(const int64_t* e_off, int64_t n_e, int64_t total, int64_t* bounds, int32_t* wg_entry,
-                          cudaStream_t s) {
+void launch_expand_bounds(const int64_t* e_off, const int32_t* e_row, int64_t n_e, int64_t total, int64_t* bounds,
+                          int4* wg_info, cudaStream_t s) {
   const int64_t n1 = (total + kExpandE - 1) / kExpandE, n2 = (n_e + kExpandCap - 1) / kExpandCap;
   (k_expand_bounds<<<grid_for(n1 + n2, 256), 256, 0, s>>>(e_off, n_e, total, n1, n2, bounds), note_launch());
-  (k_expand_wg_entry<<<grid_for(n1 + n2, 256), 256, 0, s>>>(e_off, n_e, bounds, n1 + n2, wg_entry), note_launch());
+  (k_expand_wg_info<<<grid_for(n1 + n2, 256), 256, 0, s>>>(e_off, e_row, n_e, bounds, n1 + n2, wg_info),
+   note_launch());
 }
 
 void launch_expand_split(const ExpandArgs& a, cudaStream_t s) {

@@ -6,9 +6,11 @@
 //   chunk of width w, or the whole row) is a popcount over the range. Used for
 //   the heavy rows when the hierarchy has at most one level, so the symbolic pass
 //   needs neither the outer product nor the multisplit.
-// * Numeric (light rows): prefix sums over groups of 8 bitmap words give every
-//   column its rank, i.e. its slot in the sorted row; products are summed into
-//   that slot and the row is written in column order with no sort.
+// * Light rows (symbolic and numeric): the row's products are spread evenly over
+//   the block and held in registers; in the numeric pass prefix sums over groups
+//   of 8 bitmap words give every column its rank, i.e. its slot in the sorted
+//   row; products are summed into that slot and the row is written in column
+//   order with no sort.
 //
 // Rows are taken from a global work counter (dynamic scheduling; no waiting).
 #include <algorithm>
@@ -171,28 +173,127 @@ __global__ void __launch_bounds__(kRbThreads) k_rowbm_symbolic(RowBitmapArgs a, 
 }
 
 constexpr int kGroupWords = 8;  // rank prefix kept per 8 bitmap words (256 columns)
+constexpr int kRlItems = 10;    // products per thread in k_rowbm_light: rows of up to 10240 products
+constexpr uint32_t kNoCol = 0xFFFFFFFFu;
+constexpr int64_t kLightSymRegion = 32768;  // entry-table bytes of the symbolic light kernel
 
-__global__ void __launch_bounds__(kRbThreads) k_rowbm_numeric(RowBitmapArgs a, int nwords, int cap) {
+// Light rows (u <= kRbThreads * kRlItems) with a whole-row bitmap, every product
+// held in registers: thread t takes products t, t + T, ... of the row in row
+// order, so the block's work is balanced whatever the lengths of the B rows.
+// The row's A entries are staged in shared memory (B row start, A value, and a
+// prefix of the B row lengths, te_cap entries at a time); a product finds its
+// entry by binary search over that prefix. All B loads of a thread are issued
+// before the first is used. The products' columns set the bitmap; then
+//  * symbolic: the row's nnz is the bitmap's popcount (written to c_rp[row]);
+//  * numeric: prefix sums over groups of 8 words give every column its rank,
+//    the values are summed into their rank in shared memory (the entry table's
+//    space is reused) and the row is written in column order.
+template <bool SYM>
+__global__ void __launch_bounds__(kRbThreads, 1)
+    k_rowbm_light(RowBitmapArgs a, int nwords, int cap, int te_cap, int region_bytes) {
   extern __shared__ __align__(16) unsigned char smem[];
-  double* vals = reinterpret_cast<double*>(smem);                         // cap (rounded to even)
-  uint32_t* bm = reinterpret_cast<uint32_t*>(vals + ((cap + 1) & ~1));    // ngroups * 8 words
+  int64_t* s_bs = reinterpret_cast<int64_t*>(smem);                       // te_cap
+  double* s_av = reinterpret_cast<double*>(s_bs + te_cap);                // te_cap (numeric)
+  int* s_pre = reinterpret_cast<int*>(SYM ? static_cast<void*>(s_bs + te_cap) : static_cast<void*>(s_av + te_cap));
+  double* vals = reinterpret_cast<double*>(smem);                         // numeric, after the walk
   const int ngroups = (nwords + kGroupWords - 1) / kGroupWords;
-  int* gpre = reinterpret_cast<int*>(bm + ngroups * kGroupWords);         // ngroups
+  uint32_t* bm = reinterpret_cast<uint32_t*>(smem + region_bytes);        // ngroups * kGroupWords
+  int* gpre = reinterpret_cast<int*>(bm + ngroups * kGroupWords);         // ngroups (numeric)
   __shared__ int64_t s_item;
   __shared__ int ws[33];
-  __shared__ LongRows longs;
-  const int per = (ngroups + blockDim.x - 1) / blockDim.x;
-  const int g0 = threadIdx.x * per, g1 = min(ngroups, g0 + per);
+  constexpr int T = kRbThreads;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per_g = (ngroups + T - 1) / T;
+  const int g0 = threadIdx.x * per_g, g1 = min(ngroups, g0 + per_g);
   while (true) {
     if (threadIdx.x == 0) s_item = atomicAdd(a.work_counter, 1u);
     __syncthreads();
     const int64_t item = s_item;
     if (item >= a.n_items) break;
     const int64_t r = a.rows[item];
+    const int64_t lo = a.a_rp[r], ne = a.a_rp[r + 1] - lo;
     zero_words(bm, ngroups * kGroupWords);
+    uint32_t col[kRlItems];
+    double val[kRlItems];
+#pragma unroll
+    for (int k = 0; k < kRlItems; ++k) {
+      col[k] = kNoCol;
+      val[k] = 0.0;
+    }
+    int64_t P0 = 0;  // products of the earlier entry tiles
+    for (int64_t e0 = 0; e0 < ne; e0 += te_cap) {
+      const int nt = static_cast<int>(min(static_cast<int64_t>(te_cap), ne - e0));
+      __syncthreads();  // the previous tile's table is no longer read
+      for (int i = threadIdx.x; i < nt; i += T) {
+        const int64_t p = lo + e0 + i;
+        const int kb = a.a_col[p];
+        const int64_t bs = a.b_rp[kb];
+        s_bs[i] = bs;
+        s_pre[i] = static_cast<int>(a.b_rp[kb + 1] - bs);
+        if (!SYM) s_av[i] = a.a_val[p];
+      }
+      __syncthreads();
+      int tot;
+      {
+        const int per = (nt + T - 1) / T;
+        const int i0 = threadIdx.x * per, i1 = min(nt, i0 + per);
+        int acc = 0;
+        for (int i = i0; i < i1; ++i) acc += s_pre[i];
+        int run = block_exclusive_scan(acc, ws, &tot);
+        for (int i = i0; i < i1; ++i) {
+          const int x = s_pre[i];
+          s_pre[i] = run;
+          run += x;
+        }
+      }
+      __syncthreads();
+      int ent[kRlItems];
+      int e_prev = 0;
+#pragma unroll
+      for (int k = 0; k < kRlItems; ++k) {
+        const int64_t rel = static_cast<int64_t>(k) * T + threadIdx.x - P0;
+        ent[k] = -1;
+        if (rel >= 0 && rel < tot) {
+          int lo_i = e_prev, hi_i = nt - 1;  // largest i with s_pre[i] <= rel (a non-empty entry)
+          while (lo_i < hi_i) {
+            const int mid = (lo_i + hi_i + 1) >> 1;
+            if (s_pre[mid] <= rel) lo_i = mid; else hi_i = mid - 1;
+          }
+          e_prev = lo_i;
+          ent[k] = lo_i;
+          const int64_t bi = s_bs[lo_i] + (rel - s_pre[lo_i]);
+          col[k] = static_cast<uint32_t>(a.b_col[bi]);
+          if (!SYM) val[k] = a.b_val[bi];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kRlItems; ++k) {
+        if (ent[k] >= 0) {
+          if (!SYM) val[k] *= s_av[ent[k]];
+          atomicOr(&bm[col[k] >> 5], 1u << (col[k] & 31));
+        }
+      }
+      P0 += tot;
+    }
     __syncthreads();
-    mark_row(a, r, bm, longs);
-    __syncthreads();
+    if (P0 > static_cast<int64_t>(T) * kRlItems) {  // more products than the registers hold
+      if (threadIdx.x == 0) atomicOr(a.status, kStInternal);
+      continue;  // uniform: every thread saw the same P0
+    }
+    if (SYM) {
+      int n = 0;
+      for (int w = threadIdx.x; w < nwords; w += T) n += __popc(bm[w]);
+      n = warp_reduce_sum(n);
+      if (lane == 0) ws[warp] = n;
+      __syncthreads();
+      if (warp == 0) {
+        int t = lane < T / 32 ? ws[lane] : 0;
+        t = warp_reduce_sum(t);
+        if (lane == 0) a.c_rp[r] = t;
+      }
+      __syncthreads();
+      continue;
+    }
     int acc = 0;
     for (int g = g0; g < g1; ++g)
       for (int w = 0; w < kGroupWords; ++w) acc += __popc(bm[g * kGroupWords + w]);
@@ -204,33 +305,24 @@ __global__ void __launch_bounds__(kRbThreads) k_rowbm_numeric(RowBitmapArgs a, i
     }
     const bool fits = nnz <= cap;
     if (!fits && threadIdx.x == 0) atomicOr(a.status, kStInternal);
-    for (int i = threadIdx.x; i < min(nnz, cap); i += blockDim.x) vals[i] = 0.0;
+    for (int i = threadIdx.x; i < min(nnz, cap); i += T) vals[i] = 0.0;
     __syncthreads();
     if (fits) {
-      walk_products<true>(a, r, longs, [&](const int64_t (&q)[4], double av) {
-        uint32_t c[4];
-        double bv[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          c[u] = q[u] >= 0 ? static_cast<uint32_t>(a.b_col[q[u]]) : 0u;
-          bv[u] = q[u] >= 0 ? a.b_val[q[u]] : 0.0;
+      for (int k = 0; k < kRlItems; ++k) {
+        if (col[k] != kNoCol) {
+          const uint32_t cc = col[k];
+          const int w = cc >> 5, g = w / kGroupWords;
+          int rank = gpre[g] + __popc(bm[w] & ((1u << (cc & 31)) - 1u));
+          for (int x = g * kGroupWords; x < w; ++x) rank += __popc(bm[x]);
+          atomicAdd(&vals[rank], val[k]);
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (q[u] >= 0) {
-            const uint32_t cc = c[u];
-            const int w = cc >> 5, g = w / kGroupWords;
-            int rank = gpre[g] + __popc(bm[w] & ((1u << (cc & 31)) - 1u));
-            for (int x = g * kGroupWords; x < w; ++x) rank += __popc(bm[x]);
-            atomicAdd(&vals[rank], av * bv[u]);
-          }
-        }
-      });
+      }
     }
     __syncthreads();
     if (fits) {  // words round-robin over threads: balanced emission, adjacent output ranges per warp
       const int64_t out = a.c_rp[r];
-      for (int w = threadIdx.x; w < nwords; w += blockDim.x) {
+      for (int w = threadIdx.x; w < nwords; w += T) {
         uint32_t bits = bm[w];
         if (!bits) continue;
         const int g = w / kGroupWords;
@@ -249,30 +341,49 @@ __global__ void __launch_bounds__(kRbThreads) k_rowbm_numeric(RowBitmapArgs a, i
   }
 }
 
+int64_t light_region_bytes(int cap, bool symbolic) {
+  return symbolic ? kLightSymRegion : static_cast<int64_t>((cap + 1) & ~1) * 8;
+}
+
 }  // namespace
 
 int64_t rowbm_symbolic_smem(int64_t c_m) { return ((c_m + 127) / 128) * 16; }
 
-int64_t rowbm_numeric_smem(int64_t c_m, int cap) {
+int64_t rowbm_light_smem(int64_t c_m, int cap, bool symbolic) {
   const int64_t nwords = (c_m + 31) / 32;
   const int64_t ngroups = (nwords + kGroupWords - 1) / kGroupWords;
-  return static_cast<int64_t>((cap + 1) & ~1) * 8 + ngroups * kGroupWords * 4 + ngroups * 4;
+  return light_region_bytes(cap, symbolic) + ngroups * kGroupWords * 4 + (symbolic ? 0 : ngroups * 4);
 }
 
-void launch_rowbm(const RowBitmapArgs& a, bool symbolic, int cap, int num_sms, int64_t smem_max, cudaStream_t s) {
+bool rowbm_light_fits(int64_t c_m, int cap, bool symbolic, int64_t smem_max) {
+  return cap >= 1 && cap <= kRbThreads * kRlItems && c_m <= (int64_t(1) << 31) &&
+         rowbm_light_smem(c_m, cap, symbolic) + 4096 <= smem_max;
+}
+
+void launch_rowbm_light(const RowBitmapArgs& a, bool symbolic, int cap, int num_sms, cudaStream_t s) {
+  if (a.n_items <= 0) return;
+  cudaMemsetAsync(a.work_counter, 0, sizeof(unsigned int), s);
+  const int nwords = static_cast<int>((a.c_m + 31) / 32);
+  const int64_t region = light_region_bytes(cap, symbolic);
+  const int te_cap = static_cast<int>((region - 8) / (symbolic ? 12 : 20));
+  const size_t smem = static_cast<size_t>(rowbm_light_smem(a.c_m, cap, symbolic));
+  const int64_t blocks = std::min<int64_t>(a.n_items, num_sms);
+  auto fn = symbolic ? k_rowbm_light<true> : k_rowbm_light<false>;
+  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  (fn<<<static_cast<unsigned>(blocks), kRbThreads, smem, s>>>(a, nwords, cap, te_cap, static_cast<int>(region)),
+   note_launch());
+}
+
+void launch_rowbm(const RowBitmapArgs& a, int num_sms, int64_t smem_max, cudaStream_t s) {
   if (a.n_items <= 0) return;
   cudaMemsetAsync(a.work_counter, 0, sizeof(unsigned int), s);
   const int64_t nwords4 = ((a.c_m + 127) / 128) * 4;  // whole uint4 stores
-  const size_t smem = static_cast<size_t>(symbolic ? rowbm_symbolic_smem(a.c_m) : rowbm_numeric_smem(a.c_m, cap));
+  const size_t smem = static_cast<size_t>(rowbm_symbolic_smem(a.c_m));
   const int per_sm = std::max<int>(1, static_cast<int>(smem_max / static_cast<int64_t>(smem + 1024)));
   const int64_t blocks = std::min<int64_t>(a.n_items, static_cast<int64_t>(num_sms) * std::min(per_sm, 2));
-  if (symbolic) {
-    cudaFuncSetAttribute(k_rowbm_symbolic, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    (k_rowbm_symbolic<<<static_cast<unsigned>(blocks), kRbThreads, smem, s>>>(a, static_cast<int>(nwords4)), note_launch());
-  } else {
-    cudaFuncSetAttribute(k_rowbm_numeric, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    (k_rowbm_numeric<<<static_cast<unsigned>(blocks), kRbThreads, smem, s>>>(a, static_cast<int>((a.c_m + 31) / 32), cap), note_launch());
-  }
+  cudaFuncSetAttribute(k_rowbm_symbolic, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  (k_rowbm_symbolic<<<static_cast<unsigned>(blocks), kRbThreads, smem, s>>>(a, static_cast<int>(nwords4)),
+   note_launch());
 }
 
 }  // namespace gm

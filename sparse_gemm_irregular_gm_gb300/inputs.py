@@ -229,9 +229,9 @@ def row_slice(M: CSR, lo: int, hi: int) -> CSR:
 
 # Products of two different matrices: (description, generator of (A, B)). C = A @ B.
 PAIRS = {
-    "rmat20_rows8k": ("A[2^19 : 2^19 + 8192, :] * A, A = R-MAT scale 20, edge factor 16 (profiling case: "
+    "rmat20_rows2k": ("A[2^19 : 2^19 + 2048, :] * A, A = R-MAT scale 20, edge factor 16 (profiling case: "
                       "C.m = 2^20 at a few GB)",
-                      lambda seed=1: (lambda A: (row_slice(A, 1 << 19, (1 << 19) + 8192), A))(rmat(20, 16, seed=seed))),
+                      lambda seed=1: (lambda A: (row_slice(A, 1 << 19, (1 << 19) + 2048), A))(rmat(20, 16, seed=seed))),
 }
 
 

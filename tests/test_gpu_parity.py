@@ -262,6 +262,43 @@ def test_fig1_worked_example_on_gpu():
         assert cval[crp[i]:crp[i + 1]].tolist() == [sum(prod(s) for s in labels) for _, labels in entries]
 
 
+def _light_rows_case(n_cols, seed):
+    """A with rows whose products fill every light bin (u from 1 to tau) and one
+    heavy row, some with thousands of A entries (several entry tiles of the
+    light-row kernels) and with empty B rows among the selected ones; B rows of
+    length 0, 1, 2 and a few long ones (1500). Integer values."""
+    rng = np.random.default_rng(seed)
+    nb = 12000
+    lens = np.ones(nb, np.int64)
+    lens[::7] = 2
+    lens[5::97] = 0
+    lens[:6] = 1500
+    b_rp = np.zeros(nb + 1, np.int64)
+    np.cumsum(lens, out=b_rp[1:])
+    b_col = np.concatenate([np.sort(rng.choice(n_cols, int(l), replace=False)) for l in lens]).astype(np.int32)
+    B = gi.CSR(nb, n_cols, b_rp, b_col, rng.integers(-3, 4, b_col.size).astype(np.float64))
+    rows = []
+    for target in (1, 17, 40, 100, 200, 500, 1000, 1500, 3000, 5000, 7000, 7900, 8450, 9686):
+        cols = list(rng.choice(np.arange(6, nb), min(target, nb - 6), replace=False))
+        rows.append(cols)
+    rows.append([0, 1, 2, 3, 4] + list(rng.choice(np.arange(6, nb), 40, replace=False)))  # long B rows
+    rows.append(list(range(5, nb, 97))[:50] + [6, 7, 8])  # mostly empty B rows
+    a_rp = np.zeros(len(rows) + 1, np.int64)
+    np.cumsum([len(r) for r in rows], out=a_rp[1:])
+    a_col = np.concatenate([np.sort(np.asarray(r)) for r in rows]).astype(np.int32)
+    A = gi.CSR(len(rows), nb, a_rp, a_col, rng.integers(-3, 4, a_col.size).astype(np.float64))
+    return A, B
+
+
+@pytest.mark.parametrize("n_cols", [1 << 20, 3000])
+def test_light_rows_every_bin_and_entry_tiles(n_cols):
+    A, B = _light_rows_case(n_cols, seed=n_cols % 97)
+    u = oracle.ip_counts(A, B)
+    assert u.max() > 9685 and ((u > 1024) & (u <= 9685)).sum() >= 5
+    info = check_full(A, B, exact=True)
+    assert info.n_heavy_rows == int((u > info.params.tau).sum())
+
+
 # --- the workloads ------------------------------------------------------------------
 
 def test_workload_rmat10_fp64_and_int():
