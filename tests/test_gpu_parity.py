@@ -299,6 +299,54 @@ def test_light_rows_every_bin_and_entry_tiles(n_cols):
     assert info.n_heavy_rows == int((u > info.params.tau).sum())
 
 
+def _rows_of(M, rows):
+    rows = np.asarray(rows, dtype=np.int64)
+    lens = M.row_ptr[rows + 1] - M.row_ptr[rows]
+    rp = np.zeros(rows.size + 1, np.int64)
+    np.cumsum(lens, out=rp[1:])
+    idx = np.concatenate([np.arange(M.row_ptr[r], M.row_ptr[r + 1]) for r in rows])
+    return gi.CSR(rows.size, M.n_cols, rp, M.col[idx].copy(), M.val[idx].copy())
+
+
+def test_large_chunks_many_tiles_exact():
+    """The heaviest rows of a scale-16 R-MAT times the whole matrix: chunks of
+    tens of thousands of elements (many 4096-element tiles of the large-chunk
+    accumulator) with the R-MAT's hot columns; integer values, so exact."""
+    A = gi.rmat(16, 16, seed=3, values="int")
+    u = oracle.ip_counts(A, A)
+    rows = np.concatenate([np.argsort(u)[-40:], np.random.default_rng(0).choice(A.n_rows, 40, replace=False)])
+    As = _rows_of(A, rows)
+    info = check_full(As, A, exact=True)
+    assert info.n_heavy_rows >= 40 and u[rows].max() > 16 * 4096
+
+
+@pytest.mark.parametrize("n_hot", [5000, 13000])
+def test_chunk_with_one_hot_column(n_hot):
+    """A chunk whose elements nearly all fall on one column: one run of equal rank
+    crosses every thread of every tile. Row 0: n_hot products on column 7; row 1:
+    the same plus products spread over the chunk; integer values."""
+    rng = np.random.default_rng(n_hot)
+    n_cols = 40000  # 4 chunks of 16384 at the default dense width
+    nb = n_hot + 3000
+    b_lens = np.ones(nb, np.int64)
+    b_lens[n_hot:] = 3
+    b_rp = np.zeros(nb + 1, np.int64)
+    np.cumsum(b_lens, out=b_rp[1:])
+    b_col = np.full(int(b_rp[-1]), 7, np.int32)
+    tail = b_col[b_rp[n_hot]:]
+    tail[:] = rng.integers(0, n_cols, tail.size).astype(np.int32)
+    for k in range(n_hot, nb):  # distinct columns inside each B row
+        seg = b_col[b_rp[k]:b_rp[k + 1]]
+        seg[:] = np.sort(rng.choice(n_cols, seg.size, replace=False))
+    B = gi.CSR(nb, n_cols, b_rp, b_col, rng.integers(-3, 4, b_col.size).astype(np.float64))
+    r0 = np.arange(n_hot)
+    r1 = np.arange(nb)
+    a_col = np.concatenate([r0, r1]).astype(np.int32)
+    A = gi.CSR(2, nb, np.array([0, r0.size, r0.size + r1.size], np.int64), a_col,
+               rng.integers(1, 4, a_col.size).astype(np.float64))
+    check_full(A, B, exact=True, tau=64)
+
+
 # --- the workloads ------------------------------------------------------------------
 
 def test_workload_rmat10_fp64_and_int():
