@@ -301,6 +301,8 @@ struct gm_plan {
   int64_t c_m = 1;
   bool sym_rowbm = false;  // heavy symbolic through whole-row bitmaps
   bool rowwise = false;    // numeric heavy path: row-order expansion fused with the multisplit
+  bool b_sorted = false;   // every row of B has non-decreasing columns (runs per chunk are contiguous)
+  int32_t b_unsorted_h = 0;
   gm_params P{};
   int L = 0;
   int state = 0;  // 1 analyzed, 2 symbolic done, 3 numeric done
@@ -318,6 +320,7 @@ struct gm_plan {
   gm::DevBuf<int64_t> heavy_ids64;  // x_heavy as int64
   gm::DevBuf<int64_t> anz;          // prefix of nnz(A[x_heavy[h], :]) (n_heavy + 1)
   gm::DevBuf<int64_t> cnt0;         // row-order pipeline: elements of each level-0 chunk (n_heavy * v0)
+  gm::DevBuf<int32_t> bcp;          // row-order pipeline: per-B-row level-0 chunk starts (B.n_rows * (v0 + 1))
   std::vector<int64_t> h_chat_rp;   // host copy of chat_rp
   std::vector<int64_t> h_anz;       // prefix of nnz(A[x_heavy[h], :])
   gm::GrowBuf nnz[GM_MAX_LEVELS];        // per level, per child: nnz (symbolic) then output offset
@@ -429,6 +432,16 @@ static gm_status analyze_impl(gm_plan* p) {
   launch_validate_cols(p->B.col_idx, p->B.nnz, p->B.n_cols, kStBadBCol, p->status.p, s);
   gm_status st = sync_check(p);
   if (st != GM_OK) return st;
+  {  // is every B row sorted? (decides how heavy products are scattered into chunks)
+    DevBuf<int> flag;
+    if (!flag.alloc(1, s)) return GM_ERR_OOM;
+    cudaMemsetAsync(flag.p, 0, sizeof(int), s);
+    launch_check_sorted(p->B.row_ptr, p->B.col_idx, p->B.n_rows, flag.p, s);
+    cudaMemcpyAsync(&p->b_unsorted_h, flag.p, sizeof(int), cudaMemcpyDeviceToHost, s);
+    st = sync_check(p);
+    if (st != GM_OK) return st;
+    p->b_sorted = p->b_unsorted_h == 0;
+  }
 
   BinSpec spec{};
   spec.nbins = kRowBins;
@@ -564,6 +577,102 @@ static void dbg_copy(DevBuf<T>& dst, const T* src, int64_t n, cudaStream_t s) {
 // batch's A entries are gathered in row order, their products expanded straight
 // into the level-0 chunks (k_expand_split; C-hat is not written) whose sizes the
 // symbolic pass counted, then every chunk is accumulated.
+// Accumulates the level-0 chunks of heavy batch rows [h0, h1) (already filled,
+// sizes mcount) into C: the numeric leaves of the one-level hierarchy.
+static gm_status rowwise_leaves(gm_plan* p, int64_t nb, const int64_t* rrp, const int64_t* mcount, int64_t* par_base,
+                                int32_t* c_col, double* c_val) {
+  const int v = static_cast<int>(p->P.v_chunks[0]);
+  ListArgs la{};
+  la.status = p->status.p;
+  la.c_col = c_col;
+  la.c_val = c_val;
+  la.rp = rrp;
+  la.col = p->arena_col[0].p;
+  la.val = p->arena_val[0].p;
+  la.child_base = par_base[0] * v;
+  la.v = v;
+  la.width = p->P.widths[0];
+  la.nnz_out = p->nnz[0].p;
+  la.off_in = p->nnz[0].p;
+  const int t = p->stage_begin(GM_STAGE_NUM_HEAVY);
+  const gm_status st = run_leaves(p, la, mcount, 0, nb * v, true, true);
+  p->stage_end(t);
+  par_base[0] += nb;
+  if (st != GM_OK) return st;
+  return cuda_status(p, cudaGetLastError());
+}
+
+// Row-order pipeline when B's rows are sorted: the batch rows' A entries are
+// transposed (masked CSR -> CSC, as for the outer product) and the outer
+// product writes every product straight into its level-0 chunk, reserving one
+// range per run of an entry's B row inside a chunk (k_outer_warp). C-hat is
+// never written; chunk sizes come from the symbolic pass.
+static gm_status run_batch_runs(gm_plan* p, int64_t h0, int64_t h1, int64_t* par_base, int32_t* c_col,
+                                double* c_val) {
+  const cudaStream_t s = p->s;
+  const int64_t nb = h1 - h0;
+  const int64_t ip = p->h_chat_rp[h1] - p->h_chat_rp[h0];
+  const int64_t anz = p->h_anz[h1] - p->h_anz[h0];
+  const int32_t* heavy = p->rows_by_bin.p + p->bin_start[kHeavyBin] + h0;
+  const int64_t ncols = p->A.n_cols;
+  const int v = static_cast<int>(p->P.v_chunks[0]);
+  const int64_t children = nb * v;
+  if (p->arena_col[0].n < static_cast<size_t>(ip) || p->arena_val[0].n < static_cast<size_t>(ip))
+    return GM_ERR_WORKSPACE;
+
+  int t = p->stage_begin(GM_STAGE_TRANSPOSE);
+  DevBuf<int64_t> col_ptr, slice_off;
+  DevBuf<int32_t> t_row, wg_op;
+  DevBuf<double> t_val;
+  const int64_t n_wg_op = (ip + kOuterE - 1) / kOuterE;
+  if (!col_ptr.alloc(ncols + 1, s) || !slice_off.alloc(ncols + 1, s) || !t_row.alloc(anz, s) ||
+      !t_val.alloc(anz, s) || !wg_op.alloc(n_wg_op, s))
+    return GM_ERR_OOM;
+  TransposeArgs ta{heavy, nb, p->A.row_ptr, p->A.col_idx, p->A.vals, ncols};
+  if (!masked_transpose(ta, anz, col_ptr.p, t_row.p, t_val.p, s)) return GM_ERR_OOM;
+  if (!slice_offsets(col_ptr.p, p->B.row_ptr, ncols, slice_off.p, s)) return GM_ERR_OOM;
+  launch_wg_slice(slice_off.p, ncols, ip, kOuterE, wg_op.p, s);
+  p->stage_end(t);
+
+  t = p->stage_begin(GM_STAGE_HISTOGRAM);
+  const int64_t* mcount = p->cnt0.p + h0 * v;  // chunk sizes from the symbolic pass
+  DevBuf<int64_t> rrp;
+  DevBuf<unsigned long long> cur;
+  if (!rrp.alloc(children + 1, s) || !cur.alloc(children, s)) return GM_ERR_OOM;
+  if (!scan_exclusive_i64(mcount, rrp.p, children, rrp.p + children, s)) return GM_ERR_OOM;
+  sub_to_u64(rrp.p, children, 0, cur.p, s);
+  p->stage_end(t);
+
+  t = p->stage_begin(GM_STAGE_MULTISPLIT);
+  OuterArgs oa{};
+  oa.slice_off = slice_off.p;
+  oa.col_ptr = col_ptr.p;
+  oa.t_row = t_row.p;
+  oa.t_val = t_val.p;
+  oa.b_rp = p->B.row_ptr;
+  oa.b_col = p->B.col_idx;
+  oa.b_val = p->B.vals;
+  oa.n_slices = ncols;
+  oa.total = ip;
+  oa.E = kOuterE;
+  oa.wg_first = wg_op.p;
+  oa.cursor = cur.p;
+  oa.out_col = p->arena_col[0].p;
+  oa.out_val = p->arena_val[0].p;
+  oa.v = v;
+  oa.shift = ilog2(p->P.widths[0]);
+  oa.bcp = p->bcp.p;
+  launch_outer_split(oa, s);
+  p->stage_end(t);
+  t_row.release();
+  t_val.release();
+  col_ptr.release();
+  slice_off.release();
+  wg_op.release();
+  cur.release();
+  return rowwise_leaves(p, nb, rrp.p, mcount, par_base, c_col, c_val);
+}
+
 static gm_status run_batch_rowwise(gm_plan* p, int64_t h0, int64_t h1, int64_t* par_base, int32_t* c_col,
                                    double* c_val) {
   const cudaStream_t s = p->s;
@@ -575,6 +684,7 @@ static gm_status run_batch_rowwise(gm_plan* p, int64_t h0, int64_t h1, int64_t* 
   const int64_t children = nb * v;
   if (p->arena_col[0].n < static_cast<size_t>(ip)) return GM_ERR_WORKSPACE;
 
+  if (p->b_sorted) return run_batch_runs(p, h0, h1, par_base, c_col, c_val);
   if (ne >= INT32_MAX) return GM_ERR_INDEX_OVERFLOW;  // entries are indexed by int32 inside the kernels
   int t = p->stage_begin(GM_STAGE_TRANSPOSE);
   DevBuf<int32_t> e_row;
@@ -630,25 +740,8 @@ static gm_status run_batch_rowwise(gm_plan* p, int64_t h0, int64_t h1, int64_t* 
   e_a.release();
   e_row.release();
   e_off.release();
-
-  ListArgs la{};
-  la.status = p->status.p;
-  la.c_col = c_col;
-  la.c_val = c_val;
-  la.rp = rrp.p;
-  la.col = p->arena_col[0].p;
-  la.val = p->arena_val[0].p;
-  la.child_base = par_base[0] * v;
-  la.v = v;
-  la.width = p->P.widths[0];
-  la.nnz_out = p->nnz[0].p;
-  la.off_in = p->nnz[0].p;
-  t = p->stage_begin(GM_STAGE_NUM_HEAVY);
-  const gm_status st = run_leaves(p, la, mcount, 0, children, true, true);
-  p->stage_end(t);
-  par_base[0] += nb;
-  if (st != GM_OK) return st;
-  return cuda_status(p, cudaGetLastError());
+  cur.release();
+  return rowwise_leaves(p, nb, rrp.p, mcount, par_base, c_col, c_val);
 }
 
 // Heavy rows [h0, h1): outer product, multisplit levels and chunk accumulation.
@@ -678,7 +771,7 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
   TransposeArgs ta{heavy, nb, p->A.row_ptr, p->A.col_idx, p->A.vals, ncols};
   if (!masked_transpose(ta, anz, col_ptr.p, t_row.p, t_val.p, s)) return GM_ERR_OOM;
   if (!slice_offsets(col_ptr.p, p->B.row_ptr, ncols, slice_off.p, s)) return GM_ERR_OOM;
-  launch_wg_slice(slice_off.p, ncols, kOuterE, wg_op.p, s);
+  launch_wg_slice(slice_off.p, ncols, ip, kOuterE, wg_op.p, s);
   p->stage_end(t);
 
   // 2. Outer product into C-hat (Algorithm 4), optionally counting level-0 chunks.
@@ -1083,10 +1176,11 @@ static gm_status symbolic_impl(gm_plan* p, int64_t* C_rp, int64_t* C_nnz) {
       const int ts = p->stage_begin(GM_STAGE_SYM_HEAVY);
       launch_rowbm(ra, p->num_sms, p->smem_dev, s);
       if (p->rowwise) {  // element counts of the level-0 chunks, for the numeric pass
-        if (!p->cnt0.alloc(nh * v0, s)) return GM_ERR_OOM;
+        if (!p->cnt0.alloc(nh * v0, s) || !p->bcp.alloc(std::max<int64_t>(p->B.n_rows, 1) * (v0 + 1), s))
+          return GM_ERR_OOM;
         if (!heavy_chunk_counts(p->rows_by_bin.p + p->bin_start[kHeavyBin], nh, p->anz.p, p->A.row_ptr,
                                 p->A.col_idx, p->B.row_ptr, p->B.col_idx, p->B.n_rows, static_cast<int>(v0),
-                                ilog2(p->P.widths[0]), p->cnt0.p, s))
+                                ilog2(p->P.widths[0]), p->bcp.p, p->cnt0.p, s))
           return GM_ERR_OOM;
       }
       p->stage_end(ts);

@@ -9,6 +9,8 @@
 //   elements. A work group reserves, per A-tilde entry it touches, a contiguous
 //   range of that entry's C-hat row with one atomic add on the row's cursor, then
 //   writes consecutive B-row elements to consecutive C-hat positions.
+#include <algorithm>
+
 #include "gm_device.cuh"
 #include "gm_internal.h"
 
@@ -48,11 +50,20 @@ __global__ void k_slice_sizes(const int64_t* __restrict__ col_ptr, const int64_t
     size[k] = (col_ptr[k + 1] - col_ptr[k]) * (b_rp[k + 1] - b_rp[k]);
 }
 
-__global__ void k_wg_slice(const int64_t* __restrict__ off, int64_t n_slices, int64_t E, int32_t* __restrict__ wg) {
+// wg[g] = the slice holding flattened position g * E: the largest s with
+// off[s] <= g * E (a non-empty slice; off has n_slices + 1 entries). One thread
+// per work group, binary search.
+__global__ void k_wg_slice(const int64_t* __restrict__ off, int64_t n_slices, int64_t E, int64_t n_wg,
+                           int32_t* __restrict__ wg) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t s = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; s < n_slices; s += stride) {
-    const int64_t lo = off[s], hi = off[s + 1];
-    for (int64_t g = (lo + E - 1) / E; g * E < hi; ++g) wg[g] = static_cast<int32_t>(s);
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < n_wg; g += stride) {
+    const int64_t x = g * E;
+    int64_t lo = 0, hi = n_slices - 1;
+    while (lo < hi) {
+      const int64_t mid = (lo + hi + 1) >> 1;
+      if (off[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    wg[g] = static_cast<int32_t>(lo);
   }
 }
 
@@ -154,6 +165,88 @@ __global__ void __launch_bounds__(kOpThreads) k_outer(OuterArgs a) {
   }
 }
 
+// OuterProduct into the level-0 chunks, one warp per unit of W consecutive
+// products of the flattened slice space (B rows sorted, per-B-row chunk starts in
+// a.bcp). A unit is walked entry portion by entry portion (the part of one
+// A-tilde entry's product row A~[i,k] * B[k,:] inside the unit):
+//  * the lanes read the chunk starts of B row k for the chunks the portion
+//    spans (lane l holds chunk c_lo + l, + 32, ...), and each lane reserves its
+//    run (the portion's elements in that chunk) with one atomic add on the
+//    chunk's cursor -- all runs of the portion at once;
+//  * the warp streams the portion (coalesced B reads); a product finds its run's
+//    destination in the register of the lane holding its chunk (warp shuffle),
+//    and the lanes of a run write consecutive addresses.
+constexpr int kOwU = 4;
+
+template <bool VAL, int SLOTS>
+__global__ void __launch_bounds__(256) k_outer_warp(OuterArgs a, int64_t n_units) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const uint32_t mask = (1u << a.shift) - 1u;
+  const int vp1 = a.v + 1;
+  for (int64_t g = gw; g < n_units; g += nw) {
+    int64_t p = g * a.E;
+    const int64_t stop = min(p + a.E, a.total);
+    int64_t s = a.wg_first[g];
+    while (p < stop) {
+      if (a.slice_off[s + 1] <= p) s = upper_floor(a.slice_off, s + 1, a.n_slices - 1, p);
+      const int64_t rb = a.b_rp[s];
+      const int64_t L = a.b_rp[s + 1] - rb;
+      const int64_t rel = p - a.slice_off[s];
+      const int64_t e = a.col_ptr[s] + rel / L;
+      const int64_t q0 = rel % L;
+      const int64_t q1 = min(L, q0 + (stop - p));
+      const int64_t key_row = static_cast<int64_t>(a.t_row[e]) * a.v;
+      const double av = VAL ? a.t_val[e] : 0.0;
+      const int c_lo = static_cast<int>(static_cast<uint32_t>(a.b_col[rb + q0]) >> a.shift);
+      const int c_hi = static_cast<int>(static_cast<uint32_t>(a.b_col[rb + q1 - 1]) >> a.shift);
+      const int nslots = (c_hi - c_lo + 32) >> 5;  // warp-uniform, <= SLOTS
+      const int32_t* const t = a.bcp + s * vp1;
+      int64_t base[SLOTS];
+#pragma unroll
+      for (int k = 0; k < SLOTS; ++k) {
+        base[k] = 0;
+        const int c = c_lo + k * 32 + lane;
+        if (k < nslots && c <= c_hi) {
+          const int64_t x0 = max(q0, static_cast<int64_t>(t[c])), x1 = min(q1, static_cast<int64_t>(t[c + 1]));
+          if (x1 > x0)
+            base[k] = static_cast<int64_t>(atomicAdd(&a.cursor[key_row + c], static_cast<unsigned long long>(x1 - x0))) - x0;
+        }
+      }
+      for (int64_t qb = q0; qb < q1; qb += 32 * kOwU) {
+        uint32_t col[kOwU];
+        double bv[kOwU];
+#pragma unroll
+        for (int u = 0; u < kOwU; ++u) {
+          const int64_t q = qb + u * 32 + lane;
+          col[u] = q < q1 ? static_cast<uint32_t>(a.b_col[rb + q]) : 0u;
+          bv[u] = (VAL && q < q1) ? a.b_val[rb + q] : 0.0;
+        }
+#pragma unroll
+        for (int u = 0; u < kOwU; ++u) {
+          const int64_t q = qb + u * 32 + lane;
+          const int idx = q < q1 ? static_cast<int>(col[u] >> a.shift) - c_lo : 0;
+          int64_t b = 0;
+#pragma unroll
+          for (int k = 0; k < SLOTS; ++k) {
+            if (k < nslots) {
+              const int64_t x = __shfl_sync(kFull, base[k], idx & 31);
+              if ((idx >> 5) == k) b = x;
+            }
+          }
+          if (q < q1) {
+            const int64_t dst = b + q;
+            a.out_col[dst] = static_cast<int32_t>(col[u] & mask);
+            if (VAL) a.out_val[dst] = av * bv[u];
+          }
+        }
+      }
+      p += q1 - q0;
+    }
+  }
+}
+
 }  // namespace
 
 bool masked_transpose(const TransposeArgs& a, int64_t nnz_batch, int64_t* col_ptr, int32_t* t_row,
@@ -176,9 +269,11 @@ bool slice_offsets(const int64_t* col_ptr, const int64_t* b_rp, int64_t n_cols, 
   return scan_exclusive_i64(slice_off, slice_off, n_cols + 1, nullptr, s);
 }
 
-void launch_wg_slice(const int64_t* slice_off, int64_t n_slices, int64_t E, int32_t* wg_first, cudaStream_t s) {
-  if (n_slices <= 0) return;
-  (k_wg_slice<<<grid_for(n_slices, 256), 256, 0, s>>>(slice_off, n_slices, E, wg_first), note_launch());
+void launch_wg_slice(const int64_t* slice_off, int64_t n_slices, int64_t total, int64_t E, int32_t* wg_first,
+                     cudaStream_t s) {
+  const int64_t n_wg = (total + E - 1) / E;
+  if (n_slices <= 0 || n_wg <= 0) return;
+  (k_wg_slice<<<grid_for(n_wg, 256), 256, 0, s>>>(slice_off, n_slices, E, n_wg, wg_first), note_launch());
 }
 
 void launch_outer_product(const OuterArgs& a, cudaStream_t s) {
@@ -191,6 +286,19 @@ void launch_outer_product(const OuterArgs& a, cudaStream_t s) {
   } else {
     if (a.histo) (k_outer<false, true><<<g, kOpThreads, 0, s>>>(a), note_launch());
     else (k_outer<false, false><<<g, kOpThreads, 0, s>>>(a), note_launch());
+  }
+}
+
+void launch_outer_split(const OuterArgs& a, cudaStream_t s) {
+  if (a.total <= 0) return;
+  const int64_t n_units = (a.total + a.E - 1) / a.E;  // one warp per work group of E products
+  const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((n_units + 7) / 8, 152LL * 64));
+  if (a.v <= 64) {
+    if (a.out_val) (k_outer_warp<true, 2><<<blocks, 256, 0, s>>>(a, n_units), note_launch());
+    else (k_outer_warp<false, 2><<<blocks, 256, 0, s>>>(a, n_units), note_launch());
+  } else {
+    if (a.out_val) (k_outer_warp<true, 8><<<blocks, 256, 0, s>>>(a, n_units), note_launch());
+    else (k_outer_warp<false, 8><<<blocks, 256, 0, s>>>(a, n_units), note_launch());
   }
 }
 

@@ -96,6 +96,8 @@ void launch_validate_rowptr(const int64_t* rp, int64_t n_rows, int64_t nnz, int 
                             cudaStream_t s);
 void launch_validate_cols(const int32_t* col, int64_t nnz, int64_t n_cols, int bad_bit, int* status,
                           cudaStream_t s);
+// *unsorted |= 1 when a row's columns are not non-decreasing (rows validated first).
+void launch_check_sorted(const int64_t* rp, const int32_t* col, int64_t n_rows, int* unsorted, cudaStream_t s);
 // u[i] = sum over stored A[i,k] of nnz(B[k,:]); bin[i] from spec.
 void launch_ip_count(const int64_t* a_rp, const int32_t* a_col, int64_t n_rows, const int64_t* b_rp,
                      int64_t* u, uint8_t* bin, BinSpec spec, cudaStream_t s);
@@ -129,8 +131,9 @@ bool masked_transpose(const TransposeArgs& a, int64_t nnz_batch, int64_t* col_pt
 // slice_off[k] = sum_{k'<k} (col_ptr[k'+1]-col_ptr[k']) * nnz(B[k',:]), k in [0, n_cols].
 bool slice_offsets(const int64_t* col_ptr, const int64_t* b_rp, int64_t n_cols, int64_t* slice_off,
                    cudaStream_t s);
-// wg_first[g] = the slice holding flattened position g*E (g in [0, n_wg)).
-void launch_wg_slice(const int64_t* slice_off, int64_t n_slices, int64_t E, int32_t* wg_first, cudaStream_t s);
+// wg_first[g] = the slice holding flattened position g*E (g in [0, ceil(total/E))).
+void launch_wg_slice(const int64_t* slice_off, int64_t n_slices, int64_t total, int64_t E, int32_t* wg_first,
+                     cudaStream_t s);
 
 struct OuterArgs {
   const int64_t* slice_off;   // n_cols + 1
@@ -149,10 +152,17 @@ struct OuterArgs {
   double* out_val;            // null: columns only
   // fused level-0 histogram (null when not fused)
   unsigned long long* histo;  // [rows * v]
+  const int32_t* bcp;         // per-B-row chunk starts (heavy_chunk_counts), for k_outer_warp
   int v;
   int shift;                  // chunk = col >> shift
 };
 void launch_outer_product(const OuterArgs& a, cudaStream_t s);
+// OuterProduct straight into the level-0 chunks (B rows sorted by column, v <=
+// 256, per-B-row chunk starts in a.bcp): the products of one A-tilde entry in
+// one chunk form a run of consecutive B-row elements; each run is reserved with
+// one atomic add on cursor[row * v + chunk] and written contiguously, the column
+// shifted into the chunk (col & (2^shift - 1)). One warp per E products; histo unused.
+void launch_outer_split(const OuterArgs& a, cudaStream_t s);
 
 // ---- multisplit (gm_multisplit.cu) ------------------------------------------
 // wg_first[g] = the row holding position g*E.
@@ -305,11 +315,13 @@ bool rowbm_light_fits(int64_t c_m, int cap, bool symbolic, int64_t smem_max);
 void launch_rowbm_light(const RowBitmapArgs& a, bool symbolic, int cap, int num_sms, cudaStream_t s);
 
 // cnt[h * v + c] = products of heavy row h whose column falls in level-0 chunk c
-// (col >> shift == c), from per-B-row chunk histograms. False on allocation failure.
-// anz: prefix of the heavy rows' A-row lengths (n_heavy + 1).
+// (col >> shift == c), from per-B-row chunk counts, which are left in bcp
+// (b_rows * (v + 1) entries: bcp[k * (v + 1) + c] = entries of B row k in chunks
+// below c; for a row sorted by column, chunk c is its index range [bcp[c], bcp[c+1])).
+// anz: prefix of the heavy rows' A-row lengths (n_heavy + 1). False when v > 256.
 bool heavy_chunk_counts(const int32_t* heavy_rows, int64_t n_heavy, const int64_t* anz, const int64_t* a_rp,
                         const int32_t* a_col, const int64_t* b_rp, const int32_t* b_col, int64_t b_rows, int v,
-                        int shift, int64_t* cnt, cudaStream_t s);
+                        int shift, int32_t* bcp, int64_t* cnt, cudaStream_t s);
 
 // Light-row bins: upper bounds on u and table capacity per bin.
 constexpr int kLightWarpBins = 4;   // bins 1..4 use a warp per row

@@ -392,32 +392,43 @@ namespace gm {
 
 namespace {
 
-// hist[k * v + c] = number of stored B[k, j] with j >> shift == c (one warp per B row).
-__global__ void k_b_chunk_hist(const int64_t* __restrict__ b_rp, const int32_t* __restrict__ b_col, int64_t n_rows,
-                               int v, int shift, int32_t* __restrict__ hist) {
+// bcp[k * (v + 1) + c] = number of stored B[k, j] with j >> shift < c, for c in
+// [0, v] (one warp per B row: shared per-warp histogram, then a warp scan). In a
+// row sorted by column, chunk c of the row is the index range [bcp[c], bcp[c+1]).
+__global__ void k_b_chunk_prefix(const int64_t* __restrict__ b_rp, const int32_t* __restrict__ b_col, int64_t n_rows,
+                                 int v, int shift, int32_t* __restrict__ bcp) {
   extern __shared__ int sh[];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
   int* h = sh + w * v;
+  const int per = (v + 31) / 32;  // chunks per lane, contiguous
   for (int64_t k = static_cast<int64_t>(blockIdx.x) * nw + w; k < n_rows; k += static_cast<int64_t>(gridDim.x) * nw) {
     for (int c = lane; c < v; c += 32) h[c] = 0;
     __syncwarp();
     for (int64_t q = b_rp[k] + lane; q < b_rp[k + 1]; q += 32)
       atomicAdd(&h[static_cast<uint32_t>(b_col[q]) >> shift], 1);
     __syncwarp();
-    for (int c = lane; c < v; c += 32) hist[k * v + c] = h[c];
+    int sum = 0;
+    for (int c = lane * per; c < min(v, lane * per + per); ++c) sum += h[c];
+    int run = warp_inclusive_scan(sum) - sum;
+    int32_t* const out = bcp + k * (v + 1);
+    for (int c = lane * per; c < min(v, lane * per + per); ++c) {
+      out[c] = run;
+      run += h[c];
+    }
+    if (lane == 31) out[v] = run;
     __syncwarp();
   }
 }
 
 // cnt[h * v + c] += elements of chunk c of heavy row h: the heavy rows' A entries,
 // concatenated (anz = prefix of their lengths), are cut into segments of 256 per
-// warp; each entry adds the chunk histogram of the B row it selects, and a warp
+// warp; each entry adds the chunk counts of the B row it selects, and a warp
 // flushes its sums with one atomic per chunk whenever its segment leaves a row.
 constexpr int kSegEntries = 256;
 
 __global__ void k_heavy_chunk_counts(const int32_t* __restrict__ rows, int64_t n, const int64_t* __restrict__ anz,
                                      const int64_t* __restrict__ a_rp, const int32_t* __restrict__ a_col,
-                                     const int32_t* __restrict__ hist, int v, unsigned long long* __restrict__ cnt) {
+                                     const int32_t* __restrict__ bcp, int v, unsigned long long* __restrict__ cnt) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -445,11 +456,11 @@ __global__ void k_heavy_chunk_counts(const int32_t* __restrict__ rows, int64_t n
         row_end = anz[h + 1];
         pbase = a_rp[rows[h]] - anz[h];
       }
-      const int64_t k = a_col[pbase + e];
+      const int32_t* const t = bcp + static_cast<int64_t>(a_col[pbase + e]) * (v + 1);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int c = i * 32 + lane;
-        if (i < nc && c < v) acc[i] += hist[k * v + c];
+        if (i < nc && c < v) acc[i] += t[c + 1] - t[c];
       }
     }
     for (int i = 0; i < nc; ++i) {
@@ -463,16 +474,15 @@ __global__ void k_heavy_chunk_counts(const int32_t* __restrict__ rows, int64_t n
 
 bool heavy_chunk_counts(const int32_t* heavy_rows, int64_t n_heavy, const int64_t* anz, const int64_t* a_rp,
                         const int32_t* a_col, const int64_t* b_rp, const int32_t* b_col, int64_t b_rows, int v,
-                        int shift, int64_t* cnt, cudaStream_t s) {
-  if (n_heavy <= 0) return true;
+                        int shift, int32_t* bcp, int64_t* cnt, cudaStream_t s) {
   if (v > 256) return false;
-  DevBuf<int32_t> hist;
-  if (!hist.alloc(static_cast<size_t>(b_rows) * v, s)) return false;
   const int warps = 8;
-  (k_b_chunk_hist<<<grid_for(b_rows * 32, warps * 32), warps * 32, warps * v * sizeof(int), s>>>(
-       b_rp, b_col, b_rows, v, shift, hist.p), note_launch());
+  if (b_rows > 0)
+    (k_b_chunk_prefix<<<grid_for(b_rows * 32, warps * 32), warps * 32, warps * v * sizeof(int), s>>>(
+         b_rp, b_col, b_rows, v, shift, bcp), note_launch());
+  if (n_heavy <= 0) return true;
   cudaMemsetAsync(cnt, 0, static_cast<size_t>(n_heavy) * v * sizeof(int64_t), s);
-  (k_heavy_chunk_counts<<<152 * 16, 256, 0, s>>>(heavy_rows, n_heavy, anz, a_rp, a_col, hist.p, v,
+  (k_heavy_chunk_counts<<<152 * 16, 256, 0, s>>>(heavy_rows, n_heavy, anz, a_rp, a_col, bcp, v,
                                                  reinterpret_cast<unsigned long long*>(cnt)), note_launch());
   return true;
 }

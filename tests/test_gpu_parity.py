@@ -299,6 +299,20 @@ def test_light_rows_every_bin_and_entry_tiles(n_cols):
     assert info.n_heavy_rows == int((u > info.params.tau).sum())
 
 
+@pytest.mark.parametrize("values", ["uniform", "int"])
+def test_rowwise_sorted_and_unsorted_b(values):
+    """The row-order pipeline scatters whole runs of a B row into a chunk when B's
+    rows are sorted, and product by product otherwise: both give the oracle's C."""
+    A = gi.rmat(11, 8, seed=5, values=values)
+    rng = np.random.default_rng(7)
+    perm = np.concatenate([lo + rng.permutation(hi - lo) for lo, hi in zip(A.row_ptr[:-1], A.row_ptr[1:])])
+    B_unsorted = gi.CSR(A.n_rows, A.n_cols, A.row_ptr.copy(), A.col[perm].copy(), A.val[perm].copy())
+    cfg = {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_ROWWISE}
+    for B in (A, B_unsorted):
+        info = check_full(A, B, exact=values == "int", **cfg)
+        assert info.pipeline == binding.GM_PIPE_ROWWISE and info.n_heavy_rows > 0
+
+
 def _rows_of(M, rows):
     rows = np.asarray(rows, dtype=np.int64)
     lens = M.row_ptr[rows + 1] - M.row_ptr[rows]
