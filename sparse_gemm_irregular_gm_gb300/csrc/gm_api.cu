@@ -662,7 +662,7 @@ static gm_status run_batch_runs(gm_plan* p, int64_t h0, int64_t h1, int64_t* par
   oa.v = v;
   oa.shift = ilog2(p->P.widths[0]);
   oa.bcp = p->bcp.p;
-  launch_outer_split(oa, s);
+  launch_outer_split(oa, p->work_counter.p, p->num_sms, s);
   p->stage_end(t);
   t_row.release();
   t_val.release();

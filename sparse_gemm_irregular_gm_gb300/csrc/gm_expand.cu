@@ -165,54 +165,86 @@ __global__ void __launch_bounds__(kOpThreads) k_outer(OuterArgs a) {
   }
 }
 
-// OuterProduct into the level-0 chunks, one warp per unit of W consecutive
+// OuterProduct into the level-0 chunks, one warp per unit of E consecutive
 // products of the flattened slice space (B rows sorted, per-B-row chunk starts in
-// a.bcp). A unit is walked entry portion by entry portion (the part of one
-// A-tilde entry's product row A~[i,k] * B[k,:] inside the unit):
-//  * the lanes read the chunk starts of B row k for the chunks the portion
-//    spans (lane l holds chunk c_lo + l, + 32, ...), and each lane reserves its
-//    run (the portion's elements in that chunk) with one atomic add on the
-//    chunk's cursor -- all runs of the portion at once;
-//  * the warp streams the portion (coalesced B reads); a product finds its run's
-//    destination in the register of the lane holding its chunk (warp shuffle),
-//    and the lanes of a run write consecutive addresses.
+// a.bcp); warps take units from a global counter. A unit is walked entry portion
+// by entry portion (the part of one A-tilde entry's product row A~[i,k] * B[k,:]
+// inside the unit). Per slice k the warp keeps in registers the B row's start
+// and length and, lane l for chunks c_lo + l, + 32, ..., the chunk's index range
+// [T0, T1) inside the row. A portion [q0, q1) of the row then needs only its
+// entry (row, A value: loaded one entry ahead) and the reservations: lane l
+// clips its chunks' ranges to the portion and reserves each non-empty run with
+// one atomic add on the chunk's cursor, all runs at once. The warp streams the
+// portion (coalesced B reads); a product finds its run's destination in the
+// register of the lane holding its chunk (warp shuffle), and the lanes of a run
+// write consecutive addresses.
 constexpr int kOwU = 4;
 
 template <bool VAL, int SLOTS>
-__global__ void __launch_bounds__(256) k_outer_warp(OuterArgs a, int64_t n_units) {
+__global__ void __launch_bounds__(256) k_outer_warp(OuterArgs a, int64_t n_units, unsigned* unit_counter) {
   const int lane = threadIdx.x & 31;
-  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const uint32_t mask = (1u << a.shift) - 1u;
   const int vp1 = a.v + 1;
-  for (int64_t g = gw; g < n_units; g += nw) {
+  int64_t s = -1, rb = 0, L = 1, so0 = 0, so1 = 0, cp = 0;  // cached slice
+  int c_lo = 0, nslots = 0;
+  int32_t T0[SLOTS], T1[SLOTS];
+  while (true) {
+    unsigned gu = 0;
+    if (lane == 0) gu = atomicAdd(unit_counter, 1u);
+    const int64_t g = __shfl_sync(kFull, gu, 0);
+    if (g >= n_units) break;
     int64_t p = g * a.E;
     const int64_t stop = min(p + a.E, a.total);
-    int64_t s = a.wg_first[g];
+    int64_t e_next = -1;  // entry whose row / value sit in r_next / a_next
+    int32_t r_next = 0;
+    double a_next = 0.0;
     while (p < stop) {
-      if (a.slice_off[s + 1] <= p) s = upper_floor(a.slice_off, s + 1, a.n_slices - 1, p);
-      const int64_t rb = a.b_rp[s];
-      const int64_t L = a.b_rp[s + 1] - rb;
-      const int64_t rel = p - a.slice_off[s];
-      const int64_t e = a.col_ptr[s] + rel / L;
+      if (s < 0 || p < so0 || p >= so1) {  // new slice: its B row and chunk ranges
+        s = upper_floor(a.slice_off, a.wg_first[g], a.n_slices - 1, p);
+        so0 = a.slice_off[s];
+        so1 = a.slice_off[s + 1];
+        cp = a.col_ptr[s];
+        rb = a.b_rp[s];
+        L = a.b_rp[s + 1] - rb;
+        c_lo = static_cast<int>(static_cast<uint32_t>(a.b_col[rb]) >> a.shift);
+        const int c_hi = static_cast<int>(static_cast<uint32_t>(a.b_col[rb + L - 1]) >> a.shift);
+        nslots = (c_hi - c_lo + 32) >> 5;
+        const int32_t* const t = a.bcp + s * vp1;
+#pragma unroll
+        for (int k = 0; k < SLOTS; ++k) {
+          const int c = c_lo + k * 32 + lane;
+          const bool in = k < nslots && c <= c_hi;
+          T0[k] = in ? t[c] : 0;
+          T1[k] = in ? t[c + 1] : 0;
+        }
+      }
+      const int64_t rel = p - so0;
+      const int64_t e = cp + rel / L;
       const int64_t q0 = rel % L;
       const int64_t q1 = min(L, q0 + (stop - p));
-      const int64_t key_row = static_cast<int64_t>(a.t_row[e]) * a.v;
-      const double av = VAL ? a.t_val[e] : 0.0;
-      const int c_lo = static_cast<int>(static_cast<uint32_t>(a.b_col[rb + q0]) >> a.shift);
-      const int c_hi = static_cast<int>(static_cast<uint32_t>(a.b_col[rb + q1 - 1]) >> a.shift);
-      const int nslots = (c_hi - c_lo + 32) >> 5;  // warp-uniform, <= SLOTS
-      const int32_t* const t = a.bcp + s * vp1;
+      int32_t row;
+      double av;
+      if (e == e_next) {
+        row = r_next;
+        av = a_next;
+      } else {
+        row = a.t_row[e];
+        av = VAL ? a.t_val[e] : 0.0;
+      }
+      if (e + 1 < cp + (so1 - so0) / L) {  // next entry of the slice, loaded while this one streams
+        e_next = e + 1;
+        r_next = a.t_row[e + 1];
+        a_next = VAL ? a.t_val[e + 1] : 0.0;
+      }
+      const int64_t key_row = static_cast<int64_t>(row) * a.v;
       int64_t base[SLOTS];
 #pragma unroll
       for (int k = 0; k < SLOTS; ++k) {
         base[k] = 0;
-        const int c = c_lo + k * 32 + lane;
-        if (k < nslots && c <= c_hi) {
-          const int64_t x0 = max(q0, static_cast<int64_t>(t[c])), x1 = min(q1, static_cast<int64_t>(t[c + 1]));
-          if (x1 > x0)
-            base[k] = static_cast<int64_t>(atomicAdd(&a.cursor[key_row + c], static_cast<unsigned long long>(x1 - x0))) - x0;
-        }
+        const int64_t x0 = max(q0, static_cast<int64_t>(T0[k])), x1 = min(q1, static_cast<int64_t>(T1[k]));
+        if (k < nslots && x1 > x0)
+          base[k] = static_cast<int64_t>(atomicAdd(&a.cursor[key_row + c_lo + k * 32 + lane],
+                                                   static_cast<unsigned long long>(x1 - x0))) - x0;
       }
       for (int64_t qb = q0; qb < q1; qb += 32 * kOwU) {
         uint32_t col[kOwU];
@@ -289,16 +321,17 @@ void launch_outer_product(const OuterArgs& a, cudaStream_t s) {
   }
 }
 
-void launch_outer_split(const OuterArgs& a, cudaStream_t s) {
+void launch_outer_split(const OuterArgs& a, unsigned* unit_counter, int num_sms, cudaStream_t s) {
   if (a.total <= 0) return;
-  const int64_t n_units = (a.total + a.E - 1) / a.E;  // one warp per work group of E products
-  const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((n_units + 7) / 8, 152LL * 64));
+  const int64_t n_units = (a.total + a.E - 1) / a.E;  // one warp at a time per work group of E products
+  const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((n_units + 7) / 8, static_cast<int64_t>(num_sms) * 4));
+  cudaMemsetAsync(unit_counter, 0, sizeof(unsigned), s);
   if (a.v <= 64) {
-    if (a.out_val) (k_outer_warp<true, 2><<<blocks, 256, 0, s>>>(a, n_units), note_launch());
-    else (k_outer_warp<false, 2><<<blocks, 256, 0, s>>>(a, n_units), note_launch());
+    if (a.out_val) (k_outer_warp<true, 2><<<blocks, 256, 0, s>>>(a, n_units, unit_counter), note_launch());
+    else (k_outer_warp<false, 2><<<blocks, 256, 0, s>>>(a, n_units, unit_counter), note_launch());
   } else {
-    if (a.out_val) (k_outer_warp<true, 8><<<blocks, 256, 0, s>>>(a, n_units), note_launch());
-    else (k_outer_warp<false, 8><<<blocks, 256, 0, s>>>(a, n_units), note_launch());
+    if (a.out_val) (k_outer_warp<true, 8><<<blocks, 256, 0, s>>>(a, n_units, unit_counter), note_launch());
+    else (k_outer_warp<false, 8><<<blocks, 256, 0, s>>>(a, n_units, unit_counter), note_launch());
   }
 }
 

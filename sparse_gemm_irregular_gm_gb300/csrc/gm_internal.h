@@ -161,8 +161,9 @@ void launch_outer_product(const OuterArgs& a, cudaStream_t s);
 // 256, per-B-row chunk starts in a.bcp): the products of one A-tilde entry in
 // one chunk form a run of consecutive B-row elements; each run is reserved with
 // one atomic add on cursor[row * v + chunk] and written contiguously, the column
-// shifted into the chunk (col & (2^shift - 1)). One warp per E products; histo unused.
-void launch_outer_split(const OuterArgs& a, cudaStream_t s);
+// shifted into the chunk (col & (2^shift - 1)). Warps take units of E products; histo unused.
+// unit_counter: one device word the kernel takes work units from (zeroed here).
+void launch_outer_split(const OuterArgs& a, unsigned* unit_counter, int num_sms, cudaStream_t s);
 
 // ---- multisplit (gm_multisplit.cu) ------------------------------------------
 // wg_first[g] = the row holding position g*E.

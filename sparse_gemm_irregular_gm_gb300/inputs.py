@@ -232,6 +232,9 @@ PAIRS = {
     "rmat20_rows2k": ("A[2^19 : 2^19 + 2048, :] * A, A = R-MAT scale 20, edge factor 16 (profiling case: "
                       "C.m = 2^20 at a few GB)",
                       lambda seed=1: (lambda A: (row_slice(A, 1 << 19, (1 << 19) + 2048), A))(rmat(20, 16, seed=seed))),
+    "rmat20_tail64k": ("A[2^20 - 65536 :, :] * A, A = R-MAT scale 20, edge factor 16 (profiling case: the sparse "
+                       "end of the matrix, mostly light rows)",
+                       lambda seed=1: (lambda A: (row_slice(A, (1 << 20) - 65536, 1 << 20), A))(rmat(20, 16, seed=seed))),
 }
 
 
