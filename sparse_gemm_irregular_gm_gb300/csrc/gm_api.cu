@@ -1120,7 +1120,7 @@ static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, double* c_val
       ra.c_val = c_val;
       ra.work_counter = p->work_counter.p;
       ra.status = p->status.p;
-      launch_rowbm_light(ra, !numeric, cap, p->num_sms, p->s);
+      launch_rowbm_light(ra, !numeric, cap, p->num_sms, p->smem_dev, p->s);
       continue;
     }
     LightArgs la{};

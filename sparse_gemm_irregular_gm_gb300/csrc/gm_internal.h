@@ -311,9 +311,11 @@ int64_t rowbm_symbolic_smem(int64_t c_m);
 // Heavy rows: chunk nnz (v chunks of a.width) or whole-row nnz from a whole-row bitmap.
 void launch_rowbm(const RowBitmapArgs& a, int num_sms, int64_t smem_max, cudaStream_t s);
 // Light rows of at most cap products (symbolic: whole-row nnz into c_rp; numeric: the row of C).
-int64_t rowbm_light_smem(int64_t c_m, int cap, bool symbolic);
+// Numeric: columns in windows of a bitmap that fits beside the placed values and
+// counters; int32 count-and-place by rank, no floating-point atomics.
+int64_t rowbm_light_smem(int64_t c_m, int cap, bool symbolic, int64_t smem_max);
 bool rowbm_light_fits(int64_t c_m, int cap, bool symbolic, int64_t smem_max);
-void launch_rowbm_light(const RowBitmapArgs& a, bool symbolic, int cap, int num_sms, cudaStream_t s);
+void launch_rowbm_light(const RowBitmapArgs& a, bool symbolic, int cap, int num_sms, int64_t smem_max, cudaStream_t s);
 
 // cnt[h * v + c] = products of heavy row h whose column falls in level-0 chunk c
 // (col >> shift == c), from per-B-row chunk counts, which are left in bcp

@@ -175,14 +175,31 @@ __global__ void __launch_bounds__(kRbThreads) k_rowbm_symbolic(RowBitmapArgs a, 
 constexpr int kGroupWords = 8;  // rank prefix kept per 8 bitmap words (256 columns)
 constexpr int kRlItems = 10;    // products per thread in k_rowbm_light: rows of up to 10240 products
 constexpr uint32_t kNoCol = 0xFFFFFFFFu;
-constexpr int64_t kLightSymRegion = 32768;  // entry-table bytes of the symbolic light kernel
+constexpr int64_t kLightSymRegion = 65536;  // entry-table bytes of the symbolic light kernel
+
+// Rank of column c (number of set bits below it) from the 8-word group prefix:
+// the group's 8 words come in as two 16-byte loads.
+__device__ __forceinline__ int bitmap_rank(const uint32_t* bm, const int* gpre, uint32_t c) {
+  const int w = c >> 5, g = w >> 3, wi = w & 7;
+  const uint4* g4 = reinterpret_cast<const uint4*>(bm + g * kGroupWords);
+  const uint4 q0 = g4[0], q1 = g4[1];
+  const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+  int r = gpre[g];
+#pragma unroll
+  for (int x = 0; x < 8; ++x) {
+    if (x < wi) r += __popc(words[x]);
+    else if (x == wi) r += __popc(words[x] & ((1u << (c & 31)) - 1u));
+  }
+  return r;
+}
 
 // Light rows (u <= kRbThreads * kRlItems) with a whole-row bitmap, every product
 // held in registers: thread t takes products t, t + T, ... of the row in row
 // order, so the block's work is balanced whatever the lengths of the B rows.
 // The row's A entries are staged in shared memory (B row start, A value, and a
-// prefix of the B row lengths, te_cap entries at a time); a product finds its
-// entry by binary search over that prefix. All B loads of a thread are issued
+// prefix of the B row lengths, te_cap entries at a time), and each warp writes
+// the index of its entries into every product position they cover, so a
+// product reads its entry in one load. All B loads of a thread are issued
 // before the first is used. The products' columns set the bitmap; then
 //  * symbolic: the row's nnz is the bitmap's popcount (written to c_rp[row]);
 //  * numeric: prefix sums over groups of 8 words give every column its rank,
@@ -190,21 +207,20 @@ constexpr int64_t kLightSymRegion = 32768;  // entry-table bytes of the symbolic
 //    space is reused) and the row is written in column order.
 template <bool SYM>
 __global__ void __launch_bounds__(kRbThreads, 1)
-    k_rowbm_light(RowBitmapArgs a, int nwords, int cap, int te_cap, int region_bytes) {
+    k_rowbm_light(RowBitmapArgs a, int nwords, int wwords, int cap, int te_cap, int region_bytes) {
   extern __shared__ __align__(16) unsigned char smem[];
   int64_t* s_bs = reinterpret_cast<int64_t*>(smem);                       // te_cap
   double* s_av = reinterpret_cast<double*>(s_bs + te_cap);                // te_cap (numeric)
   int* s_pre = reinterpret_cast<int*>(SYM ? static_cast<void*>(s_bs + te_cap) : static_cast<void*>(s_av + te_cap));
-  double* vals = reinterpret_cast<double*>(smem);                         // numeric, after the walk
-  const int ngroups = (nwords + kGroupWords - 1) / kGroupWords;
-  uint32_t* bm = reinterpret_cast<uint32_t*>(smem + region_bytes);        // ngroups * kGroupWords
-  int* gpre = reinterpret_cast<int*>(bm + ngroups * kGroupWords);         // ngroups (numeric)
+  uint16_t* s_ent = reinterpret_cast<uint16_t*>(s_pre + te_cap);          // cap: entry of each product position
+  double* vals = reinterpret_cast<double*>(smem);                         // numeric, after the products are loaded
+  const int ngroups = (nwords + kGroupWords - 1) / kGroupWords;           // symbolic: the whole row
+  uint32_t* bm = reinterpret_cast<uint32_t*>(smem + region_bytes);        // symbolic ngroups * 8, numeric wwords
+  int* gpre = reinterpret_cast<int*>(bm + wwords);                        // numeric: wwords / 8
   __shared__ int64_t s_item;
   __shared__ int ws[33];
   constexpr int T = kRbThreads;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int per_g = (ngroups + T - 1) / T;
-  const int g0 = threadIdx.x * per_g, g1 = min(ngroups, g0 + per_g);
   while (true) {
     if (threadIdx.x == 0) s_item = atomicAdd(a.work_counter, 1u);
     __syncthreads();
@@ -212,7 +228,7 @@ __global__ void __launch_bounds__(kRbThreads, 1)
     if (item >= a.n_items) break;
     const int64_t r = a.rows[item];
     const int64_t lo = a.a_rp[r], ne = a.a_rp[r + 1] - lo;
-    zero_words(bm, ngroups * kGroupWords);
+    if (SYM) zero_words(bm, ngroups * kGroupWords);
     uint32_t col[kRlItems];
     double val[kRlItems];
 #pragma unroll
@@ -247,19 +263,23 @@ __global__ void __launch_bounds__(kRbThreads, 1)
         }
       }
       __syncthreads();
+      {  // position -> entry map of this tile (positions beyond the registers or the map are never read)
+        const int npos = min(tot, min(cap, static_cast<int>(static_cast<int64_t>(T) * kRlItems - min(P0, static_cast<int64_t>(T) * kRlItems))));
+        for (int i = warp; i < nt; i += T / 32) {
+          const int st = s_pre[i];
+          const int en = min(i + 1 < nt ? s_pre[i + 1] : tot, npos);
+          for (int q = st + lane; q < en; q += 32) s_ent[q] = static_cast<uint16_t>(i);
+        }
+        if (tot > cap && threadIdx.x == 0) atomicOr(a.status, kStInternal);
+      }
+      __syncthreads();
       int ent[kRlItems];
-      int e_prev = 0;
 #pragma unroll
       for (int k = 0; k < kRlItems; ++k) {
         const int64_t rel = static_cast<int64_t>(k) * T + threadIdx.x - P0;
         ent[k] = -1;
-        if (rel >= 0 && rel < tot) {
-          int lo_i = e_prev, hi_i = nt - 1;  // largest i with s_pre[i] <= rel (a non-empty entry)
-          while (lo_i < hi_i) {
-            const int mid = (lo_i + hi_i + 1) >> 1;
-            if (s_pre[mid] <= rel) lo_i = mid; else hi_i = mid - 1;
-          }
-          e_prev = lo_i;
+        if (rel >= 0 && rel < tot && rel < cap) {
+          const int lo_i = s_ent[rel];
           ent[k] = lo_i;
           const int64_t bi = s_bs[lo_i] + (rel - s_pre[lo_i]);
           col[k] = static_cast<uint32_t>(a.b_col[bi]);
@@ -270,7 +290,7 @@ __global__ void __launch_bounds__(kRbThreads, 1)
       for (int k = 0; k < kRlItems; ++k) {
         if (ent[k] >= 0) {
           if (!SYM) val[k] *= s_av[ent[k]];
-          atomicOr(&bm[col[k] >> 5], 1u << (col[k] & 31));
+          if (SYM) atomicOr(&bm[col[k] >> 5], 1u << (col[k] & 31));
         }
       }
       P0 += tot;
@@ -294,84 +314,127 @@ __global__ void __launch_bounds__(kRbThreads, 1)
       __syncthreads();
       continue;
     }
-    int acc = 0;
-    for (int g = g0; g < g1; ++g)
-      for (int w = 0; w < kGroupWords; ++w) acc += __popc(bm[g * kGroupWords + w]);
-    int nnz;
-    int run = block_exclusive_scan(acc, ws, &nnz);
-    for (int g = g0; g < g1; ++g) {
-      gpre[g] = run;
-      for (int w = 0; w < kGroupWords; ++w) run += __popc(bm[g * kGroupWords + w]);
-    }
-    const bool fits = nnz <= cap;
-    if (!fits && threadIdx.x == 0) atomicOr(a.status, kStInternal);
-    for (int i = threadIdx.x; i < min(nnz, cap); i += T) vals[i] = 0.0;
-    __syncthreads();
-    if (fits) {
+    // Numeric: the columns are taken window by window (wwords bitmap words each);
+    // per window: bits, group ranks (conflict-free group counts), the products'
+    // values added into their rank's slot, then the window's part of the row
+    // written in column order.
+    double* const vals = reinterpret_cast<double*>(smem);                       // cap
+    const int64_t out = a.c_rp[r];
+    int done = 0;
+    const int ngw = wwords / kGroupWords;
+    const int per_gw = (ngw + T - 1) / T;
+    const int h0 = threadIdx.x * per_gw, h1 = min(ngw, h0 + per_gw);
+    for (int64_t base = 0; base < static_cast<int64_t>(nwords) * 32; base += static_cast<int64_t>(wwords) * 32) {
+      zero_words(bm, wwords);
+      __syncthreads();
+      uint32_t cw[kRlItems];  // column inside the window, kNoCol outside
 #pragma unroll
       for (int k = 0; k < kRlItems; ++k) {
-        if (col[k] != kNoCol) {
-          const uint32_t cc = col[k];
-          const int w = cc >> 5, g = w / kGroupWords;
-          int rank = gpre[g] + __popc(bm[w] & ((1u << (cc & 31)) - 1u));
-          for (int x = g * kGroupWords; x < w; ++x) rank += __popc(bm[x]);
-          atomicAdd(&vals[rank], val[k]);
-        }
+        const int64_t c = static_cast<int64_t>(col[k]) - base;
+        cw[k] = (col[k] != kNoCol && c >= 0 && c < static_cast<int64_t>(wwords) * 32) ? static_cast<uint32_t>(c) : kNoCol;
+        if (cw[k] != kNoCol) atomicOr(&bm[cw[k] >> 5], 1u << (cw[k] & 31));
       }
-    }
-    __syncthreads();
-    if (fits) {  // words round-robin over threads: balanced emission, adjacent output ranges per warp
-      const int64_t out = a.c_rp[r];
-      for (int w = threadIdx.x; w < nwords; w += T) {
+      __syncthreads();
+      // group counts with consecutive groups on consecutive lanes (two 16-byte loads
+      // a group), then a scan over the counts, a few consecutive ints per thread
+      for (int g = threadIdx.x; g < ngw; g += T) {
+        const uint4* g4 = reinterpret_cast<const uint4*>(bm + g * kGroupWords);
+        const uint4 q0 = g4[0], q1 = g4[1];
+        gpre[g] = __popc(q0.x) + __popc(q0.y) + __popc(q0.z) + __popc(q0.w) + __popc(q1.x) + __popc(q1.y) +
+                  __popc(q1.z) + __popc(q1.w);
+      }
+      __syncthreads();
+      int acc = 0;
+      for (int g = h0; g < h1; ++g) acc += gpre[g];
+      int nnz;
+      int run = block_exclusive_scan(acc, ws, &nnz);
+      for (int g = h0; g < h1; ++g) {
+        const int x = gpre[g];
+        gpre[g] = run;
+        run += x;
+      }
+      if (done + nnz > cap) {  // uniform: the bin promised at most cap products
+        if (threadIdx.x == 0) atomicOr(a.status, kStInternal);
+        break;
+      }
+      for (int i = threadIdx.x; i < nnz; i += T) vals[i] = 0.0;
+      __syncthreads();
+#pragma unroll
+      for (int k = 0; k < kRlItems; ++k)
+        if (cw[k] != kNoCol) atomicAdd(&vals[bitmap_rank(bm, gpre, cw[k])], val[k]);
+      __syncthreads();
+      for (int w = threadIdx.x; w < wwords; w += T) {  // words round-robin: adjacent output per warp
         uint32_t bits = bm[w];
         if (!bits) continue;
-        const int g = w / kGroupWords;
-        int pos = gpre[g];
-        for (int x = g * kGroupWords; x < w; ++x) pos += __popc(bm[x]);
+        int pos = bitmap_rank(bm, gpre, static_cast<uint32_t>(w) << 5);
         while (bits) {
           const int b = __ffs(bits) - 1;
           bits &= bits - 1;
-          a.c_col[out + pos] = w * 32 + b;
-          a.c_val[out + pos] = vals[pos];
+          a.c_col[out + done + pos] = static_cast<int32_t>(base + w * 32 + b);
+          a.c_val[out + done + pos] = vals[pos];
           ++pos;
         }
       }
+      done += nnz;
+      __syncthreads();
     }
-    __syncthreads();
   }
 }
 
+// Numeric region: the row's values by rank (8 * cap); while a row's products
+// are loaded it holds the entry table and the position map.
 int64_t light_region_bytes(int cap, bool symbolic) {
-  return symbolic ? kLightSymRegion : static_cast<int64_t>((cap + 1) & ~1) * 8;
+  return symbolic ? kLightSymRegion : ((static_cast<int64_t>(cap) * 8 + 16 + 15) & ~int64_t(15));
+}
+
+// Bitmap words per column window of the numeric kernel: the whole row when it
+// fits beside the region, else halved (a multiple of 8 words); 0 when none fits.
+int64_t light_window_words(int64_t c_m, int cap, int64_t smem_max) {
+  const int64_t nwords = (c_m + 31) / 32;
+  int64_t w = (nwords + kGroupWords - 1) / kGroupWords * kGroupWords;
+  while (w >= kGroupWords) {
+    if (light_region_bytes(cap, false) + w * 4 + (w / kGroupWords) * 4 + 4096 <= smem_max) return w;
+    w = (w / 2 + kGroupWords - 1) / kGroupWords * kGroupWords;
+    if (w == kGroupWords && light_region_bytes(cap, false) + w * 4 + 4 + 4096 > smem_max) return 0;
+  }
+  return 0;
 }
 
 }  // namespace
 
 int64_t rowbm_symbolic_smem(int64_t c_m) { return ((c_m + 127) / 128) * 16; }
 
-int64_t rowbm_light_smem(int64_t c_m, int cap, bool symbolic) {
-  const int64_t nwords = (c_m + 31) / 32;
-  const int64_t ngroups = (nwords + kGroupWords - 1) / kGroupWords;
-  return light_region_bytes(cap, symbolic) + ngroups * kGroupWords * 4 + (symbolic ? 0 : ngroups * 4);
+int64_t rowbm_light_smem(int64_t c_m, int cap, bool symbolic, int64_t smem_max) {
+  if (symbolic) {
+    const int64_t nwords = (c_m + 31) / 32;
+    const int64_t ngroups = (nwords + kGroupWords - 1) / kGroupWords;
+    return light_region_bytes(cap, true) + ngroups * kGroupWords * 4;
+  }
+  const int64_t w = light_window_words(c_m, cap, smem_max);
+  return light_region_bytes(cap, false) + w * 4 + (w / kGroupWords) * 4;
 }
 
 bool rowbm_light_fits(int64_t c_m, int cap, bool symbolic, int64_t smem_max) {
-  return cap >= 1 && cap <= kRbThreads * kRlItems && c_m <= (int64_t(1) << 31) &&
-         rowbm_light_smem(c_m, cap, symbolic) + 4096 <= smem_max;
+  if (cap < 1 || cap > kRbThreads * kRlItems || c_m > (int64_t(1) << 31)) return false;
+  const int64_t te = (light_region_bytes(cap, symbolic) - 2 * static_cast<int64_t>(cap) - 16) / (symbolic ? 12 : 20);
+  if (te < 64) return false;
+  if (!symbolic && light_window_words(c_m, cap, smem_max) < kGroupWords) return false;
+  return rowbm_light_smem(c_m, cap, symbolic, smem_max) + 4096 <= smem_max;
 }
 
-void launch_rowbm_light(const RowBitmapArgs& a, bool symbolic, int cap, int num_sms, cudaStream_t s) {
+void launch_rowbm_light(const RowBitmapArgs& a, bool symbolic, int cap, int num_sms, int64_t smem_max, cudaStream_t s) {
   if (a.n_items <= 0) return;
   cudaMemsetAsync(a.work_counter, 0, sizeof(unsigned int), s);
   const int nwords = static_cast<int>((a.c_m + 31) / 32);
   const int64_t region = light_region_bytes(cap, symbolic);
-  const int te_cap = static_cast<int>((region - 8) / (symbolic ? 12 : 20));
-  const size_t smem = static_cast<size_t>(rowbm_light_smem(a.c_m, cap, symbolic));
+  const int te_cap = static_cast<int>((region - 2 * static_cast<int64_t>(cap) - 16) / (symbolic ? 12 : 20));
+  const int wwords = symbolic ? 0 : static_cast<int>(light_window_words(a.c_m, cap, smem_max));
+  const size_t smem = static_cast<size_t>(rowbm_light_smem(a.c_m, cap, symbolic, smem_max));
   const int64_t blocks = std::min<int64_t>(a.n_items, num_sms);
   auto fn = symbolic ? k_rowbm_light<true> : k_rowbm_light<false>;
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  (fn<<<static_cast<unsigned>(blocks), kRbThreads, smem, s>>>(a, nwords, cap, te_cap, static_cast<int>(region)),
-   note_launch());
+  (fn<<<static_cast<unsigned>(blocks), kRbThreads, smem, s>>>(a, nwords, wwords, cap, te_cap,
+                                                               static_cast<int>(region)), note_launch());
 }
 
 void launch_rowbm(const RowBitmapArgs& a, int num_sms, int64_t smem_max, cudaStream_t s) {
