@@ -421,6 +421,81 @@ __global__ void __launch_bounds__(T) k_leaf_small(ListArgs a, int nwords) {
   }
 }
 
+// Small numeric chunk (at most 32 * ITEMS elements, width <= 32 * 4 * 128), one
+// warp per chunk with no block barrier, so many chunks are in flight per SM. The
+// warp's elements sit in registers; its private bitmap of the chunk's columns is
+// counted in 16-byte pieces (consecutive lanes, consecutive pieces) into a word
+// prefix, which gives every column its rank; values are added into their rank's
+// slot (chunks this small rarely repeat a column, so the atomics seldom meet),
+// and the chunk is written in column order by words.
+template <int ITEMS>
+__global__ void __launch_bounds__(128, ITEMS >= 16 ? 5 : 8) k_leaf_warpbm(ListArgs a, int nwp) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  constexpr int CAPW = 32 * ITEMS;
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  unsigned char* mine = smem + static_cast<size_t>(wib) * (static_cast<size_t>(nwp) * 8 + CAPW * 8);
+  uint32_t* bm = reinterpret_cast<uint32_t*>(mine);                 // nwp (a multiple of 128)
+  int* pre = reinterpret_cast<int*>(bm + nwp);                      // nwp
+  double* vals = reinterpret_cast<double*>(pre + nwp);              // CAPW
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + wib;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t item = gw; item < a.n_items; item += nw) {
+    const int64_t m = a.items[item];
+    const int64_t lo = a.rp[m];
+    const int n = static_cast<int>(min(a.rp[m + 1] - lo, static_cast<int64_t>(CAPW)));
+    const int64_t child_local = a.child_of ? a.child_of[m] : m;
+    const int64_t out = a.off_in[a.child_base + child_local];
+    const int64_t cb = leaf_col_base(a, child_local);
+    int key[ITEMS];
+    double val[ITEMS];
+#pragma unroll
+    for (int k = 0; k < ITEMS; ++k) {
+      const int e = k * 32 + lane;
+      key[k] = e < n ? a.col[lo + e] : -1;
+      val[k] = e < n ? a.val[lo + e] : 0.0;
+    }
+    for (int w = lane * 4; w < nwp; w += 128) *reinterpret_cast<uint4*>(bm + w) = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < ITEMS; ++k)
+      if (key[k] >= 0) atomicOr(&bm[key[k] >> 5], 1u << (key[k] & 31));
+    __syncwarp();
+    int base = 0;
+    for (int w = lane * 4; w < nwp; w += 128) {  // word prefix, 4 words a lane per round
+      const uint4 q = *reinterpret_cast<const uint4*>(bm + w);
+      const int c0 = __popc(q.x), c1 = __popc(q.y), c2 = __popc(q.z), c3 = __popc(q.w);
+      const int c = c0 + c1 + c2 + c3;
+      const int inc = warp_inclusive_scan(c);
+      const int p0 = base + inc - c;
+      *reinterpret_cast<int4*>(pre + w) = make_int4(p0, p0 + c0, p0 + c0 + c1, p0 + c0 + c1 + c2);
+      base += __shfl_sync(kFull, inc, 31);
+    }
+    const int nnz = base;
+    for (int i = lane; i < nnz; i += 32) vals[i] = 0.0;
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < ITEMS; ++k) {
+      if (key[k] >= 0) {
+        const int w = key[k] >> 5;
+        atomicAdd(&vals[pre[w] + __popc(bm[w] & ((1u << (key[k] & 31)) - 1u))], val[k]);
+      }
+    }
+    __syncwarp();
+    for (int w = lane; w < nwp; w += 32) {  // words round-robin over lanes
+      uint32_t bits = bm[w];
+      int pos = pre[w];
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        a.c_col[out + pos] = static_cast<int32_t>(cb + w * 32 + b);
+        a.c_val[out + pos] = vals[pos];
+        ++pos;
+      }
+    }
+    __syncwarp();
+  }
+}
+
 // Tiny chunk (at most CAPW elements): one warp loads it into shared memory,
 // sorts (column, value) pairs with a bitonic network, merges equal columns and
 // writes the chunk in column order. No bitmap, no block barrier.
@@ -594,6 +669,25 @@ void launch_leaf_small(const ListArgs& a, int max_elems, bool symbolic, cudaStre
     auto fn = symbolic ? k_leaf_small<true, 256, 16> : k_leaf_small<false, 256, 16>;
     set_smem(fn, smem);
     (fn<<<g, 256, smem, s>>>(a, nwords), note_launch());
+  }
+}
+
+int64_t leaf_warpbm_words(int64_t width) { return ((width + 31) / 32 + 127) & ~int64_t(127); }
+
+bool leaf_warpbm_fits(int64_t width, int max_elems, int64_t smem_max) {
+  const int64_t per_warp = leaf_warpbm_words(width) * 8 + static_cast<int64_t>(max_elems) * 8;
+  return max_elems <= 512 && 4 * per_warp + 1024 <= smem_max;
+}
+
+void launch_leaf_warpbm(const ListArgs& a, int max_elems, cudaStream_t s) {
+  if (a.n_items <= 0) return;
+  const int nwp = static_cast<int>(leaf_warpbm_words(a.width));
+  const int items = max_elems <= 128 ? 4 : 16;
+  const size_t smem = 4 * (static_cast<size_t>(nwp) * 8 + static_cast<size_t>(items) * 32 * 8);
+  const unsigned g = static_cast<unsigned>(std::min<int64_t>((a.n_items + 3) / 4, 152LL * 64));
+  switch (items) {
+    case 4: set_smem(k_leaf_warpbm<4>, smem); (k_leaf_warpbm<4><<<g, 128, smem, s>>>(a, nwp), note_launch()); break;
+    default: set_smem(k_leaf_warpbm<16>, smem); (k_leaf_warpbm<16><<<g, 128, smem, s>>>(a, nwp), note_launch()); break;
   }
 }
 

@@ -134,7 +134,8 @@ __global__ void k_leaf_class(const int64_t* __restrict__ mcount, const int64_t* 
     uint8_t k = 0;
     if (c > 0) {
       if (c <= 128) k = 1;
-      else if (c <= 1024) k = 2;
+      else if (c <= 512) k = 2;
+      else if (c <= 1024) k = 7;
       else if (c <= 4096) k = 3;
       else {
         const int64_t z = nnz[nnz_base + i];
@@ -531,7 +532,8 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
   // numeric last-level chunks with known nnz: classes sized by nnz (k_leaf_class)
   const bool by_nnz = dense && numeric && p->leaf_nnz.p && la.child_of == nullptr;
   BinSpec spec = dense ? bitmap_leaf_spec() : hash_leaf_spec();
-  if (by_nnz) spec.nbins = 7;
+  if (by_nnz) spec.nbins = 8;
+  const bool warp_ok = leaf_warpbm_fits(la.width, 512, p->smem_dev);
   DevBuf<uint8_t> bins;
   DevBuf<int32_t> idx;
   DevBuf<int64_t> starts_d, items;
@@ -556,8 +558,11 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
     a.n_items = cnt;
     p->n_leaves += numeric ? 0 : cnt;
     if (by_nnz) {
-      if (b == 1) launch_leaf_warp(a, s);
-      else if (b <= 3) launch_leaf_small(a, b == 2 ? 1024 : 4096, false, s);
+      if (b == 1 && warp_ok) launch_leaf_warpbm(a, 128, s);
+      else if (b == 1) launch_leaf_warp(a, s);
+      else if (b == 2 && warp_ok) launch_leaf_warpbm(a, 512, s);
+      else if (b == 2 || b == 7) launch_leaf_small(a, 1024, false, s);
+      else if (b == 3) launch_leaf_small(a, 4096, false, s);
       else launch_leaf_bitmap(a, static_cast<int>(std::min<int64_t>(b == 4 ? 4096 : b == 5 ? 8192 : la.width, la.width)), false, s);
     } else if (dense && b <= 2) launch_leaf_small(a, b == 1 ? 1024 : 4096, !numeric, s);
     else if (dense) launch_leaf_bitmap(a, bitmap_leaf_cap(b, la.width), !numeric, s);
