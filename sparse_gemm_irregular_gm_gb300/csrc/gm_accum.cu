@@ -421,44 +421,48 @@ __global__ void __launch_bounds__(T) k_leaf_small(ListArgs a, int nwords) {
   }
 }
 
-// Small numeric chunk (at most 32 * ITEMS elements, width <= 32 * 4 * 128), one
-// warp per chunk with no block barrier, so many chunks are in flight per SM. The
-// warp's elements sit in registers; its private bitmap of the chunk's columns is
-// counted in 16-byte pieces (consecutive lanes, consecutive pieces) into a word
-// prefix, which gives every column its rank; values are added into their rank's
-// slot (chunks this small rarely repeat a column, so the atomics seldom meet),
-// and the chunk is written in column order by words.
-template <int ITEMS>
-__global__ void __launch_bounds__(128, ITEMS >= 16 ? 5 : 8) k_leaf_warpbm(ListArgs a, int nwp) {
+// Numeric chunk of at most vcap elements, one warp per chunk with no block
+// barrier, so many chunks are in flight per SM. Elements come through registers
+// 32 * ITEMS at a time (a chunk of one such tile is read once; a longer one has
+// its columns read twice, the second time from L2). The warp's private bitmap of
+// the chunk's columns is counted in 16-byte pieces (consecutive lanes,
+// consecutive pieces) into a word prefix, which gives every column its rank;
+// values are added into their rank's slot (chunks this small rarely repeat a
+// column, so the atomics seldom meet), and the chunk is written in column order
+// by words.
+template <int ITEMS, int WARPS>
+__global__ void __launch_bounds__(32 * WARPS, (ITEMS >= 16 ? 160 : 256) / WARPS) k_leaf_warpbm(ListArgs a, int nwp, int vcap) {
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr int CAPW = 32 * ITEMS;
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  unsigned char* mine = smem + static_cast<size_t>(wib) * (static_cast<size_t>(nwp) * 8 + CAPW * 8);
+  unsigned char* mine = smem + static_cast<size_t>(wib) * (static_cast<size_t>(nwp) * 8 + static_cast<size_t>(vcap) * 8);
   uint32_t* bm = reinterpret_cast<uint32_t*>(mine);                 // nwp (a multiple of 128)
   int* pre = reinterpret_cast<int*>(bm + nwp);                      // nwp
-  double* vals = reinterpret_cast<double*>(pre + nwp);              // CAPW
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + wib;
-  const int64_t nw = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  double* vals = reinterpret_cast<double*>(pre + nwp);              // vcap
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * WARPS + wib;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * WARPS;
   for (int64_t item = gw; item < a.n_items; item += nw) {
     const int64_t m = a.items[item];
     const int64_t lo = a.rp[m];
-    const int n = static_cast<int>(min(a.rp[m + 1] - lo, static_cast<int64_t>(CAPW)));
+    const int n = static_cast<int>(min(a.rp[m + 1] - lo, static_cast<int64_t>(vcap)));
     const int64_t child_local = a.child_of ? a.child_of[m] : m;
     const int64_t out = a.off_in[a.child_base + child_local];
     const int64_t cb = leaf_col_base(a, child_local);
     int key[ITEMS];
     double val[ITEMS];
-#pragma unroll
-    for (int k = 0; k < ITEMS; ++k) {
-      const int e = k * 32 + lane;
-      key[k] = e < n ? a.col[lo + e] : -1;
-      val[k] = e < n ? a.val[lo + e] : 0.0;
-    }
     for (int w = lane * 4; w < nwp; w += 128) *reinterpret_cast<uint4*>(bm + w) = make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
+    for (int t0 = 0; t0 < n; t0 += CAPW) {  // columns: set the bits
 #pragma unroll
-    for (int k = 0; k < ITEMS; ++k)
-      if (key[k] >= 0) atomicOr(&bm[key[k] >> 5], 1u << (key[k] & 31));
+      for (int k = 0; k < ITEMS; ++k) {
+        const int e = t0 + k * 32 + lane;
+        key[k] = e < n ? a.col[lo + e] : -1;
+        if (n <= CAPW) val[k] = e < n ? a.val[lo + e] : 0.0;
+      }
+#pragma unroll
+      for (int k = 0; k < ITEMS; ++k)
+        if (key[k] >= 0) atomicOr(&bm[key[k] >> 5], 1u << (key[k] & 31));
+    }
     __syncwarp();
     int base = 0;
     for (int w = lane * 4; w < nwp; w += 128) {  // word prefix, 4 words a lane per round
@@ -473,11 +477,21 @@ __global__ void __launch_bounds__(128, ITEMS >= 16 ? 5 : 8) k_leaf_warpbm(ListAr
     const int nnz = base;
     for (int i = lane; i < nnz; i += 32) vals[i] = 0.0;
     __syncwarp();
+    for (int t0 = 0; t0 < n; t0 += CAPW) {  // values into their rank's slot
+      if (n > CAPW) {
 #pragma unroll
-    for (int k = 0; k < ITEMS; ++k) {
-      if (key[k] >= 0) {
-        const int w = key[k] >> 5;
-        atomicAdd(&vals[pre[w] + __popc(bm[w] & ((1u << (key[k] & 31)) - 1u))], val[k]);
+        for (int k = 0; k < ITEMS; ++k) {
+          const int e = t0 + k * 32 + lane;
+          key[k] = e < n ? a.col[lo + e] : -1;
+          val[k] = e < n ? a.val[lo + e] : 0.0;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < ITEMS; ++k) {
+        if (key[k] >= 0) {
+          const int w = key[k] >> 5;
+          atomicAdd(&vals[pre[w] + __popc(bm[w] & ((1u << (key[k] & 31)) - 1u))], val[k]);
+        }
       }
     }
     __syncwarp();
@@ -493,6 +507,88 @@ __global__ void __launch_bounds__(128, ITEMS >= 16 ? 5 : 8) k_leaf_warpbm(ListAr
       }
     }
     __syncwarp();
+  }
+}
+
+// The same accumulator for chunks of up to vcap elements with 4 warps per chunk:
+// elements in tiles of 128 * ITEMS through registers, bitmap word prefix by a
+// block scan over 16-byte pieces, values added into their rank's slot.
+template <int ITEMS>
+__global__ void __launch_bounds__(128) k_leaf_blkbm(ListArgs a, int nwp, int vcap) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  constexpr int T = 128;
+  constexpr int CAPB = T * ITEMS;
+  uint32_t* bm = reinterpret_cast<uint32_t*>(smem);                 // nwp (a multiple of 512)
+  int* pre = reinterpret_cast<int*>(bm + nwp);                      // nwp
+  double* vals = reinterpret_cast<double*>(pre + nwp);              // vcap
+  __shared__ int ws[33];
+  for (int64_t item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+    const int64_t m = a.items[item];
+    const int64_t lo = a.rp[m];
+    const int n = static_cast<int>(min(a.rp[m + 1] - lo, static_cast<int64_t>(vcap)));
+    const int64_t child_local = a.child_of ? a.child_of[m] : m;
+    const int64_t out = a.off_in[a.child_base + child_local];
+    const int64_t cb = leaf_col_base(a, child_local);
+    int key[ITEMS];
+    double val[ITEMS];
+    for (int w = threadIdx.x * 4; w < nwp; w += 4 * T) *reinterpret_cast<uint4*>(bm + w) = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    for (int t0 = 0; t0 < n; t0 += CAPB) {  // columns: set the bits
+#pragma unroll
+      for (int k = 0; k < ITEMS; ++k) {
+        const int e = t0 + k * T + threadIdx.x;
+        key[k] = e < n ? a.col[lo + e] : -1;
+        if (n <= CAPB) val[k] = e < n ? a.val[lo + e] : 0.0;
+      }
+#pragma unroll
+      for (int k = 0; k < ITEMS; ++k)
+        if (key[k] >= 0) atomicOr(&bm[key[k] >> 5], 1u << (key[k] & 31));
+    }
+    __syncthreads();
+    int base = 0;
+    for (int w0 = 0; w0 < nwp; w0 += 4 * T) {  // word prefix, 4 words a thread per round
+      const int w = w0 + threadIdx.x * 4;
+      const uint4 q = *reinterpret_cast<const uint4*>(bm + w);
+      const int c0 = __popc(q.x), c1 = __popc(q.y), c2 = __popc(q.z), c3 = __popc(q.w);
+      int tot;
+      const int p0 = base + block_exclusive_scan(c0 + c1 + c2 + c3, ws, &tot);
+      *reinterpret_cast<int4*>(pre + w) = make_int4(p0, p0 + c0, p0 + c0 + c1, p0 + c0 + c1 + c2);
+      base += tot;
+      __syncthreads();
+    }
+    const int nnz = base;
+    for (int i = threadIdx.x; i < nnz; i += T) vals[i] = 0.0;
+    __syncthreads();
+    for (int t0 = 0; t0 < n; t0 += CAPB) {  // values into their rank's slot
+      if (n > CAPB) {
+#pragma unroll
+        for (int k = 0; k < ITEMS; ++k) {
+          const int e = t0 + k * T + threadIdx.x;
+          key[k] = e < n ? a.col[lo + e] : -1;
+          val[k] = e < n ? a.val[lo + e] : 0.0;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < ITEMS; ++k) {
+        if (key[k] >= 0) {
+          const int w = key[k] >> 5;
+          atomicAdd(&vals[pre[w] + __popc(bm[w] & ((1u << (key[k] & 31)) - 1u))], val[k]);
+        }
+      }
+    }
+    __syncthreads();
+    for (int w = threadIdx.x; w < nwp; w += T) {  // words round-robin over threads
+      uint32_t bits = bm[w];
+      int pos = pre[w];
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        a.c_col[out + pos] = static_cast<int32_t>(cb + w * 32 + b);
+        a.c_val[out + pos] = vals[pos];
+        ++pos;
+      }
+    }
+    __syncthreads();
   }
 }
 
@@ -674,21 +770,46 @@ void launch_leaf_small(const ListArgs& a, int max_elems, bool symbolic, cudaStre
 
 int64_t leaf_warpbm_words(int64_t width) { return ((width + 31) / 32 + 127) & ~int64_t(127); }
 
+// Warps per block for chunks of at most max_elems elements (the value array of
+// every warp is sized by max_elems).
+static int warpbm_warps(int max_elems) { return max_elems <= 1024 ? 4 : 1; }
+
 bool leaf_warpbm_fits(int64_t width, int max_elems, int64_t smem_max) {
   const int64_t per_warp = leaf_warpbm_words(width) * 8 + static_cast<int64_t>(max_elems) * 8;
-  return max_elems <= 512 && 4 * per_warp + 1024 <= smem_max;
+  return max_elems <= 4096 && warpbm_warps(max_elems) * per_warp + 1024 <= smem_max;
 }
 
 void launch_leaf_warpbm(const ListArgs& a, int max_elems, cudaStream_t s) {
   if (a.n_items <= 0) return;
   const int nwp = static_cast<int>(leaf_warpbm_words(a.width));
-  const int items = max_elems <= 128 ? 4 : 16;
-  const size_t smem = 4 * (static_cast<size_t>(nwp) * 8 + static_cast<size_t>(items) * 32 * 8);
-  const unsigned g = static_cast<unsigned>(std::min<int64_t>((a.n_items + 3) / 4, 152LL * 64));
-  switch (items) {
-    case 4: set_smem(k_leaf_warpbm<4>, smem); (k_leaf_warpbm<4><<<g, 128, smem, s>>>(a, nwp), note_launch()); break;
-    default: set_smem(k_leaf_warpbm<16>, smem); (k_leaf_warpbm<16><<<g, 128, smem, s>>>(a, nwp), note_launch()); break;
+  const int W = warpbm_warps(max_elems);
+  const size_t smem = W * (static_cast<size_t>(nwp) * 8 + static_cast<size_t>(max_elems) * 8);
+  const unsigned g = static_cast<unsigned>(std::min<int64_t>((a.n_items + W - 1) / W, 152LL * 64));
+  if (max_elems <= 128) {
+    set_smem(k_leaf_warpbm<4, 4>, smem);
+    (k_leaf_warpbm<4, 4><<<g, 128, smem, s>>>(a, nwp, max_elems), note_launch());
+  } else if (W == 4) {
+    set_smem(k_leaf_warpbm<16, 4>, smem);
+    (k_leaf_warpbm<16, 4><<<g, 128, smem, s>>>(a, nwp, max_elems), note_launch());
+  } else {
+    set_smem(k_leaf_warpbm<16, 1>, smem);
+    (k_leaf_warpbm<16, 1><<<g, 32, smem, s>>>(a, nwp, max_elems), note_launch());
   }
+}
+
+int64_t leaf_blkbm_words(int64_t width) { return ((width + 31) / 32 + 511) & ~int64_t(511); }
+
+bool leaf_blkbm_fits(int64_t width, int max_elems, int64_t smem_max) {
+  return leaf_blkbm_words(width) * 8 + static_cast<int64_t>(max_elems) * 8 + 1024 <= smem_max;
+}
+
+void launch_leaf_blkbm(const ListArgs& a, int max_elems, cudaStream_t s) {
+  if (a.n_items <= 0) return;
+  const int nwp = static_cast<int>(leaf_blkbm_words(a.width));
+  const size_t smem = static_cast<size_t>(nwp) * 8 + static_cast<size_t>(max_elems) * 8;
+  const unsigned g = static_cast<unsigned>(std::min<int64_t>(a.n_items, 152LL * 32));
+  set_smem(k_leaf_blkbm<8>, smem);
+  (k_leaf_blkbm<8><<<g, 128, smem, s>>>(a, nwp, max_elems), note_launch());
 }
 
 void launch_leaf_warp(const ListArgs& a, cudaStream_t s) {

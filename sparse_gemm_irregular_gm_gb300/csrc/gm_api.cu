@@ -533,7 +533,8 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
   const bool by_nnz = dense && numeric && p->leaf_nnz.p && la.child_of == nullptr;
   BinSpec spec = dense ? bitmap_leaf_spec() : hash_leaf_spec();
   if (by_nnz) spec.nbins = 8;
-  const bool warp_ok = leaf_warpbm_fits(la.width, 512, p->smem_dev);
+  const bool warp_ok = leaf_warpbm_fits(la.width, 1024, p->smem_dev);
+  const bool blk4k_ok = leaf_blkbm_fits(la.width, 4096, p->smem_dev);
   DevBuf<uint8_t> bins;
   DevBuf<int32_t> idx;
   DevBuf<int64_t> starts_d, items;
@@ -561,6 +562,8 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
       if (b == 1 && warp_ok) launch_leaf_warpbm(a, 128, s);
       else if (b == 1) launch_leaf_warp(a, s);
       else if (b == 2 && warp_ok) launch_leaf_warpbm(a, 512, s);
+      else if (b == 7 && warp_ok) launch_leaf_warpbm(a, 1024, s);
+      else if (b == 3 && blk4k_ok) launch_leaf_blkbm(a, 4096, s);
       else if (b == 2 || b == 7) launch_leaf_small(a, 1024, false, s);
       else if (b == 3) launch_leaf_small(a, 4096, false, s);
       else launch_leaf_bitmap(a, static_cast<int>(std::min<int64_t>(b == 4 ? 4096 : b == 5 ? 8192 : la.width, la.width)), false, s);

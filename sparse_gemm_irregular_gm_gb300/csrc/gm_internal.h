@@ -284,10 +284,13 @@ int leaf_bitmap_smem(int64_t width, int cap_vals, bool symbolic);
 void launch_leaf_small(const ListArgs& a, int max_elems, bool symbolic, cudaStream_t s);
 // Numeric chunks of at most 128 elements: one warp sorts and merges each.
 void launch_leaf_warp(const ListArgs& a, cudaStream_t s);
-// Numeric chunks of at most max_elems (<= 512) elements: one warp per chunk with
-// its own bitmap and rank prefix in shared memory.
+// Numeric chunks of at most max_elems (<= 4096) elements: one warp per chunk with
+// its own bitmap, rank prefix and value array in shared memory.
 void launch_leaf_warpbm(const ListArgs& a, int max_elems, cudaStream_t s);
 bool leaf_warpbm_fits(int64_t width, int max_elems, int64_t smem_max);
+// The same with 4 warps per chunk (value array of max_elems doubles per block).
+void launch_leaf_blkbm(const ListArgs& a, int max_elems, cudaStream_t s);
+bool leaf_blkbm_fits(int64_t width, int max_elems, int64_t smem_max);
 int leaf_small_smem(int64_t width, int cap, bool symbolic);
 
 // ---- whole-row bitmaps (gm_rowbitmap.cu) -----------------------------------------
