@@ -513,10 +513,9 @@ __global__ void __launch_bounds__(32 * WARPS, (ITEMS >= 16 ? 160 : 256) / WARPS)
 // The same accumulator for chunks of up to vcap elements with 4 warps per chunk:
 // elements in tiles of 128 * ITEMS through registers, bitmap word prefix by a
 // block scan over 16-byte pieces, values added into their rank's slot.
-template <int ITEMS>
-__global__ void __launch_bounds__(128) k_leaf_blkbm(ListArgs a, int nwp, int vcap) {
+template <int ITEMS, int T>
+__global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap, int ecap) {
   extern __shared__ __align__(16) unsigned char smem[];
-  constexpr int T = 128;
   constexpr int CAPB = T * ITEMS;
   uint32_t* bm = reinterpret_cast<uint32_t*>(smem);                 // nwp (a multiple of 512)
   int* pre = reinterpret_cast<int*>(bm + nwp);                      // nwp
@@ -525,7 +524,7 @@ __global__ void __launch_bounds__(128) k_leaf_blkbm(ListArgs a, int nwp, int vca
   for (int64_t item = blockIdx.x; item < a.n_items; item += gridDim.x) {
     const int64_t m = a.items[item];
     const int64_t lo = a.rp[m];
-    const int n = static_cast<int>(min(a.rp[m + 1] - lo, static_cast<int64_t>(vcap)));
+    const int n = static_cast<int>(min(a.rp[m + 1] - lo, static_cast<int64_t>(ecap)));
     const int64_t child_local = a.child_of ? a.child_of[m] : m;
     const int64_t out = a.off_in[a.child_base + child_local];
     const int64_t cb = leaf_col_base(a, child_local);
@@ -548,15 +547,20 @@ __global__ void __launch_bounds__(128) k_leaf_blkbm(ListArgs a, int nwp, int vca
     int base = 0;
     for (int w0 = 0; w0 < nwp; w0 += 4 * T) {  // word prefix, 4 words a thread per round
       const int w = w0 + threadIdx.x * 4;
-      const uint4 q = *reinterpret_cast<const uint4*>(bm + w);
+      const uint4 q = w < nwp ? *reinterpret_cast<const uint4*>(bm + w) : make_uint4(0u, 0u, 0u, 0u);
       const int c0 = __popc(q.x), c1 = __popc(q.y), c2 = __popc(q.z), c3 = __popc(q.w);
       int tot;
       const int p0 = base + block_exclusive_scan(c0 + c1 + c2 + c3, ws, &tot);
-      *reinterpret_cast<int4*>(pre + w) = make_int4(p0, p0 + c0, p0 + c0 + c1, p0 + c0 + c1 + c2);
+      if (w < nwp) *reinterpret_cast<int4*>(pre + w) = make_int4(p0, p0 + c0, p0 + c0 + c1, p0 + c0 + c1 + c2);
       base += tot;
       __syncthreads();
     }
     const int nnz = base;
+    if (nnz > vcap) {  // uniform: the chunk's class promised at most vcap columns
+      if (threadIdx.x == 0) atomicOr(a.status, kStInternal);
+      __syncthreads();
+      continue;
+    }
     for (int i = threadIdx.x; i < nnz; i += T) vals[i] = 0.0;
     __syncthreads();
     for (int t0 = 0; t0 < n; t0 += CAPB) {  // values into their rank's slot
@@ -803,13 +807,22 @@ bool leaf_blkbm_fits(int64_t width, int max_elems, int64_t smem_max) {
   return leaf_blkbm_words(width) * 8 + static_cast<int64_t>(max_elems) * 8 + 1024 <= smem_max;
 }
 
-void launch_leaf_blkbm(const ListArgs& a, int max_elems, cudaStream_t s) {
+void launch_leaf_blkbm(const ListArgs& a, int max_nnz, int max_elems, cudaStream_t s) {
   if (a.n_items <= 0) return;
   const int nwp = static_cast<int>(leaf_blkbm_words(a.width));
-  const size_t smem = static_cast<size_t>(nwp) * 8 + static_cast<size_t>(max_elems) * 8;
+  const size_t smem = static_cast<size_t>(nwp) * 8 + static_cast<size_t>(max_nnz) * 8;
   const unsigned g = static_cast<unsigned>(std::min<int64_t>(a.n_items, 152LL * 32));
-  set_smem(k_leaf_blkbm<8>, smem);
-  (k_leaf_blkbm<8><<<g, 128, smem, s>>>(a, nwp, max_elems), note_launch());
+  // threads per chunk grow with the value array so that an SM keeps ~1000 threads busy
+  if (max_nnz <= 4096) {
+    set_smem(k_leaf_blkbm<8, 128>, smem);
+    (k_leaf_blkbm<8, 128><<<g, 128, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
+  } else if (max_nnz <= 8192) {
+    set_smem(k_leaf_blkbm<8, 256>, smem);
+    (k_leaf_blkbm<8, 256><<<g, 256, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
+  } else {
+    set_smem(k_leaf_blkbm<8, 1024>, smem);
+    (k_leaf_blkbm<8, 1024><<<g, 1024, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
+  }
 }
 
 void launch_leaf_warp(const ListArgs& a, cudaStream_t s) {

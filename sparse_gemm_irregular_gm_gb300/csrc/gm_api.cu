@@ -3,6 +3,7 @@
 // multisplit, light rows through the binned shared-memory accumulators, and the
 // prefix sums that place every row and chunk of C.
 #include <algorithm>
+#include <climits>
 #include <atomic>
 #include <cstdio>
 #include <cstdlib>
@@ -563,7 +564,11 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
       else if (b == 1) launch_leaf_warp(a, s);
       else if (b == 2 && warp_ok) launch_leaf_warpbm(a, 512, s);
       else if (b == 7 && warp_ok) launch_leaf_warpbm(a, 1024, s);
-      else if (b == 3 && blk4k_ok) launch_leaf_blkbm(a, 4096, s);
+      else if (b == 3 && blk4k_ok) launch_leaf_blkbm(a, 4096, 4096, s);
+      else if (b == 4 && blk4k_ok) launch_leaf_blkbm(a, 4096, INT_MAX, s);
+      else if (b == 5 && leaf_blkbm_fits(la.width, 8192, p->smem_dev)) launch_leaf_blkbm(a, 8192, INT_MAX, s);
+      else if (b == 6 && leaf_blkbm_fits(la.width, static_cast<int>(la.width), p->smem_dev))
+        launch_leaf_blkbm(a, static_cast<int>(la.width), INT_MAX, s);
       else if (b == 2 || b == 7) launch_leaf_small(a, 1024, false, s);
       else if (b == 3) launch_leaf_small(a, 4096, false, s);
       else launch_leaf_bitmap(a, static_cast<int>(std::min<int64_t>(b == 4 ? 4096 : b == 5 ? 8192 : la.width, la.width)), false, s);

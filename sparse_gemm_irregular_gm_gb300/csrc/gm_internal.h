@@ -288,8 +288,9 @@ void launch_leaf_warp(const ListArgs& a, cudaStream_t s);
 // its own bitmap, rank prefix and value array in shared memory.
 void launch_leaf_warpbm(const ListArgs& a, int max_elems, cudaStream_t s);
 bool leaf_warpbm_fits(int64_t width, int max_elems, int64_t smem_max);
-// The same with 4 warps per chunk (value array of max_elems doubles per block).
-void launch_leaf_blkbm(const ListArgs& a, int max_elems, cudaStream_t s);
+// The same with 4 warps per chunk: chunks of at most max_elems elements (INT_MAX:
+// any) and max_nnz output columns (the value array of the block).
+void launch_leaf_blkbm(const ListArgs& a, int max_nnz, int max_elems, cudaStream_t s);
 bool leaf_blkbm_fits(int64_t width, int max_elems, int64_t smem_max);
 int leaf_small_smem(int64_t width, int cap, bool symbolic);
 
