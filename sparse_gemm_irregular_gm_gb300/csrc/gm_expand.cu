@@ -195,12 +195,14 @@ __global__ void __launch_bounds__(256) k_outer_warp(OuterArgs a, int64_t n_units
     if (g >= n_units) break;
     int64_t p = g * a.E;
     const int64_t stop = min(p + a.E, a.total);
+    const int64_t s_first = a.wg_first[g];  // slices of this unit: [s_first, s_last]
+    const int64_t s_last = g + 1 < n_units ? a.wg_first[g + 1] : a.n_slices - 1;
     int64_t e_next = -1;  // entry whose row / value sit in r_next / a_next
     int32_t r_next = 0;
     double a_next = 0.0;
     while (p < stop) {
       if (s < 0 || p < so0 || p >= so1) {  // new slice: its B row and chunk ranges
-        s = upper_floor(a.slice_off, a.wg_first[g], a.n_slices - 1, p);
+        s = p == g * a.E ? s_first : upper_floor(a.slice_off, s_first, s_last, p);
         so0 = a.slice_off[s];
         so1 = a.slice_off[s + 1];
         cp = a.col_ptr[s];
@@ -237,6 +239,15 @@ __global__ void __launch_bounds__(256) k_outer_warp(OuterArgs a, int64_t n_units
         a_next = VAL ? a.t_val[e + 1] : 0.0;
       }
       const int64_t key_row = static_cast<int64_t>(row) * a.v;
+      // the first B loads go out before the reservations (they do not depend on them)
+      uint32_t ncol[kOwU];
+      double nbv[kOwU];
+#pragma unroll
+      for (int u = 0; u < kOwU; ++u) {
+        const int64_t q = q0 + u * 32 + lane;
+        ncol[u] = q < q1 ? static_cast<uint32_t>(a.b_col[rb + q]) : 0u;
+        nbv[u] = (VAL && q < q1) ? a.b_val[rb + q] : 0.0;
+      }
       int64_t base[SLOTS];
 #pragma unroll
       for (int k = 0; k < SLOTS; ++k) {
@@ -251,9 +262,16 @@ __global__ void __launch_bounds__(256) k_outer_warp(OuterArgs a, int64_t n_units
         double bv[kOwU];
 #pragma unroll
         for (int u = 0; u < kOwU; ++u) {
-          const int64_t q = qb + u * 32 + lane;
-          col[u] = q < q1 ? static_cast<uint32_t>(a.b_col[rb + q]) : 0u;
-          bv[u] = (VAL && q < q1) ? a.b_val[rb + q] : 0.0;
+          col[u] = ncol[u];
+          bv[u] = nbv[u];
+        }
+        if (qb + 32 * kOwU < q1) {  // the next step's loads in flight while this one is stored
+#pragma unroll
+          for (int u = 0; u < kOwU; ++u) {
+            const int64_t q = qb + 32 * kOwU + u * 32 + lane;
+            ncol[u] = q < q1 ? static_cast<uint32_t>(a.b_col[rb + q]) : 0u;
+            nbv[u] = (VAL && q < q1) ? a.b_val[rb + q] : 0.0;
+          }
         }
 #pragma unroll
         for (int u = 0; u < kOwU; ++u) {
