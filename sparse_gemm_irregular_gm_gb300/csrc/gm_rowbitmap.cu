@@ -31,22 +31,54 @@ __device__ __forceinline__ void zero_words(uint32_t* bm, int nwords) {
   for (int i = (n4 << 2) + threadIdx.x; i < nwords; i += blockDim.x) bm[i] = 0u;
 }
 
-// Walk over the products of row r. Warp w takes the A entries w, w + nwarps, ...
-// (every warp busy even on rows with few entries); their metadata is loaded 32
-// entries at a time, then the lanes run along each entry's B row with 4
-// independent loads in flight. Calls f(q, av): q[u] the position in B of product
-// u (-1 when past the row's end), av the A entry's value (when WITH_A).
-constexpr int kLongRow = 4096;   // B rows longer than this are walked by the whole block
-constexpr int kMaxLong = 64;     // deferred long rows kept per pass (more are walked by their warp)
+// Sets the bits of the B columns col[s0, s1) with a group of G threads (thread i
+// of the group): up to 3 leading columns one by one until 16-byte alignment,
+// then 4 columns per 16-byte load with 4 loads in flight per thread, then the
+// trailing columns.
+__device__ __forceinline__ void mark_segment(const int32_t* __restrict__ col, int64_t s0, int64_t s1, uint32_t* bm,
+                                             int i, int G) {
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(col + s0);
+  const int64_t head = min(static_cast<int64_t>(((16 - (addr & 15)) & 15) >> 2), s1 - s0);
+  if (i < head) {
+    const uint32_t c = static_cast<uint32_t>(col[s0 + i]);
+    atomicOr(&bm[c >> 5], 1u << (c & 31));
+  }
+  const int64_t a0 = s0 + head;
+  const int64_t n4 = (s1 - a0) >> 2;
+  const int4* v = reinterpret_cast<const int4*>(col + a0);
+  for (int64_t j = i; j < n4; j += 4 * static_cast<int64_t>(G)) {
+    int4 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = j + u * G < n4 ? v[j + u * G] : make_int4(-1, -1, -1, -1);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (x[u].x < 0) continue;
+      const uint32_t c[4] = {static_cast<uint32_t>(x[u].x), static_cast<uint32_t>(x[u].y),
+                             static_cast<uint32_t>(x[u].z), static_cast<uint32_t>(x[u].w)};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) atomicOr(&bm[c[t] >> 5], 1u << (c[t] & 31));
+    }
+  }
+  const int64_t t0 = a0 + (n4 << 2);
+  if (i < s1 - t0) {
+    const uint32_t c = static_cast<uint32_t>(col[t0 + i]);
+    atomicOr(&bm[c >> 5], 1u << (c & 31));
+  }
+}
+
+// Sets the bit of every product column of row r. Warp w takes the A entries w,
+// w + nwarps, ... (every warp busy even on rows with few entries); their
+// metadata is loaded 32 entries at a time, then the warp marks each entry's B
+// row; B rows longer than kLongRow are marked afterwards by the whole block.
+constexpr int kLongRow = 4096;
+constexpr int kMaxLong = 64;     // deferred long rows kept per row (more are marked by their warp)
 
 struct LongRows {
   int n;
   int64_t s0[kMaxLong], s1[kMaxLong];
-  double av[kMaxLong];
 };
 
-template <bool WITH_A, class F>
-__device__ __forceinline__ void walk_products(const RowBitmapArgs& a, int64_t r, LongRows& longs, F&& f) {
+__device__ __forceinline__ void mark_row(const RowBitmapArgs& a, int64_t r, uint32_t* bm, LongRows& longs) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int64_t lo = a.a_rp[r], hi = a.a_rp[r + 1];
   if (threadIdx.x == 0) longs.n = 0;
@@ -54,60 +86,28 @@ __device__ __forceinline__ void walk_products(const RowBitmapArgs& a, int64_t r,
   for (int64_t g = lo + warp; g < hi; g += static_cast<int64_t>(nwarps) * 32) {
     const int64_t p = g + static_cast<int64_t>(lane) * nwarps;
     int64_t bs = 0, be = 0;
-    double aval = 0.0;
     if (p < hi) {
       const int k = a.a_col[p];
       bs = a.b_rp[k];
       be = a.b_rp[k + 1];
-      if (WITH_A) aval = a.a_val[p];
     }
-    // long rows go to the shared list when there is room
-    if (be - bs > kLongRow) {
+    if (be - bs > kLongRow) {  // long rows go to the shared list when there is room
       const int slot = atomicAdd(&longs.n, 1);
       if (slot < kMaxLong) {
         longs.s0[slot] = bs;
         longs.s1[slot] = be;
-        longs.av[slot] = aval;
         be = bs;
       }
     }
     const unsigned live = __ballot_sync(kFull, be > bs);
     for (unsigned m = live; m; m &= m - 1) {
       const int j = __ffs(m) - 1;
-      const int64_t s0 = __shfl_sync(kFull, bs, j), s1 = __shfl_sync(kFull, be, j);
-      const double av = WITH_A ? __shfl_sync(kFull, aval, j) : 0.0;
-      for (int64_t q0 = s0 + lane; q0 < s1; q0 += 128) {
-        int64_t q[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) q[u] = q0 + u * 32 < s1 ? q0 + u * 32 : -1;
-        f(q, av);
-      }
+      mark_segment(a.b_col, __shfl_sync(kFull, bs, j), __shfl_sync(kFull, be, j), bm, lane, 32);
     }
   }
   __syncthreads();
   const int nl = min(longs.n, kMaxLong);
-  for (int i = 0; i < nl; ++i) {  // block-wide, no barrier needed between rows
-    const int64_t s0 = longs.s0[i], s1 = longs.s1[i];
-    const int T = blockDim.x;
-    for (int64_t q0 = s0 + threadIdx.x; q0 < s1; q0 += 4 * T) {
-      int64_t q[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) q[u] = q0 + u * T < s1 ? q0 + u * T : -1;
-      f(q, longs.av[i]);
-    }
-  }
-}
-
-// Sets the bit of every product column of row r.
-__device__ __forceinline__ void mark_row(const RowBitmapArgs& a, int64_t r, uint32_t* bm, LongRows& longs) {
-  walk_products<false>(a, r, longs, [&](const int64_t (&q)[4], double) {
-    uint32_t c[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) c[u] = q[u] >= 0 ? static_cast<uint32_t>(a.b_col[q[u]]) : 0u;
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (q[u] >= 0) atomicOr(&bm[c[u] >> 5], 1u << (c[u] & 31));
-  });
+  for (int i = 0; i < nl; ++i) mark_segment(a.b_col, longs.s0[i], longs.s1[i], bm, threadIdx.x, blockDim.x);
 }
 
 // Number of set bits in [lo, hi).
