@@ -137,6 +137,7 @@ __global__ void k_leaf_class(const int64_t* __restrict__ mcount, const int64_t* 
       if (c <= 128) k = 1;
       else if (c <= 512) k = 2;
       else if (c <= 1024) k = 7;
+      else if (c <= 2048) k = 8;
       else if (c <= 4096) k = 3;
       else {
         const int64_t z = nnz[nnz_base + i];
@@ -533,7 +534,7 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
   // numeric last-level chunks with known nnz: classes sized by nnz (k_leaf_class)
   const bool by_nnz = dense && numeric && p->leaf_nnz.p && la.child_of == nullptr;
   BinSpec spec = dense ? bitmap_leaf_spec() : hash_leaf_spec();
-  if (by_nnz) spec.nbins = 8;
+  if (by_nnz) spec.nbins = 9;
   const bool warp_ok = leaf_warpbm_fits(la.width, 1024, p->smem_dev);
   const bool blk4k_ok = leaf_blkbm_fits(la.width, 4096, p->smem_dev);
   DevBuf<uint8_t> bins;
@@ -564,13 +565,14 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
       else if (b == 1) launch_leaf_warp(a, s);
       else if (b == 2 && warp_ok) launch_leaf_warpbm(a, 512, s);
       else if (b == 7 && warp_ok) launch_leaf_warpbm(a, 1024, s);
+      else if (b == 8 && blk4k_ok) launch_leaf_blkbm(a, 2048, 2048, s);
       else if (b == 3 && blk4k_ok) launch_leaf_blkbm(a, 4096, 4096, s);
       else if (b == 4 && blk4k_ok) launch_leaf_blkbm(a, 4096, INT_MAX, s);
       else if (b == 5 && leaf_blkbm_fits(la.width, 8192, p->smem_dev)) launch_leaf_blkbm(a, 8192, INT_MAX, s);
       else if (b == 6 && leaf_blkbm_fits(la.width, static_cast<int>(la.width), p->smem_dev))
         launch_leaf_blkbm(a, static_cast<int>(la.width), INT_MAX, s);
       else if (b == 2 || b == 7) launch_leaf_small(a, 1024, false, s);
-      else if (b == 3) launch_leaf_small(a, 4096, false, s);
+      else if (b == 3 || b == 8) launch_leaf_small(a, 4096, false, s);
       else launch_leaf_bitmap(a, static_cast<int>(std::min<int64_t>(b == 4 ? 4096 : b == 5 ? 8192 : la.width, la.width)), false, s);
     } else if (dense && b <= 2) launch_leaf_small(a, b == 1 ? 1024 : 4096, !numeric, s);
     else if (dense) launch_leaf_bitmap(a, bitmap_leaf_cap(b, la.width), !numeric, s);

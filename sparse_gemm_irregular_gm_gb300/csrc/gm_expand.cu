@@ -181,8 +181,10 @@ __global__ void __launch_bounds__(kOpThreads) k_outer(OuterArgs a) {
 constexpr int kOwU = 4;
 
 template <bool VAL, int SLOTS>
-__global__ void __launch_bounds__(256) k_outer_warp(OuterArgs a, int64_t n_units, unsigned* unit_counter) {
+__global__ void __launch_bounds__(256, 4) k_outer_warp(OuterArgs a, int64_t n_units, unsigned* unit_counter) {
+  __shared__ int64_t s_bases[8][SLOTS * 32];  // per warp: destination base of each chunk of the portion
   const int lane = threadIdx.x & 31;
+  int64_t* const s_base = s_bases[threadIdx.x >> 5];
   const uint32_t mask = (1u << a.shift) - 1u;
   const int vp1 = a.v + 1;
   int64_t s = -1, rb = 0, L = 1, so0 = 0, so1 = 0, cp = 0;  // cached slice
@@ -197,9 +199,11 @@ __global__ void __launch_bounds__(256) k_outer_warp(OuterArgs a, int64_t n_units
     const int64_t stop = min(p + a.E, a.total);
     const int64_t s_first = a.wg_first[g];  // slices of this unit: [s_first, s_last]
     const int64_t s_last = g + 1 < n_units ? a.wg_first[g + 1] : a.n_slices - 1;
-    int64_t e_next = -1;  // entry whose row / value sit in r_next / a_next
-    int32_t r_next = 0;
-    double a_next = 0.0;
+    int64_t eb = -64;      // entries [eb, eb + 32) have their row / A value in lane (e - eb); none yet
+    int32_t rowb = 0;
+    double avb = 0.0;
+    int64_t e_res = -1;    // entry whose runs were reserved ahead (destinations in base_next)
+    int64_t base_next[SLOTS];
     while (p < stop) {
       if (s < 0 || p < so0 || p >= so1) {  // new slice: its B row and chunk ranges
         s = p == g * a.E ? s_first : upper_floor(a.slice_off, s_first, s_last, p);
@@ -211,6 +215,7 @@ __global__ void __launch_bounds__(256) k_outer_warp(OuterArgs a, int64_t n_units
         c_lo = static_cast<int>(static_cast<uint32_t>(a.b_col[rb]) >> a.shift);
         const int c_hi = static_cast<int>(static_cast<uint32_t>(a.b_col[rb + L - 1]) >> a.shift);
         nslots = (c_hi - c_lo + 32) >> 5;
+        eb = -64;  // the row batch holds entries of the previous slice only
         const int32_t* const t = a.bcp + s * vp1;
 #pragma unroll
         for (int k = 0; k < SLOTS; ++k) {
@@ -224,40 +229,61 @@ __global__ void __launch_bounds__(256) k_outer_warp(OuterArgs a, int64_t n_units
       const int64_t e = cp + rel / L;
       const int64_t q0 = rel % L;
       const int64_t q1 = min(L, q0 + (stop - p));
-      int32_t row;
-      double av;
-      if (e == e_next) {
-        row = r_next;
-        av = a_next;
-      } else {
-        row = a.t_row[e];
-        av = VAL ? a.t_val[e] : 0.0;
+      const int64_t e_end = cp + (so1 - so0) / L;  // entries of this slice end here
+      if (e < eb || e >= eb + 32) {  // rows and A values of the next 32 entries, one load each
+        eb = e;
+        rowb = e + lane < e_end ? a.t_row[e + lane] : 0;
+        avb = (VAL && e + lane < e_end) ? a.t_val[e + lane] : 0.0;
       }
-      if (e + 1 < cp + (so1 - so0) / L) {  // next entry of the slice, loaded while this one streams
-        e_next = e + 1;
-        r_next = a.t_row[e + 1];
-        a_next = VAL ? a.t_val[e + 1] : 0.0;
-      }
+      const int32_t row = __shfl_sync(kFull, rowb, static_cast<int>(e - eb));
+      const double av = VAL ? __shfl_sync(kFull, avb, static_cast<int>(e - eb)) : 0.0;
       const int64_t key_row = static_cast<int64_t>(row) * a.v;
       // the first B loads go out before the reservations (they do not depend on them)
+      const int32_t* const bc = a.b_col + rb;
+      const double* const bvp = a.b_val + rb;
+      const int iq0 = static_cast<int>(q0), iq1 = static_cast<int>(q1);
       uint32_t ncol[kOwU];
       double nbv[kOwU];
 #pragma unroll
       for (int u = 0; u < kOwU; ++u) {
-        const int64_t q = q0 + u * 32 + lane;
-        ncol[u] = q < q1 ? static_cast<uint32_t>(a.b_col[rb + q]) : 0u;
-        nbv[u] = (VAL && q < q1) ? a.b_val[rb + q] : 0.0;
+        const int q = iq0 + u * 32 + lane;
+        ncol[u] = q < iq1 ? static_cast<uint32_t>(bc[q]) : 0u;
+        nbv[u] = (VAL && q < iq1) ? bvp[q] : 0.0;
       }
-      int64_t base[SLOTS];
+      // run destinations: dst of position q in chunk c_lo + i is s_base[i] + q
+      __syncwarp();
+      if (e == e_res) {  // reserved while the previous entry streamed
 #pragma unroll
-      for (int k = 0; k < SLOTS; ++k) {
-        base[k] = 0;
-        const int64_t x0 = max(q0, static_cast<int64_t>(T0[k])), x1 = min(q1, static_cast<int64_t>(T1[k]));
-        if (k < nslots && x1 > x0)
-          base[k] = static_cast<int64_t>(atomicAdd(&a.cursor[key_row + c_lo + k * 32 + lane],
-                                                   static_cast<unsigned long long>(x1 - x0))) - x0;
+        for (int k = 0; k < SLOTS; ++k)
+          if (k < nslots) s_base[k * 32 + lane] = base_next[k];
+      } else {
+#pragma unroll
+        for (int k = 0; k < SLOTS; ++k) {
+          const int64_t x0 = max(q0, static_cast<int64_t>(T0[k])), x1 = min(q1, static_cast<int64_t>(T1[k]));
+          if (k < nslots && x1 > x0)
+            s_base[k * 32 + lane] = static_cast<int64_t>(atomicAdd(&a.cursor[key_row + c_lo + k * 32 + lane],
+                                                                   static_cast<unsigned long long>(x1 - x0))) - x0;
+        }
       }
-      for (int64_t qb = q0; qb < q1; qb += 32 * kOwU) {
+      __syncwarp();
+      {  // reserve the next entry's runs now; the results are only read after this entry streams
+        const int64_t pn = p + (q1 - q0);
+        e_res = -1;
+        if (q1 == L && pn < stop && pn < so1 && e + 1 < eb + 32) {
+          const int64_t qn1 = min(L, stop - pn);
+          const int64_t key_n = static_cast<int64_t>(__shfl_sync(kFull, rowb, static_cast<int>(e + 1 - eb))) * a.v;
+#pragma unroll
+          for (int k = 0; k < SLOTS; ++k) {
+            const int64_t x0 = static_cast<int64_t>(T0[k]), x1 = min(qn1, static_cast<int64_t>(T1[k]));
+            base_next[k] = 0;
+            if (k < nslots && x1 > x0)
+              base_next[k] = static_cast<int64_t>(atomicAdd(&a.cursor[key_n + c_lo + k * 32 + lane],
+                                                            static_cast<unsigned long long>(x1 - x0))) - x0;
+          }
+          e_res = e + 1;
+        }
+      }
+      for (int qb = iq0; qb < iq1; qb += 32 * kOwU) {
         uint32_t col[kOwU];
         double bv[kOwU];
 #pragma unroll
@@ -265,28 +291,19 @@ __global__ void __launch_bounds__(256) k_outer_warp(OuterArgs a, int64_t n_units
           col[u] = ncol[u];
           bv[u] = nbv[u];
         }
-        if (qb + 32 * kOwU < q1) {  // the next step's loads in flight while this one is stored
+        if (qb + 32 * kOwU < iq1) {  // the next step's loads in flight while this one is stored
 #pragma unroll
           for (int u = 0; u < kOwU; ++u) {
-            const int64_t q = qb + 32 * kOwU + u * 32 + lane;
-            ncol[u] = q < q1 ? static_cast<uint32_t>(a.b_col[rb + q]) : 0u;
-            nbv[u] = (VAL && q < q1) ? a.b_val[rb + q] : 0.0;
+            const int q = qb + 32 * kOwU + u * 32 + lane;
+            ncol[u] = q < iq1 ? static_cast<uint32_t>(bc[q]) : 0u;
+            nbv[u] = (VAL && q < iq1) ? bvp[q] : 0.0;
           }
         }
 #pragma unroll
         for (int u = 0; u < kOwU; ++u) {
-          const int64_t q = qb + u * 32 + lane;
-          const int idx = q < q1 ? static_cast<int>(col[u] >> a.shift) - c_lo : 0;
-          int64_t b = 0;
-#pragma unroll
-          for (int k = 0; k < SLOTS; ++k) {
-            if (k < nslots) {
-              const int64_t x = __shfl_sync(kFull, base[k], idx & 31);
-              if ((idx >> 5) == k) b = x;
-            }
-          }
-          if (q < q1) {
-            const int64_t dst = b + q;
+          const int q = qb + u * 32 + lane;
+          if (q < iq1) {
+            const int64_t dst = s_base[static_cast<int>(col[u] >> a.shift) - c_lo] + q;
             a.out_col[dst] = static_cast<int32_t>(col[u] & mask);
             if (VAL) a.out_val[dst] = av * bv[u];
           }
