@@ -617,36 +617,36 @@ static gm_status rowwise_leaves(gm_plan* p, int64_t nb, const int64_t* rrp, cons
   return cuda_status(p, cudaGetLastError());
 }
 
-// Row-order pipeline when B's rows are sorted: the batch rows' A entries are
-// transposed (masked CSR -> CSC, as for the outer product) and the outer
-// product writes every product straight into its level-0 chunk, reserving one
-// range per run of an entry's B row inside a chunk (k_outer_warp). C-hat is
-// never written; chunk sizes come from the symbolic pass.
+// Chunk-direct pipeline when B's rows are sorted: the batch rows' A entries are
+// gathered in row order, and the expansion writes every product straight into
+// its level-0 chunk, one contiguous block per (unit of products, row, chunk)
+// (k_expand_rows). C-hat is never written; chunk sizes and per-B-row chunk
+// starts come from the symbolic pass.
 static gm_status run_batch_runs(gm_plan* p, int64_t h0, int64_t h1, int64_t* par_base, int32_t* c_col,
                                 double* c_val) {
   const cudaStream_t s = p->s;
   const int64_t nb = h1 - h0;
   const int64_t ip = p->h_chat_rp[h1] - p->h_chat_rp[h0];
-  const int64_t anz = p->h_anz[h1] - p->h_anz[h0];
+  const int64_t ne = p->h_anz[h1] - p->h_anz[h0];
   const int32_t* heavy = p->rows_by_bin.p + p->bin_start[kHeavyBin] + h0;
-  const int64_t ncols = p->A.n_cols;
   const int v = static_cast<int>(p->P.v_chunks[0]);
   const int64_t children = nb * v;
   if (p->arena_col[0].n < static_cast<size_t>(ip) || p->arena_val[0].n < static_cast<size_t>(ip))
     return GM_ERR_WORKSPACE;
 
   int t = p->stage_begin(GM_STAGE_TRANSPOSE);
-  DevBuf<int64_t> col_ptr, slice_off;
-  DevBuf<int32_t> t_row, wg_op;
-  DevBuf<double> t_val;
-  const int64_t n_wg_op = (ip + kOuterE - 1) / kOuterE;
-  if (!col_ptr.alloc(ncols + 1, s) || !slice_off.alloc(ncols + 1, s) || !t_row.alloc(anz, s) ||
-      !t_val.alloc(anz, s) || !wg_op.alloc(n_wg_op, s))
+  DevBuf<int32_t> e_row, e_k;
+  DevBuf<double> e_a;
+  DevBuf<int64_t> e_b, e_off, ufirst;
+  const int64_t U = row_runs_unit(p->P.tau);
+  const int64_t n_units = (ip + U - 1) / U;
+  if (!e_b.alloc(ne, s) || !e_row.alloc(ne, s) || !e_a.alloc(ne, s) || !e_off.alloc(ne + 1, s) ||
+      !e_k.alloc(ne, s) || !ufirst.alloc(std::max<int64_t>(n_units, 1), s))
     return GM_ERR_OOM;
-  TransposeArgs ta{heavy, nb, p->A.row_ptr, p->A.col_idx, p->A.vals, ncols};
-  if (!masked_transpose(ta, anz, col_ptr.p, t_row.p, t_val.p, s)) return GM_ERR_OOM;
-  if (!slice_offsets(col_ptr.p, p->B.row_ptr, ncols, slice_off.p, s)) return GM_ERR_OOM;
-  launch_wg_slice(slice_off.p, ncols, ip, kOuterE, wg_op.p, s);
+  launch_gather_entries(heavy, nb, p->anz.p + h0, p->A.row_ptr, p->A.col_idx, p->A.vals, p->B.row_ptr, e_b.p, e_a.p,
+                        e_row.p, e_off.p, s, e_k.p);
+  cudaMemsetAsync(e_off.p + ne, 0, sizeof(int64_t), s);
+  if (!scan_exclusive_i64(e_off.p, e_off.p, ne + 1, nullptr, s)) return GM_ERR_OOM;
   p->stage_end(t);
 
   t = p->stage_begin(GM_STAGE_HISTOGRAM);
@@ -659,31 +659,35 @@ static gm_status run_batch_runs(gm_plan* p, int64_t h0, int64_t h1, int64_t* par
   p->stage_end(t);
 
   t = p->stage_begin(GM_STAGE_MULTISPLIT);
-  OuterArgs oa{};
-  oa.slice_off = slice_off.p;
-  oa.col_ptr = col_ptr.p;
-  oa.t_row = t_row.p;
-  oa.t_val = t_val.p;
-  oa.b_rp = p->B.row_ptr;
-  oa.b_col = p->B.col_idx;
-  oa.b_val = p->B.vals;
-  oa.n_slices = ncols;
-  oa.total = ip;
-  oa.E = kOuterE;
-  oa.wg_first = wg_op.p;
-  oa.cursor = cur.p;
-  oa.out_col = p->arena_col[0].p;
-  oa.out_val = p->arena_val[0].p;
-  oa.v = v;
-  oa.shift = ilog2(p->P.widths[0]);
-  oa.bcp = p->bcp.p;
-  launch_outer_split(oa, p->work_counter.p, p->num_sms, s);
+  RowRunArgs ra{};
+  ra.e_k = e_k.p;
+  ra.e_b = e_b.p;
+  ra.e_a = e_a.p;
+  ra.e_off = e_off.p;
+  ra.e_row = e_row.p;
+  ra.n_e = ne;
+  ra.total = ip;
+  ra.U = U;
+  ra.n_units = n_units;
+  ra.unit_first = ufirst.p;
+  ra.b_col = p->B.col_idx;
+  ra.b_val = p->B.vals;
+  ra.bcp = p->bcp.p;
+  ra.v = v;
+  ra.shift = ilog2(p->P.widths[0]);
+  ra.cursor = cur.p;
+  ra.out_col = p->arena_col[0].p;
+  ra.out_val = p->arena_val[0].p;
+  ra.unit_counter = p->work_counter.p;
+  ra.status = p->status.p;
+  launch_row_runs(ra, p->num_sms, s);
   p->stage_end(t);
-  t_row.release();
-  t_val.release();
-  col_ptr.release();
-  slice_off.release();
-  wg_op.release();
+  e_b.release();
+  e_a.release();
+  e_row.release();
+  e_off.release();
+  e_k.release();
+  ufirst.release();
   cur.release();
   return rowwise_leaves(p, nb, rrp.p, mcount, par_base, c_col, c_val);
 }
@@ -699,7 +703,7 @@ static gm_status run_batch_rowwise(gm_plan* p, int64_t h0, int64_t h1, int64_t* 
   const int64_t children = nb * v;
   if (p->arena_col[0].n < static_cast<size_t>(ip)) return GM_ERR_WORKSPACE;
 
-  if (p->b_sorted) return run_batch_runs(p, h0, h1, par_base, c_col, c_val);
+  if (p->b_sorted && p->P.v_chunks[0] <= 64) return run_batch_runs(p, h0, h1, par_base, c_col, c_val);
   if (ne >= INT32_MAX) return GM_ERR_INDEX_OVERFLOW;  // entries are indexed by int32 inside the kernels
   int t = p->stage_begin(GM_STAGE_TRANSPOSE);
   DevBuf<int32_t> e_row;

@@ -227,7 +227,35 @@ constexpr int kExpandCap = 1024;  // entries starting inside a work group (at mo
 // Builds the batch entry arrays (e_len into e_off, then the caller scans it).
 void launch_gather_entries(const int32_t* heavy_rows, int64_t nb, const int64_t* anz_batch, const int64_t* a_rp,
                            const int32_t* a_col, const double* a_val, const int64_t* b_rp, int64_t* e_b,
-                           double* e_a, int32_t* e_row, int64_t* e_len, cudaStream_t s);
+                           double* e_a, int32_t* e_row, int64_t* e_len, cudaStream_t s, int32_t* e_k = nullptr);
+
+// Row-order expansion into level-0 chunks with one reservation per (unit, row,
+// chunk) and contiguous writes per warp (B rows sorted; per-B-row chunk starts
+// in bcp; v <= 64). Units are U consecutive products of the batch in row order.
+struct RowRunArgs {
+  const int32_t* e_k;         // B row of each entry
+  const int64_t* e_b;         // B.rowPtr of that row
+  const double* e_a;          // A value (null: columns only)
+  const int64_t* e_off;       // flattened start of each entry's products, n_e + 1
+  const int32_t* e_row;       // batch-local row of each entry
+  int64_t n_e;
+  int64_t total;              // products of the batch
+  int64_t U;                  // products per unit (row_runs_unit)
+  int64_t n_units;
+  int64_t* unit_first;        // n_units scratch: first entry of each unit
+  const int32_t* b_col;
+  const double* b_val;
+  const int32_t* bcp;
+  int v;
+  int shift;
+  unsigned long long* cursor; // per chunk (row * v + c): write cursor
+  int32_t* out_col;
+  double* out_val;
+  unsigned* unit_counter;
+  int* status;
+};
+int64_t row_runs_unit(int64_t tau);
+void launch_row_runs(const RowRunArgs& a, int num_sms, cudaStream_t s);
 // Work-group bounds: multiples of kExpandE merged with the starts of every
 // kExpandCap-th entry; bounds has n_wg + 1 entries, wg_info n_wg.
 int64_t expand_num_wg(int64_t total, int64_t n_e);

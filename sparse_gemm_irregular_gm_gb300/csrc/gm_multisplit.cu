@@ -12,6 +12,8 @@
 // prefix sum gives local offsets, elements are permuted into shared buffers and
 // then written out chunk-run by chunk-run (consecutive threads -> consecutive
 // addresses) with the column shifted into the chunk's local range.
+#include <algorithm>
+
 #include "gm_device.cuh"
 #include "gm_internal.h"
 
@@ -250,7 +252,7 @@ __global__ void k_gather_entries(const int32_t* __restrict__ rows, int64_t nb, c
                                  const int64_t* __restrict__ a_rp, const int32_t* __restrict__ a_col,
                                  const double* __restrict__ a_val, const int64_t* __restrict__ b_rp,
                                  int64_t* __restrict__ e_b, double* __restrict__ e_a, int32_t* __restrict__ e_row,
-                                 int64_t* __restrict__ e_len) {
+                                 int64_t* __restrict__ e_len, int32_t* __restrict__ e_k) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -262,6 +264,7 @@ __global__ void k_gather_entries(const int32_t* __restrict__ rows, int64_t nb, c
       const int k = a_col[p];
       const int64_t b0 = b_rp[k];
       e_b[i] = b0;
+      if (e_k) e_k[i] = k;
       if (e_a) e_a[i] = a_val[p];
       e_row[i] = static_cast<int32_t>(h);
       e_len[i] = b_rp[k + 1] - b0;
@@ -501,10 +504,10 @@ bool expand_fits(int v, int64_t w, int64_t tau, size_t smem) {
 
 void launch_gather_entries(const int32_t* heavy_rows, int64_t nb, const int64_t* anz_batch, const int64_t* a_rp,
                            const int32_t* a_col, const double* a_val, const int64_t* b_rp, int64_t* e_b,
-                           double* e_a, int32_t* e_row, int64_t* e_len, cudaStream_t s) {
+                           double* e_a, int32_t* e_row, int64_t* e_len, cudaStream_t s, int32_t* e_k) {
   if (nb <= 0) return;
   (k_gather_entries<<<grid_for(nb * 32, 256), 256, 0, s>>>(heavy_rows, nb, anz_batch, a_rp, a_col, a_val, b_rp, e_b,
-                                                           e_a, e_row, e_len), note_launch());
+                                                           e_a, e_row, e_len, e_k), note_launch());
 }
 
 int64_t expand_num_wg(int64_t total, int64_t n_e) {
@@ -529,6 +532,154 @@ void launch_expand_split(const ExpandArgs& a, cudaStream_t s) {
     cudaFuncSetAttribute(k_expand_split<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     (k_expand_split<false><<<static_cast<unsigned>(a.n_wg), kExThreads, smem, s>>>(a), note_launch());
   }
+}
+
+namespace {
+
+// Row-order expansion into the level-0 chunks with long contiguous writes (B
+// rows sorted, per-B-row chunk starts in a.bcp). The batch's heavy products, in
+// row order, are cut into units of a.U; one block takes a unit at a time:
+//  1. each warp walks its share of the unit's A entries (entry e_lo + w, + 8, ...)
+//     and counts, from the chunk starts of each entry's B row, how many of its
+//     products fall in every (row, chunk) -- lane l holds chunks l and l + 32;
+//  2. every (row, chunk) of the unit is reserved with one atomic add, and each
+//     warp gets its own consecutive part of that range;
+//  3. the warps walk their entries again and write the products: a run of one
+//     entry in one chunk goes to the warp's cursor for that chunk.
+// So each chunk of a row receives one contiguous block per unit (about
+// U / 64 elements) instead of one short run per A entry.
+constexpr int kRrWarps = 8;
+constexpr int kRrRows = 8;   // rows a unit may touch (a.U keeps it below this)
+constexpr int kRrU = 4;
+
+template <bool VAL>
+__global__ void __launch_bounds__(kRrWarps * 32) k_expand_rows(RowRunArgs a) {
+  __shared__ int s_cnt[kRrWarps][kRrRows][64];  // counts, then each warp's offset inside the reservation
+  __shared__ int64_t s_rbase[kRrRows][64];       // reservation of each (row, chunk) of the unit
+  __shared__ int64_t s_base[kRrWarps][64];
+  __shared__ int64_t s_unit;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const uint32_t mask = (1u << a.shift) - 1u;
+  const int v = a.v, vp1 = a.v + 1;
+  while (true) {
+    if (threadIdx.x == 0) s_unit = static_cast<int64_t>(atomicAdd(a.unit_counter, 1u));
+    for (int i = threadIdx.x; i < kRrWarps * kRrRows * 64; i += blockDim.x) (&s_cnt[0][0][0])[i] = 0;
+    __syncthreads();
+    const int64_t g = s_unit;
+    if (g >= a.n_units) break;
+    const int64_t P0 = g * a.U, P1 = min(P0 + a.U, a.total);
+    const int64_t e_lo = a.unit_first[g];
+    const int32_t row0 = a.e_row[e_lo];
+    // 1. counts per (row, chunk), per warp
+    for (int64_t e = e_lo + w; e < a.n_e; e += kRrWarps) {
+      const int64_t o0 = a.e_off[e];
+      if (o0 >= P1) break;
+      const int64_t o1 = a.e_off[e + 1];
+      if (o1 <= o0) continue;
+      const int64_t q0 = max(P0, o0) - o0, q1 = min(P1, o1) - o0;
+      const int slot = a.e_row[e] - row0;
+      if (slot < 0 || slot >= kRrRows) {
+        if (lane == 0) atomicOr(a.status, kStGroupRows);
+        continue;
+      }
+      const int32_t* const t = a.bcp + static_cast<int64_t>(a.e_k[e]) * vp1;
+      for (int c = lane; c < v; c += 32)
+        s_cnt[w][slot][c] += static_cast<int>(max(int64_t(0), min(q1, static_cast<int64_t>(t[c + 1])) -
+                                                                  max(q0, static_cast<int64_t>(t[c]))));
+    }
+    __syncthreads();
+    // 2. one reservation per (row, chunk); consecutive parts per warp
+    for (int i = threadIdx.x; i < kRrRows * v; i += blockDim.x) {
+      const int slot = i / v, c = i - slot * v;
+      int tot = 0;
+#pragma unroll
+      for (int ww = 0; ww < kRrWarps; ++ww) tot += s_cnt[ww][slot][c];
+      if (tot > 0) {
+        s_rbase[slot][c] = static_cast<int64_t>(atomicAdd(&a.cursor[static_cast<int64_t>(row0 + slot) * v + c],
+                                                          static_cast<unsigned long long>(tot)));
+        int run = 0;
+#pragma unroll
+        for (int ww = 0; ww < kRrWarps; ++ww) {
+          const int x = s_cnt[ww][slot][c];
+          s_cnt[ww][slot][c] = run;
+          run += x;
+        }
+      }
+    }
+    __syncthreads();
+    // 3. products, run by run, at the warp's cursors
+    for (int64_t e = e_lo + w; e < a.n_e; e += kRrWarps) {
+      const int64_t o0 = a.e_off[e];
+      if (o0 >= P1) break;
+      const int64_t o1 = a.e_off[e + 1];
+      if (o1 <= o0) continue;
+      const int slot = a.e_row[e] - row0;
+      if (slot < 0 || slot >= kRrRows) continue;
+      const int q0 = static_cast<int>(max(P0, o0) - o0), q1 = static_cast<int>(min(P1, o1) - o0);
+      const int32_t* const t = a.bcp + static_cast<int64_t>(a.e_k[e]) * vp1;
+      const int32_t* const bc = a.b_col + a.e_b[e];
+      const double* const bvp = a.b_val + a.e_b[e];
+      const double av = VAL ? a.e_a[e] : 0.0;
+      __syncwarp();
+      for (int c = lane; c < v; c += 32) {
+        const int x0 = max(q0, t[c]), x1 = min(q1, t[c + 1]);
+        if (x1 > x0) {
+          s_base[w][c] = s_rbase[slot][c] + s_cnt[w][slot][c] - x0;
+          s_cnt[w][slot][c] += x1 - x0;
+        }
+      }
+      __syncwarp();
+      for (int qb = q0; qb < q1; qb += 32 * kRrU) {
+        uint32_t col[kRrU];
+        double bv[kRrU];
+#pragma unroll
+        for (int u = 0; u < kRrU; ++u) {
+          const int q = qb + u * 32 + lane;
+          col[u] = q < q1 ? static_cast<uint32_t>(bc[q]) : 0u;
+          bv[u] = (VAL && q < q1) ? bvp[q] : 0.0;
+        }
+#pragma unroll
+        for (int u = 0; u < kRrU; ++u) {
+          const int q = qb + u * 32 + lane;
+          if (q < q1) {
+            const int64_t dst = s_base[w][col[u] >> a.shift] + q;
+            a.out_col[dst] = static_cast<int32_t>(col[u] & mask);
+            if (VAL) a.out_val[dst] = av * bv[u];
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// first[g] = the entry holding position g * U: the largest e with e_off[e] <= g * U.
+__global__ void k_unit_first(const int64_t* __restrict__ e_off, int64_t n_e, int64_t U, int64_t n_units,
+                             int64_t* __restrict__ first) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < n_units; g += stride) {
+    const int64_t x = g * U;
+    int64_t lo = 0, hi = n_e - 1;
+    while (lo < hi) {
+      const int64_t mid = (lo + hi + 1) >> 1;
+      if (e_off[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    first[g] = lo;
+  }
+}
+
+}  // namespace
+
+int64_t row_runs_unit(int64_t tau) { return std::min<int64_t>(32768, (kRrRows - 2) * (tau + 1)); }
+
+void launch_row_runs(const RowRunArgs& a, int num_sms, cudaStream_t s) {
+  if (a.total <= 0 || a.n_e <= 0) return;
+  (k_unit_first<<<grid_for(a.n_units, 256), 256, 0, s>>>(a.e_off, a.n_e, a.U, a.n_units, a.unit_first),
+   note_launch());
+  cudaMemsetAsync(a.unit_counter, 0, sizeof(unsigned), s);
+  const unsigned blocks = static_cast<unsigned>(std::min<int64_t>(a.n_units, static_cast<int64_t>(num_sms) * 6));
+  if (a.out_val) (k_expand_rows<true><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
+  else (k_expand_rows<false><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
 }
 
 }  // namespace gm
