@@ -165,155 +165,6 @@ __global__ void __launch_bounds__(kOpThreads) k_outer(OuterArgs a) {
   }
 }
 
-// OuterProduct into the level-0 chunks, one warp per unit of E consecutive
-// products of the flattened slice space (B rows sorted, per-B-row chunk starts in
-// a.bcp); warps take units from a global counter. A unit is walked entry portion
-// by entry portion (the part of one A-tilde entry's product row A~[i,k] * B[k,:]
-// inside the unit). Per slice k the warp keeps in registers the B row's start
-// and length and, lane l for chunks c_lo + l, + 32, ..., the chunk's index range
-// [T0, T1) inside the row. A portion [q0, q1) of the row then needs only its
-// entry (row, A value: loaded one entry ahead) and the reservations: lane l
-// clips its chunks' ranges to the portion and reserves each non-empty run with
-// one atomic add on the chunk's cursor, all runs at once. The warp streams the
-// portion (coalesced B reads); a product finds its run's destination in the
-// register of the lane holding its chunk (warp shuffle), and the lanes of a run
-// write consecutive addresses.
-constexpr int kOwU = 4;
-
-template <bool VAL, int SLOTS>
-__global__ void __launch_bounds__(256, 4) k_outer_warp(OuterArgs a, int64_t n_units, unsigned* unit_counter) {
-  __shared__ int64_t s_bases[8][SLOTS * 32];  // per warp: destination base of each chunk of the portion
-  const int lane = threadIdx.x & 31;
-  int64_t* const s_base = s_bases[threadIdx.x >> 5];
-  const uint32_t mask = (1u << a.shift) - 1u;
-  const int vp1 = a.v + 1;
-  int64_t s = -1, rb = 0, L = 1, so0 = 0, so1 = 0, cp = 0;  // cached slice
-  int c_lo = 0, nslots = 0;
-  int32_t T0[SLOTS], T1[SLOTS];
-  while (true) {
-    unsigned gu = 0;
-    if (lane == 0) gu = atomicAdd(unit_counter, 1u);
-    const int64_t g = __shfl_sync(kFull, gu, 0);
-    if (g >= n_units) break;
-    int64_t p = g * a.E;
-    const int64_t stop = min(p + a.E, a.total);
-    const int64_t s_first = a.wg_first[g];  // slices of this unit: [s_first, s_last]
-    const int64_t s_last = g + 1 < n_units ? a.wg_first[g + 1] : a.n_slices - 1;
-    int64_t eb = -64;      // entries [eb, eb + 32) have their row / A value in lane (e - eb); none yet
-    int32_t rowb = 0;
-    double avb = 0.0;
-    int64_t e_res = -1;    // entry whose runs were reserved ahead (destinations in base_next)
-    int64_t base_next[SLOTS];
-    while (p < stop) {
-      if (s < 0 || p < so0 || p >= so1) {  // new slice: its B row and chunk ranges
-        s = p == g * a.E ? s_first : upper_floor(a.slice_off, s_first, s_last, p);
-        so0 = a.slice_off[s];
-        so1 = a.slice_off[s + 1];
-        cp = a.col_ptr[s];
-        rb = a.b_rp[s];
-        L = a.b_rp[s + 1] - rb;
-        c_lo = static_cast<int>(static_cast<uint32_t>(a.b_col[rb]) >> a.shift);
-        const int c_hi = static_cast<int>(static_cast<uint32_t>(a.b_col[rb + L - 1]) >> a.shift);
-        nslots = (c_hi - c_lo + 32) >> 5;
-        eb = -64;  // the row batch holds entries of the previous slice only
-        const int32_t* const t = a.bcp + s * vp1;
-#pragma unroll
-        for (int k = 0; k < SLOTS; ++k) {
-          const int c = c_lo + k * 32 + lane;
-          const bool in = k < nslots && c <= c_hi;
-          T0[k] = in ? t[c] : 0;
-          T1[k] = in ? t[c + 1] : 0;
-        }
-      }
-      const int64_t rel = p - so0;
-      const int64_t e = cp + rel / L;
-      const int64_t q0 = rel % L;
-      const int64_t q1 = min(L, q0 + (stop - p));
-      const int64_t e_end = cp + (so1 - so0) / L;  // entries of this slice end here
-      if (e < eb || e >= eb + 32) {  // rows and A values of the next 32 entries, one load each
-        eb = e;
-        rowb = e + lane < e_end ? a.t_row[e + lane] : 0;
-        avb = (VAL && e + lane < e_end) ? a.t_val[e + lane] : 0.0;
-      }
-      const int32_t row = __shfl_sync(kFull, rowb, static_cast<int>(e - eb));
-      const double av = VAL ? __shfl_sync(kFull, avb, static_cast<int>(e - eb)) : 0.0;
-      const int64_t key_row = static_cast<int64_t>(row) * a.v;
-      // the first B loads go out before the reservations (they do not depend on them)
-      const int32_t* const bc = a.b_col + rb;
-      const double* const bvp = a.b_val + rb;
-      const int iq0 = static_cast<int>(q0), iq1 = static_cast<int>(q1);
-      uint32_t ncol[kOwU];
-      double nbv[kOwU];
-#pragma unroll
-      for (int u = 0; u < kOwU; ++u) {
-        const int q = iq0 + u * 32 + lane;
-        ncol[u] = q < iq1 ? static_cast<uint32_t>(bc[q]) : 0u;
-        nbv[u] = (VAL && q < iq1) ? bvp[q] : 0.0;
-      }
-      // run destinations: dst of position q in chunk c_lo + i is s_base[i] + q
-      __syncwarp();
-      if (e == e_res) {  // reserved while the previous entry streamed
-#pragma unroll
-        for (int k = 0; k < SLOTS; ++k)
-          if (k < nslots) s_base[k * 32 + lane] = base_next[k];
-      } else {
-#pragma unroll
-        for (int k = 0; k < SLOTS; ++k) {
-          const int64_t x0 = max(q0, static_cast<int64_t>(T0[k])), x1 = min(q1, static_cast<int64_t>(T1[k]));
-          if (k < nslots && x1 > x0)
-            s_base[k * 32 + lane] = static_cast<int64_t>(atomicAdd(&a.cursor[key_row + c_lo + k * 32 + lane],
-                                                                   static_cast<unsigned long long>(x1 - x0))) - x0;
-        }
-      }
-      __syncwarp();
-      {  // reserve the next entry's runs now; the results are only read after this entry streams
-        const int64_t pn = p + (q1 - q0);
-        e_res = -1;
-        if (q1 == L && pn < stop && pn < so1 && e + 1 < eb + 32) {
-          const int64_t qn1 = min(L, stop - pn);
-          const int64_t key_n = static_cast<int64_t>(__shfl_sync(kFull, rowb, static_cast<int>(e + 1 - eb))) * a.v;
-#pragma unroll
-          for (int k = 0; k < SLOTS; ++k) {
-            const int64_t x0 = static_cast<int64_t>(T0[k]), x1 = min(qn1, static_cast<int64_t>(T1[k]));
-            base_next[k] = 0;
-            if (k < nslots && x1 > x0)
-              base_next[k] = static_cast<int64_t>(atomicAdd(&a.cursor[key_n + c_lo + k * 32 + lane],
-                                                            static_cast<unsigned long long>(x1 - x0))) - x0;
-          }
-          e_res = e + 1;
-        }
-      }
-      for (int qb = iq0; qb < iq1; qb += 32 * kOwU) {
-        uint32_t col[kOwU];
-        double bv[kOwU];
-#pragma unroll
-        for (int u = 0; u < kOwU; ++u) {
-          col[u] = ncol[u];
-          bv[u] = nbv[u];
-        }
-        if (qb + 32 * kOwU < iq1) {  // the next step's loads in flight while this one is stored
-#pragma unroll
-          for (int u = 0; u < kOwU; ++u) {
-            const int q = qb + 32 * kOwU + u * 32 + lane;
-            ncol[u] = q < iq1 ? static_cast<uint32_t>(bc[q]) : 0u;
-            nbv[u] = (VAL && q < iq1) ? bvp[q] : 0.0;
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kOwU; ++u) {
-          const int q = qb + u * 32 + lane;
-          if (q < iq1) {
-            const int64_t dst = s_base[static_cast<int>(col[u] >> a.shift) - c_lo] + q;
-            a.out_col[dst] = static_cast<int32_t>(col[u] & mask);
-            if (VAL) a.out_val[dst] = av * bv[u];
-          }
-        }
-      }
-      p += q1 - q0;
-    }
-  }
-}
-
 }  // namespace
 
 bool masked_transpose(const TransposeArgs& a, int64_t nnz_batch, int64_t* col_ptr, int32_t* t_row,
@@ -353,20 +204,6 @@ void launch_outer_product(const OuterArgs& a, cudaStream_t s) {
   } else {
     if (a.histo) (k_outer<false, true><<<g, kOpThreads, 0, s>>>(a), note_launch());
     else (k_outer<false, false><<<g, kOpThreads, 0, s>>>(a), note_launch());
-  }
-}
-
-void launch_outer_split(const OuterArgs& a, unsigned* unit_counter, int num_sms, cudaStream_t s) {
-  if (a.total <= 0) return;
-  const int64_t n_units = (a.total + a.E - 1) / a.E;  // one warp at a time per work group of E products
-  const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((n_units + 7) / 8, static_cast<int64_t>(num_sms) * 4));
-  cudaMemsetAsync(unit_counter, 0, sizeof(unsigned), s);
-  if (a.v <= 64) {
-    if (a.out_val) (k_outer_warp<true, 2><<<blocks, 256, 0, s>>>(a, n_units, unit_counter), note_launch());
-    else (k_outer_warp<false, 2><<<blocks, 256, 0, s>>>(a, n_units, unit_counter), note_launch());
-  } else {
-    if (a.out_val) (k_outer_warp<true, 8><<<blocks, 256, 0, s>>>(a, n_units, unit_counter), note_launch());
-    else (k_outer_warp<false, 8><<<blocks, 256, 0, s>>>(a, n_units, unit_counter), note_launch());
   }
 }
 

@@ -152,18 +152,10 @@ struct OuterArgs {
   double* out_val;            // null: columns only
   // fused level-0 histogram (null when not fused)
   unsigned long long* histo;  // [rows * v]
-  const int32_t* bcp;         // per-B-row chunk starts (heavy_chunk_counts), for k_outer_warp
   int v;
   int shift;                  // chunk = col >> shift
 };
 void launch_outer_product(const OuterArgs& a, cudaStream_t s);
-// OuterProduct straight into the level-0 chunks (B rows sorted by column, v <=
-// 256, per-B-row chunk starts in a.bcp): the products of one A-tilde entry in
-// one chunk form a run of consecutive B-row elements; each run is reserved with
-// one atomic add on cursor[row * v + chunk] and written contiguously, the column
-// shifted into the chunk (col & (2^shift - 1)). Warps take units of E products; histo unused.
-// unit_counter: one device word the kernel takes work units from (zeroed here).
-void launch_outer_split(const OuterArgs& a, unsigned* unit_counter, int num_sms, cudaStream_t s);
 
 // ---- multisplit (gm_multisplit.cu) ------------------------------------------
 // wg_first[g] = the row holding position g*E.

@@ -539,9 +539,10 @@ namespace {
 // Row-order expansion into the level-0 chunks with long contiguous writes (B
 // rows sorted, per-B-row chunk starts in a.bcp). The batch's heavy products, in
 // row order, are cut into units of a.U; one block takes a unit at a time:
-//  1. each warp walks its share of the unit's A entries (entry e_lo + w, + 8, ...)
-//     and counts, from the chunk starts of each entry's B row, how many of its
-//     products fall in every (row, chunk) -- lane l holds chunks l and l + 32;
+//  1. each warp takes an equal consecutive share of the unit's products (the
+//     entries at its ends only in part) and counts, from the chunk starts of
+//     each entry's B row, how many of them fall in every (row, chunk) -- lane l
+//     holds chunks l and l + 32;
 //  2. every (row, chunk) of the unit is reserved with one atomic add, and each
 //     warp gets its own consecutive part of that range;
 //  3. the warps walk their entries again and write the products: a run of one
@@ -569,14 +570,26 @@ __global__ void __launch_bounds__(kRrWarps * 32) k_expand_rows(RowRunArgs a) {
     if (g >= a.n_units) break;
     const int64_t P0 = g * a.U, P1 = min(P0 + a.U, a.total);
     const int64_t e_lo = a.unit_first[g];
+    const int64_t e_hi = g + 1 < a.n_units ? a.unit_first[g + 1] : a.n_e - 1;
     const int32_t row0 = a.e_row[e_lo];
-    // 1. counts per (row, chunk), per warp
-    for (int64_t e = e_lo + w; e < a.n_e; e += kRrWarps) {
+    // this warp's equal share [W0, W1) of the unit's products, from the entry holding W0
+    const int64_t share = (P1 - P0 + kRrWarps - 1) / kRrWarps;
+    const int64_t W0 = min(P1, P0 + w * share), W1 = min(P1, W0 + share);
+    int64_t ew = e_lo;
+    {
+      int64_t hi = e_hi;
+      while (ew < hi) {
+        const int64_t mid = (ew + hi + 1) >> 1;
+        if (a.e_off[mid] <= W0) ew = mid; else hi = mid - 1;
+      }
+    }
+    // 1. counts per (row, chunk) of this warp's share
+    for (int64_t e = ew; e < a.n_e && W0 < W1; ++e) {
       const int64_t o0 = a.e_off[e];
-      if (o0 >= P1) break;
+      if (o0 >= W1) break;
       const int64_t o1 = a.e_off[e + 1];
-      if (o1 <= o0) continue;
-      const int64_t q0 = max(P0, o0) - o0, q1 = min(P1, o1) - o0;
+      if (o1 <= max(o0, W0)) continue;
+      const int64_t q0 = max(W0, o0) - o0, q1 = min(W1, o1) - o0;
       const int slot = a.e_row[e] - row0;
       if (slot < 0 || slot >= kRrRows) {
         if (lane == 0) atomicOr(a.status, kStGroupRows);
@@ -608,14 +621,14 @@ __global__ void __launch_bounds__(kRrWarps * 32) k_expand_rows(RowRunArgs a) {
     }
     __syncthreads();
     // 3. products, run by run, at the warp's cursors
-    for (int64_t e = e_lo + w; e < a.n_e; e += kRrWarps) {
+    for (int64_t e = ew; e < a.n_e && W0 < W1; ++e) {
       const int64_t o0 = a.e_off[e];
-      if (o0 >= P1) break;
+      if (o0 >= W1) break;
       const int64_t o1 = a.e_off[e + 1];
-      if (o1 <= o0) continue;
+      if (o1 <= max(o0, W0)) continue;
       const int slot = a.e_row[e] - row0;
       if (slot < 0 || slot >= kRrRows) continue;
-      const int q0 = static_cast<int>(max(P0, o0) - o0), q1 = static_cast<int>(min(P1, o1) - o0);
+      const int q0 = static_cast<int>(max(W0, o0) - o0), q1 = static_cast<int>(min(W1, o1) - o0);
       const int32_t* const t = a.bcp + static_cast<int64_t>(a.e_k[e]) * vp1;
       const int32_t* const bc = a.b_col + a.e_b[e];
       const double* const bvp = a.b_val + a.e_b[e];
