@@ -178,19 +178,20 @@ constexpr uint32_t kNoCol = 0xFFFFFFFFu;
 constexpr int64_t kLightSymRegion = 65536;  // entry-table bytes of the symbolic light kernel
 
 // Rank of column c (number of set bits below it) from the 8-word group prefix:
-// the group's 8 words come in as two 16-byte loads.
+// the 16-byte half of the group holding c, plus the first half's count when c
+// lies in the second.
 __device__ __forceinline__ int bitmap_rank(const uint32_t* bm, const int* gpre, uint32_t c) {
-  const int w = c >> 5, g = w >> 3, wi = w & 7;
+  const int w = c >> 5, g = w >> 3, wi = w & 7, j = wi & 3;
   const uint4* g4 = reinterpret_cast<const uint4*>(bm + g * kGroupWords);
-  const uint4 q0 = g4[0], q1 = g4[1];
-  const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
   int r = gpre[g];
-#pragma unroll
-  for (int x = 0; x < 8; ++x) {
-    if (x < wi) r += __popc(words[x]);
-    else if (x == wi) r += __popc(words[x] & ((1u << (c & 31)) - 1u));
+  if (wi >= 4) {
+    const uint4 q0 = g4[0];
+    r += __popc(q0.x) + __popc(q0.y) + __popc(q0.z) + __popc(q0.w);
   }
-  return r;
+  const uint4 q = g4[wi >> 2];
+  r += (j > 0 ? __popc(q.x) : 0) + (j > 1 ? __popc(q.y) : 0) + (j > 2 ? __popc(q.z) : 0);
+  const uint32_t word = j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w;
+  return r + __popc(word & ((1u << (c & 31)) - 1u));
 }
 
 // Light rows (u <= kRbThreads * kRlItems) with a whole-row bitmap, every product
@@ -363,16 +364,21 @@ __global__ void __launch_bounds__(kRbThreads, 1)
       for (int k = 0; k < kRlItems; ++k)
         if (cw[k] != kNoCol) atomicAdd(&vals[bitmap_rank(bm, gpre, cw[k])], val[k]);
       __syncthreads();
-      for (int w = threadIdx.x; w < wwords; w += T) {  // words round-robin: adjacent output per warp
-        uint32_t bits = bm[w];
-        if (!bits) continue;
-        int pos = bitmap_rank(bm, gpre, static_cast<uint32_t>(w) << 5);
-        while (bits) {
-          const int b = __ffs(bits) - 1;
-          bits &= bits - 1;
-          a.c_col[out + done + pos] = static_cast<int32_t>(base + w * 32 + b);
-          a.c_val[out + done + pos] = vals[pos];
-          ++pos;
+      for (int g = threadIdx.x; g < ngw; g += T) {  // groups round-robin: adjacent output per warp
+        const uint4* g4 = reinterpret_cast<const uint4*>(bm + g * kGroupWords);
+        const uint4 q0 = g4[0], q1 = g4[1];
+        const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        int pos = gpre[g];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          uint32_t bits = words[x];
+          while (bits) {
+            const int b = __ffs(bits) - 1;
+            bits &= bits - 1;
+            a.c_col[out + done + pos] = static_cast<int32_t>(base + (g * kGroupWords + x) * 32 + b);
+            a.c_val[out + done + pos] = vals[pos];
+            ++pos;
+          }
         }
       }
       done += nnz;
