@@ -656,8 +656,10 @@ __global__ void __launch_bounds__(kRrWarps * 32) k_expand_rows(RowRunArgs a) {
           const int q = qb + u * 32 + lane;
           if (q < q1) {
             const int64_t dst = s_base[w][col[u] >> a.shift] + q;
-            a.out_col[dst] = static_cast<int32_t>(col[u] & mask);
-            if (VAL) a.out_val[dst] = av * bv[u];
+            // written once, read once by the accumulators: streaming stores, so that
+            // they do not push B and the cursors out of L2
+            __stcs(a.out_col + dst, static_cast<int32_t>(col[u] & mask));
+            if (VAL) __stcs(a.out_val + dst, av * bv[u]);
           }
         }
       }
