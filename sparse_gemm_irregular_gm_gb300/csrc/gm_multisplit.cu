@@ -554,7 +554,7 @@ constexpr int kRrRows = 8;   // rows a unit may touch (a.U keeps it below this)
 constexpr int kRrU = 4;
 
 template <bool VAL>
-__global__ void __launch_bounds__(kRrWarps * 32) k_expand_rows(RowRunArgs a) {
+__global__ void __launch_bounds__(kRrWarps * 32, 5) k_expand_rows(RowRunArgs a) {
   __shared__ int s_cnt[kRrWarps][kRrRows][64];  // counts, then each warp's offset inside the reservation
   __shared__ int64_t s_rbase[kRrRows][64];       // reservation of each (row, chunk) of the unit
   __shared__ int64_t s_base[kRrWarps][64];
@@ -642,14 +642,29 @@ __global__ void __launch_bounds__(kRrWarps * 32) k_expand_rows(RowRunArgs a) {
         }
       }
       __syncwarp();
+      uint32_t ncol[kRrU];
+      double nbv[kRrU];
+#pragma unroll
+      for (int u = 0; u < kRrU; ++u) {
+        const int q = q0 + u * 32 + lane;
+        ncol[u] = q < q1 ? static_cast<uint32_t>(bc[q]) : 0u;
+        nbv[u] = (VAL && q < q1) ? bvp[q] : 0.0;
+      }
       for (int qb = q0; qb < q1; qb += 32 * kRrU) {
         uint32_t col[kRrU];
         double bv[kRrU];
 #pragma unroll
         for (int u = 0; u < kRrU; ++u) {
-          const int q = qb + u * 32 + lane;
-          col[u] = q < q1 ? static_cast<uint32_t>(bc[q]) : 0u;
-          bv[u] = (VAL && q < q1) ? bvp[q] : 0.0;
+          col[u] = ncol[u];
+          bv[u] = nbv[u];
+        }
+        if (qb + 32 * kRrU < q1) {  // the next step's loads in flight while this one is stored
+#pragma unroll
+          for (int u = 0; u < kRrU; ++u) {
+            const int q = qb + 32 * kRrU + u * 32 + lane;
+            ncol[u] = q < q1 ? static_cast<uint32_t>(bc[q]) : 0u;
+            nbv[u] = (VAL && q < q1) ? bvp[q] : 0.0;
+          }
         }
 #pragma unroll
         for (int u = 0; u < kRrU; ++u) {
