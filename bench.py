@@ -45,6 +45,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--pipeline", type=int, default=0)
+    ap.add_argument("--grid", action="store_true",
+                    help="C = A*B over the R-MAT grid of distinct pairs (one JSON line per point)")
+    ap.add_argument("--grid-max-scale", type=int, default=0, help="leave out grid points above this scale")
     return ap.parse_args()
 
 
@@ -233,6 +236,25 @@ def _cpu_baseline(A, B, u, target_s, seed):
                       f"{dt:.1f} s on the host cores"}
 
 
+def make_step(A, Ad, Bd, cfg, stream):
+    """One full SpGEMM through the C ABI: analyze, symbolic, allocation of C, numeric."""
+    import torch
+
+    from sparse_gemm_irregular_gm_gb300 import binding
+
+    def step():
+        plan = binding.gm_spgemm_analyze(Ad, Bd, cfg, stream)
+        c_rp = torch.empty(A.n_rows + 1, dtype=torch.int64, device="cuda")
+        nnz = binding.gm_spgemm_symbolic(plan, c_rp)
+        c_col = torch.empty(nnz, dtype=torch.int32, device="cuda")
+        c_val = torch.empty(nnz, dtype=torch.float64, device="cuda")
+        binding.gm_spgemm_numeric(plan, c_col, c_val)
+        info = binding.gm_spgemm_plan_info(plan)
+        binding.gm_spgemm_plan_destroy(plan)
+        return info, c_rp
+    return step
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -246,17 +268,7 @@ def run_ours(args):
     Bd = Ad if B is A else binding.to_device(B)
     cfg = binding.make_config(flags=binding.GM_FLAG_TIMING, pipeline=args.pipeline)
     stream = torch.cuda.current_stream()
-
-    def step():
-        plan = binding.gm_spgemm_analyze(Ad, Bd, cfg, stream)
-        c_rp = torch.empty(A.n_rows + 1, dtype=torch.int64, device="cuda")
-        nnz = binding.gm_spgemm_symbolic(plan, c_rp)
-        c_col = torch.empty(nnz, dtype=torch.int32, device="cuda")
-        c_val = torch.empty(nnz, dtype=torch.float64, device="cuda")
-        binding.gm_spgemm_numeric(plan, c_col, c_val)
-        info = binding.gm_spgemm_plan_info(plan)
-        binding.gm_spgemm_plan_destroy(plan)
-        return info, c_rp
+    step = make_step(A, Ad, Bd, cfg, stream)
 
     log(f"workload {args.workload}: n={A.n_rows} nnz={A.nnz}")
     for w in range(args.warmup):
@@ -339,6 +351,77 @@ def run_ours(args):
         log("e2e: " + json.dumps(result["e2e"]))
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+# gMAGNUS, Sec. IV-A, Table III (RMat pairs from PaRMAT, B.nnz/B.n = 8):
+# (A.nnz/A.n, scale) -> (C.nnz/C.n, C-hat.nnz/C-hat.n); the pages print N/A for the
+# larger scales at A.nnz/A.n >= 8, and those points are not in the grid.
+TABLE_III = {
+    (4, 15): (477.6, 819.9), (4, 16): (633.5, 1068.2), (4, 17): (835.0, 1382.7),
+    (4, 18): (1112.7, 1802.7), (4, 19): (1471.9, 2342.3), (4, 20): (1944.1, 3043.1),
+    (8, 15): (782.3, 1548.9), (8, 16): (1048.4, 2021.2), (8, 17): (1397.9, 2628.5),
+    (8, 18): (1875.6, 3432.7), (8, 19): (2496.0, 4472.1),
+    (16, 15): (1233.3, 2841.0), (16, 16): (1679.4, 3746.7), (16, 17): (2267.3, 4911.0),
+    (16, 18): (3075.3, 6427.6),
+    (32, 15): (1895.6, 5149.9), (32, 16): (2597.7, 6779.1), (32, 17): (3574.5, 8979.8),
+    (32, 18): (4896.9, 11805.3),
+}
+
+
+def run_grid(args):
+    """C = A*B over the R-MAT grid of the pages' Table III (distinct A and B, B.nnz/B.n = 8):
+    one JSON line per point with the measured rate and the statistics next to the
+    table's. The table's matrices come from PaRMAT, ours from the R-MAT generator of
+    this package with the same quadrant probabilities, so the statistics agree only
+    approximately. L2 is flushed before every timed step."""
+    import torch
+
+    import __graft_entry__
+    from sparse_gemm_irregular_gm_gb300 import binding, inputs
+    rank, world, local = dist_setup(args)
+    __graft_entry__.build()
+    stream = torch.cuda.current_stream()
+    cfg = binding.make_config(flags=binding.GM_FLAG_TIMING, pipeline=args.pipeline)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    points = sorted(TABLE_III, key=lambda k: (k[1], k[0]))
+    if args.grid_max_scale:
+        points = [p for p in points if p[1] <= args.grid_max_scale]
+    for a_density, scale in points:
+        name = f"rmatAB_s{scale}_a{a_density}_b8"
+        A, B = inputs.named_pair(name, seed=args.seed)
+        Ad, Bd = binding.to_device(A), binding.to_device(B)
+        step = make_step(A, Ad, Bd, cfg, stream)
+        for _ in range(max(1, args.warmup)):
+            info, c_rp = step()
+            del c_rp
+        times = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            info, c_rp = step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+            nnz_c = int(c_rp[-1].item())
+            del c_rp
+        ms = max_over_ranks(statistics.median(times), world)
+        c_n, chat_n = TABLE_III[(a_density, scale)]
+        line = {
+            "grid": name, "metric": METRIC, "value": round(world * 2.0 * info.ip_total / ms / 1e6, 3),
+            "unit": "GFLOP/s", "ms_per_step": round(ms, 3), "steps": args.steps, "n_gpus": world,
+            "dtype": "f64", "data": "synthetic", "l2": "flushed before each timed step",
+            "n": A.n_rows, "A_nnz_per_row": round(A.nnz / A.n_rows, 2), "B_nnz_per_row": round(B.nnz / B.n_rows, 2),
+            "C_nnz_per_row": round(nnz_c / A.n_rows, 1), "Chat_nnz_per_row": round(info.ip_total / A.n_rows, 1),
+            "table_III": {"C_nnz_per_row": c_n, "Chat_nnz_per_row": chat_n},
+            "heavy_rows": info.n_heavy_rows, "chunks": list(info.params.v_chunks[:info.params.n_levels]),
+            "pipeline": binding.PIPELINES[info.pipeline],
+            "stages_ms": {binding.STAGES[i]: round(float(x), 3) for i, x in enumerate(info.stage_ms) if x > 0},
+        }
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        del Ad, Bd, step
+        torch.cuda.empty_cache()
 
 
 def run_e2e(args, A, cfg, stream, nnz_c, ip_total):
@@ -444,6 +527,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.grid:
+        run_grid(args)
     else:
         run_ours(args)
 

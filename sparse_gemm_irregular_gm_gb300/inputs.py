@@ -22,7 +22,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
-__all__ = ["CSR", "rmat", "laplacian_2d", "erdos_renyi", "random_csr", "row_slice",
+__all__ = ["CSR", "rmat", "rmat_pair", "laplacian_2d", "erdos_renyi", "random_csr", "row_slice",
            "identity", "permutation", "named_workload", "named_pair", "WORKLOADS", "PAIRS"]
 
 
@@ -242,9 +242,34 @@ def named_workload(name: str, seed: int = 1) -> CSR:
     return WORKLOADS[name][1](seed)
 
 
+def rmat_pair(scale: int, a_density: int, b_density: int, seed: int = 1, values: str = "uniform"):
+    """A and B of the pages' R-MAT grid (gMAGNUS Sec. IV-A: A.nnz/A.n from 4 to 64,
+    B.nnz/B.n from 4 to 16, scales 15 to 20): two independent R-MAT matrices of the
+    same scale, drawn with edge factors a_density and b_density (A from seed, B
+    from seed + 1000003). Duplicate edges collapse, so nnz/n ends a little below
+    the edge factor."""
+    return (rmat(scale, a_density, seed=seed, values=values),
+            rmat(scale, b_density, seed=seed + 1000003, values=values))
+
+
+def _grid_name(name: str):
+    """(scale, a_density, b_density) of a name rmatAB_s<scale>_a<A>_b<B>, else None."""
+    parts = name.split("_")
+    if len(parts) != 4 or parts[0] != "rmatAB":
+        return None
+    try:
+        return int(parts[1][1:]), int(parts[2][1:]), int(parts[3][1:])
+    except ValueError:
+        return None
+
+
 def named_pair(name: str, seed: int = 1):
-    """(A, B) of a named product: the A*A workloads give (A, A)."""
+    """(A, B) of a named product: the A*A workloads give (A, A); rmatAB_s<scale>_a<A>_b<B>
+    is the R-MAT grid pair of rmat_pair."""
     if name in PAIRS:
         return PAIRS[name][1](seed)
+    grid = _grid_name(name)
+    if grid is not None:
+        return rmat_pair(*grid, seed=seed)
     A = named_workload(name, seed)
     return A, A

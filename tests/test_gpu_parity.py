@@ -361,6 +361,17 @@ def test_chunk_with_one_hot_column(n_hot):
     check_full(A, B, exact=True, tau=64)
 
 
+@pytest.mark.parametrize("a_density", [4, 16])
+def test_rmat_grid_pairs(a_density):
+    """A*B with independent R-MAT A and B (the pages' grid: A.nnz/A.n varied, B.nnz/B.n
+    = 8) at scale 13; statistics of the kind Table III reports checked against the
+    oracle's own counts."""
+    A, B = gi.named_pair(f"rmatAB_s13_a{a_density}_b8", seed=2)
+    u = oracle.ip_counts(A, B)
+    info = check_full(A, B)
+    assert info.ip_total == int(u.sum()) and info.n_heavy_rows == int((u > info.params.tau).sum())
+
+
 # --- the workloads ------------------------------------------------------------------
 
 def test_workload_rmat10_fp64_and_int():

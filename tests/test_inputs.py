@@ -44,3 +44,13 @@ def test_random_csr_options():
     A.check()
     assert (np.diff(A.row_ptr) == 0).any()
     assert (A.val == 0).any()
+
+
+def test_rmat_grid_pair_is_seeded_and_distinct():
+    A, B = gi.named_pair("rmatAB_s10_a4_b8", seed=3)
+    A2, B2 = gi.rmat_pair(10, 4, 8, seed=3)
+    assert A.n_rows == B.n_rows == A.n_cols == B.n_cols == 1024
+    np.testing.assert_array_equal(A.col, A2.col)
+    np.testing.assert_array_equal(B.val, B2.val)
+    assert 3.0 < A.nnz / A.n_rows <= 4.0 and 6.0 < B.nnz / B.n_rows <= 8.0
+    assert A.nnz != B.nnz or not np.array_equal(A.col, B.col)
