@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--pipeline", type=int, default=0)
+    ap.add_argument("--n-chunks-max", type=int, default=0, help="plan override: chunks per multisplit level")
+    ap.add_argument("--dense-width", type=int, default=0, help="plan override: dense accumulator width")
     ap.add_argument("--grid", action="store_true",
                     help="C = A*B over the R-MAT grid of distinct pairs (one JSON line per point)")
     ap.add_argument("--grid-max-scale", type=int, default=0, help="leave out grid points above this scale")
@@ -236,6 +238,11 @@ def _cpu_baseline(A, B, u, target_s, seed):
                       f"{dt:.1f} s on the host cores"}
 
 
+def plan_overrides(args) -> dict:
+    """gm_config fields set on the command line (zero keeps the automatic value)."""
+    return {k: v for k, v in (("n_chunks_max", args.n_chunks_max), ("dense_width", args.dense_width)) if v}
+
+
 def make_step(A, Ad, Bd, cfg, stream):
     """One full SpGEMM through the C ABI: analyze, symbolic, allocation of C, numeric."""
     import torch
@@ -266,7 +273,7 @@ def run_ours(args):
     A, B = inputs.named_pair(args.workload, seed=args.seed)
     Ad = binding.to_device(A)
     Bd = Ad if B is A else binding.to_device(B)
-    cfg = binding.make_config(flags=binding.GM_FLAG_TIMING, pipeline=args.pipeline)
+    cfg = binding.make_config(flags=binding.GM_FLAG_TIMING, pipeline=args.pipeline, **plan_overrides(args))
     stream = torch.cuda.current_stream()
     step = make_step(A, Ad, Bd, cfg, stream)
 
@@ -325,7 +332,9 @@ def run_ours(args):
                    "n": A.n_rows, "nnz_A": A.nnz, "intermediate_products": info.ip_total,
                    "heavy_products": info.ip_heavy, "nnz_C": nnz_c, "heavy_rows": info.n_heavy_rows,
                    "levels": info.params.n_levels, "chunks": list(info.params.v_chunks[:info.params.n_levels]),
-                   "batches": info.n_batches, "pipeline": binding.PIPELINES[info.pipeline], "parallelism": "replicas" if world > 1 else "single GPU",
+                   "batches": info.n_batches, "pipeline": binding.PIPELINES[info.pipeline],
+                   "plan_overrides": plan_overrides(args) or None,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs and outputs larger than L2 (C alone is %.0f GB)" % (12 * nnz_c / 1e9)},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,

@@ -18,10 +18,11 @@ GM_NUM_STAGES = 16
 STATUS_NAMES = ["GM_OK", "GM_ERR_INVALID_ARG", "GM_ERR_DIM_MISMATCH", "GM_ERR_INDEX_OVERFLOW", "GM_ERR_OOM",
                 "GM_ERR_WORKSPACE", "GM_ERR_CUDA", "GM_ERR_DEVICE_TIMEOUT", "GM_ERR_STATE", "GM_ERR_BAD_INDEX"]
 GM_FLAG_TIMING, GM_FLAG_KEEP_INTERMEDIATES, GM_FLAG_LOG = 1, 2, 4
-GM_PIPE_AUTO, GM_PIPE_UNFUSED, GM_PIPE_FUSED_HISTO, GM_PIPE_ROWWISE = 0, 1, 2, 3
+GM_PIPE_AUTO, GM_PIPE_UNFUSED, GM_PIPE_FUSED_HISTO, GM_PIPE_ROWWISE, GM_PIPE_WALK = 0, 1, 2, 3, 4
 PIPELINES = {GM_PIPE_AUTO: "auto", GM_PIPE_UNFUSED: "outer-product, unfused",
              GM_PIPE_FUSED_HISTO: "outer-product, fused level-0 histogram",
-             GM_PIPE_ROWWISE: "direct to level-0 chunks (C-hat not written)"}
+             GM_PIPE_ROWWISE: "direct to level-0 chunks (C-hat not written)",
+             GM_PIPE_WALK: "level-0 chunks summed from B's ranges (no C-hat, no chunk lists)"}
 (GM_DBG_IP_COUNTS, GM_DBG_HEAVY_ROWS, GM_DBG_LIGHT_ROWS, GM_DBG_CHAT_ROWPTR, GM_DBG_CHAT_COL, GM_DBG_CHAT_VAL,
  GM_DBG_REORD_ROWPTR, GM_DBG_REORD_COL, GM_DBG_REORD_VAL, GM_DBG_REORD_CHILD) = range(10)
 STAGES = ["analyze", "transpose", "outer", "histogram", "multisplit", "sym_heavy", "sym_light", "scan",

@@ -34,17 +34,22 @@ __global__ void k_validate_cols(const int32_t* __restrict__ col, int64_t nnz, in
   if (__any_sync(kFull, bad) && (threadIdx.x & 31) == 0) atomicOr(status, bad_bit);
 }
 
-// *unsorted = 1 when some row has a column greater than the next one in that row
-// (one warp per row, lanes compare neighbouring entries).
+// *flags |= 1 when some row has a column greater than the next one in that row,
+// |= 2 when some row holds a column twice in a row (one warp per row, lanes
+// compare neighbouring entries).
 __global__ void k_rows_sorted(const int64_t* __restrict__ rp, const int32_t* __restrict__ col, int64_t n_rows,
-                              int* unsorted) {
+                              int* flags) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  bool bad = false;
+  bool down = false, same = false;
   for (int64_t r = warp; r < n_rows; r += nw)
-    for (int64_t q = rp[r] + lane; q + 1 < rp[r + 1]; q += 32) bad |= col[q] > col[q + 1];
-  if (__any_sync(kFull, bad) && lane == 0) atomicOr(unsorted, 1);
+    for (int64_t q = rp[r] + lane; q + 1 < rp[r + 1]; q += 32) {
+      down |= col[q] > col[q + 1];
+      same |= col[q] == col[q + 1];
+    }
+  const int f = (__any_sync(kFull, down) ? 1 : 0) | (__any_sync(kFull, same) ? 2 : 0);
+  if (f && lane == 0) atomicOr(flags, f);
 }
 
 __device__ __forceinline__ uint8_t bin_of(int64_t size, const BinSpec& spec) {
@@ -190,9 +195,9 @@ void launch_validate_cols(const int32_t* col, int64_t nnz, int64_t n_cols, int b
   (k_validate_cols<<<grid_for(nnz, 256), 256, 0, s>>>(col, nnz, n_cols, bad_bit, status), note_launch());
 }
 
-void launch_check_sorted(const int64_t* rp, const int32_t* col, int64_t n_rows, int* unsorted, cudaStream_t s) {
+void launch_check_sorted(const int64_t* rp, const int32_t* col, int64_t n_rows, int* flags, cudaStream_t s) {
   if (n_rows <= 0) return;
-  (k_rows_sorted<<<grid_for(n_rows * 32, 256), 256, 0, s>>>(rp, col, n_rows, unsorted), note_launch());
+  (k_rows_sorted<<<grid_for(n_rows * 32, 256), 256, 0, s>>>(rp, col, n_rows, flags), note_launch());
 }
 
 void launch_ip_count(const int64_t* a_rp, const int32_t* a_col, int64_t n_rows, const int64_t* b_rp,

@@ -305,7 +305,10 @@ struct gm_plan {
   bool sym_rowbm = false;  // heavy symbolic through whole-row bitmaps
   bool rowwise = false;    // numeric heavy path: row-order expansion fused with the multisplit
   bool b_sorted = false;   // every row of B has non-decreasing columns (runs per chunk are contiguous)
-  int32_t b_unsorted_h = 0;
+  int32_t b_unsorted_h = 0;  // 1: some B row decreases, 2: some B row repeats a column
+  bool b_strict = false;   // every row of B has strictly increasing columns
+  bool walk_ok = false;    // the walk pipeline applies when B is strict and the bitmaps fit
+  bool walk = false;       // numeric heavy path: chunks summed straight from B's ranges (gm_walk.cu)
   gm_params P{};
   int L = 0;
   int state = 0;  // 1 analyzed, 2 symbolic done, 3 numeric done
@@ -324,6 +327,7 @@ struct gm_plan {
   gm::DevBuf<int64_t> anz;          // prefix of nnz(A[x_heavy[h], :]) (n_heavy + 1)
   gm::DevBuf<int64_t> cnt0;         // row-order pipeline: elements of each level-0 chunk (n_heavy * v0)
   gm::DevBuf<int32_t> bcp;          // row-order pipeline: per-B-row level-0 chunk starts (B.n_rows * (v0 + 1))
+  gm::DevBuf<uint32_t> hbits;       // walk pipeline: the heavy rows' bitmaps (n_heavy * rowbm_words(C.m))
   std::vector<int64_t> h_chat_rp;   // host copy of chat_rp
   std::vector<int64_t> h_anz;       // prefix of nnz(A[x_heavy[h], :])
   gm::GrowBuf nnz[GM_MAX_LEVELS];        // per level, per child: nnz (symbolic) then output offset
@@ -443,7 +447,8 @@ static gm_status analyze_impl(gm_plan* p) {
     cudaMemcpyAsync(&p->b_unsorted_h, flag.p, sizeof(int), cudaMemcpyDeviceToHost, s);
     st = sync_check(p);
     if (st != GM_OK) return st;
-    p->b_sorted = p->b_unsorted_h == 0;
+    p->b_sorted = (p->b_unsorted_h & 1) == 0;
+    p->b_strict = p->b_unsorted_h == 0;
   }
 
   BinSpec spec{};
@@ -1193,13 +1198,28 @@ static gm_status symbolic_impl(gm_plan* p, int64_t* C_rp, int64_t* C_nnz) {
       ra.work_counter = p->work_counter.p;
       ra.status = p->status.p;
       const int ts = p->stage_begin(GM_STAGE_SYM_HEAVY);
+      const int32_t* hrows = p->rows_by_bin.p + p->bin_start[kHeavyBin];
+      const int shift0 = ilog2(p->P.widths[0]);
+      if (p->rowwise) {  // per-B-row chunk starts
+        if (!p->bcp.alloc(std::max<int64_t>(p->B.n_rows, 1) * (v0 + 1), s)) return GM_ERR_OOM;
+        build_chunk_starts(p->B.row_ptr, p->B.col_idx, p->B.n_rows, static_cast<int>(v0), shift0, p->bcp.p, s);
+      }
+      p->walk = false;
+      if (p->walk_ok && p->b_strict && L == 1) {
+        // walk pipeline: the heavy rows' bitmaps are kept for the numeric pass
+        // when they take at most a quarter of the memory the workspace may use
+        const int64_t bits_words = nh * rowbm_words(p->c_m);
+        p->walk = bits_words * 4 <= workspace_cap(p) / 4 && p->hbits.alloc(bits_words, s);
+        if (p->walk) {
+          p->pipeline = GM_PIPE_WALK;
+          ra.bits_out = p->hbits.p;
+        }
+      }
       launch_rowbm(ra, p->num_sms, p->smem_dev, s);
-      if (p->rowwise) {  // element counts of the level-0 chunks, for the numeric pass
-        if (!p->cnt0.alloc(nh * v0, s) || !p->bcp.alloc(std::max<int64_t>(p->B.n_rows, 1) * (v0 + 1), s))
-          return GM_ERR_OOM;
-        if (!heavy_chunk_counts(p->rows_by_bin.p + p->bin_start[kHeavyBin], nh, p->anz.p, p->A.row_ptr,
-                                p->A.col_idx, p->B.row_ptr, p->B.col_idx, p->B.n_rows, static_cast<int>(v0),
-                                ilog2(p->P.widths[0]), p->bcp.p, p->cnt0.p, s))
+      if (p->rowwise && !p->walk) {  // level-0 chunk sizes, for the expansion
+        if (!p->cnt0.alloc(nh * v0, s)) return GM_ERR_OOM;
+        if (!heavy_chunk_counts(hrows, nh, p->anz.p, p->A.row_ptr, p->A.col_idx, nullptr, p->B.col_idx,
+                                p->B.n_rows, static_cast<int>(v0), shift0, p->bcp.p, p->cnt0.p, s))
           return GM_ERR_OOM;
       }
       p->stage_end(ts);
@@ -1272,11 +1292,68 @@ heavy_done:
   return GM_OK;
 }
 
+// Walk pipeline, numeric heavy rows: every (heavy row, level-0 chunk) with
+// columns is an item; items are classed by the chunk's nnz in chunk-major order
+// and each class is summed straight from B's ranges (gm_walk.cu).
+static gm_status run_heavy_walk(gm_plan* p, int32_t* c_col, double* c_val) {
+  const cudaStream_t s = p->s;
+  const int64_t nh = p->n_heavy;
+  const int v = static_cast<int>(p->P.v_chunks[0]);
+  const int64_t n = nh * v;
+  if (n >= INT32_MAX) return GM_ERR_INDEX_OVERFLOW;  // item ids are int32 in the partition
+  const int t = p->stage_begin(GM_STAGE_NUM_HEAVY);
+  constexpr int kClasses = 6;
+  DevBuf<uint8_t> cls;
+  DevBuf<int32_t> idx;
+  DevBuf<int64_t> starts_d, items;
+  if (!cls.alloc(n, s) || !idx.alloc(n, s) || !starts_d.alloc(kClasses + 1, s) || !items.alloc(n, s))
+    return GM_ERR_OOM;
+  launch_walk_class(p->leaf_nnz.p, nh, v, cls.p, s);
+  if (!partition_by_bin(cls.p, n, kClasses, idx.p, starts_d.p, s)) return GM_ERR_OOM;
+  int64_t starts[kClasses + 1];
+  cudaMemcpyAsync(starts, starts_d.p, sizeof(starts), cudaMemcpyDeviceToHost, s);
+  const cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_status(p, e);
+  i32_to_i64(idx.p, n, 0, items.p, s);
+  WalkArgs wa{};
+  wa.heavy_rows = p->rows_by_bin.p + p->bin_start[kHeavyBin];
+  wa.nh = nh;
+  wa.v = v;
+  wa.shift = ilog2(p->P.widths[0]);
+  wa.nwc = static_cast<int>(p->P.widths[0] / 32);
+  wa.nwr = rowbm_words(p->c_m);
+  wa.bits = p->hbits.p;
+  wa.a_rp = p->A.row_ptr;
+  wa.a_col = p->A.col_idx;
+  wa.a_val = p->A.vals;
+  wa.b_rp = p->B.row_ptr;
+  wa.b_col = p->B.col_idx;
+  wa.b_val = p->B.vals;
+  wa.bcp = p->bcp.p;
+  wa.off = p->nnz[0].p;
+  wa.counter = p->work_counter.p;
+  wa.c_col = c_col;
+  wa.c_val = c_val;
+  wa.status = p->status.p;
+  for (int c = 1; c < kClasses; ++c) {
+    wa.items = items.p + starts[c];
+    wa.n_items = starts[c + 1] - starts[c];
+    launch_walk(wa, c, p->num_sms, p->smem_dev, s);
+  }
+  p->stage_end(t);
+  p->n_batches = std::max<int64_t>(p->n_batches, 1);
+  return cuda_status(p, cudaGetLastError());
+}
+
 static gm_status numeric_impl(gm_plan* p, int32_t* C_col, double* C_val) {
   int t = p->stage_begin(GM_STAGE_NUM_LIGHT);
   launch_light(p, true, C_col, C_val);
   p->stage_end(t);
-  if (p->n_heavy > 0) {
+  if (p->n_heavy > 0 && p->walk) {
+    const gm_status st = run_heavy_walk(p, C_col, C_val);
+    p->hbits.release();
+    if (st != GM_OK) return st;
+  } else if (p->n_heavy > 0) {
     const bool keep = p->keep;
     p->keep = false;
     std::vector<std::pair<int64_t, int64_t>> batches;
@@ -1355,8 +1432,10 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
                  gm::rowbm_symbolic_smem(p->c_m) + 4096 <= p->smem_dev;
   p->rowwise = p->sym_rowbm && p->L == 1 && p->P.v_chunks[0] <= 256 &&
                gm::expand_fits(static_cast<int>(p->P.v_chunks[0]), p->P.widths[0], p->P.tau, p->smem_dev) &&
-               (p->cfg.pipeline == GM_PIPE_AUTO || p->cfg.pipeline == GM_PIPE_ROWWISE);
+               (p->cfg.pipeline == GM_PIPE_AUTO || p->cfg.pipeline == GM_PIPE_ROWWISE ||
+                p->cfg.pipeline == GM_PIPE_WALK);
   if (p->rowwise) p->pipeline = GM_PIPE_ROWWISE;
+  p->walk_ok = p->rowwise && p->cfg.pipeline == GM_PIPE_WALK && gm::walk_fits(p->P.widths[0], p->smem_dev);
   gm::g_ws_peak = gm::g_ws_now.load();
   const int64_t l0 = gm::launch_count();
   st = gm::analyze_impl(p.get());

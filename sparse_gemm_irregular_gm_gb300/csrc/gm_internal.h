@@ -97,7 +97,9 @@ void launch_validate_rowptr(const int64_t* rp, int64_t n_rows, int64_t nnz, int 
 void launch_validate_cols(const int32_t* col, int64_t nnz, int64_t n_cols, int bad_bit, int* status,
                           cudaStream_t s);
 // *unsorted |= 1 when a row's columns are not non-decreasing (rows validated first).
-void launch_check_sorted(const int64_t* rp, const int32_t* col, int64_t n_rows, int* unsorted, cudaStream_t s);
+// *flags |= 1 when some row of B has a column greater than the next one, |= 2
+// when some row repeats a column.
+void launch_check_sorted(const int64_t* rp, const int32_t* col, int64_t n_rows, int* flags, cudaStream_t s);
 // u[i] = sum over stored A[i,k] of nnz(B[k,:]); bin[i] from spec.
 void launch_ip_count(const int64_t* a_rp, const int32_t* a_col, int64_t n_rows, const int64_t* b_rp,
                      int64_t* u, uint8_t* bin, BinSpec spec, cudaStream_t s);
@@ -334,8 +336,11 @@ struct RowBitmapArgs {
   double* c_val;
   unsigned int* work_counter; // device counter for dynamic row scheduling
   int* status;
+  uint32_t* bits_out;         // symbolic: each row's bitmap, rowbm_words(c_m) words a row (null: not kept)
 };
 int64_t rowbm_symbolic_smem(int64_t c_m);
+// Words of a whole-row bitmap of C.m columns (whole 16-byte pieces).
+inline int64_t rowbm_words(int64_t c_m) { return ((c_m + 127) / 128) * 4; }
 // Heavy rows: chunk nnz (v chunks of a.width) or whole-row nnz from a whole-row bitmap.
 void launch_rowbm(const RowBitmapArgs& a, int num_sms, int64_t smem_max, cudaStream_t s);
 // Light rows of at most cap products (symbolic: whole-row nnz into c_rp; numeric: the row of C).
@@ -345,11 +350,48 @@ int64_t rowbm_light_smem(int64_t c_m, int cap, bool symbolic, int64_t smem_max);
 bool rowbm_light_fits(int64_t c_m, int cap, bool symbolic, int64_t smem_max);
 void launch_rowbm_light(const RowBitmapArgs& a, bool symbolic, int cap, int num_sms, int64_t smem_max, cudaStream_t s);
 
+// bcp only (see heavy_chunk_counts), v <= 256.
+void build_chunk_starts(const int64_t* b_rp, const int32_t* b_col, int64_t b_rows, int v, int shift, int32_t* bcp,
+                        cudaStream_t s);
+// Heavy rows' level-0 chunks summed straight from the B ranges inside each chunk
+// (gm_walk.cu). Items j = c * nh + h (chunk-major) name chunk c of heavy row h.
+struct WalkArgs {
+  const int32_t* heavy_rows;  // nh original row ids
+  int64_t nh;
+  int v;                      // level-0 chunks per row
+  int shift;                  // log2 of the chunk width
+  int nwc;                    // bitmap words per chunk (width / 32, a multiple of 4)
+  int64_t nwr;                // bitmap words per row (rowbm_words(C.m))
+  const uint32_t* bits;       // nh whole-row bitmaps from the symbolic pass
+  const int64_t* a_rp;
+  const int32_t* a_col;
+  const double* a_val;
+  const int64_t* b_rp;
+  const int32_t* b_col;
+  const double* b_val;
+  const int32_t* bcp;         // per-B-row chunk starts, B.n_rows * (v + 1)
+  const int64_t* off;         // output offset of chunk c of heavy row h at [h * v + c]
+  const int64_t* items;       // item ids j of one class
+  int64_t n_items;
+  unsigned int* counter;      // dynamic item scheduling
+  int32_t* c_col;
+  double* c_val;
+  int* status;
+};
+// Classes 1-3: one warp per item of at most 256 / 1024 / 2048 columns; 4-5: one
+// block per item, atomic adds.
+int64_t walk_class_cap(int cls, int64_t width);
+int64_t walk_smem(int cls, int64_t width);
+bool walk_fits(int64_t width, int64_t smem_max);
+void launch_walk_class(const int64_t* cnnz, int64_t nh, int v, uint8_t* cls, cudaStream_t s);
+void launch_walk(const WalkArgs& a, int cls, int num_sms, int64_t smem_max, cudaStream_t s);
+
 // cnt[h * v + c] = products of heavy row h whose column falls in level-0 chunk c
 // (col >> shift == c), from per-B-row chunk counts, which are left in bcp
 // (b_rows * (v + 1) entries: bcp[k * (v + 1) + c] = entries of B row k in chunks
 // below c; for a row sorted by column, chunk c is its index range [bcp[c], bcp[c+1])).
-// anz: prefix of the heavy rows' A-row lengths (n_heavy + 1). False when v > 256.
+// anz: prefix of the heavy rows' A-row lengths (n_heavy + 1). cnt null: bcp only;
+// b_rp null: bcp is already built. False when v > 256.
 bool heavy_chunk_counts(const int32_t* heavy_rows, int64_t n_heavy, const int64_t* anz, const int64_t* a_rp,
                         const int32_t* a_col, const int64_t* b_rp, const int32_t* b_col, int64_t b_rows, int v,
                         int shift, int32_t* bcp, int64_t* cnt, cudaStream_t s);

@@ -142,6 +142,11 @@ __global__ void __launch_bounds__(kRbThreads) k_rowbm_symbolic(RowBitmapArgs a, 
     __syncthreads();
     mark_row(a, r, bm, longs);
     __syncthreads();
+    if (a.bits_out) {  // the row's bitmap stays for the numeric pass
+      uint4* dst = reinterpret_cast<uint4*>(a.bits_out + item * static_cast<int64_t>(nwords));
+      const uint4* b4 = reinterpret_cast<const uint4*>(bm);
+      for (int i = threadIdx.x; i < (nwords >> 2); i += blockDim.x) dst[i] = b4[i];
+    }
     if (a.v == 1 && a.width >= nbits) {  // whole row
       int n = 0;
       for (int w = threadIdx.x; w < nwords; w += blockDim.x) n += __popc(bm[w]);
@@ -446,7 +451,7 @@ void launch_rowbm_light(const RowBitmapArgs& a, bool symbolic, int cap, int num_
 void launch_rowbm(const RowBitmapArgs& a, int num_sms, int64_t smem_max, cudaStream_t s) {
   if (a.n_items <= 0) return;
   cudaMemsetAsync(a.work_counter, 0, sizeof(unsigned int), s);
-  const int64_t nwords4 = ((a.c_m + 127) / 128) * 4;  // whole uint4 stores
+  const int64_t nwords4 = rowbm_words(a.c_m);  // whole uint4 stores
   const size_t smem = static_cast<size_t>(rowbm_symbolic_smem(a.c_m));
   const int per_sm = std::max<int>(1, static_cast<int>(smem_max / static_cast<int64_t>(smem + 1024)));
   const int64_t blocks = std::min<int64_t>(a.n_items, static_cast<int64_t>(num_sms) * std::min(per_sm, 2));
@@ -541,15 +546,20 @@ __global__ void k_heavy_chunk_counts(const int32_t* __restrict__ rows, int64_t n
 
 }  // namespace
 
-bool heavy_chunk_counts(const int32_t* heavy_rows, int64_t n_heavy, const int64_t* anz, const int64_t* a_rp,
-                        const int32_t* a_col, const int64_t* b_rp, const int32_t* b_col, int64_t b_rows, int v,
-                        int shift, int32_t* bcp, int64_t* cnt, cudaStream_t s) {
-  if (v > 256) return false;
+void build_chunk_starts(const int64_t* b_rp, const int32_t* b_col, int64_t b_rows, int v, int shift, int32_t* bcp,
+                        cudaStream_t s) {
   const int warps = 8;
   if (b_rows > 0)
     (k_b_chunk_prefix<<<grid_for(b_rows * 32, warps * 32), warps * 32, warps * v * sizeof(int), s>>>(
          b_rp, b_col, b_rows, v, shift, bcp), note_launch());
-  if (n_heavy <= 0) return true;
+}
+
+bool heavy_chunk_counts(const int32_t* heavy_rows, int64_t n_heavy, const int64_t* anz, const int64_t* a_rp,
+                        const int32_t* a_col, const int64_t* b_rp, const int32_t* b_col, int64_t b_rows, int v,
+                        int shift, int32_t* bcp, int64_t* cnt, cudaStream_t s) {
+  if (v > 256) return false;
+  if (b_rp) build_chunk_starts(b_rp, b_col, b_rows, v, shift, bcp, s);
+  if (n_heavy <= 0 || cnt == nullptr) return true;
   cudaMemsetAsync(cnt, 0, static_cast<size_t>(n_heavy) * v * sizeof(int64_t), s);
   (k_heavy_chunk_counts<<<152 * 16, 256, 0, s>>>(heavy_rows, n_heavy, anz, a_rp, a_col, bcp, v,
                                                  reinterpret_cast<unsigned long long*>(cnt)), note_launch());

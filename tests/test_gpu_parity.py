@@ -45,6 +45,10 @@ FORCED = [
     ("L1_outer", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_FUSED_HISTO}),
     ("L1_rowwise_batched", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "workspace_cap_bytes": 5 << 20,
                             "pipeline": binding.GM_PIPE_ROWWISE}),
+    ("L1_rowwise", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_ROWWISE}),
+    ("L1_walk_128", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_WALK}),
+    ("L1_walk_256", {"tau": 16, "dense_width": 256, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_WALK}),
+    ("L1_walk_wide", {"tau": 64, "dense_width": 512, "pipeline": binding.GM_PIPE_WALK}),
 ]
 
 
@@ -57,8 +61,10 @@ def test_rmat10_forced_paths(name, cfg, values):
         assert info.n_heavy_rows > 0
         if "batched" in name:
             assert info.n_batches > 1
-        if name in ("heavy_L1", "L1_wide_chunks", "L1_rowwise_batched"):
+        if name in ("heavy_L1", "L1_wide_chunks", "L1_rowwise_batched", "L1_rowwise"):
             assert info.pipeline == binding.GM_PIPE_ROWWISE
+        if name.startswith("L1_walk"):
+            assert info.pipeline == binding.GM_PIPE_WALK
         if name == "L1_outer":
             assert info.pipeline == binding.GM_PIPE_FUSED_HISTO
 
@@ -322,20 +328,24 @@ def _rows_of(M, rows):
     return gi.CSR(rows.size, M.n_cols, rp, M.col[idx].copy(), M.val[idx].copy())
 
 
-def test_large_chunks_many_tiles_exact():
+@pytest.mark.parametrize("pipeline", [binding.GM_PIPE_WALK, binding.GM_PIPE_AUTO], ids=["walk", "auto"])
+def test_large_chunks_many_tiles_exact(pipeline):
     """The heaviest rows of a scale-16 R-MAT times the whole matrix: chunks of
     tens of thousands of elements (many 4096-element tiles of the large-chunk
-    accumulator) with the R-MAT's hot columns; integer values, so exact."""
+    accumulator, block items of the walk) with the R-MAT's hot columns; integer
+    values, so exact."""
     A = gi.rmat(16, 16, seed=3, values="int")
     u = oracle.ip_counts(A, A)
     rows = np.concatenate([np.argsort(u)[-40:], np.random.default_rng(0).choice(A.n_rows, 40, replace=False)])
     As = _rows_of(A, rows)
-    info = check_full(As, A, exact=True)
+    info = check_full(As, A, exact=True, pipeline=pipeline)
     assert info.n_heavy_rows >= 40 and u[rows].max() > 16 * 4096
+    assert info.pipeline == (binding.GM_PIPE_ROWWISE if pipeline == binding.GM_PIPE_AUTO else pipeline)
 
 
+@pytest.mark.parametrize("pipeline", [binding.GM_PIPE_WALK, binding.GM_PIPE_AUTO], ids=["walk", "auto"])
 @pytest.mark.parametrize("n_hot", [5000, 13000])
-def test_chunk_with_one_hot_column(n_hot):
+def test_chunk_with_one_hot_column(n_hot, pipeline):
     """A chunk whose elements nearly all fall on one column: one run of equal rank
     crosses every thread of every tile. Row 0: n_hot products on column 7; row 1:
     the same plus products spread over the chunk; integer values."""
@@ -358,7 +368,30 @@ def test_chunk_with_one_hot_column(n_hot):
     a_col = np.concatenate([r0, r1]).astype(np.int32)
     A = gi.CSR(2, nb, np.array([0, r0.size, r0.size + r1.size], np.int64), a_col,
                rng.integers(1, 4, a_col.size).astype(np.float64))
-    check_full(A, B, exact=True, tau=64)
+    info = check_full(A, B, exact=True, tau=64, pipeline=pipeline)
+    assert info.pipeline == (binding.GM_PIPE_ROWWISE if pipeline == binding.GM_PIPE_AUTO else pipeline)
+
+
+@pytest.mark.parametrize("values", ["uniform", "int"])
+def test_walk_needs_strictly_increasing_b_rows(values):
+    """The walk adds a product without an atomic when no other lane holds its rank,
+    which needs every B row to hold each column once. Asked for the walk, a B
+    whose row repeats a column (still sorted) must get the row-order pipeline;
+    both give the oracle's C."""
+    A = gi.rmat(11, 8, seed=5, values=values)
+    rp, col, val = A.row_ptr, A.col, A.val
+    rows = [r for r in range(A.n_rows) if rp[r + 1] - rp[r] >= 2][:50]
+    col2 = np.insert(col, rp[rows], col[rp[rows]])  # each chosen row starts with its first column twice
+    val2 = np.insert(val, rp[rows], val[rp[rows]])
+    rp2 = rp + np.searchsorted(np.asarray(rows), np.arange(A.n_rows + 1), side="left")
+    B_dup = gi.CSR(A.n_rows, A.n_cols, rp2.astype(np.int64), col2.astype(np.int32), val2)
+    B_dup.check()
+    assert np.all(np.diff(B_dup.col[B_dup.row_ptr[rows[0]]:B_dup.row_ptr[rows[0] + 1]]) >= 0)
+    cfg = {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_WALK}
+    info = check_full(A, A, exact=values == "int", **cfg)
+    assert info.pipeline == binding.GM_PIPE_WALK
+    info = check_full(A, B_dup, exact=values == "int", **cfg)
+    assert info.pipeline == binding.GM_PIPE_ROWWISE and info.n_heavy_rows > 0
 
 
 @pytest.mark.parametrize("a_density", [4, 16])
