@@ -524,6 +524,11 @@ BinSpec hash_leaf_spec() {
   s.ub[10] = INT64_MAX;
   return s;
 }
+// Most elements (hence columns) of a light chunk in hash bin b: the bin's bound,
+// tau for the top bin (a light chunk holds at most tau elements).
+int light_chunk_cap(int b, int64_t tau) {
+  return static_cast<int>(b <= 9 ? light_bin_ub(b) : tau);
+}
 int hash_leaf_cap(int b, int64_t tau, int64_t smem_max) {
   if (b <= 9) return static_cast<int>(std::max<int64_t>(64, 2 * light_bin_ub(b)));
   return light_bin_cap(10, tau, smem_max);
@@ -531,7 +536,9 @@ int hash_leaf_cap(int b, int64_t tau, int64_t smem_max) {
 }  // namespace
 
 // Accumulates the chunks [lo, lo + n) (mapped rows of one level's output) whose
-// element counts are mcount[lo ...]: bitmap accumulator when `dense`, hash otherwise.
+// element counts are mcount[lo ...]: bitmap accumulator when `dense`, hash
+// otherwise, except numeric light chunks of more than 512 elements, which take
+// the bitmap-rank block accumulator when a bitmap of the level's width fits.
 static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int64_t lo, int64_t n, bool dense,
                             bool numeric) {
   if (n <= 0) return GM_OK;
@@ -581,6 +588,8 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
       else launch_leaf_bitmap(a, static_cast<int>(std::min<int64_t>(b == 4 ? 4096 : b == 5 ? 8192 : la.width, la.width)), false, s);
     } else if (dense && b <= 2) launch_leaf_small(a, b == 1 ? 1024 : 4096, !numeric, s);
     else if (dense) launch_leaf_bitmap(a, bitmap_leaf_cap(b, la.width), !numeric, s);
+    else if (numeric && b >= 6 && leaf_blkbm_fits(la.width, light_chunk_cap(b, p->P.tau), p->smem_dev))
+      launch_leaf_blkbm(a, light_chunk_cap(b, p->P.tau), INT_MAX, s);  // wide light chunk of > 512 elements
     else launch_leaf_hash(a, hash_leaf_cap(b, p->P.tau, p->smem_dev), !numeric, s);
   }
   e = cudaGetLastError();

@@ -373,6 +373,16 @@ def test_chunk_with_one_hot_column(n_hot, pipeline):
 
 
 @pytest.mark.parametrize("values", ["uniform", "int"])
+def test_multilevel_wide_light_chunks(values):
+    """Three levels (4, 4, 2 chunks of 4096, 1024, 512 columns) with tau = 2048:
+    about 8900 level-0 chunks of 513-2048 elements leave the hierarchy as light
+    chunks, summed by the bitmap-rank accumulator at width 4096."""
+    A = gi.rmat(14, 16, seed=4, values=values)
+    info = check_full(A, A, exact=values == "int", tau=2048, dense_width=512, n_chunks_max=4)
+    assert info.params.n_levels == 3 and info.n_heavy_rows > 4000
+
+
+@pytest.mark.parametrize("values", ["uniform", "int"])
 def test_walk_needs_strictly_increasing_b_rows(values):
     """The walk adds a product without an atomic when no other lane holds its rank,
     which needs every B row to hold each column once. Asked for the walk, a B
