@@ -53,6 +53,28 @@ def parse_args():
     return ap.parse_args()
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_rmat20_ef16_AxA.json")
+
+
+def captured_traffic(workload: str, stage: str):
+    """DRAM bytes (read + write) of one step of `stage`, from the committed ncu
+    capture, while the kernel sources still hash as they did then; else None."""
+    import hashlib
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        if d["workload"] != workload or stage not in d["stages"]:
+            return None
+        for rel, digest in d["sources_sha256"].items():
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None
+        st = d["stages"][stage]
+        return int(st["dram_read_bytes"]) + int(st["dram_write_bytes"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -337,7 +359,11 @@ def run_ours(args):
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs and outputs larger than L2 (C alone is %.0f GB)" % (12 * nnz_c / 1e9)},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": captured_traffic(args.workload, dom) if args.pipeline == 0 and
+                     not plan_overrides(args) else None,
+                     "traffic_note": "DRAM read + write bytes of the stage's kernels in one step (ncu, "
+                                     "profiles/traffic_rmat20_ef16_AxA.json); null once they change",
                      "peak_kind": peak_kind, "alg_bytes_per_step": int(stage_bytes[dom])},
         "path_roofline": {"alg_bytes": int(b_alg), "frac": round((b_alg / (peak * 1e9)) / (ms / 1e3), 4),
                           "peak": peak, "unit": "GB/s", "peak_kind": peak_kind,

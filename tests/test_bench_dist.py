@@ -49,3 +49,24 @@ def test_single_rank_needs_no_process_group(monkeypatch):
     import bench
     assert bench.max_over_ranks(1.5, 1) == 1.5
     bench.barrier(1)
+
+
+def test_captured_traffic_only_while_sources_match(tmp_path, monkeypatch):
+    """bench.py reports the committed DRAM-byte capture only for its workload and
+    stage, and only while the kernel sources hash as they did at capture time."""
+    import hashlib
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1")
+    rec = {"workload": "rmat20", "stages": {"num_heavy": {"dram_read_bytes": 7, "dram_write_bytes": 5}},
+           "sources_sha256": {str(src): hashlib.sha256(b"kernel v1").hexdigest()}}
+    f = tmp_path / "traffic.json"
+    f.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.captured_traffic("rmat20", "num_heavy") == 12
+    assert bench.captured_traffic("rmat18", "num_heavy") is None
+    assert bench.captured_traffic("rmat20", "multisplit") is None
+    src.write_text("kernel v2")
+    assert bench.captured_traffic("rmat20", "num_heavy") is None
