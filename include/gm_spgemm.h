@@ -15,8 +15,10 @@
  *
  * Conventions common to every call
  *   - Matrices are CSR: row_ptr int64[n_rows+1] (row_ptr[0] = 0, non-decreasing,
- *     row_ptr[n_rows] = nnz), col_idx int32[nnz] in [0, n_cols), vals double[nnz].
- *     Rows need not be sorted and may repeat a column; repeated entries add.
+ *     row_ptr[n_rows] = nnz), col_idx int32[nnz] in [0, n_cols), vals[nnz] of
+ *     the value type gm_config.value_type selects (double, the default, or float;
+ *     A, B and C share it). Rows need not be sorted and may repeat a column;
+ *     repeated entries add.
  *   - Pointers documented "device" must be device (or managed) memory of the
  *     current CUDA device; "host" pointers are ordinary host memory.
  *   - Every call returns a gm_status; nothing is thrown across the ABI. A call
@@ -26,7 +28,7 @@
  *     count must be known on the host (documented per call).
  *   - Results: C rows sorted by column; an entry exists when some stored A[i,k]
  *     meets a stored B[k,j], also when its value is zero (structure is symbolic).
- *     fp64 sums are formed in an unspecified order.
+ *     Sums are formed in the value type, in an unspecified order.
  */
 #ifndef GM_SPGEMM_H
 #define GM_SPGEMM_H
@@ -59,8 +61,14 @@ typedef struct gm_csr {
   int64_t nnz;
   const int64_t* row_ptr; /* device, n_rows + 1 */
   const int32_t* col_idx; /* device, nnz        */
-  const double* vals;     /* device, nnz        */
+  const void* vals;       /* device, nnz values of gm_config.value_type (double by default) */
 } gm_csr;
+
+/* Value types for gm_config.value_type. The planner takes the value size into
+ * Eqs. (4)-(6) (gMAGNUS Sec. III-D: s_C.val), so float values get a larger tau
+ * and dense width than double ones. */
+#define GM_VALUE_F64 0 /* double */
+#define GM_VALUE_F32 1 /* float  */
 
 /* Flags for gm_config.flags. */
 #define GM_FLAG_TIMING 1             /* record per-stage device times (gm_plan_info.stage_ms) */
@@ -73,7 +81,7 @@ typedef struct gm_csr {
 #define GM_PIPE_FUSED_HISTO 2 /* outer product counts the level-0 chunk histogram while it writes C-hat */
 #define GM_PIPE_ROWWISE 3     /* one level only: heavy rows expanded in row order straight into their
                                  chunks (C-hat is not written); chunk sizes come from the symbolic pass */
-#define GM_PIPE_WALK 4        /* one level only, rows of B with strictly increasing columns: each heavy
+#define GM_PIPE_WALK 4        /* double values, one level only, rows of B with strictly increasing columns: each heavy
                                  row's level-0 chunk is summed straight from the ranges of the B rows
                                  that fall into it (neither C-hat nor chunk lists are written); the
                                  symbolic pass keeps the heavy rows' bitmaps (C.m / 8 bytes a row) until
@@ -92,6 +100,7 @@ typedef struct gm_config {
   int64_t workspace_cap_bytes; /* cap on heavy-path workspace; 0 = free memory minus a reserve  */
   int32_t pipeline;            /* GM_PIPE_*                                                    */
   int32_t flags;               /* GM_FLAG_*                                                    */
+  int32_t value_type;          /* GM_VALUE_*: element type of A.vals, B.vals and C's values    */
 } gm_config;
 
 #define GM_MAX_LEVELS 16
@@ -150,6 +159,8 @@ typedef struct gm_plan_info {
   int32_t device_status;       /* device-side error bits, 0 if none     */
   float stage_ms[GM_NUM_STAGES];
   int64_t kernel_launches;     /* kernels this plan has launched so far */
+  int32_t value_type;          /* GM_VALUE_* of the plan                */
+  int32_t reserved;
 } gm_plan_info;
 
 typedef struct gm_plan gm_plan; /* opaque; owns every workspace buffer */
@@ -167,10 +178,12 @@ typedef int64_t (*gm_avail_fn)(void* ctx);
 void gm_set_allocator(gm_alloc_fn alloc_fn, gm_free_fn free_fn, gm_avail_fn avail_fn, void* ctx);
 
 /* Host only. Fills *out with the parameters gMAGNUS Sec. III-D derives for a
- * product with c_m columns (Eqs. (4)-(7)), honouring the overrides in cfg
- * (nullable). cfg->smem_budget_bytes == 0 means 232448 bytes (227 KB, the opt-in
- * shared memory per block of sm_103a). Errors: GM_ERR_INVALID_ARG for c_m < 1,
- * a null out, or overrides that are not powers of two / too small. */
+ * product with c_m columns (Eqs. (4)-(7)) for int32 columns, int64 row pointers
+ * and the value type of cfg (8-byte double by default, 4-byte float), honouring
+ * the overrides in cfg (nullable). cfg->smem_budget_bytes == 0 means 232448
+ * bytes (227 KB, the opt-in shared memory per block of sm_103a). Errors:
+ * GM_ERR_INVALID_ARG for c_m < 1, a null out, an unknown value type, or
+ * overrides that are not powers of two / too small. */
 gm_status gm_spgemm_params(int64_t c_m, const gm_config* cfg, gm_params* out);
 
 /* Algorithm 3 lines 2-5. Validates A and B (sizes on the host, indices on the
@@ -196,12 +209,13 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
  * GM_ERR_CUDA, GM_ERR_DEVICE_TIMEOUT. */
 gm_status gm_spgemm_symbolic(gm_plan* plan, int64_t* C_row_ptr, int64_t* C_nnz);
 
-/* Algorithm 3 lines 26-28. Fills C.col (device int32[C_nnz]) and C.val (device
- * double[C_nnz]), both caller allocated after gm_spgemm_symbolic; each row sorted
+/* Algorithm 3 lines 26-28. Fills C.col (device int32[C_nnz]) and C.val (device,
+ * C_nnz values of the plan's value type), both caller allocated after
+ * gm_spgemm_symbolic; each row sorted
  * by column. Returns once the work is issued and has completed (stream synchronised).
  * Errors: GM_ERR_STATE (symbolic not done, or numeric already done),
  * GM_ERR_INVALID_ARG, GM_ERR_WORKSPACE, GM_ERR_OOM, GM_ERR_CUDA. */
-gm_status gm_spgemm_numeric(gm_plan* plan, int32_t* C_col_idx, double* C_vals);
+gm_status gm_spgemm_numeric(gm_plan* plan, int32_t* C_col_idx, void* C_vals);
 
 /* Copies the plan's parameters, sizes and statistics (gMAGNUS Tables V/VI:
  * C-hat size, heavy IP and row fractions, chunks per level) into *out (host). */
@@ -226,10 +240,10 @@ enum {
   GM_DBG_LIGHT_ROWS = 2,   /* int32[n_light + n_empty] x_light, ascending   */
   GM_DBG_CHAT_ROWPTR = 3,  /* int64[n_heavy+1] C-hat.rowPtr                 */
   GM_DBG_CHAT_COL = 4,     /* int32[ip_heavy] C-hat.col                     */
-  GM_DBG_CHAT_VAL = 5,     /* double[ip_heavy] C-hat.val                    */
+  GM_DBG_CHAT_VAL = 5,     /* value type[ip_heavy] C-hat.val                */
   GM_DBG_REORD_ROWPTR = 6, /* int64[rows+1]   C-hat_reord.rowPtr at `level` */
   GM_DBG_REORD_COL = 7,    /* int32[...]      chunk-local columns           */
-  GM_DBG_REORD_VAL = 8,    /* double[...]                                   */
+  GM_DBG_REORD_VAL = 8,    /* value type[...]                               */
   GM_DBG_REORD_CHILD = 9   /* int64[rows]     id (parent * v + chunk) of each C-hat_reord row */
 };
 gm_status gm_spgemm_debug_copy(const gm_plan* plan, int view, int level, void* dst, int64_t bytes,

@@ -18,6 +18,7 @@ GM_NUM_STAGES = 16
 STATUS_NAMES = ["GM_OK", "GM_ERR_INVALID_ARG", "GM_ERR_DIM_MISMATCH", "GM_ERR_INDEX_OVERFLOW", "GM_ERR_OOM",
                 "GM_ERR_WORKSPACE", "GM_ERR_CUDA", "GM_ERR_DEVICE_TIMEOUT", "GM_ERR_STATE", "GM_ERR_BAD_INDEX"]
 GM_FLAG_TIMING, GM_FLAG_KEEP_INTERMEDIATES, GM_FLAG_LOG = 1, 2, 4
+GM_VALUE_F64, GM_VALUE_F32 = 0, 1
 GM_PIPE_AUTO, GM_PIPE_UNFUSED, GM_PIPE_FUSED_HISTO, GM_PIPE_ROWWISE, GM_PIPE_WALK = 0, 1, 2, 3, 4
 PIPELINES = {GM_PIPE_AUTO: "auto", GM_PIPE_UNFUSED: "outer-product, unfused",
              GM_PIPE_FUSED_HISTO: "outer-product, fused level-0 histogram",
@@ -41,7 +42,7 @@ class gm_csr(ctypes.Structure):
 class gm_config(ctypes.Structure):
     _fields_ = [("smem_budget_bytes", ctypes.c_int64), ("tau", ctypes.c_int64), ("dense_width", ctypes.c_int64),
                 ("n_chunks_max", ctypes.c_int64), ("workspace_cap_bytes", ctypes.c_int64),
-                ("pipeline", ctypes.c_int32), ("flags", ctypes.c_int32)]
+                ("pipeline", ctypes.c_int32), ("flags", ctypes.c_int32), ("value_type", ctypes.c_int32)]
 
 
 class gm_params(ctypes.Structure):
@@ -59,7 +60,8 @@ class gm_plan_info(ctypes.Structure):
                 ("workspace_peak_bytes", ctypes.c_int64), ("n_leaves", ctypes.c_int64),
                 ("keeps_reordered", ctypes.c_int32), ("pipeline", ctypes.c_int32),
                 ("cuda_error", ctypes.c_int32), ("device_status", ctypes.c_int32),
-                ("stage_ms", ctypes.c_float * GM_NUM_STAGES), ("kernel_launches", ctypes.c_int64)]
+                ("stage_ms", ctypes.c_float * GM_NUM_STAGES), ("kernel_launches", ctypes.c_int64),
+                ("value_type", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class GmError(RuntimeError):
@@ -189,7 +191,7 @@ def gm_spgemm_params(c_m: int, cfg: gm_config | None = None) -> gm_params:
 
 @dataclass
 class DeviceCSR:
-    """CSR operand whose arrays are torch CUDA tensors (int64 / int32 / float64)."""
+    """CSR operand whose arrays are torch CUDA tensors (int64 / int32 / float64 or float32)."""
 
     n_rows: int
     n_cols: int
@@ -206,11 +208,23 @@ class DeviceCSR:
                       self.col.data_ptr() if self.nnz else None, self.val.data_ptr() if self.nnz else None)
 
 
-def to_device(M, device="cuda") -> DeviceCSR:
-    """Copy a host CSR (``inputs.CSR``) to torch CUDA tensors."""
+def to_device(M, device="cuda", dtype=None) -> DeviceCSR:
+    """Copy a host CSR (``inputs.CSR``) to torch CUDA tensors; values as ``dtype``
+    (numpy float32 or float64, default: as stored)."""
     import torch
+    val = M.val if dtype is None else M.val.astype(dtype)
     return DeviceCSR(M.n_rows, M.n_cols, torch.from_numpy(M.row_ptr).to(device),
-                     torch.from_numpy(M.col).to(device), torch.from_numpy(M.val).to(device))
+                     torch.from_numpy(M.col).to(device), torch.from_numpy(val).to(device))
+
+
+def _value_type(A: DeviceCSR, B: DeviceCSR) -> int:
+    """GM_VALUE_* of the operands' value tensors (A and B must agree)."""
+    import torch
+    kinds = {torch.float64: GM_VALUE_F64, torch.float32: GM_VALUE_F32}
+    ta, tb = kinds.get(A.val.dtype), kinds.get(B.val.dtype)
+    if ta is None or tb is None or ta != tb:
+        raise GmError(1, f"values must be float64 or float32 in both A and B, not {A.val.dtype} and {B.val.dtype}")
+    return ta
 
 
 def _stream_handle(stream):
@@ -220,8 +234,15 @@ def _stream_handle(stream):
 
 
 def gm_spgemm_analyze(A: DeviceCSR, B: DeviceCSR, cfg: gm_config | None = None, stream=None):
+    """gm_spgemm_analyze with cfg.value_type taken from the operands' value dtype."""
     plan = ctypes.c_void_p()
     a, b = A.desc(), B.desc()
+    vt = _value_type(A, B)
+    if cfg is None and vt != GM_VALUE_F64:
+        cfg = gm_config()
+    if cfg is not None:
+        cfg = gm_config.from_buffer_copy(cfg)
+        cfg.value_type = vt
     _check(load().gm_spgemm_analyze(ctypes.byref(a), ctypes.byref(b), ctypes.byref(cfg) if cfg else None,
                                     _stream_handle(stream), ctypes.byref(plan)), "gm_spgemm_analyze")
     return plan
@@ -253,8 +274,9 @@ def gm_spgemm_debug_copy(plan, view: int, level: int = 0):
     import numpy as np
     size = ctypes.c_int64(0)
     _check(load().gm_spgemm_debug_copy(plan, view, level, None, 0, ctypes.byref(size)), "gm_spgemm_debug_copy")
+    vdt = np.float32 if gm_spgemm_plan_info(plan).value_type == GM_VALUE_F32 else np.float64
     dtype = {GM_DBG_HEAVY_ROWS: np.int32, GM_DBG_LIGHT_ROWS: np.int32, GM_DBG_CHAT_COL: np.int32,
-             GM_DBG_REORD_COL: np.int32, GM_DBG_CHAT_VAL: np.float64, GM_DBG_REORD_VAL: np.float64}.get(view, np.int64)
+             GM_DBG_REORD_COL: np.int32, GM_DBG_CHAT_VAL: vdt, GM_DBG_REORD_VAL: vdt}.get(view, np.int64)
     out = np.empty(size.value // np.dtype(dtype).itemsize, dtype=dtype)
     if size.value:
         _check(load().gm_spgemm_debug_copy(plan, view, level, out.ctypes.data, size.value, None),
@@ -279,7 +301,7 @@ def spgemm(A: DeviceCSR, B: DeviceCSR, cfg: gm_config | None = None, stream=None
         c_rp = torch.empty(A.n_rows + 1, dtype=torch.int64, device=dev)
         nnz = gm_spgemm_symbolic(plan, c_rp)
         c_col = torch.empty(nnz, dtype=torch.int32, device=dev)
-        c_val = torch.empty(nnz, dtype=torch.float64, device=dev)
+        c_val = torch.empty(nnz, dtype=A.val.dtype, device=dev)
         gm_spgemm_numeric(plan, c_col, c_val)
         info = gm_spgemm_plan_info(plan) if return_info else None
     finally:

@@ -28,13 +28,17 @@ constexpr int32_t kEmpty = -1;
 
 // ---- light rows: one warp per row, sort-based ---------------------------------
 
-template <bool SYM, int CAPW, int WARPS>
+template <typename V, bool SYM, int CAPW, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32) k_light_warp(LightArgs a) {
+  const V* __restrict__ a_val = static_cast<const V*>(a.a_val);
+  const V* __restrict__ b_val = static_cast<const V*>(a.b_val);
+  V* __restrict__ c_val = static_cast<V*>(a.c_val);
+
   __shared__ int32_t s_key[WARPS][CAPW];
-  __shared__ double s_val[SYM ? 1 : WARPS][SYM ? 1 : CAPW];
+  __shared__ V s_val[SYM ? 1 : WARPS][SYM ? 1 : CAPW];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   int32_t* key = s_key[w];
-  double* val = SYM ? nullptr : s_val[w];
+  V* val = SYM ? nullptr : s_val[w];
   for (int64_t item = static_cast<int64_t>(blockIdx.x) * WARPS + w; item < a.n_items;
        item += static_cast<int64_t>(gridDim.x) * WARPS) {
     const int64_t r = a.rows[item];
@@ -44,19 +48,19 @@ __global__ void __launch_bounds__(WARPS * 32) k_light_warp(LightArgs a) {
       const int64_t p = p0 + lane;
       int len = 0;
       int64_t bs = 0;
-      double av = 0.0;
+      V av = 0.0;
       if (p < hi) {
         const int k = a.a_col[p];
         bs = a.b_rp[k];
         len = static_cast<int>(a.b_rp[k + 1] - bs);
-        if (!SYM) av = a.a_val[p];
+        if (!SYM) av = a_val[p];
       }
       const int inc = warp_inclusive_scan(len);
       const int off = pos + inc - len;
       for (int q = 0; q < len; ++q) {
         if (off + q < CAPW) {
           key[off + q] = a.b_col[bs + q];
-          if (!SYM) val[off + q] = av * a.b_val[bs + q];
+          if (!SYM) val[off + q] = av * b_val[bs + q];
         }
       }
       pos += __shfl_sync(kFull, inc, 31);
@@ -76,7 +80,7 @@ __global__ void __launch_bounds__(WARPS * 32) k_light_warp(LightArgs a) {
               key[i] = kj;
               key[ixj] = ki;
               if (!SYM) {
-                const double t = val[i];
+                const V t = val[i];
                 val[i] = val[ixj];
                 val[ixj] = t;
               }
@@ -94,12 +98,12 @@ __global__ void __launch_bounds__(WARPS * 32) k_light_warp(LightArgs a) {
       const bool head = i < nn && (i == 0 || key[i] != key[i - 1]);
       const unsigned hb = __ballot_sync(kFull, head);
       if (!SYM && head) {
-        double s = 0.0;
+        V s = 0.0;
         const int32_t c = key[i];
         for (int t = i; t < nn && key[t] == c; ++t) s += val[t];
         const int rank = run + __popc(hb & lanemask_lt());
         a.c_col[out + rank] = c;
-        a.c_val[out + rank] = s;
+        c_val[out + rank] = s;
       }
       run += __popc(hb);
     }
@@ -139,14 +143,15 @@ __device__ __forceinline__ int hash_insert(int32_t* keys, int cap, int32_t c, bo
 
 // After accumulation: move the occupied slots to the front (order kept), sort
 // them by column and write nnz entries at out. keys/vals hold cap slots.
-__device__ void compact_sort_write(int32_t* keys, double* vals, int cap, int nnz, int32_t* c_col, double* c_val,
+template <typename V>
+__device__ void compact_sort_write(int32_t* keys, V* vals, int cap, int nnz, int32_t* c_col, V* c_val,
                                    int64_t out, int64_t col_base) {
   __shared__ int ws[33];
   int run = 0;
   for (int base = 0; base < cap; base += blockDim.x) {
     const int i = base + threadIdx.x;
     const int32_t k = i < cap ? keys[i] : kEmpty;
-    const double v = i < cap ? vals[i] : 0.0;
+    const V v = i < cap ? vals[i] : 0.0;
     const int flag = k != kEmpty;
     int tot;
     const int pre = block_exclusive_scan(flag, ws, &tot);
@@ -172,7 +177,7 @@ __device__ void compact_sort_write(int32_t* keys, double* vals, int cap, int nnz
           if ((ki > kj) == up) {
             keys[i] = kj;
             keys[ixj] = ki;
-            const double t = vals[i];
+            const V t = vals[i];
             vals[i] = vals[ixj];
             vals[ixj] = t;
           }
@@ -187,11 +192,15 @@ __device__ void compact_sort_write(int32_t* keys, double* vals, int cap, int nnz
   }
 }
 
-template <bool SYM, bool POW2>
+template <typename V, bool SYM, bool POW2>
 __global__ void k_light_hash(LightArgs a, int cap) {
+  const V* __restrict__ a_val = static_cast<const V*>(a.a_val);
+  const V* __restrict__ b_val = static_cast<const V*>(a.b_val);
+  V* __restrict__ c_val = static_cast<V*>(a.c_val);
+
   extern __shared__ __align__(16) unsigned char smem[];
-  double* vals = reinterpret_cast<double*>(smem);
-  int32_t* keys = reinterpret_cast<int32_t*>(smem + (SYM ? 0 : static_cast<size_t>(cap) * 8));
+  V* vals = reinterpret_cast<V*>(smem);
+  int32_t* keys = reinterpret_cast<int32_t*>(smem + (SYM ? 0 : static_cast<size_t>(cap) * sizeof(V)));
   __shared__ int ws[33];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   for (int64_t item = blockIdx.x; item < a.n_items; item += gridDim.x) {
@@ -205,12 +214,12 @@ __global__ void k_light_hash(LightArgs a, int cap) {
     bool full = false;
     for (int64_t p = a.a_rp[r] + warp; p < a.a_rp[r + 1]; p += nwarps) {
       const int k = a.a_col[p];
-      const double av = SYM ? 0.0 : a.a_val[p];
+      const V av = SYM ? 0.0 : a_val[p];
       for (int64_t q = a.b_rp[k] + lane; q < a.b_rp[k + 1]; q += 32) {
         bool fresh = false;
         const int s = hash_insert<POW2>(keys, cap, a.b_col[q], &fresh, &full);
         fresh_count += fresh;
-        if (!SYM && s >= 0) atomicAdd(&vals[s], av * a.b_val[q]);
+        if (!SYM && s >= 0) atomicAdd(&vals[s], av * b_val[q]);
       }
     }
     if (full) atomicOr(a.status, kStHashFull);
@@ -222,7 +231,7 @@ __global__ void k_light_hash(LightArgs a, int cap) {
     } else {
       const int64_t out = a.c_rp[r];
       const int nnz = static_cast<int>(a.c_rp[r + 1] - out);
-      compact_sort_write(keys, vals, cap, nnz, a.c_col, a.c_val, out, 0);
+      compact_sort_write(keys, vals, cap, nnz, a.c_col, c_val, out, 0);
     }
     __syncthreads();
   }
@@ -240,11 +249,14 @@ __device__ __forceinline__ int64_t leaf_col_base(const ListArgs& a, int64_t chil
 
 // Chunk of width <= dense width: bitmap of its columns, prefix sum over the
 // bitmap words, values summed into their rank (= sorted output position).
-template <bool SYM>
+template <typename V, bool SYM>
 __global__ void k_leaf_bitmap(ListArgs a, int nwords, int cap_vals) {
+  const V* __restrict__ in_val = static_cast<const V*>(a.val);
+  V* __restrict__ c_val = static_cast<V*>(a.c_val);
+
   extern __shared__ __align__(16) unsigned char smem[];
-  double* vals = reinterpret_cast<double*>(smem);                                                  // cap_vals
-  uint32_t* bm = reinterpret_cast<uint32_t*>(smem + (SYM ? 0 : static_cast<size_t>(cap_vals) * 8));  // nwords
+  V* vals = reinterpret_cast<V*>(smem);                                                  // cap_vals
+  uint32_t* bm = reinterpret_cast<uint32_t*>(smem + (SYM ? 0 : (static_cast<size_t>(cap_vals) * sizeof(V) + 15) & ~size_t(15)));  // nwords
   int* pre = reinterpret_cast<int*>(bm + nwords);                                                    // nwords
   __shared__ int ws[33];
   const int T = blockDim.x;
@@ -287,12 +299,12 @@ __global__ void k_leaf_bitmap(ListArgs a, int nwords, int cap_vals) {
     __syncthreads();
     for (int64_t e0 = lo + threadIdx.x; e0 < hi; e0 += 4 * T) {
       uint32_t c[4];
-      double v[4];
+      V v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const bool in = e0 + u * T < hi;
         c[u] = in ? static_cast<uint32_t>(a.col[e0 + u * T]) : ~0u;
-        v[u] = in ? a.val[e0 + u * T] : 0.0;
+        v[u] = in ? in_val[e0 + u * T] : 0.0;
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -314,7 +326,7 @@ __global__ void k_leaf_bitmap(ListArgs a, int nwords, int cap_vals) {
         const int b = __ffs(bits) - 1;
         bits &= bits - 1;
         a.c_col[out + pos] = static_cast<int32_t>(cb + w * 32 + b);
-        a.c_val[out + pos] = vals[pos];
+        c_val[out + pos] = vals[pos];
         ++pos;
       }
     }
@@ -328,11 +340,14 @@ __global__ void k_leaf_bitmap(ListArgs a, int nwords, int cap_vals) {
 // cnt[r] gives its arrival index j; a prefix sum over cnt turns counts into
 // segment starts; values are placed at seg[r] + j and each output entry sums its
 // own segment.
-template <bool SYM, int T, int ITEMS>
+template <typename V, bool SYM, int T, int ITEMS>
 __global__ void __launch_bounds__(T) k_leaf_small(ListArgs a, int nwords) {
+  const V* __restrict__ in_val = static_cast<const V*>(a.val);
+  V* __restrict__ c_val = static_cast<V*>(a.c_val);
+
   constexpr int CAP = T * ITEMS;
   extern __shared__ __align__(16) unsigned char smem[];
-  double* vbuf = reinterpret_cast<double*>(smem);                              // CAP
+  V* vbuf = reinterpret_cast<V*>(smem);                              // CAP
   int32_t* cols = reinterpret_cast<int32_t*>(vbuf + (SYM ? 0 : CAP));           // CAP
   int* seg = reinterpret_cast<int*>(cols + (SYM ? 0 : CAP));                     // CAP + 1
   uint32_t* bm = reinterpret_cast<uint32_t*>(seg + (SYM ? 0 : CAP + 1));         // nwords
@@ -346,7 +361,7 @@ __global__ void __launch_bounds__(T) k_leaf_small(ListArgs a, int nwords) {
     const int64_t child_local = a.child_of ? a.child_of[m] : m;
     int key[ITEMS];   // column, later rank
     int arr[ITEMS];   // arrival index within the rank
-    double val[ITEMS];
+    V val[ITEMS];
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
       const int64_t e = lo + k * T + threadIdx.x;
@@ -354,7 +369,7 @@ __global__ void __launch_bounds__(T) k_leaf_small(ListArgs a, int nwords) {
       val[k] = 0.0;
       if (e < hi) {
         key[k] = a.col[e];
-        if (!SYM) val[k] = a.val[e];
+        if (!SYM) val[k] = in_val[e];
       }
     }
     for (int w = threadIdx.x; w < nwords; w += T) bm[w] = 0u;
@@ -412,10 +427,10 @@ __global__ void __launch_bounds__(T) k_leaf_small(ListArgs a, int nwords) {
     const int64_t out = a.off_in[a.child_base + child_local];
     const int64_t cb = leaf_col_base(a, child_local);
     for (int r = threadIdx.x; r < nnz; r += T) {
-      double sum = 0.0;
+      V sum = 0.0;
       for (int q = seg[r]; q < seg[r + 1]; ++q) sum += vbuf[q];
       a.c_col[out + r] = static_cast<int32_t>(cb + cols[r]);
-      a.c_val[out + r] = sum;
+      c_val[out + r] = sum;
     }
     __syncthreads();
   }
@@ -430,15 +445,18 @@ __global__ void __launch_bounds__(T) k_leaf_small(ListArgs a, int nwords) {
 // values are added into their rank's slot (chunks this small rarely repeat a
 // column, so the atomics seldom meet), and the chunk is written in column order
 // by words.
-template <int ITEMS, int WARPS>
+template <typename V, int ITEMS, int WARPS>
 __global__ void __launch_bounds__(32 * WARPS, (ITEMS >= 16 ? 160 : 256) / WARPS) k_leaf_warpbm(ListArgs a, int nwp, int vcap) {
+  const V* __restrict__ in_val = static_cast<const V*>(a.val);
+  V* __restrict__ c_val = static_cast<V*>(a.c_val);
+
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr int CAPW = 32 * ITEMS;
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  unsigned char* mine = smem + static_cast<size_t>(wib) * (static_cast<size_t>(nwp) * 8 + static_cast<size_t>(vcap) * 8);
+  unsigned char* mine = smem + static_cast<size_t>(wib) * (static_cast<size_t>(nwp) * 8 + ((static_cast<size_t>(vcap) * sizeof(V) + 15) & ~size_t(15)));
   uint32_t* bm = reinterpret_cast<uint32_t*>(mine);                 // nwp (a multiple of 128)
   int* pre = reinterpret_cast<int*>(bm + nwp);                      // nwp
-  double* vals = reinterpret_cast<double*>(pre + nwp);              // vcap
+  V* vals = reinterpret_cast<V*>(pre + nwp);              // vcap
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * WARPS + wib;
   const int64_t nw = static_cast<int64_t>(gridDim.x) * WARPS;
   for (int64_t item = gw; item < a.n_items; item += nw) {
@@ -449,7 +467,7 @@ __global__ void __launch_bounds__(32 * WARPS, (ITEMS >= 16 ? 160 : 256) / WARPS)
     const int64_t out = a.off_in[a.child_base + child_local];
     const int64_t cb = leaf_col_base(a, child_local);
     int key[ITEMS];
-    double val[ITEMS];
+    V val[ITEMS];
     for (int w = lane * 4; w < nwp; w += 128) *reinterpret_cast<uint4*>(bm + w) = make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
     for (int t0 = 0; t0 < n; t0 += CAPW) {  // columns: set the bits
@@ -457,7 +475,7 @@ __global__ void __launch_bounds__(32 * WARPS, (ITEMS >= 16 ? 160 : 256) / WARPS)
       for (int k = 0; k < ITEMS; ++k) {
         const int e = t0 + k * 32 + lane;
         key[k] = e < n ? a.col[lo + e] : -1;
-        if (n <= CAPW) val[k] = e < n ? a.val[lo + e] : 0.0;
+        if (n <= CAPW) val[k] = e < n ? in_val[lo + e] : 0.0;
       }
 #pragma unroll
       for (int k = 0; k < ITEMS; ++k)
@@ -483,7 +501,7 @@ __global__ void __launch_bounds__(32 * WARPS, (ITEMS >= 16 ? 160 : 256) / WARPS)
         for (int k = 0; k < ITEMS; ++k) {
           const int e = t0 + k * 32 + lane;
           key[k] = e < n ? a.col[lo + e] : -1;
-          val[k] = e < n ? a.val[lo + e] : 0.0;
+          val[k] = e < n ? in_val[lo + e] : 0.0;
         }
       }
 #pragma unroll
@@ -502,7 +520,7 @@ __global__ void __launch_bounds__(32 * WARPS, (ITEMS >= 16 ? 160 : 256) / WARPS)
         const int b = __ffs(bits) - 1;
         bits &= bits - 1;
         a.c_col[out + pos] = static_cast<int32_t>(cb + w * 32 + b);
-        a.c_val[out + pos] = vals[pos];
+        c_val[out + pos] = vals[pos];
         ++pos;
       }
     }
@@ -513,13 +531,16 @@ __global__ void __launch_bounds__(32 * WARPS, (ITEMS >= 16 ? 160 : 256) / WARPS)
 // The same accumulator for chunks of up to vcap elements with 4 warps per chunk:
 // elements in tiles of 128 * ITEMS through registers, bitmap word prefix by a
 // block scan over 16-byte pieces, values added into their rank's slot.
-template <int ITEMS, int T>
+template <typename V, int ITEMS, int T>
 __global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap, int ecap) {
+  const V* __restrict__ in_val = static_cast<const V*>(a.val);
+  V* __restrict__ c_val = static_cast<V*>(a.c_val);
+
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr int CAPB = T * ITEMS;
   uint32_t* bm = reinterpret_cast<uint32_t*>(smem);                 // nwp (a multiple of 512)
   int* pre = reinterpret_cast<int*>(bm + nwp);                      // nwp
-  double* vals = reinterpret_cast<double*>(pre + nwp);              // vcap
+  V* vals = reinterpret_cast<V*>(pre + nwp);              // vcap
   __shared__ int ws[33];
   for (int64_t item = blockIdx.x; item < a.n_items; item += gridDim.x) {
     const int64_t m = a.items[item];
@@ -529,7 +550,7 @@ __global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap,
     const int64_t out = a.off_in[a.child_base + child_local];
     const int64_t cb = leaf_col_base(a, child_local);
     int key[ITEMS];
-    double val[ITEMS];
+    V val[ITEMS];
     for (int w = threadIdx.x * 4; w < nwp; w += 4 * T) *reinterpret_cast<uint4*>(bm + w) = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
     for (int t0 = 0; t0 < n; t0 += CAPB) {  // columns: set the bits
@@ -537,7 +558,7 @@ __global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap,
       for (int k = 0; k < ITEMS; ++k) {
         const int e = t0 + k * T + threadIdx.x;
         key[k] = e < n ? a.col[lo + e] : -1;
-        if (n <= CAPB) val[k] = e < n ? a.val[lo + e] : 0.0;
+        if (n <= CAPB) val[k] = e < n ? in_val[lo + e] : 0.0;
       }
 #pragma unroll
       for (int k = 0; k < ITEMS; ++k)
@@ -569,7 +590,7 @@ __global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap,
         for (int k = 0; k < ITEMS; ++k) {
           const int e = t0 + k * T + threadIdx.x;
           key[k] = e < n ? a.col[lo + e] : -1;
-          val[k] = e < n ? a.val[lo + e] : 0.0;
+          val[k] = e < n ? in_val[lo + e] : 0.0;
         }
       }
 #pragma unroll
@@ -588,7 +609,7 @@ __global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap,
         const int b = __ffs(bits) - 1;
         bits &= bits - 1;
         a.c_col[out + pos] = static_cast<int32_t>(cb + w * 32 + b);
-        a.c_val[out + pos] = vals[pos];
+        c_val[out + pos] = vals[pos];
         ++pos;
       }
     }
@@ -599,13 +620,16 @@ __global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap,
 // Tiny chunk (at most CAPW elements): one warp loads it into shared memory,
 // sorts (column, value) pairs with a bitonic network, merges equal columns and
 // writes the chunk in column order. No bitmap, no block barrier.
-template <int CAPW, int WARPS>
+template <typename V, int CAPW, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32) k_leaf_warp(ListArgs a) {
+  const V* __restrict__ in_val = static_cast<const V*>(a.val);
+  V* __restrict__ c_val = static_cast<V*>(a.c_val);
+
   __shared__ int32_t s_key[WARPS][CAPW];
-  __shared__ double s_val[WARPS][CAPW];
+  __shared__ V s_val[WARPS][CAPW];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   int32_t* key = s_key[w];
-  double* val = s_val[w];
+  V* val = s_val[w];
   for (int64_t item = static_cast<int64_t>(blockIdx.x) * WARPS + w; item < a.n_items;
        item += static_cast<int64_t>(gridDim.x) * WARPS) {
     const int64_t m = a.items[item];
@@ -614,7 +638,7 @@ __global__ void __launch_bounds__(WARPS * 32) k_leaf_warp(ListArgs a) {
     const int64_t child_local = a.child_of ? a.child_of[m] : m;
     for (int i = lane; i < CAPW; i += 32) {
       key[i] = i < n ? a.col[lo + i] : INT_MAX;
-      val[i] = i < n ? a.val[lo + i] : 0.0;
+      val[i] = i < n ? in_val[lo + i] : 0.0;
     }
     __syncwarp();
     for (int k = 2; k <= CAPW; k <<= 1) {
@@ -626,7 +650,7 @@ __global__ void __launch_bounds__(WARPS * 32) k_leaf_warp(ListArgs a) {
             if ((ki > kj) == ((i & k) == 0)) {
               key[i] = kj;
               key[ixj] = ki;
-              const double t = val[i];
+              const V t = val[i];
               val[i] = val[ixj];
               val[ixj] = t;
             }
@@ -643,12 +667,12 @@ __global__ void __launch_bounds__(WARPS * 32) k_leaf_warp(ListArgs a) {
       const bool head = i < n && (i == 0 || key[i] != key[i - 1]);
       const unsigned hb = __ballot_sync(kFull, head);
       if (head) {
-        double sum = 0.0;
+        V sum = 0.0;
         const int32_t c = key[i];
         for (int t = i; t < n && key[t] == c; ++t) sum += val[t];
         const int r = run + __popc(hb & lanemask_lt());
         a.c_col[out + r] = static_cast<int32_t>(cb + c);
-        a.c_val[out + r] = sum;
+        c_val[out + r] = sum;
       }
       run += __popc(hb);
     }
@@ -657,11 +681,14 @@ __global__ void __launch_bounds__(WARPS * 32) k_leaf_warp(ListArgs a) {
 }
 
 // Light chunk of a level wider than the dense width: block hash accumulator.
-template <bool SYM, bool POW2>
+template <typename V, bool SYM, bool POW2>
 __global__ void k_leaf_hash(ListArgs a, int cap) {
+  const V* __restrict__ in_val = static_cast<const V*>(a.val);
+  V* __restrict__ c_val = static_cast<V*>(a.c_val);
+
   extern __shared__ __align__(16) unsigned char smem[];
-  double* vals = reinterpret_cast<double*>(smem);
-  int32_t* keys = reinterpret_cast<int32_t*>(smem + (SYM ? 0 : static_cast<size_t>(cap) * 8));
+  V* vals = reinterpret_cast<V*>(smem);
+  int32_t* keys = reinterpret_cast<int32_t*>(smem + (SYM ? 0 : static_cast<size_t>(cap) * sizeof(V)));
   __shared__ int ws[33];
   for (int64_t item = blockIdx.x; item < a.n_items; item += gridDim.x) {
     const int64_t m = a.items[item];
@@ -677,7 +704,7 @@ __global__ void k_leaf_hash(ListArgs a, int cap) {
       bool fresh = false;
       const int s = hash_insert<POW2>(keys, cap, a.col[e], &fresh, &full);
       fresh_count += fresh;
-      if (!SYM && s >= 0) atomicAdd(&vals[s], a.val[e]);
+      if (!SYM && s >= 0) atomicAdd(&vals[s], in_val[e]);
     }
     if (full) atomicOr(a.status, kStHashFull);
     int nnz;
@@ -685,7 +712,7 @@ __global__ void k_leaf_hash(ListArgs a, int cap) {
     if (SYM) {
       if (threadIdx.x == 0) a.nnz_out[a.child_base + child_local] = nnz;
     } else {
-      compact_sort_write(keys, vals, cap, nnz, a.c_col, a.c_val, a.off_in[a.child_base + child_local],
+      compact_sort_write(keys, vals, cap, nnz, a.c_col, c_val, a.off_in[a.child_base + child_local],
                          leaf_col_base(a, child_local));
     }
     __syncthreads();
@@ -711,65 +738,141 @@ int hash_threads(int cap) { return cap <= 1024 ? 128 : cap <= 2048 ? 256 : cap <
 
 int64_t light_bin_ub(int b) { return int64_t(16) << b; }  // bins 1..9: 32 .. 8192
 
-int light_bin_cap(int b, int64_t tau, int64_t smem_max) {
+int light_bin_cap(int b, int64_t tau, int64_t smem_max, int vb) {
   if (b <= kLightWarpBins) return static_cast<int>(light_bin_ub(b));
   if (b <= 9) return static_cast<int>(2 * light_bin_ub(b));
-  return static_cast<int>(std::min<int64_t>(2 * tau, (smem_max - 1024) / 12));
+  return static_cast<int>(std::min<int64_t>(2 * tau, (smem_max - 1024) / (4 + vb)));
 }
 
-void launch_light_rows(const LightArgs& a, int cap, bool symbolic, cudaStream_t s) {
-  if (a.n_items <= 0) return;
+namespace {
+
+template <typename V>
+void launch_light_rows_t(const LightArgs& a, int cap, bool symbolic, cudaStream_t s) {
+  constexpr size_t vb = sizeof(V);
   if (cap <= 256) {
     constexpr int W = 8;
     const unsigned g = static_cast<unsigned>(std::min<int64_t>((a.n_items + W - 1) / W, 152LL * 64));
     switch (cap) {
-      case 32: symbolic ? (k_light_warp<true, 32, W><<<g, W * 32, 0, s>>>(a), note_launch()) : (k_light_warp<false, 32, W><<<g, W * 32, 0, s>>>(a), note_launch()); break;
-      case 64: symbolic ? (k_light_warp<true, 64, W><<<g, W * 32, 0, s>>>(a), note_launch()) : (k_light_warp<false, 64, W><<<g, W * 32, 0, s>>>(a), note_launch()); break;
-      case 128: symbolic ? (k_light_warp<true, 128, W><<<g, W * 32, 0, s>>>(a), note_launch()) : (k_light_warp<false, 128, W><<<g, W * 32, 0, s>>>(a), note_launch()); break;
-      default: symbolic ? (k_light_warp<true, 256, W><<<g, W * 32, 0, s>>>(a), note_launch()) : (k_light_warp<false, 256, W><<<g, W * 32, 0, s>>>(a), note_launch()); break;
+      case 32: symbolic ? (k_light_warp<V, true, 32, W><<<g, W * 32, 0, s>>>(a), note_launch()) : (k_light_warp<V, false, 32, W><<<g, W * 32, 0, s>>>(a), note_launch()); break;
+      case 64: symbolic ? (k_light_warp<V, true, 64, W><<<g, W * 32, 0, s>>>(a), note_launch()) : (k_light_warp<V, false, 64, W><<<g, W * 32, 0, s>>>(a), note_launch()); break;
+      case 128: symbolic ? (k_light_warp<V, true, 128, W><<<g, W * 32, 0, s>>>(a), note_launch()) : (k_light_warp<V, false, 128, W><<<g, W * 32, 0, s>>>(a), note_launch()); break;
+      default: symbolic ? (k_light_warp<V, true, 256, W><<<g, W * 32, 0, s>>>(a), note_launch()) : (k_light_warp<V, false, 256, W><<<g, W * 32, 0, s>>>(a), note_launch()); break;
     }
     return;
   }
   const bool pow2 = (cap & (cap - 1)) == 0;
-  const size_t smem = static_cast<size_t>(cap) * (symbolic ? 4 : 12);
+  const size_t smem = static_cast<size_t>(cap) * (symbolic ? 4 : 4 + vb);
   const int T = hash_threads(cap);
   const unsigned g = item_grid(a.n_items, 2);
   if (symbolic) {
-    auto fn = pow2 ? k_light_hash<true, true> : k_light_hash<true, false>;
+    auto fn = pow2 ? k_light_hash<V, true, true> : k_light_hash<V, true, false>;
     set_smem(fn, smem);
     (fn<<<g, T, smem, s>>>(a, cap), note_launch());
   } else {
-    auto fn = pow2 ? k_light_hash<false, true> : k_light_hash<false, false>;
+    auto fn = pow2 ? k_light_hash<V, false, true> : k_light_hash<V, false, false>;
     set_smem(fn, smem);
     (fn<<<g, T, smem, s>>>(a, cap), note_launch());
   }
 }
 
-int leaf_bitmap_smem(int64_t width, int cap_vals, bool symbolic) {
-  const int64_t nwords = (width + 31) / 32;
-  return static_cast<int>(nwords * 8 + (symbolic ? 0 : static_cast<int64_t>(cap_vals) * 8));
+template <typename V>
+void launch_leaf_small_t(const ListArgs& a, int max_elems, bool symbolic, cudaStream_t s) {
+  const int nwords = static_cast<int>((a.width + 31) / 32);
+  const unsigned g = item_grid(a.n_items, 8);
+  if (max_elems <= 1024) {
+    const size_t smem = static_cast<size_t>(leaf_small_smem(a.width, 1024, symbolic, sizeof(V)));
+    auto fn = symbolic ? k_leaf_small<V, true, 128, 8> : k_leaf_small<V, false, 128, 8>;
+    set_smem(fn, smem);
+    (fn<<<g, 128, smem, s>>>(a, nwords), note_launch());
+  } else {
+    const size_t smem = static_cast<size_t>(leaf_small_smem(a.width, 4096, symbolic, sizeof(V)));
+    auto fn = symbolic ? k_leaf_small<V, true, 256, 16> : k_leaf_small<V, false, 256, 16>;
+    set_smem(fn, smem);
+    (fn<<<g, 256, smem, s>>>(a, nwords), note_launch());
+  }
 }
 
-int leaf_small_smem(int64_t width, int cap, bool symbolic) {
+template <typename V>
+void launch_leaf_warpbm_t(const ListArgs& a, int max_elems, int nwp, int W, size_t smem, cudaStream_t s) {
+  const unsigned g = static_cast<unsigned>(std::min<int64_t>((a.n_items + W - 1) / W, 152LL * 64));
+  if (max_elems <= 128) {
+    set_smem(k_leaf_warpbm<V, 4, 4>, smem);
+    (k_leaf_warpbm<V, 4, 4><<<g, 128, smem, s>>>(a, nwp, max_elems), note_launch());
+  } else if (W == 4) {
+    set_smem(k_leaf_warpbm<V, 16, 4>, smem);
+    (k_leaf_warpbm<V, 16, 4><<<g, 128, smem, s>>>(a, nwp, max_elems), note_launch());
+  } else {
+    set_smem(k_leaf_warpbm<V, 16, 1>, smem);
+    (k_leaf_warpbm<V, 16, 1><<<g, 32, smem, s>>>(a, nwp, max_elems), note_launch());
+  }
+}
+
+template <typename V>
+void launch_leaf_blkbm_t(const ListArgs& a, int max_nnz, int max_elems, int nwp, size_t smem, cudaStream_t s) {
+  const unsigned g = static_cast<unsigned>(std::min<int64_t>(a.n_items, 152LL * 32));
+  // threads per chunk grow with the value array so that an SM keeps ~1000 threads busy
+  if (max_nnz <= 4096) {
+    set_smem(k_leaf_blkbm<V, 8, 128>, smem);
+    (k_leaf_blkbm<V, 8, 128><<<g, 128, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
+  } else if (max_nnz <= 8192) {
+    set_smem(k_leaf_blkbm<V, 8, 256>, smem);
+    (k_leaf_blkbm<V, 8, 256><<<g, 256, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
+  } else {
+    set_smem(k_leaf_blkbm<V, 8, 1024>, smem);
+    (k_leaf_blkbm<V, 8, 1024><<<g, 1024, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
+  }
+}
+
+template <typename V>
+void launch_leaf_bitmap_t(const ListArgs& a, int cap_vals, bool symbolic, cudaStream_t s) {
+  const int nwords = static_cast<int>((a.width + 31) / 32);
+  const size_t smem = static_cast<size_t>(leaf_bitmap_smem(a.width, cap_vals, symbolic, sizeof(V)));
+  const int T = symbolic ? 256 : (cap_vals <= 1024 ? 256 : cap_vals <= 8192 ? 512 : 1024);
+  const unsigned g = item_grid(a.n_items, 4);
+  auto fn = symbolic ? k_leaf_bitmap<V, true> : k_leaf_bitmap<V, false>;
+  set_smem(fn, smem);
+  (fn<<<g, T, smem, s>>>(a, nwords, cap_vals), note_launch());
+}
+
+template <typename V>
+void launch_leaf_hash_t(const ListArgs& a, int cap, bool symbolic, cudaStream_t s) {
+  const bool pow2 = (cap & (cap - 1)) == 0;
+  const size_t smem = static_cast<size_t>(cap) * (symbolic ? 4 : 4 + sizeof(V));
+  const int T = hash_threads(cap);
+  const unsigned g = item_grid(a.n_items, 2);
+  if (symbolic) {
+    auto fn = pow2 ? k_leaf_hash<V, true, true> : k_leaf_hash<V, true, false>;
+    set_smem(fn, smem);
+    (fn<<<g, T, smem, s>>>(a, cap), note_launch());
+  } else {
+    auto fn = pow2 ? k_leaf_hash<V, false, true> : k_leaf_hash<V, false, false>;
+    set_smem(fn, smem);
+    (fn<<<g, T, smem, s>>>(a, cap), note_launch());
+  }
+}
+
+}  // namespace
+
+void launch_light_rows(const LightArgs& a, int cap, bool symbolic, cudaStream_t s) {
+  if (a.n_items <= 0) return;
+  if (a.f32) launch_light_rows_t<float>(a, cap, symbolic, s);
+  else launch_light_rows_t<double>(a, cap, symbolic, s);
+}
+
+int leaf_bitmap_smem(int64_t width, int cap_vals, bool symbolic, int vb) {
   const int64_t nwords = (width + 31) / 32;
-  return static_cast<int>(nwords * 8 + (symbolic ? 0 : static_cast<int64_t>(cap) * 16 + 4));
+  return static_cast<int>(nwords * 8 + (symbolic ? 0 : (static_cast<int64_t>(cap_vals) * vb + 15) & ~int64_t(15)));
+}
+
+int leaf_small_smem(int64_t width, int cap, bool symbolic, int vb) {
+  const int64_t nwords = (width + 31) / 32;
+  return static_cast<int>(nwords * 8 + (symbolic ? 0 : static_cast<int64_t>(cap) * (vb + 8) + 4));
 }
 
 void launch_leaf_small(const ListArgs& a, int max_elems, bool symbolic, cudaStream_t s) {
   if (a.n_items <= 0) return;
-  const int nwords = static_cast<int>((a.width + 31) / 32);
-  const unsigned g = item_grid(a.n_items, 8);
-  if (max_elems <= 1024) {
-    const size_t smem = static_cast<size_t>(leaf_small_smem(a.width, 1024, symbolic));
-    auto fn = symbolic ? k_leaf_small<true, 128, 8> : k_leaf_small<false, 128, 8>;
-    set_smem(fn, smem);
-    (fn<<<g, 128, smem, s>>>(a, nwords), note_launch());
-  } else {
-    const size_t smem = static_cast<size_t>(leaf_small_smem(a.width, 4096, symbolic));
-    auto fn = symbolic ? k_leaf_small<true, 256, 16> : k_leaf_small<false, 256, 16>;
-    set_smem(fn, smem);
-    (fn<<<g, 256, smem, s>>>(a, nwords), note_launch());
-  }
+  if (a.f32) launch_leaf_small_t<float>(a, max_elems, symbolic, s);
+  else launch_leaf_small_t<double>(a, max_elems, symbolic, s);
 }
 
 int64_t leaf_warpbm_words(int64_t width) { return ((width + 31) / 32 + 127) & ~int64_t(127); }
@@ -778,8 +881,12 @@ int64_t leaf_warpbm_words(int64_t width) { return ((width + 31) / 32 + 127) & ~i
 // every warp is sized by max_elems).
 static int warpbm_warps(int max_elems) { return max_elems <= 1024 ? 4 : 1; }
 
-bool leaf_warpbm_fits(int64_t width, int max_elems, int64_t smem_max) {
-  const int64_t per_warp = leaf_warpbm_words(width) * 8 + static_cast<int64_t>(max_elems) * 8;
+static int64_t warpbm_region(int64_t nwp, int max_elems, int vb) {
+  return nwp * 8 + ((static_cast<int64_t>(max_elems) * vb + 15) & ~int64_t(15));
+}
+
+bool leaf_warpbm_fits(int64_t width, int max_elems, int64_t smem_max, int vb) {
+  const int64_t per_warp = warpbm_region(leaf_warpbm_words(width), max_elems, vb);
   return max_elems <= 4096 && warpbm_warps(max_elems) * per_warp + 1024 <= smem_max;
 }
 
@@ -787,77 +894,43 @@ void launch_leaf_warpbm(const ListArgs& a, int max_elems, cudaStream_t s) {
   if (a.n_items <= 0) return;
   const int nwp = static_cast<int>(leaf_warpbm_words(a.width));
   const int W = warpbm_warps(max_elems);
-  const size_t smem = W * (static_cast<size_t>(nwp) * 8 + static_cast<size_t>(max_elems) * 8);
-  const unsigned g = static_cast<unsigned>(std::min<int64_t>((a.n_items + W - 1) / W, 152LL * 64));
-  if (max_elems <= 128) {
-    set_smem(k_leaf_warpbm<4, 4>, smem);
-    (k_leaf_warpbm<4, 4><<<g, 128, smem, s>>>(a, nwp, max_elems), note_launch());
-  } else if (W == 4) {
-    set_smem(k_leaf_warpbm<16, 4>, smem);
-    (k_leaf_warpbm<16, 4><<<g, 128, smem, s>>>(a, nwp, max_elems), note_launch());
-  } else {
-    set_smem(k_leaf_warpbm<16, 1>, smem);
-    (k_leaf_warpbm<16, 1><<<g, 32, smem, s>>>(a, nwp, max_elems), note_launch());
-  }
+  const size_t smem = static_cast<size_t>(W * warpbm_region(nwp, max_elems, a.f32 ? 4 : 8));
+  if (a.f32) launch_leaf_warpbm_t<float>(a, max_elems, nwp, W, smem, s);
+  else launch_leaf_warpbm_t<double>(a, max_elems, nwp, W, smem, s);
 }
 
 int64_t leaf_blkbm_words(int64_t width) { return ((width + 31) / 32 + 511) & ~int64_t(511); }
 
-bool leaf_blkbm_fits(int64_t width, int max_elems, int64_t smem_max) {
-  return leaf_blkbm_words(width) * 8 + static_cast<int64_t>(max_elems) * 8 + 1024 <= smem_max;
+bool leaf_blkbm_fits(int64_t width, int max_elems, int64_t smem_max, int vb) {
+  return leaf_blkbm_words(width) * 8 + static_cast<int64_t>(max_elems) * vb + 1024 <= smem_max;
 }
 
 void launch_leaf_blkbm(const ListArgs& a, int max_nnz, int max_elems, cudaStream_t s) {
   if (a.n_items <= 0) return;
   const int nwp = static_cast<int>(leaf_blkbm_words(a.width));
-  const size_t smem = static_cast<size_t>(nwp) * 8 + static_cast<size_t>(max_nnz) * 8;
-  const unsigned g = static_cast<unsigned>(std::min<int64_t>(a.n_items, 152LL * 32));
-  // threads per chunk grow with the value array so that an SM keeps ~1000 threads busy
-  if (max_nnz <= 4096) {
-    set_smem(k_leaf_blkbm<8, 128>, smem);
-    (k_leaf_blkbm<8, 128><<<g, 128, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
-  } else if (max_nnz <= 8192) {
-    set_smem(k_leaf_blkbm<8, 256>, smem);
-    (k_leaf_blkbm<8, 256><<<g, 256, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
-  } else {
-    set_smem(k_leaf_blkbm<8, 1024>, smem);
-    (k_leaf_blkbm<8, 1024><<<g, 1024, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
-  }
+  const size_t smem = static_cast<size_t>(nwp) * 8 + static_cast<size_t>(max_nnz) * (a.f32 ? 4 : 8);
+  if (a.f32) launch_leaf_blkbm_t<float>(a, max_nnz, max_elems, nwp, smem, s);
+  else launch_leaf_blkbm_t<double>(a, max_nnz, max_elems, nwp, smem, s);
 }
 
 void launch_leaf_warp(const ListArgs& a, cudaStream_t s) {
   if (a.n_items <= 0) return;
   constexpr int W = 8;
   const unsigned g = static_cast<unsigned>(std::min<int64_t>((a.n_items + W - 1) / W, 152LL * 64));
-  (k_leaf_warp<128, W><<<g, W * 32, 0, s>>>(a), note_launch());
+  if (a.f32) (k_leaf_warp<float, 128, W><<<g, W * 32, 0, s>>>(a), note_launch());
+  else (k_leaf_warp<double, 128, W><<<g, W * 32, 0, s>>>(a), note_launch());
 }
 
 void launch_leaf_bitmap(const ListArgs& a, int cap_vals, bool symbolic, cudaStream_t s) {
   if (a.n_items <= 0) return;
-  const int nwords = static_cast<int>((a.width + 31) / 32);
-  const size_t smem = static_cast<size_t>(leaf_bitmap_smem(a.width, cap_vals, symbolic));
-  const int T = symbolic ? 256 : (cap_vals <= 1024 ? 256 : cap_vals <= 8192 ? 512 : 1024);
-  const unsigned g = item_grid(a.n_items, 4);
-  auto fn = symbolic ? k_leaf_bitmap<true> : k_leaf_bitmap<false>;
-  set_smem(fn, smem);
-  (fn<<<g, T, smem, s>>>(a, nwords, cap_vals), note_launch());
+  if (a.f32) launch_leaf_bitmap_t<float>(a, cap_vals, symbolic, s);
+  else launch_leaf_bitmap_t<double>(a, cap_vals, symbolic, s);
 }
 
 void launch_leaf_hash(const ListArgs& a, int cap, bool symbolic, cudaStream_t s) {
   if (a.n_items <= 0) return;
-  const bool pow2 = (cap & (cap - 1)) == 0;
-  const size_t smem = static_cast<size_t>(cap) * (symbolic ? 4 : 12);
-  const int T = hash_threads(cap);
-  const unsigned g = item_grid(a.n_items, 2);
-  if (symbolic) {
-    auto fn = pow2 ? k_leaf_hash<true, true> : k_leaf_hash<true, false>;
-    set_smem(fn, smem);
-    (fn<<<g, T, smem, s>>>(a, cap), note_launch());
-  } else {
-    auto fn = pow2 ? k_leaf_hash<false, true> : k_leaf_hash<false, false>;
-    set_smem(fn, smem);
-    (fn<<<g, T, smem, s>>>(a, cap), note_launch());
-  }
+  if (a.f32) launch_leaf_hash_t<float>(a, cap, symbolic, s);
+  else launch_leaf_hash_t<double>(a, cap, symbolic, s);
 }
 
 }  // namespace gm

@@ -179,7 +179,13 @@ static int ilog2(int64_t x) {
 }
 static bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
-constexpr int64_t kSizeCol = 4, kSizeVal = 8, kSizeRowPtr = 8, kSizeHisto = 4, kSizeBitmap = 1, kSubGroups = 32;
+constexpr int64_t kSizeCol = 4, kSizeRowPtr = 8, kSizeHisto = 4, kSizeBitmap = 1, kSubGroups = 32;
+
+// s_C.val of Sec. III-D: bytes of one value of the configured type (0 for an unknown type).
+static int64_t value_bytes(const gm_config* cfg) {
+  const int32_t t = cfg ? cfg->value_type : GM_VALUE_F64;
+  return t == GM_VALUE_F64 ? 8 : t == GM_VALUE_F32 ? 4 : 0;
+}
 constexpr int64_t kDefaultSmem = 232448;  // opt-in shared memory per block on sm_103a
 
 // GetMagnusParams: Eq. (4) tau, n_denseNumeric, Eq. (5)-(6) n_chunksMax, Eq. (7) levels.
@@ -187,6 +193,8 @@ static gm_status compute_params(int64_t c_m, const gm_config* cfg, int64_t smem_
   if (!out || c_m < 1) return GM_ERR_INVALID_ARG;
   gm_params p;
   std::memset(&p, 0, sizeof(p));
+  const int64_t kSizeVal = value_bytes(cfg);
+  if (kSizeVal == 0) return GM_ERR_INVALID_ARG;
   p.s_lm = (cfg && cfg->smem_budget_bytes) ? cfg->smem_budget_bytes : smem_dev;
   if (p.s_lm < 1024 || p.s_lm > smem_dev) return GM_ERR_INVALID_ARG;
   const int64_t tau_eq4 = p.s_lm / (2 * (kSizeCol + kSizeVal));
@@ -194,7 +202,9 @@ static gm_status compute_params(int64_t c_m, const gm_config* cfg, int64_t smem_
   if (p.tau < 1 || p.tau > tau_eq4) return GM_ERR_INVALID_ARG;
   const int64_t n_dense = p.s_lm / (kSizeVal + kSizeBitmap);
   p.dense_width = (cfg && cfg->dense_width) ? cfg->dense_width : floor_pow2(n_dense);
-  if (!is_pow2(p.dense_width) || p.dense_width * 12 + p.dense_width / 4 + 1024 > smem_dev) return GM_ERR_INVALID_ARG;
+  // the widest chunk's values and its bitmap with word prefix must fit one block
+  if (!is_pow2(p.dense_width) || p.dense_width * kSizeVal + p.dense_width / 4 + 1024 > smem_dev)
+    return GM_ERR_INVALID_ARG;
   p.n_chunks_required = next_pow2((c_m + p.dense_width - 1) / p.dense_width);
   const int64_t n_min = p.s_lm / (2 * (kSizeCol + kSizeVal));
   const int64_t n_gr = (n_min - 1 + p.tau - 1) / p.tau + 1;
@@ -283,7 +293,7 @@ struct StageEv {
 struct LevelDbg {
   DevBuf<int64_t> rp;
   DevBuf<int32_t> col;
-  DevBuf<double> val;
+  DevBuf<unsigned char> val;  // bytes of the plan's value type
   DevBuf<int64_t> child;
   int64_t rows = 0, nnz = 0;
 };
@@ -307,6 +317,8 @@ struct gm_plan {
   bool b_sorted = false;   // every row of B has non-decreasing columns (runs per chunk are contiguous)
   int32_t b_unsorted_h = 0;  // 1: some B row decreases, 2: some B row repeats a column
   bool b_strict = false;   // every row of B has strictly increasing columns
+  bool f32 = false;        // values are float (GM_VALUE_F32), else double
+  int vb = 8;              // bytes of a value
   bool walk_ok = false;    // the walk pipeline applies when B is strict and the bitmaps fit
   bool walk = false;       // numeric heavy path: chunks summed straight from B's ranges (gm_walk.cu)
   gm_params P{};
@@ -351,11 +363,11 @@ struct gm_plan {
     size_t n = 0;
   } arena_col[2];
   struct {
-    double* p = nullptr;
+    void* p = nullptr;  // n values of the plan's value type
     size_t n = 0;
   } arena_val[2];
   gm::DevBuf<int32_t> dbg_chat_col;
-  gm::DevBuf<double> dbg_chat_val;
+  gm::DevBuf<unsigned char> dbg_chat_val;
   gm::DevBuf<int64_t> dbg_chat_rp;
   std::vector<std::unique_ptr<gm::LevelDbg>> dbg_levels;
   bool dbg_ok = false;
@@ -529,9 +541,9 @@ BinSpec hash_leaf_spec() {
 int light_chunk_cap(int b, int64_t tau) {
   return static_cast<int>(b <= 9 ? light_bin_ub(b) : tau);
 }
-int hash_leaf_cap(int b, int64_t tau, int64_t smem_max) {
+int hash_leaf_cap(int b, int64_t tau, int64_t smem_max, int vb) {
   if (b <= 9) return static_cast<int>(std::max<int64_t>(64, 2 * light_bin_ub(b)));
-  return light_bin_cap(10, tau, smem_max);
+  return light_bin_cap(10, tau, smem_max, vb);
 }
 }  // namespace
 
@@ -547,8 +559,8 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
   const bool by_nnz = dense && numeric && p->leaf_nnz.p && la.child_of == nullptr;
   BinSpec spec = dense ? bitmap_leaf_spec() : hash_leaf_spec();
   if (by_nnz) spec.nbins = 9;
-  const bool warp_ok = leaf_warpbm_fits(la.width, 1024, p->smem_dev);
-  const bool blk4k_ok = leaf_blkbm_fits(la.width, 4096, p->smem_dev);
+  const bool warp_ok = leaf_warpbm_fits(la.width, 1024, p->smem_dev, p->vb);
+  const bool blk4k_ok = leaf_blkbm_fits(la.width, 4096, p->smem_dev, p->vb);
   DevBuf<uint8_t> bins;
   DevBuf<int32_t> idx;
   DevBuf<int64_t> starts_d, items;
@@ -580,17 +592,17 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
       else if (b == 8 && blk4k_ok) launch_leaf_blkbm(a, 2048, 2048, s);
       else if (b == 3 && blk4k_ok) launch_leaf_blkbm(a, 4096, 4096, s);
       else if (b == 4 && blk4k_ok) launch_leaf_blkbm(a, 4096, INT_MAX, s);
-      else if (b == 5 && leaf_blkbm_fits(la.width, 8192, p->smem_dev)) launch_leaf_blkbm(a, 8192, INT_MAX, s);
-      else if (b == 6 && leaf_blkbm_fits(la.width, static_cast<int>(la.width), p->smem_dev))
+      else if (b == 5 && leaf_blkbm_fits(la.width, 8192, p->smem_dev, p->vb)) launch_leaf_blkbm(a, 8192, INT_MAX, s);
+      else if (b == 6 && leaf_blkbm_fits(la.width, static_cast<int>(la.width), p->smem_dev, p->vb))
         launch_leaf_blkbm(a, static_cast<int>(la.width), INT_MAX, s);
       else if (b == 2 || b == 7) launch_leaf_small(a, 1024, false, s);
       else if (b == 3 || b == 8) launch_leaf_small(a, 4096, false, s);
       else launch_leaf_bitmap(a, static_cast<int>(std::min<int64_t>(b == 4 ? 4096 : b == 5 ? 8192 : la.width, la.width)), false, s);
     } else if (dense && b <= 2) launch_leaf_small(a, b == 1 ? 1024 : 4096, !numeric, s);
     else if (dense) launch_leaf_bitmap(a, bitmap_leaf_cap(b, la.width), !numeric, s);
-    else if (numeric && b >= 6 && leaf_blkbm_fits(la.width, light_chunk_cap(b, p->P.tau), p->smem_dev))
+    else if (numeric && b >= 6 && leaf_blkbm_fits(la.width, light_chunk_cap(b, p->P.tau), p->smem_dev, p->vb))
       launch_leaf_blkbm(a, light_chunk_cap(b, p->P.tau), INT_MAX, s);  // wide light chunk of > 512 elements
-    else launch_leaf_hash(a, hash_leaf_cap(b, p->P.tau, p->smem_dev), !numeric, s);
+    else launch_leaf_hash(a, hash_leaf_cap(b, p->P.tau, p->smem_dev, p->vb), !numeric, s);
   }
   e = cudaGetLastError();
   return cuda_status(p, e);
@@ -609,9 +621,10 @@ static void dbg_copy(DevBuf<T>& dst, const T* src, int64_t n, cudaStream_t s) {
 // Accumulates the level-0 chunks of heavy batch rows [h0, h1) (already filled,
 // sizes mcount) into C: the numeric leaves of the one-level hierarchy.
 static gm_status rowwise_leaves(gm_plan* p, int64_t nb, const int64_t* rrp, const int64_t* mcount, int64_t* par_base,
-                                int32_t* c_col, double* c_val) {
+                                int32_t* c_col, void* c_val) {
   const int v = static_cast<int>(p->P.v_chunks[0]);
   ListArgs la{};
+  la.f32 = p->f32;
   la.status = p->status.p;
   la.c_col = c_col;
   la.c_val = c_val;
@@ -637,7 +650,7 @@ static gm_status rowwise_leaves(gm_plan* p, int64_t nb, const int64_t* rrp, cons
 // (k_expand_rows). C-hat is never written; chunk sizes and per-B-row chunk
 // starts come from the symbolic pass.
 static gm_status run_batch_runs(gm_plan* p, int64_t h0, int64_t h1, int64_t* par_base, int32_t* c_col,
-                                double* c_val) {
+                                void* c_val) {
   const cudaStream_t s = p->s;
   const int64_t nb = h1 - h0;
   const int64_t ip = p->h_chat_rp[h1] - p->h_chat_rp[h0];
@@ -657,7 +670,7 @@ static gm_status run_batch_runs(gm_plan* p, int64_t h0, int64_t h1, int64_t* par
   if (!e_b.alloc(ne, s) || !e_row.alloc(ne, s) || !e_a.alloc(ne, s) || !e_off.alloc(ne + 1, s) ||
       !e_k.alloc(ne, s) || !ufirst.alloc(std::max<int64_t>(n_units, 1), s))
     return GM_ERR_OOM;
-  launch_gather_entries(heavy, nb, p->anz.p + h0, p->A.row_ptr, p->A.col_idx, p->A.vals, p->B.row_ptr, e_b.p, e_a.p,
+  launch_gather_entries(heavy, nb, p->anz.p + h0, p->A.row_ptr, p->A.col_idx, p->A.vals, p->f32, p->B.row_ptr, e_b.p, e_a.p,
                         e_row.p, e_off.p, s, e_k.p);
   cudaMemsetAsync(e_off.p + ne, 0, sizeof(int64_t), s);
   if (!scan_exclusive_i64(e_off.p, e_off.p, ne + 1, nullptr, s)) return GM_ERR_OOM;
@@ -674,6 +687,7 @@ static gm_status run_batch_runs(gm_plan* p, int64_t h0, int64_t h1, int64_t* par
 
   t = p->stage_begin(GM_STAGE_MULTISPLIT);
   RowRunArgs ra{};
+  ra.f32 = p->f32;
   ra.e_k = e_k.p;
   ra.e_b = e_b.p;
   ra.e_a = e_a.p;
@@ -707,7 +721,7 @@ static gm_status run_batch_runs(gm_plan* p, int64_t h0, int64_t h1, int64_t* par
 }
 
 static gm_status run_batch_rowwise(gm_plan* p, int64_t h0, int64_t h1, int64_t* par_base, int32_t* c_col,
-                                   double* c_val) {
+                                   void* c_val) {
   const cudaStream_t s = p->s;
   const int64_t nb = h1 - h0;
   const int64_t ip = p->h_chat_rp[h1] - p->h_chat_rp[h0];
@@ -728,7 +742,7 @@ static gm_status run_batch_rowwise(gm_plan* p, int64_t h0, int64_t h1, int64_t* 
   if (!e_b.alloc(ne, s) || !e_row.alloc(ne, s) || !e_a.alloc(ne, s) || !e_off.alloc(ne + 1, s) ||
       !lrp.alloc(nb + 1, s) || !bounds.alloc(n_wg + 1, s) || !wg_info.alloc(n_wg, s))
     return GM_ERR_OOM;
-  launch_gather_entries(heavy, nb, p->anz.p + h0, p->A.row_ptr, p->A.col_idx, p->A.vals, p->B.row_ptr, e_b.p, e_a.p,
+  launch_gather_entries(heavy, nb, p->anz.p + h0, p->A.row_ptr, p->A.col_idx, p->A.vals, p->f32, p->B.row_ptr, e_b.p, e_a.p,
                         e_row.p, e_off.p, s);
   cudaMemsetAsync(e_off.p + ne, 0, sizeof(int64_t), s);
   if (!scan_exclusive_i64(e_off.p, e_off.p, ne + 1, nullptr, s)) return GM_ERR_OOM;
@@ -747,6 +761,7 @@ static gm_status run_batch_rowwise(gm_plan* p, int64_t h0, int64_t h1, int64_t* 
 
   t = p->stage_begin(GM_STAGE_MULTISPLIT);
   ExpandArgs ea{};
+  ea.f32 = p->f32;
   ea.e_b = e_b.p;
   ea.e_a = e_a.p;
   ea.e_off = e_off.p;
@@ -781,7 +796,7 @@ static gm_status run_batch_rowwise(gm_plan* p, int64_t h0, int64_t h1, int64_t* 
 // Symbolic: leaf nnz into p->nnz[level], heavy children into p->heavy_list / p->pbase.
 // Numeric: C entries at the offsets held in p->nnz[level].
 static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int64_t* par_base, int32_t* c_col,
-                           double* c_val) {
+                           void* c_val) {
   const cudaStream_t s = p->s;
   const int64_t nb = h1 - h0;
   const int64_t ip = p->h_chat_rp[h1] - p->h_chat_rp[h0];
@@ -801,7 +816,7 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
   if (!col_ptr.alloc(ncols + 1, s) || !slice_off.alloc(ncols + 1, s) || !t_row.alloc(anz, s) ||
       !t_val.alloc(anz, s) || !wg_op.alloc(n_wg_op, s))
     return GM_ERR_OOM;
-  TransposeArgs ta{heavy, nb, p->A.row_ptr, p->A.col_idx, p->A.vals, ncols};
+  TransposeArgs ta{heavy, nb, p->A.row_ptr, p->A.col_idx, p->A.vals, ncols, p->f32};
   if (!masked_transpose(ta, anz, col_ptr.p, t_row.p, t_val.p, s)) return GM_ERR_OOM;
   if (!slice_offsets(col_ptr.p, p->B.row_ptr, ncols, slice_off.p, s)) return GM_ERR_OOM;
   launch_wg_slice(slice_off.p, ncols, ip, kOuterE, wg_op.p, s);
@@ -812,7 +827,7 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
   if (p->arena_col[0].n < static_cast<size_t>(ip) || (with_val && p->arena_val[0].n < static_cast<size_t>(ip)))
     return GM_ERR_WORKSPACE;
   int32_t* const chat_col = p->arena_col[0].p;
-  double* const chat_val = with_val ? p->arena_val[0].p : nullptr;
+  void* const chat_val = with_val ? p->arena_val[0].p : nullptr;
   DevBuf<int64_t> lrp;
   DevBuf<unsigned long long> cursor, cnt0;
   if (!lrp.alloc(nb + 1, s) || !cursor.alloc(nb, s)) return GM_ERR_OOM;
@@ -824,6 +839,7 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
     cudaMemsetAsync(cnt0.p, 0, cnt0.bytes(), s);
   }
   OuterArgs oa{};
+  oa.f32 = p->f32;
   oa.slice_off = slice_off.p;
   oa.col_ptr = col_ptr.p;
   oa.t_row = t_row.p;
@@ -851,11 +867,12 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
   cursor.release();
   if (p->keep) {
     dbg_copy(p->dbg_chat_col, static_cast<const int32_t*>(chat_col), ip, s);
-    if (with_val) dbg_copy(p->dbg_chat_val, static_cast<const double*>(chat_val), ip, s);
+    if (with_val) dbg_copy(p->dbg_chat_val, static_cast<const unsigned char*>(chat_val), ip * p->vb, s);
     dbg_copy(p->dbg_chat_rp, lrp.p, nb + 1, s);
   }
 
   ListArgs base_la{};
+  base_la.f32 = p->f32;
   base_la.status = p->status.p;
   base_la.c_col = c_col;
   base_la.c_val = c_val;
@@ -884,7 +901,7 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
   //    chunks that leave the hierarchy at each level.
   const int64_t* in_rp = lrp.p;
   const int32_t* in_col = chat_col;
-  const double* in_val = chat_val;
+  const void* in_val = chat_val;
   int64_t P_b = nb, in_total = ip;
   std::unique_ptr<DevBuf<int64_t>> prev_rp;
   for (int i = 0; i < L; ++i) {
@@ -901,6 +918,7 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
     if (!wg.alloc((in_total + E - 1) / E, s)) return GM_ERR_OOM;
     launch_wg_row(in_rp, P_b, E, wg.p, s);
     SplitArgs sa{};
+    sa.f32 = p->f32;
     sa.in_rp = in_rp;
     sa.n_parents = P_b;
     sa.in_col = in_col;
@@ -953,7 +971,7 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
 
     t = p->stage_begin(numeric ? GM_STAGE_MULTISPLIT : GM_STAGE_MULTISPLIT_SYM);
     int32_t* const out_col = p->arena_col[(i + 1) % 2].p;
-    double* const out_val = with_val ? p->arena_val[(i + 1) % 2].p : nullptr;
+    void* const out_val = with_val ? p->arena_val[(i + 1) % 2].p : nullptr;
     sa.inv = last ? nullptr : inv.p;
     sa.cursor = cur.p;
     sa.out_col = out_col;
@@ -965,7 +983,7 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
       auto d = std::make_unique<LevelDbg>();
       dbg_copy(d->rp, rrp->p, children + 1, s);
       dbg_copy(d->col, static_cast<const int32_t*>(out_col), in_total, s);
-      if (with_val) dbg_copy(d->val, static_cast<const double*>(out_val), in_total, s);
+      if (with_val) dbg_copy(d->val, static_cast<const unsigned char*>(out_val), in_total * p->vb, s);
       if (!d->child.alloc(children, s)) return GM_ERR_OOM;
       if (last) launch_iota_i64(d->child.p, children, 0, s);
       else cudaMemcpyAsync(d->child.p, perm64.p, children * sizeof(int64_t), cudaMemcpyDeviceToDevice, s);
@@ -1067,7 +1085,7 @@ static gm_status alloc_arena(gm_plan* p, const std::vector<std::pair<int64_t, in
     std::fprintf(stderr, "[gm_spgemm] %zu batch(es), largest %lld products, arena %.2f GB\n", batches.size(),
                  (long long)mx, mx * (with_val ? 24.0 : 8.0) / 1e9);
   const size_t col_b = ((static_cast<size_t>(mx) * 4 + 255) / 256) * 256;
-  const size_t val_b = with_val ? static_cast<size_t>(mx) * 8 : 0;
+  const size_t val_b = with_val ? ((static_cast<size_t>(mx) * p->vb + 255) / 256) * 256 : 0;
   if (!p->arena_block.alloc(nbuf * (col_b + val_b), p->s)) return GM_ERR_OOM;
   unsigned char* base = p->arena_block.p;
   for (int k = 0; k < 2; ++k) {
@@ -1075,7 +1093,7 @@ static gm_status alloc_arena(gm_plan* p, const std::vector<std::pair<int64_t, in
     p->arena_val[k] = {};
   }
   for (int k = 0; k < nbuf; ++k) {
-    p->arena_val[k].p = with_val ? reinterpret_cast<double*>(base + k * val_b) : nullptr;
+    p->arena_val[k].p = with_val ? static_cast<void*>(base + k * val_b) : nullptr;
     p->arena_val[k].n = with_val ? mx : 0;
     p->arena_col[k].p = reinterpret_cast<int32_t*>(base + nbuf * val_b + k * col_b);
     p->arena_col[k].n = mx;
@@ -1132,13 +1150,14 @@ static int64_t workspace_cap(gm_plan* p) {
   return cap;
 }
 
-static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, double* c_val) {
+static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, void* c_val) {
   for (int b = 1; b <= 10; ++b) {
     const int64_t cnt = p->bin_start[b + 1] - p->bin_start[b];
     if (cnt <= 0) continue;
     const int cap = b <= 9 ? static_cast<int>(light_bin_ub(b)) : static_cast<int>(p->P.tau);
     if (b >= 7 && rowbm_light_fits(p->c_m, cap, !numeric, p->smem_dev)) {
       RowBitmapArgs ra{};
+      ra.f32 = p->f32;
       ra.rows = p->rows_by_bin.p + p->bin_start[b];
       ra.n_items = cnt;
       ra.a_rp = p->A.row_ptr;
@@ -1157,6 +1176,7 @@ static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, double* c_val
       continue;
     }
     LightArgs la{};
+    la.f32 = p->f32;
     la.rows = p->rows_by_bin.p + p->bin_start[b];
     la.n_items = cnt;
     la.a_rp = p->A.row_ptr;
@@ -1169,7 +1189,7 @@ static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, double* c_val
     la.c_col = c_col;
     la.c_val = c_val;
     la.status = p->status.p;
-    launch_light_rows(la, light_bin_cap(b, p->P.tau, p->smem_dev), !numeric, p->s);
+    launch_light_rows(la, light_bin_cap(b, p->P.tau, p->smem_dev, p->vb), !numeric, p->s);
   }
 }
 
@@ -1190,6 +1210,7 @@ static gm_status symbolic_impl(gm_plan* p, int64_t* C_rp, int64_t* C_nnz) {
     if (p->sym_rowbm) {
       // whole-row bitmaps: chunk nnz without expanding C-hat (at most one level)
       RowBitmapArgs ra{};
+      ra.f32 = p->f32;
       ra.rows = p->rows_by_bin.p + p->bin_start[kHeavyBin];
       ra.n_items = nh;
       ra.a_rp = p->A.row_ptr;
@@ -1304,7 +1325,7 @@ heavy_done:
 // Walk pipeline, numeric heavy rows: every (heavy row, level-0 chunk) with
 // columns is an item; items are classed by the chunk's nnz in chunk-major order
 // and each class is summed straight from B's ranges (gm_walk.cu).
-static gm_status run_heavy_walk(gm_plan* p, int32_t* c_col, double* c_val) {
+static gm_status run_heavy_walk(gm_plan* p, int32_t* c_col, void* c_val) {
   const cudaStream_t s = p->s;
   const int64_t nh = p->n_heavy;
   const int v = static_cast<int>(p->P.v_chunks[0]);
@@ -1354,7 +1375,7 @@ static gm_status run_heavy_walk(gm_plan* p, int32_t* c_col, double* c_val) {
   return cuda_status(p, cudaGetLastError());
 }
 
-static gm_status numeric_impl(gm_plan* p, int32_t* C_col, double* C_val) {
+static gm_status numeric_impl(gm_plan* p, int32_t* C_col, void* C_val) {
   int t = p->stage_begin(GM_STAGE_NUM_LIGHT);
   launch_light(p, true, C_col, C_val);
   p->stage_end(t);
@@ -1421,6 +1442,8 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
   if (cfg) p->cfg = *cfg;
   p->s = static_cast<cudaStream_t>(stream);
   p->pipeline = p->cfg.pipeline == GM_PIPE_UNFUSED ? GM_PIPE_UNFUSED : GM_PIPE_FUSED_HISTO;  // may become ROWWISE
+  p->f32 = p->cfg.value_type == GM_VALUE_F32;
+  p->vb = p->f32 ? 4 : 8;
   p->timing = (p->cfg.flags & GM_FLAG_TIMING) != 0;
   p->keep = (p->cfg.flags & GM_FLAG_KEEP_INTERMEDIATES) != 0;
   p->log = (p->cfg.flags & GM_FLAG_LOG) != 0 || gm::env_log();
@@ -1444,7 +1467,8 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
                (p->cfg.pipeline == GM_PIPE_AUTO || p->cfg.pipeline == GM_PIPE_ROWWISE ||
                 p->cfg.pipeline == GM_PIPE_WALK);
   if (p->rowwise) p->pipeline = GM_PIPE_ROWWISE;
-  p->walk_ok = p->rowwise && p->cfg.pipeline == GM_PIPE_WALK && gm::walk_fits(p->P.widths[0], p->smem_dev);
+  p->walk_ok = p->rowwise && p->cfg.pipeline == GM_PIPE_WALK && !p->f32 &&
+               gm::walk_fits(p->P.widths[0], p->smem_dev);
   gm::g_ws_peak = gm::g_ws_now.load();
   const int64_t l0 = gm::launch_count();
   st = gm::analyze_impl(p.get());
@@ -1477,7 +1501,7 @@ gm_status gm_spgemm_symbolic(gm_plan* plan, int64_t* C_row_ptr, int64_t* C_nnz) 
   return st;
 }
 
-gm_status gm_spgemm_numeric(gm_plan* plan, int32_t* C_col_idx, double* C_vals) {
+gm_status gm_spgemm_numeric(gm_plan* plan, int32_t* C_col_idx, void* C_vals) {
   if (!plan) return GM_ERR_INVALID_ARG;
   if (plan->state != 2) return GM_ERR_STATE;
   if (plan->c_nnz > 0 && (!C_col_idx || !C_vals)) return GM_ERR_INVALID_ARG;
@@ -1515,6 +1539,7 @@ gm_status gm_spgemm_plan_info(const gm_plan* plan, gm_plan_info* out) {
   out->device_status = plan->dev_status;
   for (int i = 0; i < GM_NUM_STAGES; ++i) out->stage_ms[i] = plan->stage_ms[i];
   out->kernel_launches = plan->launches;
+  out->value_type = plan->f32 ? GM_VALUE_F32 : GM_VALUE_F64;
   return GM_OK;
 }
 
@@ -1562,10 +1587,10 @@ gm_status gm_spgemm_debug_copy(const gm_plan* plan, int view, int level, void* d
     case GM_DBG_LIGHT_ROWS: src = plan->rows_by_bin.p; size = plan->bin_start[gm::kHeavyBin] * 4; break;
     case GM_DBG_CHAT_ROWPTR: src = plan->chat_rp.p; size = (nh + 1) * 8; break;
     case GM_DBG_CHAT_COL: src = plan->dbg_chat_col.p; size = plan->ip_heavy * 4; break;
-    case GM_DBG_CHAT_VAL: src = plan->dbg_chat_val.p; size = plan->ip_heavy * 8; break;
+    case GM_DBG_CHAT_VAL: src = plan->dbg_chat_val.p; size = plan->ip_heavy * plan->vb; break;
     case GM_DBG_REORD_ROWPTR: src = L->rp.p; size = (L->rows + 1) * 8; break;
     case GM_DBG_REORD_COL: src = L->col.p; size = L->nnz * 4; break;
-    case GM_DBG_REORD_VAL: src = L->val.p; size = L->nnz * 8; break;
+    case GM_DBG_REORD_VAL: src = L->val.p; size = L->nnz * plan->vb; break;
     case GM_DBG_REORD_CHILD: src = L->child.p; size = L->rows * 8; break;
     default: return GM_ERR_INVALID_ARG;
   }

@@ -28,8 +28,10 @@ __global__ void k_col_count(TransposeArgs a, unsigned long long* __restrict__ cn
   }
 }
 
+template <typename V>
 __global__ void k_csc_fill(TransposeArgs a, unsigned long long* __restrict__ cursor, int32_t* __restrict__ t_row,
-                           double* __restrict__ t_val) {
+                           V* __restrict__ t_val) {
+  const V* __restrict__ a_val = static_cast<const V*>(a.a_val);
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -38,7 +40,7 @@ __global__ void k_csc_fill(TransposeArgs a, unsigned long long* __restrict__ cur
     for (int64_t p = a.a_rp[r] + lane; p < a.a_rp[r + 1]; p += 32) {
       const unsigned long long pos = atomicAdd(&cursor[a.a_col[p]], 1ull);
       t_row[pos] = static_cast<int32_t>(h);
-      t_val[pos] = a.a_val[p];
+      t_val[pos] = a_val[p];
     }
   }
 }
@@ -85,12 +87,15 @@ __device__ __forceinline__ int64_t upper_floor(const int64_t* __restrict__ arr, 
   return lo;
 }
 
-template <bool VAL, bool HISTO>
+template <typename V, bool VAL, bool HISTO>
 __global__ void __launch_bounds__(kOpThreads) k_outer(OuterArgs a) {
+  const V* __restrict__ t_val = static_cast<const V*>(a.t_val);
+  const V* __restrict__ b_val = static_cast<const V*>(a.b_val);
+  V* __restrict__ out_val = static_cast<V*>(a.out_val);
   __shared__ int32_t s_lo[kOpCap];      // local flattened start of each entry's portion
   __shared__ int64_t s_dst[kOpCap];     // C-hat index of local position p: s_dst + p
   __shared__ int64_t s_b[kOpCap];       // B index of local position p: s_b + p
-  __shared__ double s_a[kOpCap];
+  __shared__ V s_a[kOpCap];
   __shared__ int32_t s_row[kOpCap];
   __shared__ int s_end;
   const int64_t S = static_cast<int64_t>(blockIdx.x) * a.E;
@@ -121,7 +126,7 @@ __global__ void __launch_bounds__(kOpThreads) k_outer(OuterArgs a) {
         const unsigned long long d = atomicAdd(&a.cursor[row], static_cast<unsigned long long>(cnt));
         s_dst[j] = static_cast<int64_t>(d) - lo_loc;
         s_b[j] = a.b_rp[s] + (lo - seg) - lo_loc;
-        s_a[j] = a.t_val[e];
+        s_a[j] = VAL ? t_val[e] : V(0);
         s_row[j] = row;
         atomicMax(&s_end, static_cast<int>(hi - S));
       }
@@ -150,7 +155,7 @@ __global__ void __launch_bounds__(kOpThreads) k_outer(OuterArgs a) {
         col = a.b_col[bi];
         const int64_t d = s_dst[jj] + p;
         a.out_col[d] = col;
-        if (VAL) a.out_val[d] = s_a[jj] * a.b_val[bi];
+        if (VAL) out_val[d] = s_a[jj] * b_val[bi];
       }
       if (HISTO) {
         const unsigned long long key =
@@ -168,7 +173,7 @@ __global__ void __launch_bounds__(kOpThreads) k_outer(OuterArgs a) {
 }  // namespace
 
 bool masked_transpose(const TransposeArgs& a, int64_t nnz_batch, int64_t* col_ptr, int32_t* t_row,
-                      double* t_val, cudaStream_t s) {
+                      void* t_val, cudaStream_t s) {
   DevBuf<unsigned long long> cnt;
   if (!cnt.alloc(a.n_cols + 1, s)) return false;
   cudaMemsetAsync(cnt.p, 0, (a.n_cols + 1) * sizeof(unsigned long long), s);
@@ -176,7 +181,11 @@ bool masked_transpose(const TransposeArgs& a, int64_t nnz_batch, int64_t* col_pt
   // counts -> exclusive offsets; the extra last slot (zero) receives the total
   if (!scan_exclusive_i64(reinterpret_cast<int64_t*>(cnt.p), col_ptr, a.n_cols + 1, nullptr, s)) return false;
   (k_copy_u64<<<grid_for(a.n_cols + 1, 256), 256, 0, s>>>(col_ptr, cnt.p, a.n_cols + 1), note_launch());
-  if (a.n_batch > 0 && nnz_batch > 0) (k_csc_fill<<<grid_for(a.n_batch * 32, 256), 256, 0, s>>>(a, cnt.p, t_row, t_val), note_launch());
+  if (a.n_batch > 0 && nnz_batch > 0) {
+    const unsigned g = grid_for(a.n_batch * 32, 256);
+    if (a.f32) (k_csc_fill<float><<<g, 256, 0, s>>>(a, cnt.p, t_row, static_cast<float*>(t_val)), note_launch());
+    else (k_csc_fill<double><<<g, 256, 0, s>>>(a, cnt.p, t_row, static_cast<double*>(t_val)), note_launch());
+  }
   return true;
 }
 
@@ -198,12 +207,15 @@ void launch_outer_product(const OuterArgs& a, cudaStream_t s) {
   if (a.total <= 0) return;
   const int64_t n_wg = (a.total + a.E - 1) / a.E;
   const unsigned g = static_cast<unsigned>(n_wg);
-  if (a.out_val) {
-    if (a.histo) (k_outer<true, true><<<g, kOpThreads, 0, s>>>(a), note_launch());
-    else (k_outer<true, false><<<g, kOpThreads, 0, s>>>(a), note_launch());
+  if (a.out_val && a.f32) {
+    if (a.histo) (k_outer<float, true, true><<<g, kOpThreads, 0, s>>>(a), note_launch());
+    else (k_outer<float, true, false><<<g, kOpThreads, 0, s>>>(a), note_launch());
+  } else if (a.out_val) {
+    if (a.histo) (k_outer<double, true, true><<<g, kOpThreads, 0, s>>>(a), note_launch());
+    else (k_outer<double, true, false><<<g, kOpThreads, 0, s>>>(a), note_launch());
   } else {
-    if (a.histo) (k_outer<false, true><<<g, kOpThreads, 0, s>>>(a), note_launch());
-    else (k_outer<false, false><<<g, kOpThreads, 0, s>>>(a), note_launch());
+    if (a.histo) (k_outer<double, false, true><<<g, kOpThreads, 0, s>>>(a), note_launch());
+    else (k_outer<double, false, false><<<g, kOpThreads, 0, s>>>(a), note_launch());
   }
 }
 

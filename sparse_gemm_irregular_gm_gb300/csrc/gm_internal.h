@@ -123,13 +123,14 @@ struct TransposeArgs {
   int64_t n_batch;
   const int64_t* a_rp;
   const int32_t* a_col;
-  const double* a_val;
+  const void* a_val;          // float or double (f32)
   int64_t n_cols;             // A.n_cols
+  bool f32;
 };
 // Masked CSR -> CSC of A[heavy_rows, :] (counting sort by column):
 // col_ptr[n_cols+1], t_row[nnz_batch] (batch-local row), t_val[nnz_batch].
 bool masked_transpose(const TransposeArgs& a, int64_t nnz_batch, int64_t* col_ptr, int32_t* t_row,
-                      double* t_val, cudaStream_t s);
+                      void* t_val, cudaStream_t s);
 // slice_off[k] = sum_{k'<k} (col_ptr[k'+1]-col_ptr[k']) * nnz(B[k',:]), k in [0, n_cols].
 bool slice_offsets(const int64_t* col_ptr, const int64_t* b_rp, int64_t n_cols, int64_t* slice_off,
                    cudaStream_t s);
@@ -141,17 +142,18 @@ struct OuterArgs {
   const int64_t* slice_off;   // n_cols + 1
   const int64_t* col_ptr;     // n_cols + 1 (A-tilde CSC)
   const int32_t* t_row;       // A-tilde rows (batch-local C-hat rows)
-  const double* t_val;
+  const void* t_val;          // values are float or double (f32)
   const int64_t* b_rp;
   const int32_t* b_col;
-  const double* b_val;
+  const void* b_val;
   int64_t n_slices;
   int64_t total;              // C-hat.nnz of the batch
   int64_t E;                  // flattened elements per work group
   const int32_t* wg_first;
   unsigned long long* cursor; // write cursor per C-hat row (starts at C-hat.rowPtr)
   int32_t* out_col;
-  double* out_val;            // null: columns only
+  void* out_val;              // null: columns only
+  bool f32;
   // fused level-0 histogram (null when not fused)
   unsigned long long* histo;  // [rows * v]
   int v;
@@ -167,7 +169,8 @@ struct SplitArgs {
   const int64_t* in_rp;       // parent row pointers (batch-local, in_rp[0] may be > 0)
   int64_t n_parents;
   const int32_t* in_col;      // parent-local columns
-  const double* in_val;       // null: columns only
+  const void* in_val;         // null: columns only; float or double (f32)
+  bool f32;
   int64_t base;               // in_rp[0]
   int64_t total;              // in_rp[n_parents] - in_rp[0]
   int v;                      // chunks per parent
@@ -182,7 +185,7 @@ struct SplitArgs {
   const int64_t* inv;         // child -> mapped row (null: identity)
   unsigned long long* cursor; // write cursor per mapped row (starts at its row pointer)
   int32_t* out_col;
-  double* out_val;
+  void* out_val;
 };
 void launch_histogram(const SplitArgs& a, cudaStream_t s);
 void launch_multisplit(const SplitArgs& a, cudaStream_t s);
@@ -196,13 +199,14 @@ int64_t multisplit_pick_E(int v, int64_t tau, bool with_val, int64_t smem_max, i
 // written. Entries of the batch are concatenated in row order.
 struct ExpandArgs {
   const int64_t* e_b;         // B.rowPtr of the B row each entry selects (B.rowPtr[A.col])
-  const double* e_a;          // A value of each entry (null: columns only)
+  const void* e_a;            // A value of each entry (null: columns only); float or double (f32)
+  bool f32;
   const int64_t* e_off;       // flattened start of each entry's products, n_e + 1
   const int32_t* e_row;       // batch-local row of each entry
   int64_t n_e;
   const int64_t* b_rp;
   const int32_t* b_col;
-  const double* b_val;
+  const void* b_val;
   const int64_t* in_rp;       // batch row starts in the flattened space, n_parents + 1
   int64_t n_parents;
   const int64_t* bounds;      // work group g covers [bounds[g], bounds[g+1])
@@ -214,14 +218,14 @@ struct ExpandArgs {
   int* status;
   unsigned long long* cursor; // per chunk (row * v + c): write cursor from its row pointer
   int32_t* out_col;
-  double* out_val;            // null: columns only
+  void* out_val;              // null: columns only
 };
 constexpr int kExpandE = 4096;    // elements per work group (at most)
 constexpr int kExpandCap = 1024;  // entries starting inside a work group (at most)
 // Builds the batch entry arrays (e_len into e_off, then the caller scans it).
 void launch_gather_entries(const int32_t* heavy_rows, int64_t nb, const int64_t* anz_batch, const int64_t* a_rp,
-                           const int32_t* a_col, const double* a_val, const int64_t* b_rp, int64_t* e_b,
-                           double* e_a, int32_t* e_row, int64_t* e_len, cudaStream_t s, int32_t* e_k = nullptr);
+                           const int32_t* a_col, const void* a_val, bool f32, const int64_t* b_rp, int64_t* e_b,
+                           void* e_a, int32_t* e_row, int64_t* e_len, cudaStream_t s, int32_t* e_k = nullptr);
 
 // Row-order expansion into level-0 chunks with one reservation per (unit, row,
 // chunk) and contiguous writes per warp (B rows sorted; per-B-row chunk starts
@@ -229,7 +233,8 @@ void launch_gather_entries(const int32_t* heavy_rows, int64_t nb, const int64_t*
 struct RowRunArgs {
   const int32_t* e_k;         // B row of each entry
   const int64_t* e_b;         // B.rowPtr of that row
-  const double* e_a;          // A value (null: columns only)
+  const void* e_a;            // A value (null: columns only); float or double (f32)
+  bool f32;
   const int64_t* e_off;       // flattened start of each entry's products, n_e + 1
   const int32_t* e_row;       // batch-local row of each entry
   int64_t n_e;
@@ -238,13 +243,13 @@ struct RowRunArgs {
   int64_t n_units;
   int64_t* unit_first;        // n_units scratch: first entry of each unit
   const int32_t* b_col;
-  const double* b_val;
+  const void* b_val;
   const int32_t* bcp;
   int v;
   int shift;
   unsigned long long* cursor; // per chunk (row * v + c): write cursor
   int32_t* out_col;
-  double* out_val;
+  void* out_val;
   unsigned* unit_counter;
   int* status;
 };
@@ -267,14 +272,15 @@ struct LightArgs {
   int64_t n_items;
   const int64_t* a_rp;
   const int32_t* a_col;
-  const double* a_val;
+  const void* a_val;          // values are float or double (f32)
   const int64_t* b_rp;
   const int32_t* b_col;
-  const double* b_val;
+  const void* b_val;
   int64_t* c_rp;              // symbolic: counts out at c_rp[row]; numeric: row offsets in
   int32_t* c_col;
-  double* c_val;
+  void* c_val;
   int* status;
+  bool f32;
 };
 // Light rows of one bin: cap = table slots (>= 2 * max u in bin).
 void launch_light_rows(const LightArgs& a, int bin_cap, bool symbolic, cudaStream_t s);
@@ -284,7 +290,7 @@ struct ListArgs {
   int64_t n_items;
   const int64_t* rp;          // C-hat_reord row pointers (mapped order)
   const int32_t* col;         // chunk-local columns
-  const double* val;
+  const void* val;            // float or double (f32)
   const int64_t* child_of;    // mapped row -> batch-local child id (null: identity)
   int64_t child_base;         // global child id of batch-local child 0
   int v;                      // chunks per parent (child = parent * v + chunk)
@@ -293,14 +299,15 @@ struct ListArgs {
   int64_t* nnz_out;           // symbolic: [global child] nnz
   const int64_t* off_in;      // numeric: [global child] output offset
   int32_t* c_col;
-  double* c_val;
+  void* c_val;
   int* status;
+  bool f32;
 };
 // Chunks narrower than the dense width: shared-memory bitmap + rank accumulator.
 void launch_leaf_bitmap(const ListArgs& a, int cap_vals, bool symbolic, cudaStream_t s);
 // Light chunks of a wide level: shared-memory hash accumulator (cap slots).
 void launch_leaf_hash(const ListArgs& a, int cap, bool symbolic, cudaStream_t s);
-int leaf_bitmap_smem(int64_t width, int cap_vals, bool symbolic);
+int leaf_bitmap_smem(int64_t width, int cap_vals, bool symbolic, int vb = 8);  // vb: bytes a value
 // Chunks with at most max_elems (<= 4096) elements, held in registers; no
 // floating-point atomics.
 void launch_leaf_small(const ListArgs& a, int max_elems, bool symbolic, cudaStream_t s);
@@ -309,12 +316,12 @@ void launch_leaf_warp(const ListArgs& a, cudaStream_t s);
 // Numeric chunks of at most max_elems (<= 4096) elements: one warp per chunk with
 // its own bitmap, rank prefix and value array in shared memory.
 void launch_leaf_warpbm(const ListArgs& a, int max_elems, cudaStream_t s);
-bool leaf_warpbm_fits(int64_t width, int max_elems, int64_t smem_max);
+bool leaf_warpbm_fits(int64_t width, int max_elems, int64_t smem_max, int vb = 8);
 // The same with 4 warps per chunk: chunks of at most max_elems elements (INT_MAX:
 // any) and max_nnz output columns (the value array of the block).
 void launch_leaf_blkbm(const ListArgs& a, int max_nnz, int max_elems, cudaStream_t s);
-bool leaf_blkbm_fits(int64_t width, int max_elems, int64_t smem_max);
-int leaf_small_smem(int64_t width, int cap, bool symbolic);
+bool leaf_blkbm_fits(int64_t width, int max_elems, int64_t smem_max, int vb = 8);
+int leaf_small_smem(int64_t width, int cap, bool symbolic, int vb = 8);
 
 // ---- whole-row bitmaps (gm_rowbitmap.cu) -----------------------------------------
 struct RowBitmapArgs {
@@ -322,10 +329,10 @@ struct RowBitmapArgs {
   int64_t n_items;
   const int64_t* a_rp;
   const int32_t* a_col;
-  const double* a_val;
+  const void* a_val;          // values are float or double (f32)
   const int64_t* b_rp;
   const int32_t* b_col;
-  const double* b_val;
+  const void* b_val;
   int64_t c_m;                // columns of C
   int v;                      // symbolic: chunks per row (1 with width >= C.m: whole row)
   int64_t width;              // symbolic: chunk width
@@ -333,10 +340,11 @@ struct RowBitmapArgs {
   int64_t item_base;
   int64_t* c_rp;              // whole-row symbolic: counts out; numeric: row offsets in
   int32_t* c_col;
-  double* c_val;
+  void* c_val;
   unsigned int* work_counter; // device counter for dynamic row scheduling
   int* status;
   uint32_t* bits_out;         // symbolic: each row's bitmap, rowbm_words(c_m) words a row (null: not kept)
+  bool f32;
 };
 int64_t rowbm_symbolic_smem(int64_t c_m);
 // Words of a whole-row bitmap of C.m columns (whole 16-byte pieces).
@@ -365,18 +373,19 @@ struct WalkArgs {
   const uint32_t* bits;       // nh whole-row bitmaps from the symbolic pass
   const int64_t* a_rp;
   const int32_t* a_col;
-  const double* a_val;
+  const void* a_val;          // values are float or double (f32)
   const int64_t* b_rp;
   const int32_t* b_col;
-  const double* b_val;
+  const void* b_val;
   const int32_t* bcp;         // per-B-row chunk starts, B.n_rows * (v + 1)
   const int64_t* off;         // output offset of chunk c of heavy row h at [h * v + c]
   const int64_t* items;       // item ids j of one class
   int64_t n_items;
   unsigned int* counter;      // dynamic item scheduling
   int32_t* c_col;
-  double* c_val;
+  void* c_val;
   int* status;
+  bool f32;
 };
 // Classes 1-3: one warp per item of at most 256 / 1024 / 2048 columns; 4-5: one
 // block per item, atomic adds.
@@ -401,6 +410,6 @@ constexpr int kLightWarpBins = 4;   // bins 1..4 use a warp per row
 int64_t light_bin_ub(int b);        // b in [1, 10]
 // Table slots for bin b; the top bin holds 2 * tau slots, fewer when they would
 // not leave 1 KB of the block's shared memory (smem_max bytes) for static arrays.
-int light_bin_cap(int b, int64_t tau, int64_t smem_max);
+int light_bin_cap(int b, int64_t tau, int64_t smem_max, int vb = 8);
 
 }  // namespace gm

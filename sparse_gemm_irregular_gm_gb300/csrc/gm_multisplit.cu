@@ -48,7 +48,7 @@ struct Layout {
   int* loff;
   int* row_end;
   int32_t* col_buf;
-  double* val_buf;
+  void* val_buf;              // E values (8 bytes a slot: room for float or double)
 };
 
 __device__ __forceinline__ Layout carve(unsigned char* smem, int nk, int ngr, int E, bool with_buf) {
@@ -60,7 +60,7 @@ __device__ __forceinline__ Layout carve(unsigned char* smem, int nk, int ngr, in
   unsigned char* p = reinterpret_cast<unsigned char*>(L.row_end + ngr);
   p = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 15) & ~uintptr_t(15));
   L.col_buf = with_buf ? reinterpret_cast<int32_t*>(p) : nullptr;
-  L.val_buf = with_buf ? reinterpret_cast<double*>(p + ((static_cast<size_t>(E) * 4 + 15) & ~size_t(15))) : nullptr;
+  L.val_buf = with_buf ? static_cast<void*>(p + ((static_cast<size_t>(E) * 4 + 15) & ~size_t(15))) : nullptr;
   return L;
 }
 
@@ -75,8 +75,10 @@ __device__ __forceinline__ void setup_rows(const SplitArgs& a, const Layout& L, 
   }
 }
 
-template <bool VAL, int ITEMS, bool SPLIT>
+template <typename V, bool VAL, int ITEMS, bool SPLIT>
 __global__ void __launch_bounds__(kMsThreads, 3) k_split(SplitArgs a) {
+  const V* __restrict__ in_val = static_cast<const V*>(a.in_val);
+  V* __restrict__ out_val = static_cast<V*>(a.out_val);
   extern __shared__ __align__(16) unsigned char smem[];
   const int T = blockDim.x;
   const int E = T * ITEMS;
@@ -162,12 +164,13 @@ __global__ void __launch_bounds__(kMsThreads, 3) k_split(SplitArgs a) {
     if (key[k] >= 0) L.col_buf[pos[k]] = col[k];
   }
   if (VAL) {
-    double v[ITEMS];
+    V v[ITEMS];
+    V* const vbuf = static_cast<V*>(L.val_buf);
 #pragma unroll
-    for (int k = 0; k < ITEMS; ++k) v[k] = key[k] >= 0 ? a.in_val[a.base + S + k * T + threadIdx.x] : 0.0;
+    for (int k = 0; k < ITEMS; ++k) v[k] = key[k] >= 0 ? in_val[a.base + S + k * T + threadIdx.x] : V(0);
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k)
-      if (key[k] >= 0) L.val_buf[pos[k]] = v[k];
+      if (key[k] >= 0) vbuf[pos[k]] = v[k];
   }
   __syncthreads();
 
@@ -180,7 +183,7 @@ __global__ void __launch_bounds__(kMsThreads, 3) k_split(SplitArgs a) {
     const int kk = j * a.v + (static_cast<uint32_t>(c) >> a.shift);
     const int64_t dest = L.gpos[kk] + (i - L.loff[kk]);
     a.out_col[dest] = c & mask;
-    if (VAL) a.out_val[dest] = L.val_buf[i];
+    if (VAL) out_val[dest] = static_cast<const V*>(L.val_buf)[i];
   }
 }
 
@@ -191,11 +194,11 @@ size_t split_smem_bytes(int v, int ngr, int E, bool with_buf, bool with_val) {
   return b;
 }
 
-template <bool VAL, int ITEMS, bool SPLIT>
+template <typename V, bool VAL, int ITEMS, bool SPLIT>
 void launch_split_t(const SplitArgs& a, cudaStream_t s) {
   const int E = kMsThreads * ITEMS;
   const size_t smem = split_smem_bytes(a.v, a.n_group_rows, E, SPLIT, VAL);
-  auto fn = k_split<VAL, ITEMS, SPLIT>;
+  auto fn = k_split<V, VAL, ITEMS, SPLIT>;
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   const int64_t n_wg = (a.total + E - 1) / E;
   (fn<<<static_cast<unsigned>(n_wg), kMsThreads, smem, s>>>(a), note_launch());
@@ -206,9 +209,21 @@ void launch_split(const SplitArgs& a, cudaStream_t s) {
   if (a.total <= 0) return;
   const bool val = a.in_val != nullptr && SPLIT;
   switch (a.E / kMsThreads) {
-    case 8: val ? launch_split_t<true, 8, SPLIT>(a, s) : launch_split_t<false, 8, SPLIT>(a, s); break;
-    case 4: val ? launch_split_t<true, 4, SPLIT>(a, s) : launch_split_t<false, 4, SPLIT>(a, s); break;
-    default: val ? launch_split_t<true, 1, SPLIT>(a, s) : launch_split_t<false, 1, SPLIT>(a, s); break;
+    case 8:
+      if (!val) launch_split_t<double, false, 8, SPLIT>(a, s);
+      else if (a.f32) launch_split_t<float, true, 8, SPLIT>(a, s);
+      else launch_split_t<double, true, 8, SPLIT>(a, s);
+      break;
+    case 4:
+      if (!val) launch_split_t<double, false, 4, SPLIT>(a, s);
+      else if (a.f32) launch_split_t<float, true, 4, SPLIT>(a, s);
+      else launch_split_t<double, true, 4, SPLIT>(a, s);
+      break;
+    default:
+      if (!val) launch_split_t<double, false, 1, SPLIT>(a, s);
+      else if (a.f32) launch_split_t<float, true, 1, SPLIT>(a, s);
+      else launch_split_t<double, true, 1, SPLIT>(a, s);
+      break;
   }
 }
 
@@ -248,10 +263,11 @@ namespace {
 constexpr int kExThreads = 512;
 constexpr int kExItems = kExpandE / kExThreads;  // 8
 
+template <typename V>
 __global__ void k_gather_entries(const int32_t* __restrict__ rows, int64_t nb, const int64_t* __restrict__ anz,
                                  const int64_t* __restrict__ a_rp, const int32_t* __restrict__ a_col,
-                                 const double* __restrict__ a_val, const int64_t* __restrict__ b_rp,
-                                 int64_t* __restrict__ e_b, double* __restrict__ e_a, int32_t* __restrict__ e_row,
+                                 const V* __restrict__ a_val, const int64_t* __restrict__ b_rp,
+                                 int64_t* __restrict__ e_b, V* __restrict__ e_a, int32_t* __restrict__ e_row,
                                  int64_t* __restrict__ e_len, int32_t* __restrict__ e_k) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -329,17 +345,21 @@ constexpr uint32_t kNoKey = 0xFFFFFFFFu;
 // memory so that each chunk's run is written contiguously. A product is carried
 // as one word: its key (local row * v + chunk) in the high 16 bits and its
 // column inside the chunk in the low 16 bits.
-template <bool VAL>
+template <typename V, bool VAL>
 __global__ void __launch_bounds__(kExThreads, 3) k_expand_split(ExpandArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int T = kExThreads;
   const int nk = a.n_group_rows * a.v;
   const Layout L = carve(smem, nk, a.n_group_rows, kExpandE, true);
   uint32_t* const pk_buf = reinterpret_cast<uint32_t*>(L.col_buf);
-  // entry table after the multisplit layout
-  unsigned char* tail = reinterpret_cast<unsigned char*>(L.val_buf + kExpandE);
+  V* const vbuf = static_cast<V*>(L.val_buf);
+  const V* __restrict__ e_a = static_cast<const V*>(a.e_a);
+  const V* __restrict__ b_val = static_cast<const V*>(a.b_val);
+  V* __restrict__ out_val = static_cast<V*>(a.out_val);
+  // entry table after the multisplit layout (whose value buffer has 8 bytes a slot)
+  unsigned char* tail = static_cast<unsigned char*>(L.val_buf) + static_cast<size_t>(kExpandE) * 8;
   int64_t* s_b = reinterpret_cast<int64_t*>(tail);                    // kExpandCap + 2
-  double* s_a = reinterpret_cast<double*>(s_b + kExpandCap + 2);      // kExpandCap + 2
+  V* s_a = reinterpret_cast<V*>(s_b + kExpandCap + 2);                // kExpandCap + 2
   int* s_lo = reinterpret_cast<int*>(s_a + kExpandCap + 2);           // kExpandCap + 2
   __shared__ int s_total;
 
@@ -363,7 +383,7 @@ __global__ void __launch_bounds__(kExThreads, 3) k_expand_split(ExpandArgs a) {
     const int lo_loc = static_cast<int>(min(lo, end) - S);
     s_lo[i] = lo_loc;
     s_b[i] = a.e_b[j] + (lo - off) - lo_loc;  // B index of local position p: s_b + p
-    s_a[i] = VAL ? a.e_a[j] : 0.0;
+    s_a[i] = VAL ? e_a[j] : V(0);
   }
   int* const s_ent = reinterpret_cast<int*>(L.col_buf);  // entry of each position (until the permute)
   for (int q = threadIdx.x; q < kExpandE; q += T) s_ent[q] = -1;
@@ -408,13 +428,13 @@ __global__ void __launch_bounds__(kExThreads, 3) k_expand_split(ExpandArgs a) {
   __syncthreads();
   // all B loads of the thread in flight together
   int32_t col[kExItems];
-  double vv[kExItems];
+  V vv[kExItems];
 #pragma unroll
   for (int k = 0; k < kExItems; ++k) {
     const int p = k * T + threadIdx.x;
     const int64_t bi = s_b[max(s_ent[p], 0)] + p;
     col[k] = p < n ? a.b_col[bi] : 0;
-    if (VAL) vv[k] = p < n ? a.b_val[bi] : 0.0;
+    if (VAL) vv[k] = p < n ? b_val[bi] : V(0);
   }
   uint32_t pk[kExItems];
   bool bad = false;
@@ -475,7 +495,7 @@ __global__ void __launch_bounds__(kExThreads, 3) k_expand_split(ExpandArgs a) {
     if (key >= 0) {
       const int pos = b + (lane - leader);
       pk_buf[pos] = pk[k];
-      if (VAL) L.val_buf[pos] = vv[k];
+      if (VAL) vbuf[pos] = vv[k];
     }
   }
   __syncthreads();
@@ -485,7 +505,7 @@ __global__ void __launch_bounds__(kExThreads, 3) k_expand_split(ExpandArgs a) {
     const int kk = static_cast<int>(q >> 16);
     const int64_t dest = L.gpos[kk] + (i - L.loff[kk]);
     a.out_col[dest] = static_cast<int32_t>(q & 0xFFFFu);
-    if (VAL) a.out_val[dest] = L.val_buf[i];
+    if (VAL) out_val[dest] = vbuf[i];
   }
 }
 
@@ -503,11 +523,17 @@ bool expand_fits(int v, int64_t w, int64_t tau, size_t smem) {
 }
 
 void launch_gather_entries(const int32_t* heavy_rows, int64_t nb, const int64_t* anz_batch, const int64_t* a_rp,
-                           const int32_t* a_col, const double* a_val, const int64_t* b_rp, int64_t* e_b,
-                           double* e_a, int32_t* e_row, int64_t* e_len, cudaStream_t s, int32_t* e_k) {
+                           const int32_t* a_col, const void* a_val, bool f32, const int64_t* b_rp, int64_t* e_b,
+                           void* e_a, int32_t* e_row, int64_t* e_len, cudaStream_t s, int32_t* e_k) {
   if (nb <= 0) return;
-  (k_gather_entries<<<grid_for(nb * 32, 256), 256, 0, s>>>(heavy_rows, nb, anz_batch, a_rp, a_col, a_val, b_rp, e_b,
-                                                           e_a, e_row, e_len, e_k), note_launch());
+  const unsigned g = grid_for(nb * 32, 256);
+  if (f32)
+    (k_gather_entries<float><<<g, 256, 0, s>>>(heavy_rows, nb, anz_batch, a_rp, a_col, static_cast<const float*>(a_val),
+                                               b_rp, e_b, static_cast<float*>(e_a), e_row, e_len, e_k), note_launch());
+  else
+    (k_gather_entries<double><<<g, 256, 0, s>>>(heavy_rows, nb, anz_batch, a_rp, a_col,
+                                                static_cast<const double*>(a_val), b_rp, e_b,
+                                                static_cast<double*>(e_a), e_row, e_len, e_k), note_launch());
 }
 
 int64_t expand_num_wg(int64_t total, int64_t n_e) {
@@ -525,12 +551,16 @@ void launch_expand_bounds(const int64_t* e_off, const int32_t* e_row, int64_t n_
 void launch_expand_split(const ExpandArgs& a, cudaStream_t s) {
   if (a.n_wg <= 0) return;
   const size_t smem = expand_smem_bytes(a.v, a.n_group_rows);
-  if (a.out_val) {
-    cudaFuncSetAttribute(k_expand_split<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    (k_expand_split<true><<<static_cast<unsigned>(a.n_wg), kExThreads, smem, s>>>(a), note_launch());
+  const unsigned g = static_cast<unsigned>(a.n_wg);
+  if (a.out_val && a.f32) {
+    cudaFuncSetAttribute(k_expand_split<float, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    (k_expand_split<float, true><<<g, kExThreads, smem, s>>>(a), note_launch());
+  } else if (a.out_val) {
+    cudaFuncSetAttribute(k_expand_split<double, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    (k_expand_split<double, true><<<g, kExThreads, smem, s>>>(a), note_launch());
   } else {
-    cudaFuncSetAttribute(k_expand_split<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    (k_expand_split<false><<<static_cast<unsigned>(a.n_wg), kExThreads, smem, s>>>(a), note_launch());
+    cudaFuncSetAttribute(k_expand_split<double, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    (k_expand_split<double, false><<<g, kExThreads, smem, s>>>(a), note_launch());
   }
 }
 
@@ -553,8 +583,10 @@ constexpr int kRrWarps = 8;
 constexpr int kRrRows = 8;   // rows a unit may touch (a.U keeps it below this)
 constexpr int kRrU = 4;
 
-template <bool VAL>
+template <typename V, bool VAL>
 __global__ void __launch_bounds__(kRrWarps * 32, 5) k_expand_rows(RowRunArgs a) {
+  const V* __restrict__ e_a = static_cast<const V*>(a.e_a);
+  V* __restrict__ out_val = static_cast<V*>(a.out_val);
   __shared__ int s_cnt[kRrWarps][kRrRows][64];  // counts, then each warp's offset inside the reservation
   __shared__ int64_t s_rbase[kRrRows][64];       // reservation of each (row, chunk) of the unit
   __shared__ int64_t s_base[kRrWarps][64];
@@ -631,8 +663,8 @@ __global__ void __launch_bounds__(kRrWarps * 32, 5) k_expand_rows(RowRunArgs a) 
       const int q0 = static_cast<int>(max(W0, o0) - o0), q1 = static_cast<int>(min(W1, o1) - o0);
       const int32_t* const t = a.bcp + static_cast<int64_t>(a.e_k[e]) * vp1;
       const int32_t* const bc = a.b_col + a.e_b[e];
-      const double* const bvp = a.b_val + a.e_b[e];
-      const double av = VAL ? a.e_a[e] : 0.0;
+      const V* const bvp = static_cast<const V*>(a.b_val) + a.e_b[e];
+      const V av = VAL ? e_a[e] : V(0);
       __syncwarp();
       for (int c = lane; c < v; c += 32) {
         const int x0 = max(q0, t[c]), x1 = min(q1, t[c + 1]);
@@ -643,16 +675,16 @@ __global__ void __launch_bounds__(kRrWarps * 32, 5) k_expand_rows(RowRunArgs a) 
       }
       __syncwarp();
       uint32_t ncol[kRrU];
-      double nbv[kRrU];
+      V nbv[kRrU];
 #pragma unroll
       for (int u = 0; u < kRrU; ++u) {
         const int q = q0 + u * 32 + lane;
         ncol[u] = q < q1 ? static_cast<uint32_t>(bc[q]) : 0u;
-        nbv[u] = (VAL && q < q1) ? bvp[q] : 0.0;
+        nbv[u] = (VAL && q < q1) ? bvp[q] : V(0);
       }
       for (int qb = q0; qb < q1; qb += 32 * kRrU) {
         uint32_t col[kRrU];
-        double bv[kRrU];
+        V bv[kRrU];
 #pragma unroll
         for (int u = 0; u < kRrU; ++u) {
           col[u] = ncol[u];
@@ -663,7 +695,7 @@ __global__ void __launch_bounds__(kRrWarps * 32, 5) k_expand_rows(RowRunArgs a) 
           for (int u = 0; u < kRrU; ++u) {
             const int q = qb + 32 * kRrU + u * 32 + lane;
             ncol[u] = q < q1 ? static_cast<uint32_t>(bc[q]) : 0u;
-            nbv[u] = (VAL && q < q1) ? bvp[q] : 0.0;
+            nbv[u] = (VAL && q < q1) ? bvp[q] : V(0);
           }
         }
 #pragma unroll
@@ -674,7 +706,7 @@ __global__ void __launch_bounds__(kRrWarps * 32, 5) k_expand_rows(RowRunArgs a) 
             // written once, read once by the accumulators: streaming stores, so that
             // they do not push B and the cursors out of L2
             __stcs(a.out_col + dst, static_cast<int32_t>(col[u] & mask));
-            if (VAL) __stcs(a.out_val + dst, av * bv[u]);
+            if (VAL) __stcs(out_val + dst, av * bv[u]);
           }
         }
       }
@@ -708,8 +740,9 @@ void launch_row_runs(const RowRunArgs& a, int num_sms, cudaStream_t s) {
    note_launch());
   cudaMemsetAsync(a.unit_counter, 0, sizeof(unsigned), s);
   const unsigned blocks = static_cast<unsigned>(std::min<int64_t>(a.n_units, static_cast<int64_t>(num_sms) * 6));
-  if (a.out_val) (k_expand_rows<true><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
-  else (k_expand_rows<false><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
+  if (a.out_val && a.f32) (k_expand_rows<float, true><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
+  else if (a.out_val) (k_expand_rows<double, true><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
+  else (k_expand_rows<double, false><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
 }
 
 }  // namespace gm

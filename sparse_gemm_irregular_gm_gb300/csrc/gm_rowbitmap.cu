@@ -211,15 +211,19 @@ __device__ __forceinline__ int bitmap_rank(const uint32_t* bm, const int* gpre, 
 //  * numeric: prefix sums over groups of 8 words give every column its rank,
 //    the values are summed into their rank in shared memory (the entry table's
 //    space is reused) and the row is written in column order.
-template <bool SYM>
+template <typename V, bool SYM>
 __global__ void __launch_bounds__(kRbThreads, 1)
     k_rowbm_light(RowBitmapArgs a, int nwords, int wwords, int cap, int te_cap, int region_bytes) {
+  const V* __restrict__ a_val = static_cast<const V*>(a.a_val);
+  const V* __restrict__ b_val = static_cast<const V*>(a.b_val);
+  V* __restrict__ c_val = static_cast<V*>(a.c_val);
+
   extern __shared__ __align__(16) unsigned char smem[];
   int64_t* s_bs = reinterpret_cast<int64_t*>(smem);                       // te_cap
-  double* s_av = reinterpret_cast<double*>(s_bs + te_cap);                // te_cap (numeric)
+  V* s_av = reinterpret_cast<V*>(s_bs + te_cap);                // te_cap (numeric)
   int* s_pre = reinterpret_cast<int*>(SYM ? static_cast<void*>(s_bs + te_cap) : static_cast<void*>(s_av + te_cap));
   uint16_t* s_ent = reinterpret_cast<uint16_t*>(s_pre + te_cap);          // cap: entry of each product position
-  double* vals = reinterpret_cast<double*>(smem);                         // numeric, after the products are loaded
+  V* vals = reinterpret_cast<V*>(smem);                         // numeric, after the products are loaded
   const int ngroups = (nwords + kGroupWords - 1) / kGroupWords;           // symbolic: the whole row
   uint32_t* bm = reinterpret_cast<uint32_t*>(smem + region_bytes);        // symbolic ngroups * 8, numeric wwords
   int* gpre = reinterpret_cast<int*>(bm + wwords);                        // numeric: wwords / 8
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(kRbThreads, 1)
     const int64_t lo = a.a_rp[r], ne = a.a_rp[r + 1] - lo;
     if (SYM) zero_words(bm, ngroups * kGroupWords);
     uint32_t col[kRlItems];
-    double val[kRlItems];
+    V val[kRlItems];
 #pragma unroll
     for (int k = 0; k < kRlItems; ++k) {
       col[k] = kNoCol;
@@ -252,7 +256,7 @@ __global__ void __launch_bounds__(kRbThreads, 1)
         const int64_t bs = a.b_rp[kb];
         s_bs[i] = bs;
         s_pre[i] = static_cast<int>(a.b_rp[kb + 1] - bs);
-        if (!SYM) s_av[i] = a.a_val[p];
+        if (!SYM) s_av[i] = a_val[p];
       }
       __syncthreads();
       int tot;
@@ -289,7 +293,7 @@ __global__ void __launch_bounds__(kRbThreads, 1)
           ent[k] = lo_i;
           const int64_t bi = s_bs[lo_i] + (rel - s_pre[lo_i]);
           col[k] = static_cast<uint32_t>(a.b_col[bi]);
-          if (!SYM) val[k] = a.b_val[bi];
+          if (!SYM) val[k] = b_val[bi];
         }
       }
 #pragma unroll
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(kRbThreads, 1)
     // per window: bits, group ranks (conflict-free group counts), the products'
     // values added into their rank's slot, then the window's part of the row
     // written in column order.
-    double* const vals = reinterpret_cast<double*>(smem);                       // cap
+    V* const vals = reinterpret_cast<V*>(smem);                       // cap
     const int64_t out = a.c_rp[r];
     int done = 0;
     const int ngw = wwords / kGroupWords;
@@ -381,7 +385,7 @@ __global__ void __launch_bounds__(kRbThreads, 1)
             const int b = __ffs(bits) - 1;
             bits &= bits - 1;
             a.c_col[out + done + pos] = static_cast<int32_t>(base + (g * kGroupWords + x) * 32 + b);
-            a.c_val[out + done + pos] = vals[pos];
+            c_val[out + done + pos] = vals[pos];
             ++pos;
           }
         }
@@ -442,7 +446,7 @@ void launch_rowbm_light(const RowBitmapArgs& a, bool symbolic, int cap, int num_
   const int wwords = symbolic ? 0 : static_cast<int>(light_window_words(a.c_m, cap, smem_max));
   const size_t smem = static_cast<size_t>(rowbm_light_smem(a.c_m, cap, symbolic, smem_max));
   const int64_t blocks = std::min<int64_t>(a.n_items, num_sms);
-  auto fn = symbolic ? k_rowbm_light<true> : k_rowbm_light<false>;
+  auto fn = symbolic ? k_rowbm_light<double, true> : a.f32 ? k_rowbm_light<float, false> : k_rowbm_light<double, false>;
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   (fn<<<static_cast<unsigned>(blocks), kRbThreads, smem, s>>>(a, nwords, wwords, cap, te_cap,
                                                                static_cast<int>(region)), note_launch());

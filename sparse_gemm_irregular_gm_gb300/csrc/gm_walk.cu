@@ -64,7 +64,7 @@ __device__ __forceinline__ void add_range(const WalkArgs& a, int64_t s, int64_t 
     for (int u = 0; u < 4; ++u) {
       const int64_t q = q0 + u * 32 + lane;
       cc[u] = q < e ? (static_cast<uint32_t>(a.b_col[q]) & mask) : kNone;
-      bv[u] = q < e ? a.b_val[q] : 0.0;
+      bv[u] = q < e ? static_cast<const double*>(a.b_val)[q] : 0.0;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -110,7 +110,7 @@ __device__ __forceinline__ void range_of(const WalkArgs& a, int64_t p, int64_t h
   av = 0.0;
   if (p < hi) {
     const int k = a.a_col[p];
-    av = a.a_val[p];
+    av = static_cast<const double*>(a.a_val)[p];
     const int32_t* t = a.bcp + static_cast<int64_t>(k) * (a.v + 1) + c;
     const int32_t t0 = t[0];
     s = a.b_rp[k] + t0;
@@ -178,7 +178,7 @@ __device__ __forceinline__ void walk_row(const WalkArgs& a, int64_t row, int c, 
         const bool ok = g < total;
         const int64_t q = sj + (g - ej);
         cc[u] = ok ? (static_cast<uint32_t>(a.b_col[q]) & mask) : kNone;
-        bv[u] = ok ? a.b_val[q] : 0.0;
+        bv[u] = ok ? static_cast<const double*>(a.b_val)[q] : 0.0;
       }
 #pragma unroll
       for (int u = 0; u < kSteps; ++u) {
@@ -209,7 +209,7 @@ __device__ __forceinline__ void write_chunk(const WalkArgs& a, int64_t out, int 
       const int b = __ffs(bits) - 1;
       bits &= bits - 1;
       a.c_col[out + pos] = cbase + w * 32 + b;
-      a.c_val[out + pos] = vals[pos];
+      static_cast<double*>(a.c_val)[out + pos] = vals[pos];
       ++pos;
     }
   }

@@ -9,9 +9,12 @@ from sparse_gemm_irregular_gm_gb300 import binding
 REL_TOL = 1e-12
 
 
-def run_gpu(A, B, return_info=False, **cfg):
+F32_EPS = 2.0 ** -24  # unit roundoff of float
+
+
+def run_gpu(A, B, return_info=False, dtype=None, **cfg):
     import torch
-    Ad, Bd = binding.to_device(A), binding.to_device(B)
+    Ad, Bd = binding.to_device(A, dtype=dtype), binding.to_device(B, dtype=dtype)
     C, info = binding.spgemm(Ad, Bd, binding.make_config(**cfg) if cfg else None, return_info=True)
     torch.cuda.synchronize()
     out = (C.row_ptr.cpu().numpy(), C.col.cpu().numpy(), C.val.cpu().numpy())
@@ -78,3 +81,38 @@ def check_invariants(C, u):
         assert int(c.min()) >= 0 and int(c.max()) < C.n_cols
     del start
     return n
+
+
+def _rounded_to_f32(M):
+    """M with its values rounded to float (and held as float64, for the oracle)."""
+    return M.__class__(M.n_rows, M.n_cols, M.row_ptr, M.col, M.val.astype(np.float32).astype(np.float64))
+
+
+def _ones(M):
+    return M.__class__(M.n_rows, M.n_cols, M.row_ptr, M.col, np.ones_like(M.val))
+
+
+def check_full_f32(A, B, exact=False, **cfg):
+    """C = A*B with float values (gm_config.value_type = GM_VALUE_F32). The inputs
+    are rounded to float first and the oracle sums the same float values in fp64.
+    Structure bit-exact; integer-valued inputs exactly; otherwise every entry
+    within 2 k u sum|a_ik b_kj|, u = 2^-24 and k = the entry's number of products
+    (the oracle's value on all-ones inputs): a float product is within u of the
+    exact one and a sum of k terms in any order within (k - 1) u of the exact sum,
+    relative to the sum of the magnitudes."""
+    A32, B32 = _rounded_to_f32(A), _rounded_to_f32(B)
+    (rp, col, val), info = run_gpu(A32, B32, return_info=True, dtype=np.float32, **cfg)
+    assert val.dtype == np.float32 and info.value_type == binding.GM_VALUE_F32
+    ref = oracle.spgemm(A32, B32)
+    np.testing.assert_array_equal(np.diff(rp), np.diff(ref.row_ptr), err_msg="row nnz differ")
+    np.testing.assert_array_equal(col, ref.col, err_msg="columns differ")
+    v = val.astype(np.float64)
+    if exact:
+        np.testing.assert_array_equal(v, ref.val, err_msg="integer-valued float results differ")
+    else:
+        k = oracle.spgemm(_ones(A), _ones(B)).val
+        bound = 2.0 * k * F32_EPS * ref.abs_scale
+        err = np.abs(v - ref.val)
+        bad = np.nonzero(err > bound)[0]
+        assert bad.size == 0, f"{bad.size} float values outside 2 k u sum|ab|"
+    return info

@@ -73,6 +73,45 @@ def test_params_match_oracle(lib, c_m, over):
     assert list(got.widths[:got.n_levels]) == ref.widths
 
 
+@pytest.mark.parametrize("c_m", [1, 1000, (1 << 14) + 1, 1 << 18, 1 << 20, (1 << 21) + 7, 10 ** 8])
+@pytest.mark.parametrize("over", [{}, {"tau": 64, "dense_width": 64, "n_chunks_max": 4}, {"smem_budget_bytes": 65536}])
+def test_params_float_values_match_oracle(lib, c_m, over):
+    """The planner with 4-byte values (gm_config.value_type = GM_VALUE_F32) is
+    GetMagnusParams with s_C.val = 4: at 227 KB tau = 232448 / (2 * 8) = 14528 and
+    the dense width floor_pow2(232448 / 5) = 32768, twice the double one."""
+    kw = {"s_lm": over["smem_budget_bytes"]} if "smem_budget_bytes" in over else {}
+    kw.update({k: over[k] for k in ("tau", "dense_width", "n_chunks_max") if k in over})
+    ref = oracle.magnus_params(c_m, s_val=4, **kw)
+    if ref.n_levels > binding.GM_MAX_LEVELS:
+        return
+    got = _lib_params(c_m, value_type=binding.GM_VALUE_F32, **over)
+    assert (got.tau, got.dense_width, got.n_chunks_max) == (ref.tau, ref.dense_width, ref.n_chunks_max)
+    assert got.n_chunks_required == ref.n_chunks_required and got.n_levels == ref.n_levels
+    assert list(got.v_chunks[:got.n_levels]) == ref.v_chunks
+    assert list(got.widths[:got.n_levels]) == ref.widths
+    if not over:
+        assert (got.tau, got.dense_width) == (14528, 32768)
+        dbl = _lib_params(c_m)
+        assert (dbl.tau, dbl.dense_width) == (9685, 16384)
+
+
+def test_params_float_rejects_what_the_oracle_rejects(lib):
+    """With 4-byte values and tau = 16, Eq. (6) leaves no room for a histogram
+    (n_chunksMax < 1): the oracle raises and the library returns an error."""
+    with pytest.raises(ValueError):
+        oracle.magnus_params(1024, s_val=4, tau=16)
+    with pytest.raises(binding.GmError) as e:
+        _lib_params(1024, tau=16, value_type=binding.GM_VALUE_F32)
+    assert e.value.status == 1
+    assert _lib_params(1024, tau=32, value_type=binding.GM_VALUE_F32).n_levels == 0
+
+
+def test_params_rejects_unknown_value_type(lib):
+    with pytest.raises(binding.GmError) as e:
+        _lib_params(1 << 20, value_type=7)
+    assert e.value.status == 1
+
+
 def test_params_tables_v_vi(lib):
     with open(os.path.join(ROOT, "tests", "golden", "magnus_chunk_tables.json")) as f:
         g = json.load(f)

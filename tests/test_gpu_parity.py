@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 from sparse_gemm_irregular_gm_gb300 import binding, inputs as gi
-from tests.gpu_common import assert_matches, check_full, check_invariants, gather_rows, run_gpu
+from tests.gpu_common import assert_matches, check_full, check_full_f32, check_invariants, gather_rows, run_gpu
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -413,6 +413,53 @@ def test_rmat_grid_pairs(a_density):
     u = oracle.ip_counts(A, B)
     info = check_full(A, B)
     assert info.ip_total == int(u.sum()) and info.n_heavy_rows == int((u > info.params.tau).sum())
+
+
+# --- float values (gm_config.value_type = GM_VALUE_F32) -----------------------------
+
+# heavy_L0 takes tau = 32: with 4-byte values Eq. (6) gives no multisplit chunk
+# count at tau = 16 (n_chunksMax < 1), and the planner rejects it as the oracle does
+F32_FORCED = [("heavy_L0", {"tau": 32}) if f[0] == "heavy_L0" else f for f in FORCED
+              if f[0] in ("auto", "heavy_L0", "heavy_L1", "heavy_L2", "heavy_L3", "unfused", "batched",
+                          "L1_wide_chunks", "L1_outer", "L1_rowwise")]
+
+
+@pytest.mark.parametrize("name,cfg", F32_FORCED, ids=[f[0] for f in F32_FORCED])
+@pytest.mark.parametrize("values", ["uniform", "int"])
+def test_f32_forced_paths(name, cfg, values):
+    """Every pipeline and hierarchy depth with float values."""
+    A = gi.rmat(10, 8, seed=1, values=values)
+    info = check_full_f32(A, A, exact=values == "int", **cfg)
+    if name != "auto":
+        assert info.n_heavy_rows > 0
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_f32_random_irregular(seed):
+    """Unsorted rows with repeated columns and explicit zeros (the row-order
+    pipeline then splits each tile in shared memory), float values."""
+    A = gi.random_csr(64, 90, 0.3, seed, values="int", unsorted=True, duplicates=True, explicit_zeros=True,
+                      empty_rows=0.2)
+    B = gi.random_csr(90, 70, 0.3, seed + 50, values="int", unsorted=True, duplicates=True, explicit_zeros=True,
+                      empty_rows=0.2)
+    check_full_f32(A, B, exact=True, tau=2, dense_width=4, n_chunks_max=2)
+
+
+@pytest.mark.parametrize("scale", [14, 16])
+def test_f32_planner_defaults_on_rmat(scale):
+    """Default float plan: tau = 14528 and chunks of 32768 columns (Sec. III-D with
+    s_C.val = 4); scale 14 needs no multisplit level, scale 16 has two chunks."""
+    A = gi.rmat(scale, 16, seed=scale)
+    u = oracle.ip_counts(A, A)
+    info = check_full_f32(A, A)
+    assert info.params.tau == 14528 and info.params.dense_width == 32768
+    assert info.n_heavy_rows == int((u > 14528).sum()) > 0
+    assert info.params.n_levels == (0 if scale == 14 else 1)
+
+
+def test_f32_light_rows_laplacian():
+    A = gi.laplacian_2d(64)
+    check_full_f32(A, A, exact=True)
 
 
 # --- the workloads ------------------------------------------------------------------
