@@ -45,6 +45,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--pipeline", type=int, default=0)
+    ap.add_argument("--dtype", choices=["f64", "f32"], default="f64", help="value type of A, B and C")
     ap.add_argument("--n-chunks-max", type=int, default=0, help="plan override: chunks per multisplit level")
     ap.add_argument("--dense-width", type=int, default=0, help="plan override: dense accumulator width")
     ap.add_argument("--grid", action="store_true",
@@ -138,7 +139,7 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power)}
 
 
-def byte_model(info, A, nnz_c, rowwise):
+def byte_model(info, A, nnz_c, rowwise, vb=8):
     """Algorithmic bytes per step.
 
     Whole path, outer-product pipelines (the method's byte model, one multisplit
@@ -150,28 +151,30 @@ def byte_model(info, A, nnz_c, rowwise):
     B columns it walks (4) and the numeric pass reads the chunks once (12).
     Per stage: the bytes that stage must move in this implementation (symbolic
     passes carry columns only, numeric passes columns and values; the level-0
-    histogram is counted inside the outer product).
+    histogram is counted inside the outer product). Element sizes are for vb-byte
+    values (12 B for a column and a double, 8 B with floats).
     """
+    e = 4 + vb
     ip_h = info.ip_heavy
     L = max(1, info.params.n_levels)
-    a_bytes = 8 * (A.n_rows + 1) + 12 * A.nnz
-    c_bytes = 8 * (A.n_rows + 1) + 12 * nnz_c
+    a_bytes = 8 * (A.n_rows + 1) + e * A.nnz
+    c_bytes = 8 * (A.n_rows + 1) + e * nnz_c
     if rowwise:
-        b_alg = 2 * a_bytes + ip_h * (12 + 4 + 12) + c_bytes
+        b_alg = 2 * a_bytes + ip_h * (e + 4 + e) + c_bytes
         stages = {
-            "multisplit": ip_h * 12,    # products written once, into their level-0 chunks
+            "multisplit": ip_h * e,     # products written once, into their level-0 chunks
             "sym_heavy": ip_h * 4,      # B columns walked
-            "num_heavy": ip_h * 12,     # chunk columns and values read (+ C writes, added by the caller)
+            "num_heavy": ip_h * e,      # chunk columns and values read (+ C writes, added by the caller)
         }
         return b_alg, stages
-    b_alg = 2 * a_bytes + ip_h * (12 + L * (4 + 12 + 12) + 4 + 12) + c_bytes
+    b_alg = 2 * a_bytes + ip_h * (e + L * (4 + e + e) + 4 + e) + c_bytes
     stages = {
         "outer_sym": ip_h * 4,          # C-hat columns written (symbolic pass)
-        "outer": ip_h * 12,             # C-hat columns and values written (numeric pass)
+        "outer": ip_h * e,              # C-hat columns and values written (numeric pass)
         "multisplit_sym": ip_h * 8,     # columns read and written
-        "multisplit": ip_h * 24,        # columns and values read and written
+        "multisplit": ip_h * 2 * e,     # columns and values read and written
         "sym_heavy": ip_h * 4,          # chunk columns read
-        "num_heavy": ip_h * 12,         # chunk columns and values read (+ C writes, added by the caller)
+        "num_heavy": ip_h * e,          # chunk columns and values read (+ C writes, added by the caller)
     }
     return b_alg, stages
 
@@ -265,6 +268,13 @@ def plan_overrides(args) -> dict:
     return {k: v for k, v in (("n_chunks_max", args.n_chunks_max), ("dense_width", args.dense_width)) if v}
 
 
+def workload_name(args) -> str:
+    vals = "fp32 U[-1,1)" if args.dtype == "f32" else "fp64 U[-1,1)"
+    if args.workload == "rmat20":
+        return f"A*A, A = R-MAT scale 20, edge factor 16, a=.57 b=.19 c=.19, {vals}, seed 1"
+    return args.workload if args.dtype == "f64" else f"{args.workload} ({vals})"
+
+
 def make_step(A, Ad, Bd, cfg, stream):
     """One full SpGEMM through the C ABI: analyze, symbolic, allocation of C, numeric."""
     import torch
@@ -276,7 +286,7 @@ def make_step(A, Ad, Bd, cfg, stream):
         c_rp = torch.empty(A.n_rows + 1, dtype=torch.int64, device="cuda")
         nnz = binding.gm_spgemm_symbolic(plan, c_rp)
         c_col = torch.empty(nnz, dtype=torch.int32, device="cuda")
-        c_val = torch.empty(nnz, dtype=torch.float64, device="cuda")
+        c_val = torch.empty(nnz, dtype=Ad.val.dtype, device="cuda")
         binding.gm_spgemm_numeric(plan, c_col, c_val)
         info = binding.gm_spgemm_plan_info(plan)
         binding.gm_spgemm_plan_destroy(plan)
@@ -293,9 +303,13 @@ def run_ours(args):
     rank, world, local = dist_setup(args)
     __graft_entry__.build()
     A, B = inputs.named_pair(args.workload, seed=args.seed)
-    Ad = binding.to_device(A)
-    Bd = Ad if B is A else binding.to_device(B)
+    vdt = np.float32 if args.dtype == "f32" else None
+    vb = 4 if args.dtype == "f32" else 8
+    Ad = binding.to_device(A, dtype=vdt)
+    Bd = Ad if B is A else binding.to_device(B, dtype=vdt)
     cfg = binding.make_config(flags=binding.GM_FLAG_TIMING, pipeline=args.pipeline, **plan_overrides(args))
+    if args.dtype == "f32":
+        cfg.value_type = binding.GM_VALUE_F32
     stream = torch.cuda.current_stream()
     step = make_step(A, Ad, Bd, cfg, stream)
 
@@ -337,9 +351,9 @@ def run_ours(args):
     flops = 2.0 * info.ip_total
     value = world * flops / (ms / 1e3) / 1e9
     peak, peak_kind = peaks()
-    b_alg, stage_bytes = byte_model(info, A, nnz_c, info.pipeline == binding.GM_PIPE_ROWWISE)
-    b_method, _ = byte_model(info, A, nnz_c, False)
-    stage_bytes["num_heavy"] += 12 * nnz_heavy + 8 * len(heavy)
+    b_alg, stage_bytes = byte_model(info, A, nnz_c, info.pipeline == binding.GM_PIPE_ROWWISE, vb)
+    b_method, _ = byte_model(info, A, nnz_c, False, vb)
+    stage_bytes["num_heavy"] += (4 + vb) * nnz_heavy + 8 * len(heavy)
     names = binding.STAGES
     stage_table = {names[i]: round(float(stage_ms[i]), 3) for i in range(len(names)) if stage_ms[i] > 0}
     dom = max(stage_bytes, key=lambda k: stage_ms[names.index(k)])
@@ -348,20 +362,19 @@ def run_ours(args):
     result = {
         "metric": METRIC, "value": round(value, 3), "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "A*A, A = R-MAT scale 20, edge factor 16, a=.57 b=.19 c=.19, fp64 U[-1,1), seed 1"
-                   if args.workload == "rmat20" else args.workload,
+        "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
+        "config": {"workload": workload_name(args),
                    "n": A.n_rows, "nnz_A": A.nnz, "intermediate_products": info.ip_total,
                    "heavy_products": info.ip_heavy, "nnz_C": nnz_c, "heavy_rows": info.n_heavy_rows,
                    "levels": info.params.n_levels, "chunks": list(info.params.v_chunks[:info.params.n_levels]),
                    "batches": info.n_batches, "pipeline": binding.PIPELINES[info.pipeline],
                    "plan_overrides": plan_overrides(args) or None,
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs and outputs larger than L2 (C alone is %.0f GB)" % (12 * nnz_c / 1e9)},
+                   "l2": "inputs and outputs larger than L2 (C alone is %.0f GB)" % ((4 + vb) * nnz_c / 1e9)},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": captured_traffic(args.workload, dom) if args.pipeline == 0 and
-                     not plan_overrides(args) else None,
+                     not plan_overrides(args) and args.dtype == "f64" else None,
                      "traffic_note": "DRAM read + write bytes of the stage's kernels in one step (ncu, "
                                      "profiles/traffic_rmat20_ef16_AxA.json); null once they change",
                      "peak_kind": peak_kind, "alg_bytes_per_step": int(stage_bytes[dom])},
@@ -461,22 +474,24 @@ def run_grid(args):
 
 def run_e2e(args, A, cfg, stream, nnz_c, ip_total):
     """Same metric with host buffers: copy A in from pinned memory, run, copy C out."""
+    import numpy as np
     import torch
 
     from sparse_gemm_irregular_gm_gb300 import binding
-    h2d = (A.n_rows + 1) * 8 + A.nnz * 12
-    d2h = (A.n_rows + 1) * 8 + nnz_c * 12
+    vb = 4 if args.dtype == "f32" else 8
+    h2d = (A.n_rows + 1) * 8 + A.nnz * (4 + vb)
+    d2h = (A.n_rows + 1) * 8 + nnz_c * (4 + vb)
     avail = host_available_bytes()
     if avail is not None and d2h + h2d > 0.85 * avail:
         return {"value": None, "unit": "GFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "skipped": f"C needs {d2h / 1e9:.0f} GB of pinned host memory, {avail / 1e9:.0f} GB available"}
     h_rp = torch.from_numpy(A.row_ptr).pin_memory()
     h_col = torch.from_numpy(A.col).pin_memory()
-    h_val = torch.from_numpy(A.val).pin_memory()
+    h_val = torch.from_numpy(A.val.astype(np.float32) if vb == 4 else A.val).pin_memory()
     t0 = time.perf_counter()
     o_rp = torch.empty(A.n_rows + 1, dtype=torch.int64, pin_memory=True)
     o_col = torch.empty(nnz_c, dtype=torch.int32, pin_memory=True)
-    o_val = torch.empty(nnz_c, dtype=torch.float64, pin_memory=True)
+    o_val = torch.empty(nnz_c, dtype=h_val.dtype, pin_memory=True)
     log(f"e2e: pinned {d2h / 1e9:.1f} GB of host memory in {time.perf_counter() - t0:.1f} s")
 
     torch.cuda.empty_cache()  # let this leg's own allocation sizes form the cache

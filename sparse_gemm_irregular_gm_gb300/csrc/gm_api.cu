@@ -1155,7 +1155,9 @@ static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, void* c_val) 
     const int64_t cnt = p->bin_start[b + 1] - p->bin_start[b];
     if (cnt <= 0) continue;
     const int cap = b <= 9 ? static_cast<int>(light_bin_ub(b)) : static_cast<int>(p->P.tau);
-    if (b >= 7 && rowbm_light_fits(p->c_m, cap, !numeric, p->smem_dev)) {
+    // the same kernel family for both passes of a bin (symbolic rows hold no values)
+    if (b >= 7 && rowbm_light_fits(p->c_m, cap, false, p->smem_dev, p->vb) &&
+        rowbm_light_fits(p->c_m, cap, true, p->smem_dev, p->vb)) {
       RowBitmapArgs ra{};
       ra.f32 = p->f32;
       ra.rows = p->rows_by_bin.p + p->bin_start[b];

@@ -355,7 +355,7 @@ void launch_rowbm(const RowBitmapArgs& a, int num_sms, int64_t smem_max, cudaStr
 // Numeric: columns in windows of a bitmap that fits beside the placed values and
 // counters; int32 count-and-place by rank, no floating-point atomics.
 int64_t rowbm_light_smem(int64_t c_m, int cap, bool symbolic, int64_t smem_max);
-bool rowbm_light_fits(int64_t c_m, int cap, bool symbolic, int64_t smem_max);
+bool rowbm_light_fits(int64_t c_m, int cap, bool symbolic, int64_t smem_max, int vb = 8);
 void launch_rowbm_light(const RowBitmapArgs& a, bool symbolic, int cap, int num_sms, int64_t smem_max, cudaStream_t s);
 
 // bcp only (see heavy_chunk_counts), v <= 256.

@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(kRbThreads) k_rowbm_symbolic(RowBitmapArgs a, 
 
 constexpr int kGroupWords = 8;  // rank prefix kept per 8 bitmap words (256 columns)
 constexpr int kRlItems = 10;    // products per thread in k_rowbm_light: rows of up to 10240 products
+constexpr int kRlItemsWide = 16; // ... for the symbolic pass and float values: up to 16384 products
 constexpr uint32_t kNoCol = 0xFFFFFFFFu;
 constexpr int64_t kLightSymRegion = 65536;  // entry-table bytes of the symbolic light kernel
 
@@ -211,7 +212,7 @@ __device__ __forceinline__ int bitmap_rank(const uint32_t* bm, const int* gpre, 
 //  * numeric: prefix sums over groups of 8 words give every column its rank,
 //    the values are summed into their rank in shared memory (the entry table's
 //    space is reused) and the row is written in column order.
-template <typename V, bool SYM>
+template <typename V, bool SYM, int kRlItems>
 __global__ void __launch_bounds__(kRbThreads, 1)
     k_rowbm_light(RowBitmapArgs a, int nwords, int wwords, int cap, int te_cap, int region_bytes) {
   const V* __restrict__ a_val = static_cast<const V*>(a.a_val);
@@ -429,8 +430,9 @@ int64_t rowbm_light_smem(int64_t c_m, int cap, bool symbolic, int64_t smem_max) 
   return light_region_bytes(cap, false) + w * 4 + (w / kGroupWords) * 4;
 }
 
-bool rowbm_light_fits(int64_t c_m, int cap, bool symbolic, int64_t smem_max) {
-  if (cap < 1 || cap > kRbThreads * kRlItems || c_m > (int64_t(1) << 31)) return false;
+bool rowbm_light_fits(int64_t c_m, int cap, bool symbolic, int64_t smem_max, int vb) {
+  const int items = (symbolic || vb == 4) ? kRlItemsWide : kRlItems;
+  if (cap < 1 || cap > kRbThreads * items || c_m > (int64_t(1) << 31)) return false;
   const int64_t te = (light_region_bytes(cap, symbolic) - 2 * static_cast<int64_t>(cap) - 16) / (symbolic ? 12 : 20);
   if (te < 64) return false;
   if (!symbolic && light_window_words(c_m, cap, smem_max) < kGroupWords) return false;
@@ -446,7 +448,10 @@ void launch_rowbm_light(const RowBitmapArgs& a, bool symbolic, int cap, int num_
   const int wwords = symbolic ? 0 : static_cast<int>(light_window_words(a.c_m, cap, smem_max));
   const size_t smem = static_cast<size_t>(rowbm_light_smem(a.c_m, cap, symbolic, smem_max));
   const int64_t blocks = std::min<int64_t>(a.n_items, num_sms);
-  auto fn = symbolic ? k_rowbm_light<double, true> : a.f32 ? k_rowbm_light<float, false> : k_rowbm_light<double, false>;
+  const bool wide = cap > kRbThreads * kRlItems;  // only symbolic passes and float values get here
+  auto fn = symbolic ? (wide ? k_rowbm_light<double, true, kRlItemsWide> : k_rowbm_light<double, true, kRlItems>)
+            : a.f32  ? (wide ? k_rowbm_light<float, false, kRlItemsWide> : k_rowbm_light<float, false, kRlItems>)
+                     : k_rowbm_light<double, false, kRlItems>;
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   (fn<<<static_cast<unsigned>(blocks), kRbThreads, smem, s>>>(a, nwords, wwords, cap, te_cap,
                                                                static_cast<int>(region)), note_launch());
