@@ -81,8 +81,9 @@ typedef struct gm_csr {
 #define GM_PIPE_FUSED_HISTO 2 /* outer product counts the level-0 chunk histogram while it writes C-hat */
 #define GM_PIPE_ROWWISE 3     /* one level only: heavy rows expanded in row order straight into their
                                  chunks (C-hat is not written); chunk sizes come from the symbolic pass */
-#define GM_PIPE_WALK 4        /* double values, one level only, rows of B with strictly increasing columns: each heavy
-                                 row's level-0 chunk is summed straight from the ranges of the B rows
+#define GM_PIPE_WALK 4        /* double values, one level only, rows of B with strictly increasing
+                                 columns: each heavy row's level-0 chunk is summed straight from the
+                                 ranges of the B rows
                                  that fall into it (neither C-hat nor chunk lists are written); the
                                  symbolic pass keeps the heavy rows' bitmaps (C.m / 8 bytes a row) until
                                  numeric, when they take at most a quarter of the free workspace;

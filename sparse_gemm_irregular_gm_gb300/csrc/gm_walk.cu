@@ -20,6 +20,7 @@
 // with a plain fused multiply-add unless another lane holds the same rank in
 // that step. Block items (more columns): a block per item, every add atomic;
 // ranges of at least kLongRange entries are split evenly over the block's warps.
+// Values are double only: the planner does not offer this pipeline for float.
 #include <algorithm>
 #include <climits>
 
