@@ -139,7 +139,7 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power)}
 
 
-def byte_model(info, A, nnz_c, rowwise, vb=8):
+def byte_model(info, A, nnz_c, rowwise, vb=8, cb=4):
     """Algorithmic bytes per step.
 
     Whole path, outer-product pipelines (the method's byte model, one multisplit
@@ -152,19 +152,21 @@ def byte_model(info, A, nnz_c, rowwise, vb=8):
     Per stage: the bytes that stage must move in this implementation (symbolic
     passes carry columns only, numeric passes columns and values; the level-0
     histogram is counted inside the outer product). Element sizes are for vb-byte
-    values (12 B for a column and a double, 8 B with floats).
+    values (12 B for a column and a double, 8 B with floats); the row-order
+    pipeline stores chunk-local columns in cb bytes (2: uint16).
     """
     e = 4 + vb
+    ec = cb + vb
     ip_h = info.ip_heavy
     L = max(1, info.params.n_levels)
     a_bytes = 8 * (A.n_rows + 1) + e * A.nnz
     c_bytes = 8 * (A.n_rows + 1) + e * nnz_c
     if rowwise:
-        b_alg = 2 * a_bytes + ip_h * (e + 4 + e) + c_bytes
+        b_alg = 2 * a_bytes + ip_h * (ec + 4 + ec) + c_bytes
         stages = {
-            "multisplit": ip_h * e,     # products written once, into their level-0 chunks
+            "multisplit": ip_h * ec,    # products written once, into their level-0 chunks
             "sym_heavy": ip_h * 4,      # B columns walked
-            "num_heavy": ip_h * e,      # chunk columns and values read (+ C writes, added by the caller)
+            "num_heavy": ip_h * ec,     # chunk columns and values read (+ C writes, added by the caller)
         }
         return b_alg, stages
     b_alg = 2 * a_bytes + ip_h * (e + L * (4 + e + e) + 4 + e) + c_bytes
@@ -351,7 +353,8 @@ def run_ours(args):
     flops = 2.0 * info.ip_total
     value = world * flops / (ms / 1e3) / 1e9
     peak, peak_kind = peaks()
-    b_alg, stage_bytes = byte_model(info, A, nnz_c, info.pipeline == binding.GM_PIPE_ROWWISE, vb)
+    b_alg, stage_bytes = byte_model(info, A, nnz_c, info.pipeline == binding.GM_PIPE_ROWWISE, vb,
+                                    info.chunk_col_bytes or 4)
     b_method, _ = byte_model(info, A, nnz_c, False, vb)
     stage_bytes["num_heavy"] += (4 + vb) * nnz_heavy + 8 * len(heavy)
     names = binding.STAGES

@@ -161,7 +161,8 @@ typedef struct gm_plan_info {
   float stage_ms[GM_NUM_STAGES];
   int64_t kernel_launches;     /* kernels this plan has launched so far */
   int32_t value_type;          /* GM_VALUE_* of the plan                */
-  int32_t reserved;
+  int32_t chunk_col_bytes;     /* bytes of a stored chunk column in the numeric pass
+                                  (2: chunk-local uint16, 4: int32)      */
 } gm_plan_info;
 
 typedef struct gm_plan gm_plan; /* opaque; owns every workspace buffer */

@@ -61,7 +61,7 @@ class gm_plan_info(ctypes.Structure):
                 ("keeps_reordered", ctypes.c_int32), ("pipeline", ctypes.c_int32),
                 ("cuda_error", ctypes.c_int32), ("device_status", ctypes.c_int32),
                 ("stage_ms", ctypes.c_float * GM_NUM_STAGES), ("kernel_launches", ctypes.c_int64),
-                ("value_type", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("value_type", ctypes.c_int32), ("chunk_col_bytes", ctypes.c_int32)]
 
 
 class GmError(RuntimeError):

@@ -249,8 +249,10 @@ __device__ __forceinline__ int64_t leaf_col_base(const ListArgs& a, int64_t chil
 
 // Chunk of width <= dense width: bitmap of its columns, prefix sum over the
 // bitmap words, values summed into their rank (= sorted output position).
-template <typename V, bool SYM>
+template <typename V, typename CT, bool SYM>
 __global__ void k_leaf_bitmap(ListArgs a, int nwords, int cap_vals) {
+  const CT* __restrict__ in_col = static_cast<const CT*>(a.col);
+
   const V* __restrict__ in_val = static_cast<const V*>(a.val);
   V* __restrict__ c_val = static_cast<V*>(a.c_val);
 
@@ -271,7 +273,7 @@ __global__ void k_leaf_bitmap(ListArgs a, int nwords, int cap_vals) {
     for (int64_t e0 = lo + threadIdx.x; e0 < hi; e0 += 4 * T) {  // 4 loads in flight per thread
       uint32_t c[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) c[u] = e0 + u * T < hi ? static_cast<uint32_t>(a.col[e0 + u * T]) : ~0u;
+      for (int u = 0; u < 4; ++u) c[u] = e0 + u * T < hi ? static_cast<uint32_t>(in_col[e0 + u * T]) : ~0u;
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         if (c[u] != ~0u) atomicOr(&bm[c[u] >> 5], 1u << (c[u] & 31));
@@ -303,7 +305,7 @@ __global__ void k_leaf_bitmap(ListArgs a, int nwords, int cap_vals) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const bool in = e0 + u * T < hi;
-        c[u] = in ? static_cast<uint32_t>(a.col[e0 + u * T]) : ~0u;
+        c[u] = in ? static_cast<uint32_t>(in_col[e0 + u * T]) : ~0u;
         v[u] = in ? in_val[e0 + u * T] : 0.0;
       }
 #pragma unroll
@@ -340,8 +342,10 @@ __global__ void k_leaf_bitmap(ListArgs a, int nwords, int cap_vals) {
 // cnt[r] gives its arrival index j; a prefix sum over cnt turns counts into
 // segment starts; values are placed at seg[r] + j and each output entry sums its
 // own segment.
-template <typename V, bool SYM, int T, int ITEMS>
+template <typename V, typename CT, bool SYM, int T, int ITEMS>
 __global__ void __launch_bounds__(T) k_leaf_small(ListArgs a, int nwords) {
+  const CT* __restrict__ in_col = static_cast<const CT*>(a.col);
+
   const V* __restrict__ in_val = static_cast<const V*>(a.val);
   V* __restrict__ c_val = static_cast<V*>(a.c_val);
 
@@ -368,7 +372,7 @@ __global__ void __launch_bounds__(T) k_leaf_small(ListArgs a, int nwords) {
       key[k] = -1;
       val[k] = 0.0;
       if (e < hi) {
-        key[k] = a.col[e];
+        key[k] = in_col[e];
         if (!SYM) val[k] = in_val[e];
       }
     }
@@ -445,8 +449,10 @@ __global__ void __launch_bounds__(T) k_leaf_small(ListArgs a, int nwords) {
 // values are added into their rank's slot (chunks this small rarely repeat a
 // column, so the atomics seldom meet), and the chunk is written in column order
 // by words.
-template <typename V, int ITEMS, int WARPS>
+template <typename V, typename CT, int ITEMS, int WARPS>
 __global__ void __launch_bounds__(32 * WARPS, (ITEMS >= 16 ? 160 : 256) / WARPS) k_leaf_warpbm(ListArgs a, int nwp, int vcap) {
+  const CT* __restrict__ in_col = static_cast<const CT*>(a.col);
+
   const V* __restrict__ in_val = static_cast<const V*>(a.val);
   V* __restrict__ c_val = static_cast<V*>(a.c_val);
 
@@ -474,7 +480,7 @@ __global__ void __launch_bounds__(32 * WARPS, (ITEMS >= 16 ? 160 : 256) / WARPS)
 #pragma unroll
       for (int k = 0; k < ITEMS; ++k) {
         const int e = t0 + k * 32 + lane;
-        key[k] = e < n ? a.col[lo + e] : -1;
+        key[k] = e < n ? in_col[lo + e] : -1;
         if (n <= CAPW) val[k] = e < n ? in_val[lo + e] : 0.0;
       }
 #pragma unroll
@@ -500,7 +506,7 @@ __global__ void __launch_bounds__(32 * WARPS, (ITEMS >= 16 ? 160 : 256) / WARPS)
 #pragma unroll
         for (int k = 0; k < ITEMS; ++k) {
           const int e = t0 + k * 32 + lane;
-          key[k] = e < n ? a.col[lo + e] : -1;
+          key[k] = e < n ? in_col[lo + e] : -1;
           val[k] = e < n ? in_val[lo + e] : 0.0;
         }
       }
@@ -531,8 +537,10 @@ __global__ void __launch_bounds__(32 * WARPS, (ITEMS >= 16 ? 160 : 256) / WARPS)
 // The same accumulator for chunks of up to vcap elements with 4 warps per chunk:
 // elements in tiles of 128 * ITEMS through registers, bitmap word prefix by a
 // block scan over 16-byte pieces, values added into their rank's slot.
-template <typename V, int ITEMS, int T>
+template <typename V, typename CT, int ITEMS, int T>
 __global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap, int ecap) {
+  const CT* __restrict__ in_col = static_cast<const CT*>(a.col);
+
   const V* __restrict__ in_val = static_cast<const V*>(a.val);
   V* __restrict__ c_val = static_cast<V*>(a.c_val);
 
@@ -557,7 +565,7 @@ __global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap,
 #pragma unroll
       for (int k = 0; k < ITEMS; ++k) {
         const int e = t0 + k * T + threadIdx.x;
-        key[k] = e < n ? a.col[lo + e] : -1;
+        key[k] = e < n ? in_col[lo + e] : -1;
         if (n <= CAPB) val[k] = e < n ? in_val[lo + e] : 0.0;
       }
 #pragma unroll
@@ -589,7 +597,7 @@ __global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap,
 #pragma unroll
         for (int k = 0; k < ITEMS; ++k) {
           const int e = t0 + k * T + threadIdx.x;
-          key[k] = e < n ? a.col[lo + e] : -1;
+          key[k] = e < n ? in_col[lo + e] : -1;
           val[k] = e < n ? in_val[lo + e] : 0.0;
         }
       }
@@ -620,8 +628,10 @@ __global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap,
 // Tiny chunk (at most CAPW elements): one warp loads it into shared memory,
 // sorts (column, value) pairs with a bitonic network, merges equal columns and
 // writes the chunk in column order. No bitmap, no block barrier.
-template <typename V, int CAPW, int WARPS>
+template <typename V, typename CT, int CAPW, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32) k_leaf_warp(ListArgs a) {
+  const CT* __restrict__ in_col = static_cast<const CT*>(a.col);
+
   const V* __restrict__ in_val = static_cast<const V*>(a.val);
   V* __restrict__ c_val = static_cast<V*>(a.c_val);
 
@@ -637,7 +647,7 @@ __global__ void __launch_bounds__(WARPS * 32) k_leaf_warp(ListArgs a) {
     const int n = static_cast<int>(min(a.rp[m + 1] - lo, static_cast<int64_t>(CAPW)));
     const int64_t child_local = a.child_of ? a.child_of[m] : m;
     for (int i = lane; i < CAPW; i += 32) {
-      key[i] = i < n ? a.col[lo + i] : INT_MAX;
+      key[i] = i < n ? in_col[lo + i] : INT_MAX;
       val[i] = i < n ? in_val[lo + i] : 0.0;
     }
     __syncwarp();
@@ -702,7 +712,7 @@ __global__ void k_leaf_hash(ListArgs a, int cap) {
     bool full = false;
     for (int64_t e = a.rp[m] + threadIdx.x; e < a.rp[m + 1]; e += blockDim.x) {
       bool fresh = false;
-      const int s = hash_insert<POW2>(keys, cap, a.col[e], &fresh, &full);
+      const int s = hash_insert<POW2>(keys, cap, static_cast<const int32_t*>(a.col)[e], &fresh, &full);
       fresh_count += fresh;
       if (!SYM && s >= 0) atomicAdd(&vals[s], in_val[e]);
     }
@@ -775,61 +785,61 @@ void launch_light_rows_t(const LightArgs& a, int cap, bool symbolic, cudaStream_
   }
 }
 
-template <typename V>
+template <typename V, typename CT>
 void launch_leaf_small_t(const ListArgs& a, int max_elems, bool symbolic, cudaStream_t s) {
   const int nwords = static_cast<int>((a.width + 31) / 32);
   const unsigned g = item_grid(a.n_items, 8);
   if (max_elems <= 1024) {
     const size_t smem = static_cast<size_t>(leaf_small_smem(a.width, 1024, symbolic, sizeof(V)));
-    auto fn = symbolic ? k_leaf_small<V, true, 128, 8> : k_leaf_small<V, false, 128, 8>;
+    auto fn = symbolic ? k_leaf_small<V, CT, true, 128, 8> : k_leaf_small<V, CT, false, 128, 8>;
     set_smem(fn, smem);
     (fn<<<g, 128, smem, s>>>(a, nwords), note_launch());
   } else {
     const size_t smem = static_cast<size_t>(leaf_small_smem(a.width, 4096, symbolic, sizeof(V)));
-    auto fn = symbolic ? k_leaf_small<V, true, 256, 16> : k_leaf_small<V, false, 256, 16>;
+    auto fn = symbolic ? k_leaf_small<V, CT, true, 256, 16> : k_leaf_small<V, CT, false, 256, 16>;
     set_smem(fn, smem);
     (fn<<<g, 256, smem, s>>>(a, nwords), note_launch());
   }
 }
 
-template <typename V>
+template <typename V, typename CT>
 void launch_leaf_warpbm_t(const ListArgs& a, int max_elems, int nwp, int W, size_t smem, cudaStream_t s) {
   const unsigned g = static_cast<unsigned>(std::min<int64_t>((a.n_items + W - 1) / W, 152LL * 64));
   if (max_elems <= 128) {
-    set_smem(k_leaf_warpbm<V, 4, 4>, smem);
-    (k_leaf_warpbm<V, 4, 4><<<g, 128, smem, s>>>(a, nwp, max_elems), note_launch());
+    set_smem(k_leaf_warpbm<V, CT, 4, 4>, smem);
+    (k_leaf_warpbm<V, CT, 4, 4><<<g, 128, smem, s>>>(a, nwp, max_elems), note_launch());
   } else if (W == 4) {
-    set_smem(k_leaf_warpbm<V, 16, 4>, smem);
-    (k_leaf_warpbm<V, 16, 4><<<g, 128, smem, s>>>(a, nwp, max_elems), note_launch());
+    set_smem(k_leaf_warpbm<V, CT, 16, 4>, smem);
+    (k_leaf_warpbm<V, CT, 16, 4><<<g, 128, smem, s>>>(a, nwp, max_elems), note_launch());
   } else {
-    set_smem(k_leaf_warpbm<V, 16, 1>, smem);
-    (k_leaf_warpbm<V, 16, 1><<<g, 32, smem, s>>>(a, nwp, max_elems), note_launch());
+    set_smem(k_leaf_warpbm<V, CT, 16, 1>, smem);
+    (k_leaf_warpbm<V, CT, 16, 1><<<g, 32, smem, s>>>(a, nwp, max_elems), note_launch());
   }
 }
 
-template <typename V>
+template <typename V, typename CT>
 void launch_leaf_blkbm_t(const ListArgs& a, int max_nnz, int max_elems, int nwp, size_t smem, cudaStream_t s) {
   const unsigned g = static_cast<unsigned>(std::min<int64_t>(a.n_items, 152LL * 32));
   // threads per chunk grow with the value array so that an SM keeps ~1000 threads busy
   if (max_nnz <= 4096) {
-    set_smem(k_leaf_blkbm<V, 8, 128>, smem);
-    (k_leaf_blkbm<V, 8, 128><<<g, 128, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
+    set_smem(k_leaf_blkbm<V, CT, 8, 128>, smem);
+    (k_leaf_blkbm<V, CT, 8, 128><<<g, 128, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
   } else if (max_nnz <= 8192) {
-    set_smem(k_leaf_blkbm<V, 8, 256>, smem);
-    (k_leaf_blkbm<V, 8, 256><<<g, 256, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
+    set_smem(k_leaf_blkbm<V, CT, 8, 256>, smem);
+    (k_leaf_blkbm<V, CT, 8, 256><<<g, 256, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
   } else {
-    set_smem(k_leaf_blkbm<V, 8, 1024>, smem);
-    (k_leaf_blkbm<V, 8, 1024><<<g, 1024, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
+    set_smem(k_leaf_blkbm<V, CT, 8, 1024>, smem);
+    (k_leaf_blkbm<V, CT, 8, 1024><<<g, 1024, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
   }
 }
 
-template <typename V>
+template <typename V, typename CT>
 void launch_leaf_bitmap_t(const ListArgs& a, int cap_vals, bool symbolic, cudaStream_t s) {
   const int nwords = static_cast<int>((a.width + 31) / 32);
   const size_t smem = static_cast<size_t>(leaf_bitmap_smem(a.width, cap_vals, symbolic, sizeof(V)));
   const int T = symbolic ? 256 : (cap_vals <= 1024 ? 256 : cap_vals <= 8192 ? 512 : 1024);
   const unsigned g = item_grid(a.n_items, 4);
-  auto fn = symbolic ? k_leaf_bitmap<V, true> : k_leaf_bitmap<V, false>;
+  auto fn = symbolic ? k_leaf_bitmap<V, CT, true> : k_leaf_bitmap<V, CT, false>;
   set_smem(fn, smem);
   (fn<<<g, T, smem, s>>>(a, nwords, cap_vals), note_launch());
 }
@@ -871,8 +881,10 @@ int leaf_small_smem(int64_t width, int cap, bool symbolic, int vb) {
 
 void launch_leaf_small(const ListArgs& a, int max_elems, bool symbolic, cudaStream_t s) {
   if (a.n_items <= 0) return;
-  if (a.f32) launch_leaf_small_t<float>(a, max_elems, symbolic, s);
-  else launch_leaf_small_t<double>(a, max_elems, symbolic, s);
+  if (a.f32 && a.col16) launch_leaf_small_t<float, uint16_t>(a, max_elems, symbolic, s);
+  else if (a.f32) launch_leaf_small_t<float, int32_t>(a, max_elems, symbolic, s);
+  else if (a.col16) launch_leaf_small_t<double, uint16_t>(a, max_elems, symbolic, s);
+  else launch_leaf_small_t<double, int32_t>(a, max_elems, symbolic, s);
 }
 
 int64_t leaf_warpbm_words(int64_t width) { return ((width + 31) / 32 + 127) & ~int64_t(127); }
@@ -895,8 +907,10 @@ void launch_leaf_warpbm(const ListArgs& a, int max_elems, cudaStream_t s) {
   const int nwp = static_cast<int>(leaf_warpbm_words(a.width));
   const int W = warpbm_warps(max_elems);
   const size_t smem = static_cast<size_t>(W * warpbm_region(nwp, max_elems, a.f32 ? 4 : 8));
-  if (a.f32) launch_leaf_warpbm_t<float>(a, max_elems, nwp, W, smem, s);
-  else launch_leaf_warpbm_t<double>(a, max_elems, nwp, W, smem, s);
+  if (a.f32 && a.col16) launch_leaf_warpbm_t<float, uint16_t>(a, max_elems, nwp, W, smem, s);
+  else if (a.f32) launch_leaf_warpbm_t<float, int32_t>(a, max_elems, nwp, W, smem, s);
+  else if (a.col16) launch_leaf_warpbm_t<double, uint16_t>(a, max_elems, nwp, W, smem, s);
+  else launch_leaf_warpbm_t<double, int32_t>(a, max_elems, nwp, W, smem, s);
 }
 
 int64_t leaf_blkbm_words(int64_t width) { return ((width + 31) / 32 + 511) & ~int64_t(511); }
@@ -909,22 +923,28 @@ void launch_leaf_blkbm(const ListArgs& a, int max_nnz, int max_elems, cudaStream
   if (a.n_items <= 0) return;
   const int nwp = static_cast<int>(leaf_blkbm_words(a.width));
   const size_t smem = static_cast<size_t>(nwp) * 8 + static_cast<size_t>(max_nnz) * (a.f32 ? 4 : 8);
-  if (a.f32) launch_leaf_blkbm_t<float>(a, max_nnz, max_elems, nwp, smem, s);
-  else launch_leaf_blkbm_t<double>(a, max_nnz, max_elems, nwp, smem, s);
+  if (a.f32 && a.col16) launch_leaf_blkbm_t<float, uint16_t>(a, max_nnz, max_elems, nwp, smem, s);
+  else if (a.f32) launch_leaf_blkbm_t<float, int32_t>(a, max_nnz, max_elems, nwp, smem, s);
+  else if (a.col16) launch_leaf_blkbm_t<double, uint16_t>(a, max_nnz, max_elems, nwp, smem, s);
+  else launch_leaf_blkbm_t<double, int32_t>(a, max_nnz, max_elems, nwp, smem, s);
 }
 
 void launch_leaf_warp(const ListArgs& a, cudaStream_t s) {
   if (a.n_items <= 0) return;
   constexpr int W = 8;
   const unsigned g = static_cast<unsigned>(std::min<int64_t>((a.n_items + W - 1) / W, 152LL * 64));
-  if (a.f32) (k_leaf_warp<float, 128, W><<<g, W * 32, 0, s>>>(a), note_launch());
-  else (k_leaf_warp<double, 128, W><<<g, W * 32, 0, s>>>(a), note_launch());
+  if (a.f32 && a.col16) (k_leaf_warp<float, uint16_t, 128, W><<<g, W * 32, 0, s>>>(a), note_launch());
+  else if (a.f32) (k_leaf_warp<float, int32_t, 128, W><<<g, W * 32, 0, s>>>(a), note_launch());
+  else if (a.col16) (k_leaf_warp<double, uint16_t, 128, W><<<g, W * 32, 0, s>>>(a), note_launch());
+  else (k_leaf_warp<double, int32_t, 128, W><<<g, W * 32, 0, s>>>(a), note_launch());
 }
 
 void launch_leaf_bitmap(const ListArgs& a, int cap_vals, bool symbolic, cudaStream_t s) {
   if (a.n_items <= 0) return;
-  if (a.f32) launch_leaf_bitmap_t<float>(a, cap_vals, symbolic, s);
-  else launch_leaf_bitmap_t<double>(a, cap_vals, symbolic, s);
+  if (a.f32 && a.col16) launch_leaf_bitmap_t<float, uint16_t>(a, cap_vals, symbolic, s);
+  else if (a.f32) launch_leaf_bitmap_t<float, int32_t>(a, cap_vals, symbolic, s);
+  else if (a.col16) launch_leaf_bitmap_t<double, uint16_t>(a, cap_vals, symbolic, s);
+  else launch_leaf_bitmap_t<double, int32_t>(a, cap_vals, symbolic, s);
 }
 
 void launch_leaf_hash(const ListArgs& a, int cap, bool symbolic, cudaStream_t s) {

@@ -319,6 +319,7 @@ struct gm_plan {
   bool b_strict = false;   // every row of B has strictly increasing columns
   bool f32 = false;        // values are float (GM_VALUE_F32), else double
   int vb = 8;              // bytes of a value
+  int arena_cb = 4;        // bytes of a column in the element arenas (2: chunk-local uint16)
   bool walk_ok = false;    // the walk pipeline applies when B is strict and the bitmaps fit
   bool walk = false;       // numeric heavy path: chunks summed straight from B's ranges (gm_walk.cu)
   gm_params P{};
@@ -621,7 +622,7 @@ static void dbg_copy(DevBuf<T>& dst, const T* src, int64_t n, cudaStream_t s) {
 // Accumulates the level-0 chunks of heavy batch rows [h0, h1) (already filled,
 // sizes mcount) into C: the numeric leaves of the one-level hierarchy.
 static gm_status rowwise_leaves(gm_plan* p, int64_t nb, const int64_t* rrp, const int64_t* mcount, int64_t* par_base,
-                                int32_t* c_col, void* c_val) {
+                                int32_t* c_col, void* c_val, bool col16) {
   const int v = static_cast<int>(p->P.v_chunks[0]);
   ListArgs la{};
   la.f32 = p->f32;
@@ -630,6 +631,7 @@ static gm_status rowwise_leaves(gm_plan* p, int64_t nb, const int64_t* rrp, cons
   la.c_val = c_val;
   la.rp = rrp;
   la.col = p->arena_col[0].p;
+  la.col16 = col16;
   la.val = p->arena_val[0].p;
   la.child_base = par_base[0] * v;
   la.v = v;
@@ -705,6 +707,7 @@ static gm_status run_batch_runs(gm_plan* p, int64_t h0, int64_t h1, int64_t* par
   ra.shift = ilog2(p->P.widths[0]);
   ra.cursor = cur.p;
   ra.out_col = p->arena_col[0].p;
+  ra.col16 = p->arena_cb == 2;  // chunk-local columns in 16 bits: 10 (or 6) bytes a product
   ra.out_val = p->arena_val[0].p;
   ra.unit_counter = p->work_counter.p;
   ra.status = p->status.p;
@@ -717,7 +720,7 @@ static gm_status run_batch_runs(gm_plan* p, int64_t h0, int64_t h1, int64_t* par
   e_k.release();
   ufirst.release();
   cur.release();
-  return rowwise_leaves(p, nb, rrp.p, mcount, par_base, c_col, c_val);
+  return rowwise_leaves(p, nb, rrp.p, mcount, par_base, c_col, c_val, ra.col16);
 }
 
 static gm_status run_batch_rowwise(gm_plan* p, int64_t h0, int64_t h1, int64_t* par_base, int32_t* c_col,
@@ -789,7 +792,7 @@ static gm_status run_batch_rowwise(gm_plan* p, int64_t h0, int64_t h1, int64_t* 
   e_row.release();
   e_off.release();
   cur.release();
-  return rowwise_leaves(p, nb, rrp.p, mcount, par_base, c_col, c_val);
+  return rowwise_leaves(p, nb, rrp.p, mcount, par_base, c_col, c_val, false);
 }
 
 // Heavy rows [h0, h1): outer product, multisplit levels and chunk accumulation.
@@ -1084,7 +1087,7 @@ static gm_status alloc_arena(gm_plan* p, const std::vector<std::pair<int64_t, in
   if (p->log)
     std::fprintf(stderr, "[gm_spgemm] %zu batch(es), largest %lld products, arena %.2f GB\n", batches.size(),
                  (long long)mx, mx * (with_val ? 24.0 : 8.0) / 1e9);
-  const size_t col_b = ((static_cast<size_t>(mx) * 4 + 255) / 256) * 256;
+  const size_t col_b = ((static_cast<size_t>(mx) * p->arena_cb + 255) / 256) * 256;
   const size_t val_b = with_val ? ((static_cast<size_t>(mx) * p->vb + 255) / 256) * 256 : 0;
   if (!p->arena_block.alloc(nbuf * (col_b + val_b), p->s)) return GM_ERR_OOM;
   unsigned char* base = p->arena_block.p;
@@ -1389,7 +1392,10 @@ static gm_status numeric_impl(gm_plan* p, int32_t* C_col, void* C_val) {
     const bool keep = p->keep;
     p->keep = false;
     std::vector<std::pair<int64_t, int64_t>> batches;
-    gm_status st = p->rowwise ? plan_and_alloc(p, 12, true, batches, 1) : plan_and_alloc(p, 24, true, batches);
+    // the chunk-direct expansion stores chunk-local columns in 16 bits
+    p->arena_cb = p->rowwise && p->b_sorted && p->P.v_chunks[0] <= 64 && p->P.widths[0] <= 65536 ? 2 : 4;
+    gm_status st = p->rowwise ? plan_and_alloc(p, p->arena_cb + p->vb, true, batches, 1)
+                              : plan_and_alloc(p, 24, true, batches);
     if (st != GM_OK) return st;
     p->n_batches = std::max<int64_t>(p->n_batches, static_cast<int64_t>(batches.size()));
     int64_t par_base[GM_MAX_LEVELS + 1] = {};
@@ -1542,6 +1548,7 @@ gm_status gm_spgemm_plan_info(const gm_plan* plan, gm_plan_info* out) {
   for (int i = 0; i < GM_NUM_STAGES; ++i) out->stage_ms[i] = plan->stage_ms[i];
   out->kernel_launches = plan->launches;
   out->value_type = plan->f32 ? GM_VALUE_F32 : GM_VALUE_F64;
+  out->chunk_col_bytes = plan->arena_cb;
   return GM_OK;
 }
 

@@ -248,8 +248,9 @@ struct RowRunArgs {
   int v;
   int shift;
   unsigned long long* cursor; // per chunk (row * v + c): write cursor
-  int32_t* out_col;
+  void* out_col;              // chunk-local columns: int32, or uint16 with col16
   void* out_val;
+  bool col16;
   unsigned* unit_counter;
   int* status;
 };
@@ -289,8 +290,9 @@ struct ListArgs {
   const int64_t* items;       // mapped C-hat_reord rows to accumulate
   int64_t n_items;
   const int64_t* rp;          // C-hat_reord row pointers (mapped order)
-  const int32_t* col;         // chunk-local columns
+  const void* col;            // chunk-local columns: int32, or uint16 with col16
   const void* val;            // float or double (f32)
+  bool col16;                 // columns stored in 16 bits (chunks at most 65536 wide)
   const int64_t* child_of;    // mapped row -> batch-local child id (null: identity)
   int64_t child_base;         // global child id of batch-local child 0
   int v;                      // chunks per parent (child = parent * v + chunk)

@@ -583,10 +583,11 @@ constexpr int kRrWarps = 8;
 constexpr int kRrRows = 8;   // rows a unit may touch (a.U keeps it below this)
 constexpr int kRrU = 4;
 
-template <typename V, bool VAL>
+template <typename V, typename CT, bool VAL>
 __global__ void __launch_bounds__(kRrWarps * 32, 5) k_expand_rows(RowRunArgs a) {
   const V* __restrict__ e_a = static_cast<const V*>(a.e_a);
   V* __restrict__ out_val = static_cast<V*>(a.out_val);
+  CT* __restrict__ out_col = static_cast<CT*>(a.out_col);
   __shared__ int s_cnt[kRrWarps][kRrRows][64];  // counts, then each warp's offset inside the reservation
   __shared__ int64_t s_rbase[kRrRows][64];       // reservation of each (row, chunk) of the unit
   __shared__ int64_t s_base[kRrWarps][64];
@@ -705,7 +706,7 @@ __global__ void __launch_bounds__(kRrWarps * 32, 5) k_expand_rows(RowRunArgs a) 
             const int64_t dst = s_base[w][col[u] >> a.shift] + q;
             // written once, read once by the accumulators: streaming stores, so that
             // they do not push B and the cursors out of L2
-            __stcs(a.out_col + dst, static_cast<int32_t>(col[u] & mask));
+            __stcs(out_col + dst, static_cast<CT>(col[u] & mask));
             if (VAL) __stcs(out_val + dst, av * bv[u]);
           }
         }
@@ -740,9 +741,13 @@ void launch_row_runs(const RowRunArgs& a, int num_sms, cudaStream_t s) {
    note_launch());
   cudaMemsetAsync(a.unit_counter, 0, sizeof(unsigned), s);
   const unsigned blocks = static_cast<unsigned>(std::min<int64_t>(a.n_units, static_cast<int64_t>(num_sms) * 6));
-  if (a.out_val && a.f32) (k_expand_rows<float, true><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
-  else if (a.out_val) (k_expand_rows<double, true><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
-  else (k_expand_rows<double, false><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
+  if (a.out_val && a.f32 && a.col16)
+    (k_expand_rows<float, uint16_t, true><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
+  else if (a.out_val && a.f32) (k_expand_rows<float, int32_t, true><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
+  else if (a.out_val && a.col16)
+    (k_expand_rows<double, uint16_t, true><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
+  else if (a.out_val) (k_expand_rows<double, int32_t, true><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
+  else (k_expand_rows<double, int32_t, false><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
 }
 
 }  // namespace gm

@@ -83,13 +83,24 @@ def check_invariants(C, u):
     return n
 
 
-def _rounded_to_f32(M):
+def rounded_to_f32(M):
     """M with its values rounded to float (and held as float64, for the oracle)."""
     return M.__class__(M.n_rows, M.n_cols, M.row_ptr, M.col, M.val.astype(np.float32).astype(np.float64))
 
 
-def _ones(M):
+def ones_like_csr(M):
     return M.__class__(M.n_rows, M.n_cols, M.row_ptr, M.col, np.ones_like(M.val))
+
+
+def assert_matches_f32(ref, ref_k, rp, col, val):
+    """Float results against the oracle over the same float inputs: structure
+    bit-exact, every entry within 2 k u sum|ab| (k from ref_k, the oracle on
+    all-ones values)."""
+    np.testing.assert_array_equal(np.diff(rp), np.diff(ref.row_ptr), err_msg="row nnz differ")
+    np.testing.assert_array_equal(col, ref.col, err_msg="columns differ")
+    err = np.abs(val.astype(np.float64) - ref.val)
+    bad = np.nonzero(err > 2.0 * ref_k.val * F32_EPS * ref.abs_scale)[0]
+    assert bad.size == 0, f"{bad.size} float values outside 2 k u sum|ab|"
 
 
 def check_full_f32(A, B, exact=False, **cfg):
@@ -100,7 +111,7 @@ def check_full_f32(A, B, exact=False, **cfg):
     (the oracle's value on all-ones inputs): a float product is within u of the
     exact one and a sum of k terms in any order within (k - 1) u of the exact sum,
     relative to the sum of the magnitudes."""
-    A32, B32 = _rounded_to_f32(A), _rounded_to_f32(B)
+    A32, B32 = rounded_to_f32(A), rounded_to_f32(B)
     (rp, col, val), info = run_gpu(A32, B32, return_info=True, dtype=np.float32, **cfg)
     assert val.dtype == np.float32 and info.value_type == binding.GM_VALUE_F32
     ref = oracle.spgemm(A32, B32)
@@ -110,7 +121,7 @@ def check_full_f32(A, B, exact=False, **cfg):
     if exact:
         np.testing.assert_array_equal(v, ref.val, err_msg="integer-valued float results differ")
     else:
-        k = oracle.spgemm(_ones(A), _ones(B)).val
+        k = oracle.spgemm(ones_like_csr(A), ones_like_csr(B)).val
         bound = 2.0 * k * F32_EPS * ref.abs_scale
         err = np.abs(v - ref.val)
         bad = np.nonzero(err > bound)[0]

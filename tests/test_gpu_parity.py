@@ -14,7 +14,8 @@ import pytest
 
 import oracle
 from sparse_gemm_irregular_gm_gb300 import binding, inputs as gi
-from tests.gpu_common import assert_matches, check_full, check_full_f32, check_invariants, gather_rows, run_gpu
+from tests.gpu_common import (assert_matches, assert_matches_f32, check_full, check_full_f32, check_invariants,
+                               gather_rows, ones_like_csr, rounded_to_f32, run_gpu)
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -483,10 +484,12 @@ def test_workload_erdos_renyi_2_21():
     assert info.ip_total == 64 << 21
 
 
-def _sampled_check(name, n_random=400, seed=0):
+def _sampled_check(name, n_random=400, seed=0, f32=False):
     A = gi.named_workload(name)
+    if f32:
+        A = rounded_to_f32(A)
     u = oracle.ip_counts(A, A)
-    Ad = binding.to_device(A)
+    Ad = binding.to_device(A, dtype=np.float32 if f32 else None)
     C, info = binding.spgemm(Ad, Ad, return_info=True)
     torch.cuda.synchronize()
     assert info.ip_total == int(u.sum()) and info.n_heavy_rows == int((u > info.params.tau).sum())
@@ -499,7 +502,11 @@ def _sampled_check(name, n_random=400, seed=0):
                                      rng.choice(light, min(n_random, light.size), replace=False)]))
     ref = oracle.spgemm_rows(A, A, rows)
     srp, col, val = gather_rows(C, rows)
-    assert_matches(ref, srp, col, val)
+    if f32:
+        ones = ones_like_csr(A)
+        assert_matches_f32(ref, oracle.spgemm_rows(ones, ones, rows), srp, col, val)
+    else:
+        assert_matches(ref, srp, col, val)
     return info
 
 
@@ -513,3 +520,11 @@ def test_workload_rmat18_sampled():
 def test_workload_rmat20_sampled():
     info = _sampled_check("rmat20", n_random=200)
     assert info.n_heavy_rows > 0
+
+
+@pytest.mark.slow
+def test_workload_rmat20_f32_sampled():
+    """The benchmark workload with float values, as `bench.py --dtype f32` runs it:
+    tau 14528, 32 level-0 chunks, sampled rows against the oracle."""
+    info = _sampled_check("rmat20", n_random=150, f32=True)
+    assert info.params.tau == 14528 and list(info.params.v_chunks[:1]) == [32] and info.n_heavy_rows > 0
