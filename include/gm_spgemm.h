@@ -79,8 +79,10 @@ typedef struct gm_csr {
 #define GM_PIPE_AUTO 0        /* GM_PIPE_ROWWISE when it applies, else GM_PIPE_FUSED_HISTO */
 #define GM_PIPE_UNFUSED 1     /* outer product -> C-hat -> histogram -> multisplit (Algorithm 3 as printed) */
 #define GM_PIPE_FUSED_HISTO 2 /* outer product counts the level-0 chunk histogram while it writes C-hat */
-#define GM_PIPE_ROWWISE 3     /* one level only: heavy rows expanded in row order straight into their
-                                 chunks (C-hat is not written); chunk sizes come from the symbolic pass */
+#define GM_PIPE_ROWWISE 3     /* heavy rows expanded in row order straight into their level-0 chunks
+                                 (C-hat is not written); with one level the chunk sizes come from the
+                                 symbolic pass, with more (GM_PIPE_AUTO, B rows sorted, at most 64
+                                 level-0 chunks) the chunks then go through the multisplit levels */
 #define GM_PIPE_WALK 4        /* double values, one level only, rows of B with strictly increasing
                                  columns: each heavy row's level-0 chunk is summed straight from the
                                  ranges of the B rows

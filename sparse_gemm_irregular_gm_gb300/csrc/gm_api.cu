@@ -108,6 +108,13 @@ __global__ void k_mapped_counts(const unsigned long long* __restrict__ cnt, cons
     if (inv) inv[c] = m;
   }
 }
+// cursor of child c = the start of the mapped row it became: rrp[inv[c]]
+__global__ void k_child_cursor(const int64_t* __restrict__ rrp, const int64_t* __restrict__ inv, int64_t n,
+                               unsigned long long* __restrict__ out) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < n; c += stride)
+    out[c] = static_cast<unsigned long long>(rrp[inv[c]]);
+}
 // column base of each new parent: base_prev[g / v] + (g % v) * w, g = global child id at the previous level
 __global__ void k_child_colbase(const int64_t* __restrict__ ids, int64_t n, const int64_t* __restrict__ base_prev,
                                 int64_t v, int64_t w, int64_t* __restrict__ out) {
@@ -322,6 +329,7 @@ struct gm_plan {
   int arena_cb = 4;        // bytes of a column in the element arenas (2: chunk-local uint16)
   bool walk_ok = false;    // the walk pipeline applies when B is strict and the bitmaps fit
   bool walk = false;       // numeric heavy path: chunks summed straight from B's ranges (gm_walk.cu)
+  bool rowexp0 = false;    // two or more levels: level 0 by the row-order expansion, no C-hat
   gm_params P{};
   int L = 0;
   int state = 0;  // 1 analyzed, 2 symbolic done, 3 numeric done
@@ -646,24 +654,20 @@ static gm_status rowwise_leaves(gm_plan* p, int64_t nb, const int64_t* rrp, cons
   return cuda_status(p, cudaGetLastError());
 }
 
-// Chunk-direct pipeline when B's rows are sorted: the batch rows' A entries are
-// gathered in row order, and the expansion writes every product straight into
-// its level-0 chunk, one contiguous block per (unit of products, row, chunk)
-// (k_expand_rows). C-hat is never written; chunk sizes and per-B-row chunk
-// starts come from the symbolic pass.
-static gm_status run_batch_runs(gm_plan* p, int64_t h0, int64_t h1, int64_t* par_base, int32_t* c_col,
-                                void* c_val) {
+// Writes the products of heavy rows [h0, h1) straight into their level-0 chunks
+// (B rows sorted, per-B-row chunk starts in p->bcp, v0 <= 64): the batch rows'
+// A entries are gathered in row order and k_expand_rows writes each product at
+// its chunk's cursor, one contiguous block per (unit of products, row, chunk).
+// cursor[c] (child c = batch row * v0 + chunk) is where chunk c's elements start
+// in the caller's layout; columns are stored chunk-local (16 bits with col16).
+static gm_status expand_into_chunks(gm_plan* p, int64_t h0, int64_t h1, unsigned long long* cursor, void* out_col,
+                                    void* out_val, bool col16, bool numeric) {
   const cudaStream_t s = p->s;
   const int64_t nb = h1 - h0;
   const int64_t ip = p->h_chat_rp[h1] - p->h_chat_rp[h0];
   const int64_t ne = p->h_anz[h1] - p->h_anz[h0];
   const int32_t* heavy = p->rows_by_bin.p + p->bin_start[kHeavyBin] + h0;
-  const int v = static_cast<int>(p->P.v_chunks[0]);
-  const int64_t children = nb * v;
-  if (p->arena_col[0].n < static_cast<size_t>(ip) || p->arena_val[0].n < static_cast<size_t>(ip))
-    return GM_ERR_WORKSPACE;
-
-  int t = p->stage_begin(GM_STAGE_TRANSPOSE);
+  int t = p->stage_begin(numeric ? GM_STAGE_TRANSPOSE : GM_STAGE_TRANSPOSE_SYM);
   DevBuf<int32_t> e_row, e_k;
   DevBuf<double> e_a;
   DevBuf<int64_t> e_b, e_off, ufirst;
@@ -672,27 +676,18 @@ static gm_status run_batch_runs(gm_plan* p, int64_t h0, int64_t h1, int64_t* par
   if (!e_b.alloc(ne, s) || !e_row.alloc(ne, s) || !e_a.alloc(ne, s) || !e_off.alloc(ne + 1, s) ||
       !e_k.alloc(ne, s) || !ufirst.alloc(std::max<int64_t>(n_units, 1), s))
     return GM_ERR_OOM;
-  launch_gather_entries(heavy, nb, p->anz.p + h0, p->A.row_ptr, p->A.col_idx, p->A.vals, p->f32, p->B.row_ptr, e_b.p, e_a.p,
-                        e_row.p, e_off.p, s, e_k.p);
+  launch_gather_entries(heavy, nb, p->anz.p + h0, p->A.row_ptr, p->A.col_idx, p->A.vals, p->f32, p->B.row_ptr,
+                        e_b.p, e_a.p, e_row.p, e_off.p, s, e_k.p);
   cudaMemsetAsync(e_off.p + ne, 0, sizeof(int64_t), s);
   if (!scan_exclusive_i64(e_off.p, e_off.p, ne + 1, nullptr, s)) return GM_ERR_OOM;
   p->stage_end(t);
 
-  t = p->stage_begin(GM_STAGE_HISTOGRAM);
-  const int64_t* mcount = p->cnt0.p + h0 * v;  // chunk sizes from the symbolic pass
-  DevBuf<int64_t> rrp;
-  DevBuf<unsigned long long> cur;
-  if (!rrp.alloc(children + 1, s) || !cur.alloc(children, s)) return GM_ERR_OOM;
-  if (!scan_exclusive_i64(mcount, rrp.p, children, rrp.p + children, s)) return GM_ERR_OOM;
-  sub_to_u64(rrp.p, children, 0, cur.p, s);
-  p->stage_end(t);
-
-  t = p->stage_begin(GM_STAGE_MULTISPLIT);
+  t = p->stage_begin(numeric ? GM_STAGE_MULTISPLIT : GM_STAGE_MULTISPLIT_SYM);
   RowRunArgs ra{};
   ra.f32 = p->f32;
   ra.e_k = e_k.p;
   ra.e_b = e_b.p;
-  ra.e_a = e_a.p;
+  ra.e_a = out_val ? e_a.p : nullptr;
   ra.e_off = e_off.p;
   ra.e_row = e_row.p;
   ra.n_e = ne;
@@ -703,24 +698,44 @@ static gm_status run_batch_runs(gm_plan* p, int64_t h0, int64_t h1, int64_t* par
   ra.b_col = p->B.col_idx;
   ra.b_val = p->B.vals;
   ra.bcp = p->bcp.p;
-  ra.v = v;
+  ra.v = static_cast<int>(p->P.v_chunks[0]);
   ra.shift = ilog2(p->P.widths[0]);
-  ra.cursor = cur.p;
-  ra.out_col = p->arena_col[0].p;
-  ra.col16 = p->arena_cb == 2;  // chunk-local columns in 16 bits: 10 (or 6) bytes a product
-  ra.out_val = p->arena_val[0].p;
+  ra.cursor = cursor;
+  ra.out_col = out_col;
+  ra.col16 = col16;
+  ra.out_val = out_val;
   ra.unit_counter = p->work_counter.p;
   ra.status = p->status.p;
   launch_row_runs(ra, p->num_sms, s);
   p->stage_end(t);
-  e_b.release();
-  e_a.release();
-  e_row.release();
-  e_off.release();
-  e_k.release();
-  ufirst.release();
+  return cuda_status(p, cudaGetLastError());
+}
+
+// Chunk-direct pipeline when B's rows are sorted (one level): the products go
+// straight into the level-0 chunks, laid out child by child (chunk sizes from the
+// symbolic pass); C-hat is never written.
+static gm_status run_batch_runs(gm_plan* p, int64_t h0, int64_t h1, int64_t* par_base, int32_t* c_col,
+                                void* c_val) {
+  const cudaStream_t s = p->s;
+  const int64_t nb = h1 - h0;
+  const int64_t ip = p->h_chat_rp[h1] - p->h_chat_rp[h0];
+  const int v = static_cast<int>(p->P.v_chunks[0]);
+  const int64_t children = nb * v;
+  if (p->arena_col[0].n < static_cast<size_t>(ip) || p->arena_val[0].n < static_cast<size_t>(ip))
+    return GM_ERR_WORKSPACE;
+  int t = p->stage_begin(GM_STAGE_HISTOGRAM);
+  const int64_t* mcount = p->cnt0.p + h0 * v;  // chunk sizes from the symbolic pass
+  DevBuf<int64_t> rrp;
+  DevBuf<unsigned long long> cur;
+  if (!rrp.alloc(children + 1, s) || !cur.alloc(children, s)) return GM_ERR_OOM;
+  if (!scan_exclusive_i64(mcount, rrp.p, children, rrp.p + children, s)) return GM_ERR_OOM;
+  sub_to_u64(rrp.p, children, 0, cur.p, s);
+  p->stage_end(t);
+  const bool col16 = p->arena_cb == 2;  // chunk-local columns in 16 bits: 10 (or 6) bytes a product
+  const gm_status st = expand_into_chunks(p, h0, h1, cur.p, p->arena_col[0].p, p->arena_val[0].p, col16, true);
+  if (st != GM_OK) return st;
   cur.release();
-  return rowwise_leaves(p, nb, rrp.p, mcount, par_base, c_col, c_val, ra.col16);
+  return rowwise_leaves(p, nb, rrp.p, mcount, par_base, c_col, c_val, col16);
 }
 
 static gm_status run_batch_rowwise(gm_plan* p, int64_t h0, int64_t h1, int64_t* par_base, int32_t* c_col,
@@ -810,8 +825,28 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
   const int L = p->L;
   gm_status st = GM_OK;
 
+  const bool rowexp = p->rowexp0;  // level 0 written by the row-order expansion (no C-hat)
+  int t = 0;
+  int32_t* chat_col = p->arena_col[0].p;
+  void* chat_val = with_val ? p->arena_val[0].p : nullptr;
+  DevBuf<int64_t> lrp;
+  DevBuf<unsigned long long> cnt0;
+  const bool fused = L >= 1 && p->pipeline == GM_PIPE_FUSED_HISTO;
+  if (rowexp) {  // level-0 chunk sizes of the batch from the per-B-row chunk starts
+    t = p->stage_begin(numeric ? GM_STAGE_HISTOGRAM : GM_STAGE_HISTOGRAM_SYM);
+    if (p->arena_col[1].n < static_cast<size_t>(ip) || (with_val && p->arena_val[1].n < static_cast<size_t>(ip)))
+      return GM_ERR_WORKSPACE;
+    DevBuf<int64_t> anz_b;  // the batch's A-entry prefix, rebased to 0
+    if (!anz_b.alloc(nb + 1, s) || !cnt0.alloc(nb * p->P.v_chunks[0], s)) return GM_ERR_OOM;
+    sub_i64(p->anz.p + h0, nb + 1, p->h_anz[h0], anz_b.p, s);
+    if (!heavy_chunk_counts(heavy, nb, anz_b.p, p->A.row_ptr, p->A.col_idx, nullptr, p->B.col_idx, p->B.n_rows,
+                            static_cast<int>(p->P.v_chunks[0]), ilog2(p->P.widths[0]), p->bcp.p,
+                            reinterpret_cast<int64_t*>(cnt0.p), s))
+      return GM_ERR_OOM;
+    p->stage_end(t);
+  } else {
   // 1. Masked CSR -> CSC of the batch rows and the slice offsets (Algorithm 3 line 7).
-  int t = p->stage_begin(numeric ? GM_STAGE_TRANSPOSE : GM_STAGE_TRANSPOSE_SYM);
+  t = p->stage_begin(numeric ? GM_STAGE_TRANSPOSE : GM_STAGE_TRANSPOSE_SYM);
   DevBuf<int64_t> col_ptr, slice_off;
   DevBuf<int32_t> t_row, wg_op;
   DevBuf<double> t_val;
@@ -829,14 +864,10 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
   t = p->stage_begin(numeric ? GM_STAGE_OUTER : GM_STAGE_OUTER_SYM);
   if (p->arena_col[0].n < static_cast<size_t>(ip) || (with_val && p->arena_val[0].n < static_cast<size_t>(ip)))
     return GM_ERR_WORKSPACE;
-  int32_t* const chat_col = p->arena_col[0].p;
-  void* const chat_val = with_val ? p->arena_val[0].p : nullptr;
-  DevBuf<int64_t> lrp;
-  DevBuf<unsigned long long> cursor, cnt0;
+  DevBuf<unsigned long long> cursor;
   if (!lrp.alloc(nb + 1, s) || !cursor.alloc(nb, s)) return GM_ERR_OOM;
   sub_i64(p->chat_rp.p + h0, nb + 1, p->h_chat_rp[h0], lrp.p, s);
   sub_to_u64(p->chat_rp.p + h0, nb, p->h_chat_rp[h0], cursor.p, s);
-  const bool fused = L >= 1 && p->pipeline == GM_PIPE_FUSED_HISTO;
   if (L >= 1) {
     if (!cnt0.alloc(nb * p->P.v_chunks[0], s)) return GM_ERR_OOM;
     cudaMemsetAsync(cnt0.p, 0, cnt0.bytes(), s);
@@ -873,6 +904,7 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
     if (with_val) dbg_copy(p->dbg_chat_val, static_cast<const unsigned char*>(chat_val), ip * p->vb, s);
     dbg_copy(p->dbg_chat_rp, lrp.p, nb + 1, s);
   }
+  }  // C-hat
 
   ListArgs base_la{};
   base_la.f32 = p->f32;
@@ -917,9 +949,12 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
     if (E == 0) return GM_ERR_INVALID_ARG;
 
     t = p->stage_begin(numeric ? GM_STAGE_HISTOGRAM : GM_STAGE_HISTOGRAM_SYM);
+    const bool expand_here = i == 0 && rowexp;  // level 0 comes from the expansion, not a multisplit
     DevBuf<int32_t> wg;
-    if (!wg.alloc((in_total + E - 1) / E, s)) return GM_ERR_OOM;
-    launch_wg_row(in_rp, P_b, E, wg.p, s);
+    if (!expand_here) {
+      if (!wg.alloc((in_total + E - 1) / E, s)) return GM_ERR_OOM;
+      launch_wg_row(in_rp, P_b, E, wg.p, s);
+    }
     SplitArgs sa{};
     sa.f32 = p->f32;
     sa.in_rp = in_rp;
@@ -936,7 +971,7 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
     sa.status = p->status.p;
     DevBuf<unsigned long long> cnt_own;
     unsigned long long* cnt = cnt0.p;
-    if (!(i == 0 && fused)) {
+    if (!(i == 0 && (fused || rowexp))) {
       if (!cnt_own.alloc(children, s)) return GM_ERR_OOM;
       cudaMemsetAsync(cnt_own.p, 0, cnt_own.bytes(), s);
       cnt = cnt_own.p;
@@ -979,7 +1014,17 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
     sa.cursor = cur.p;
     sa.out_col = out_col;
     sa.out_val = out_val;
-    launch_multisplit(sa, s);
+    if (expand_here) {  // each child's products go to the start of the row it is mapped to
+      p->stage_end(t);
+      DevBuf<unsigned long long> ccur;
+      if (!ccur.alloc(children, s)) return GM_ERR_OOM;
+      (k_child_cursor<<<grid_for(children, 256), 256, 0, s>>>(rrp->p, inv.p, children, ccur.p), note_launch());
+      st = expand_into_chunks(p, h0, h1, ccur.p, out_col, out_val, false, numeric);
+      if (st != GM_OK) return st;
+      t = p->stage_begin(numeric ? GM_STAGE_MULTISPLIT : GM_STAGE_MULTISPLIT_SYM);
+    } else {
+      launch_multisplit(sa, s);
+    }
     p->stage_end(t);
     if (i == 0) cnt0.release();
     if (p->keep) {
@@ -1267,6 +1312,11 @@ static gm_status symbolic_impl(gm_plan* p, int64_t* C_rp, int64_t* C_nnz) {
     std::vector<std::pair<int64_t, int64_t>> batches;
     gm_status st = plan_and_alloc(p, p->keep ? 24 : 8, p->keep, batches);
     if (st != GM_OK) return st;
+    if (p->rowexp0) {  // per-B-row starts of the level-0 chunks, for both passes
+      if (!p->bcp.alloc(std::max<int64_t>(p->B.n_rows, 1) * (v0 + 1), s)) return GM_ERR_OOM;
+      build_chunk_starts(p->B.row_ptr, p->B.col_idx, p->B.n_rows, static_cast<int>(v0), ilog2(p->P.widths[0]),
+                         p->bcp.p, s);
+    }
     if (p->keep && batches.size() != 1) {  // intermediates are kept for a single batch only
       p->keep = false;
       free_arena(p);
@@ -1487,6 +1537,10 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
     cudaGetLastError();
     return st;
   }
+  // two or more levels, B's rows sorted: level 0 by the row-order expansion
+  p->rowexp0 = !p->rowwise && p->L >= 2 && p->b_sorted && p->P.v_chunks[0] <= 64 &&
+               p->cfg.pipeline == GM_PIPE_AUTO && !p->keep;
+  if (p->rowexp0) p->pipeline = GM_PIPE_ROWWISE;
   p->state = 1;
   if (p->log) gm::log_plan(p.get());
   *plan_out = p.release();
