@@ -47,6 +47,8 @@ FORCED = [
     ("L1_rowwise_batched", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "workspace_cap_bytes": 5 << 20,
                             "pipeline": binding.GM_PIPE_ROWWISE}),
     ("L1_rowwise", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_ROWWISE}),
+    ("L2_outer", {"tau": 16, "dense_width": 64, "n_chunks_max": 4, "pipeline": binding.GM_PIPE_FUSED_HISTO}),
+    ("L3_outer", {"tau": 16, "dense_width": 16, "n_chunks_max": 4, "pipeline": binding.GM_PIPE_FUSED_HISTO}),
     ("L1_walk_128", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_WALK}),
     ("L1_walk_256", {"tau": 16, "dense_width": 256, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_WALK}),
     ("L1_walk_wide", {"tau": 64, "dense_width": 512, "pipeline": binding.GM_PIPE_WALK}),
@@ -66,6 +68,10 @@ def test_rmat10_forced_paths(name, cfg, values):
             assert info.pipeline == binding.GM_PIPE_ROWWISE
         if name.startswith("L1_walk"):
             assert info.pipeline == binding.GM_PIPE_WALK
+        if name in ("heavy_L2", "heavy_L3"):  # level 0 by the row-order expansion
+            assert info.pipeline == binding.GM_PIPE_ROWWISE and info.params.n_levels >= 2
+        if name in ("L2_outer", "L3_outer"):
+            assert info.pipeline == binding.GM_PIPE_FUSED_HISTO and info.params.n_levels >= 2
         if name == "L1_outer":
             assert info.pipeline == binding.GM_PIPE_FUSED_HISTO
 
@@ -373,14 +379,17 @@ def test_chunk_with_one_hot_column(n_hot, pipeline):
     assert info.pipeline == (binding.GM_PIPE_ROWWISE if pipeline == binding.GM_PIPE_AUTO else pipeline)
 
 
+@pytest.mark.parametrize("pipeline", [binding.GM_PIPE_AUTO, binding.GM_PIPE_FUSED_HISTO], ids=["rowexp", "outer"])
 @pytest.mark.parametrize("values", ["uniform", "int"])
-def test_multilevel_wide_light_chunks(values):
+def test_multilevel_wide_light_chunks(values, pipeline):
     """Three levels (4, 4, 2 chunks of 4096, 1024, 512 columns) with tau = 2048:
     about 8900 level-0 chunks of 513-2048 elements leave the hierarchy as light
-    chunks, summed by the bitmap-rank accumulator at width 4096."""
+    chunks, summed by the bitmap-rank accumulator at width 4096; level 0 from the
+    row-order expansion or from C-hat."""
     A = gi.rmat(14, 16, seed=4, values=values)
-    info = check_full(A, A, exact=values == "int", tau=2048, dense_width=512, n_chunks_max=4)
+    info = check_full(A, A, exact=values == "int", tau=2048, dense_width=512, n_chunks_max=4, pipeline=pipeline)
     assert info.params.n_levels == 3 and info.n_heavy_rows > 4000
+    assert info.pipeline == (binding.GM_PIPE_ROWWISE if pipeline == binding.GM_PIPE_AUTO else pipeline)
 
 
 @pytest.mark.parametrize("values", ["uniform", "int"])
