@@ -14,11 +14,12 @@
  *   gm_spgemm_numeric   -- lines 26-28: numeric accumulation, C.col / C.val.
  *
  * Conventions common to every call
- *   - Matrices are CSR: row_ptr int64[n_rows+1] (row_ptr[0] = 0, non-decreasing,
- *     row_ptr[n_rows] = nnz), col_idx int32[nnz] in [0, n_cols), vals[nnz] of
- *     the value type gm_config.value_type selects (double, the default, or float;
- *     A, B and C share it). Rows need not be sorted and may repeat a column;
- *     repeated entries add.
+ *   - Matrices are CSR: row_ptr[n_rows+1] (row_ptr[0] = 0, non-decreasing,
+ *     row_ptr[n_rows] = nnz), col_idx[nnz] in [0, n_cols), vals[nnz]. Row
+ *     pointers are int64 and columns int32 unless gm_config.index_type says
+ *     otherwise; values are of the type gm_config.value_type selects (double,
+ *     the default, or float). A, B and C share these types. Rows need not be
+ *     sorted and may repeat a column; repeated entries add.
  *   - Pointers documented "device" must be device (or managed) memory of the
  *     current CUDA device; "host" pointers are ordinary host memory.
  *   - Every call returns a gm_status; nothing is thrown across the ABI. A call
@@ -59,8 +60,8 @@ typedef struct gm_csr {
   int64_t n_rows;
   int64_t n_cols;
   int64_t nnz;
-  const int64_t* row_ptr; /* device, n_rows + 1 */
-  const int32_t* col_idx; /* device, nnz        */
+  const void* row_ptr;    /* device, n_rows + 1 int64 (int32 with GM_INDEX_ROWPTR32) */
+  const void* col_idx;    /* device, nnz int32 (int64 with GM_INDEX_COL64)           */
   const void* vals;       /* device, nnz values of gm_config.value_type (double by default) */
 } gm_csr;
 
@@ -69,6 +70,19 @@ typedef struct gm_csr {
  * and dense width than double ones. */
 #define GM_VALUE_F64 0 /* double */
 #define GM_VALUE_F32 1 /* float  */
+
+/* Index types for gm_config.index_type, flags that may be combined; 0 means int64
+ * row pointers and int32 columns. They set the element type of every row-pointer
+ * array (A, B and C.rowPtr) and of every column array (A, B and C.col) at this
+ * interface. Inside, the path keeps int64 row pointers and int32 columns: int32
+ * row pointers are widened and int64 columns narrowed into copies the plan owns
+ * (12 bytes per row and 4 per stored entry of A and B, once when A and B share
+ * an array), and C's arrays are written through plan-owned buffers that are then
+ * converted into the caller's. The planner's s_C.col stays 4 bytes, the width of
+ * the columns held in shared memory. */
+#define GM_INDEX_ROWPTR32 1 /* row pointers int32: nnz of A, B and C at most 2^31 - 1 */
+#define GM_INDEX_COL64 2    /* columns int64, each in [0, n_cols) (n_cols <= 2^31 as always);
+                               numeric needs 4 more bytes of workspace per entry of C */
 
 /* Flags for gm_config.flags. */
 #define GM_FLAG_TIMING 1             /* record per-stage device times (gm_plan_info.stage_ms) */
@@ -104,6 +118,7 @@ typedef struct gm_config {
   int32_t pipeline;            /* GM_PIPE_*                                                    */
   int32_t flags;               /* GM_FLAG_*                                                    */
   int32_t value_type;          /* GM_VALUE_*: element type of A.vals, B.vals and C's values    */
+  int32_t index_type;          /* GM_INDEX_* flags: row-pointer and column types of A, B and C */
 } gm_config;
 
 #define GM_MAX_LEVELS 16
@@ -165,6 +180,7 @@ typedef struct gm_plan_info {
   int32_t value_type;          /* GM_VALUE_* of the plan                */
   int32_t chunk_col_bytes;     /* bytes of a stored chunk column in the numeric pass
                                   (2: chunk-local uint16, 4: int32)      */
+  int32_t index_type;          /* GM_INDEX_* flags of the plan          */
 } gm_plan_info;
 
 typedef struct gm_plan gm_plan; /* opaque; owns every workspace buffer */
@@ -183,7 +199,7 @@ void gm_set_allocator(gm_alloc_fn alloc_fn, gm_free_fn free_fn, gm_avail_fn avai
 
 /* Host only. Fills *out with the parameters gMAGNUS Sec. III-D derives for a
  * product with c_m columns (Eqs. (4)-(7)) for int32 columns, int64 row pointers
- * and the value type of cfg (8-byte double by default, 4-byte float), honouring
+ * (the widths held in shared memory, whatever cfg->index_type) and the value type of cfg (8-byte double by default, 4-byte float), honouring
  * the overrides in cfg (nullable). cfg->smem_budget_bytes == 0 means 232448
  * bytes (227 KB, the opt-in shared memory per block of sm_103a). Errors:
  * GM_ERR_INVALID_ARG for c_m < 1, a null out, an unknown value type, or
@@ -199,27 +215,31 @@ gm_status gm_spgemm_params(int64_t c_m, const gm_config* cfg, gm_params* out);
  * Blocks until the row counts are on the host. On success *plan_out owns all
  * workspace; release it with gm_spgemm_plan_destroy.
  * Errors: GM_ERR_INVALID_ARG, GM_ERR_DIM_MISMATCH, GM_ERR_INDEX_OVERFLOW,
- * GM_ERR_BAD_INDEX (a column out of range or a malformed row_ptr), GM_ERR_OOM,
- * GM_ERR_CUDA. *plan_out is NULL on error. */
+ * GM_ERR_BAD_INDEX (a column out of range, also an int64 column that does not
+ * fit 32 bits, or a malformed row_ptr), GM_ERR_OOM, GM_ERR_CUDA. GM_ERR_INVALID_ARG
+ * also for an unknown value type or index flag. *plan_out is NULL on error. */
 gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* cfg, void* stream,
                             gm_plan** plan_out);
 
-/* Algorithm 3 lines 7-25. Writes C.rowPtr (device, A.n_rows + 1 int64, caller
- * allocated) and *C_nnz (host). Heavy rows go through the outer product and the
- * hierarchical multisplit in batches that fit the workspace cap; light rows are
- * counted with a shared-memory accumulator. Blocks until C.nnz is on the host.
+/* Algorithm 3 lines 7-25. Writes C.rowPtr (device, A.n_rows + 1 row pointers of
+ * the plan's index type, caller allocated) and *C_nnz (host). Heavy rows go
+ * through the outer product and the hierarchical multisplit in batches that fit
+ * the workspace cap; light rows are counted with a shared-memory accumulator.
+ * Blocks until C.rowPtr is written and C.nnz is on the host.
  * Errors: GM_ERR_STATE (not right after analyze), GM_ERR_INVALID_ARG,
  * GM_ERR_WORKSPACE (a single heavy row does not fit the cap), GM_ERR_OOM,
- * GM_ERR_CUDA, GM_ERR_DEVICE_TIMEOUT. */
-gm_status gm_spgemm_symbolic(gm_plan* plan, int64_t* C_row_ptr, int64_t* C_nnz);
+ * GM_ERR_CUDA, GM_ERR_DEVICE_TIMEOUT, GM_ERR_INDEX_OVERFLOW (GM_INDEX_ROWPTR32
+ * and C.nnz above 2^31 - 1: *C_nnz holds C.nnz, C_row_ptr is not written and
+ * the plan takes no further symbolic or numeric call). */
+gm_status gm_spgemm_symbolic(gm_plan* plan, void* C_row_ptr, int64_t* C_nnz);
 
-/* Algorithm 3 lines 26-28. Fills C.col (device int32[C_nnz]) and C.val (device,
- * C_nnz values of the plan's value type), both caller allocated after
- * gm_spgemm_symbolic; each row sorted
- * by column. Returns once the work is issued and has completed (stream synchronised).
+/* Algorithm 3 lines 26-28. Fills C.col (device, C_nnz columns of the plan's
+ * index type) and C.val (device, C_nnz values of the plan's value type), both
+ * caller allocated after gm_spgemm_symbolic; each row sorted by column. Returns
+ * once the work is issued and has completed (stream synchronised).
  * Errors: GM_ERR_STATE (symbolic not done, or numeric already done),
  * GM_ERR_INVALID_ARG, GM_ERR_WORKSPACE, GM_ERR_OOM, GM_ERR_CUDA. */
-gm_status gm_spgemm_numeric(gm_plan* plan, int32_t* C_col_idx, void* C_vals);
+gm_status gm_spgemm_numeric(gm_plan* plan, void* C_col_idx, void* C_vals);
 
 /* Copies the plan's parameters, sizes and statistics (gMAGNUS Tables V/VI:
  * C-hat size, heavy IP and row fractions, chunks per level) into *out (host). */

@@ -19,6 +19,7 @@ STATUS_NAMES = ["GM_OK", "GM_ERR_INVALID_ARG", "GM_ERR_DIM_MISMATCH", "GM_ERR_IN
                 "GM_ERR_WORKSPACE", "GM_ERR_CUDA", "GM_ERR_DEVICE_TIMEOUT", "GM_ERR_STATE", "GM_ERR_BAD_INDEX"]
 GM_FLAG_TIMING, GM_FLAG_KEEP_INTERMEDIATES, GM_FLAG_LOG = 1, 2, 4
 GM_VALUE_F64, GM_VALUE_F32 = 0, 1
+GM_INDEX_ROWPTR32, GM_INDEX_COL64 = 1, 2
 GM_PIPE_AUTO, GM_PIPE_UNFUSED, GM_PIPE_FUSED_HISTO, GM_PIPE_ROWWISE, GM_PIPE_WALK = 0, 1, 2, 3, 4
 PIPELINES = {GM_PIPE_AUTO: "auto", GM_PIPE_UNFUSED: "outer-product, unfused",
              GM_PIPE_FUSED_HISTO: "outer-product, fused level-0 histogram",
@@ -42,7 +43,8 @@ class gm_csr(ctypes.Structure):
 class gm_config(ctypes.Structure):
     _fields_ = [("smem_budget_bytes", ctypes.c_int64), ("tau", ctypes.c_int64), ("dense_width", ctypes.c_int64),
                 ("n_chunks_max", ctypes.c_int64), ("workspace_cap_bytes", ctypes.c_int64),
-                ("pipeline", ctypes.c_int32), ("flags", ctypes.c_int32), ("value_type", ctypes.c_int32)]
+                ("pipeline", ctypes.c_int32), ("flags", ctypes.c_int32), ("value_type", ctypes.c_int32),
+                ("index_type", ctypes.c_int32)]
 
 
 class gm_params(ctypes.Structure):
@@ -61,7 +63,8 @@ class gm_plan_info(ctypes.Structure):
                 ("keeps_reordered", ctypes.c_int32), ("pipeline", ctypes.c_int32),
                 ("cuda_error", ctypes.c_int32), ("device_status", ctypes.c_int32),
                 ("stage_ms", ctypes.c_float * GM_NUM_STAGES), ("kernel_launches", ctypes.c_int64),
-                ("value_type", ctypes.c_int32), ("chunk_col_bytes", ctypes.c_int32)]
+                ("value_type", ctypes.c_int32), ("chunk_col_bytes", ctypes.c_int32),
+                ("index_type", ctypes.c_int32)]
 
 
 class GmError(RuntimeError):
@@ -191,7 +194,8 @@ def gm_spgemm_params(c_m: int, cfg: gm_config | None = None) -> gm_params:
 
 @dataclass
 class DeviceCSR:
-    """CSR operand whose arrays are torch CUDA tensors (int64 / int32 / float64 or float32)."""
+    """CSR operand whose arrays are torch CUDA tensors: row pointers int64 or int32, columns int32 or
+    int64, values float64 or float32."""
 
     n_rows: int
     n_cols: int
@@ -208,13 +212,16 @@ class DeviceCSR:
                       self.col.data_ptr() if self.nnz else None, self.val.data_ptr() if self.nnz else None)
 
 
-def to_device(M, device="cuda", dtype=None) -> DeviceCSR:
+def to_device(M, device="cuda", dtype=None, row_ptr_dtype=None, col_dtype=None) -> DeviceCSR:
     """Copy a host CSR (``inputs.CSR``) to torch CUDA tensors; values as ``dtype``
-    (numpy float32 or float64, default: as stored)."""
+    (numpy float32 or float64), row pointers as ``row_ptr_dtype`` (int64 or
+    int32), columns as ``col_dtype`` (int32 or int64); default: as stored."""
     import torch
     val = M.val if dtype is None else M.val.astype(dtype)
-    return DeviceCSR(M.n_rows, M.n_cols, torch.from_numpy(M.row_ptr).to(device),
-                     torch.from_numpy(M.col).to(device), torch.from_numpy(val).to(device))
+    rp = M.row_ptr if row_ptr_dtype is None else M.row_ptr.astype(row_ptr_dtype)
+    col = M.col if col_dtype is None else M.col.astype(col_dtype)
+    return DeviceCSR(M.n_rows, M.n_cols, torch.from_numpy(rp).to(device),
+                     torch.from_numpy(col).to(device), torch.from_numpy(val).to(device))
 
 
 def _value_type(A: DeviceCSR, B: DeviceCSR) -> int:
@@ -227,6 +234,21 @@ def _value_type(A: DeviceCSR, B: DeviceCSR) -> int:
     return ta
 
 
+def _index_type(A: DeviceCSR, B: DeviceCSR) -> int:
+    """GM_INDEX_* flags of the operands' row-pointer and column tensors (A and B must agree)."""
+    import torch
+    rp = {torch.int64: 0, torch.int32: GM_INDEX_ROWPTR32}
+    col = {torch.int32: 0, torch.int64: GM_INDEX_COL64}
+    ra, rb = rp.get(A.row_ptr.dtype), rp.get(B.row_ptr.dtype)
+    ca, cb = col.get(A.col.dtype), col.get(B.col.dtype)
+    if ra is None or ra != rb:
+        raise GmError(1, f"row pointers must be int64 or int32 in both A and B, not {A.row_ptr.dtype} and "
+                         f"{B.row_ptr.dtype}")
+    if ca is None or ca != cb:
+        raise GmError(1, f"columns must be int32 or int64 in both A and B, not {A.col.dtype} and {B.col.dtype}")
+    return ra | ca
+
+
 def _stream_handle(stream):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
@@ -234,15 +256,18 @@ def _stream_handle(stream):
 
 
 def gm_spgemm_analyze(A: DeviceCSR, B: DeviceCSR, cfg: gm_config | None = None, stream=None):
-    """gm_spgemm_analyze with cfg.value_type taken from the operands' value dtype."""
+    """gm_spgemm_analyze with cfg.value_type and cfg.index_type taken from the
+    operands' tensor dtypes."""
     plan = ctypes.c_void_p()
     a, b = A.desc(), B.desc()
     vt = _value_type(A, B)
-    if cfg is None and vt != GM_VALUE_F64:
+    it = _index_type(A, B)
+    if cfg is None and (vt != GM_VALUE_F64 or it != 0):
         cfg = gm_config()
     if cfg is not None:
         cfg = gm_config.from_buffer_copy(cfg)
         cfg.value_type = vt
+        cfg.index_type = it
     _check(load().gm_spgemm_analyze(ctypes.byref(a), ctypes.byref(b), ctypes.byref(cfg) if cfg else None,
                                     _stream_handle(stream), ctypes.byref(plan)), "gm_spgemm_analyze")
     return plan
@@ -298,9 +323,9 @@ def spgemm(A: DeviceCSR, B: DeviceCSR, cfg: gm_config | None = None, stream=None
     dev = A.row_ptr.device
     plan = gm_spgemm_analyze(A, B, cfg, stream)
     try:
-        c_rp = torch.empty(A.n_rows + 1, dtype=torch.int64, device=dev)
+        c_rp = torch.empty(A.n_rows + 1, dtype=A.row_ptr.dtype, device=dev)
         nnz = gm_spgemm_symbolic(plan, c_rp)
-        c_col = torch.empty(nnz, dtype=torch.int32, device=dev)
+        c_col = torch.empty(nnz, dtype=A.col.dtype, device=dev)
         c_val = torch.empty(nnz, dtype=A.val.dtype, device=dev)
         gm_spgemm_numeric(plan, c_col, c_val)
         info = gm_spgemm_plan_info(plan) if return_info else None

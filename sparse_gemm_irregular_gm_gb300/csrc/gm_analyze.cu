@@ -182,7 +182,33 @@ __global__ void k_fill_i64(int64_t* __restrict__ dst, int64_t n, int64_t v) {
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) dst[i] = v;
 }
 
+// out[i] = in[i] widened to 64 bits.
+__global__ void k_widen_i32(const int32_t* __restrict__ in, int64_t* __restrict__ out, int64_t n) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) out[i] = in[i];
+}
+
+// out[i] = in[i] narrowed to 32 bits when it lies in [0, bound), else -1 (which
+// the index validation that follows reports; bound <= 2^31).
+__global__ void k_narrow_i64(const int64_t* __restrict__ in, int32_t* __restrict__ out, int64_t n, int64_t bound) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int64_t v = in[i];
+    out[i] = v >= 0 && v < bound ? static_cast<int32_t>(v) : -1;
+  }
+}
+
 }  // namespace
+
+void launch_widen_i32(const int32_t* in, int64_t* out, int64_t n, cudaStream_t s) {
+  if (n <= 0) return;
+  (k_widen_i32<<<grid_for(n, 256), 256, 0, s>>>(in, out, n), note_launch());
+}
+
+void launch_narrow_i64(const int64_t* in, int32_t* out, int64_t n, int64_t bound, cudaStream_t s) {
+  if (n <= 0) return;
+  (k_narrow_i64<<<grid_for(n, 256), 256, 0, s>>>(in, out, n, bound), note_launch());
+}
 
 void launch_validate_rowptr(const int64_t* rp, int64_t n_rows, int64_t nnz, int bad_bit, int* status,
                             cudaStream_t s) {

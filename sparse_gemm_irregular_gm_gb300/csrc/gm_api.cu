@@ -311,8 +311,19 @@ constexpr int kHeavyBin = 11;
 
 }  // namespace gm
 
+namespace gm {
+// A CSR operand as the path reads it: int64 row pointers, int32 columns (the
+// caller's arrays, or the plan's converted copies for other index types).
+struct CsrDev {
+  int64_t n_rows = 0, n_cols = 0, nnz = 0;
+  const int64_t* row_ptr = nullptr;
+  const int32_t* col_idx = nullptr;
+  const void* vals = nullptr;
+};
+}  // namespace gm
+
 struct gm_plan {
-  gm_csr A{}, B{};
+  gm::CsrDev A{}, B{};
   gm_config cfg{};
   cudaStream_t s = nullptr;
   int device = 0;
@@ -330,9 +341,12 @@ struct gm_plan {
   bool walk_ok = false;    // the walk pipeline applies when B is strict and the bitmaps fit
   bool walk = false;       // numeric heavy path: chunks summed straight from B's ranges (gm_walk.cu)
   bool rowexp0 = false;    // two or more levels: level 0 by the row-order expansion, no C-hat
+  int32_t index_type = 0;  // GM_INDEX_* flags of the caller's arrays
+  gm::DevBuf<int64_t> a_rp64, b_rp64, c_rp64;  // int32 row pointers widened (C: until numeric)
+  gm::DevBuf<int32_t> a_col32, b_col32;        // int64 columns narrowed
   gm_params P{};
   int L = 0;
-  int state = 0;  // 1 analyzed, 2 symbolic done, 3 numeric done
+  int state = 0;  // 1 analyzed, 2 symbolic done, 3 numeric done, 4 C.nnz does not fit int32 row pointers
   int pipeline = GM_PIPE_FUSED_HISTO;
   bool timing = false, log = false, keep = false;
   gm::DevBuf<int> status;
@@ -440,10 +454,56 @@ static bool env_log() {
   return e && e[0] == '1';
 }
 
-static gm_status check_csr(const gm_csr* M) {
+static gm_status check_csr(const gm_csr* M, int32_t index_type) {
   if (!M || M->n_rows < 0 || M->n_cols < 0 || M->nnz < 0 || !M->row_ptr) return GM_ERR_INVALID_ARG;
   if (M->nnz > 0 && (!M->col_idx || !M->vals)) return GM_ERR_INVALID_ARG;
   if (M->n_rows >= (int64_t(1) << 31) || M->n_cols > (int64_t(1) << 31)) return GM_ERR_INDEX_OVERFLOW;
+  if ((index_type & GM_INDEX_ROWPTR32) && M->nnz >= (int64_t(1) << 31)) return GM_ERR_INDEX_OVERFLOW;
+  return GM_OK;
+}
+
+// The caller's index types (gm_config.index_type) turned into the int64 row
+// pointers and int32 columns the path reads: converted copies owned by the plan,
+// one per distinct array (A and B of A*A share theirs). Out-of-range int64
+// columns become -1, which the validation in analyze_impl reports.
+static gm_status adapt_inputs(gm_plan* p, const gm_csr* A, const gm_csr* B) {
+  auto take = [](const gm_csr* M) {
+    CsrDev d;
+    d.n_rows = M->n_rows;
+    d.n_cols = M->n_cols;
+    d.nnz = M->nnz;
+    d.row_ptr = static_cast<const int64_t*>(M->row_ptr);
+    d.col_idx = static_cast<const int32_t*>(M->col_idx);
+    d.vals = M->vals;
+    return d;
+  };
+  p->A = take(A);
+  p->B = take(B);
+  const cudaStream_t s = p->s;
+  if (p->index_type & GM_INDEX_ROWPTR32) {
+    if (!p->a_rp64.alloc(A->n_rows + 1, s)) return GM_ERR_OOM;
+    launch_widen_i32(static_cast<const int32_t*>(A->row_ptr), p->a_rp64.p, A->n_rows + 1, s);
+    p->A.row_ptr = p->a_rp64.p;
+    if (B->row_ptr == A->row_ptr && B->n_rows == A->n_rows) {
+      p->B.row_ptr = p->a_rp64.p;
+    } else {
+      if (!p->b_rp64.alloc(B->n_rows + 1, s)) return GM_ERR_OOM;
+      launch_widen_i32(static_cast<const int32_t*>(B->row_ptr), p->b_rp64.p, B->n_rows + 1, s);
+      p->B.row_ptr = p->b_rp64.p;
+    }
+  }
+  if (p->index_type & GM_INDEX_COL64) {
+    if (!p->a_col32.alloc(A->nnz, s)) return GM_ERR_OOM;
+    launch_narrow_i64(static_cast<const int64_t*>(A->col_idx), p->a_col32.p, A->nnz, A->n_cols, s);
+    p->A.col_idx = p->a_col32.p;
+    if (B->col_idx == A->col_idx && B->nnz == A->nnz && B->n_cols == A->n_cols) {
+      p->B.col_idx = p->a_col32.p;
+    } else {
+      if (!p->b_col32.alloc(B->nnz, s)) return GM_ERR_OOM;
+      launch_narrow_i64(static_cast<const int64_t*>(B->col_idx), p->b_col32.p, B->nnz, B->n_cols, s);
+      p->B.col_idx = p->b_col32.p;
+    }
+  }
   return GM_OK;
 }
 
@@ -1489,15 +1549,16 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
                             gm_plan** plan_out) {
   if (!plan_out) return GM_ERR_INVALID_ARG;
   *plan_out = nullptr;
-  gm_status st = gm::check_csr(A);
-  if (st == GM_OK) st = gm::check_csr(B);
+  const int32_t index_type = cfg ? cfg->index_type : 0;
+  if (index_type & ~(GM_INDEX_ROWPTR32 | GM_INDEX_COL64)) return GM_ERR_INVALID_ARG;
+  gm_status st = gm::check_csr(A, index_type);
+  if (st == GM_OK) st = gm::check_csr(B, index_type);
   if (st != GM_OK) return st;
   if (A->n_cols != B->n_rows) return GM_ERR_DIM_MISMATCH;
   std::unique_ptr<gm_plan> p(new (std::nothrow) gm_plan);
   if (!p) return GM_ERR_OOM;
-  p->A = *A;
-  p->B = *B;
   if (cfg) p->cfg = *cfg;
+  p->index_type = index_type;
   p->s = static_cast<cudaStream_t>(stream);
   p->pipeline = p->cfg.pipeline == GM_PIPE_UNFUSED ? GM_PIPE_UNFUSED : GM_PIPE_FUSED_HISTO;  // may become ROWWISE
   p->f32 = p->cfg.value_type == GM_VALUE_F32;
@@ -1529,7 +1590,8 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
                gm::walk_fits(p->P.widths[0], p->smem_dev);
   gm::g_ws_peak = gm::g_ws_now.load();
   const int64_t l0 = gm::launch_count();
-  st = gm::analyze_impl(p.get());
+  st = gm::adapt_inputs(p.get(), A, B);
+  if (st == GM_OK) st = gm::analyze_impl(p.get());
   p->launches += gm::launch_count() - l0;
   if (p->timing) p->collect_times();
   if (st != GM_OK) {
@@ -1547,12 +1609,26 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
   return GM_OK;
 }
 
-gm_status gm_spgemm_symbolic(gm_plan* plan, int64_t* C_row_ptr, int64_t* C_nnz) {
+gm_status gm_spgemm_symbolic(gm_plan* plan, void* C_row_ptr, int64_t* C_nnz) {
   if (!plan) return GM_ERR_INVALID_ARG;
   if (plan->state != 1) return GM_ERR_STATE;
   if (!C_row_ptr) return GM_ERR_INVALID_ARG;
   const int64_t l0 = gm::launch_count();
-  gm_status st = gm::symbolic_impl(plan, C_row_ptr, C_nnz);
+  const bool rp32 = (plan->index_type & GM_INDEX_ROWPTR32) != 0;
+  gm_status st = GM_OK;
+  if (rp32 && !plan->c_rp64.alloc(plan->A.n_rows + 1, plan->s)) st = GM_ERR_OOM;
+  if (st == GM_OK)
+    st = gm::symbolic_impl(plan, rp32 ? plan->c_rp64.p : static_cast<int64_t*>(C_row_ptr), C_nnz);
+  if (st == GM_OK && rp32) {  // C.rowPtr narrowed into the caller's int32 array
+    if (plan->c_nnz >= (int64_t(1) << 31)) {
+      st = GM_ERR_INDEX_OVERFLOW;
+      plan->state = 4;  // C cannot be given in this index type: no further calls
+    } else {
+      gm::launch_narrow_i64(plan->c_rp64.p, static_cast<int32_t*>(C_row_ptr), plan->A.n_rows + 1,
+                            int64_t(1) << 31, plan->s);
+      st = gm::sync_check(plan);
+    }
+  }
   plan->launches += gm::launch_count() - l0;
   if (plan->timing) {
     cudaStreamSynchronize(plan->s);
@@ -1563,12 +1639,27 @@ gm_status gm_spgemm_symbolic(gm_plan* plan, int64_t* C_row_ptr, int64_t* C_nnz) 
   return st;
 }
 
-gm_status gm_spgemm_numeric(gm_plan* plan, int32_t* C_col_idx, void* C_vals) {
+gm_status gm_spgemm_numeric(gm_plan* plan, void* C_col_idx, void* C_vals) {
   if (!plan) return GM_ERR_INVALID_ARG;
   if (plan->state != 2) return GM_ERR_STATE;
   if (plan->c_nnz > 0 && (!C_col_idx || !C_vals)) return GM_ERR_INVALID_ARG;
   const int64_t l0 = gm::launch_count();
-  gm_status st = gm::numeric_impl(plan, C_col_idx, C_vals);
+  gm_status st = GM_OK;
+  if (plan->index_type & GM_INDEX_COL64) {  // int32 columns in a plan buffer, then widened
+    gm::DevBuf<int32_t> col32;
+    if (!col32.alloc(plan->c_nnz, plan->s)) {
+      st = GM_ERR_OOM;
+    } else {
+      st = gm::numeric_impl(plan, col32.p, C_vals);
+      if (st == GM_OK) {
+        gm::launch_widen_i32(col32.p, static_cast<int64_t*>(C_col_idx), plan->c_nnz, plan->s);
+        st = gm::sync_check(plan);
+      }
+    }
+  } else {
+    st = gm::numeric_impl(plan, static_cast<int32_t*>(C_col_idx), C_vals);
+  }
+  if (st == GM_OK) plan->c_rp64.release();
   plan->launches += gm::launch_count() - l0;
   if (plan->timing) {
     cudaStreamSynchronize(plan->s);
@@ -1603,6 +1694,7 @@ gm_status gm_spgemm_plan_info(const gm_plan* plan, gm_plan_info* out) {
   out->kernel_launches = plan->launches;
   out->value_type = plan->f32 ? GM_VALUE_F32 : GM_VALUE_F64;
   out->chunk_col_bytes = plan->arena_cb;
+  out->index_type = plan->index_type;
   return GM_OK;
 }
 

@@ -92,6 +92,10 @@ void sum_children(const int64_t* src, const int64_t* parent_slot, int64_t* dst, 
                   cudaStream_t s);
 
 // ---- analysis (gm_analyze.cu) ---------------------------------------------
+// Index-type conversions at the interface: out[i] = in[i] (int32 -> int64), and
+// int64 -> int32 with values outside [0, bound) written as -1.
+void launch_widen_i32(const int32_t* in, int64_t* out, int64_t n, cudaStream_t s);
+void launch_narrow_i64(const int64_t* in, int32_t* out, int64_t n, int64_t bound, cudaStream_t s);
 void launch_validate_rowptr(const int64_t* rp, int64_t n_rows, int64_t nnz, int bad_bit, int* status,
                             cudaStream_t s);
 void launch_validate_cols(const int32_t* col, int64_t nnz, int64_t n_cols, int bad_bit, int* status,

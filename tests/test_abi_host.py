@@ -173,3 +173,82 @@ def test_params_no_level_needed_with_small_tau(lib):
     assert (got.n_chunks_max, got.n_levels) == (ref.n_chunks_max, ref.n_levels) == (1, 0)
     with pytest.raises(binding.GmError):
         _lib_params(1 << 20, tau=16)
+
+
+def test_analyze_index_type_host_errors(lib):
+    """Unknown index flags are rejected, and int32 row pointers cannot describe a
+    matrix with 2^31 or more entries; both before any device work."""
+    fake = 0x1000  # never dereferenced
+    A = binding.gm_csr(4, 5, 3, fake, fake, fake)
+    B = binding.gm_csr(5, 5, 3, fake, fake, fake)
+    plan = ctypes.c_void_p()
+    for flags in (4, 8, -1):
+        cfg = binding.make_config(index_type=flags)
+        assert lib.gm_spgemm_analyze(ctypes.byref(A), ctypes.byref(B), ctypes.byref(cfg), None,
+                                     ctypes.byref(plan)) == 1
+    big = binding.gm_csr(4, 5, 1 << 31, fake, fake, fake)
+    cfg = binding.make_config(index_type=binding.GM_INDEX_ROWPTR32)
+    assert lib.gm_spgemm_analyze(ctypes.byref(big), ctypes.byref(B), ctypes.byref(cfg), None,
+                                 ctypes.byref(plan)) == 3
+    assert lib.gm_spgemm_analyze(ctypes.byref(A), ctypes.byref(big), ctypes.byref(cfg), None,
+                                 ctypes.byref(plan)) == 3
+    assert not plan.value
+
+
+@pytest.mark.parametrize("c_m", [1 << 10, 1 << 20, 1 << 24])
+def test_params_do_not_depend_on_index_type(lib, c_m):
+    """The planner sizes shared memory by the widths held there (int32 columns,
+    int64 row pointers), which the interface's index types do not change."""
+    ref = _lib_params(c_m)
+    for flags in (binding.GM_INDEX_ROWPTR32, binding.GM_INDEX_COL64, 3):
+        got = _lib_params(c_m, index_type=flags)
+        assert (got.tau, got.dense_width, got.n_chunks_max, got.n_levels) == \
+               (ref.tau, ref.dense_width, ref.n_chunks_max, ref.n_levels)
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """The binding's ctypes structures have the sizes and field offsets a C
+    compiler gives the header's structs."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"gm_csr": binding.gm_csr, "gm_config": binding.gm_config, "gm_params": binding.gm_params,
+               "gm_plan_info": binding.gm_plan_info}
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "gm_spgemm.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'  printf("{name} %zu\\n", sizeof({name}));')
+        for field, _ in cls._fields_:
+            lines.append(f'  printf("{name}.{field} %zu\\n", offsetof({name}, {field}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                       text=True).stdout.splitlines())
+    for name, cls in structs.items():
+        assert int(got[name]) == ctypes.sizeof(cls), name
+        for field, _ in cls._fields_:
+            assert int(got[f"{name}.{field}"]) == getattr(cls, field).offset, f"{name}.{field}"
+
+
+def test_binding_index_type_from_dtypes():
+    """The binding derives gm_config.index_type from the operands' tensor dtypes
+    and refuses mixed or unsupported ones (host logic only)."""
+    torch = pytest.importorskip("torch")
+
+    def csr(rp_dt, col_dt):
+        return binding.DeviceCSR(2, 2, torch.zeros(3, dtype=rp_dt), torch.zeros(0, dtype=col_dt),
+                                 torch.zeros(0, dtype=torch.float64))
+
+    i64, i32 = torch.int64, torch.int32
+    assert binding._index_type(csr(i64, i32), csr(i64, i32)) == 0
+    assert binding._index_type(csr(i32, i32), csr(i32, i32)) == binding.GM_INDEX_ROWPTR32
+    assert binding._index_type(csr(i64, i64), csr(i64, i64)) == binding.GM_INDEX_COL64
+    assert binding._index_type(csr(i32, i64), csr(i32, i64)) == binding.GM_INDEX_ROWPTR32 | binding.GM_INDEX_COL64
+    for a, b in ((csr(i32, i32), csr(i64, i32)), (csr(i64, i64), csr(i64, i32)), (csr(torch.int16, i32),) * 2,
+                 (csr(i64, torch.uint8),) * 2):
+        with pytest.raises(binding.GmError):
+            binding._index_type(a, b)

@@ -537,3 +537,94 @@ def test_workload_rmat20_f32_sampled():
     tau 14528, 32 level-0 chunks, sampled rows against the oracle."""
     info = _sampled_check("rmat20", n_random=150, f32=True)
     assert info.params.tau == 14528 and list(info.params.v_chunks[:1]) == [32] and info.n_heavy_rows > 0
+
+
+# --- index types (gm_config.index_type) ---------------------------------------------
+
+# (name, row-pointer dtype, column dtype) at the interface
+INDEX_TYPES = [("rowptr32", np.int32, np.int32), ("col64", np.int64, np.int64), ("both", np.int32, np.int64)]
+INDEX_PLANS = ["auto", "heavy_L0", "heavy_L2", "L2_outer", "L1_walk_128"]
+
+
+def _index_flags(rp_dt, col_dt):
+    return (binding.GM_INDEX_ROWPTR32 if rp_dt == np.int32 else 0) | (binding.GM_INDEX_COL64 if col_dt == np.int64
+                                                                    else 0)
+
+
+def _run_indexed(A, B, rp_dt, col_dt, dtype=None, **cfg):
+    Ad = binding.to_device(A, dtype=dtype, row_ptr_dtype=rp_dt, col_dtype=col_dt)
+    Bd = Ad if B is A else binding.to_device(B, dtype=dtype, row_ptr_dtype=rp_dt, col_dtype=col_dt)
+    C, info = binding.spgemm(Ad, Bd, binding.make_config(**cfg) if cfg else None, return_info=True)
+    torch.cuda.synchronize()
+    rp, col, val = C.row_ptr.cpu().numpy(), C.col.cpu().numpy(), C.val.cpu().numpy()
+    assert rp.dtype == rp_dt and col.dtype == col_dt
+    assert info.index_type == _index_flags(rp_dt, col_dt)
+    return rp, col, val, info
+
+
+@pytest.mark.parametrize("name,rp_dt,col_dt", INDEX_TYPES, ids=[t[0] for t in INDEX_TYPES])
+@pytest.mark.parametrize("plan", INDEX_PLANS)
+def test_index_types_forced_paths(name, rp_dt, col_dt, plan):
+    """int32 row pointers and int64 columns at the interface, A*A (A and B share
+    their converted copies): structure and integer values equal to the oracle's
+    through every hierarchy depth and pipeline."""
+    cfg = dict(FORCED)[plan]
+    A = gi.rmat(10, 8, seed=1, values="int")
+    rp, col, val, info = _run_indexed(A, A, rp_dt, col_dt, **cfg)
+    if plan != "auto":
+        assert info.n_heavy_rows > 0
+    assert_matches(oracle.spgemm(A, A), rp, col, val, exact=True)
+
+
+@pytest.mark.parametrize("name,rp_dt,col_dt", INDEX_TYPES, ids=[t[0] for t in INDEX_TYPES])
+def test_index_types_distinct_operands(name, rp_dt, col_dt):
+    """A*B with separate arrays (each converted on its own), unsorted rows with
+    repeated columns and explicit zeros, fp64 and float values."""
+    A = gi.random_csr(64, 90, 0.3, 7, values="int", unsorted=True, duplicates=True, explicit_zeros=True,
+                      empty_rows=0.2)
+    B = gi.random_csr(90, 70, 0.3, 8, values="int", unsorted=True, duplicates=True, explicit_zeros=True,
+                      empty_rows=0.2)
+    ref = oracle.spgemm(A, B)
+    for dtype in (None, np.float32):
+        rp, col, val, _ = _run_indexed(A, B, rp_dt, col_dt, dtype=dtype, tau=2, dense_width=4, n_chunks_max=2)
+        assert_matches(ref, rp, col, val.astype(np.float64), exact=True)
+    A, B = gi.named_pair("rmatAB_s13_a4_b8", seed=2)
+    rp, col, val, info = _run_indexed(A, B, rp_dt, col_dt)
+    assert info.n_heavy_rows > 0
+    assert_matches(oracle.spgemm(A, B), rp, col, val)
+
+
+def test_col64_columns_out_of_range_are_reported():
+    """int64 columns outside [0, n_cols) -- also ones whose low 32 bits would be in
+    range -- are reported as GM_ERR_BAD_INDEX, in A and in B."""
+    A = gi.random_csr(10, 10, 0.4, 1)
+    good = binding.to_device(A, col_dtype=np.int64)
+    for v in (10, -1, (1 << 31) + 3, (1 << 32) + 2):
+        col = A.col.astype(np.int64)
+        col[3] = v
+        bad = binding.DeviceCSR(A.n_rows, A.n_cols, good.row_ptr, torch.from_numpy(col).cuda(), good.val)
+        for lhs, rhs in ((bad, good), (good, bad)):
+            with pytest.raises(binding.GmError) as e:
+                binding.spgemm(lhs, rhs)
+            assert e.value.status == 9
+
+
+@pytest.mark.slow
+def test_rowptr32_overflow_is_reported():
+    """C = A*A of the scale-20 R-MAT has 9,708,253,274 entries: int32 row pointers
+    cannot hold C.rowPtr, so symbolic returns GM_ERR_INDEX_OVERFLOW with C.nnz on
+    the host, writes nothing, and takes no further call."""
+    import ctypes
+    A = gi.named_workload("rmat20")
+    Ad = binding.to_device(A, row_ptr_dtype=np.int32)
+    plan = binding.gm_spgemm_analyze(Ad, Ad)
+    try:
+        c_rp = torch.full((A.n_rows + 1,), -7, dtype=torch.int32, device="cuda")
+        nnz = ctypes.c_int64(-1)
+        lib = binding.load()
+        assert lib.gm_spgemm_symbolic(plan, c_rp.data_ptr(), ctypes.byref(nnz)) == 3
+        assert nnz.value == 9_708_253_274
+        assert bool((c_rp == -7).all())
+        assert lib.gm_spgemm_symbolic(plan, c_rp.data_ptr(), ctypes.byref(nnz)) == 8
+    finally:
+        binding.gm_spgemm_plan_destroy(plan)
