@@ -252,3 +252,12 @@ def test_binding_index_type_from_dtypes():
                  (csr(i64, torch.uint8),) * 2):
         with pytest.raises(binding.GmError):
             binding._index_type(a, b)
+
+
+def test_c_program_compiles_and_links_against_the_library(lib, tmp_path):
+    """A plain C program (tests/c_abi_driver.c) builds against include/gm_spgemm.h
+    and links every call it makes from libgm_spgemm.so (running it needs a GPU:
+    tests/test_gpu_parity.py::test_c_program_through_the_abi)."""
+    from tests.c_driver import build_c_driver
+    exe = build_c_driver(str(tmp_path))
+    assert os.access(exe, os.X_OK)

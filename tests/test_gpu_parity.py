@@ -628,3 +628,24 @@ def test_rowptr32_overflow_is_reported():
         assert lib.gm_spgemm_symbolic(plan, c_rp.data_ptr(), ctypes.byref(nnz)) == 8
     finally:
         binding.gm_spgemm_plan_destroy(plan)
+
+
+def test_c_program_through_the_abi(tmp_path):
+    """C = A*B computed by a plain C program (tests/c_abi_driver.c: CUDA runtime
+    copies, analyze / symbolic / numeric with a NULL config, no Python on the
+    path) matches the oracle: A*A with heavy and light rows, and a distinct A*B."""
+    import subprocess
+    from tests.c_driver import build_c_driver, read_csr, write_csr
+    exe = build_c_driver(str(tmp_path))
+    A = gi.rmat(12, 16, seed=4)
+    A2, B2 = gi.named_pair("rmatAB_s13_a4_b8", seed=2)
+    for a, b in ((A, A), (A2, B2)):
+        fa, fb, fc = (str(tmp_path / n) for n in ("a.bin", "b.bin", "c.bin"))
+        write_csr(fa, a)
+        write_csr(fb, b)
+        out = subprocess.run([exe, fa, fb, fc], capture_output=True, text=True, timeout=120)
+        assert out.returncode == 0, out.stderr
+        C = read_csr(fc)
+        assert C.row_ptr[0] == 0
+        assert_matches(oracle.spgemm(a, b), C.row_ptr, C.col, C.val)
+    assert " heavy 0 " not in out.stdout
