@@ -46,6 +46,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--pipeline", type=int, default=0)
     ap.add_argument("--dtype", choices=["f64", "f32"], default="f64", help="value type of A, B and C")
+    ap.add_argument("--index-type", choices=list(INDEX_TYPES), default="default",
+                    help="row-pointer / column types of A, B and C at the interface")
     ap.add_argument("--tau", type=int, default=0, help="plan override: heavy-row threshold")
     ap.add_argument("--n-chunks-max", type=int, default=0, help="plan override: chunks per multisplit level")
     ap.add_argument("--dense-width", type=int, default=0, help="plan override: dense accumulator width")
@@ -140,7 +142,7 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power)}
 
 
-def byte_model(info, A, nnz_c, rowwise, vb=8, cb=4):
+def byte_model(info, A, nnz_c, rowwise, vb=8, cb=4, rp_b=8, col_b=4):
     """Algorithmic bytes per step.
 
     Whole path, outer-product pipelines (the method's byte model, one multisplit
@@ -154,14 +156,15 @@ def byte_model(info, A, nnz_c, rowwise, vb=8, cb=4):
     passes carry columns only, numeric passes columns and values; the level-0
     histogram is counted inside the outer product). Element sizes are for vb-byte
     values (12 B for a column and a double, 8 B with floats); the row-order
-    pipeline stores chunk-local columns in cb bytes (2: uint16).
+    pipeline stores chunk-local columns in cb bytes (2: uint16). A and C are
+    counted at the interface's widths: rp_b bytes a row pointer, col_b a column.
     """
     e = 4 + vb
     ec = cb + vb
     ip_h = info.ip_heavy
     L = max(1, info.params.n_levels)
-    a_bytes = 8 * (A.n_rows + 1) + e * A.nnz
-    c_bytes = 8 * (A.n_rows + 1) + e * nnz_c
+    a_bytes = rp_b * (A.n_rows + 1) + (col_b + vb) * A.nnz
+    c_bytes = rp_b * (A.n_rows + 1) + (col_b + vb) * nnz_c
     if rowwise:
         b_alg = 2 * a_bytes + ip_h * (ec + 4 + ec) + c_bytes
         stages = {
@@ -285,6 +288,17 @@ def _cpu_baseline(A, B, u, target_s, seed):
                       f"{dt:.1f} s on the host cores"}
 
 
+# --index-type: (row-pointer dtype, column dtype) of the arrays handed to the library
+INDEX_TYPES = {"default": ("int64", "int32"), "rowptr32": ("int32", "int32"), "col64": ("int64", "int64"),
+               "both": ("int32", "int64")}
+
+
+def index_dtypes(args):
+    import numpy as np
+    rp, col = INDEX_TYPES[args.index_type]
+    return np.dtype(rp), np.dtype(col)
+
+
 def plan_overrides(args) -> dict:
     """gm_config fields set on the command line (zero keeps the automatic value)."""
     return {k: v for k, v in (("n_chunks_max", args.n_chunks_max), ("dense_width", args.dense_width),
@@ -293,9 +307,12 @@ def plan_overrides(args) -> dict:
 
 def workload_name(args) -> str:
     vals = "fp32 U[-1,1)" if args.dtype == "f32" else "fp64 U[-1,1)"
+    idx = "" if args.index_type == "default" else ", %s row pointers, %s columns" % INDEX_TYPES[args.index_type]
     if args.workload == "rmat20":
-        return f"A*A, A = R-MAT scale 20, edge factor 16, a=.57 b=.19 c=.19, {vals}, seed 1"
-    return args.workload if args.dtype == "f64" else f"{args.workload} ({vals})"
+        return f"A*A, A = R-MAT scale 20, edge factor 16, a=.57 b=.19 c=.19, {vals}, seed 1{idx}"
+    if args.dtype == "f64" and not idx:
+        return args.workload
+    return f"{args.workload} ({vals}{idx})"
 
 
 def make_step(A, Ad, Bd, cfg, stream):
@@ -306,9 +323,9 @@ def make_step(A, Ad, Bd, cfg, stream):
 
     def step():
         plan = binding.gm_spgemm_analyze(Ad, Bd, cfg, stream)
-        c_rp = torch.empty(A.n_rows + 1, dtype=torch.int64, device="cuda")
+        c_rp = torch.empty(A.n_rows + 1, dtype=Ad.row_ptr.dtype, device="cuda")
         nnz = binding.gm_spgemm_symbolic(plan, c_rp)
-        c_col = torch.empty(nnz, dtype=torch.int32, device="cuda")
+        c_col = torch.empty(nnz, dtype=Ad.col.dtype, device="cuda")
         c_val = torch.empty(nnz, dtype=Ad.val.dtype, device="cuda")
         binding.gm_spgemm_numeric(plan, c_col, c_val)
         info = binding.gm_spgemm_plan_info(plan)
@@ -328,8 +345,9 @@ def run_ours(args):
     A, B = inputs.named_pair(args.workload, seed=args.seed)
     vdt = np.float32 if args.dtype == "f32" else None
     vb = 4 if args.dtype == "f32" else 8
-    Ad = binding.to_device(A, dtype=vdt)
-    Bd = Ad if B is A else binding.to_device(B, dtype=vdt)
+    rp_dt, col_dt = index_dtypes(args)
+    Ad = binding.to_device(A, dtype=vdt, row_ptr_dtype=rp_dt, col_dtype=col_dt)
+    Bd = Ad if B is A else binding.to_device(B, dtype=vdt, row_ptr_dtype=rp_dt, col_dtype=col_dt)
     cfg = binding.make_config(flags=binding.GM_FLAG_TIMING, pipeline=args.pipeline, **plan_overrides(args))
     if args.dtype == "f32":
         cfg.value_type = binding.GM_VALUE_F32
@@ -375,8 +393,8 @@ def run_ours(args):
     value = world * flops / (ms / 1e3) / 1e9
     peak, peak_kind = peaks()
     b_alg, stage_bytes = byte_model(info, A, nnz_c, info.pipeline == binding.GM_PIPE_ROWWISE, vb,
-                                    info.chunk_col_bytes or 4)
-    b_method, _ = byte_model(info, A, nnz_c, False, vb)
+                                    info.chunk_col_bytes or 4, rp_dt.itemsize, col_dt.itemsize)
+    b_method, _ = byte_model(info, A, nnz_c, False, vb, 4, rp_dt.itemsize, col_dt.itemsize)
     stage_bytes["num_heavy"] += (4 + vb) * nnz_heavy + 8 * len(heavy)
     names = binding.STAGES
     stage_table = {names[i]: round(float(stage_ms[i]), 3) for i in range(len(names)) if stage_ms[i] > 0}
@@ -393,12 +411,13 @@ def run_ours(args):
                    "levels": info.params.n_levels, "chunks": list(info.params.v_chunks[:info.params.n_levels]),
                    "batches": info.n_batches, "pipeline": binding.PIPELINES[info.pipeline],
                    "plan_overrides": plan_overrides(args) or None,
+                   "index_type": None if args.index_type == "default" else args.index_type,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs and outputs larger than L2 (C alone is %.0f GB)" % ((4 + vb) * nnz_c / 1e9)},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": captured_traffic(args.workload, dom) if args.pipeline == 0 and
-                     not plan_overrides(args) and args.dtype == "f64" else None,
+                     not plan_overrides(args) and args.dtype == "f64" and args.index_type == "default" else None,
                      "traffic_note": "DRAM read + write bytes of the stage's kernels in one step (ncu, "
                                      "profiles/traffic_rmat20_ef16_AxA.json); null once they change",
                      "peak_kind": peak_kind, "alg_bytes_per_step": int(stage_bytes[dom])},
@@ -502,8 +521,9 @@ def run_e2e(args, A, cfg, stream, nnz_c, ip_total):
     import torch
 
     vb = 4 if args.dtype == "f32" else 8
-    h2d = (A.n_rows + 1) * 8 + A.nnz * (4 + vb)
-    d2h = (A.n_rows + 1) * 8 + nnz_c * (4 + vb)
+    rp_dt, col_dt = index_dtypes(args)
+    h2d = (A.n_rows + 1) * rp_dt.itemsize + A.nnz * (col_dt.itemsize + vb)
+    d2h = (A.n_rows + 1) * rp_dt.itemsize + nnz_c * (col_dt.itemsize + vb)
     avail = host_available_bytes()
     if avail is not None and d2h + h2d > 0.8 * avail:
         return {"value": None, "unit": "GFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -526,12 +546,13 @@ def _run_e2e_pinned(args, A, cfg, stream, nnz_c, ip_total, vb, h2d, d2h):
     import torch
 
     from sparse_gemm_irregular_gm_gb300 import binding
-    h_rp = torch.from_numpy(A.row_ptr).pin_memory()
-    h_col = torch.from_numpy(A.col).pin_memory()
+    rp_dt, col_dt = index_dtypes(args)
+    h_rp = torch.from_numpy(A.row_ptr.astype(rp_dt)).pin_memory()
+    h_col = torch.from_numpy(A.col.astype(col_dt)).pin_memory()
     h_val = torch.from_numpy(A.val.astype(np.float32) if vb == 4 else A.val).pin_memory()
     t0 = time.perf_counter()
-    o_rp = torch.empty(A.n_rows + 1, dtype=torch.int64, pin_memory=True)
-    o_col = torch.empty(nnz_c, dtype=torch.int32, pin_memory=True)
+    o_rp = torch.empty(A.n_rows + 1, dtype=h_rp.dtype, pin_memory=True)
+    o_col = torch.empty(nnz_c, dtype=h_col.dtype, pin_memory=True)
     o_val = torch.empty(nnz_c, dtype=h_val.dtype, pin_memory=True)
     log(f"e2e: pinned {d2h / 1e9:.1f} GB of host memory in {time.perf_counter() - t0:.1f} s")
 

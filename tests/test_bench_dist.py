@@ -70,3 +70,23 @@ def test_captured_traffic_only_while_sources_match(tmp_path, monkeypatch):
     assert bench.captured_traffic("rmat20", "multisplit") is None
     src.write_text("kernel v2")
     assert bench.captured_traffic("rmat20", "num_heavy") is None
+
+
+def test_byte_model_counts_a_and_c_at_the_interface_widths():
+    """With int32 row pointers and int64 columns the byte model counts A and C
+    (read once, written once) at those widths; the per-stage bytes, which are
+    the path's own element layouts, do not change."""
+    from types import SimpleNamespace
+    sys.path.insert(0, ROOT)
+    import bench
+    A = SimpleNamespace(n_rows=1000, nnz=16000)
+    info = SimpleNamespace(ip_heavy=10 ** 6, params=SimpleNamespace(n_levels=1))
+    nnz_c = 50000
+    base, st0 = bench.byte_model(info, A, nnz_c, True, 8, 2)
+    both, st1 = bench.byte_model(info, A, nnz_c, True, 8, 2, 4, 8)
+    # A twice (read by the count and the expansion) and C once: -4 B a row pointer, +4 B a column
+    assert both - base == 2 * (-4 * 1001 + 4 * 16000) + (-4 * 1001 + 4 * nnz_c)
+    assert st0 == st1
+    args = SimpleNamespace(index_type="both")
+    assert [d.itemsize for d in bench.index_dtypes(args)] == [4, 8]
+    assert set(bench.INDEX_TYPES) == {"default", "rowptr32", "col64", "both"}
