@@ -261,3 +261,21 @@ def test_c_program_compiles_and_links_against_the_library(lib, tmp_path):
     from tests.c_driver import build_c_driver
     exe = build_c_driver(str(tmp_path))
     assert os.access(exe, os.X_OK)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without the CUDA library the binding raises when it loads: there is no CPU
+    fallback (run in a fresh interpreter, since a loaded library is cached)."""
+    import subprocess
+    import sys
+    code = ("import sys\n"
+            f"sys.path.insert(0, {ROOT!r})\n"
+            "from sparse_gemm_irregular_gm_gb300 import binding\n"
+            "try:\n"
+            f"    binding.load({str(tmp_path / 'absent.so')!r})\n"
+            "except RuntimeError as e:\n"
+            "    print('raised:', e)\n"
+            "    sys.exit(3)\n")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 3, r.stdout + r.stderr
+    assert "missing" in r.stdout
