@@ -167,7 +167,8 @@ typedef struct gm_plan_info {
   int64_t ip_total;            /* sum of u(i): intermediate products    */
   int64_t ip_heavy;            /* C-hat.nnz                             */
   int64_t c_nnz;               /* -1 before symbolic                    */
-  int64_t chat_bytes;          /* C-hat size (col + val) in bytes       */
+  int64_t chat_bytes;          /* C-hat size in bytes: an int32 column and a value a
+                                  product (12 bytes with double values, 8 with float) */
   int64_t n_batches;           /* heavy-row batches under the workspace cap */
   int64_t workspace_peak_bytes;
   int64_t n_leaves;            /* chunks accumulated                    */

@@ -1682,7 +1682,7 @@ gm_status gm_spgemm_plan_info(const gm_plan* plan, gm_plan_info* out) {
   out->ip_total = plan->ip_total;
   out->ip_heavy = plan->ip_heavy;
   out->c_nnz = plan->c_nnz;
-  out->chat_bytes = plan->ip_heavy * 12;
+  out->chat_bytes = plan->ip_heavy * (4 + plan->vb);  // int32 column + value a product
   out->n_batches = plan->n_batches;
   out->workspace_peak_bytes = plan->ws_peak;
   out->n_leaves = plan->n_leaves;
