@@ -22,7 +22,8 @@
  *     sorted and may repeat a column; repeated entries add.
  *   - Pointers documented "device" must be device (or managed) memory of the
  *     current CUDA device; "host" pointers are ordinary host memory.
- *   - Every call returns a gm_status; nothing is thrown across the ABI. A call
+ *   - Every call but gm_spgemm_plan_destroy, gm_set_allocator and
+ *     gm_status_string returns a gm_status; nothing is thrown across the ABI. A call
  *     made out of order returns GM_ERR_STATE and leaves the plan unchanged.
  *   - Work is issued on the stream given to gm_spgemm_analyze (a cudaStream_t;
  *     NULL is the legacy default stream). Calls block the host only where a
