@@ -181,6 +181,27 @@ def test_stage1_counts_partition_and_chat_rowptr():
         binding.gm_spgemm_plan_destroy(plan)
 
 
+def test_heavy_threshold_is_strict():
+    """A row whose intermediate products equal tau exactly is light: heavy means
+    exceeding tau (gMAGNUS Sec. I, Sec. II-B). tau is set to a product count that
+    occurs; the partition is checked against the rows with u > tau and the
+    product against the oracle."""
+    A = gi.rmat(10, 8, seed=2)
+    u = oracle.ip_counts(A, A)
+    cand = np.unique(u[(u >= 64) & (u <= 2000)])
+    tau = int(cand[len(cand) // 2])
+    assert (u == tau).any()
+    plan, keep = _analyze_keep(A, A, tau=tau)
+    try:
+        heavy = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_HEAVY_ROWS)
+        np.testing.assert_array_equal(heavy, np.nonzero(u > tau)[0])
+        assert not np.isin(np.nonzero(u == tau)[0], heavy).any()
+    finally:
+        binding.gm_spgemm_plan_destroy(plan)
+    info = check_full(A, A, tau=tau)
+    assert info.n_heavy_rows == int((u > tau).sum()) > 0
+
+
 def _run_symbolic(plan, n_rows):
     rp = torch.empty(n_rows + 1, dtype=torch.int64, device="cuda")
     return binding.gm_spgemm_symbolic(plan, rp)
