@@ -1453,6 +1453,7 @@ static gm_status run_heavy_walk(gm_plan* p, int32_t* c_col, void* c_val) {
   DevBuf<int64_t> starts_d, items;
   if (!cls.alloc(n, s) || !idx.alloc(n, s) || !starts_d.alloc(kClasses + 1, s) || !items.alloc(n, s))
     return GM_ERR_OOM;
+  if (!p->leaf_nnz.p) return GM_ERR_OOM;  // the symbolic pass could not keep the chunks' nnz
   launch_walk_class(p->leaf_nnz.p, nh, v, cls.p, s);
   if (!partition_by_bin(cls.p, n, kClasses, idx.p, starts_d.p, s)) return GM_ERR_OOM;
   int64_t starts[kClasses + 1];
