@@ -301,3 +301,65 @@ def test_fig1_result():
     assert heavy.tolist() == g["heavy_rows"] and light.tolist() == [0]
     p = oracle.magnus_params(g["C_m"], dense_width=4, n_chunks_max=2, tau=2)
     assert p.v_chunks == [g["n_chunks"]] and p.widths == [g["chunk_width"]]
+
+
+# --- intermediate matrices: C-hat and the chunk split, on random inputs ---------
+
+@pytest.mark.parametrize("seed", range(4))
+def test_expand_rows_against_dense_and_counts(seed):
+    """C-hat rows (Sec. II-C Eq. (2)): row i holds u(i) elements (the count of
+    the C-hat size formula), and summing its elements by column gives row i of
+    the dense product A @ B, over exactly the columns the pattern product
+    reaches."""
+    A = gi.random_csr(12, 15, 0.3, seed, values="int", unsorted=True, duplicates=True, empty_rows=0.2)
+    B = gi.random_csr(15, 40, 0.25, seed + 100, values="int", unsorted=True, duplicates=True, empty_rows=0.2)
+    rows = list(range(A.n_rows))
+    ex = oracle.expand_rows(A, B, rows)
+    u = oracle.ip_counts(A, B)
+    D = dense(A) @ dense(B)
+    reach = (pattern(A) @ pattern(B)) > 0
+    for i, items in zip(rows, ex):
+        assert len(items) == u[i]
+        acc = np.zeros(B.n_cols)
+        seen = np.zeros(B.n_cols, dtype=bool)
+        for c, v in items:
+            acc[c] += v
+            seen[c] = True
+        np.testing.assert_array_equal(seen, reach[i])
+        np.testing.assert_array_equal(acc, D[i])
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_split_chunks_partitions_a_row(seed):
+    """The chunk split (Sec. III-C): every element lands in the chunk of its
+    column range with a chunk-local column below the width, nothing is lost or
+    duplicated, and restoring c * width + local gives the row back."""
+    rng = np.random.default_rng(seed)
+    width, n_chunks = 16, 8
+    items = [(int(c), float(v)) for c, v in zip(rng.integers(0, width * n_chunks, 300), rng.normal(size=300))]
+    chunks = oracle.split_chunks(items, n_chunks, width)
+    assert len(chunks) == n_chunks
+    assert sum(len(ch) for ch in chunks) == len(items)
+    back = []
+    for c, ch in enumerate(chunks):
+        for local, v in ch:
+            assert 0 <= local < width
+            back.append((c * width + local, v))
+    assert sorted(back) == sorted(items)
+    with pytest.raises(ValueError):
+        oracle.split_chunks([(width * n_chunks, 1.0)], n_chunks, width)
+
+
+def test_split_chunks_two_levels_equal_one_finer_split():
+    """Hierarchy of chunks (Fig. 1, Sec. III-C): splitting a row into v0 chunks
+    of width w0 and each of those into v1 chunks of width w0 / v1 yields the same
+    element sets, with the same local columns, as one split into v0 * v1 chunks of
+    width w0 / v1, chunk c0 * v1 + c1."""
+    rng = np.random.default_rng(7)
+    v0, v1, w1 = 4, 8, 32
+    w0 = v1 * w1
+    items = [(int(c), float(i)) for i, c in enumerate(rng.integers(0, v0 * w0, 2000))]
+    fine = oracle.split_chunks(items, v0 * v1, w1)
+    for c0, ch in enumerate(oracle.split_chunks(items, v0, w0)):
+        for c1, sub in enumerate(oracle.split_chunks(ch, v1, w1)):
+            assert sorted(sub) == sorted(fine[c0 * v1 + c1])
