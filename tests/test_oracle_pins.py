@@ -3,7 +3,8 @@
 Each test fixes the oracle to something independent of its own code: dense
 brute force on tiny inputs, matrix identities, a closed form (the 13-point
 stencil of the squared 5-point Laplacian; the C-hat size formula), the worked
-example printed in gMAGNUS Fig. 1 and the chunk counts printed in Tables V/VI.
+example printed in gMAGNUS Fig. 1, the chunk counts printed in Tables V/VI, and
+the partition and nesting properties any column-range split must have.
 """
 import json
 import os
