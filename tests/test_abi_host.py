@@ -279,3 +279,18 @@ def test_missing_library_fails_loudly(tmp_path):
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
     assert r.returncode == 3, r.stdout + r.stderr
     assert "missing" in r.stdout
+
+
+def test_params_at_the_widest_products(lib):
+    """C.m = 2^31 (the widest C the interface takes) gets the oracle's plan, three
+    levels of 256, 256 and 2 chunks at 227 KB; the planner's chunk space ends at
+    D * n_chunksRequired = 2^32 columns, beyond which it reports an overflow."""
+    for c_m in (1 << 31, 1 << 32):
+        got, ref = _lib_params(c_m), oracle.magnus_params(c_m)
+        assert got.n_levels == ref.n_levels == 3
+        assert list(got.v_chunks[:3]) == list(ref.v_chunks)
+    assert list(_lib_params(1 << 31).v_chunks[:3]) == [256, 256, 2]
+    for c_m in ((1 << 32) + 1, 1 << 40):
+        with pytest.raises(binding.GmError) as e:
+            _lib_params(c_m)
+        assert e.value.status == 3
