@@ -184,18 +184,19 @@ def test_stage1_counts_partition_and_chat_rowptr():
 def test_heavy_threshold_is_strict():
     """A row whose intermediate products equal tau exactly is light: heavy means
     exceeding tau (gMAGNUS Sec. I, Sec. II-B). tau is set to a product count that
-    occurs; the partition is checked against the rows with u > tau and the
+    occurs; the partition is checked against the oracle's ThreshPartition and the
     product against the oracle."""
     A = gi.rmat(10, 8, seed=2)
     u = oracle.ip_counts(A, A)
     cand = np.unique(u[(u >= 64) & (u <= 2000)])
     tau = int(cand[len(cand) // 2])
     assert (u == tau).any()
+    ref_heavy, ref_light = oracle.thresh_partition(u, tau)
     plan, keep = _analyze_keep(A, A, tau=tau)
     try:
         heavy = binding.gm_spgemm_debug_copy(plan, binding.GM_DBG_HEAVY_ROWS)
-        np.testing.assert_array_equal(heavy, np.nonzero(u > tau)[0])
-        assert not np.isin(np.nonzero(u == tau)[0], heavy).any()
+        np.testing.assert_array_equal(heavy, ref_heavy)
+        assert np.isin(np.nonzero(u == tau)[0], ref_light).all()
     finally:
         binding.gm_spgemm_plan_destroy(plan)
     info = check_full(A, A, tau=tau)

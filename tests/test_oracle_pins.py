@@ -304,6 +304,28 @@ def test_fig1_result():
     assert p.v_chunks == [g["n_chunks"]] and p.widths == [g["chunk_width"]]
 
 
+def test_heavy_means_exceeding_tau():
+    """A row is heavy only when its products exceed tau (gMAGNUS Sec. I and
+    Sec. II-B: the rows whose intermediate products do not fit the local-memory
+    accumulator of capacity tau). A row with exactly tau products still fits, so
+    it is light; a ">=" test would call it heavy. The Fig. 1 rows have u = 7 and
+    u = 3, so tau = 3 and tau = 7 each put one row exactly on the threshold."""
+    g, A, B, _ = _fig1()
+    u = oracle.ip_counts(A, B)
+    assert u.tolist() == [0, 7, 3]
+    heavy, light = oracle.thresh_partition(u, 3)
+    assert heavy.tolist() == [1] and light.tolist() == [0, 2]
+    heavy, light = oracle.thresh_partition(u, 7)
+    assert heavy.tolist() == [] and light.tolist() == [0, 1, 2]
+    heavy, light = oracle.thresh_partition(u, 6)
+    assert heavy.tolist() == [1] and light.tolist() == [0, 2]
+    # every row lands in exactly one of the two lists, order preserved
+    for tau in range(0, 9):
+        heavy, light = oracle.thresh_partition(u, tau)
+        assert sorted(heavy.tolist() + light.tolist()) == [0, 1, 2]
+        assert heavy.tolist() == sorted(heavy.tolist()) and light.tolist() == sorted(light.tolist())
+
+
 # --- intermediate matrices: C-hat and the chunk split, on random inputs ---------
 
 @pytest.mark.parametrize("seed", range(4))
