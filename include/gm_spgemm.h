@@ -52,7 +52,10 @@ typedef enum gm_status {
   GM_ERR_CUDA = 6,            /* a CUDA call failed; see gm_plan_info.cuda_error */
   GM_ERR_DEVICE_TIMEOUT = 7,  /* a bounded device-side wait gave up              */
   GM_ERR_STATE = 8,           /* call out of order (analyze, symbolic, numeric)  */
-  GM_ERR_BAD_INDEX = 9        /* a column index out of range, found on device    */
+  GM_ERR_BAD_INDEX = 9,       /* a column index out of range, found on device    */
+  GM_ERR_INTERNAL = 10        /* a device-side consistency check of the library
+                                 failed (a bug in this library, not in the input or
+                                 the driver); gm_plan_info.device_status holds the bits */
 } gm_status;
 
 /* A CSR matrix. The library only reads these arrays; they stay owned by the
@@ -89,6 +92,10 @@ typedef struct gm_csr {
 #define GM_FLAG_TIMING 1             /* record per-stage device times (gm_plan_info.stage_ms) */
 #define GM_FLAG_KEEP_INTERMEDIATES 2 /* keep C-hat / C-hat_reord of a single batch for gm_spgemm_debug_copy */
 #define GM_FLAG_LOG 4                /* print the plan to stderr (also env GM_SPGEMM_LOG=1) */
+#define GM_FLAG_OVERLAP 8            /* light rows on a second stream, concurrently with the heavy rows
+                                        (gMAGNUS Algorithm 3 runs its light and heavy queues at once);
+                                        the plan creates the stream and joins it into the plan's stream
+                                        before C.rowPtr is scanned and before numeric returns */
 
 /* Heavy-path pipelines for gm_config.pipeline. */
 #define GM_PIPE_AUTO 0        /* GM_PIPE_ROWWISE when it applies, else GM_PIPE_FUSED_HISTO */
@@ -98,14 +105,6 @@ typedef struct gm_csr {
                                  (C-hat is not written); with one level the chunk sizes come from the
                                  symbolic pass, with more (GM_PIPE_AUTO, B rows sorted, at most 64
                                  level-0 chunks) the chunks then go through the multisplit levels */
-#define GM_PIPE_WALK 4        /* double values, one level only, rows of B with strictly increasing
-                                 columns: each heavy row's level-0 chunk is summed straight from the
-                                 ranges of the B rows
-                                 that fall into it (neither C-hat nor chunk lists are written); the
-                                 symbolic pass keeps the heavy rows' bitmaps (C.m / 8 bytes a row) until
-                                 numeric, when they take at most a quarter of the free workspace;
-                                 otherwise GM_PIPE_ROWWISE runs. Requested only: on the scale-20
-                                 R-MAT it is slower than GM_PIPE_ROWWISE */
 
 /* Tuning and test overrides; zero selects the automatic value for every field.
  * Overrides change how the work is split, never the result. A NULL config is
@@ -116,7 +115,7 @@ typedef struct gm_config {
   int64_t dense_width;         /* last-level chunk width (power of two); 0 = derived           */
   int64_t n_chunks_max;        /* chunks per multisplit level (power of two >= 2); 0 = Eq. (6) */
   int64_t workspace_cap_bytes; /* cap on heavy-path workspace; 0 = free memory minus a reserve  */
-  int32_t pipeline;            /* GM_PIPE_*                                                    */
+  int32_t pipeline;            /* GM_PIPE_*; another value is GM_ERR_INVALID_ARG               */
   int32_t flags;               /* GM_FLAG_*                                                    */
   int32_t value_type;          /* GM_VALUE_*: element type of A.vals, B.vals and C's values    */
   int32_t index_type;          /* GM_INDEX_* flags: row-pointer and column types of A, B and C */
@@ -223,6 +222,48 @@ gm_status gm_spgemm_params(int64_t c_m, const gm_config* cfg, gm_params* out);
 gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* cfg, void* stream,
                             gm_plan** plan_out);
 
+/* gm_spgemm_analyze for the rows [row_begin, row_end) of A only: the plan computes
+ * those rows of C = A * B (C.rowPtr then has row_end - row_begin + 1 entries and
+ * starts at 0; gm_row_ptr_shift places it inside a larger C). A's row pointers
+ * are validated whole first; the range's row pointers are copied and rebased by
+ * the plan, its columns and values read in place. B is used whole. This is the
+ * per-GPU part of a product split by rows over several GPUs (gm_spgemm_row_split);
+ * the gMAGNUS paper runs on one GPU and has no such split.
+ * Errors: those of gm_spgemm_analyze, and GM_ERR_INVALID_ARG unless
+ * 0 <= row_begin <= row_end <= A.n_rows. */
+gm_status gm_spgemm_analyze_rows(const gm_csr* A, const gm_csr* B, int64_t row_begin, int64_t row_end,
+                                 const gm_config* cfg, void* stream, gm_plan** plan_out);
+
+/* Split of A's rows into n_parts consecutive ranges with about equal work, for
+ * running one product on n_parts GPUs (one process a GPU, each holding A and B):
+ * the work of a row is its intermediate products u(i) (gMAGNUS Sec. III-A, the
+ * quantity the method's cost follows); with S(r) the products of rows [0, r) and
+ * T = S(A.n_rows), bounds[q] (host, n_parts + 1 entries) is 0 for q = 0, A.n_rows
+ * for q = n_parts, and otherwise the row r at which n_parts * S(r) comes nearest
+ * to q * T (of the last r below q * T and the first r reaching it, the nearer one,
+ * the lower on a tie), so part q, rows [bounds[q], bounds[q+1]), holds T / n_parts
+ * products give or take one row's. Without any products the rows are split
+ * evenly (bounds[q] = q * A.n_rows / n_parts, rounded down). The paper runs on
+ * one GPU and has no such split. A and B are validated as in gm_spgemm_analyze.
+ * Blocks until bounds is written. Workspace: 17 bytes a row of A, taken through
+ * the allocator hooks and returned before the call returns.
+ * Errors: those of gm_spgemm_analyze; GM_ERR_INVALID_ARG also for bounds NULL or
+ * n_parts outside [1, 2^20]. */
+gm_status gm_spgemm_row_split(const gm_csr* A, const gm_csr* B, const gm_config* cfg, int64_t n_parts,
+                              void* stream, int64_t* bounds);
+
+/* Adds base to the n entries of a row-pointer array (device; int64, or int32 with
+ * GM_INDEX_ROWPTR32 in index_type): places the C.rowPtr of one row range (which
+ * starts at 0) inside the C of the whole product, whose entries before the range
+ * number base. Stream-ordered on stream; with int32 row pointers the call first
+ * reads the array's last entry (blocking) and returns GM_ERR_INDEX_OVERFLOW when
+ * base plus it does not fit int32, changing nothing. The paper has no counterpart
+ * (it runs on one GPU).
+ * Errors: GM_ERR_INVALID_ARG (n < 0, base < 0, NULL row_ptr with n > 0, unknown
+ * index flags), GM_ERR_INDEX_OVERFLOW, GM_ERR_CUDA (a launch failed, or a CUDA
+ * error from earlier work was still pending: left pending, nothing queued). */
+gm_status gm_row_ptr_shift(void* row_ptr, int64_t n, int64_t base, int32_t index_type, void* stream);
+
 /* Algorithm 3 lines 7-25. Writes C.rowPtr (device, A.n_rows + 1 row pointers of
  * the plan's index type, caller allocated) and *C_nnz (host). Heavy rows go
  * through the outer product and the hierarchical multisplit in batches that fit
@@ -230,7 +271,7 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
  * Blocks until C.rowPtr is written and C.nnz is on the host.
  * Errors: GM_ERR_STATE (not right after analyze), GM_ERR_INVALID_ARG,
  * GM_ERR_WORKSPACE (a single heavy row does not fit the cap), GM_ERR_OOM,
- * GM_ERR_CUDA, GM_ERR_DEVICE_TIMEOUT, GM_ERR_INDEX_OVERFLOW (GM_INDEX_ROWPTR32
+ * GM_ERR_CUDA, GM_ERR_DEVICE_TIMEOUT, GM_ERR_INTERNAL, GM_ERR_INDEX_OVERFLOW (GM_INDEX_ROWPTR32
  * and C.nnz above 2^31 - 1: *C_nnz holds C.nnz, C_row_ptr is not written and
  * the plan takes no further symbolic or numeric call). */
 gm_status gm_spgemm_symbolic(gm_plan* plan, void* C_row_ptr, int64_t* C_nnz);
@@ -240,7 +281,7 @@ gm_status gm_spgemm_symbolic(gm_plan* plan, void* C_row_ptr, int64_t* C_nnz);
  * caller allocated after gm_spgemm_symbolic; each row sorted by column. Returns
  * once the work is issued and has completed (stream synchronised).
  * Errors: GM_ERR_STATE (symbolic not done, or numeric already done),
- * GM_ERR_INVALID_ARG, GM_ERR_WORKSPACE, GM_ERR_OOM, GM_ERR_CUDA. */
+ * GM_ERR_INVALID_ARG, GM_ERR_WORKSPACE, GM_ERR_OOM, GM_ERR_CUDA, GM_ERR_INTERNAL. */
 gm_status gm_spgemm_numeric(gm_plan* plan, void* C_col_idx, void* C_vals);
 
 /* Copies the plan's parameters, sizes and statistics (gMAGNUS Tables V/VI:
@@ -287,12 +328,15 @@ gm_status gm_spgemm_debug_copy(const gm_plan* plan, int view, int level, void* d
  * Scratch: a fixed array inside the library, 65,600 int64 (about 525 KB) on every
  * device that loads the library, held until the process exits. Largest n:
  * 134,217,728 (2^27); larger n returns GM_ERR_WORKSPACE and queues nothing.
- * The first call on a device looks the array's device address up (make that
- * first call before any stream capture). Every call shares the array: calls whose
+ * The first call on a device looks the array's device address up, and so does
+ * the first call after the device's context was replaced (cudaDeviceReset): make
+ * that call before any stream capture. Every call shares the array: calls whose
  * work overlaps on the GPU race, so serialise them. Nothing needs clearing
  * between calls.
  * Errors: GM_ERR_INVALID_ARG (n < 0, or NULL in/out with n > 0), GM_ERR_WORKSPACE
- * (n too large), GM_ERR_CUDA (the device lookup or a launch failed). */
+ * (n too large), GM_ERR_CUDA (the device lookup or a launch of this call failed,
+ * or a CUDA error from earlier work was still pending: that one is left pending
+ * for its owner and nothing is queued). */
 gm_status gm_prefix_sum_noalloc(const int64_t* in, int64_t* out, int64_t n, int64_t* total, void* stream);
 
 #ifdef __cplusplus

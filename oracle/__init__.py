@@ -14,6 +14,9 @@ Matrices via Hierarchical Multisplit"):
   (InterOffsets); the same closed form is SparseDitto "SpGEMM" Eq. (1).
 * ``thresh_partition`` -- heavy rows are those whose u(i) exceeds tau, Sec. III-A
   (Algorithm 3, ThreshPartition), order preserved.
+* ``row_split``        -- consecutive row ranges of about equal intermediate
+  products, for one product spread over several GPUs (not in the pages, which
+  run on one GPU; the balance follows the u(i) of Sec. III-A).
 * ``magnus_params``    -- Sec. III-D, Eqs. (4)-(7): tau, dense width, required
   and maximum chunk counts, number of levels and chunks per level.
 * ``expand_rows``      -- the intermediate matrix C-hat of the heavy rows as a
@@ -156,6 +159,40 @@ def thresh_partition(u: np.ndarray, tau: int):
     heavy = np.nonzero(u > tau)[0].astype(np.int64)
     light = np.nonzero(u <= tau)[0].astype(np.int64)
     return heavy, light
+
+
+# ---------------------------------------------------------------------------
+# Row split over several GPUs (the pages run on one GPU; see row_split)
+# ---------------------------------------------------------------------------
+
+def row_split(u: np.ndarray, n_parts: int) -> np.ndarray:
+    """Bounds of n_parts consecutive row ranges with about equal products.
+
+    The pages measure one GPU only; spreading one product over several takes a
+    split of A's rows, and the plainest one balances the quantity the method's
+    work follows, the intermediate products u(i) of each row (Sec. III-A). With
+    S(r) = u(0) + ... + u(r-1) and T = S(n): bounds[0] = 0, bounds[n_parts] = n,
+    and bounds[q] is the r at which n_parts * S(r) is nearest to q * T, taken
+    between the last r below q * T and the first r reaching it (the lower one on
+    a tie). Without products the rows are split evenly: q * n // n_parts.
+    Exact integer arithmetic (Python ints)."""
+    u = [int(x) for x in np.asarray(u, dtype=np.int64)]
+    n = len(u)
+    S = [0]
+    for x in u:
+        S.append(S[-1] + x)
+    T = S[-1]
+    bounds = [0]
+    for q in range(1, n_parts):
+        if T == 0:
+            bounds.append(q * n // n_parts)
+            continue
+        want = q * T
+        first = next(r for r in range(n + 1) if n_parts * S[r] >= want)
+        below, above = want - n_parts * S[first - 1], n_parts * S[first] - want
+        bounds.append(first - 1 if below <= above else first)
+    bounds.append(n)
+    return np.asarray(bounds, dtype=np.int64)
 
 
 # ---------------------------------------------------------------------------

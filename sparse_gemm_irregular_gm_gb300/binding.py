@@ -16,15 +16,15 @@ LIB_PATH = os.path.join(HERE, "libgm_spgemm.so")
 GM_MAX_LEVELS = 16
 GM_NUM_STAGES = 16
 STATUS_NAMES = ["GM_OK", "GM_ERR_INVALID_ARG", "GM_ERR_DIM_MISMATCH", "GM_ERR_INDEX_OVERFLOW", "GM_ERR_OOM",
-                "GM_ERR_WORKSPACE", "GM_ERR_CUDA", "GM_ERR_DEVICE_TIMEOUT", "GM_ERR_STATE", "GM_ERR_BAD_INDEX"]
-GM_FLAG_TIMING, GM_FLAG_KEEP_INTERMEDIATES, GM_FLAG_LOG = 1, 2, 4
+                "GM_ERR_WORKSPACE", "GM_ERR_CUDA", "GM_ERR_DEVICE_TIMEOUT", "GM_ERR_STATE", "GM_ERR_BAD_INDEX",
+                "GM_ERR_INTERNAL"]
+GM_FLAG_TIMING, GM_FLAG_KEEP_INTERMEDIATES, GM_FLAG_LOG, GM_FLAG_OVERLAP = 1, 2, 4, 8
 GM_VALUE_F64, GM_VALUE_F32 = 0, 1
 GM_INDEX_ROWPTR32, GM_INDEX_COL64 = 1, 2
-GM_PIPE_AUTO, GM_PIPE_UNFUSED, GM_PIPE_FUSED_HISTO, GM_PIPE_ROWWISE, GM_PIPE_WALK = 0, 1, 2, 3, 4
+GM_PIPE_AUTO, GM_PIPE_UNFUSED, GM_PIPE_FUSED_HISTO, GM_PIPE_ROWWISE = 0, 1, 2, 3
 PIPELINES = {GM_PIPE_AUTO: "auto", GM_PIPE_UNFUSED: "outer-product, unfused",
              GM_PIPE_FUSED_HISTO: "outer-product, fused level-0 histogram",
-             GM_PIPE_ROWWISE: "direct to level-0 chunks (C-hat not written)",
-             GM_PIPE_WALK: "level-0 chunks summed from B's ranges (no C-hat, no chunk lists)"}
+             GM_PIPE_ROWWISE: "direct to level-0 chunks (C-hat not written)"}
 (GM_DBG_IP_COUNTS, GM_DBG_HEAVY_ROWS, GM_DBG_LIGHT_ROWS, GM_DBG_CHAT_ROWPTR, GM_DBG_CHAT_COL, GM_DBG_CHAT_VAL,
  GM_DBG_REORD_ROWPTR, GM_DBG_REORD_COL, GM_DBG_REORD_VAL, GM_DBG_REORD_CHILD) = range(10)
 STAGES = ["analyze", "transpose", "outer", "histogram", "multisplit", "sym_heavy", "sym_light", "scan",
@@ -32,7 +32,7 @@ STAGES = ["analyze", "transpose", "outer", "histogram", "multisplit", "sym_heavy
           "unused"]
 EXPORTS = ["gm_set_allocator", "gm_spgemm_params", "gm_spgemm_analyze", "gm_spgemm_symbolic", "gm_spgemm_numeric",
            "gm_spgemm_plan_info", "gm_spgemm_plan_destroy", "gm_status_string", "gm_spgemm_debug_copy",
-           "gm_prefix_sum_noalloc"]
+           "gm_prefix_sum_noalloc", "gm_spgemm_analyze_rows", "gm_spgemm_row_split", "gm_row_ptr_shift"]
 
 
 class gm_csr(ctypes.Structure):
@@ -105,6 +105,15 @@ def load(path: str = LIB_PATH):
     lib.gm_spgemm_debug_copy.restype = ctypes.c_int
     lib.gm_spgemm_debug_copy.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                          ctypes.c_int64, P(ctypes.c_int64)]
+    lib.gm_spgemm_analyze_rows.restype = ctypes.c_int
+    lib.gm_spgemm_analyze_rows.argtypes = [P(gm_csr), P(gm_csr), ctypes.c_int64, ctypes.c_int64, P(gm_config),
+                                           ctypes.c_void_p, P(ctypes.c_void_p)]
+    lib.gm_spgemm_row_split.restype = ctypes.c_int
+    lib.gm_spgemm_row_split.argtypes = [P(gm_csr), P(gm_csr), P(gm_config), ctypes.c_int64, ctypes.c_void_p,
+                                        P(ctypes.c_int64)]
+    lib.gm_row_ptr_shift.restype = ctypes.c_int
+    lib.gm_row_ptr_shift.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                     ctypes.c_void_p]
     lib.gm_prefix_sum_noalloc.restype = ctypes.c_int
     lib.gm_prefix_sum_noalloc.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                                           ctypes.c_void_p]
@@ -255,11 +264,8 @@ def _stream_handle(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def gm_spgemm_analyze(A: DeviceCSR, B: DeviceCSR, cfg: gm_config | None = None, stream=None):
-    """gm_spgemm_analyze with cfg.value_type and cfg.index_type taken from the
-    operands' tensor dtypes."""
-    plan = ctypes.c_void_p()
-    a, b = A.desc(), B.desc()
+def _typed_config(A: DeviceCSR, B: DeviceCSR, cfg: gm_config | None):
+    """cfg (or None) with value_type and index_type taken from the operands' tensor dtypes."""
     vt = _value_type(A, B)
     it = _index_type(A, B)
     if cfg is None and (vt != GM_VALUE_F64 or it != 0):
@@ -268,9 +274,45 @@ def gm_spgemm_analyze(A: DeviceCSR, B: DeviceCSR, cfg: gm_config | None = None, 
         cfg = gm_config.from_buffer_copy(cfg)
         cfg.value_type = vt
         cfg.index_type = it
-    _check(load().gm_spgemm_analyze(ctypes.byref(a), ctypes.byref(b), ctypes.byref(cfg) if cfg else None,
-                                    _stream_handle(stream), ctypes.byref(plan)), "gm_spgemm_analyze")
+    return cfg
+
+
+def gm_spgemm_analyze(A: DeviceCSR, B: DeviceCSR, cfg: gm_config | None = None, stream=None, rows=None):
+    """gm_spgemm_analyze (or, with rows = (row_begin, row_end), gm_spgemm_analyze_rows)
+    with cfg.value_type and cfg.index_type taken from the operands' tensor dtypes."""
+    plan = ctypes.c_void_p()
+    a, b = A.desc(), B.desc()
+    cfg = _typed_config(A, B, cfg)
+    c = ctypes.byref(cfg) if cfg else None
+    if rows is None:
+        _check(load().gm_spgemm_analyze(ctypes.byref(a), ctypes.byref(b), c, _stream_handle(stream),
+                                        ctypes.byref(plan)), "gm_spgemm_analyze")
+    else:
+        _check(load().gm_spgemm_analyze_rows(ctypes.byref(a), ctypes.byref(b), int(rows[0]), int(rows[1]), c,
+                                             _stream_handle(stream), ctypes.byref(plan)), "gm_spgemm_analyze_rows")
     return plan
+
+
+def gm_spgemm_row_split(A: DeviceCSR, B: DeviceCSR, n_parts: int, cfg: gm_config | None = None, stream=None):
+    """Row bounds (numpy int64, n_parts + 1) of a split of A's rows into parts of about equal products."""
+    import numpy as np
+    a, b = A.desc(), B.desc()
+    cfg = _typed_config(A, B, cfg)
+    out = np.zeros(int(n_parts) + 1, dtype=np.int64)
+    _check(load().gm_spgemm_row_split(ctypes.byref(a), ctypes.byref(b), ctypes.byref(cfg) if cfg else None,
+                                      int(n_parts), _stream_handle(stream),
+                                      out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))), "gm_spgemm_row_split")
+    return out
+
+
+def gm_row_ptr_shift(row_ptr, base: int, stream=None):
+    """Adds base to every entry of a CUDA row-pointer tensor (int64 or int32), in place."""
+    import torch
+    if row_ptr.dtype not in (torch.int64, torch.int32) or not row_ptr.is_contiguous() or not row_ptr.is_cuda:
+        raise ValueError("row_ptr must be a contiguous int64 or int32 CUDA tensor")
+    it = GM_INDEX_ROWPTR32 if row_ptr.dtype == torch.int32 else 0
+    _check(load().gm_row_ptr_shift(row_ptr.data_ptr() if row_ptr.numel() else None, row_ptr.numel(), int(base),
+                                   it, _stream_handle(stream)), "gm_row_ptr_shift")
 
 
 def gm_spgemm_symbolic(plan, c_row_ptr) -> int:
@@ -310,20 +352,38 @@ def gm_spgemm_debug_copy(plan, view: int, level: int = 0):
 
 
 def gm_prefix_sum_noalloc(inp, out, total=None, stream=None):
-    """Exclusive scan of an int64 CUDA tensor into ``out`` using the library's fixed scratch."""
+    """Exclusive scan of an int64 CUDA tensor into ``out`` using the library's fixed scratch.
+
+    ``inp`` and ``out`` are contiguous int64 tensors on the current CUDA device,
+    ``out`` at least as long as ``inp`` (it may be ``inp`` itself); ``total``, when
+    given, a contiguous int64 tensor of at least one element on the same device.
+    Anything else raises ValueError before the library is called."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    named = [("inp", inp), ("out", out)] + ([("total", total)] if total is not None else [])
+    for name, t in named:
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.int64 or not t.is_contiguous() or t.device != dev:
+            raise ValueError(f"{name} must be a contiguous int64 tensor on {dev}")
+    if out.numel() < inp.numel():
+        raise ValueError(f"out holds {out.numel()} elements, the scan writes {inp.numel()}")
+    if total is not None and total.numel() < 1:
+        raise ValueError("total must hold at least one element")
     _check(load().gm_prefix_sum_noalloc(inp.data_ptr() if inp.numel() else None,
                                         out.data_ptr() if out.numel() else None, inp.numel(),
                                         total.data_ptr() if total is not None else None,
                                         _stream_handle(stream)), "gm_prefix_sum_noalloc")
 
 
-def spgemm(A: DeviceCSR, B: DeviceCSR, cfg: gm_config | None = None, stream=None, return_info: bool = False):
-    """C = A @ B on the GPU: analyze, symbolic, allocate C with torch, numeric."""
+def spgemm(A: DeviceCSR, B: DeviceCSR, cfg: gm_config | None = None, stream=None, return_info: bool = False,
+           rows=None):
+    """C = A @ B on the GPU: analyze, symbolic, allocate C with torch, numeric.
+    With rows = (row_begin, row_end): those rows of C only (row pointers from 0)."""
     import torch
     dev = A.row_ptr.device
-    plan = gm_spgemm_analyze(A, B, cfg, stream)
+    plan = gm_spgemm_analyze(A, B, cfg, stream, rows=rows)
+    n_out = A.n_rows if rows is None else int(rows[1]) - int(rows[0])
     try:
-        c_rp = torch.empty(A.n_rows + 1, dtype=A.row_ptr.dtype, device=dev)
+        c_rp = torch.empty(n_out + 1, dtype=A.row_ptr.dtype, device=dev)
         nnz = gm_spgemm_symbolic(plan, c_rp)
         c_col = torch.empty(nnz, dtype=A.col.dtype, device=dev)
         c_val = torch.empty(nnz, dtype=A.val.dtype, device=dev)
@@ -331,5 +391,5 @@ def spgemm(A: DeviceCSR, B: DeviceCSR, cfg: gm_config | None = None, stream=None
         info = gm_spgemm_plan_info(plan) if return_info else None
     finally:
         gm_spgemm_plan_destroy(plan)
-    C = DeviceCSR(A.n_rows, B.n_cols, c_rp, c_col, c_val)
+    C = DeviceCSR(n_out, B.n_cols, c_rp, c_col, c_val)
     return (C, info) if return_info else C

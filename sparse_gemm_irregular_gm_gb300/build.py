@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgm_spgemm.so")
-SOURCES = ["gm_api.cu", "gm_analyze.cu", "gm_scan.cu", "gm_expand.cu", "gm_multisplit.cu", "gm_accum.cu", "gm_rowbitmap.cu", "gm_walk.cu", "gm_noalloc.cu"]
+SOURCES = ["gm_api.cu", "gm_analyze.cu", "gm_scan.cu", "gm_expand.cu", "gm_multisplit.cu", "gm_accum.cu", "gm_rowbitmap.cu",
+           "gm_stream.cu", "gm_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

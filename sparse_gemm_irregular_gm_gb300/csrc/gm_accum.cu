@@ -534,10 +534,13 @@ __global__ void __launch_bounds__(32 * WARPS, (ITEMS >= 16 ? 160 : 256) / WARPS)
   }
 }
 
-// The same accumulator for chunks of up to vcap elements with 4 warps per chunk:
-// elements in tiles of 128 * ITEMS through registers, bitmap word prefix by a
-// block scan over 16-byte pieces, values added into their rank's slot.
-template <typename V, typename CT, int ITEMS, int T>
+// The same accumulator for chunks of up to vcap output columns with T threads per
+// chunk: elements in tiles of T * ITEMS through registers, bitmap word prefix by
+// a block scan over 16-byte pieces, values added into their rank's slot; the
+// column of every rank is then taken from the bitmap into shared memory, so
+// that the chunk's row of C is written with consecutive threads on consecutive
+// entries. CR holds a column inside the chunk (uint16_t up to 65536 columns).
+template <typename V, typename CT, int ITEMS, int T, typename CR>
 __global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap, int ecap) {
   const CT* __restrict__ in_col = static_cast<const CT*>(a.col);
 
@@ -610,15 +613,21 @@ __global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap,
       }
     }
     __syncthreads();
-    for (int w = threadIdx.x; w < nwp; w += T) {  // words round-robin over threads
-      uint32_t bits = bm[w];
-      int pos = pre[w];
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1;
-        a.c_col[out + pos] = static_cast<int32_t>(cb + w * 32 + b);
-        c_val[out + pos] = vals[pos];
-        ++pos;
+    {  // columns of every rank into shared memory, then coalesced rows of C
+      CR* colr = reinterpret_cast<CR*>(vals + vcap);
+      for (int w = threadIdx.x; w < nwp; w += T) {
+        uint32_t bits = bm[w];
+        int pos = pre[w];
+        while (bits) {
+          const int b = __ffs(bits) - 1;
+          bits &= bits - 1;
+          colr[pos++] = static_cast<CR>(w * 32 + b);
+        }
+      }
+      __syncthreads();
+      for (int r = threadIdx.x; r < nnz; r += T) {
+        a.c_col[out + r] = static_cast<int32_t>(cb + colr[r]);
+        c_val[out + r] = vals[r];
       }
     }
     __syncthreads();
@@ -817,20 +826,27 @@ void launch_leaf_warpbm_t(const ListArgs& a, int max_elems, int nwp, int W, size
   }
 }
 
-template <typename V, typename CT>
-void launch_leaf_blkbm_t(const ListArgs& a, int max_nnz, int max_elems, int nwp, size_t smem, cudaStream_t s) {
+// smem: bitmap and prefix (nwp words each), the value array and the column of
+// every rank (max_nnz entries each).
+template <typename V, typename CT, typename CR>
+void launch_leaf_blkbm_c(const ListArgs& a, int max_nnz, int max_elems, int nwp, size_t smem, cudaStream_t s) {
   const unsigned g = static_cast<unsigned>(std::min<int64_t>(a.n_items, 152LL * 32));
   // threads per chunk grow with the value array so that an SM keeps ~1000 threads busy
   if (max_nnz <= 4096) {
-    set_smem(k_leaf_blkbm<V, CT, 8, 128>, smem);
-    (k_leaf_blkbm<V, CT, 8, 128><<<g, 128, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
+    set_smem(k_leaf_blkbm<V, CT, 8, 128, CR>, smem);
+    (k_leaf_blkbm<V, CT, 8, 128, CR><<<g, 128, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
   } else if (max_nnz <= 8192) {
-    set_smem(k_leaf_blkbm<V, CT, 8, 256>, smem);
-    (k_leaf_blkbm<V, CT, 8, 256><<<g, 256, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
+    set_smem(k_leaf_blkbm<V, CT, 8, 256, CR>, smem);
+    (k_leaf_blkbm<V, CT, 8, 256, CR><<<g, 256, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
   } else {
-    set_smem(k_leaf_blkbm<V, CT, 8, 1024>, smem);
-    (k_leaf_blkbm<V, CT, 8, 1024><<<g, 1024, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
+    set_smem(k_leaf_blkbm<V, CT, 8, 1024, CR>, smem);
+    (k_leaf_blkbm<V, CT, 8, 1024, CR><<<g, 1024, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
   }
+}
+template <typename V, typename CT>
+void launch_leaf_blkbm_t(const ListArgs& a, int max_nnz, int max_elems, int nwp, size_t smem, cudaStream_t s) {
+  if (a.width <= 65536) launch_leaf_blkbm_c<V, CT, uint16_t>(a, max_nnz, max_elems, nwp, smem, s);
+  else launch_leaf_blkbm_c<V, CT, uint32_t>(a, max_nnz, max_elems, nwp, smem, s);
 }
 
 template <typename V, typename CT>
@@ -915,14 +931,18 @@ void launch_leaf_warpbm(const ListArgs& a, int max_elems, cudaStream_t s) {
 
 int64_t leaf_blkbm_words(int64_t width) { return ((width + 31) / 32 + 511) & ~int64_t(511); }
 
-bool leaf_blkbm_fits(int64_t width, int max_elems, int64_t smem_max, int vb) {
-  return leaf_blkbm_words(width) * 8 + static_cast<int64_t>(max_elems) * vb + 1024 <= smem_max;
+static int blkbm_col_bytes(int64_t width) { return width <= 65536 ? 2 : 4; }
+
+bool leaf_blkbm_fits(int64_t width, int max_nnz, int64_t smem_max, int vb) {
+  return leaf_blkbm_words(width) * 8 + static_cast<int64_t>(max_nnz) * (vb + blkbm_col_bytes(width)) + 1024 <=
+         smem_max;
 }
 
 void launch_leaf_blkbm(const ListArgs& a, int max_nnz, int max_elems, cudaStream_t s) {
   if (a.n_items <= 0) return;
   const int nwp = static_cast<int>(leaf_blkbm_words(a.width));
-  const size_t smem = static_cast<size_t>(nwp) * 8 + static_cast<size_t>(max_nnz) * (a.f32 ? 4 : 8);
+  const size_t smem =
+      static_cast<size_t>(nwp) * 8 + static_cast<size_t>(max_nnz) * ((a.f32 ? 4 : 8) + blkbm_col_bytes(a.width));
   if (a.f32 && a.col16) launch_leaf_blkbm_t<float, uint16_t>(a, max_nnz, max_elems, nwp, smem, s);
   else if (a.f32) launch_leaf_blkbm_t<float, int32_t>(a, max_nnz, max_elems, nwp, smem, s);
   else if (a.col16) launch_leaf_blkbm_t<double, uint16_t>(a, max_nnz, max_elems, nwp, smem, s);

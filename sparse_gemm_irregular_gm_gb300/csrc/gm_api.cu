@@ -35,6 +35,14 @@ void note_launch(int n) {
 }
 int64_t launch_count() { return g_launches.load(); }
 
+int exp_flags() {
+  static const int f = [] {
+    const char* e = std::getenv("GM_EXP");
+    return e ? std::atoi(e) : 0;
+  }();
+  return f;
+}
+
 static bool env_log_enabled() {
   static const bool on = [] {
     const char* e = std::getenv("GM_SPGEMM_LOG");
@@ -295,6 +303,7 @@ struct GrowBuf {
 struct StageEv {
   int stage;
   cudaEvent_t a, b;
+  cudaStream_t on;  // the stream the stage's work runs on
 };
 
 struct LevelDbg {
@@ -338,11 +347,10 @@ struct gm_plan {
   bool f32 = false;        // values are float (GM_VALUE_F32), else double
   int vb = 8;              // bytes of a value
   int arena_cb = 4;        // bytes of a column in the element arenas (2: chunk-local uint16)
-  bool walk_ok = false;    // the walk pipeline applies when B is strict and the bitmaps fit
-  bool walk = false;       // numeric heavy path: chunks summed straight from B's ranges (gm_walk.cu)
   bool rowexp0 = false;    // two or more levels: level 0 by the row-order expansion, no C-hat
   int32_t index_type = 0;  // GM_INDEX_* flags of the caller's arrays
   gm::DevBuf<int64_t> a_rp64, b_rp64, c_rp64;  // int32 row pointers widened (C: until numeric)
+  gm::DevBuf<int64_t> a_rps;                   // row pointers of a row range of A, rebased to 0
   gm::DevBuf<int32_t> a_col32, b_col32;        // int64 columns narrowed
   gm_params P{};
   int L = 0;
@@ -362,7 +370,6 @@ struct gm_plan {
   gm::DevBuf<int64_t> anz;          // prefix of nnz(A[x_heavy[h], :]) (n_heavy + 1)
   gm::DevBuf<int64_t> cnt0;         // row-order pipeline: elements of each level-0 chunk (n_heavy * v0)
   gm::DevBuf<int32_t> bcp;          // row-order pipeline: per-B-row level-0 chunk starts (B.n_rows * (v0 + 1))
-  gm::DevBuf<uint32_t> hbits;       // walk pipeline: the heavy rows' bitmaps (n_heavy * rowbm_words(C.m))
   std::vector<int64_t> h_chat_rp;   // host copy of chat_rp
   std::vector<int64_t> h_anz;       // prefix of nnz(A[x_heavy[h], :])
   gm::GrowBuf nnz[GM_MAX_LEVELS];        // per level, per child: nnz (symbolic) then output offset
@@ -395,17 +402,25 @@ struct gm_plan {
   std::vector<std::unique_ptr<gm::LevelDbg>> dbg_levels;
   bool dbg_ok = false;
 
-  int stage_begin(int stage) {
+  // GM_FLAG_OVERLAP: the light rows run on a second stream with their own
+  // status word and work counter, forked from and joined into the plan's stream
+  bool overlap = false;
+  cudaStream_t s2 = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  gm::DevBuf<int> status2;
+  gm::DevBuf<unsigned int> work_counter2;
+
+  int stage_begin(int stage, cudaStream_t on = nullptr) {
     if (!timing) return -1;
-    gm::StageEv e{stage, nullptr, nullptr};
+    gm::StageEv e{stage, nullptr, nullptr, on ? on : s};
     cudaEventCreate(&e.a);
     cudaEventCreate(&e.b);
-    cudaEventRecord(e.a, s);
+    cudaEventRecord(e.a, e.on);
     evs.push_back(e);
     return static_cast<int>(evs.size()) - 1;
   }
   void stage_end(int idx) {
-    if (idx >= 0) cudaEventRecord(evs[idx].b, s);
+    if (idx >= 0) cudaEventRecord(evs[idx].b, evs[idx].on);
   }
   void collect_times() {
     for (auto& e : evs) {
@@ -418,10 +433,14 @@ struct gm_plan {
     cudaGetLastError();
   }
   ~gm_plan() {
+    if (s2) cudaStreamSynchronize(s2);
     if (!evs.empty()) {
       cudaStreamSynchronize(s);
       collect_times();
     }
+    if (ev_fork) cudaEventDestroy(ev_fork);
+    if (ev_join) cudaEventDestroy(ev_join);
+    if (s2) cudaStreamDestroy(s2);
   }
 };
 
@@ -443,9 +462,15 @@ static gm_status sync_check(gm_plan* p) {
   int st = 0;
   e = cudaMemcpy(&st, p->status.p, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_status(p, e);
+  if (p->overlap && p->status2.p) {  // the light stream's word (its work is joined into p->s)
+    int st2 = 0;
+    e = cudaMemcpy(&st2, p->status2.p, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(p, e);
+    st |= st2;
+  }
   p->dev_status |= st;
   if (st & (kStBadARowPtr | kStBadBRowPtr | kStBadACol | kStBadBCol)) return GM_ERR_BAD_INDEX;
-  if (st) return GM_ERR_CUDA;
+  if (st) return GM_ERR_INTERNAL;  // the library's own checks: never the input's or the driver's fault
   return GM_OK;
 }
 
@@ -466,59 +491,154 @@ static gm_status check_csr(const gm_csr* M, int32_t index_type) {
 // pointers and int32 columns the path reads: converted copies owned by the plan,
 // one per distinct array (A and B of A*A share theirs). Out-of-range int64
 // columns become -1, which the validation in analyze_impl reports.
-static gm_status adapt_inputs(gm_plan* p, const gm_csr* A, const gm_csr* B) {
-  auto take = [](const gm_csr* M) {
-    CsrDev d;
-    d.n_rows = M->n_rows;
-    d.n_cols = M->n_cols;
-    d.nnz = M->nnz;
-    d.row_ptr = static_cast<const int64_t*>(M->row_ptr);
-    d.col_idx = static_cast<const int32_t*>(M->col_idx);
-    d.vals = M->vals;
-    return d;
-  };
-  p->A = take(A);
-  p->B = take(B);
+// Rows [r0, r1) of A only (the whole of A when r0 = 0 and r1 = A.n_rows): the
+// caller's row pointers are validated whole first, then the range's pointers are
+// copied and rebased to start at 0 and its columns and values addressed in
+// place, from the range's first entry on.
+static gm_status adapt_inputs(gm_plan* p, const gm_csr* A, const gm_csr* B, int64_t r0, int64_t r1) {
   const cudaStream_t s = p->s;
-  if (p->index_type & GM_INDEX_ROWPTR32) {
+  const bool rp32 = (p->index_type & GM_INDEX_ROWPTR32) != 0;
+  const bool col64 = (p->index_type & GM_INDEX_COL64) != 0;
+  const bool sliced = r0 != 0 || r1 != A->n_rows;
+  const bool shared_rp = B->row_ptr == A->row_ptr && B->n_rows == A->n_rows;
+  // whole row pointers as int64
+  const int64_t* a_rp = static_cast<const int64_t*>(A->row_ptr);
+  const int64_t* b_rp = static_cast<const int64_t*>(B->row_ptr);
+  if (rp32) {
     if (!p->a_rp64.alloc(A->n_rows + 1, s)) return GM_ERR_OOM;
     launch_widen_i32(static_cast<const int32_t*>(A->row_ptr), p->a_rp64.p, A->n_rows + 1, s);
-    p->A.row_ptr = p->a_rp64.p;
-    if (B->row_ptr == A->row_ptr && B->n_rows == A->n_rows) {
-      p->B.row_ptr = p->a_rp64.p;
+    a_rp = p->a_rp64.p;
+    if (shared_rp) {
+      b_rp = a_rp;
     } else {
       if (!p->b_rp64.alloc(B->n_rows + 1, s)) return GM_ERR_OOM;
       launch_widen_i32(static_cast<const int32_t*>(B->row_ptr), p->b_rp64.p, B->n_rows + 1, s);
-      p->B.row_ptr = p->b_rp64.p;
+      b_rp = p->b_rp64.p;
     }
   }
-  if (p->index_type & GM_INDEX_COL64) {
-    if (!p->a_col32.alloc(A->nnz, s)) return GM_ERR_OOM;
-    launch_narrow_i64(static_cast<const int64_t*>(A->col_idx), p->a_col32.p, A->nnz, A->n_cols, s);
+  int64_t lo = 0, hi = A->nnz;
+  const int64_t* a_rp_used = a_rp;
+  if (sliced) {
+    launch_validate_rowptr(a_rp, A->n_rows, A->nnz, kStBadARowPtr, p->status.p, s);
+    const gm_status st = sync_check(p);
+    if (st != GM_OK) return st;
+    int64_t ends[2] = {0, 0};
+    cudaMemcpyAsync(&ends[0], a_rp + r0, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+    cudaMemcpyAsync(&ends[1], a_rp + r1, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+    const cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_status(p, e);
+    lo = ends[0];
+    hi = ends[1];
+    if (!p->a_rps.alloc(r1 - r0 + 1, s)) return GM_ERR_OOM;
+    sub_i64(a_rp + r0, r1 - r0 + 1, lo, p->a_rps.p, s);
+    a_rp_used = p->a_rps.p;
+  }
+  p->A.n_rows = r1 - r0;
+  p->A.n_cols = A->n_cols;
+  p->A.nnz = hi - lo;
+  p->A.row_ptr = a_rp_used;
+  p->A.vals = static_cast<const unsigned char*>(A->vals) + lo * p->vb;
+  p->B.n_rows = B->n_rows;
+  p->B.n_cols = B->n_cols;
+  p->B.nnz = B->nnz;
+  p->B.row_ptr = b_rp;
+  p->B.vals = B->vals;
+  if (col64) {
+    const int64_t* a_col = static_cast<const int64_t*>(A->col_idx) + lo;
+    if (!p->a_col32.alloc(p->A.nnz, s)) return GM_ERR_OOM;
+    launch_narrow_i64(a_col, p->a_col32.p, p->A.nnz, A->n_cols, s);
     p->A.col_idx = p->a_col32.p;
-    if (B->col_idx == A->col_idx && B->nnz == A->nnz && B->n_cols == A->n_cols) {
+    if (!sliced && B->col_idx == A->col_idx && B->nnz == A->nnz && B->n_cols == A->n_cols) {
       p->B.col_idx = p->a_col32.p;
     } else {
       if (!p->b_col32.alloc(B->nnz, s)) return GM_ERR_OOM;
       launch_narrow_i64(static_cast<const int64_t*>(B->col_idx), p->b_col32.p, B->nnz, B->n_cols, s);
       p->B.col_idx = p->b_col32.p;
     }
+  } else {
+    p->A.col_idx = static_cast<const int32_t*>(A->col_idx) + lo;
+    p->B.col_idx = static_cast<const int32_t*>(B->col_idx);
   }
   return GM_OK;
+}
+
+// Validation first: nothing after it may index with unchecked row pointers or columns.
+static gm_status validate_inputs(gm_plan* p) {
+  const cudaStream_t s = p->s;
+  launch_validate_rowptr(p->A.row_ptr, p->A.n_rows, p->A.nnz, kStBadARowPtr, p->status.p, s);
+  launch_validate_rowptr(p->B.row_ptr, p->B.n_rows, p->B.nnz, kStBadBRowPtr, p->status.p, s);
+  launch_validate_cols(p->A.col_idx, p->A.nnz, p->A.n_cols, kStBadACol, p->status.p, s);
+  launch_validate_cols(p->B.col_idx, p->B.nnz, p->B.n_cols, kStBadBCol, p->status.p, s);
+  return sync_check(p);
+}
+
+namespace {
+// bounds[q] for q in [0, n_parts]: 0, then for 0 < q < n_parts the row r where
+// n_parts * S[r] comes closest to q * S[n] (S = exclusive prefix of the row
+// products, S[n] their total): of the last r below that target and the first r
+// reaching it, the nearer one, the lower on a tie; then n. Without products the
+// rows are split evenly.
+__global__ void k_row_split(const int64_t* __restrict__ S, int64_t n, int64_t n_parts, int64_t* __restrict__ bounds) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t T = S[n];
+  for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q <= n_parts; q += stride) {
+    int64_t r;
+    if (q == 0) r = 0;
+    else if (q == n_parts) r = n;
+    else if (T == 0) r = static_cast<int64_t>(static_cast<__int128>(q) * n / n_parts);
+    else {
+      const __int128 want = static_cast<__int128>(q) * T;
+      int64_t lo = 0, hi = n;  // S[n] * n_parts >= want always holds
+      while (lo < hi) {
+        const int64_t mid = (lo + hi) >> 1;
+        if (static_cast<__int128>(n_parts) * S[mid] >= want) hi = mid; else lo = mid + 1;
+      }
+      r = lo;  // the first row reaching the target; lo > 0 since S[0] = 0 < want
+      const __int128 above = static_cast<__int128>(n_parts) * S[lo] - want;
+      const __int128 below = want - static_cast<__int128>(n_parts) * S[lo - 1];
+      if (below <= above) r = lo - 1;
+    }
+    bounds[q] = r;
+  }
+}
+template <typename T>
+__global__ void k_add_base(T* __restrict__ x, int64_t n, int64_t base) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    x[i] = static_cast<T>(x[i] + base);
+}
+}  // namespace
+
+// Row split for several GPUs: the products of every row, their prefix, and the
+// split points (k_row_split).
+static gm_status row_split_impl(gm_plan* p, int64_t n_parts, int64_t* bounds) {
+  const cudaStream_t s = p->s;
+  const int64_t n = p->A.n_rows;
+  gm_status st = validate_inputs(p);
+  if (st != GM_OK) return st;
+  BinSpec spec{};
+  spec.nbins = 2;
+  spec.ub[0] = 0;
+  spec.ub[1] = INT64_MAX;
+  DevBuf<int64_t> u, S, out;
+  DevBuf<uint8_t> bin;
+  if (!u.alloc(std::max<int64_t>(n, 1), s) || !bin.alloc(std::max<int64_t>(n, 1), s) || !S.alloc(n + 1, s) ||
+      !out.alloc(n_parts + 1, s))
+    return GM_ERR_OOM;
+  launch_ip_count(p->A.row_ptr, p->A.col_idx, n, p->B.row_ptr, u.p, bin.p, spec, s);
+  if (n == 0) cudaMemsetAsync(S.p, 0, sizeof(int64_t), s);
+  else if (!scan_exclusive_i64(u.p, S.p, n, S.p + n, s)) return GM_ERR_OOM;
+  (k_row_split<<<grid_for(n_parts + 1, 256), 256, 0, s>>>(S.p, n, n_parts, out.p), note_launch());
+  cudaMemcpyAsync(bounds, out.p, (n_parts + 1) * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+  return sync_check(p);
 }
 
 static gm_status analyze_impl(gm_plan* p) {
   const cudaStream_t s = p->s;
   const int64_t n = p->A.n_rows;
-  if (!p->status.alloc(1, s) || !p->work_counter.alloc(1, s)) return GM_ERR_OOM;
-  cudaMemsetAsync(p->status.p, 0, sizeof(int), s);
+  if (!p->work_counter.alloc(1, s)) return GM_ERR_OOM;
   const int t0 = p->stage_begin(GM_STAGE_ANALYZE);
-  // Validation first: nothing below may index with unchecked row pointers or columns.
-  launch_validate_rowptr(p->A.row_ptr, p->A.n_rows, p->A.nnz, kStBadARowPtr, p->status.p, s);
-  launch_validate_rowptr(p->B.row_ptr, p->B.n_rows, p->B.nnz, kStBadBRowPtr, p->status.p, s);
-  launch_validate_cols(p->A.col_idx, p->A.nnz, p->A.n_cols, kStBadACol, p->status.p, s);
-  launch_validate_cols(p->B.col_idx, p->B.nnz, p->B.n_cols, kStBadBCol, p->status.p, s);
-  gm_status st = sync_check(p);
+  gm_status st = validate_inputs(p);
   if (st != GM_OK) return st;
   {  // is every B row sorted? (decides how heavy products are scattered into chunks)
     DevBuf<int> flag;
@@ -630,6 +750,9 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
   if (by_nnz) spec.nbins = 9;
   const bool warp_ok = leaf_warpbm_fits(la.width, 1024, p->smem_dev, p->vb);
   const bool blk4k_ok = leaf_blkbm_fits(la.width, 4096, p->smem_dev, p->vb);
+  // chunks of more than 4096 elements: streamed through shared memory by bulk copies
+  const bool stream_ok = (exp_flags() & 8) && leaf_stream_fits(la.width, la.col16, p->smem_dev, p->vb);
+  la.counter = p->work_counter.p;
   DevBuf<uint8_t> bins;
   DevBuf<int32_t> idx;
   DevBuf<int64_t> starts_d, items;
@@ -660,6 +783,7 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
       else if (b == 7 && warp_ok) launch_leaf_warpbm(a, 1024, s);
       else if (b == 8 && blk4k_ok) launch_leaf_blkbm(a, 2048, 2048, s);
       else if (b == 3 && blk4k_ok) launch_leaf_blkbm(a, 4096, 4096, s);
+      else if (b >= 4 && b <= 6 && stream_ok) launch_leaf_stream(a, p->num_sms, s);
       else if (b == 4 && blk4k_ok) launch_leaf_blkbm(a, 4096, INT_MAX, s);
       else if (b == 5 && leaf_blkbm_fits(la.width, 8192, p->smem_dev, p->vb)) launch_leaf_blkbm(a, 8192, INT_MAX, s);
       else if (b == 6 && leaf_blkbm_fits(la.width, static_cast<int>(la.width), p->smem_dev, p->vb))
@@ -1192,8 +1316,10 @@ static gm_status alloc_arena(gm_plan* p, const std::vector<std::pair<int64_t, in
   if (p->log)
     std::fprintf(stderr, "[gm_spgemm] %zu batch(es), largest %lld products, arena %.2f GB\n", batches.size(),
                  (long long)mx, mx * (with_val ? 24.0 : 8.0) / 1e9);
-  const size_t col_b = ((static_cast<size_t>(mx) * p->arena_cb + 255) / 256) * 256;
-  const size_t val_b = with_val ? ((static_cast<size_t>(mx) * p->vb + 255) / 256) * 256 : 0;
+  // 256 bytes past each array's end: the streamed accumulator's bulk copies end
+  // at the 16-byte boundary at or above a chunk's last element
+  const size_t col_b = ((static_cast<size_t>(mx) * p->arena_cb + 255) / 256) * 256 + 256;
+  const size_t val_b = with_val ? ((static_cast<size_t>(mx) * p->vb + 255) / 256) * 256 + 256 : 0;
   if (!p->arena_block.alloc(nbuf * (col_b + val_b), p->s)) return GM_ERR_OOM;
   unsigned char* base = p->arena_block.p;
   for (int k = 0; k < 2; ++k) {
@@ -1258,7 +1384,9 @@ static int64_t workspace_cap(gm_plan* p) {
   return cap;
 }
 
-static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, void* c_val) {
+// Light rows, bin by bin, on stream `on` with the given work counter and status word.
+static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, void* c_val, cudaStream_t on,
+                         unsigned int* counter, int* status) {
   for (int b = 1; b <= 10; ++b) {
     const int64_t cnt = p->bin_start[b + 1] - p->bin_start[b];
     if (cnt <= 0) continue;
@@ -1280,9 +1408,9 @@ static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, void* c_val) 
       ra.c_rp = p->c_rp;
       ra.c_col = c_col;
       ra.c_val = c_val;
-      ra.work_counter = p->work_counter.p;
-      ra.status = p->status.p;
-      launch_rowbm_light(ra, !numeric, cap, p->num_sms, p->smem_dev, p->s);
+      ra.work_counter = counter;
+      ra.status = status;
+      launch_rowbm_light(ra, !numeric, cap, p->num_sms, p->smem_dev, on);
       continue;
     }
     LightArgs la{};
@@ -1298,9 +1426,31 @@ static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, void* c_val) 
     la.c_rp = p->c_rp;
     la.c_col = c_col;
     la.c_val = c_val;
-    la.status = p->status.p;
-    launch_light_rows(la, light_bin_cap(b, p->P.tau, p->smem_dev, p->vb), !numeric, p->s);
+    la.status = status;
+    launch_light_rows(la, light_bin_cap(b, p->P.tau, p->smem_dev, p->vb), !numeric, on);
   }
+}
+
+// The light rows of one pass: on the plan's stream, or (GM_FLAG_OVERLAP) on the
+// second stream after everything queued so far on the plan's stream; join_light
+// makes the plan's stream wait for them.
+static void run_light(gm_plan* p, bool numeric, int32_t* c_col, void* c_val) {
+  const int stage = numeric ? GM_STAGE_NUM_LIGHT : GM_STAGE_SYM_LIGHT;
+  if (!p->overlap) {
+    const int t = p->stage_begin(stage);
+    launch_light(p, numeric, c_col, c_val, p->s, p->work_counter.p, p->status.p);
+    p->stage_end(t);
+    return;
+  }
+  cudaEventRecord(p->ev_fork, p->s);
+  cudaStreamWaitEvent(p->s2, p->ev_fork, 0);
+  const int t = p->stage_begin(stage, p->s2);
+  launch_light(p, numeric, c_col, c_val, p->s2, p->work_counter2.p, p->status2.p);
+  p->stage_end(t);
+  cudaEventRecord(p->ev_join, p->s2);
+}
+static void join_light(gm_plan* p) {
+  if (p->overlap) cudaStreamWaitEvent(p->s, p->ev_join, 0);
 }
 
 static gm_status symbolic_impl(gm_plan* p, int64_t* C_rp, int64_t* C_nnz) {
@@ -1308,9 +1458,8 @@ static gm_status symbolic_impl(gm_plan* p, int64_t* C_rp, int64_t* C_nnz) {
   const int64_t n = p->A.n_rows;
   p->c_rp = C_rp;
   cudaMemsetAsync(C_rp, 0, (n + 1) * sizeof(int64_t), s);
-  int t = p->stage_begin(GM_STAGE_SYM_LIGHT);
-  launch_light(p, false, nullptr, nullptr);
-  p->stage_end(t);
+  run_light(p, false, nullptr, nullptr);
+  int t = -1;
   const int L = p->L;
   const int64_t nh = p->n_heavy;
   if (nh > 0) {
@@ -1344,19 +1493,8 @@ static gm_status symbolic_impl(gm_plan* p, int64_t* C_rp, int64_t* C_nnz) {
         if (!p->bcp.alloc(std::max<int64_t>(p->B.n_rows, 1) * (v0 + 1), s)) return GM_ERR_OOM;
         build_chunk_starts(p->B.row_ptr, p->B.col_idx, p->B.n_rows, static_cast<int>(v0), shift0, p->bcp.p, s);
       }
-      p->walk = false;
-      if (p->walk_ok && p->b_strict && L == 1) {
-        // walk pipeline: the heavy rows' bitmaps are kept for the numeric pass
-        // when they take at most a quarter of the memory the workspace may use
-        const int64_t bits_words = nh * rowbm_words(p->c_m);
-        p->walk = bits_words * 4 <= workspace_cap(p) / 4 && p->hbits.alloc(bits_words, s);
-        if (p->walk) {
-          p->pipeline = GM_PIPE_WALK;
-          ra.bits_out = p->hbits.p;
-        }
-      }
       launch_rowbm(ra, p->num_sms, p->smem_dev, s);
-      if (p->rowwise && !p->walk) {  // level-0 chunk sizes, for the expansion
+      if (p->rowwise) {  // level-0 chunk sizes, for the expansion
         if (!p->cnt0.alloc(nh * v0, s)) return GM_ERR_OOM;
         if (!heavy_chunk_counts(hrows, nh, p->anz.p, p->A.row_ptr, p->A.col_idx, nullptr, p->B.col_idx,
                                 p->B.n_rows, static_cast<int>(v0), shift0, p->bcp.p, p->cnt0.p, s))
@@ -1407,6 +1545,7 @@ heavy_done:
     if (cnt > 0 && p->leaf_nnz.alloc(cnt, s))
       cudaMemcpyAsync(p->leaf_nnz.p, p->nnz[li].p, cnt * sizeof(int64_t), cudaMemcpyDeviceToDevice, s);
   }
+  join_light(p);  // the light rows' counts are in C_rp
   t = p->stage_begin(GM_STAGE_SCAN);
   if (!scan_exclusive_i64(C_rp, C_rp, n + 1, nullptr, s)) return GM_ERR_OOM;
   cudaMemcpyAsync(&p->c_nnz, C_rp + n, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
@@ -1437,69 +1576,9 @@ heavy_done:
   return GM_OK;
 }
 
-// Walk pipeline, numeric heavy rows: every (heavy row, level-0 chunk) with
-// columns is an item; items are classed by the chunk's nnz in chunk-major order
-// and each class is summed straight from B's ranges (gm_walk.cu).
-static gm_status run_heavy_walk(gm_plan* p, int32_t* c_col, void* c_val) {
-  const cudaStream_t s = p->s;
-  const int64_t nh = p->n_heavy;
-  const int v = static_cast<int>(p->P.v_chunks[0]);
-  const int64_t n = nh * v;
-  if (n >= INT32_MAX) return GM_ERR_INDEX_OVERFLOW;  // item ids are int32 in the partition
-  const int t = p->stage_begin(GM_STAGE_NUM_HEAVY);
-  constexpr int kClasses = 6;
-  DevBuf<uint8_t> cls;
-  DevBuf<int32_t> idx;
-  DevBuf<int64_t> starts_d, items;
-  if (!cls.alloc(n, s) || !idx.alloc(n, s) || !starts_d.alloc(kClasses + 1, s) || !items.alloc(n, s))
-    return GM_ERR_OOM;
-  if (!p->leaf_nnz.p) return GM_ERR_OOM;  // the symbolic pass could not keep the chunks' nnz
-  launch_walk_class(p->leaf_nnz.p, nh, v, cls.p, s);
-  if (!partition_by_bin(cls.p, n, kClasses, idx.p, starts_d.p, s)) return GM_ERR_OOM;
-  int64_t starts[kClasses + 1];
-  cudaMemcpyAsync(starts, starts_d.p, sizeof(starts), cudaMemcpyDeviceToHost, s);
-  const cudaError_t e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return cuda_status(p, e);
-  i32_to_i64(idx.p, n, 0, items.p, s);
-  WalkArgs wa{};
-  wa.heavy_rows = p->rows_by_bin.p + p->bin_start[kHeavyBin];
-  wa.nh = nh;
-  wa.v = v;
-  wa.shift = ilog2(p->P.widths[0]);
-  wa.nwc = static_cast<int>(p->P.widths[0] / 32);
-  wa.nwr = rowbm_words(p->c_m);
-  wa.bits = p->hbits.p;
-  wa.a_rp = p->A.row_ptr;
-  wa.a_col = p->A.col_idx;
-  wa.a_val = p->A.vals;
-  wa.b_rp = p->B.row_ptr;
-  wa.b_col = p->B.col_idx;
-  wa.b_val = p->B.vals;
-  wa.bcp = p->bcp.p;
-  wa.off = p->nnz[0].p;
-  wa.counter = p->work_counter.p;
-  wa.c_col = c_col;
-  wa.c_val = c_val;
-  wa.status = p->status.p;
-  for (int c = 1; c < kClasses; ++c) {
-    wa.items = items.p + starts[c];
-    wa.n_items = starts[c + 1] - starts[c];
-    launch_walk(wa, c, p->num_sms, p->smem_dev, s);
-  }
-  p->stage_end(t);
-  p->n_batches = std::max<int64_t>(p->n_batches, 1);
-  return cuda_status(p, cudaGetLastError());
-}
-
 static gm_status numeric_impl(gm_plan* p, int32_t* C_col, void* C_val) {
-  int t = p->stage_begin(GM_STAGE_NUM_LIGHT);
-  launch_light(p, true, C_col, C_val);
-  p->stage_end(t);
-  if (p->n_heavy > 0 && p->walk) {
-    const gm_status st = run_heavy_walk(p, C_col, C_val);
-    p->hbits.release();
-    if (st != GM_OK) return st;
-  } else if (p->n_heavy > 0) {
+  run_light(p, true, C_col, C_val);
+  if (p->n_heavy > 0) {
     const bool keep = p->keep;
     p->keep = false;
     std::vector<std::pair<int64_t, int64_t>> batches;
@@ -1518,6 +1597,7 @@ static gm_status numeric_impl(gm_plan* p, int32_t* C_col, void* C_val) {
     free_arena(p);
     p->keep = keep;
   }
+  join_light(p);
   return sync_check(p);
 }
 
@@ -1546,17 +1626,21 @@ gm_status gm_spgemm_params(int64_t c_m, const gm_config* cfg, gm_params* out) {
   return gm::compute_params(c_m, cfg, gm::kDefaultSmem, out);
 }
 
-gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* cfg, void* stream,
-                            gm_plan** plan_out) {
-  if (!plan_out) return GM_ERR_INVALID_ARG;
-  *plan_out = nullptr;
+}  // extern "C"
+
+namespace gm {
+// Argument checks and the plan object (no device work yet): parameters, device
+// properties, pipeline choice.
+static gm_status plan_setup(const gm_csr* A, const gm_csr* B, const gm_config* cfg, void* stream,
+                            std::unique_ptr<gm_plan>& p) {
   const int32_t index_type = cfg ? cfg->index_type : 0;
   if (index_type & ~(GM_INDEX_ROWPTR32 | GM_INDEX_COL64)) return GM_ERR_INVALID_ARG;
-  gm_status st = gm::check_csr(A, index_type);
-  if (st == GM_OK) st = gm::check_csr(B, index_type);
+  if (cfg && (cfg->pipeline < GM_PIPE_AUTO || cfg->pipeline > GM_PIPE_ROWWISE)) return GM_ERR_INVALID_ARG;
+  gm_status st = check_csr(A, index_type);
+  if (st == GM_OK) st = check_csr(B, index_type);
   if (st != GM_OK) return st;
   if (A->n_cols != B->n_rows) return GM_ERR_DIM_MISMATCH;
-  std::unique_ptr<gm_plan> p(new (std::nothrow) gm_plan);
+  p.reset(new (std::nothrow) gm_plan);
   if (!p) return GM_ERR_OOM;
   if (cfg) p->cfg = *cfg;
   p->index_type = index_type;
@@ -1566,7 +1650,7 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
   p->vb = p->f32 ? 4 : 8;
   p->timing = (p->cfg.flags & GM_FLAG_TIMING) != 0;
   p->keep = (p->cfg.flags & GM_FLAG_KEEP_INTERMEDIATES) != 0;
-  p->log = (p->cfg.flags & GM_FLAG_LOG) != 0 || gm::env_log();
+  p->log = (p->cfg.flags & GM_FLAG_LOG) != 0 || env_log();
   cudaError_t e = cudaGetDevice(&p->device);
   int smem = 0;
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device);
@@ -1577,21 +1661,51 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
   }
   p->smem_dev = smem;
   p->c_m = std::max<int64_t>(B->n_cols, 1);
-  st = gm::compute_params(p->c_m, &p->cfg, p->smem_dev, &p->P);
+  st = compute_params(p->c_m, &p->cfg, p->smem_dev, &p->P);
   if (st != GM_OK) return st;
   p->L = static_cast<int>(p->P.n_levels);
   p->sym_rowbm = p->L <= 1 && p->pipeline != GM_PIPE_UNFUSED && !p->keep &&
-                 gm::rowbm_symbolic_smem(p->c_m) + 4096 <= p->smem_dev;
+                 rowbm_symbolic_smem(p->c_m) + 4096 <= p->smem_dev;
   p->rowwise = p->sym_rowbm && p->L == 1 && p->P.v_chunks[0] <= 256 &&
-               gm::expand_fits(static_cast<int>(p->P.v_chunks[0]), p->P.widths[0], p->P.tau, p->smem_dev) &&
-               (p->cfg.pipeline == GM_PIPE_AUTO || p->cfg.pipeline == GM_PIPE_ROWWISE ||
-                p->cfg.pipeline == GM_PIPE_WALK);
+               expand_fits(static_cast<int>(p->P.v_chunks[0]), p->P.widths[0], p->P.tau, p->smem_dev) &&
+               (p->cfg.pipeline == GM_PIPE_AUTO || p->cfg.pipeline == GM_PIPE_ROWWISE);
   if (p->rowwise) p->pipeline = GM_PIPE_ROWWISE;
-  p->walk_ok = p->rowwise && p->cfg.pipeline == GM_PIPE_WALK && !p->f32 &&
-               gm::walk_fits(p->P.widths[0], p->smem_dev);
+  if (!p->status.alloc(1, p->s)) return GM_ERR_OOM;
+  cudaMemsetAsync(p->status.p, 0, sizeof(int), p->s);
+  p->overlap = (p->cfg.flags & GM_FLAG_OVERLAP) != 0;
+  if (p->overlap) {
+    if (!p->status2.alloc(1, p->s) || !p->work_counter2.alloc(1, p->s)) return GM_ERR_OOM;
+    cudaMemsetAsync(p->status2.p, 0, sizeof(int), p->s);
+    if (cudaStreamCreateWithFlags(&p->s2, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return GM_ERR_CUDA;
+    }
+  }
+  return GM_OK;
+}
+}  // namespace gm
+
+extern "C" {
+
+gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* cfg, void* stream,
+                            gm_plan** plan_out) {
+  if (!A) return GM_ERR_INVALID_ARG;
+  return gm_spgemm_analyze_rows(A, B, 0, A->n_rows, cfg, stream, plan_out);
+}
+
+gm_status gm_spgemm_analyze_rows(const gm_csr* A, const gm_csr* B, int64_t row_begin, int64_t row_end,
+                                 const gm_config* cfg, void* stream, gm_plan** plan_out) {
+  if (!plan_out) return GM_ERR_INVALID_ARG;
+  *plan_out = nullptr;
+  std::unique_ptr<gm_plan> p;
+  gm_status st = gm::plan_setup(A, B, cfg, stream, p);
+  if (st != GM_OK) return st;
+  if (row_begin < 0 || row_end < row_begin || row_end > A->n_rows) return GM_ERR_INVALID_ARG;
   gm::g_ws_peak = gm::g_ws_now.load();
   const int64_t l0 = gm::launch_count();
-  st = gm::adapt_inputs(p.get(), A, B);
+  st = gm::adapt_inputs(p.get(), A, B, row_begin, row_end);
   if (st == GM_OK) st = gm::analyze_impl(p.get());
   p->launches += gm::launch_count() - l0;
   if (p->timing) p->collect_times();
@@ -1610,6 +1724,46 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
   return GM_OK;
 }
 
+gm_status gm_spgemm_row_split(const gm_csr* A, const gm_csr* B, const gm_config* cfg, int64_t n_parts,
+                              void* stream, int64_t* bounds) {
+  if (!bounds || n_parts < 1 || n_parts > (int64_t(1) << 20)) return GM_ERR_INVALID_ARG;
+  std::unique_ptr<gm_plan> p;
+  gm_status st = gm::plan_setup(A, B, cfg, stream, p);
+  if (st != GM_OK) return st;
+  st = gm::adapt_inputs(p.get(), A, B, 0, A->n_rows);
+  if (st == GM_OK) st = gm::row_split_impl(p.get(), n_parts, bounds);
+  if (st != GM_OK) {
+    cudaStreamSynchronize(p->s);
+    cudaGetLastError();
+  }
+  return st;
+}
+
+gm_status gm_row_ptr_shift(void* row_ptr, int64_t n, int64_t base, int32_t index_type, void* stream) {
+  if (n < 0 || (n > 0 && !row_ptr) || base < 0) return GM_ERR_INVALID_ARG;
+  if (index_type & ~(GM_INDEX_ROWPTR32 | GM_INDEX_COL64)) return GM_ERR_INVALID_ARG;
+  if (n == 0 || base == 0) return GM_OK;
+  if (cudaPeekAtLastError() != cudaSuccess) return GM_ERR_CUDA;  // an earlier error stays with its owner
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (index_type & GM_INDEX_ROWPTR32) {
+    int32_t last = 0;  // the largest entry of a valid row-pointer array
+    cudaError_t e = cudaMemcpyAsync(&last, static_cast<int32_t*>(row_ptr) + (n - 1), sizeof(int32_t),
+                                    cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return GM_ERR_CUDA;
+    }
+    if (base + static_cast<int64_t>(last) >= (int64_t(1) << 31)) return GM_ERR_INDEX_OVERFLOW;
+    (gm::k_add_base<int32_t><<<gm::grid_for(n, 256), 256, 0, s>>>(static_cast<int32_t*>(row_ptr), n, base),
+     gm::note_launch());
+  } else {
+    (gm::k_add_base<int64_t><<<gm::grid_for(n, 256), 256, 0, s>>>(static_cast<int64_t*>(row_ptr), n, base),
+     gm::note_launch());
+  }
+  return cudaGetLastError() == cudaSuccess ? GM_OK : GM_ERR_CUDA;
+}
+
 gm_status gm_spgemm_symbolic(gm_plan* plan, void* C_row_ptr, int64_t* C_nnz) {
   if (!plan) return GM_ERR_INVALID_ARG;
   if (plan->state != 1) return GM_ERR_STATE;
@@ -1620,6 +1774,7 @@ gm_status gm_spgemm_symbolic(gm_plan* plan, void* C_row_ptr, int64_t* C_nnz) {
   if (rp32 && !plan->c_rp64.alloc(plan->A.n_rows + 1, plan->s)) st = GM_ERR_OOM;
   if (st == GM_OK)
     st = gm::symbolic_impl(plan, rp32 ? plan->c_rp64.p : static_cast<int64_t*>(C_row_ptr), C_nnz);
+  if (plan->s2) cudaStreamSynchronize(plan->s2);  // no light work outlives the call, error or not
   if (st == GM_OK && rp32) {  // C.rowPtr narrowed into the caller's int32 array
     if (plan->c_nnz >= (int64_t(1) << 31)) {
       st = GM_ERR_INDEX_OVERFLOW;
@@ -1660,6 +1815,7 @@ gm_status gm_spgemm_numeric(gm_plan* plan, void* C_col_idx, void* C_vals) {
   } else {
     st = gm::numeric_impl(plan, static_cast<int32_t*>(C_col_idx), C_vals);
   }
+  if (plan->s2) cudaStreamSynchronize(plan->s2);  // no light work outlives the call, error or not
   if (st == GM_OK) plan->c_rp64.release();
   plan->launches += gm::launch_count() - l0;
   if (plan->timing) {
@@ -1718,6 +1874,7 @@ const char* gm_status_string(gm_status s) {
     case GM_ERR_DEVICE_TIMEOUT: return "GM_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
     case GM_ERR_STATE: return "GM_ERR_STATE: call out of order";
     case GM_ERR_BAD_INDEX: return "GM_ERR_BAD_INDEX: column index or row pointer out of range";
+    case GM_ERR_INTERNAL: return "GM_ERR_INTERNAL: a device-side consistency check of the library failed";
   }
   return "unknown gm_status";
 }

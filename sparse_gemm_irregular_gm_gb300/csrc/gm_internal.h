@@ -25,6 +25,7 @@ enum : int {
   kStHashFull = 1 << 4,     // a probe sequence ran through the whole table
   kStGroupRows = 1 << 5,    // a multisplit work group met more rows than planned
   kStInternal = 1 << 6,     // an internal consistency check failed
+  kStWaitTimeout = 1 << 7,  // a bounded wait inside a kernel gave up
 };
 
 constexpr int kMaxBins = 16;
@@ -40,6 +41,8 @@ struct BinSpec {
 // Every launch site calls note_launch(); plans report the count they caused.
 void note_launch(int n = 1);
 int64_t launch_count();
+// Experimental kernel variants (environment GM_EXP, a bit mask; 0 by default).
+int exp_flags();
 
 // ---- workspace ------------------------------------------------------------
 // Stream-ordered device allocations routed through the caller's hooks (or
@@ -308,6 +311,7 @@ struct ListArgs {
   void* c_val;
   int* status;
   bool f32;
+  unsigned int* counter;      // dynamic chunk scheduling (launch_leaf_stream)
 };
 // Chunks narrower than the dense width: shared-memory bitmap + rank accumulator.
 void launch_leaf_bitmap(const ListArgs& a, int cap_vals, bool symbolic, cudaStream_t s);
@@ -326,7 +330,14 @@ bool leaf_warpbm_fits(int64_t width, int max_elems, int64_t smem_max, int vb = 8
 // The same with 4 warps per chunk: chunks of at most max_elems elements (INT_MAX:
 // any) and max_nnz output columns (the value array of the block).
 void launch_leaf_blkbm(const ListArgs& a, int max_nnz, int max_elems, cudaStream_t s);
-bool leaf_blkbm_fits(int64_t width, int max_elems, int64_t smem_max, int vb = 8);
+bool leaf_blkbm_fits(int64_t width, int max_nnz, int64_t smem_max, int vb = 8);
+// Numeric chunks of any size, streamed: one producer warp copies each chunk's
+// tiles into a shared-memory ring with bulk asynchronous copies, the consumer
+// warps add them into a dense accumulator of the chunk's width. One block per
+// SM; a.counter is reset by the launch. Needs a.width <= 65536 and the chunk
+// element arrays readable 16 bytes past their last element.
+bool leaf_stream_fits(int64_t width, bool col16, int64_t smem_max, int vb = 8);
+void launch_leaf_stream(const ListArgs& a, int num_sms, cudaStream_t s);
 int leaf_small_smem(int64_t width, int cap, bool symbolic, int vb = 8);
 
 // ---- whole-row bitmaps (gm_rowbitmap.cu) -----------------------------------------
@@ -349,7 +360,6 @@ struct RowBitmapArgs {
   void* c_val;
   unsigned int* work_counter; // device counter for dynamic row scheduling
   int* status;
-  uint32_t* bits_out;         // symbolic: each row's bitmap, rowbm_words(c_m) words a row (null: not kept)
   bool f32;
 };
 int64_t rowbm_symbolic_smem(int64_t c_m);
@@ -367,40 +377,6 @@ void launch_rowbm_light(const RowBitmapArgs& a, bool symbolic, int cap, int num_
 // bcp only (see heavy_chunk_counts), v <= 256.
 void build_chunk_starts(const int64_t* b_rp, const int32_t* b_col, int64_t b_rows, int v, int shift, int32_t* bcp,
                         cudaStream_t s);
-// Heavy rows' level-0 chunks summed straight from the B ranges inside each chunk
-// (gm_walk.cu). Items j = c * nh + h (chunk-major) name chunk c of heavy row h.
-struct WalkArgs {
-  const int32_t* heavy_rows;  // nh original row ids
-  int64_t nh;
-  int v;                      // level-0 chunks per row
-  int shift;                  // log2 of the chunk width
-  int nwc;                    // bitmap words per chunk (width / 32, a multiple of 4)
-  int64_t nwr;                // bitmap words per row (rowbm_words(C.m))
-  const uint32_t* bits;       // nh whole-row bitmaps from the symbolic pass
-  const int64_t* a_rp;
-  const int32_t* a_col;
-  const void* a_val;          // values are float or double (f32)
-  const int64_t* b_rp;
-  const int32_t* b_col;
-  const void* b_val;
-  const int32_t* bcp;         // per-B-row chunk starts, B.n_rows * (v + 1)
-  const int64_t* off;         // output offset of chunk c of heavy row h at [h * v + c]
-  const int64_t* items;       // item ids j of one class
-  int64_t n_items;
-  unsigned int* counter;      // dynamic item scheduling
-  int32_t* c_col;
-  void* c_val;
-  int* status;
-  bool f32;
-};
-// Classes 1-3: one warp per item of at most 256 / 1024 / 2048 columns; 4-5: one
-// block per item, atomic adds.
-int64_t walk_class_cap(int cls, int64_t width);
-int64_t walk_smem(int cls, int64_t width);
-bool walk_fits(int64_t width, int64_t smem_max);
-void launch_walk_class(const int64_t* cnnz, int64_t nh, int v, uint8_t* cls, cudaStream_t s);
-void launch_walk(const WalkArgs& a, int cls, int num_sms, int64_t smem_max, cudaStream_t s);
-
 // cnt[h * v + c] = products of heavy row h whose column falls in level-0 chunk c
 // (col >> shift == c), from per-B-row chunk counts, which are left in bcp
 // (b_rows * (v + 1) entries: bcp[k * (v + 1) + c] = entries of B row k in chunks

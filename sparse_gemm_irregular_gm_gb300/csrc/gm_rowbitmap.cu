@@ -142,11 +142,6 @@ __global__ void __launch_bounds__(kRbThreads) k_rowbm_symbolic(RowBitmapArgs a, 
     __syncthreads();
     mark_row(a, r, bm, longs);
     __syncthreads();
-    if (a.bits_out) {  // the row's bitmap stays for the numeric pass
-      uint4* dst = reinterpret_cast<uint4*>(a.bits_out + item * static_cast<int64_t>(nwords));
-      const uint4* b4 = reinterpret_cast<const uint4*>(bm);
-      for (int i = threadIdx.x; i < (nwords >> 2); i += blockDim.x) dst[i] = b4[i];
-    }
     if (a.v == 1 && a.width >= nbits) {  // whole row
       int n = 0;
       for (int w = threadIdx.x; w < nwords; w += blockDim.x) n += __popc(bm[w]);

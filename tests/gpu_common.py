@@ -45,15 +45,16 @@ def check_full(A, B, exact=False, **cfg):
 def gather_rows(C, rows):
     """Host copies of the given rows of a device CSR result."""
     import torch
-    rp = C.row_ptr.cpu().numpy()
-    lo, hi = rp[rows], rp[np.asarray(rows) + 1]
+    rp = C.row_ptr.cpu().numpy().astype(np.int64)
+    rows = np.asarray(rows, dtype=np.int64)
+    lo, hi = rp[rows], rp[rows + 1]
     lens = hi - lo
-    idx = np.concatenate([np.arange(a, b) for a, b in zip(lo, hi)]) if len(rows) else np.zeros(0, np.int64)
-    t = torch.from_numpy(idx.astype(np.int64)).to(C.col.device)
-    col = C.col[t].cpu().numpy()
-    val = C.val[t].cpu().numpy()
     srp = np.zeros(len(rows) + 1, dtype=np.int64)
     np.cumsum(lens, out=srp[1:])
+    idx = np.repeat(lo - srp[:-1], lens) + np.arange(srp[-1], dtype=np.int64)  # entry positions in C
+    t = torch.from_numpy(idx).to(C.col.device)
+    col = C.col[t].cpu().numpy()
+    val = C.val[t].cpu().numpy()
     return srp, col, val
 
 

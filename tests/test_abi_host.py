@@ -195,6 +195,20 @@ def test_analyze_index_type_host_errors(lib):
     assert not plan.value
 
 
+def test_analyze_rejects_unknown_pipelines(lib):
+    """gm_config.pipeline takes GM_PIPE_AUTO .. GM_PIPE_ROWWISE; any other value is
+    an argument error found on the host."""
+    fake = 0x1000  # never dereferenced
+    A = binding.gm_csr(4, 5, 3, fake, fake, fake)
+    B = binding.gm_csr(5, 5, 3, fake, fake, fake)
+    plan = ctypes.c_void_p()
+    for pipeline in (-1, 4, 99):
+        cfg = binding.make_config(pipeline=pipeline)
+        assert lib.gm_spgemm_analyze(ctypes.byref(A), ctypes.byref(B), ctypes.byref(cfg), None,
+                                     ctypes.byref(plan)) == 1
+    assert not plan.value
+
+
 @pytest.mark.parametrize("c_m", [1 << 10, 1 << 20, 1 << 24])
 def test_params_do_not_depend_on_index_type(lib, c_m):
     """The planner sizes shared memory by the widths held there (int32 columns,

@@ -4,7 +4,9 @@ Structure (row pointers, columns, nnz) must match bit for bit; fp64 values
 within 1e-12 * sum|a_ik * b_kj| per entry; integer-valued inputs exactly.
 Small inputs force every path (heavy rows, one and several multisplit levels,
 no level, several workspace batches, both pipelines); the five workloads run
-at their full sizes, the two largest checked on sampled rows plus invariants.
+at their full sizes: R-MAT scale 18 is compared row by row in full, scale 20
+on 50,000 rows stratified by their products plus invariants on every row (in
+full with GM_FULL_PARITY_20=1).
 """
 import json
 import os
@@ -49,9 +51,7 @@ FORCED = [
     ("L1_rowwise", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_ROWWISE}),
     ("L2_outer", {"tau": 16, "dense_width": 64, "n_chunks_max": 4, "pipeline": binding.GM_PIPE_FUSED_HISTO}),
     ("L3_outer", {"tau": 16, "dense_width": 16, "n_chunks_max": 4, "pipeline": binding.GM_PIPE_FUSED_HISTO}),
-    ("L1_walk_128", {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_WALK}),
-    ("L1_walk_256", {"tau": 16, "dense_width": 256, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_WALK}),
-    ("L1_walk_wide", {"tau": 64, "dense_width": 512, "pipeline": binding.GM_PIPE_WALK}),
+    ("L1_rowwise_256", {"tau": 16, "dense_width": 256, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_ROWWISE}),
 ]
 
 
@@ -66,8 +66,8 @@ def test_rmat10_forced_paths(name, cfg, values):
             assert info.n_batches > 1
         if name in ("heavy_L1", "L1_wide_chunks", "L1_rowwise_batched", "L1_rowwise"):
             assert info.pipeline == binding.GM_PIPE_ROWWISE
-        if name.startswith("L1_walk"):
-            assert info.pipeline == binding.GM_PIPE_WALK
+        if name == "L1_rowwise_256":
+            assert info.pipeline == binding.GM_PIPE_ROWWISE
         if name in ("heavy_L2", "heavy_L3"):  # level 0 by the row-order expansion
             assert info.pipeline == binding.GM_PIPE_ROWWISE and info.params.n_levels >= 2
         if name in ("L2_outer", "L3_outer"):
@@ -357,12 +357,11 @@ def _rows_of(M, rows):
     return gi.CSR(rows.size, M.n_cols, rp, M.col[idx].copy(), M.val[idx].copy())
 
 
-@pytest.mark.parametrize("pipeline", [binding.GM_PIPE_WALK, binding.GM_PIPE_AUTO], ids=["walk", "auto"])
+@pytest.mark.parametrize("pipeline", [binding.GM_PIPE_FUSED_HISTO, binding.GM_PIPE_AUTO], ids=["outer", "auto"])
 def test_large_chunks_many_tiles_exact(pipeline):
     """The heaviest rows of a scale-16 R-MAT times the whole matrix: chunks of
-    tens of thousands of elements (many 4096-element tiles of the large-chunk
-    accumulator, block items of the walk) with the R-MAT's hot columns; integer
-    values, so exact."""
+    tens of thousands of elements (many tiles of the large-chunk accumulators)
+    with the R-MAT's hot columns; integer values, so exact."""
     A = gi.rmat(16, 16, seed=3, values="int")
     u = oracle.ip_counts(A, A)
     rows = np.concatenate([np.argsort(u)[-40:], np.random.default_rng(0).choice(A.n_rows, 40, replace=False)])
@@ -372,7 +371,7 @@ def test_large_chunks_many_tiles_exact(pipeline):
     assert info.pipeline == (binding.GM_PIPE_ROWWISE if pipeline == binding.GM_PIPE_AUTO else pipeline)
 
 
-@pytest.mark.parametrize("pipeline", [binding.GM_PIPE_WALK, binding.GM_PIPE_AUTO], ids=["walk", "auto"])
+@pytest.mark.parametrize("pipeline", [binding.GM_PIPE_FUSED_HISTO, binding.GM_PIPE_AUTO], ids=["outer", "auto"])
 @pytest.mark.parametrize("n_hot", [5000, 13000])
 def test_chunk_with_one_hot_column(n_hot, pipeline):
     """A chunk whose elements nearly all fall on one column: one run of equal rank
@@ -415,11 +414,10 @@ def test_multilevel_wide_light_chunks(values, pipeline):
 
 
 @pytest.mark.parametrize("values", ["uniform", "int"])
-def test_walk_needs_strictly_increasing_b_rows(values):
-    """The walk adds a product without an atomic when no other lane holds its rank,
-    which needs every B row to hold each column once. Asked for the walk, a B
-    whose row repeats a column (still sorted) must get the row-order pipeline;
-    both give the oracle's C."""
+def test_sorted_b_rows_that_repeat_a_column(values):
+    """B rows sorted but repeating a column: the row-order expansion still writes
+    each run of a B row into its chunk contiguously, and the repeated column's
+    products add. Both the plain and the repeating B give the oracle's C."""
     A = gi.rmat(11, 8, seed=5, values=values)
     rp, col, val = A.row_ptr, A.col, A.val
     rows = [r for r in range(A.n_rows) if rp[r + 1] - rp[r] >= 2][:50]
@@ -429,9 +427,9 @@ def test_walk_needs_strictly_increasing_b_rows(values):
     B_dup = gi.CSR(A.n_rows, A.n_cols, rp2.astype(np.int64), col2.astype(np.int32), val2)
     B_dup.check()
     assert np.all(np.diff(B_dup.col[B_dup.row_ptr[rows[0]]:B_dup.row_ptr[rows[0] + 1]]) >= 0)
-    cfg = {"tau": 16, "dense_width": 128, "n_chunks_max": 16, "pipeline": binding.GM_PIPE_WALK}
+    cfg = {"tau": 16, "dense_width": 128, "n_chunks_max": 16}
     info = check_full(A, A, exact=values == "int", **cfg)
-    assert info.pipeline == binding.GM_PIPE_WALK
+    assert info.pipeline == binding.GM_PIPE_ROWWISE
     info = check_full(A, B_dup, exact=values == "int", **cfg)
     assert info.pipeline == binding.GM_PIPE_ROWWISE and info.n_heavy_rows > 0
 
@@ -541,16 +539,78 @@ def _sampled_check(name, n_random=400, seed=0, f32=False):
     return info
 
 
+def _full_streamed_check(A, C, block_rows):
+    """Every row of C against the oracle, one block of rows at a time, so that
+    neither the oracle's C nor the GPU's is ever whole on the host."""
+    rp = C.row_ptr.cpu().numpy()
+    assert rp[0] == 0 and rp[-1] == C.col.numel()
+    for r0 in range(0, A.n_rows, block_rows):
+        r1 = min(A.n_rows, r0 + block_rows)
+        ref = oracle.spgemm_rows(A, A, np.arange(r0, r1))
+        lo, hi = int(rp[r0]), int(rp[r1])
+        assert_matches(ref, rp[r0:r1 + 1] - lo, C.col[lo:hi].cpu().numpy(), C.val[lo:hi].cpu().numpy())
+
+
 @pytest.mark.slow
-def test_workload_rmat18_sampled():
-    info = _sampled_check("rmat18")
+def test_workload_rmat18_every_row():
+    """R-MAT scale 18, edge factor 16 (2.9e9 products, 1.28e9 entries of C): every
+    row of C compared with the oracle, structure bit-exact, values within
+    1e-12 * sum|ab|."""
+    A = gi.named_workload("rmat18")
+    Ad = binding.to_device(A)
+    C, info = binding.spgemm(Ad, Ad, return_info=True)
+    torch.cuda.synchronize()
     assert info.n_heavy_rows > 0 and info.params.n_levels == 1
+    _full_streamed_check(A, C, 8192)
+
+
+def _stratified_rows(u, tau, n_heavy, n_light, rng):
+    """Rows drawn evenly from ten strata of u among the heavy rows and among the
+    light rows (so every chunk-size class and both heavy batches appear), plus the
+    six rows with the most products."""
+    picks = [np.argsort(u)[-6:]]
+    for sel, n in ((u > tau, n_heavy), ((u > 0) & (u <= tau), n_light)):
+        ids = np.nonzero(sel)[0]
+        order = ids[np.argsort(u[ids], kind="stable")]
+        for part in np.array_split(order, 10):
+            if part.size:
+                picks.append(rng.choice(part, min(part.size, n // 10), replace=False))
+    return np.unique(np.concatenate(picks))
 
 
 @pytest.mark.slow
-def test_workload_rmat20_sampled():
-    info = _sampled_check("rmat20", n_random=200)
-    assert info.n_heavy_rows > 0
+def test_workload_rmat20_50k_rows():
+    """R-MAT scale 20, edge factor 16 (the benchmark workload): 25,000 heavy and
+    25,000 light rows, stratified by their products, compared row by row with the
+    oracle over each row's full extent; every row checked for the properties that
+    hold at any size (sorted, in range, at most u(i) entries). The opt-in
+    GM_FULL_PARITY_20=1 runs test_workload_rmat20_every_row instead of sampling."""
+    A = gi.named_workload("rmat20")
+    u = oracle.ip_counts(A, A)
+    Ad = binding.to_device(A)
+    C, info = binding.spgemm(Ad, Ad, return_info=True)
+    torch.cuda.synchronize()
+    assert info.ip_total == int(u.sum()) and info.n_heavy_rows == int((u > info.params.tau).sum())
+    assert info.n_batches >= 2
+    check_invariants(C, u)
+    rows = _stratified_rows(u, info.params.tau, 25000, 25000, np.random.default_rng(20))
+    assert rows.size >= 50000
+    for grp in np.array_split(rows, max(1, rows.size // 2000)):
+        ref = oracle.spgemm_rows(A, A, grp)
+        srp, col, val = gather_rows(C, grp)
+        assert_matches(ref, srp, col, val)
+
+
+@pytest.mark.slow
+@pytest.mark.skipif(os.environ.get("GM_FULL_PARITY_20") != "1", reason="opt-in: about 6 minutes of oracle time")
+def test_workload_rmat20_every_row():
+    """Every row of the scale-20 product (9.7e9 entries of C) against the oracle,
+    streamed in blocks of rows."""
+    A = gi.named_workload("rmat20")
+    Ad = binding.to_device(A)
+    C = binding.spgemm(Ad, Ad)
+    torch.cuda.synchronize()
+    _full_streamed_check(A, C, 16384)
 
 
 @pytest.mark.slow
@@ -565,7 +625,7 @@ def test_workload_rmat20_f32_sampled():
 
 # (name, row-pointer dtype, column dtype) at the interface
 INDEX_TYPES = [("rowptr32", np.int32, np.int32), ("col64", np.int64, np.int64), ("both", np.int32, np.int64)]
-INDEX_PLANS = ["auto", "heavy_L0", "heavy_L2", "L2_outer", "L1_walk_128"]
+INDEX_PLANS = ["auto", "heavy_L0", "heavy_L2", "L2_outer", "L1_rowwise_256"]
 
 
 def _index_flags(rp_dt, col_dt):
@@ -671,3 +731,43 @@ def test_c_program_through_the_abi(tmp_path):
         assert C.row_ptr[0] == 0
         assert_matches(oracle.spgemm(a, b), C.row_ptr, C.col, C.val)
     assert " heavy 0 " not in out.stdout
+
+
+@pytest.mark.parametrize("values", ["uniform", "int"])
+def test_light_chunks_wider_than_65536_columns(values):
+    """C.m = 2^19 with chunks of 4 per level down to 4096 columns: four levels
+    (131072, 32768, 8192, 4096 columns). The heavy rows' level-0 chunks hold about
+    750 elements, below tau, so they leave the hierarchy as light chunks 131072
+    columns wide; the bitmap-rank block accumulator then keeps each rank's column
+    in 32 bits (16 bits hold chunk-local columns only up to 65536)."""
+    rng = np.random.default_rng(17)
+    n_mid, n_cols = 3000, 1 << 19
+
+    def rand_csr(n_rows, n_c, per_row):
+        rp = np.arange(n_rows + 1, dtype=np.int64) * per_row
+        col = np.concatenate([np.sort(rng.choice(n_c, per_row, replace=False)) for _ in range(n_rows)])
+        val = (rng.integers(-3, 4, col.size) if values == "int" else rng.uniform(-1, 1, col.size)).astype(np.float64)
+        return gi.CSR(n_rows, n_c, rp, col.astype(np.int32), val)
+
+    A = rand_csr(300, n_mid, 30)
+    B = rand_csr(n_mid, n_cols, 100)
+    info = check_full(A, B, exact=values == "int", tau=2048, dense_width=4096, n_chunks_max=4)
+    assert info.params.n_levels == 4 and info.params.widths[0] == 131072 and info.n_heavy_rows > 250
+
+
+OVERLAP_CASES = [f for f in FORCED if f[0] in ("auto", "heavy_L1", "heavy_L2", "L1_outer", "L1_rowwise_batched")]
+
+
+@pytest.mark.parametrize("name,cfg", OVERLAP_CASES, ids=[f[0] for f in OVERLAP_CASES])
+@pytest.mark.parametrize("values", ["uniform", "int"])
+def test_light_and_heavy_rows_on_two_streams(name, cfg, values):
+    """GM_FLAG_OVERLAP: the light rows run on the plan's second stream while the
+    heavy rows run on its own; the result is the oracle's."""
+    A = gi.rmat(12, 8, seed=6, values=values)
+    info = check_full(A, A, exact=values == "int", flags=binding.GM_FLAG_OVERLAP, **cfg)
+    assert info.n_light_rows > 0 and (name == "auto" or info.n_heavy_rows > 0)
+
+
+def test_two_streams_on_every_light_bin():
+    A, B = _light_rows_case(1 << 20, 5)
+    check_full(A, B, exact=True, flags=binding.GM_FLAG_OVERLAP)

@@ -386,3 +386,40 @@ def test_split_chunks_two_levels_equal_one_finer_split():
     for c0, ch in enumerate(oracle.split_chunks(items, v0, w0)):
         for c1, sub in enumerate(oracle.split_chunks(ch, v1, w1)):
             assert sorted(sub) == sorted(fine[c0 * v1 + c1])
+
+
+# --- the row split over several GPUs -------------------------------------------
+
+def test_row_split_worked_cases():
+    """Hand-worked splits. u = [5, 0, 3, 8, 2, 2] (T = 20), two parts: the target
+    10 lies between S(3) = 8 and S(4) = 16, nearer 8, so rows [0, 3) and [3, 6)
+    (8 and 12 products). Equal rows split evenly; no products split rows evenly;
+    one giant row stays alone."""
+    assert oracle.row_split([5, 0, 3, 8, 2, 2], 2).tolist() == [0, 3, 6]
+    assert oracle.row_split([1] * 10, 5).tolist() == [0, 2, 4, 6, 8, 10]
+    assert oracle.row_split([0, 0, 0], 2).tolist() == [0, 1, 3]
+    assert oracle.row_split([100, 1, 1, 1], 3).tolist() == [0, 0, 1, 4]
+    assert oracle.row_split([7], 1).tolist() == [0, 1]
+    assert oracle.row_split([], 3).tolist() == [0, 0, 0, 0]
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("n_parts", [1, 2, 3, 8])
+def test_row_split_balances_products(seed, n_parts):
+    """Every split covers the rows once, in order, and no part is further from
+    T / n_parts than the largest row's products (each bound sits next to its
+    target); on R-MAT row counts, against a brute-force search over all bounds of
+    the best achievable balance for two parts."""
+    rng = np.random.default_rng(seed)
+    u = rng.integers(0, 50, 40) * (rng.random(40) < 0.8)
+    b = oracle.row_split(u, n_parts)
+    assert b[0] == 0 and b[-1] == u.size and np.all(np.diff(b) >= 0)
+    T = int(u.sum())
+    parts = [int(u[b[q]:b[q + 1]].sum()) for q in range(n_parts)]
+    assert sum(parts) == T
+    S = np.concatenate([[0], np.cumsum(u)])
+    for q in range(1, n_parts):  # each bound is at most one row away from its target
+        assert abs(n_parts * S[b[q]] - q * T) <= n_parts * max(int(u.max()), 0)
+    if n_parts == 2:
+        best = min(abs(2 * int(S[r]) - T) for r in range(u.size + 1))
+        assert abs(2 * int(S[b[1]]) - T) == best
