@@ -11,7 +11,9 @@ import os
 from dataclasses import dataclass
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libgm_spgemm.so")
+# GM_SPGEMM_CHECKED=1 selects the GM_BOUNDS_CHECK build of the library (build.py)
+LIB_PATH = os.path.join(HERE, "libgm_spgemm_checked.so" if os.environ.get("GM_SPGEMM_CHECKED") == "1"
+                        else "libgm_spgemm.so")
 
 GM_MAX_LEVELS = 16
 GM_NUM_STAGES = 16

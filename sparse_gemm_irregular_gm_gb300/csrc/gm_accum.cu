@@ -102,8 +102,10 @@ __global__ void __launch_bounds__(WARPS * 32) k_light_warp(LightArgs a) {
         const int32_t c = key[i];
         for (int t = i; t < nn && key[t] == c; ++t) s += val[t];
         const int rank = run + __popc(hb & lanemask_lt());
-        a.c_col[out + rank] = c;
-        c_val[out + rank] = s;
+        if (GM_CHECKED(out + rank < a.c_nnz, a.status)) {
+          a.c_col[out + rank] = c;
+          c_val[out + rank] = s;
+        }
       }
       run += __popc(hb);
     }
@@ -145,7 +147,7 @@ __device__ __forceinline__ int hash_insert(int32_t* keys, int cap, int32_t c, bo
 // them by column and write nnz entries at out. keys/vals hold cap slots.
 template <typename V>
 __device__ void compact_sort_write(int32_t* keys, V* vals, int cap, int nnz, int32_t* c_col, V* c_val,
-                                   int64_t out, int64_t col_base) {
+                                   int64_t out, int64_t col_base, int64_t c_nnz, int* status) {
   __shared__ int ws[33];
   int run = 0;
   for (int base = 0; base < cap; base += blockDim.x) {
@@ -187,8 +189,10 @@ __device__ void compact_sort_write(int32_t* keys, V* vals, int cap, int nnz, int
     }
   }
   for (int i = threadIdx.x; i < nnz; i += blockDim.x) {
-    c_col[out + i] = static_cast<int32_t>(col_base + keys[i]);
-    c_val[out + i] = vals[i];
+    if (GM_CHECKED(out + i < c_nnz, status)) {
+      c_col[out + i] = static_cast<int32_t>(col_base + keys[i]);
+      c_val[out + i] = vals[i];
+    }
   }
 }
 
@@ -231,7 +235,7 @@ __global__ void k_light_hash(LightArgs a, int cap) {
     } else {
       const int64_t out = a.c_rp[r];
       const int nnz = static_cast<int>(a.c_rp[r + 1] - out);
-      compact_sort_write(keys, vals, cap, nnz, a.c_col, c_val, out, 0);
+      compact_sort_write(keys, vals, cap, nnz, a.c_col, c_val, out, 0, a.c_nnz, a.status);
     }
     __syncthreads();
   }
@@ -327,8 +331,10 @@ __global__ void k_leaf_bitmap(ListArgs a, int nwords, int cap_vals) {
       while (bits) {
         const int b = __ffs(bits) - 1;
         bits &= bits - 1;
-        a.c_col[out + pos] = static_cast<int32_t>(cb + w * 32 + b);
-        c_val[out + pos] = vals[pos];
+        if (GM_CHECKED(out + pos < a.c_nnz, a.status)) {
+          a.c_col[out + pos] = static_cast<int32_t>(cb + w * 32 + b);
+          c_val[out + pos] = vals[pos];
+        }
         ++pos;
       }
     }
@@ -433,8 +439,10 @@ __global__ void __launch_bounds__(T) k_leaf_small(ListArgs a, int nwords) {
     for (int r = threadIdx.x; r < nnz; r += T) {
       V sum = 0.0;
       for (int q = seg[r]; q < seg[r + 1]; ++q) sum += vbuf[q];
-      a.c_col[out + r] = static_cast<int32_t>(cb + cols[r]);
-      c_val[out + r] = sum;
+      if (GM_CHECKED(out + r < a.c_nnz, a.status)) {
+        a.c_col[out + r] = static_cast<int32_t>(cb + cols[r]);
+        c_val[out + r] = sum;
+      }
     }
     __syncthreads();
   }
@@ -499,6 +507,7 @@ __global__ void __launch_bounds__(32 * WARPS, (ITEMS >= 16 ? 160 : 256) / WARPS)
       base += __shfl_sync(kFull, inc, 31);
     }
     const int nnz = base;
+    if (a.expect_nnz) GM_CHECKED(nnz == a.expect_nnz[a.child_base + child_local], a.status);
     for (int i = lane; i < nnz; i += 32) vals[i] = 0.0;
     __syncwarp();
     for (int t0 = 0; t0 < n; t0 += CAPW) {  // values into their rank's slot
@@ -525,8 +534,10 @@ __global__ void __launch_bounds__(32 * WARPS, (ITEMS >= 16 ? 160 : 256) / WARPS)
       while (bits) {
         const int b = __ffs(bits) - 1;
         bits &= bits - 1;
-        a.c_col[out + pos] = static_cast<int32_t>(cb + w * 32 + b);
-        c_val[out + pos] = vals[pos];
+        if (GM_CHECKED(out + pos < a.c_nnz, a.status)) {
+          a.c_col[out + pos] = static_cast<int32_t>(cb + w * 32 + b);
+          c_val[out + pos] = vals[pos];
+        }
         ++pos;
       }
     }
@@ -588,6 +599,7 @@ __global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap,
       __syncthreads();
     }
     const int nnz = base;
+    if (a.expect_nnz && threadIdx.x == 0) GM_CHECKED(nnz == a.expect_nnz[a.child_base + child_local], a.status);
     if (nnz > vcap) {  // uniform: the chunk's class promised at most vcap columns
       if (threadIdx.x == 0) atomicOr(a.status, kStInternal);
       __syncthreads();
@@ -626,8 +638,10 @@ __global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap,
       }
       __syncthreads();
       for (int r = threadIdx.x; r < nnz; r += T) {
-        a.c_col[out + r] = static_cast<int32_t>(cb + colr[r]);
-        c_val[out + r] = vals[r];
+        if (GM_CHECKED(out + r < a.c_nnz, a.status)) {
+          a.c_col[out + r] = static_cast<int32_t>(cb + colr[r]);
+          c_val[out + r] = vals[r];
+        }
       }
     }
     __syncthreads();
@@ -690,8 +704,10 @@ __global__ void __launch_bounds__(WARPS * 32) k_leaf_warp(ListArgs a) {
         const int32_t c = key[i];
         for (int t = i; t < n && key[t] == c; ++t) sum += val[t];
         const int r = run + __popc(hb & lanemask_lt());
-        a.c_col[out + r] = static_cast<int32_t>(cb + c);
-        c_val[out + r] = sum;
+        if (GM_CHECKED(out + r < a.c_nnz, a.status)) {
+          a.c_col[out + r] = static_cast<int32_t>(cb + c);
+          c_val[out + r] = sum;
+        }
       }
       run += __popc(hb);
     }
@@ -732,7 +748,7 @@ __global__ void k_leaf_hash(ListArgs a, int cap) {
       if (threadIdx.x == 0) a.nnz_out[a.child_base + child_local] = nnz;
     } else {
       compact_sort_write(keys, vals, cap, nnz, a.c_col, c_val, a.off_in[a.child_base + child_local],
-                         leaf_col_base(a, child_local));
+                         leaf_col_base(a, child_local), a.c_nnz, a.status);
     }
     __syncthreads();
   }

@@ -753,6 +753,8 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
   // chunks of more than 4096 elements: streamed through shared memory by bulk copies
   const bool stream_ok = (exp_flags() & 8) && leaf_stream_fits(la.width, la.col16, p->smem_dev, p->vb);
   la.counter = p->work_counter.p;
+  la.c_nnz = p->c_nnz;
+  la.expect_nnz = by_nnz ? p->leaf_nnz.p : nullptr;
   DevBuf<uint8_t> bins;
   DevBuf<int32_t> idx;
   DevBuf<int64_t> starts_d, items;
@@ -845,7 +847,7 @@ static gm_status rowwise_leaves(gm_plan* p, int64_t nb, const int64_t* rrp, cons
 // cursor[c] (child c = batch row * v0 + chunk) is where chunk c's elements start
 // in the caller's layout; columns are stored chunk-local (16 bits with col16).
 static gm_status expand_into_chunks(gm_plan* p, int64_t h0, int64_t h1, unsigned long long* cursor, void* out_col,
-                                    void* out_val, bool col16, bool numeric) {
+                                    void* out_val, bool col16, bool numeric, const int64_t* chunk_rp = nullptr) {
   const cudaStream_t s = p->s;
   const int64_t nb = h1 - h0;
   const int64_t ip = p->h_chat_rp[h1] - p->h_chat_rp[h0];
@@ -890,6 +892,7 @@ static gm_status expand_into_chunks(gm_plan* p, int64_t h0, int64_t h1, unsigned
   ra.out_val = out_val;
   ra.unit_counter = p->work_counter.p;
   ra.status = p->status.p;
+  ra.chunk_rp = chunk_rp;
   launch_row_runs(ra, p->num_sms, s);
   p->stage_end(t);
   return cuda_status(p, cudaGetLastError());
@@ -916,7 +919,8 @@ static gm_status run_batch_runs(gm_plan* p, int64_t h0, int64_t h1, int64_t* par
   sub_to_u64(rrp.p, children, 0, cur.p, s);
   p->stage_end(t);
   const bool col16 = p->arena_cb == 2;  // chunk-local columns in 16 bits: 10 (or 6) bytes a product
-  const gm_status st = expand_into_chunks(p, h0, h1, cur.p, p->arena_col[0].p, p->arena_val[0].p, col16, true);
+  const gm_status st =
+      expand_into_chunks(p, h0, h1, cur.p, p->arena_col[0].p, p->arena_val[0].p, col16, true, rrp.p);
   if (st != GM_OK) return st;
   cur.release();
   return rowwise_leaves(p, nb, rrp.p, mcount, par_base, c_col, c_val, col16);
@@ -1351,7 +1355,8 @@ static gm_status plan_and_alloc(gm_plan* p, int64_t bytes_per_ip, bool with_val,
   int64_t cap = workspace_cap(p);
   for (int attempt = 0; attempt < 6; ++attempt) {
     gm_status st = plan_batches(p, bytes_per_ip, cap, batches);
-    if (st != GM_OK) return st;
+    // after a failed arena, a budget halved below one row's needs is still an allocation failure
+    if (st != GM_OK) return attempt == 0 ? st : GM_ERR_OOM;
     st = alloc_arena(p, batches, with_val, nbuf);
     if (st == GM_OK) return GM_OK;
     free_arena(p);
@@ -1410,6 +1415,7 @@ static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, void* c_val, 
       ra.c_val = c_val;
       ra.work_counter = counter;
       ra.status = status;
+      ra.c_nnz = p->c_nnz;
       launch_rowbm_light(ra, !numeric, cap, p->num_sms, p->smem_dev, on);
       continue;
     }
@@ -1427,6 +1433,7 @@ static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, void* c_val, 
     la.c_col = c_col;
     la.c_val = c_val;
     la.status = status;
+    la.c_nnz = p->c_nnz;
     launch_light_rows(la, light_bin_cap(b, p->P.tau, p->smem_dev, p->vb), !numeric, on);
   }
 }

@@ -26,7 +26,18 @@ enum : int {
   kStGroupRows = 1 << 5,    // a multisplit work group met more rows than planned
   kStInternal = 1 << 6,     // an internal consistency check failed
   kStWaitTimeout = 1 << 7,  // a bounded wait inside a kernel gave up
+  kStBounds = 1 << 8,       // GM_BOUNDS_CHECK builds: a cursor or slot outside its range
 };
+
+// GM_BOUNDS_CHECK builds check the index of every write of C and of the chunk
+// elements before it is made: an index out of its range sets kStBounds in the
+// status word and the write is skipped (never a trap). Other builds compile the
+// checks away.
+#ifdef GM_BOUNDS_CHECK
+#define GM_CHECKED(cond, status) ((cond) || (atomicOr((status), ::gm::kStBounds), false))
+#else
+#define GM_CHECKED(cond, status) true
+#endif
 
 constexpr int kMaxBins = 16;
 
@@ -260,6 +271,7 @@ struct RowRunArgs {
   bool col16;
   unsigned* unit_counter;
   int* status;
+  const int64_t* chunk_rp;    // GM_BOUNDS_CHECK: chunk c's elements lie in [chunk_rp[c], chunk_rp[c+1]) (null: unchecked)
 };
 int64_t row_runs_unit(int64_t tau);
 void launch_row_runs(const RowRunArgs& a, int num_sms, cudaStream_t s);
@@ -289,6 +301,7 @@ struct LightArgs {
   void* c_val;
   int* status;
   bool f32;
+  int64_t c_nnz;              // GM_BOUNDS_CHECK: entries of C (numeric)
 };
 // Light rows of one bin: cap = table slots (>= 2 * max u in bin).
 void launch_light_rows(const LightArgs& a, int bin_cap, bool symbolic, cudaStream_t s);
@@ -312,6 +325,8 @@ struct ListArgs {
   int* status;
   bool f32;
   unsigned int* counter;      // dynamic chunk scheduling (launch_leaf_stream)
+  int64_t c_nnz;              // GM_BOUNDS_CHECK: entries of C (numeric)
+  const int64_t* expect_nnz;  // GM_BOUNDS_CHECK: the symbolic pass's nnz of each chunk (null: unchecked)
 };
 // Chunks narrower than the dense width: shared-memory bitmap + rank accumulator.
 void launch_leaf_bitmap(const ListArgs& a, int cap_vals, bool symbolic, cudaStream_t s);
@@ -361,6 +376,7 @@ struct RowBitmapArgs {
   unsigned int* work_counter; // device counter for dynamic row scheduling
   int* status;
   bool f32;
+  int64_t c_nnz;              // GM_BOUNDS_CHECK: entries of C (numeric)
 };
 int64_t rowbm_symbolic_smem(int64_t c_m);
 // Words of a whole-row bitmap of C.m columns (whole 16-byte pieces).

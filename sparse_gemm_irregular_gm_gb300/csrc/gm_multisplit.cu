@@ -736,6 +736,12 @@ __global__ void __launch_bounds__(kRrWarps * 32, 5) k_expand_rows(RowRunArgs a) 
           const int q = qb + u * 32 + lane;
           if (q < q1) {
             const int64_t dst = s_base[w][col[u] >> a.shift] + q;
+#ifdef GM_BOUNDS_CHECK
+            if (a.chunk_rp) {  // inside the (row, chunk) range the symbolic pass counted
+              const int64_t ch = static_cast<int64_t>(row0 + slot) * v + (col[u] >> a.shift);
+              if (!GM_CHECKED(dst >= a.chunk_rp[ch] && dst < a.chunk_rp[ch + 1], a.status)) continue;
+            }
+#endif
             // written once, read once by the accumulators: streaming stores, so that
             // they do not push B and the cursors out of L2
             __stcs(out_col + dst, static_cast<CT>(col[u] & mask));

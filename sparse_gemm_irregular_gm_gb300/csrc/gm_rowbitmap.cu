@@ -380,8 +380,10 @@ __global__ void __launch_bounds__(kRbThreads, 1)
           while (bits) {
             const int b = __ffs(bits) - 1;
             bits &= bits - 1;
-            a.c_col[out + done + pos] = static_cast<int32_t>(base + (g * kGroupWords + x) * 32 + b);
-            c_val[out + done + pos] = vals[pos];
+            if (GM_CHECKED(out + done + pos < a.c_nnz, a.status)) {
+              a.c_col[out + done + pos] = static_cast<int32_t>(base + (g * kGroupWords + x) * 32 + b);
+              c_val[out + done + pos] = vals[pos];
+            }
             ++pos;
           }
         }

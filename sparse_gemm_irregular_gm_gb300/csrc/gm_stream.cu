@@ -247,6 +247,7 @@ __global__ void __launch_bounds__(kConsumers + 32, 1) k_leaf_stream(ListArgs a, 
 #pragma unroll 4
     for (int i = tid; i < h.n; i += kConsumers) {
       const uint32_t c = static_cast<uint32_t>(cs[i]);
+      if (!GM_CHECKED(c < static_cast<uint32_t>(width), a.status)) continue;
       atomicOr(&bm[c >> 5], 1u << (c & 31));
       atomicAdd(&vals[c], vs[i]);
     }
@@ -272,14 +273,17 @@ __global__ void __launch_bounds__(kConsumers + 32, 1) k_leaf_stream(ListArgs a, 
       ok = false;
       break;
     }
+    if (a.expect_nnz && tid == 0) GM_CHECKED(total == a.expect_nnz[a.child_base + child_local], a.status);
     for (int j = 0; j < per; ++j) {
       const int w = w0 + j;
       uint32_t bits = bm[w];
       while (bits) {
         const int col = w * 32 + __ffs(bits) - 1;
         bits &= bits - 1;
-        a.c_col[out + pos] = static_cast<int32_t>(cbase + col);
-        c_val[out + pos] = vals[col];
+        if (GM_CHECKED(out + pos < a.c_nnz, a.status)) {
+          a.c_col[out + pos] = static_cast<int32_t>(cbase + col);
+          c_val[out + pos] = vals[col];
+        }
         vals[col] = V(0);
         ++pos;
       }
