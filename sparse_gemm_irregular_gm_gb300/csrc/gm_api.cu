@@ -35,14 +35,6 @@ void note_launch(int n) {
 }
 int64_t launch_count() { return g_launches.load(); }
 
-int exp_flags() {
-  static const int f = [] {
-    const char* e = std::getenv("GM_EXP");
-    return e ? std::atoi(e) : 0;
-  }();
-  return f;
-}
-
 static bool env_log_enabled() {
   static const bool on = [] {
     const char* e = std::getenv("GM_SPGEMM_LOG");
@@ -139,9 +131,11 @@ __global__ void k_i32_gather_to_i64(const int32_t* __restrict__ perm, int64_t n,
     out[i] = perm[i] + add;
 }
 
-// Size class of a last-level chunk for the numeric accumulators: 0 empty,
-// 1 (<= 128 elements, one warp sorts), 2 (<= 1024) and 3 (<= 4096) in registers,
-// 4 / 5 / 6 with a value array of 4096 / 8192 / width entries chosen by nnz.
+// Size class of a last-level chunk for the numeric accumulators: 0 empty; by
+// elements 1 (<= 128), 2 (<= 512), 7 (<= 1024): one warp a chunk; 8 (<= 2048),
+// 3 (<= 4096): one block; more elements, by columns: 4 (<= 4096), 5 (<= 8192)
+// one block, 6 (more) one block with a value array of the chunk's width, or with
+// double values the streamed accumulator.
 __global__ void k_leaf_class(const int64_t* __restrict__ mcount, const int64_t* __restrict__ nnz, int64_t n,
                              int64_t nnz_base, uint8_t* __restrict__ cls) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -750,8 +744,10 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
   if (by_nnz) spec.nbins = 9;
   const bool warp_ok = leaf_warpbm_fits(la.width, 1024, p->smem_dev, p->vb);
   const bool blk4k_ok = leaf_blkbm_fits(la.width, 4096, p->smem_dev, p->vb);
-  // chunks of more than 4096 elements: streamed through shared memory by bulk copies
-  const bool stream_ok = (exp_flags() & 8) && leaf_stream_fits(la.width, la.col16, p->smem_dev, p->vb);
+  // chunks of more than 8192 columns with double values: streamed through shared
+  // memory by bulk copies (measured faster than the block accumulator there, slower
+  // for smaller chunks and for float values)
+  const bool stream_ok = !p->f32 && leaf_stream_fits(la.width, la.col16, p->smem_dev, p->vb);
   la.counter = p->work_counter.p;
   la.c_nnz = p->c_nnz;
   la.expect_nnz = by_nnz ? p->leaf_nnz.p : nullptr;
@@ -785,7 +781,7 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
       else if (b == 7 && warp_ok) launch_leaf_warpbm(a, 1024, s);
       else if (b == 8 && blk4k_ok) launch_leaf_blkbm(a, 2048, 2048, s);
       else if (b == 3 && blk4k_ok) launch_leaf_blkbm(a, 4096, 4096, s);
-      else if (b >= 4 && b <= 6 && stream_ok) launch_leaf_stream(a, p->num_sms, s);
+      else if (b == 6 && stream_ok) launch_leaf_stream(a, p->num_sms, s);
       else if (b == 4 && blk4k_ok) launch_leaf_blkbm(a, 4096, INT_MAX, s);
       else if (b == 5 && leaf_blkbm_fits(la.width, 8192, p->smem_dev, p->vb)) launch_leaf_blkbm(a, 8192, INT_MAX, s);
       else if (b == 6 && leaf_blkbm_fits(la.width, static_cast<int>(la.width), p->smem_dev, p->vb))

@@ -52,8 +52,6 @@ struct BinSpec {
 // Every launch site calls note_launch(); plans report the count they caused.
 void note_launch(int n = 1);
 int64_t launch_count();
-// Experimental kernel variants (environment GM_EXP, a bit mask; 0 by default).
-int exp_flags();
 
 // ---- workspace ------------------------------------------------------------
 // Stream-ordered device allocations routed through the caller's hooks (or

@@ -13,9 +13,11 @@
 //    skip at the front.
 //  * the consumer warps wait for a stage, add every element into a dense value
 //    array of the chunk's width (shared fp64 / fp32 atomics) and mark its column
-//    in a bitmap, then release the stage ("empty" mbarrier, one arrival a warp).
-//    After a chunk's last tile they scan the bitmap, write the chunk's row of C
-//    in column order and clear what they used.
+//    with a plain byte store (lanes holding a sorted run of columns would all
+//    meet on one word of a bitmap), then release the stage ("empty" mbarrier,
+//    one arrival a warp). After a chunk's last tile they pack the marks into
+//    bitmap words, scan them, write the chunk's row of C in column order and
+//    clear what they used.
 // Each element is read once from HBM (10 bytes with 16-bit chunk columns and
 // double values), and the copies of the next tiles overlap the adds of the
 // current one. Every wait is bounded in time; a wait that gives up sets
@@ -125,6 +127,21 @@ __device__ __forceinline__ bool consumer_scan(int x, int* ws, uint64_t* bar, uin
   return true;
 }
 
+constexpr int kMaxWordsPerThread = 4;  // bitmap words a consumer thread packs (chunks up to 65536 columns)
+
+// The 32 marks (bytes, 0 or 1) of columns 32w .. 32w + 31 as one bitmap word:
+// multiplying the 4 marks of a 32-bit word by 0x01020408 gathers them into bits
+// 24..27 (no two partial products share a bit, so nothing carries).
+__device__ __forceinline__ uint32_t pack_marks(const uint8_t* m) {
+  const uint4* m4 = reinterpret_cast<const uint4*>(m);
+  const uint4 q0 = m4[0], q1 = m4[1];
+  const uint32_t x[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+  uint32_t bits = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) bits |= (((x[i] & 0x01010101u) * 0x01020408u) >> 24 & 0xFu) << (4 * i);
+  return bits;
+}
+
 __device__ __forceinline__ int64_t chunk_col_base(const ListArgs& a, int64_t child_local) {
   const int64_t parent = child_local / a.v;
   const int64_t base = a.parent_colbase ? a.parent_colbase[parent] : 0;
@@ -142,8 +159,8 @@ __global__ void __launch_bounds__(kConsumers + 32, 1) k_leaf_stream(ListArgs a, 
   extern __shared__ __align__(128) unsigned char smem[];
   const int width = nwords * 32;
   V* vals = reinterpret_cast<V*>(smem);                                // width
-  uint32_t* bm = reinterpret_cast<uint32_t*>(vals + width);             // nwords
-  unsigned char* stages = reinterpret_cast<unsigned char*>(bm + nwords);  // kStages * kStageBytes, 16-aligned
+  uint8_t* touched = reinterpret_cast<uint8_t*>(vals + width);         // width: 1 where a column was met
+  unsigned char* stages = touched + width;                             // kStages * kStageBytes, 16-aligned
   __shared__ StageHdr hdr[kStages];
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], cbar;
   __shared__ int ws[33];
@@ -151,7 +168,7 @@ __global__ void __launch_bounds__(kConsumers + 32, 1) k_leaf_stream(ListArgs a, 
 
   const int tid = threadIdx.x;
   for (int i = tid; i < width; i += blockDim.x) vals[i] = V(0);
-  for (int i = tid; i < nwords; i += blockDim.x) bm[i] = 0u;
+  for (int i = tid; i < width / 16; i += blockDim.x) reinterpret_cast<uint4*>(touched)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -248,7 +265,7 @@ __global__ void __launch_bounds__(kConsumers + 32, 1) k_leaf_stream(ListArgs a, 
     for (int i = tid; i < h.n; i += kConsumers) {
       const uint32_t c = static_cast<uint32_t>(cs[i]);
       if (!GM_CHECKED(c < static_cast<uint32_t>(width), a.status)) continue;
-      atomicOr(&bm[c >> 5], 1u << (c & 31));
+      touched[c] = 1;
       atomicAdd(&vals[c], vs[i]);
     }
     __syncwarp();
@@ -266,17 +283,24 @@ __global__ void __launch_bounds__(kConsumers + 32, 1) k_leaf_stream(ListArgs a, 
     const int64_t cbase = chunk_col_base(a, child_local);
     const int per = nwords / kConsumers;  // words a thread, consecutive (nwords is a multiple of kConsumers)
     const int w0 = tid * per;
+    uint32_t words[kMaxWordsPerThread];
     int cnt = 0;
-    for (int j = 0; j < per; ++j) cnt += __popc(bm[w0 + j]);
+#pragma unroll
+    for (int j = 0; j < kMaxWordsPerThread; ++j) {
+      words[j] = j < per ? pack_marks(touched + (w0 + j) * 32) : 0u;
+      cnt += __popc(words[j]);
+    }
     int pos = 0, total = 0;
     if (!consumer_scan(cnt, ws, &cbar, cphase, &pos, &total)) {
       ok = false;
       break;
     }
     if (a.expect_nnz && tid == 0) GM_CHECKED(total == a.expect_nnz[a.child_base + child_local], a.status);
-    for (int j = 0; j < per; ++j) {
+#pragma unroll
+    for (int j = 0; j < kMaxWordsPerThread; ++j) {
+      if (j >= per) break;
       const int w = w0 + j;
-      uint32_t bits = bm[w];
+      uint32_t bits = words[j];
       while (bits) {
         const int col = w * 32 + __ffs(bits) - 1;
         bits &= bits - 1;
@@ -287,7 +311,9 @@ __global__ void __launch_bounds__(kConsumers + 32, 1) k_leaf_stream(ListArgs a, 
         vals[col] = V(0);
         ++pos;
       }
-      bm[w] = 0u;
+      uint4* t4 = reinterpret_cast<uint4*>(touched + w * 32);
+      t4[0] = make_uint4(0u, 0u, 0u, 0u);
+      t4[1] = make_uint4(0u, 0u, 0u, 0u);
     }
     if (!consumers_sync(&cbar, cphase)) {
       ok = false;
@@ -299,7 +325,7 @@ __global__ void __launch_bounds__(kConsumers + 32, 1) k_leaf_stream(ListArgs a, 
 
 template <typename V, typename CT>
 size_t stream_smem(int nwords) {
-  return static_cast<size_t>(nwords) * 32 * sizeof(V) + static_cast<size_t>(nwords) * 4 +
+  return static_cast<size_t>(nwords) * 32 * sizeof(V) + static_cast<size_t>(nwords) * 32 +
          static_cast<size_t>(kStages) * (col_stage_bytes<CT>() + val_stage_bytes<V>());
 }
 

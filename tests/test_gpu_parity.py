@@ -368,6 +368,12 @@ def test_large_chunks_many_tiles_exact(pipeline):
     As = _rows_of(A, rows)
     info = check_full(As, A, exact=True, pipeline=pipeline)
     assert info.n_heavy_rows >= 40 and u[rows].max() > 16 * 4096
+    # some chunks have more than 8192 columns: with double values the streamed
+    # accumulator (bulk copies into shared memory) takes them in the row-order pipeline
+    ref = oracle.spgemm(As, A)
+    widest = max(np.bincount(ref.col[ref.row_ptr[i]:ref.row_ptr[i + 1]] >> 14).max() for i in range(As.n_rows)
+                 if ref.row_ptr[i + 1] > ref.row_ptr[i])
+    assert widest > 8192
     assert info.pipeline == (binding.GM_PIPE_ROWWISE if pipeline == binding.GM_PIPE_AUTO else pipeline)
 
 
