@@ -8,8 +8,14 @@
  * File layout (little endian): int64 n_rows, n_cols, nnz; int64 row_ptr[n_rows + 1];
  * int32 col[nnz]; double val[nnz].
  *
- * Usage: c_abi_driver A.bin B.bin C.bin. Exit status 0 on success, 2 when a
- * library call fails (its gm_status_string is printed), 1 on any other error.
+ * Usage: c_abi_driver A.bin B.bin C.bin [parts]. With parts > 1 the product is
+ * computed the way one rank of a multi-GPU run computes its share, here one part
+ * after another: gm_spgemm_row_split cuts A's rows into parts of about equal
+ * products, each part runs gm_spgemm_analyze_rows, symbolic and numeric, and
+ * gm_row_ptr_shift places its row pointers behind the entries of the parts
+ * before it; the parts are put together on the host.
+ * Exit status 0 on success, 2 when a library call fails (its gm_status_string is
+ * printed), 1 on any other error.
  */
 #include <stdint.h>
 #include <stdio.h>
@@ -93,11 +99,53 @@ static int fail(const char* call, gm_status st) {
   return 2;
 }
 
+/* Rows [r0, r1) of C = A * B through the ABI, their row pointers shifted by
+ * base; the part's arrays are copied into C (row pointers r0 .. r1, entries from
+ * base on). Returns 0, or the driver's exit status. */
+static int run_part(const gm_csr* dA, const gm_csr* dB, int64_t r0, int64_t r1, int64_t base, host_csr* C,
+                    int64_t* nnz_out, gm_plan_info* info) {
+  gm_plan* plan = NULL;
+  gm_status st = gm_spgemm_analyze_rows(dA, dB, r0, r1, NULL, NULL, &plan);
+  if (st != GM_OK) return fail("gm_spgemm_analyze_rows", st);
+  const int64_t rows = r1 - r0;
+  void* c_rp = NULL;
+  if (cudaMalloc(&c_rp, (size_t)(rows + 1) * sizeof(int64_t)) != cudaSuccess) return 1;
+  int64_t nnz = -1;
+  st = gm_spgemm_symbolic(plan, c_rp, &nnz);
+  if (st != GM_OK) return fail("gm_spgemm_symbolic", st);
+  void *c_col = NULL, *c_val = NULL;
+  if (nnz > 0 && (cudaMalloc(&c_col, (size_t)nnz * sizeof(int32_t)) != cudaSuccess ||
+                  cudaMalloc(&c_val, (size_t)nnz * sizeof(double)) != cudaSuccess))
+    return 1;
+  st = gm_spgemm_numeric(plan, c_col, c_val);
+  if (st != GM_OK) return fail("gm_spgemm_numeric", st);
+  st = gm_spgemm_plan_info(plan, info);
+  if (st != GM_OK) return fail("gm_spgemm_plan_info", st);
+  gm_spgemm_plan_destroy(plan);
+  st = gm_row_ptr_shift(c_rp, rows + 1, base, 0, NULL);
+  if (st != GM_OK) return fail("gm_row_ptr_shift", st);
+  if (cudaDeviceSynchronize() != cudaSuccess) return 1;
+  C->col = realloc(C->col, (size_t)(base + nnz + 1) * sizeof(int32_t));
+  C->val = realloc(C->val, (size_t)(base + nnz + 1) * sizeof(double));
+  if (!C->col || !C->val) return 1;
+  if (cudaMemcpy(C->row_ptr + r0, c_rp, (size_t)(rows + 1) * sizeof(int64_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return 1;
+  if (nnz > 0 && (cudaMemcpy(C->col + base, c_col, (size_t)nnz * sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess ||
+                  cudaMemcpy(C->val + base, c_val, (size_t)nnz * sizeof(double), cudaMemcpyDeviceToHost) != cudaSuccess))
+    return 1;
+  cudaFree(c_rp);
+  cudaFree(c_col);
+  cudaFree(c_val);
+  *nnz_out = nnz;
+  return 0;
+}
+
 int main(int argc, char** argv) {
-  if (argc != 4) {
-    fprintf(stderr, "usage: %s A.bin B.bin C.bin\n", argv[0]);
+  if (argc != 4 && argc != 5) {
+    fprintf(stderr, "usage: %s A.bin B.bin C.bin [parts]\n", argv[0]);
     return 1;
   }
+  const int64_t parts = argc == 5 ? atoll(argv[4]) : 1;
   host_csr A, B, C;
   if (!read_csr(argv[1], &A) || !read_csr(argv[2], &B)) {
     fprintf(stderr, "cannot read the input matrices\n");
@@ -107,6 +155,34 @@ int main(int argc, char** argv) {
   if (!to_device(&A, &dA) || !to_device(&B, &dB)) {
     fprintf(stderr, "device copies failed\n");
     return 1;
+  }
+
+  if (parts > 1) {  /* the product part by part, as the ranks of a row split compute it */
+    int64_t* bounds = xmalloc((size_t)(parts + 1) * sizeof(int64_t));
+    gm_status st = gm_spgemm_row_split(&dA, &dB, NULL, parts, NULL, bounds);
+    if (st != GM_OK) return fail("gm_spgemm_row_split", st);
+    C.n_rows = A.n_rows;
+    C.n_cols = B.n_cols;
+    C.row_ptr = xmalloc((size_t)(C.n_rows + 1) * sizeof(int64_t));
+    C.col = xmalloc(sizeof(int32_t));
+    C.val = xmalloc(sizeof(double));
+    C.row_ptr[0] = 0;
+    int64_t base = 0, heavy = 0;
+    gm_plan_info info;
+    for (int64_t q = 0; q < parts; ++q) {
+      int64_t nnz = 0;
+      const int rc = run_part(&dA, &dB, bounds[q], bounds[q + 1], base, &C, &nnz, &info);
+      if (rc) return rc;
+      base += nnz;
+      heavy += info.n_heavy_rows;
+    }
+    C.nnz = base;
+    if (!write_csr(argv[3], &C)) {
+      fprintf(stderr, "cannot write C\n");
+      return 1;
+    }
+    printf("nnz %lld heavy %lld parts %lld\n", (long long)base, (long long)heavy, (long long)parts);
+    return 0;
   }
 
   gm_plan* plan = NULL;

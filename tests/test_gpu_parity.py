@@ -737,6 +737,15 @@ def test_c_program_through_the_abi(tmp_path):
         assert C.row_ptr[0] == 0
         assert_matches(oracle.spgemm(a, b), C.row_ptr, C.col, C.val)
     assert " heavy 0 " not in out.stdout
+    # the row split of the multi-GPU run, its parts one after another from C
+    for parts in (2, 5):
+        write_csr(fa, A)
+        write_csr(fb, A)
+        out = subprocess.run([exe, fa, fb, fc, str(parts)], capture_output=True, text=True, timeout=120)
+        assert out.returncode == 0, out.stderr
+        assert f"parts {parts}" in out.stdout and " heavy 0 " not in out.stdout
+        C = read_csr(fc)
+        assert_matches(oracle.spgemm(A, A), C.row_ptr, C.col, C.val)
 
 
 @pytest.mark.parametrize("values", ["uniform", "int"])
