@@ -847,10 +847,16 @@ void launch_leaf_warpbm_t(const ListArgs& a, int max_elems, int nwp, int W, size
 template <typename V, typename CT, typename CR>
 void launch_leaf_blkbm_c(const ListArgs& a, int max_nnz, int max_elems, int nwp, size_t smem, cudaStream_t s) {
   const unsigned g = static_cast<unsigned>(std::min<int64_t>(a.n_items, 152LL * 32));
-  // threads per chunk grow with the value array so that an SM keeps ~1000 threads busy
+  // threads per chunk grow with the value array; float chunks of up to 8192
+  // columns take more threads than double ones (measured: the C = A·A product
+  // of an R-MAT scale-20 matrix is fastest with 256 / 256 threads for doubles
+  // and 256 / 512 for floats)
   if (max_nnz <= 4096) {
-    set_smem(k_leaf_blkbm<V, CT, 8, 128, CR>, smem);
-    (k_leaf_blkbm<V, CT, 8, 128, CR><<<g, 128, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
+    set_smem(k_leaf_blkbm<V, CT, 8, 256, CR>, smem);
+    (k_leaf_blkbm<V, CT, 8, 256, CR><<<g, 256, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
+  } else if (max_nnz <= 8192 && sizeof(V) == 4) {
+    set_smem(k_leaf_blkbm<V, CT, 8, 512, CR>, smem);
+    (k_leaf_blkbm<V, CT, 8, 512, CR><<<g, 512, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
   } else if (max_nnz <= 8192) {
     set_smem(k_leaf_blkbm<V, CT, 8, 256, CR>, smem);
     (k_leaf_blkbm<V, CT, 8, 256, CR><<<g, 256, smem, s>>>(a, nwp, max_nnz, max_elems), note_launch());
