@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(kRbThreads) k_rowbm_symbolic(RowBitmapArgs a, 
 }
 
 constexpr int kGroupWords = 8;  // rank prefix kept per 8 bitmap words (256 columns)
+__host__ __device__ constexpr int64_t light_a16(int64_t b) { return (b + 15) & ~int64_t(15); }
 constexpr int kRlItems = 10;    // products per thread in k_rowbm_light: rows of up to 10240 products
 constexpr int kRlItemsWide = 16; // ... for the symbolic pass and float values: up to 16384 products
 constexpr uint32_t kNoCol = 0xFFFFFFFFu;
@@ -181,7 +182,7 @@ constexpr int64_t kLightSymRegion = 65536;  // entry-table bytes of the symbolic
 // Rank of column c (number of set bits below it) from the 8-word group prefix:
 // the 16-byte half of the group holding c, plus the first half's count when c
 // lies in the second.
-__device__ __forceinline__ int bitmap_rank(const uint32_t* bm, const int* gpre, uint32_t c) {
+__device__ __forceinline__ int bitmap_rank(const uint32_t* bm, const uint16_t* gpre, uint32_t c) {
   const int w = c >> 5, g = w >> 3, wi = w & 7, j = wi & 3;
   const uint4* g4 = reinterpret_cast<const uint4*>(bm + g * kGroupWords);
   int r = gpre[g];
@@ -195,6 +196,40 @@ __device__ __forceinline__ int bitmap_rank(const uint32_t* bm, const int* gpre, 
   return r + __popc(word & ((1u << (c & 31)) - 1u));
 }
 
+// Writes, in increasing order, the index of every group whose bit is set in the
+// group summary gsum (nsw words) to glist and returns their number. Every thread
+// of the block must call it; it ends with a barrier.
+__device__ __forceinline__ int list_groups(const uint32_t* gsum, int nsw, uint16_t* glist, int* ws) {
+  int ng = 0;
+  for (int s0 = 0; s0 < nsw; s0 += blockDim.x) {
+    const int sw = s0 + threadIdx.x;
+    uint32_t w = sw < nsw ? gsum[sw] : 0u;
+    int tot;
+    int off = ng + block_exclusive_scan(__popc(w), ws, &tot);
+    while (w) {
+      const int b = __ffs(w) - 1;
+      w &= w - 1;
+      glist[off++] = static_cast<uint16_t>((sw << 5) + b);
+    }
+    ng += tot;
+    __syncthreads();
+  }
+  return ng;
+}
+
+__device__ __forceinline__ int group_popc(const uint32_t* bm, int g) {
+  const uint4* g4 = reinterpret_cast<const uint4*>(bm + g * kGroupWords);
+  const uint4 q0 = g4[0], q1 = g4[1];
+  return __popc(q0.x) + __popc(q0.y) + __popc(q0.z) + __popc(q0.w) + __popc(q1.x) + __popc(q1.y) + __popc(q1.z) +
+         __popc(q1.w);
+}
+
+__device__ __forceinline__ void zero_group(uint32_t* bm, int g) {
+  uint4* g4 = reinterpret_cast<uint4*>(bm + g * kGroupWords);
+  g4[0] = make_uint4(0u, 0u, 0u, 0u);
+  g4[1] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // Light rows (u <= kRbThreads * kRlItems) with a whole-row bitmap, every product
 // held in registers: thread t takes products t, t + T, ... of the row in row
 // order, so the block's work is balanced whatever the lengths of the B rows.
@@ -203,10 +238,15 @@ __device__ __forceinline__ int bitmap_rank(const uint32_t* bm, const int* gpre, 
 // the index of its entries into every product position they cover, so a
 // product reads its entry in one load. All B loads of a thread are issued
 // before the first is used. The products' columns set the bitmap; then
-//  * symbolic: the row's nnz is the bitmap's popcount (written to c_rp[row]);
-//  * numeric: prefix sums over groups of 8 words give every column its rank,
-//    the values are summed into their rank in shared memory (the entry table's
-//    space is reused) and the row is written in column order.
+//  * symbolic: the row's nnz is the bitmap's popcount (written to c_rp[row]),
+//    and the words are cleared as they are counted;
+//  * numeric: the first bit set in a word also sets its group's bit (8 words,
+//    256 columns) in a summary, and only the groups listed from the summary are
+//    visited afterwards (a light row touches a few thousand of the row's groups
+//    at most): prefix sums over them give every column its rank, the values are
+//    summed into their rank in shared memory (the entry table's space is
+//    reused), the row is written in column order and the listed groups are
+//    cleared. The bitmap is zeroed once per block, not once per row.
 template <typename V, bool SYM, int kRlItems>
 __global__ void __launch_bounds__(kRbThreads, 1)
     k_rowbm_light(RowBitmapArgs a, int nwords, int wwords, int cap, int te_cap, int region_bytes) {
@@ -221,12 +261,22 @@ __global__ void __launch_bounds__(kRbThreads, 1)
   uint16_t* s_ent = reinterpret_cast<uint16_t*>(s_pre + te_cap);          // cap: entry of each product position
   V* vals = reinterpret_cast<V*>(smem);                         // numeric, after the products are loaded
   const int ngroups = (nwords + kGroupWords - 1) / kGroupWords;           // symbolic: the whole row
-  uint32_t* bm = reinterpret_cast<uint32_t*>(smem + region_bytes);        // symbolic ngroups * 8, numeric wwords
-  int* gpre = reinterpret_cast<int*>(bm + wwords);                        // numeric: wwords / 8
+  const int nbw = SYM ? ngroups * kGroupWords : wwords;                   // bitmap words (whole groups)
+  const int nbg = nbw / kGroupWords, nsw = (nbg + 31) / 32;               // groups, summary words
+  uint32_t* bm = reinterpret_cast<uint32_t*>(smem + region_bytes);
+  unsigned char* tail = reinterpret_cast<unsigned char*>(bm + nbw);
+  // numeric only: nbg group prefixes, the nsw-word group summary, the list of up to nbg groups
+  uint16_t* gpre = reinterpret_cast<uint16_t*>(tail);
+  uint32_t* gsum = reinterpret_cast<uint32_t*>(tail + light_a16(static_cast<int64_t>(nbg) * 2));
+  uint16_t* glist = reinterpret_cast<uint16_t*>(reinterpret_cast<unsigned char*>(gsum) +
+                                                light_a16(static_cast<int64_t>(nsw) * 4));
   __shared__ int64_t s_item;
   __shared__ int ws[33];
   constexpr int T = kRbThreads;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  zero_words(bm, nbw);  // rows leave the bitmap and the summary clear
+  if (!SYM)
+    for (int i = threadIdx.x; i < nsw; i += T) gsum[i] = 0u;
   while (true) {
     if (threadIdx.x == 0) s_item = atomicAdd(a.work_counter, 1u);
     __syncthreads();
@@ -234,7 +284,6 @@ __global__ void __launch_bounds__(kRbThreads, 1)
     if (item >= a.n_items) break;
     const int64_t r = a.rows[item];
     const int64_t lo = a.a_rp[r], ne = a.a_rp[r + 1] - lo;
-    if (SYM) zero_words(bm, ngroups * kGroupWords);
     uint32_t col[kRlItems];
     V val[kRlItems];
 #pragma unroll
@@ -306,9 +355,14 @@ __global__ void __launch_bounds__(kRbThreads, 1)
       if (threadIdx.x == 0) atomicOr(a.status, kStInternal);
       continue;  // uniform: every thread saw the same P0
     }
-    if (SYM) {
+    if (SYM) {  // popcount and clear of the whole row (cheaper here than a group summary)
       int n = 0;
-      for (int w = threadIdx.x; w < nwords; w += T) n += __popc(bm[w]);
+      uint4* b4 = reinterpret_cast<uint4*>(bm);
+      for (int i = threadIdx.x; i < nbw / 4; i += T) {
+        const uint4 q = b4[i];
+        n += __popc(q.x) + __popc(q.y) + __popc(q.z) + __popc(q.w);
+        b4[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
       n = warp_reduce_sum(n);
       if (lane == 0) ws[warp] = n;
       __syncthreads();
@@ -327,36 +381,34 @@ __global__ void __launch_bounds__(kRbThreads, 1)
     V* const vals = reinterpret_cast<V*>(smem);                       // cap
     const int64_t out = a.c_rp[r];
     int done = 0;
-    const int ngw = wwords / kGroupWords;
-    const int per_gw = (ngw + T - 1) / T;
-    const int h0 = threadIdx.x * per_gw, h1 = min(ngw, h0 + per_gw);
     for (int64_t base = 0; base < static_cast<int64_t>(nwords) * 32; base += static_cast<int64_t>(wwords) * 32) {
-      zero_words(bm, wwords);
-      __syncthreads();
       uint32_t cw[kRlItems];  // column inside the window, kNoCol outside
 #pragma unroll
       for (int k = 0; k < kRlItems; ++k) {
         const int64_t c = static_cast<int64_t>(col[k]) - base;
         cw[k] = (col[k] != kNoCol && c >= 0 && c < static_cast<int64_t>(wwords) * 32) ? static_cast<uint32_t>(c) : kNoCol;
-        if (cw[k] != kNoCol) atomicOr(&bm[cw[k] >> 5], 1u << (cw[k] & 31));
+        if (cw[k] != kNoCol && atomicOr(&bm[cw[k] >> 5], 1u << (cw[k] & 31)) == 0u)
+          atomicOr(&gsum[cw[k] >> 13], 1u << ((cw[k] >> 8) & 31));  // the word's first bit marks its group
       }
       __syncthreads();
-      // group counts with consecutive groups on consecutive lanes (two 16-byte loads
-      // a group), then a scan over the counts, a few consecutive ints per thread
-      for (int g = threadIdx.x; g < ngw; g += T) {
-        const uint4* g4 = reinterpret_cast<const uint4*>(bm + g * kGroupWords);
-        const uint4 q0 = g4[0], q1 = g4[1];
-        gpre[g] = __popc(q0.x) + __popc(q0.y) + __popc(q0.z) + __popc(q0.w) + __popc(q1.x) + __popc(q1.y) +
-                  __popc(q1.z) + __popc(q1.w);
-      }
-      __syncthreads();
+      // the window's groups in column order; counts of consecutive listed groups
+      // per thread, scanned into group prefixes
+      const int ng = list_groups(gsum, nsw, glist, ws);
+      const int per = (ng + T - 1) / T;
+      const int j0 = min(ng, static_cast<int>(threadIdx.x) * per), j1 = min(ng, j0 + per);
       int acc = 0;
-      for (int g = h0; g < h1; ++g) acc += gpre[g];
+      for (int j = j0; j < j1; ++j) {
+        const int g = glist[j];
+        const int c = group_popc(bm, g);
+        gpre[g] = static_cast<uint16_t>(c);
+        acc += c;
+      }
       int nnz;
       int run = block_exclusive_scan(acc, ws, &nnz);
-      for (int g = h0; g < h1; ++g) {
+      for (int j = j0; j < j1; ++j) {
+        const int g = glist[j];
         const int x = gpre[g];
-        gpre[g] = run;
+        gpre[g] = static_cast<uint16_t>(run);
         run += x;
       }
       if (done + nnz > cap) {  // uniform: the bin promised at most cap products
@@ -369,7 +421,8 @@ __global__ void __launch_bounds__(kRbThreads, 1)
       for (int k = 0; k < kRlItems; ++k)
         if (cw[k] != kNoCol) atomicAdd(&vals[bitmap_rank(bm, gpre, cw[k])], val[k]);
       __syncthreads();
-      for (int g = threadIdx.x; g < ngw; g += T) {  // groups round-robin: adjacent output per warp
+      for (int j = threadIdx.x; j < ng; j += T) {  // listed groups round-robin: adjacent output per warp
+        const int g = glist[j];
         const uint4* g4 = reinterpret_cast<const uint4*>(bm + g * kGroupWords);
         const uint4 q0 = g4[0], q1 = g4[1];
         const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
@@ -387,7 +440,9 @@ __global__ void __launch_bounds__(kRbThreads, 1)
             ++pos;
           }
         }
+        zero_group(bm, g);
       }
+      for (int i = threadIdx.x; i < nsw; i += T) gsum[i] = 0u;
       done += nnz;
       __syncthreads();
     }
@@ -396,6 +451,12 @@ __global__ void __launch_bounds__(kRbThreads, 1)
 
 // Numeric region: the row's values by rank (8 * cap); while a row's products
 // are loaded it holds the entry table and the position map.
+// After the numeric bitmap: 16-bit group prefixes, the group summary and the
+// 16-bit list of the groups it marks, each on a 16-byte boundary.
+int64_t light_tail_bytes(int64_t words, bool symbolic) {
+  const int64_t g = words / kGroupWords;
+  return symbolic ? 0 : light_a16(g * 2) + light_a16((g + 31) / 32 * 4) + light_a16(g * 2);
+}
 int64_t light_region_bytes(int cap, bool symbolic) {
   return symbolic ? kLightSymRegion : ((static_cast<int64_t>(cap) * 8 + 16 + 15) & ~int64_t(15));
 }
@@ -406,9 +467,10 @@ int64_t light_window_words(int64_t c_m, int cap, int64_t smem_max) {
   const int64_t nwords = (c_m + 31) / 32;
   int64_t w = (nwords + kGroupWords - 1) / kGroupWords * kGroupWords;
   while (w >= kGroupWords) {
-    if (light_region_bytes(cap, false) + w * 4 + (w / kGroupWords) * 4 + 4096 <= smem_max) return w;
+    if (light_region_bytes(cap, false) + w * 4 + light_tail_bytes(w, false) + 4096 <= smem_max) return w;
     w = (w / 2 + kGroupWords - 1) / kGroupWords * kGroupWords;
-    if (w == kGroupWords && light_region_bytes(cap, false) + w * 4 + 4 + 4096 > smem_max) return 0;
+    if (w == kGroupWords && light_region_bytes(cap, false) + w * 4 + light_tail_bytes(w, false) + 4096 > smem_max)
+      return 0;
   }
   return 0;
 }
@@ -421,10 +483,10 @@ int64_t rowbm_light_smem(int64_t c_m, int cap, bool symbolic, int64_t smem_max) 
   if (symbolic) {
     const int64_t nwords = (c_m + 31) / 32;
     const int64_t ngroups = (nwords + kGroupWords - 1) / kGroupWords;
-    return light_region_bytes(cap, true) + ngroups * kGroupWords * 4;
+    return light_region_bytes(cap, true) + ngroups * kGroupWords * 4 + light_tail_bytes(ngroups * kGroupWords, true);
   }
   const int64_t w = light_window_words(c_m, cap, smem_max);
-  return light_region_bytes(cap, false) + w * 4 + (w / kGroupWords) * 4;
+  return light_region_bytes(cap, false) + w * 4 + light_tail_bytes(w, false);
 }
 
 bool rowbm_light_fits(int64_t c_m, int cap, bool symbolic, int64_t smem_max, int vb) {

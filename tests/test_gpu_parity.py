@@ -770,6 +770,33 @@ def test_light_chunks_wider_than_65536_columns(values):
     assert info.params.n_levels == 4 and info.params.widths[0] == 131072 and info.n_heavy_rows > 250
 
 
+@pytest.mark.parametrize("values", ["uniform", "int", "f32"])
+def test_light_rows_over_several_column_windows(values):
+    """C.m = 2^21 + 4099: a light row's whole bitmap (256 KB) does not fit beside
+    its values, so the numeric light kernel takes the columns in windows of 2^20
+    columns, the last one ragged. Every row has about 4000 products (light), so
+    each window lists, counts, ranks, writes and clears only its touched groups."""
+    rng = np.random.default_rng(23)
+    n_mid, n_cols = 5000, (1 << 21) + 4099
+
+    def rand_csr(n_rows, n_c, lo, hi):
+        per = rng.integers(lo, hi + 1, n_rows)
+        rp = np.concatenate([[0], np.cumsum(per)]).astype(np.int64)
+        col = np.concatenate([np.sort(rng.choice(n_c, k, replace=False)) for k in per])
+        val = (rng.integers(-3, 4, col.size) if values == "int" else rng.uniform(-1, 1, col.size)).astype(np.float64)
+        return gi.CSR(n_rows, n_c, rp, col.astype(np.int32), val)
+
+    A = rand_csr(400, n_mid, 10, 60)  # u <= 60 * 140 < tau
+    B = rand_csr(n_mid, n_cols, 60, 140)
+    B.col[B.row_ptr[7]] = n_cols - 1  # the last column, in the ragged window
+    B.col[B.row_ptr[7]:B.row_ptr[8]].sort()
+    if values == "f32":
+        info = check_full_f32(A, B)
+    else:
+        info = check_full(A, B, exact=values == "int")
+    assert info.n_heavy_rows == 0 and info.n_light_rows == 400
+
+
 OVERLAP_CASES = [f for f in FORCED if f[0] in ("auto", "heavy_L1", "heavy_L2", "L1_outer", "L1_rowwise_batched")]
 
 
