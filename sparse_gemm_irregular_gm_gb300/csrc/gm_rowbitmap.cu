@@ -328,11 +328,16 @@ __global__ void __launch_bounds__(kRbThreads, 1)
         if (tot > cap && threadIdx.x == 0) atomicOr(a.status, kStInternal);
       }
       __syncthreads();
+      // register slots this tile fills (the same for every thread): the symbolic
+      // pass skips the others (in the numeric pass the branches cost registers)
+      const int k0 = static_cast<int>(min(static_cast<int64_t>(kRlItems), P0 / T));
+      const int k1 = static_cast<int>(min(static_cast<int64_t>(kRlItems), (P0 + tot + T - 1) / T));
       int ent[kRlItems];
 #pragma unroll
       for (int k = 0; k < kRlItems; ++k) {
-        const int64_t rel = static_cast<int64_t>(k) * T + threadIdx.x - P0;
         ent[k] = -1;
+        if (SYM && (k < k0 || k >= k1)) continue;
+        const int64_t rel = static_cast<int64_t>(k) * T + threadIdx.x - P0;
         if (rel >= 0 && rel < tot && rel < cap) {
           const int lo_i = s_ent[rel];
           ent[k] = lo_i;
@@ -343,7 +348,7 @@ __global__ void __launch_bounds__(kRbThreads, 1)
       }
 #pragma unroll
       for (int k = 0; k < kRlItems; ++k) {
-        if (ent[k] >= 0) {
+        if ((!SYM || (k >= k0 && k < k1)) && ent[k] >= 0) {
           if (!SYM) val[k] *= s_av[ent[k]];
           if (SYM) atomicOr(&bm[col[k] >> 5], 1u << (col[k] & 31));
         }
@@ -507,10 +512,23 @@ void launch_rowbm_light(const RowBitmapArgs& a, bool symbolic, int cap, int num_
   const int wwords = symbolic ? 0 : static_cast<int>(light_window_words(a.c_m, cap, smem_max));
   const size_t smem = static_cast<size_t>(rowbm_light_smem(a.c_m, cap, symbolic, smem_max));
   const int64_t blocks = std::min<int64_t>(a.n_items, num_sms);
-  const bool wide = cap > kRbThreads * kRlItems;  // only symbolic passes and float values get here
-  auto fn = symbolic ? (wide ? k_rowbm_light<double, true, kRlItemsWide> : k_rowbm_light<double, true, kRlItems>)
-            : a.f32  ? (wide ? k_rowbm_light<float, false, kRlItemsWide> : k_rowbm_light<float, false, kRlItems>)
-                     : k_rowbm_light<double, false, kRlItems>;
+  // products a thread holds: the fewest that cover the bin's cap, so that the
+  // unrolled per-product loops carry no empty slots (more than kRlItems only for
+  // symbolic passes and float values)
+  const int items = cap <= 2 * kRbThreads ? 2 : cap <= 4 * kRbThreads ? 4 : cap <= 8 * kRbThreads ? 8
+                    : cap <= kRlItems * kRbThreads ? kRlItems : kRlItemsWide;
+  auto pick = [items](auto f2, auto f4, auto f8, auto f10, auto f16) {
+    return items == 2 ? f2 : items == 4 ? f4 : items == 8 ? f8 : items == kRlItems ? f10 : f16;
+  };
+  auto fn = symbolic ? pick(k_rowbm_light<double, true, 2>, k_rowbm_light<double, true, 4>,
+                            k_rowbm_light<double, true, 8>, k_rowbm_light<double, true, kRlItems>,
+                            k_rowbm_light<double, true, kRlItemsWide>)
+            : a.f32  ? pick(k_rowbm_light<float, false, 2>, k_rowbm_light<float, false, 4>,
+                            k_rowbm_light<float, false, 8>, k_rowbm_light<float, false, kRlItems>,
+                            k_rowbm_light<float, false, kRlItemsWide>)
+                     : pick(k_rowbm_light<double, false, 2>, k_rowbm_light<double, false, 4>,
+                            k_rowbm_light<double, false, 8>, k_rowbm_light<double, false, kRlItems>,
+                            k_rowbm_light<double, false, kRlItems>);
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   (fn<<<static_cast<unsigned>(blocks), kRbThreads, smem, s>>>(a, nwords, wwords, cap, te_cap,
                                                                static_cast<int>(region)), note_launch());
