@@ -364,6 +364,8 @@ struct gm_plan {
   gm::DevBuf<int64_t> anz;          // prefix of nnz(A[x_heavy[h], :]) (n_heavy + 1)
   gm::DevBuf<int64_t> cnt0;         // row-order pipeline: elements of each level-0 chunk (n_heavy * v0)
   gm::DevBuf<int32_t> bcp;          // row-order pipeline: per-B-row level-0 chunk starts (B.n_rows * (v0 + 1))
+  gm::DevBuf<int64_t> bct;          // numeric, chunk-direct: chunk-major starts of B's copy
+  gm::DevBuf<uint8_t> bc_col, bc_val;  // ... and the chunk-major copy of B (live during numeric)
   std::vector<int64_t> h_chat_rp;   // host copy of chat_rp
   std::vector<int64_t> h_anz;       // prefix of nnz(A[x_heavy[h], :])
   gm::GrowBuf nnz[GM_MAX_LEVELS];        // per level, per child: nnz (symbolic) then output offset
@@ -894,6 +896,46 @@ static gm_status expand_into_chunks(gm_plan* p, int64_t h0, int64_t h1, unsigned
   return cuda_status(p, cudaGetLastError());
 }
 
+// The products of heavy rows [h0, h1) into their level-0 chunks from the
+// chunk-major copy of B (p->bct, p->bc_col, p->bc_val): the batch rows' A
+// entries are gathered in row order, then k_expand_cm writes each (row, chunk)
+// pair's products as one run at rrp[pair].
+static gm_status expand_chunk_major(gm_plan* p, int64_t h0, int64_t h1, const int64_t* rrp, bool col16) {
+  const cudaStream_t s = p->s;
+  const int64_t nb = h1 - h0;
+  const int64_t ne = p->h_anz[h1] - p->h_anz[h0];
+  const int32_t* heavy = p->rows_by_bin.p + p->bin_start[kHeavyBin] + h0;
+  int t = p->stage_begin(GM_STAGE_TRANSPOSE);
+  DevBuf<int32_t> e_k;
+  DevBuf<double> e_a;
+  DevBuf<unsigned long long> counter;
+  if (!e_a.alloc(ne, s) || !e_k.alloc(ne, s) || !counter.alloc(1, s)) return GM_ERR_OOM;
+  launch_gather_entries(heavy, nb, p->anz.p + h0, p->A.row_ptr, p->A.col_idx, p->A.vals, p->f32, p->B.row_ptr,
+                        nullptr, e_a.p, nullptr, nullptr, s, e_k.p);
+  p->stage_end(t);
+  t = p->stage_begin(GM_STAGE_MULTISPLIT);
+  ChunkMajorArgs ca{};
+  ca.nb = nb;
+  ca.v = static_cast<int>(p->P.v_chunks[0]);
+  ca.anz = p->anz.p + h0;
+  ca.e_k = e_k.p;
+  ca.e_a = e_a.p;
+  ca.f32 = p->f32;
+  ca.bct = p->bct.p;
+  ca.nB1 = p->B.n_rows + 1;
+  ca.bc_col = p->bc_col.p;
+  ca.bc_val = p->bc_val.p;
+  ca.rrp = rrp;
+  ca.out_col = p->arena_col[0].p;
+  ca.out_val = p->arena_val[0].p;
+  ca.col16 = col16;
+  ca.counter = counter.p;
+  ca.status = p->status.p;
+  launch_expand_cm(ca, p->num_sms, s);
+  p->stage_end(t);
+  return cuda_status(p, cudaGetLastError());
+}
+
 // Chunk-direct pipeline when B's rows are sorted (one level): the products go
 // straight into the level-0 chunks, laid out child by child (chunk sizes from the
 // symbolic pass); C-hat is never written.
@@ -915,8 +957,9 @@ static gm_status run_batch_runs(gm_plan* p, int64_t h0, int64_t h1, int64_t* par
   sub_to_u64(rrp.p, children, 0, cur.p, s);
   p->stage_end(t);
   const bool col16 = p->arena_cb == 2;  // chunk-local columns in 16 bits: 10 (or 6) bytes a product
-  const gm_status st =
-      expand_into_chunks(p, h0, h1, cur.p, p->arena_col[0].p, p->arena_val[0].p, col16, true, rrp.p);
+  const gm_status st = p->bct.p ? expand_chunk_major(p, h0, h1, rrp.p, col16)
+                                : expand_into_chunks(p, h0, h1, cur.p, p->arena_col[0].p, p->arena_val[0].p, col16,
+                                                     true, rrp.p);
   if (st != GM_OK) return st;
   cur.release();
   return rowwise_leaves(p, nb, rrp.p, mcount, par_base, c_col, c_val, col16);
@@ -1587,6 +1630,22 @@ static gm_status numeric_impl(gm_plan* p, int32_t* C_col, void* C_val) {
     std::vector<std::pair<int64_t, int64_t>> batches;
     // the chunk-direct expansion stores chunk-local columns in 16 bits
     p->arena_cb = p->rowwise && p->b_sorted && p->P.v_chunks[0] <= 64 && p->P.widths[0] <= 65536 ? 2 : 4;
+    if (p->rowwise && p->b_sorted && p->P.v_chunks[0] <= 64) {
+      // chunk-major copy of B for the expansion (when it does not fit, the row-order one runs)
+      const int v0 = static_cast<int>(p->P.v_chunks[0]);
+      const int t = p->stage_begin(GM_STAGE_TRANSPOSE);
+      if (p->bct.alloc(bchunk_starts_len(p->B.n_rows, v0), p->s) &&
+          p->bc_col.alloc(std::max<int64_t>(p->B.nnz, 1) * p->arena_cb, p->s) &&
+          p->bc_val.alloc(std::max<int64_t>(p->B.nnz, 1) * p->vb, p->s) &&
+          build_bchunks(p->B.row_ptr, p->B.col_idx, p->B.vals, p->f32, p->B.n_rows, p->bcp.p, v0,
+                        ilog2(p->P.widths[0]), p->arena_cb == 2, p->bct.p, p->bc_col.p, p->bc_val.p, p->s)) {
+      } else {
+        p->bct.release();
+        p->bc_col.release();
+        p->bc_val.release();
+      }
+      p->stage_end(t);
+    }
     gm_status st = p->rowwise ? plan_and_alloc(p, p->arena_cb + p->vb, true, batches, 1)
                               : plan_and_alloc(p, 24, true, batches);
     if (st != GM_OK) return st;
@@ -1598,6 +1657,9 @@ static gm_status numeric_impl(gm_plan* p, int32_t* C_col, void* C_val) {
       if (st != GM_OK) return st;
     }
     free_arena(p);
+    p->bct.release();
+    p->bc_col.release();
+    p->bc_val.release();
     p->keep = keep;
   }
   join_light(p);

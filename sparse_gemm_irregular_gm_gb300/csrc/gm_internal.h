@@ -271,6 +271,32 @@ struct RowRunArgs {
   int* status;
   const int64_t* chunk_rp;    // GM_BOUNDS_CHECK: chunk c's elements lie in [chunk_rp[c], chunk_rp[c+1]) (null: unchecked)
 };
+// Chunk-major expansion (rows of B sorted, one level of at most 64 chunks).
+struct ChunkMajorArgs {
+  int64_t nb;                 // heavy rows of the batch
+  int v;                      // level-0 chunks a row
+  const int64_t* anz;         // prefix of the batch rows' A entries (nb + 1, absolute)
+  const int32_t* e_k;         // B row of each gathered A entry (batch-relative, row order)
+  const void* e_a;            // A value of each entry (null: columns only); float or double (f32)
+  bool f32;
+  const int64_t* bct;         // chunk-major starts (bchunk_starts_len entries)
+  int64_t nB1;                // B.n_rows + 1
+  const void* bc_col;         // chunk-major copy of B: chunk-local columns (uint16 with col16, else int32)
+  const void* bc_val;         // and values
+  const int64_t* rrp;         // region of (row, chunk) pair i = h * v + c: [rrp[i], rrp[i + 1])
+  void* out_col;
+  void* out_val;
+  bool col16;
+  unsigned long long* counter;
+  int* status;
+};
+int64_t bchunk_starts_len(int64_t b_rows, int v);
+// bct (bchunk_starts_len entries), bc_col and bc_val (B.nnz entries each) from the
+// per-B-row chunk starts bcp; B's rows must be sorted by column.
+bool build_bchunks(const int64_t* b_rp, const int32_t* b_col, const void* b_val, bool f32, int64_t b_rows,
+                   const int32_t* bcp, int v, int shift, bool col16, int64_t* bct, void* bc_col, void* bc_val,
+                   cudaStream_t s);
+void launch_expand_cm(const ChunkMajorArgs& a, int num_sms, cudaStream_t s);
 int64_t row_runs_unit(int64_t tau);
 void launch_row_runs(const RowRunArgs& a, int num_sms, cudaStream_t s);
 // Work-group bounds: multiples of kExpandE merged with the starts of every

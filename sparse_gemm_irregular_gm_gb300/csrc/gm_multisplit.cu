@@ -278,12 +278,14 @@ __global__ void k_gather_entries(const int32_t* __restrict__ rows, int64_t nb, c
     for (int64_t p = a_rp[r] + lane; p < a_rp[r + 1]; p += 32) {
       const int64_t i = base + (p - a_rp[r]);
       const int k = a_col[p];
-      const int64_t b0 = b_rp[k];
-      e_b[i] = b0;
       if (e_k) e_k[i] = k;
       if (e_a) e_a[i] = a_val[p];
-      e_row[i] = static_cast<int32_t>(h);
-      e_len[i] = b_rp[k + 1] - b0;
+      if (e_row) e_row[i] = static_cast<int32_t>(h);
+      if (e_b || e_len) {  // null for the chunk-major expansion
+        const int64_t b0 = b_rp[k];
+        if (e_b) e_b[i] = b0;
+        if (e_len) e_len[i] = b_rp[k + 1] - b0;
+      }
     }
   }
 }
@@ -769,6 +771,146 @@ __global__ void k_unit_first(const int64_t* __restrict__ e_off, int64_t n_e, int
   }
 }
 
+// ---- chunk-major expansion -------------------------------------------------
+// B is copied once per numeric pass into chunk-major order: the entries of every
+// B row that fall into level-0 chunk c, for c = 0, 1, ..., with chunk-local
+// columns. bct[c * (nB + 1) + k] is where row k's part of chunk c starts in the
+// copy (bct[c * (nB + 1) + nB] is the end of chunk c). The expansion then takes
+// the (heavy row, chunk) pairs chunk by chunk, so the part of B it reads (one
+// chunk's copy and its starts, a few MB) stays in L2, and each pair's products
+// are written as one contiguous run into the chunk's region.
+
+// cnt[c * (nB + 1) + k]: entries of B row k in chunk c (0 for k == nB).
+__global__ void k_bc_counts(const int32_t* __restrict__ bcp, int64_t nB, int v, int64_t* __restrict__ cnt) {
+  const int64_t n = static_cast<int64_t>(v) * (nB + 1);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int64_t c = i / (nB + 1), k = i - c * (nB + 1);
+    cnt[i] = k < nB ? bcp[k * (v + 1) + c + 1] - bcp[k * (v + 1) + c] : 0;
+  }
+}
+
+// One warp per B row (rows sorted by column): entry j of row k, in chunk c,
+// goes to bct[c * (nB + 1) + k] + j - (row k's entries below chunk c).
+template <typename V, typename CT>
+__global__ void k_bc_fill(const int64_t* __restrict__ b_rp, const int32_t* __restrict__ b_col,
+                          const V* __restrict__ b_val, int64_t nB, const int32_t* __restrict__ bcp, int v, int shift,
+                          const int64_t* __restrict__ bct, CT* __restrict__ bc_col, V* __restrict__ bc_val) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const uint32_t mask = (1u << shift) - 1u;
+  for (int64_t k = warp; k < nB; k += nw) {
+    const int64_t rs = b_rp[k], len = b_rp[k + 1] - rs;
+    const int32_t* t = bcp + k * (v + 1);
+    for (int64_t j = lane; j < len; j += 32) {
+      const uint32_t col = static_cast<uint32_t>(b_col[rs + j]);
+      const int c = static_cast<int>(col >> shift);
+      const int64_t pos = bct[static_cast<int64_t>(c) * (nB + 1) + k] + (j - t[c]);
+      bc_col[pos] = static_cast<CT>(col & mask);
+      if (bc_val) bc_val[pos] = b_val[rs + j];
+    }
+  }
+}
+
+constexpr int kCmWarps = 8;
+constexpr int kCmU = 4;  // products a lane has in flight
+
+// One warp per (heavy row h, chunk c) pair, taken chunk-major from a counter one
+// pair at a time (warps that took several consecutive pairs each wrote slower:
+// 79 against 60 ms for the C = A·A product of an R-MAT scale-20 matrix).
+// The warp walks the row's A entries 32 at a time: lane l looks up entry l's
+// part of chunk c (start and length in the chunk-major copy of B), a warp scan
+// gives each part its offset in the pair's run, and the lanes then write the
+// run's products at consecutive positions (lane l the products l, l + 32, ...,
+// each lane stepping forward through the 32 parts), multiplying by the entry's
+// A value.
+template <typename V, typename CT, bool VAL>
+__global__ void __launch_bounds__(kCmWarps * 32) k_expand_cm(ChunkMajorArgs a) {
+  const V* __restrict__ e_a = static_cast<const V*>(a.e_a);
+  const CT* __restrict__ bc_col = static_cast<const CT*>(a.bc_col);
+  const V* __restrict__ bc_val = static_cast<const V*>(a.bc_val);
+  CT* __restrict__ out_col = static_cast<CT*>(a.out_col);
+  V* __restrict__ out_val = static_cast<V*>(a.out_val);
+  __shared__ int64_t s_src[kCmWarps][32];
+  __shared__ V s_av[kCmWarps][32];
+  __shared__ int s_ex[kCmWarps][33];  // s_ex[j]: products of the parts before part j; s_ex[32] = all
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t n_items = a.nb * a.v;
+  const int64_t e_base = a.anz[0];
+  while (true) {
+    unsigned long long t = 0;
+    if (lane == 0) t = atomicAdd(a.counter, 1ull);
+    const int64_t g = static_cast<int64_t>(__shfl_sync(kFull, t, 0));
+    if (g >= n_items) break;
+    const int64_t c = g / a.nb, h = g - c * a.nb;
+    const int64_t e0 = a.anz[h] - e_base, e1 = a.anz[h + 1] - e_base;
+    const int64_t child = h * a.v + c;
+    int64_t dst = a.rrp[child];
+    const int64_t* __restrict__ bc = a.bct + c * a.nB1;
+    for (int64_t eb = e0; eb < e1; eb += 32) {
+      const int64_t e = eb + lane;
+      int64_t src = 0;
+      int len = 0;
+      V av = V(0);
+      if (e < e1) {
+        const int k = a.e_k[e];
+        src = bc[k];
+        len = static_cast<int>(bc[k + 1] - src);
+        if (VAL) av = e_a[e];
+      }
+      const int incl = warp_inclusive_scan(len);
+      const int tot = __shfl_sync(kFull, incl, 31);
+      s_src[w][lane] = src;
+      if (VAL) s_av[w][lane] = av;
+      s_ex[w][lane] = incl - len;
+      if (lane == 31) s_ex[w][32] = tot;
+      __syncwarp();
+#ifdef GM_BOUNDS_CHECK
+      if (lane == 0) GM_CHECKED(dst + tot <= a.rrp[child + 1], a.status);
+#endif
+      int j = 0;
+      for (int p0 = 0; p0 < tot; p0 += 32 * kCmU) {
+        int64_t from[kCmU];
+        V f[kCmU];
+#pragma unroll
+        for (int u = 0; u < kCmU; ++u) {
+          const int q = p0 + u * 32 + lane;
+          from[u] = -1;
+          if (q < tot) {
+            while (s_ex[w][j + 1] <= q) ++j;
+            from[u] = s_src[w][j] + (q - s_ex[w][j]);
+            if (VAL) f[u] = s_av[w][j];
+          }
+        }
+        CT cc[kCmU];
+        V bv[kCmU];
+#pragma unroll
+        for (int u = 0; u < kCmU; ++u) {
+          if (from[u] >= 0) {
+            cc[u] = bc_col[from[u]];
+            if (VAL) bv[u] = bc_val[from[u]];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kCmU; ++u) {
+          if (from[u] >= 0) {
+            const int64_t o = dst + p0 + u * 32 + lane;
+#ifdef GM_BOUNDS_CHECK
+            if (!GM_CHECKED(o < a.rrp[child + 1], a.status)) continue;
+#endif
+            // written once, read once by the accumulators: streaming stores
+            __stcs(out_col + o, cc[u]);
+            if (VAL) __stcs(out_val + o, f[u] * bv[u]);
+          }
+        }
+      }
+      dst += tot;
+      __syncwarp();
+    }
+  }
+}
+
 }  // namespace
 
 int64_t row_runs_unit(int64_t tau) { return std::min<int64_t>(32768, (kRrRows - 2) * (tau + 1)); }
@@ -786,6 +928,46 @@ void launch_row_runs(const RowRunArgs& a, int num_sms, cudaStream_t s) {
     (k_expand_rows<double, uint16_t, true, true><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
   else if (a.out_val) (k_expand_rows<double, int32_t, true, true><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
   else (k_expand_rows<double, int32_t, false><<<blocks, kRrWarps * 32, 0, s>>>(a), note_launch());
+}
+
+int64_t bchunk_starts_len(int64_t b_rows, int v) { return static_cast<int64_t>(v) * (b_rows + 1); }
+
+bool build_bchunks(const int64_t* b_rp, const int32_t* b_col, const void* b_val, bool f32, int64_t b_rows,
+                   const int32_t* bcp, int v, int shift, bool col16, int64_t* bct, void* bc_col, void* bc_val,
+                   cudaStream_t s) {
+  const int64_t n = bchunk_starts_len(b_rows, v);
+  (k_bc_counts<<<grid_for(n, 256), 256, 0, s>>>(bcp, b_rows, v, bct), note_launch());
+  if (!scan_exclusive_i64(bct, bct, n, nullptr, s)) return false;
+  const unsigned g = grid_for(std::max<int64_t>(b_rows, 1) * 32, 256);
+  if (f32 && col16)
+    (k_bc_fill<float, uint16_t><<<g, 256, 0, s>>>(b_rp, b_col, static_cast<const float*>(b_val), b_rows, bcp, v, shift,
+                                                  bct, static_cast<uint16_t*>(bc_col), static_cast<float*>(bc_val)), note_launch());
+  else if (f32)
+    (k_bc_fill<float, int32_t><<<g, 256, 0, s>>>(b_rp, b_col, static_cast<const float*>(b_val), b_rows, bcp, v, shift,
+                                                 bct, static_cast<int32_t*>(bc_col), static_cast<float*>(bc_val)), note_launch());
+  else if (col16)
+    (k_bc_fill<double, uint16_t><<<g, 256, 0, s>>>(b_rp, b_col, static_cast<const double*>(b_val), b_rows, bcp, v,
+                                                   shift, bct, static_cast<uint16_t*>(bc_col),
+                                                   static_cast<double*>(bc_val)), note_launch());
+  else
+    (k_bc_fill<double, int32_t><<<g, 256, 0, s>>>(b_rp, b_col, static_cast<const double*>(b_val), b_rows, bcp, v,
+                                                  shift, bct, static_cast<int32_t*>(bc_col),
+                                                  static_cast<double*>(bc_val)), note_launch());
+  return true;
+}
+
+void launch_expand_cm(const ChunkMajorArgs& a, int num_sms, cudaStream_t s) {
+  if (a.nb <= 0) return;
+  cudaMemsetAsync(a.counter, 0, sizeof(unsigned long long), s);
+  const unsigned blocks = static_cast<unsigned>(
+      std::min<int64_t>((a.nb * a.v + kCmWarps - 1) / kCmWarps, static_cast<int64_t>(num_sms) * 8));
+  const unsigned T = kCmWarps * 32;
+  if (a.out_val && a.f32 && a.col16) (k_expand_cm<float, uint16_t, true><<<blocks, T, 0, s>>>(a), note_launch());
+  else if (a.out_val && a.f32) (k_expand_cm<float, int32_t, true><<<blocks, T, 0, s>>>(a), note_launch());
+  else if (a.out_val && a.col16) (k_expand_cm<double, uint16_t, true><<<blocks, T, 0, s>>>(a), note_launch());
+  else if (a.out_val) (k_expand_cm<double, int32_t, true><<<blocks, T, 0, s>>>(a), note_launch());
+  else if (a.col16) (k_expand_cm<double, uint16_t, false><<<blocks, T, 0, s>>>(a), note_launch());
+  else (k_expand_cm<double, int32_t, false><<<blocks, T, 0, s>>>(a), note_launch());
 }
 
 }  // namespace gm
