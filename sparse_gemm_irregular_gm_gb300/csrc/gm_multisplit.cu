@@ -828,9 +828,8 @@ constexpr int kCmU = 4;  // products a lane has in flight (8 measured slower: 71
 // The warp walks the row's A entries 32 at a time: lane l looks up entry l's
 // part of chunk c (start and length in the chunk-major copy of B), a warp scan
 // gives each part its offset in the pair's run, and the lanes then write the
-// run's products at consecutive positions (lane l the products l, l + 32, ...,
-// each lane stepping forward through the 32 parts), multiplying by the entry's
-// A value.
+// run's products at consecutive positions (lane l the products l, l + 32, ...),
+// multiplying by the entry's A value.
 template <typename V, typename CT, bool VAL>
 __global__ void __launch_bounds__(kCmWarps * 32) k_expand_cm(ChunkMajorArgs a) {
   const V* __restrict__ e_a = static_cast<const V*>(a.e_a);
@@ -838,10 +837,13 @@ __global__ void __launch_bounds__(kCmWarps * 32) k_expand_cm(ChunkMajorArgs a) {
   const V* __restrict__ bc_val = static_cast<const V*>(a.bc_val);
   CT* __restrict__ out_col = static_cast<CT*>(a.out_col);
   V* __restrict__ out_val = static_cast<V*>(a.out_val);
+  // the group's parts with at least one product, in order: their start in the
+  // copy of B, their A value and their offset in the run
   __shared__ int64_t s_src[kCmWarps][32];
   __shared__ V s_av[kCmWarps][32];
-  __shared__ int s_ex[kCmWarps][33];  // s_ex[j]: products of the parts before part j; s_ex[32] = all
+  __shared__ int s_ex[kCmWarps][32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const unsigned le_mask = lane == 31 ? kFull : ((2u << lane) - 1u);  // lanes 0..lane
   const int64_t n_items = a.nb * a.v;
   const int64_t e_base = a.anz[0];
   while (true) {
@@ -867,26 +869,35 @@ __global__ void __launch_bounds__(kCmWarps * 32) k_expand_cm(ChunkMajorArgs a) {
       }
       const int incl = warp_inclusive_scan(len);
       const int tot = __shfl_sync(kFull, incl, 31);
-      s_src[w][lane] = src;
-      if (VAL) s_av[w][lane] = av;
-      s_ex[w][lane] = incl - len;
-      if (lane == 31) s_ex[w][32] = tot;
+      const int ex = incl - len;
+      const unsigned ne = __ballot_sync(kFull, len > 0);
+      if (len > 0) {  // compacted: rank among the non-empty parts
+        const int r = __popc(ne & lanemask_lt());
+        s_src[w][r] = src;
+        if (VAL) s_av[w][r] = av;
+        s_ex[w][r] = ex;
+      }
       __syncwarp();
 #ifdef GM_BOUNDS_CHECK
       if (lane == 0) GM_CHECKED(dst + tot <= a.rrp[child + 1], a.status);
 #endif
-      int j = 0;
+      // Position q of the run belongs to the last non-empty part starting at or
+      // before q. Per window of 32 positions: the parts starting before it are
+      // counted by a ballot, those starting inside it form a bit mask (an OR
+      // over the lanes), and a lane's part is the count up to its position.
       for (int p0 = 0; p0 < tot; p0 += 32 * kCmU) {
         int64_t from[kCmU];
         V f[kCmU];
 #pragma unroll
         for (int u = 0; u < kCmU; ++u) {
-          const int q = p0 + u * 32 + lane;
+          const int ws = p0 + u * 32;
+          const unsigned starts = __reduce_or_sync(kFull, (len > 0 && ex >= ws && ex < ws + 32) ? 1u << (ex - ws) : 0u);
+          const int before = __popc(__ballot_sync(kFull, len > 0 && ex < ws));
+          const int r = before + __popc(starts & le_mask) - 1;
           from[u] = -1;
-          if (q < tot) {
-            while (s_ex[w][j + 1] <= q) ++j;
-            from[u] = s_src[w][j] + (q - s_ex[w][j]);
-            if (VAL) f[u] = s_av[w][j];
+          if (ws + lane < tot) {
+            from[u] = s_src[w][r] + (ws + lane - s_ex[w][r]);
+            if (VAL) f[u] = s_av[w][r];
           }
         }
         CT cc[kCmU];
