@@ -573,9 +573,16 @@ __global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap,
     const int64_t cb = leaf_col_base(a, child_local);
     int key[ITEMS];
     V val[ITEMS];
-    for (int w = threadIdx.x * 4; w < nwp; w += 4 * T) *reinterpret_cast<uint4*>(bm + w) = make_uint4(0u, 0u, 0u, 0u);
+    // the chunk's column bitmap: kept by the symbolic pass (then no marks), or built
+    const int32_t slot = a.bm_slot ? a.bm_slot[a.child_base + child_local] : -1;
+    if (slot >= 0) {
+      const uint4* kept = reinterpret_cast<const uint4*>(a.bm_store + static_cast<int64_t>(slot) * nwp);
+      for (int w = threadIdx.x; w < nwp / 4; w += T) reinterpret_cast<uint4*>(bm)[w] = kept[w];
+    } else {
+      for (int w = threadIdx.x * 4; w < nwp; w += 4 * T) *reinterpret_cast<uint4*>(bm + w) = make_uint4(0u, 0u, 0u, 0u);
+    }
     __syncthreads();
-    for (int t0 = 0; t0 < n; t0 += CAPB) {  // columns: set the bits
+    for (int t0 = 0; slot < 0 && t0 < n; t0 += CAPB) {  // columns: set the bits
 #pragma unroll
       for (int k = 0; k < ITEMS; ++k) {
         const int e = t0 + k * T + threadIdx.x;
@@ -608,7 +615,7 @@ __global__ void __launch_bounds__(T) k_leaf_blkbm(ListArgs a, int nwp, int vcap,
     for (int i = threadIdx.x; i < nnz; i += T) vals[i] = 0.0;
     __syncthreads();
     for (int t0 = 0; t0 < n; t0 += CAPB) {  // values into their rank's slot
-      if (n > CAPB) {
+      if (n > CAPB || slot >= 0) {
 #pragma unroll
         for (int k = 0; k < ITEMS; ++k) {
           const int e = t0 + k * T + threadIdx.x;

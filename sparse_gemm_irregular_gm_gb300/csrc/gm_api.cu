@@ -157,6 +157,19 @@ __global__ void k_leaf_class(const int64_t* __restrict__ mcount, const int64_t* 
   }
 }
 
+// f[i] = 1 when chunk i has more than min_elems elements (its bitmap is kept)
+__global__ void k_keep_flags(const int64_t* __restrict__ cnt, int64_t n, int64_t min_elems, int64_t* __restrict__ f) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    f[i] = cnt[i] > min_elems ? 1 : 0;
+}
+__global__ void k_keep_slots(const int64_t* __restrict__ cnt, const int64_t* __restrict__ pre, int64_t n,
+                             int64_t min_elems, int32_t* __restrict__ slot) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    slot[i] = cnt[i] > min_elems ? static_cast<int32_t>(pre[i]) : -1;
+}
+
 }  // namespace
 
 static void sub_to_u64(const int64_t* src, int64_t n, int64_t base, unsigned long long* dst, cudaStream_t s) {
@@ -364,6 +377,8 @@ struct gm_plan {
   gm::DevBuf<int64_t> anz;          // prefix of nnz(A[x_heavy[h], :]) (n_heavy + 1)
   gm::DevBuf<int64_t> cnt0;         // row-order pipeline: elements of each level-0 chunk (n_heavy * v0)
   gm::DevBuf<int32_t> bcp;          // row-order pipeline: per-B-row level-0 chunk starts (B.n_rows * (v0 + 1))
+  gm::DevBuf<int32_t> bm_slot;      // chunk-direct: [heavy row * v0 + chunk] slot of a kept bitmap, -1: none
+  gm::DevBuf<uint32_t> bm_store;    // ... the column bitmaps of the larger chunks, symbolic to numeric
   gm::DevBuf<int64_t> bct;          // numeric, chunk-direct: chunk-major starts of B's copy
   gm::DevBuf<uint8_t> bc_col, bc_val;  // ... and the chunk-major copy of B (live during numeric)
   std::vector<int64_t> h_chat_rp;   // host copy of chat_rp
@@ -830,6 +845,8 @@ static gm_status rowwise_leaves(gm_plan* p, int64_t nb, const int64_t* rrp, cons
   la.width = p->P.widths[0];
   la.nnz_out = p->nnz[0].p;
   la.off_in = p->nnz[0].p;
+  la.bm_slot = p->bm_slot.p;
+  la.bm_store = p->bm_store.p;
   const int t = p->stage_begin(GM_STAGE_NUM_HEAVY);
   const gm_status st = run_leaves(p, la, mcount, 0, nb * v, true, true);
   p->stage_end(t);
@@ -1499,6 +1516,39 @@ static void join_light(gm_plan* p) {
   if (p->overlap) cudaStreamWaitEvent(p->s, p->ev_join, 0);
 }
 
+// Chunk-direct pipeline: the symbolic pass keeps the column bitmap of every
+// level-0 chunk of more than 1024 elements (the chunks of the block accumulators
+// and of the streamed one), so that the numeric pass loads it instead of marking
+// the chunk's columns again. When the store cannot be allocated nothing is kept.
+static gm_status keep_chunk_bitmaps(gm_plan* p, int64_t n, RowBitmapArgs& ra) {
+  const cudaStream_t s = p->s;
+  p->bm_slot.release();
+  p->bm_store.release();
+  const int64_t width = p->P.widths[0];
+  if (width % 32 != 0 || n <= 0) return GM_OK;
+  constexpr int64_t kKeepAbove = 1024;
+  DevBuf<int64_t> pre;
+  if (!pre.alloc(n + 1, s)) return GM_ERR_OOM;
+  (k_keep_flags<<<grid_for(n, 256), 256, 0, s>>>(p->cnt0.p, n, kKeepAbove, pre.p), note_launch());
+  if (!scan_exclusive_i64(pre.p, pre.p, n, pre.p + n, s)) return GM_ERR_OOM;
+  int64_t kept = 0;
+  cudaMemcpyAsync(&kept, pre.p + n, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+  const cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_status(p, e);
+  const int64_t words = leaf_blkbm_words(width);
+  if (kept <= 0 || kept >= (int64_t(1) << 31)) return GM_OK;
+  if (!p->bm_slot.alloc(n, s) || !p->bm_store.alloc(kept * words, s)) {
+    p->bm_slot.release();
+    p->bm_store.release();
+    return GM_OK;
+  }
+  (k_keep_slots<<<grid_for(n, 256), 256, 0, s>>>(p->cnt0.p, pre.p, n, kKeepAbove, p->bm_slot.p), note_launch());
+  ra.bm_slot = p->bm_slot.p;
+  ra.bm_store = p->bm_store.p;
+  ra.store_words = static_cast<int>(words);
+  return GM_OK;
+}
+
 static gm_status symbolic_impl(gm_plan* p, int64_t* C_rp, int64_t* C_nnz) {
   const cudaStream_t s = p->s;
   const int64_t n = p->A.n_rows;
@@ -1535,17 +1585,17 @@ static gm_status symbolic_impl(gm_plan* p, int64_t* C_rp, int64_t* C_nnz) {
       const int ts = p->stage_begin(GM_STAGE_SYM_HEAVY);
       const int32_t* hrows = p->rows_by_bin.p + p->bin_start[kHeavyBin];
       const int shift0 = ilog2(p->P.widths[0]);
-      if (p->rowwise) {  // per-B-row chunk starts
+      if (p->rowwise) {  // per-B-row chunk starts, and the level-0 chunk sizes for the expansion
         if (!p->bcp.alloc(std::max<int64_t>(p->B.n_rows, 1) * (v0 + 1), s)) return GM_ERR_OOM;
         build_chunk_starts(p->B.row_ptr, p->B.col_idx, p->B.n_rows, static_cast<int>(v0), shift0, p->bcp.p, s);
-      }
-      launch_rowbm(ra, p->num_sms, p->smem_dev, s);
-      if (p->rowwise) {  // level-0 chunk sizes, for the expansion
         if (!p->cnt0.alloc(nh * v0, s)) return GM_ERR_OOM;
         if (!heavy_chunk_counts(hrows, nh, p->anz.p, p->A.row_ptr, p->A.col_idx, nullptr, p->B.col_idx,
                                 p->B.n_rows, static_cast<int>(v0), shift0, p->bcp.p, p->cnt0.p, s))
           return GM_ERR_OOM;
+        const gm_status kst = keep_chunk_bitmaps(p, nh * v0, ra);
+        if (kst != GM_OK) return kst;
       }
+      launch_rowbm(ra, p->num_sms, p->smem_dev, s);
       p->stage_end(ts);
       p->n_batches = 0;
       p->n_leaves += nh * v0;
@@ -1660,6 +1710,8 @@ static gm_status numeric_impl(gm_plan* p, int32_t* C_col, void* C_val) {
     p->bct.release();
     p->bc_col.release();
     p->bc_val.release();
+    p->bm_slot.release();  // the kept bitmaps serve one numeric pass
+    p->bm_store.release();
     p->keep = keep;
   }
   join_light(p);

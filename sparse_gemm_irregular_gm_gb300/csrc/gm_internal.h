@@ -351,6 +351,10 @@ struct ListArgs {
   unsigned int* counter;      // dynamic chunk scheduling (launch_leaf_stream)
   int64_t c_nnz;              // GM_BOUNDS_CHECK: entries of C (numeric)
   const int64_t* expect_nnz;  // GM_BOUNDS_CHECK: the symbolic pass's nnz of each chunk (null: unchecked)
+  // block accumulator: [global child] slot of the chunk's column bitmap kept by the
+  // symbolic pass (-1: none), and the kept bitmaps (leaf_blkbm_words(width) words a slot)
+  const int32_t* bm_slot;
+  const uint32_t* bm_store;
 };
 // Chunks narrower than the dense width: shared-memory bitmap + rank accumulator.
 void launch_leaf_bitmap(const ListArgs& a, int cap_vals, bool symbolic, cudaStream_t s);
@@ -370,6 +374,7 @@ bool leaf_warpbm_fits(int64_t width, int max_elems, int64_t smem_max, int vb = 8
 // any) and max_nnz output columns (the value array of the block).
 void launch_leaf_blkbm(const ListArgs& a, int max_nnz, int max_elems, cudaStream_t s);
 bool leaf_blkbm_fits(int64_t width, int max_nnz, int64_t smem_max, int vb = 8);
+int64_t leaf_blkbm_words(int64_t width);
 // Numeric chunks of any size, streamed: one producer warp copies each chunk's
 // tiles into a shared-memory ring with bulk asynchronous copies, the consumer
 // warps add them into a dense accumulator of the chunk's width. One block per
@@ -401,6 +406,11 @@ struct RowBitmapArgs {
   int* status;
   bool f32;
   int64_t c_nnz;              // GM_BOUNDS_CHECK: entries of C (numeric)
+  // symbolic, chunks: [global child] slot where the chunk's bitmap words are kept
+  // for the numeric pass (-1: not kept), store_words words a slot
+  const int32_t* bm_slot;
+  uint32_t* bm_store;
+  int store_words;
 };
 int64_t rowbm_symbolic_smem(int64_t c_m);
 // Words of a whole-row bitmap of C.m columns (whole 16-byte pieces).

@@ -165,7 +165,16 @@ __global__ void __launch_bounds__(kRbThreads) k_rowbm_symbolic(RowBitmapArgs a, 
         int n = 0;
         for (int64_t j = lane; j < span; j += 32) n += count_range(bm, lo + j * 32, min(hi, lo + j * 32 + 32));
         n = warp_reduce_sum(n);
-        if (lane == 0) a.nnz_out[(a.item_base + item) * a.v + c] = n;
+        const int64_t child = (a.item_base + item) * a.v + c;
+        if (lane == 0) a.nnz_out[child] = n;
+        if (a.bm_slot) {  // keep the chunk's words for the numeric pass (width a multiple of 32)
+          const int32_t slot = a.bm_slot[child];
+          if (slot >= 0) {
+            uint32_t* dst = a.bm_store + static_cast<int64_t>(slot) * a.store_words;
+            const uint32_t* src = bm + (lo >> 5);
+            for (int j = lane; j < a.store_words; j += 32) dst[j] = j < span ? src[j] : 0u;
+          }
+        }
       }
     }
     __syncthreads();
