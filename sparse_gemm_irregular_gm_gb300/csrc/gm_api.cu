@@ -1538,6 +1538,7 @@ static gm_status keep_chunk_bitmaps(gm_plan* p, int64_t n, RowBitmapArgs& ra) {
   const int64_t words = leaf_blkbm_words(width);
   if (kept <= 0 || kept >= (int64_t(1) << 31)) return GM_OK;
   if (!p->bm_slot.alloc(n, s) || !p->bm_store.alloc(kept * words, s)) {
+    if (p->log) std::fprintf(stderr, "[gm_spgemm] no room to keep %lld chunk bitmaps; marking them again\n", (long long)kept);
     p->bm_slot.release();
     p->bm_store.release();
     return GM_OK;
@@ -1690,6 +1691,7 @@ static gm_status numeric_impl(gm_plan* p, int32_t* C_col, void* C_val) {
           build_bchunks(p->B.row_ptr, p->B.col_idx, p->B.vals, p->f32, p->B.n_rows, p->bcp.p, v0,
                         ilog2(p->P.widths[0]), p->arena_cb == 2, p->bct.p, p->bc_col.p, p->bc_val.p, p->s)) {
       } else {
+        if (p->log) std::fprintf(stderr, "[gm_spgemm] no room for the chunk-major copy of B; row-order expansion\n");
         p->bct.release();
         p->bc_col.release();
         p->bc_val.release();
