@@ -9,6 +9,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <memory>
+#include <mutex>
 #include <vector>
 
 #include "gm_device.cuh"
@@ -464,6 +465,59 @@ static gm_status cuda_status(gm_plan* p, cudaError_t e) {
   return GM_ERR_CUDA;
 }
 
+// Small device-to-host reads (counts, totals, row pointers of the heavy rows)
+// go through a pinned, device-mapped staging buffer written by a kernel, not
+// through a copy engine: a caller that copies large results to the host on
+// other streams (C of one part while the next part is computed) keeps the copy
+// engines busy, and a readback queued behind such a copy would stall the plan.
+// One buffer for the process, taken under a lock; reads larger than it, or when
+// it cannot be had, use cudaMemcpyAsync.
+namespace {
+constexpr size_t kStageBytes = size_t(64) << 20;
+std::mutex g_stage_mu;
+unsigned char* g_stage_host = nullptr;
+unsigned char* g_stage_dev = nullptr;
+bool g_stage_failed = false;
+
+__global__ void k_stage_copy(const unsigned char* __restrict__ src, unsigned char* __restrict__ dst, size_t n) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) dst[i] = src[i];
+}
+}  // namespace
+
+// Copies bytes from device memory to host memory after the work queued on s, and
+// waits for it.
+static cudaError_t read_to_host(void* dst, const void* src, size_t bytes, cudaStream_t s) {
+  if (bytes == 0) return cudaSuccess;
+  std::unique_lock<std::mutex> lk(g_stage_mu);
+  if (!g_stage_host && !g_stage_failed) {
+    void* h = nullptr;
+    void* d = nullptr;
+    if (cudaHostAlloc(&h, kStageBytes, cudaHostAllocMapped | cudaHostAllocPortable) == cudaSuccess &&
+        cudaHostGetDevicePointer(&d, h, 0) == cudaSuccess) {
+      g_stage_host = static_cast<unsigned char*>(h);
+      g_stage_dev = static_cast<unsigned char*>(d);
+    } else {
+      if (h) cudaFreeHost(h);
+      cudaGetLastError();
+      g_stage_failed = true;
+    }
+  }
+  if (!g_stage_host || bytes > kStageBytes) {
+    lk.unlock();
+    cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return e;
+  }
+  const int threads = 256;
+  const unsigned blocks = static_cast<unsigned>(std::min<size_t>((bytes + threads - 1) / threads, 1024));
+  (k_stage_copy<<<blocks, threads, 0, s>>>(static_cast<const unsigned char*>(src), g_stage_dev, bytes), note_launch());
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) std::memcpy(dst, g_stage_host, bytes);
+  return e;
+}
+
 // Synchronise the plan's stream and turn CUDA errors and device status bits into a status.
 static gm_status sync_check(gm_plan* p) {
   cudaError_t e = cudaStreamSynchronize(p->s);
@@ -471,11 +525,11 @@ static gm_status sync_check(gm_plan* p) {
   if (e == cudaSuccess && g_launch_err.load() != 0) e = static_cast<cudaError_t>(g_launch_err.exchange(0));
   if (e != cudaSuccess) return cuda_status(p, e);
   int st = 0;
-  e = cudaMemcpy(&st, p->status.p, sizeof(int), cudaMemcpyDeviceToHost);
+  e = read_to_host(&st, p->status.p, sizeof(int), p->s);
   if (e != cudaSuccess) return cuda_status(p, e);
   if (p->overlap && p->status2.p) {  // the light stream's word (its work is joined into p->s)
     int st2 = 0;
-    e = cudaMemcpy(&st2, p->status2.p, sizeof(int), cudaMemcpyDeviceToHost);
+    e = read_to_host(&st2, p->status2.p, sizeof(int), p->s);
     if (e != cudaSuccess) return cuda_status(p, e);
     st |= st2;
   }
@@ -534,9 +588,8 @@ static gm_status adapt_inputs(gm_plan* p, const gm_csr* A, const gm_csr* B, int6
     const gm_status st = sync_check(p);
     if (st != GM_OK) return st;
     int64_t ends[2] = {0, 0};
-    cudaMemcpyAsync(&ends[0], a_rp + r0, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
-    cudaMemcpyAsync(&ends[1], a_rp + r1, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
-    const cudaError_t e = cudaStreamSynchronize(s);
+    cudaError_t e = read_to_host(&ends[0], a_rp + r0, sizeof(int64_t), s);
+    if (e == cudaSuccess) e = read_to_host(&ends[1], a_rp + r1, sizeof(int64_t), s);
     if (e != cudaSuccess) return cuda_status(p, e);
     lo = ends[0];
     hi = ends[1];
@@ -640,7 +693,8 @@ static gm_status row_split_impl(gm_plan* p, int64_t n_parts, int64_t* bounds) {
   if (n == 0) cudaMemsetAsync(S.p, 0, sizeof(int64_t), s);
   else if (!scan_exclusive_i64(u.p, S.p, n, S.p + n, s)) return GM_ERR_OOM;
   (k_row_split<<<grid_for(n_parts + 1, 256), 256, 0, s>>>(S.p, n, n_parts, out.p), note_launch());
-  cudaMemcpyAsync(bounds, out.p, (n_parts + 1) * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+  const cudaError_t e = read_to_host(bounds, out.p, (n_parts + 1) * sizeof(int64_t), s);
+  if (e != cudaSuccess) return cuda_status(p, e);
   return sync_check(p);
 }
 
@@ -656,7 +710,8 @@ static gm_status analyze_impl(gm_plan* p) {
     if (!flag.alloc(1, s)) return GM_ERR_OOM;
     cudaMemsetAsync(flag.p, 0, sizeof(int), s);
     launch_check_sorted(p->B.row_ptr, p->B.col_idx, p->B.n_rows, flag.p, s);
-    cudaMemcpyAsync(&p->b_unsorted_h, flag.p, sizeof(int), cudaMemcpyDeviceToHost, s);
+    const cudaError_t e = read_to_host(&p->b_unsorted_h, flag.p, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_status(p, e);
     st = sync_check(p);
     if (st != GM_OK) return st;
     p->b_sorted = (p->b_unsorted_h & 1) == 0;
@@ -677,8 +732,9 @@ static gm_status analyze_impl(gm_plan* p) {
   DevBuf<int64_t> tmp, tot;
   if (!tmp.alloc(std::max<int64_t>(n, 1), s) || !tot.alloc(2, s)) return GM_ERR_OOM;
   if (!scan_exclusive_i64(p->u.p, tmp.p, n, tot.p, s)) return GM_ERR_OOM;
-  cudaMemcpyAsync(p->bin_start, p->bin_start_d.p, (kRowBins + 1) * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
-  cudaMemcpyAsync(&p->ip_total, tot.p, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+  cudaError_t re = read_to_host(p->bin_start, p->bin_start_d.p, (kRowBins + 1) * sizeof(int64_t), s);
+  if (re == cudaSuccess) re = read_to_host(&p->ip_total, tot.p, sizeof(int64_t), s);
+  if (re != cudaSuccess) return cuda_status(p, re);
   st = sync_check(p);
   if (st != GM_OK) return st;
   p->n_empty = p->bin_start[1] - p->bin_start[0];
@@ -700,8 +756,9 @@ static gm_status analyze_impl(gm_plan* p) {
   i32_to_i64(heavy, nh, 0, p->heavy_ids64.p, s);
   p->h_chat_rp.resize(nh + 1);
   p->h_anz.resize(nh + 1);
-  cudaMemcpyAsync(p->h_chat_rp.data(), p->chat_rp.p, (nh + 1) * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
-  cudaMemcpyAsync(p->h_anz.data(), anz.p, (nh + 1) * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+  re = read_to_host(p->h_chat_rp.data(), p->chat_rp.p, (nh + 1) * sizeof(int64_t), s);
+  if (re == cudaSuccess) re = read_to_host(p->h_anz.data(), anz.p, (nh + 1) * sizeof(int64_t), s);
+  if (re != cudaSuccess) return cuda_status(p, re);
   p->stage_end(t0);
   st = sync_check(p);
   if (st != GM_OK) return st;
@@ -780,8 +837,7 @@ static gm_status run_leaves(gm_plan* p, ListArgs la, const int64_t* mcount, int6
     launch_bin_sizes(mcount + lo, n, bins.p, spec, s);
   if (!partition_by_bin(bins.p, n, spec.nbins, idx.p, starts_d.p, s)) return GM_ERR_OOM;
   int64_t starts[kMaxBins + 1];
-  cudaMemcpyAsync(starts, starts_d.p, (spec.nbins + 1) * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
-  cudaError_t e = cudaStreamSynchronize(s);
+  cudaError_t e = read_to_host(starts, starts_d.p, (spec.nbins + 1) * sizeof(int64_t), s);
   if (e != cudaSuccess) return cuda_status(p, e);
   i32_to_i64(idx.p, n, lo, items.p, s);
   for (int b = 1; b < spec.nbins; ++b) {
@@ -1235,8 +1291,7 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
       (k_heavy_bin<<<grid_for(children, 256), 256, 0, s>>>(cnt, children, p->P.tau, hb.p), note_launch());
       if (!partition_by_bin(hb.p, children, 2, perm.p, st2.p, s)) return GM_ERR_OOM;
       int64_t hst[3];
-      cudaMemcpyAsync(hst, st2.p, sizeof(hst), cudaMemcpyDeviceToHost, s);
-      cudaError_t e = cudaStreamSynchronize(s);
+      cudaError_t e = read_to_host(hst, st2.p, sizeof(hst), s);
       if (e != cudaSuccess) return cuda_status(p, e);
       nH = hst[1] - hst[0];
       i32_to_i64(perm.p, children, 0, perm64.p, s);
@@ -1310,7 +1365,8 @@ static gm_status run_batch(gm_plan* p, int64_t h0, int64_t h1, bool numeric, int
     const int64_t P_old = P_b;
     if (!last && nH > 0) {
       int64_t next_total = 0;
-      cudaMemcpyAsync(&next_total, rrp->p + nH, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+      const cudaError_t re = read_to_host(&next_total, rrp->p + nH, sizeof(int64_t), s);
+      if (re != cudaSuccess) return cuda_status(p, re);
       if (!numeric) {
         const int64_t at = par_base[i + 1];
         if (!p->heavy_list[i].ensure(at + nH, at, s) || !p->pbase[i + 1].ensure(at + nH, at, s)) return GM_ERR_OOM;
@@ -1532,8 +1588,7 @@ static gm_status keep_chunk_bitmaps(gm_plan* p, int64_t n, RowBitmapArgs& ra) {
   (k_keep_flags<<<grid_for(n, 256), 256, 0, s>>>(p->cnt0.p, n, kKeepAbove, pre.p), note_launch());
   if (!scan_exclusive_i64(pre.p, pre.p, n, pre.p + n, s)) return GM_ERR_OOM;
   int64_t kept = 0;
-  cudaMemcpyAsync(&kept, pre.p + n, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
-  const cudaError_t e = cudaStreamSynchronize(s);
+  const cudaError_t e = read_to_host(&kept, pre.p + n, sizeof(int64_t), s);
   if (e != cudaSuccess) return cuda_status(p, e);
   const int64_t words = leaf_blkbm_words(width);
   if (kept <= 0 || kept >= (int64_t(1) << 31)) return GM_OK;
@@ -1645,7 +1700,10 @@ heavy_done:
   join_light(p);  // the light rows' counts are in C_rp
   t = p->stage_begin(GM_STAGE_SCAN);
   if (!scan_exclusive_i64(C_rp, C_rp, n + 1, nullptr, s)) return GM_ERR_OOM;
-  cudaMemcpyAsync(&p->c_nnz, C_rp + n, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+  {
+    const cudaError_t re = read_to_host(&p->c_nnz, C_rp + n, sizeof(int64_t), s);
+    if (re != cudaSuccess) return cuda_status(p, re);
+  }
   // top-down: output offset of every chunk = its parent's offset + nnz of earlier siblings
   if (nh > 0) {
     if (L >= 1) {
@@ -1866,9 +1924,7 @@ gm_status gm_row_ptr_shift(void* row_ptr, int64_t n, int64_t base, int32_t index
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (index_type & GM_INDEX_ROWPTR32) {
     int32_t last = 0;  // the largest entry of a valid row-pointer array
-    cudaError_t e = cudaMemcpyAsync(&last, static_cast<int32_t*>(row_ptr) + (n - 1), sizeof(int32_t),
-                                    cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    const cudaError_t e = gm::read_to_host(&last, static_cast<int32_t*>(row_ptr) + (n - 1), sizeof(int32_t), s);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return GM_ERR_CUDA;
