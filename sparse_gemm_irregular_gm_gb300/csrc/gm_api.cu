@@ -1508,8 +1508,11 @@ static void launch_light(gm_plan* p, bool numeric, int32_t* c_col, void* c_val, 
     const int64_t cnt = p->bin_start[b + 1] - p->bin_start[b];
     if (cnt <= 0) continue;
     const int cap = b <= 9 ? static_cast<int>(light_bin_ub(b)) : static_cast<int>(p->P.tau);
-    // the same kernel family for both passes of a bin (symbolic rows hold no values)
-    if (b >= 7 && rowbm_light_fits(p->c_m, cap, false, p->smem_dev, p->vb) &&
+    // the whole-row bitmap kernel for rows of more than 1024 products in both passes,
+    // and in the numeric pass also for rows of 513-1024 products (measured: the hash
+    // table and sort were faster for their symbolic pass, slower for the numeric one;
+    // both give the same rows of C)
+    if ((b >= 7 || (b == 6 && numeric)) && rowbm_light_fits(p->c_m, cap, false, p->smem_dev, p->vb) &&
         rowbm_light_fits(p->c_m, cap, true, p->smem_dev, p->vb)) {
       RowBitmapArgs ra{};
       ra.f32 = p->f32;

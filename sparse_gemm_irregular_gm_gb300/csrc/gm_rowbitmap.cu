@@ -524,20 +524,20 @@ void launch_rowbm_light(const RowBitmapArgs& a, bool symbolic, int cap, int num_
   // products a thread holds: the fewest that cover the bin's cap, so that the
   // unrolled per-product loops carry no empty slots (more than kRlItems only for
   // symbolic passes and float values)
-  const int items = cap <= 2 * kRbThreads ? 2 : cap <= 4 * kRbThreads ? 4 : cap <= 8 * kRbThreads ? 8
-                    : cap <= kRlItems * kRbThreads ? kRlItems : kRlItemsWide;
-  auto pick = [items](auto f2, auto f4, auto f8, auto f10, auto f16) {
-    return items == 2 ? f2 : items == 4 ? f4 : items == 8 ? f8 : items == kRlItems ? f10 : f16;
+  const int items = cap <= kRbThreads ? 1 : cap <= 2 * kRbThreads ? 2 : cap <= 4 * kRbThreads ? 4
+                    : cap <= 8 * kRbThreads ? 8 : cap <= kRlItems * kRbThreads ? kRlItems : kRlItemsWide;
+  auto pick = [items](auto f1, auto f2, auto f4, auto f8, auto f10, auto f16) {
+    return items == 1 ? f1 : items == 2 ? f2 : items == 4 ? f4 : items == 8 ? f8 : items == kRlItems ? f10 : f16;
   };
-  auto fn = symbolic ? pick(k_rowbm_light<double, true, 2>, k_rowbm_light<double, true, 4>,
-                            k_rowbm_light<double, true, 8>, k_rowbm_light<double, true, kRlItems>,
-                            k_rowbm_light<double, true, kRlItemsWide>)
-            : a.f32  ? pick(k_rowbm_light<float, false, 2>, k_rowbm_light<float, false, 4>,
-                            k_rowbm_light<float, false, 8>, k_rowbm_light<float, false, kRlItems>,
-                            k_rowbm_light<float, false, kRlItemsWide>)
-                     : pick(k_rowbm_light<double, false, 2>, k_rowbm_light<double, false, 4>,
-                            k_rowbm_light<double, false, 8>, k_rowbm_light<double, false, kRlItems>,
-                            k_rowbm_light<double, false, kRlItems>);
+  auto fn = symbolic ? pick(k_rowbm_light<double, true, 2>, k_rowbm_light<double, true, 2>,
+                            k_rowbm_light<double, true, 4>, k_rowbm_light<double, true, 8>,
+                            k_rowbm_light<double, true, kRlItems>, k_rowbm_light<double, true, kRlItemsWide>)
+            : a.f32  ? pick(k_rowbm_light<float, false, 1>, k_rowbm_light<float, false, 2>,
+                            k_rowbm_light<float, false, 4>, k_rowbm_light<float, false, 8>,
+                            k_rowbm_light<float, false, kRlItems>, k_rowbm_light<float, false, kRlItemsWide>)
+                     : pick(k_rowbm_light<double, false, 1>, k_rowbm_light<double, false, 2>,
+                            k_rowbm_light<double, false, 4>, k_rowbm_light<double, false, 8>,
+                            k_rowbm_light<double, false, kRlItems>, k_rowbm_light<double, false, kRlItems>);
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   (fn<<<static_cast<unsigned>(blocks), kRbThreads, smem, s>>>(a, nwords, wwords, cap, te_cap,
                                                                static_cast<int>(region)), note_launch());
