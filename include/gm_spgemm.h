@@ -138,7 +138,11 @@ typedef struct gm_params {
 #define GM_NUM_STAGES 16
 /* Stage indices of gm_plan_info.stage_ms (device time, filled with GM_FLAG_TIMING).
  * The heavy-row expansion and multisplit run once in the symbolic pass (columns
- * only) and once in the numeric pass (columns and values); they are timed apart. */
+ * only) and once in the numeric pass (columns and values); they are timed apart.
+ * Whatever the flags, the host calls of each stage form an NVTX range named
+ * "gm:" and the stage's name (gm:analyze, gm:num_heavy, ...), and every
+ * analyze, row split, symbolic and numeric call an NVTX range with the call's
+ * name, for profilers that record NVTX. */
 enum {
   GM_STAGE_ANALYZE = 0,        /* counts, validation, partition, heavy row pointers */
   GM_STAGE_TRANSPOSE = 1,      /* masked CSR -> CSC of the heavy rows (numeric pass) */

@@ -64,7 +64,7 @@ def build(force: bool = False, verbose: bool = False, checked: bool = False) -> 
     with ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = lib + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
+    cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs, "-ldl",  # NVTX loads a profiler's hooks
            "-Xlinker", "-rpath=/usr/local/cuda/lib64"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:

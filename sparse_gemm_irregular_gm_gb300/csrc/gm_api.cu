@@ -12,6 +12,8 @@
 #include <mutex>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "gm_device.cuh"
 #include "gm_internal.h"
 
@@ -310,8 +312,23 @@ struct GrowBuf {
 
 struct StageEv {
   int stage;
-  cudaEvent_t a, b;
-  cudaStream_t on;  // the stream the stage's work runs on
+  cudaEvent_t a, b;      // with GM_FLAG_TIMING only
+  cudaStream_t on;       // the stream the stage's work runs on
+  nvtxRangeId_t range;   // NVTX range of the stage's host calls (0 once ended)
+};
+
+// NVTX names of the stages (gm_stage order) and of the public calls; a profiler
+// shows where each stage's work was issued, with or without GM_FLAG_TIMING.
+const char* const kStageNvtx[GM_NUM_STAGES] = {
+    "gm:analyze",   "gm:transpose",     "gm:outer",      "gm:histogram",     "gm:multisplit", "gm:sym_heavy",
+    "gm:sym_light", "gm:scan",          "gm:num_heavy",  "gm:num_light",     "gm:other",      "gm:transpose_sym",
+    "gm:outer_sym", "gm:histogram_sym", "gm:multisplit_sym", "gm:unused"};
+
+struct NvtxCall {  // one range around a public call, ended on every return path
+  explicit NvtxCall(const char* name) { nvtxRangePushA(name); }
+  ~NvtxCall() { nvtxRangePop(); }
+  NvtxCall(const NvtxCall&) = delete;
+  NvtxCall& operator=(const NvtxCall&) = delete;
 };
 
 struct LevelDbg {
@@ -423,31 +440,42 @@ struct gm_plan {
   gm::DevBuf<unsigned int> work_counter2;
 
   int stage_begin(int stage, cudaStream_t on = nullptr) {
-    if (!timing) return -1;
-    gm::StageEv e{stage, nullptr, nullptr, on ? on : s};
-    cudaEventCreate(&e.a);
-    cudaEventCreate(&e.b);
-    cudaEventRecord(e.a, e.on);
+    gm::StageEv e{stage, nullptr, nullptr, on ? on : s, nvtxRangeStartA(gm::kStageNvtx[stage])};
+    if (timing) {
+      cudaEventCreate(&e.a);
+      cudaEventCreate(&e.b);
+      cudaEventRecord(e.a, e.on);
+    }
     evs.push_back(e);
     return static_cast<int>(evs.size()) - 1;
   }
   void stage_end(int idx) {
-    if (idx >= 0) cudaEventRecord(evs[idx].b, evs[idx].on);
+    if (idx < 0) return;
+    gm::StageEv& e = evs[idx];
+    if (e.b) cudaEventRecord(e.b, e.on);
+    if (e.range) nvtxRangeEnd(e.range);
+    e.range = 0;
   }
+  // Adds the recorded stage times (GM_FLAG_TIMING: after the plan's streams are
+  // done) and ends any range an early return left open.
   void collect_times() {
+    bool events = false;
     for (auto& e : evs) {
+      if (e.range) nvtxRangeEnd(e.range);
+      if (!e.a) continue;
+      events = true;
       float ms = 0.f;
       if (cudaEventElapsedTime(&ms, e.a, e.b) == cudaSuccess) stage_ms[e.stage] += ms;
       cudaEventDestroy(e.a);
       cudaEventDestroy(e.b);
     }
     evs.clear();
-    cudaGetLastError();
+    if (events) cudaGetLastError();  // an event never recorded (a stage an error cut short)
   }
   ~gm_plan() {
     if (s2) cudaStreamSynchronize(s2);
     if (!evs.empty()) {
-      cudaStreamSynchronize(s);
+      if (timing) cudaStreamSynchronize(s);  // the events must be complete before they are destroyed
       collect_times();
     }
     if (ev_fork) cudaEventDestroy(ev_fork);
@@ -1877,6 +1905,7 @@ gm_status gm_spgemm_analyze(const gm_csr* A, const gm_csr* B, const gm_config* c
 
 gm_status gm_spgemm_analyze_rows(const gm_csr* A, const gm_csr* B, int64_t row_begin, int64_t row_end,
                                  const gm_config* cfg, void* stream, gm_plan** plan_out) {
+  const gm::NvtxCall nvtx_call("gm_spgemm_analyze_rows");
   if (!plan_out) return GM_ERR_INVALID_ARG;
   *plan_out = nullptr;
   std::unique_ptr<gm_plan> p;
@@ -1888,7 +1917,7 @@ gm_status gm_spgemm_analyze_rows(const gm_csr* A, const gm_csr* B, int64_t row_b
   st = gm::adapt_inputs(p.get(), A, B, row_begin, row_end);
   if (st == GM_OK) st = gm::analyze_impl(p.get());
   p->launches += gm::launch_count() - l0;
-  if (p->timing) p->collect_times();
+  p->collect_times();
   if (st != GM_OK) {
     cudaStreamSynchronize(p->s);
     cudaGetLastError();
@@ -1906,6 +1935,7 @@ gm_status gm_spgemm_analyze_rows(const gm_csr* A, const gm_csr* B, int64_t row_b
 
 gm_status gm_spgemm_row_split(const gm_csr* A, const gm_csr* B, const gm_config* cfg, int64_t n_parts,
                               void* stream, int64_t* bounds) {
+  const gm::NvtxCall nvtx_call("gm_spgemm_row_split");
   if (!bounds || n_parts < 1 || n_parts > (int64_t(1) << 20)) return GM_ERR_INVALID_ARG;
   std::unique_ptr<gm_plan> p;
   gm_status st = gm::plan_setup(A, B, cfg, stream, p);
@@ -1943,6 +1973,7 @@ gm_status gm_row_ptr_shift(void* row_ptr, int64_t n, int64_t base, int32_t index
 }
 
 gm_status gm_spgemm_symbolic(gm_plan* plan, void* C_row_ptr, int64_t* C_nnz) {
+  const gm::NvtxCall nvtx_call("gm_spgemm_symbolic");
   if (!plan) return GM_ERR_INVALID_ARG;
   if (plan->state != 1) return GM_ERR_STATE;
   if (!C_row_ptr) return GM_ERR_INVALID_ARG;
@@ -1964,16 +1995,15 @@ gm_status gm_spgemm_symbolic(gm_plan* plan, void* C_row_ptr, int64_t* C_nnz) {
     }
   }
   plan->launches += gm::launch_count() - l0;
-  if (plan->timing) {
-    cudaStreamSynchronize(plan->s);
-    plan->collect_times();
-  }
+  if (plan->timing) cudaStreamSynchronize(plan->s);
+  plan->collect_times();
   plan->ws_peak = std::max<int64_t>(plan->ws_peak, gm::g_ws_peak.load());
   if (st == GM_OK) plan->state = 2;
   return st;
 }
 
 gm_status gm_spgemm_numeric(gm_plan* plan, void* C_col_idx, void* C_vals) {
+  const gm::NvtxCall nvtx_call("gm_spgemm_numeric");
   if (!plan) return GM_ERR_INVALID_ARG;
   if (plan->state != 2) return GM_ERR_STATE;
   if (plan->c_nnz > 0 && (!C_col_idx || !C_vals)) return GM_ERR_INVALID_ARG;
@@ -1996,10 +2026,8 @@ gm_status gm_spgemm_numeric(gm_plan* plan, void* C_col_idx, void* C_vals) {
   if (plan->s2) cudaStreamSynchronize(plan->s2);  // no light work outlives the call, error or not
   if (st == GM_OK) plan->c_rp64.release();
   plan->launches += gm::launch_count() - l0;
-  if (plan->timing) {
-    cudaStreamSynchronize(plan->s);
-    plan->collect_times();
-  }
+  if (plan->timing) cudaStreamSynchronize(plan->s);
+  plan->collect_times();
   plan->ws_peak = std::max<int64_t>(plan->ws_peak, gm::g_ws_peak.load());
   if (st == GM_OK) plan->state = 3;
   return st;
